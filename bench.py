@@ -1,0 +1,411 @@
+"""Benchmark: batch-1 decode tokens/s of the Qwen3-0.6B-shaped decoder, plus cold GEMV GB/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one token-to-logits forward with greedy argmax (the whole decode
+hot path: embedding, 28 layers, final norm, tied vocabulary projection,
+argmax). Steps run back to back through dec_generate, each reading the
+previous step's token on the device. The FP32 weights stream 2.4 GB per step,
+far beyond the 129 MB L2, so every step is cold by construction.
+
+Beside the headline line the JSON carries:
+  e2e         the same metric through dec_step with host token in / host token
+              out every step (4 B each way, host synchronisation included);
+  roofline    the dominant kernel (the GEMV streaming engine at the gate/up
+              shape) against the measured HBM copy bandwidth;
+  gemv_cold   cold GB/s of gemv / gemv_q4 on the five layer shapes, each
+              cycling >= 1 GiB of distinct matrices;
+  cpu_baseline the float64 oracle's decode rate on the host cores.
+
+--impl reference times the oracle (the CPU restatement of the same forward)
+on a bounded sample of the same workload, on the host cores.
+
+N > 1: independent replicas, one per GPU (the batch-1 step does not shard);
+value is the total tokens/s over all ranks, timed by the slowest rank.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as Wl  # noqa: E402
+
+METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
+PROMPT = 32
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while a region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+def dist_setup():
+    import torch
+    import torch.distributed as dist
+
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return ws, rank, local
+
+
+def barrier_max(value: float, ws: int) -> float:
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- GPU arm ----
+
+def bytes_per_step(s, pos):
+    """Algorithmic bytes of one FP32 decode step at position pos: every weight once plus the KV read."""
+    H, I, d = s.hidden, s.inter, s.head_dim
+    per_layer = (s.q_width + 2 * s.kv_width) * H + H * s.q_width + 2 * I * H + H * I
+    weights = s.layers * per_layer + s.vocab * H
+    kv = s.layers * 2 * s.kv_width * (pos + 1)
+    return 4 * (weights + kv) + 4 * s.vocab  # plus the logits write
+
+
+def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=3, min_bytes=1 << 30, ntok=1, gen=None):
+    """Cold GB/s: cycle >= 1 GiB of distinct matrices; returns (GB/s, bytes per launch, avg launch s, launches)."""
+    if dtype == "q4":
+        per = out * inp // 2 + out * (inp // 64) * 4
+    else:
+        per = out * inp * (4 if dtype == "f32" else 2)
+    count = max(2, -(-min_bytes // per))
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    if dtype == "q4":
+        codes = [torch.randint(-2**31, 2**31 - 1, (out, inp // 8), dtype=torch.int32, device="cuda", generator=gen)
+                 for _ in range(count)]
+        sc = [torch.empty((out, inp // 64), dtype=torch.float16, device="cuda").uniform_(0.001, 0.01, generator=gen)
+              for _ in range(count)]
+        bi = [torch.empty((out, inp // 64), dtype=torch.float16, device="cuda").normal_(0, 0.02, generator=gen)
+              for _ in range(count)]
+        x = torch.randn((ntok, inp), device="cuda", generator=gen).to(torch.bfloat16)
+        y = torch.empty((ntok, out), device="cuda")
+
+        def call(i):
+            W.gemv_q4(codes[i], sc[i], bi[i], x, y, out, inp, ntok, stream)
+        per_launch = per + ntok * (inp * 2 + out * 4)
+    else:
+        mats = [(0.02 * torch.randn((out, inp), device="cuda", generator=gen)).to(tdt) for _ in range(count)]
+        x = (0.02 * torch.randn(inp, device="cuda", generator=gen)).to(tdt)
+        y = torch.empty(out, device="cuda")
+        code = W.DEC_F32 if dtype == "f32" else W.DEC_BF16
+
+        def call(i):
+            W.gemv(code, mats[i], x, y, out, inp, stream)
+        per_launch = per + inp * (4 if dtype == "f32" else 2) + out * 4
+    for i in range(count):  # warm-up: one pass
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = rounds * count
+    e0.record(stream)
+    for r in range(rounds):
+        for i in range(count):
+            call(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    avg = sec / n
+    if dtype == "q4":
+        del codes, sc, bi
+    else:
+        del mats
+    torch.cuda.empty_cache()
+    return per_launch / avg / 1e9, per_launch, avg, n
+
+
+def gpu_arm(args):
+    import torch
+
+    ws, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    from weight_streaming_gemv_token_gb300 import build
+
+    build.build()
+    import weight_streaming_gemv_token_gb300 as W
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.QWEN3_06B
+    weights = Wl.decoder_weights(s, seed=1)
+    prompt = Wl.prompt_uniform(PROMPT, s.vocab, seed=0)
+    K, Wm = args.steps, args.warmup
+    max_seq = PROMPT + 1 + Wm + K + 1 + 2 * args.e2e_steps + 8
+    stream = torch.cuda.current_stream()
+    dec = Decoder(s, weights, kv_dtype="f32", max_seq=max_seq, stream=stream)
+    dec.reset()
+    first = dec.prefill(prompt, is_last=True)
+    out_buf = torch.empty(max(Wm, 1) + K, dtype=torch.int32, device="cuda")
+    # warm-up steps (untimed)
+    dec.generate(first, Wm, out_buf[:Wm]) if Wm > 0 else None
+    torch.cuda.synchronize()
+    tok = int(out_buf[Wm - 1].item()) if Wm > 0 else first
+    pos0 = dec.position
+    hbm, peak_kind = measured_peaks()
+
+    # ---- timed region: K decode steps on the device ----
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with Clocks(local) as clk:
+        e0.record(stream)
+        dec.generate(tok, K, out_buf[Wm:Wm + K])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    sec = barrier_max(e0.elapsed_time(e1) / 1e3, ws)
+    value = ws * K / sec
+    assert dec.device_errors() == 0, "device error during the timed region"
+    mid_pos = pos0 + K // 2
+    step_bytes = bytes_per_step(s, mid_pos)
+
+    # ---- e2e: host token in, host token out, every step ----
+    tok = int(out_buf[Wm + K - 1].item())
+    n_e2e = args.e2e_steps
+    for _ in range(3):
+        tok = dec.step(tok)
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(n_e2e):
+        tok = dec.step(tok)          # H2D of the token, graph, D2H of the next token, sync
+    f1.record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    e2e_sec = barrier_max(max(wall, f0.elapsed_time(f1) / 1e3), ws)
+    e2e_value = ws * n_e2e / e2e_sec
+    dec.close()
+    del dec
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if rank == 0:
+        gen = torch.Generator(device="cuda")
+        gen.manual_seed(1234)
+        # dominant kernel: the streaming GEMV at the gate/up shape, cold
+        gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", 6144, 1024, stream, gen=gen)
+        extra["roofline"] = {
+            "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
+            "traffic": None, "peak_kind": peak_kind,
+            "kernel": "gemv_stream_kernel<f32> 6144x1024 (gate/up shape), standalone gemv entry, cold round-robin",
+            "bytes_per_launch": per_launch, "avg_launch_us": round(avg * 1e6, 3), "launches": launches}
+        if not args.no_sweep:
+            sweep = {}
+            for dt in ("f32", "bf16"):
+                for (o, i) in Wl.GEMV_SHAPES:
+                    g, _, a, _ = time_gemv_cold(W, torch, dt, o, i, stream, gen=gen)
+                    sweep[f"{dt} {o}x{i}"] = {"GB/s": round(g, 1), "frac": round(g / hbm, 4), "us": round(a * 1e6, 3)}
+            for ntok in (1, 2):
+                best = None
+                for r in (1, 2, 4, 8):
+                    W.gemv_q4_rows_per_warp(ntok, r)
+                    tot = 0.0
+                    for (o, i) in Wl.GEMV_SHAPES:
+                        g, _, a, _ = time_gemv_cold(W, torch, "q4", o, i, stream, ntok=ntok, gen=gen, rounds=2)
+                        tot += g
+                    if best is None or tot > best[1]:
+                        best = (r, tot)
+                W.gemv_q4_rows_per_warp(ntok, best[0])
+                for (o, i) in Wl.GEMV_SHAPES:
+                    g, _, a, _ = time_gemv_cold(W, torch, "q4", o, i, stream, ntok=ntok, gen=gen)
+                    sweep[f"q4 ntok={ntok} {o}x{i}"] = {"GB/s": round(g, 1), "frac": round(g / hbm, 4),
+                                                       "us": round(a * 1e6, 3), "rows_per_warp": best[0]}
+            extra["gemv_cold"] = sweep
+
+    if rank == 0:
+        cpu = None if args.no_cpu else cpu_baseline_sample(weights, prompt, budget_s=args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": Wm,
+            "ms_per_step": round(sec / K * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded N(0,0.02) weights, uniform prompt)",
+            "config": {
+                "workload": "Qwen3-0.6B-shaped decoder, FP32 weights/activations/KV, batch-1 greedy decode "
+                            f"after a {PROMPT}-token prompt (positions {pos0}..{pos0 + K - 1})",
+                "layers": s.layers, "hidden": s.hidden, "inter": s.inter, "heads": f"{s.n_q}q/{s.n_kv}kv",
+                "head_dim": s.head_dim, "vocab": s.vocab, "global_batch": 1, "seq_len": pos0 + K,
+                "parallelism": "replicas" if ws > 1 else "single GPU",
+                "l2": "inputs larger than L2 (2.38 GB of weights streamed per step)",
+            },
+            "step_roofline": {"bytes_per_step": step_bytes, "achieved_GB/s": round(step_bytes * K / sec / 1e9, 1),
+                              "peak": hbm, "frac": round(step_bytes * K / sec / 1e9 / hbm, 4),
+                              "roofline_tokens_per_s": round(hbm * 1e9 / step_bytes, 1)},
+            "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
+                    "d2h_bytes_per_step": 4, "steps": n_e2e},
+            "gpu_launches": K * (5 * s.layers + 1),
+            "clocks": clk.summary(),
+            "cpu_baseline": cpu,
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------- CPU side ----
+
+def cpu_baseline_sample(weights, prompt, budget_s=15.0, min_tokens=3):
+    """The oracle's decode rate on the host cores: a bounded number of tokens after a short prompt."""
+    import oracle as O
+
+    s = Wl.QWEN3_06B
+    m = O.OracleDecoder(s, weights, kv_dtype="f32", max_seq=len(prompt) + 256)
+    for t in prompt[:-1]:
+        m.body(int(t))
+    cur = int(prompt[-1])
+    n = 0
+    t0 = time.perf_counter()
+    while n < min_tokens or (time.perf_counter() - t0 < budget_s and n < 200):
+        lg = m.step(cur)
+        cur, _ = O.argmax_lowest(lg)
+        n += 1
+    sec = time.perf_counter() - t0
+    return {"value": round(n / sec, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} greedy decode forwards of the FP32 Qwen3-0.6B-shaped decoder after the {len(prompt)}-token "
+                      f"prompt (float64 numpy oracle, BLAS threads = host cores)"}
+
+
+def reference_arm(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle as O
+
+    s = Wl.QWEN3_06B
+    weights = Wl.decoder_weights(s, seed=1)
+    prompt = Wl.prompt_uniform(PROMPT, s.vocab, seed=0)
+    m = O.OracleDecoder(s, weights, kv_dtype="f32", max_seq=PROMPT + args.warmup + args.steps + 4)
+    for t in prompt[:-1]:
+        m.body(int(t))
+    cur = int(prompt[-1])
+    for _ in range(args.warmup):
+        cur, _ = O.argmax_lowest(m.step(cur))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        cur, _ = O.argmax_lowest(m.step(cur))
+    sec = time.perf_counter() - t0
+    value = args.steps / sec
+    sample = f"{args.steps} greedy decode forwards (after {args.warmup} warm-up) of the FP32 Qwen3-0.6B-shaped decoder"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "Qwen3-0.6B-shaped decoder, FP32 weights, batch-1 greedy decode after a "
+                               f"{PROMPT}-token prompt, run by the float64 CPU oracle"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-sweep", action="store_true", help="skip the cold GEMV sweep")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        args.steps = args.steps if args.steps is not None else 5
+        args.warmup = args.warmup if args.warmup is not None else 1
+        # each reference step is one oracle forward (~0.1-1 s); keep the run to a few minutes
+        args.steps = min(args.steps, 60)
+        args.warmup = min(args.warmup, 5)
+        reference_arm(args)
+        return
+    args.steps = args.steps if args.steps is not None else 500
+    args.warmup = max(3, args.warmup if args.warmup is not None else 20)
+    gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

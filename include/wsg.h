@@ -1,0 +1,213 @@
+/*
+ * wsg.h - C ABI of the weight-streaming decode library (GB300, sm_103a).
+ *
+ * The library computes the batch-1 token-to-logits forward of a
+ * Qwen3-shaped decoder and the standalone matrix-vector products that
+ * dominate it. All arithmetic runs in this library's CUDA kernels.
+ *
+ * Sources (page title, section):
+ *   "Megakernels", "What runs in the DSL": the forward pass
+ *       token ID -> embedding; per layer RMSNorm -> Q/K/V projections ->
+ *       per-head Q/K RMSNorm -> RoPE -> grouped-query attention + KV update
+ *       -> output projection -> residual add -> RMSNorm -> gate/up
+ *       projections -> SwiGLU -> down projection -> residual add; then final
+ *       RMSNorm -> tied vocabulary projection -> logits.
+ *   "Megakernels", "GPU-wide end-to-end generation": greedy argmax on the
+ *       GPU with ties broken by lowest token ID; the host reads the ID;
+ *       prompt tokens processed one at a time skip only the final norm and
+ *       vocabulary projection; the first output comes from the final prompt
+ *       row.
+ *   "Megakernels", "Chunked prefill for long prompts": a chunk is a run of
+ *       consecutive positions of the single request; every row attends to
+ *       its whole causal prefix; only the final valid row reaches the
+ *       vocabulary projection.
+ *   "Our Kernel Benchmark Was Measuring the System Cache", "Summary": the
+ *       4-bit matrix-vector product and its two-token variant.
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* are device pointers, h_* host pointers. All device
+ *     memory belongs to the caller; the library never frees it.
+ *   - `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream. Calls are asynchronous on that stream unless stated.
+ *   - Every call returns a dec_status. On failure nothing has been enqueued
+ *     and dec_last_error() describes the cause. No call aborts the process.
+ *   - Device-side problems that can only be seen while kernels run (a token
+ *     ID outside the vocabulary, an all-NaN logit vector, a bounded wait
+ *     that gave up) set bits of a device error word, read with
+ *     dec_device_errors() or gemv_device_errors().
+ */
+#ifndef WSG_H
+#define WSG_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DEC_OK = 0,
+  DEC_EINVAL = 1,     /* bad argument: NULL, size, alignment, dtype */
+  DEC_ESTATE = 2,     /* call out of order (e.g. step before weights) */
+  DEC_ECAPACITY = 3,  /* position or chunk beyond the configured capacity */
+  DEC_ENOMEM = 4,     /* workspace too small, or a host allocation failed */
+  DEC_ECUDA = 5,      /* a CUDA runtime call failed (message has the name) */
+  DEC_EDEVICE = 6     /* device is not an sm_103 GPU */
+} dec_status;
+
+typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
+
+/* Device error bits (dec_device_errors / gemv_device_errors). */
+#define DEC_DEVERR_WAIT_TIMEOUT 0x1u /* a bounded mbarrier wait gave up */
+#define DEC_DEVERR_ARGMAX_NAN 0x2u   /* all logits NaN; token 0 was returned */
+#define DEC_DEVERR_BAD_TOKEN 0x4u    /* a token ID outside [0, vocab) was read as 0 */
+
+/* dec_step flags */
+#define DEC_SKIP_LOGITS 0x1u /* body only: no final norm, vocabulary projection or argmax */
+
+/* Decoder geometry and storage ("Megakernels", "What runs in the DSL").
+ * Requirements: layers, hidden, inter, n_q, n_kv, head_dim, vocab > 0;
+ * n_q % n_kv == 0; head_dim a multiple of 4 and <= 128; hidden, inter and
+ * n_q*head_dim multiples of 8; wdtype DEC_F32 or DEC_BF16; kvdtype DEC_F32
+ * or DEC_BF16; max_seq >= 1 is the KV capacity in positions; chunk_cap is
+ * the largest row count of one dec_prefill_chunk call that runs batched
+ * (0: prompts are processed one token at a time). */
+typedef struct {
+  int32_t layers, hidden, inter, n_q, n_kv, head_dim, vocab;
+  float eps;        /* RMSNorm epsilon, e.g. 1e-6 */
+  float rope_theta; /* RoPE base, e.g. 1e6 */
+  int32_t wdtype;   /* dec_dtype of projections and the tied embedding */
+  int32_t kvdtype;  /* dec_dtype of the KV cache */
+  int32_t max_seq;
+  int32_t chunk_cap;
+} dec_config;
+
+/* One layer's tensors, device pointers, row-major [out][in] in wdtype.
+ * w_q [n_q*head_dim][hidden], w_k and w_v [n_kv*head_dim][hidden],
+ * w_o [hidden][n_q*head_dim], w_gate and w_up [inter][hidden],
+ * w_down [hidden][inter]; gains are float32: g_in and g_post [hidden],
+ * g_q and g_k [head_dim] (one per layer, shared by all heads). Every
+ * pointer must be 16-byte aligned. */
+typedef struct {
+  const void *w_q, *w_k, *w_v, *w_o, *w_gate, *w_up, *w_down;
+  const float *g_in, *g_post, *g_q, *g_k;
+} dec_layer_weights;
+
+/* embed: [vocab][hidden] in wdtype, also the vocabulary head (tied).
+ * layers: HOST array of cfg.layers entries (copied by dec_load_weights). */
+typedef struct {
+  const void* embed;
+  const float* g_final;
+  const dec_layer_weights* layers;
+} dec_weights;
+
+typedef struct dec_ctx dec_ctx;
+
+/* Bytes of device workspace dec_create needs for cfg (KV cache, rotary
+ * table, activations, argmax and attention partials, prefill scratch).
+ * Returns 0 if cfg is invalid. */
+size_t dec_workspace_bytes(const dec_config* cfg);
+
+/* Creates a decoder on the current CUDA device. d_workspace (>= 256-byte
+ * aligned, at least dec_workspace_bytes(cfg) bytes) must stay allocated
+ * until dec_destroy. Builds the rotary table and clears the cache; returns
+ * after that work has finished. stream: the stream later calls run on.
+ * Errors: DEC_EINVAL (cfg, NULL, alignment), DEC_ENOMEM (workspace too
+ * small), DEC_EDEVICE (not sm_103), DEC_ECUDA. */
+dec_status dec_create(const dec_config* cfg, void* d_workspace, size_t workspace_bytes, void* stream,
+                      dec_ctx** out);
+
+/* Registers the caller's weight tensors (no copy: they must outlive the
+ * context). Errors: DEC_EINVAL on a NULL or misaligned pointer. */
+dec_status dec_load_weights(dec_ctx* ctx, const dec_weights* w);
+
+/* Position back to 0 and every cache entry invalidated (the cache is
+ * zeroed). Timed by the pages' protocol ("Benchmark methodology",
+ * "Long-document chunked prefill": timing starts before cache reset). */
+dec_status dec_reset(dec_ctx* ctx);
+
+/* One forward of `token` at the current position p; writes K/V at p and
+ * advances the position to p+1.
+ * Without DEC_SKIP_LOGITS: final RMSNorm, tied vocabulary projection and
+ * argmax (lowest ID on ties) run too. d_logits (nullable, float32[vocab])
+ * receives the logits; h_next (nullable) receives the greedy token, and
+ * then the call synchronizes the stream to read it.
+ * With DEC_SKIP_LOGITS: only the body runs; d_logits and h_next must be NULL.
+ * Errors: DEC_ESTATE (no weights), DEC_ECAPACITY (p == max_seq),
+ * DEC_EINVAL (token outside [0, vocab), bad flags). */
+dec_status dec_step(dec_ctx* ctx, int32_t token, uint32_t flags, float* d_logits, int32_t* h_next);
+
+/* Prompt rows h_tokens[0..n) at positions p..p+n-1 ("Chunked prefill for
+ * long prompts"). If cfg.chunk_cap > 0 and n <= chunk_cap the rows run
+ * batched (tensor-core projections, causal attention over cache + chunk);
+ * otherwise, or with chunk_cap == 0, one token at a time.
+ * is_last != 0: the final row also runs the final norm, the vocabulary
+ * projection and the argmax; d_logits / h_next as in dec_step (h_next
+ * synchronizes). is_last == 0: d_logits and h_next must be NULL.
+ * Errors: DEC_EINVAL (n < 1, token out of range), DEC_ECAPACITY
+ * (p + n > max_seq), DEC_ESTATE. */
+dec_status dec_prefill_chunk(dec_ctx* ctx, const int32_t* h_tokens, int32_t n, int32_t is_last, float* d_logits,
+                             int32_t* h_next);
+
+/* n greedy forwards without host involvement: the first input is `token`
+ * at the current position, each later input is the previous output. Writes
+ * the n outputs to d_tokens_out (device int32[n]). Asynchronous.
+ * Errors: DEC_ECAPACITY (p + n > max_seq), DEC_EINVAL, DEC_ESTATE. */
+dec_status dec_generate(dec_ctx* ctx, int32_t token, int32_t n, int32_t* d_tokens_out);
+
+/* Read access to one layer's cache: device pointers to K and V, each laid
+ * out [n_kv][max_seq][head_dim] in kvdtype, and the number of valid
+ * positions. Keys are stored after Q/K-norm and RoPE, values raw. */
+dec_status dec_get_kv(const dec_ctx* ctx, int32_t layer, const void** d_k, const void** d_v, int32_t* n_valid);
+
+/* Current position (number of valid cache entries). -1 if ctx is NULL. */
+int32_t dec_position(const dec_ctx* ctx);
+
+/* Synchronizes the context's stream and returns (and, if clear != 0,
+ * clears) the device error bits DEC_DEVERR_*. */
+dec_status dec_device_errors(dec_ctx* ctx, int32_t clear, uint32_t* bits);
+
+/* Frees host-side state and CUDA graphs. The workspace stays the caller's. */
+void dec_destroy(dec_ctx* ctx);
+
+/* Message for the last failed call on ctx (ctx == NULL: last failure of a
+ * context-free call on this thread). Never NULL. */
+const char* dec_last_error(const dec_ctx* ctx);
+
+/* y = W x ("Our Kernel Benchmark Was Measuring the System Cache":
+ * the matrix-vector product of the decode step).
+ * wdtype DEC_F32: W float32 [out][in], x float32 [in];
+ * wdtype DEC_BF16: W bfloat16 [out][in], x bfloat16 [in].
+ * y float32 [out]; products accumulated in float32, partial sums reduced
+ * in a fixed order (bit-reproducible). out, in >= 0 (out == 0: no work;
+ * in == 0: y = 0). Any alignment is accepted; 16-byte aligned W with
+ * in*sizeof(elem) a multiple of 16 takes the bulk-copy streaming path.
+ * Errors: DEC_EINVAL, DEC_ECUDA. */
+dec_status gemv(int32_t wdtype, const void* d_W, const void* d_x, float* d_y, int32_t out, int32_t in, void* stream);
+
+/* y[t] = W x[t] for a 4-bit groupwise-affine W ("Our Kernel Benchmark Was
+ * Measuring the System Cache", Summary and "Why it mattered, concretely":
+ * the one-token matvec and the two-token variant). Each group of 64
+ * consecutive columns of a row has an fp16 scale s and bias b, and
+ * w = s*q + b for the 4-bit code q.
+ * d_codes: uint32 [out][in/8], code j of word w in bits [4j, 4j+4), column
+ * 8w+j; d_scale, d_bias: fp16 bits [out][in/64]; d_x: bfloat16 [ntok][in];
+ * d_y: float32 [ntok][out]. ntok is 1 or 2; in % 64 == 0; d_codes 16-byte
+ * aligned. Errors: DEC_EINVAL, DEC_ECUDA. */
+dec_status gemv_q4(const uint32_t* d_codes, const uint16_t* d_scale, const uint16_t* d_bias, const uint16_t* d_x,
+                   float* d_y, int32_t out, int32_t in, int32_t ntok, void* stream);
+
+/* Rows of W each warp of gemv_q4 handles per pass (1, 2, 4 or 8), for the
+ * given ntok. r > 0 sets it, r == 0 only reads it. Returns the value in
+ * effect, or -1 for a bad argument. Process-wide. */
+int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r);
+
+/* Reads (and if clear != 0 clears) the device error bits of gemv/gemv_q4
+ * on the current device; synchronizes the device. */
+dec_status gemv_device_errors(int32_t clear, uint32_t* bits);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* WSG_H */

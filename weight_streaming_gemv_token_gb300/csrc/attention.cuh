@@ -1,0 +1,283 @@
+// Decode attention for one token with the Q/K RMSNorm, RoPE and KV-cache
+// append fused in front ("Megakernels", "What runs in the DSL": per-head Q/K
+// RMSNorm -> RoPE -> grouped-query attention + KV update; "GPU-wide end-to-end
+// generation": attention distributed over heads; "Chunked prefill for long
+// prompts": single-token decode keeps a key-parallel attention path).
+//
+// Grid: (n_kv, nsplit_max). CTA (g, s) serves key/value head g and the
+// n_q/n_kv query heads that read it, over one contiguous range of key
+// positions (key-parallel split). Every CTA normalises and rotates the
+// current token's q and k itself (a few hundred floats), so no separate
+// kernel is needed; the CTA whose range holds the current position writes
+// its k and v into the cache and uses the same stored values for the current
+// key. Each warp runs an online softmax over its keys; warps merge in shared
+// memory; splits merge through a last-CTA-done reduction (partials in the
+// workspace, an atomic counter that the last CTA resets), with no spinning.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace wsg {
+
+struct AttnArgs {
+  const float* qkv;  // q [n_q*d], k [n_kv*d], v [n_kv*d] (raw projections)
+  const float* g_q;
+  const float* g_k;
+  float eps;
+  const float* rope_cos;  // [max_seq][d/2]
+  const float* rope_sin;
+  const int32_t* ctrl;  // ctrl[0] = position of the current token
+  void* kc;             // this layer's cache, [n_kv][max_seq][d]
+  void* vc;
+  int32_t max_seq, n_q, n_kv, d;
+  float* out;  // [n_q*d]
+  float* part;  // [n_kv][nsplit_max][group][d+2]
+  uint32_t* counter;  // [n_kv]
+  int32_t nsplit_max, tmin;
+  float scale;  // 1/sqrt(d)
+  uint32_t* err;
+};
+
+template <typename KT>
+__device__ __forceinline__ float4 load4(const void* base, size_t idx);
+template <>
+__device__ __forceinline__ float4 load4<float>(const void* base, size_t idx) {
+  return __ldcg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + idx));
+}
+template <>
+__device__ __forceinline__ float4 load4<uint16_t>(const void* base, size_t idx) {
+  const uint2 u = __ldcg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + idx));
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+template <typename KT>
+__device__ __forceinline__ float round_store(float v);
+template <>
+__device__ __forceinline__ float round_store<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float round_store<uint16_t>(float v) {
+  return bf16_to_f32(f32_to_bf16_rn(v));
+}
+
+template <typename KT>
+__device__ __forceinline__ void store1(void* base, size_t idx, float v);
+template <>
+__device__ __forceinline__ void store1<float>(void* base, size_t idx, float v) {
+  static_cast<float*>(base)[idx] = v;
+}
+template <>
+__device__ __forceinline__ void store1<uint16_t>(void* base, size_t idx, float v) {
+  static_cast<uint16_t*>(base)[idx] = f32_to_bf16_rn(v);
+}
+
+// RMSNorm over d elements held in shared memory, then RoPE at position pos,
+// in place; one warp.
+__device__ __forceinline__ void norm_rope_warp(float* v, const float* g, float eps, int d, const float* cs,
+                                               const float* sn, int lane) {
+  float ss = 0.f;
+  for (int e = lane; e < d; e += 32) ss = fmaf(v[e], v[e], ss);
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  for (int e = lane; e < d; e += 32) v[e] = v[e] * inv * g[e];
+  __syncwarp();
+  const int half = d >> 1;
+  for (int i = lane; i < half; i += 32) {
+    const float a = v[i], b = v[i + half], c = cs[i], s = sn[i];
+    v[i] = a * c - b * s;
+    v[i + half] = a * s + b * c;
+  }
+  __syncwarp();
+}
+
+constexpr int kAttnWarps = 8;
+
+inline size_t attn_smem_bytes(int group, int d) {
+  // qn[group][d], kn[d], vn[d], per-warp (m, l)[group] and o[group][d]
+  return sizeof(float) * (static_cast<size_t>(group) * d + 2 * d + kAttnWarps * group * 2 +
+                          static_cast<size_t>(kAttnWarps) * group * d) +
+         16;
+}
+
+template <typename KT, int GMAX>
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const AttnArgs a) {
+  extern __shared__ __align__(16) float asmem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d = a.d, group = a.n_q / a.n_kv;
+  const int g = blockIdx.x, s = blockIdx.y;
+
+  pdl_trigger();
+  pdl_wait();
+  const int pos = a.ctrl[0];
+  if (pos < 0 || pos >= a.max_seq) {
+    if (tid == 0 && g == 0 && s == 0) atomicOr(a.err, ERR_BAD_POSITION);
+    return;
+  }
+  const int n = pos + 1;
+  int nsplit = (n + a.tmin - 1) / a.tmin;
+  if (nsplit > a.nsplit_max) nsplit = a.nsplit_max;
+  const int per = (n + nsplit - 1) / nsplit;
+  nsplit = (n + per - 1) / per;
+  if (s >= nsplit) return;
+  const int t0 = s * per, t1 = min(n, t0 + per);
+
+  float* qn = asmem;                       // [group][d]
+  float* kn = qn + group * d;              // [d]
+  float* vn = kn + d;                      // [d]
+  float* wm = vn + d;                      // [warps][group]
+  float* wl = wm + kAttnWarps * group;     // [warps][group]
+  float* wo = wl + kAttnWarps * group;     // [warps][group][d]
+
+  // Current token: raw projections -> RMSNorm -> RoPE (q, k); v as is.
+  const float* cs = a.rope_cos + static_cast<size_t>(pos) * (d >> 1);
+  const float* sn = a.rope_sin + static_cast<size_t>(pos) * (d >> 1);
+  const float* kraw = a.qkv + a.n_q * d + g * d;
+  const float* vraw = a.qkv + a.n_q * d + a.n_kv * d + g * d;
+  for (int i = tid; i < group * d; i += blockDim.x) qn[i] = a.qkv[(g * group) * d + i];
+  for (int i = tid; i < d; i += blockDim.x) {
+    kn[i] = kraw[i];
+    vn[i] = round_store<KT>(vraw[i]);
+  }
+  __syncthreads();
+  for (int h = warp; h <= group; h += kAttnWarps) {
+    if (h < group)
+      norm_rope_warp(qn + h * d, a.g_q, a.eps, d, cs, sn, lane);
+    else
+      norm_rope_warp(kn, a.g_k, a.eps, d, cs, sn, lane);
+  }
+  __syncthreads();
+  for (int i = tid; i < d; i += blockDim.x) kn[i] = round_store<KT>(kn[i]);
+  __syncthreads();
+  const size_t head_base = static_cast<size_t>(g) * a.max_seq * d;
+  if (t1 == n) {  // this CTA's range holds the current position: append to the cache
+    for (int i = tid; i < d; i += blockDim.x) {
+      store1<KT>(a.kc, head_base + static_cast<size_t>(pos) * d + i, kn[i]);
+      store1<KT>(a.vc, head_base + static_cast<size_t>(pos) * d + i, vn[i]);
+    }
+  }
+
+  // Each lane owns 4 consecutive elements [4 lane, 4 lane + 4) of a head vector.
+  const bool active = 4 * lane < d;
+  float4 q[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h)
+    q[h] = (h < group && active) ? *reinterpret_cast<const float4*>(qn + h * d + 4 * lane) : make_float4(0, 0, 0, 0);
+  float m[GMAX], l[GMAX];
+  float4 o[GMAX];
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+    o[h] = make_float4(0, 0, 0, 0);
+  }
+
+  for (int t = t0 + warp; t < t1; t += 2 * kAttnWarps) {
+    const int tb = t + kAttnWarps;
+    const bool two = tb < t1;
+    float4 k0 = make_float4(0, 0, 0, 0), v0 = k0, k1 = k0, v1 = k0;
+    if (active) {
+      if (t == pos) {
+        k0 = *reinterpret_cast<const float4*>(kn + 4 * lane);
+        v0 = *reinterpret_cast<const float4*>(vn + 4 * lane);
+      } else {
+        k0 = load4<KT>(a.kc, head_base + static_cast<size_t>(t) * d + 4 * lane);
+        v0 = load4<KT>(a.vc, head_base + static_cast<size_t>(t) * d + 4 * lane);
+      }
+      if (two) {
+        if (tb == pos) {
+          k1 = *reinterpret_cast<const float4*>(kn + 4 * lane);
+          v1 = *reinterpret_cast<const float4*>(vn + 4 * lane);
+        } else {
+          k1 = load4<KT>(a.kc, head_base + static_cast<size_t>(tb) * d + 4 * lane);
+          v1 = load4<KT>(a.vc, head_base + static_cast<size_t>(tb) * d + 4 * lane);
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < GMAX; ++h) {
+      if (h >= group) break;
+      float s0 = q[h].x * k0.x + q[h].y * k0.y + q[h].z * k0.z + q[h].w * k0.w;
+      float s1 = q[h].x * k1.x + q[h].y * k1.y + q[h].z * k1.z + q[h].w * k1.w;
+      s0 = warp_sum(s0) * a.scale;
+      s1 = warp_sum(s1) * a.scale;
+      float mn = fmaxf(m[h], s0);
+      if (two) mn = fmaxf(mn, s1);
+      const float corr = expf(m[h] - mn);
+      const float p0 = expf(s0 - mn);
+      const float p1 = two ? expf(s1 - mn) : 0.f;
+      l[h] = l[h] * corr + p0 + p1;
+      o[h].x = o[h].x * corr + p0 * v0.x + p1 * v1.x;
+      o[h].y = o[h].y * corr + p0 * v0.y + p1 * v1.y;
+      o[h].z = o[h].z * corr + p0 * v0.z + p1 * v1.z;
+      o[h].w = o[h].w * corr + p0 * v0.w + p1 * v1.w;
+      m[h] = mn;
+    }
+  }
+
+  // Merge the warps of this CTA.
+#pragma unroll
+  for (int h = 0; h < GMAX; ++h) {
+    if (h >= group) break;
+    if (lane == 0) {
+      wm[warp * group + h] = m[h];
+      wl[warp * group + h] = l[h];
+    }
+    if (active) *reinterpret_cast<float4*>(wo + (warp * group + h) * d + 4 * lane) = o[h];
+  }
+  __syncthreads();
+  const int parts = gridDim.y;
+  for (int idx = tid; idx < group * d; idx += blockDim.x) {
+    const int h = idx / d, e = idx - h * d;
+    float M = -INFINITY;
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w * group + h]);
+    float L = 0.f, O = 0.f;
+    for (int w = 0; w < kAttnWarps; ++w) {
+      const float f = expf(wm[w * group + h] - M);
+      L += wl[w * group + h] * f;
+      O += wo[(w * group + h) * d + e] * f;
+    }
+    if (nsplit == 1) {
+      a.out[(g * group + h) * d + e] = O / L;
+    } else {
+      float* p = a.part + ((static_cast<size_t>(g) * a.nsplit_max + s) * group + h) * (d + 2);
+      p[e] = O;
+      if (e == 0) {
+        p[d] = M;
+        p[d + 1] = L;
+      }
+    }
+  }
+  (void)parts;
+  if (nsplit == 1) return;
+
+  // Split merge: the last CTA of this key/value head to finish combines all splits.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = (atomicAdd(a.counter + g, 1u) == static_cast<uint32_t>(nsplit - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int idx = tid; idx < group * d; idx += blockDim.x) {
+    const int h = idx / d, e = idx - h * d;
+    float M = -INFINITY;
+    for (int k = 0; k < nsplit; ++k) {
+      const float* p = a.part + ((static_cast<size_t>(g) * a.nsplit_max + k) * group + h) * (d + 2);
+      M = fmaxf(M, __ldcg(p + d));
+    }
+    float L = 0.f, O = 0.f;
+    for (int k = 0; k < nsplit; ++k) {
+      const float* p = a.part + ((static_cast<size_t>(g) * a.nsplit_max + k) * group + h) * (d + 2);
+      const float f = expf(__ldcg(p + d) - M);
+      L += __ldcg(p + d + 1) * f;
+      O += __ldcg(p + e) * f;
+    }
+    a.out[(g * group + h) * d + e] = O / L;
+  }
+  if (tid == 0) a.counter[g] = 0u;
+}
+
+}  // namespace wsg

@@ -1,0 +1,577 @@
+// Decoder runtime: the batch-1 token-to-logits forward as one CUDA graph.
+//
+// Step structure ("Megakernels", "GPU-wide end-to-end generation" lists eight
+// ordered stages per layer plus embedding, final norm and vocabulary
+// projection, then two argmax passes). Here fusion leaves five kernels per
+// layer and one for the head:
+//
+//   layer l:  QKV GEMV      (input RMSNorm fused as prologue; layer 0 also
+//                            gathers the embedding row of the token)
+//             attention     (per-head Q/K RMSNorm, RoPE and KV append fused)
+//             O GEMV        (residual add fused as epilogue)
+//             gate/up GEMV  (post-attention RMSNorm prologue, SwiGLU epilogue)
+//             down GEMV     (residual add epilogue)
+//   head:     vocab GEMV    (final RMSNorm prologue; logits; both argmax
+//                            passes; next token and position advance)
+//
+// Token and position live in device memory, so the same instantiated graph
+// replays for every step. Kernels after the first carry a programmatic
+// dependent-launch edge: each GEMV starts streaming its weights while its
+// predecessor finishes, and waits only before reading activations.
+#include <cmath>
+#include <cstring>
+#include <vector>
+
+#include "attention.cuh"
+#include "common.h"
+#include "gemv_stream.cuh"
+
+using namespace wsg;
+
+namespace {
+
+constexpr int kNW = 8, kNS = 3, kSEG = 4096;
+constexpr int kArgmaxPartsMax = 4096;
+constexpr int kSplitMax = 64;
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
+
+struct Layout {
+  size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, rope_cos, rope_sin, kc, vc;
+  size_t total;
+};
+
+bool config_ok(const dec_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (!c) return bad("NULL config");
+  if (c->layers < 1 || c->hidden < 1 || c->inter < 1 || c->n_q < 1 || c->n_kv < 1 || c->head_dim < 1 || c->vocab < 1)
+    return bad("every geometry field must be positive");
+  if (c->n_q % c->n_kv) return bad("n_q must be a multiple of n_kv");
+  if (c->n_q / c->n_kv > 8) return bad("at most 8 query heads per key/value head");
+  if (c->head_dim % 4 || c->head_dim > 128) return bad("head_dim must be a multiple of 4 and <= 128");
+  if (c->hidden % 8 || c->inter % 8 || (c->n_q * c->head_dim) % 8)
+    return bad("hidden, inter and n_q*head_dim must be multiples of 8");
+  if (c->wdtype != DEC_F32 && c->wdtype != DEC_BF16) return bad("wdtype must be DEC_F32 or DEC_BF16");
+  if (c->kvdtype != DEC_F32 && c->kvdtype != DEC_BF16) return bad("kvdtype must be DEC_F32 or DEC_BF16");
+  if (c->max_seq < 1) return bad("max_seq must be >= 1");
+  if (c->chunk_cap < 0) return bad("chunk_cap must be >= 0");
+  if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("eps >= 0 and rope_theta > 0 required");
+  return true;
+}
+
+Layout make_layout(const dec_config& c) {
+  Layout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + bytes);
+    return at;
+  };
+  const size_t qw = static_cast<size_t>(c.n_q) * c.head_dim, kvw = static_cast<size_t>(c.n_kv) * c.head_dim;
+  const int group = c.n_q / c.n_kv;
+  L.ctrl = take(64 * 4);
+  L.err = take(16);
+  L.tok = take((static_cast<size_t>(c.max_seq) + 1) * 4);
+  L.h = take(static_cast<size_t>(c.hidden) * 4);
+  L.qkv = take((qw + 2 * kvw) * 4);
+  L.attn = take(qw * 4);
+  L.act = take(static_cast<size_t>(c.inter) * 4);
+  L.logits = take(static_cast<size_t>(c.vocab) * 4);
+  L.apart = take(static_cast<size_t>(c.n_kv) * kSplitMax * group * (c.head_dim + 2) * 4);
+  L.acnt = take(static_cast<size_t>(c.n_kv) * 4);
+  L.mval = take(kArgmaxPartsMax * 4);
+  L.midx = take(kArgmaxPartsMax * 4);
+  L.mcnt = take(16);
+  L.rope_cos = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
+  L.rope_sin = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
+  const size_t cache = static_cast<size_t>(c.layers) * kvw * c.max_seq * dtype_bytes(c.kvdtype);
+  L.kc = take(cache);
+  L.vc = take(cache);
+  L.total = o;
+  return L;
+}
+
+struct Plan {  // launch shape of one decoder GEMV
+  int grid = 0, seg = 0, spr = 0;
+  size_t smem = 0;
+};
+
+Plan plan_gemv(int out, int in, int elem, int row_unit, int sms, int max_grid) {
+  Plan p;
+  const long long rb = static_cast<long long>(in) * elem;
+  int spr = static_cast<int>((rb + kSEG - 1) / kSEG);
+  p.seg = static_cast<int>(((rb + spr - 1) / spr + 15) / 16 * 16);
+  p.spr = static_cast<int>((rb + p.seg - 1) / p.seg);
+  const int units = out / row_unit;
+  p.grid = units < sms ? units : sms;
+  if (p.grid > max_grid) p.grid = max_grid;
+  int max_rows = (units + p.grid - 1) / p.grid * row_unit;
+  while (static_cast<size_t>(max_rows) * p.spr * 4 > 64 * 1024 && p.grid * 2 <= max_grid) {
+    p.grid *= 2;
+    max_rows = (units + p.grid - 1) / p.grid * row_unit;
+  }
+  p.smem = gemv_smem_bytes(gemv_ring_bytes<kNW, kNS, kSEG>(), in, max_rows, p.spr);
+  return p;
+}
+
+__global__ void advance_kernel(int32_t* ctrl) {
+  pdl_wait();
+  if (threadIdx.x == 0) ctrl[0] += 1;
+}
+
+}  // namespace
+
+struct dec_ctx {
+  dec_config cfg{};
+  DeviceInfo di{};
+  char* ws = nullptr;
+  size_t ws_bytes = 0;
+  Layout L{};
+  cudaStream_t stream = nullptr;
+  cudaStream_t cap = nullptr;
+  bool have_weights = false;
+  dec_weights w{};
+  std::vector<dec_layer_weights> layers;
+  int32_t pos = 0;
+  int32_t* h_tok = nullptr;   // pinned [max_seq + 1], one slot per position
+  int32_t* h_next = nullptr;  // pinned
+  cudaGraphExec_t g_full = nullptr, g_body = nullptr;
+  Plan p_qkv, p_o, p_gu, p_down, p_vocab;
+  size_t attn_smem = 0;
+  int nsplit_max = 1;
+  std::string err;
+
+  template <typename T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(ws + off);
+  }
+  size_t kv_layer_elems() const { return static_cast<size_t>(cfg.n_kv) * cfg.max_seq * cfg.head_dim; }
+};
+
+namespace {
+
+template <typename WT, int PRO, int EPI>
+dec_status launch_dec_gemv(dec_ctx* c, const Plan& p, const GemvArgs& a, cudaStream_t st, bool pdl) {
+  auto kern = gemv_stream_kernel<WT, float, PRO, EPI, kNW, kNS, kSEG>;
+  WSG_CUDA_TRY(&c->err, launch_k(kern, dim3(p.grid), dim3(kNW * 32), p.smem, st, pdl, a));
+  return DEC_OK;
+}
+
+// Raise the dynamic shared-memory limit of every kernel a step launches (once,
+// outside stream capture).
+template <typename WT>
+dec_status prepare_kernels(dec_ctx* c) {
+  std::string* e = &c->err;
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_EMBED_NORM, EPI_STORE, kNW, kNS, kSEG>, c->p_qkv.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_STORE, kNW, kNS, kSEG>, c->p_qkv.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_X, EPI_RESID, kNW, kNS, kSEG>,
+                             c->p_o.smem > c->p_down.smem ? c->p_o.smem : c->p_down.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_SWIGLU, kNW, kNS, kSEG>, c->p_gu.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_ARGMAX, kNW, kNS, kSEG>, c->p_vocab.smem));
+  WSG_CUDA_TRY(e, allow_smem(attn_decode_kernel<float, 2>, c->attn_smem));
+  WSG_CUDA_TRY(e, allow_smem(attn_decode_kernel<float, 8>, c->attn_smem));
+  WSG_CUDA_TRY(e, allow_smem(attn_decode_kernel<uint16_t, 2>, c->attn_smem));
+  WSG_CUDA_TRY(e, allow_smem(attn_decode_kernel<uint16_t, 8>, c->attn_smem));
+  return DEC_OK;
+}
+
+GemvArgs base_args(dec_ctx* c, const Plan& p, int out, int in) {
+  GemvArgs a = {};
+  a.out = out;
+  a.in = in;
+  a.row_bytes = in * static_cast<int>(dtype_bytes(c->cfg.wdtype));
+  a.seg_bytes = p.seg;
+  a.segs_per_row = p.spr;
+  a.row_unit = 1;
+  a.eps = c->cfg.eps;
+  a.vocab = c->cfg.vocab;
+  a.ctrl = c->at<int32_t>(c->L.ctrl);
+  a.tok = c->at<int32_t>(c->L.tok);
+  a.err = c->at<uint32_t>(c->L.err);
+  return a;
+}
+
+RowMap single(const void* p, int out) {
+  RowMap m = {};
+  m.base[0] = m.base[1] = m.base[2] = static_cast<const char*>(p);
+  m.split1 = m.split2 = out;
+  return m;
+}
+
+template <typename WT>
+dec_status enqueue_step_t(dec_ctx* c, cudaStream_t st, bool full) {
+  const dec_config& g = c->cfg;
+  const int H = g.hidden, I = g.inter, d = g.head_dim;
+  const int qw = g.n_q * d, kvw = g.n_kv * d;
+  const int group = g.n_q / g.n_kv;
+  dec_status s;
+  for (int l = 0; l < g.layers; ++l) {
+    const dec_layer_weights& lw = c->layers[l];
+    // QKV projection with the input RMSNorm (layer 0: of the embedding row).
+    {
+      GemvArgs a = base_args(c, c->p_qkv, qw + 2 * kvw, H);
+      a.w.base[0] = static_cast<const char*>(lw.w_q);
+      a.w.base[1] = static_cast<const char*>(lw.w_k);
+      a.w.base[2] = static_cast<const char*>(lw.w_v);
+      a.w.split1 = qw;
+      a.w.split2 = qw + kvw;
+      a.norm_g = lw.g_in;
+      a.y = c->at<float>(c->L.qkv);
+      if (l == 0) {
+        a.embed = c->w.embed;
+        a.h_out = c->at<float>(c->L.h);
+        s = launch_dec_gemv<WT, PRO_EMBED_NORM, EPI_STORE>(c, c->p_qkv, a, st, false);
+      } else {
+        a.x = c->at<float>(c->L.h);
+        s = launch_dec_gemv<WT, PRO_NORM, EPI_STORE>(c, c->p_qkv, a, st, true);
+      }
+      if (s != DEC_OK) return s;
+    }
+    // Attention with Q/K norm, RoPE and the KV append.
+    {
+      AttnArgs a = {};
+      a.qkv = c->at<float>(c->L.qkv);
+      a.g_q = lw.g_q;
+      a.g_k = lw.g_k;
+      a.eps = g.eps;
+      a.rope_cos = c->at<float>(c->L.rope_cos);
+      a.rope_sin = c->at<float>(c->L.rope_sin);
+      a.ctrl = c->at<int32_t>(c->L.ctrl);
+      const size_t off = static_cast<size_t>(l) * c->kv_layer_elems() * dtype_bytes(g.kvdtype);
+      a.kc = c->ws + c->L.kc + off;
+      a.vc = c->ws + c->L.vc + off;
+      a.max_seq = g.max_seq;
+      a.n_q = g.n_q;
+      a.n_kv = g.n_kv;
+      a.d = d;
+      a.out = c->at<float>(c->L.attn);
+      a.part = c->at<float>(c->L.apart);
+      a.counter = c->at<uint32_t>(c->L.acnt);
+      a.nsplit_max = c->nsplit_max;
+      a.tmin = 64;
+      a.scale = 1.0f / sqrtf(static_cast<float>(d));
+      a.err = c->at<uint32_t>(c->L.err);
+      cudaError_t e;
+      if (g.kvdtype == DEC_F32) {
+        auto k = (group <= 2) ? attn_decode_kernel<float, 2> : attn_decode_kernel<float, 8>;
+        e = launch_k(k, dim3(g.n_kv, c->nsplit_max), dim3(kAttnWarps * 32), c->attn_smem, st, true, a);
+      } else {
+        auto k = (group <= 2) ? attn_decode_kernel<uint16_t, 2> : attn_decode_kernel<uint16_t, 8>;
+        e = launch_k(k, dim3(g.n_kv, c->nsplit_max), dim3(kAttnWarps * 32), c->attn_smem, st, true, a);
+      }
+      WSG_CUDA_TRY(&c->err, e);
+    }
+    // Output projection + residual.
+    {
+      GemvArgs a = base_args(c, c->p_o, H, qw);
+      a.w = single(lw.w_o, H);
+      a.x = c->at<float>(c->L.attn);
+      a.y = c->at<float>(c->L.h);
+      if ((s = launch_dec_gemv<WT, PRO_X, EPI_RESID>(c, c->p_o, a, st, true)) != DEC_OK) return s;
+    }
+    // Gate/up projection (rows interleaved gate_i, up_i) with RMSNorm and SwiGLU.
+    {
+      GemvArgs a = base_args(c, c->p_gu, 2 * I, H);
+      a.w.base[0] = static_cast<const char*>(lw.w_gate);
+      a.w.base[1] = static_cast<const char*>(lw.w_up);
+      a.w.base[2] = a.w.base[0];
+      a.w.interleave = 1;
+      a.row_unit = 2;
+      a.x = c->at<float>(c->L.h);
+      a.norm_g = lw.g_post;
+      a.y = c->at<float>(c->L.act);
+      if ((s = launch_dec_gemv<WT, PRO_NORM, EPI_SWIGLU>(c, c->p_gu, a, st, true)) != DEC_OK) return s;
+    }
+    // Down projection + residual.
+    {
+      GemvArgs a = base_args(c, c->p_down, H, I);
+      a.w = single(lw.w_down, H);
+      a.x = c->at<float>(c->L.act);
+      a.y = c->at<float>(c->L.h);
+      if ((s = launch_dec_gemv<WT, PRO_X, EPI_RESID>(c, c->p_down, a, st, true)) != DEC_OK) return s;
+    }
+  }
+  if (full) {
+    GemvArgs a = base_args(c, c->p_vocab, g.vocab, H);
+    a.w = single(c->w.embed, g.vocab);
+    a.x = c->at<float>(c->L.h);
+    a.norm_g = c->w.g_final;
+    a.y = c->at<float>(c->L.logits);
+    a.part_val = c->at<float>(c->L.mval);
+    a.part_idx = c->at<int32_t>(c->L.midx);
+    a.counter = c->at<uint32_t>(c->L.mcnt);
+    a.tok_w = c->at<int32_t>(c->L.tok);
+    if ((s = launch_dec_gemv<WT, PRO_NORM, EPI_ARGMAX>(c, c->p_vocab, a, st, true)) != DEC_OK) return s;
+  } else {
+    WSG_CUDA_TRY(&c->err, launch_k(advance_kernel, dim3(1), dim3(32), 0, st, true, c->at<int32_t>(c->L.ctrl)));
+  }
+  return DEC_OK;
+}
+
+dec_status capture(dec_ctx* c, bool full, cudaGraphExec_t* out) {
+  WSG_CUDA_TRY(&c->err, cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
+  dec_status s = c->cfg.wdtype == DEC_F32 ? enqueue_step_t<float>(c, c->cap, full)
+                                          : enqueue_step_t<uint16_t>(c, c->cap, full);
+  cudaGraph_t graph = nullptr;
+  cudaError_t e = cudaStreamEndCapture(c->cap, &graph);
+  if (s != DEC_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return s;
+  }
+  if (e != cudaSuccess) return fail(&c->err, DEC_ECUDA, "graph capture failed: %s", cudaGetErrorString(e));
+  e = cudaGraphInstantiate(out, graph, 0);
+  cudaGraphDestroy(graph);
+  if (e != cudaSuccess) return fail(&c->err, DEC_ECUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  return DEC_OK;
+}
+
+dec_status ensure_graphs(dec_ctx* c, bool full) {
+  if (full && !c->g_full) return capture(c, true, &c->g_full);
+  if (!full && !c->g_body) return capture(c, false, &c->g_body);
+  return DEC_OK;
+}
+
+dec_status run_steps(dec_ctx* c, bool full, int n) {
+  dec_status s = ensure_graphs(c, full);
+  if (s != DEC_OK) return s;
+  for (int i = 0; i < n; ++i) WSG_CUDA_TRY(&c->err, cudaGraphLaunch(full ? c->g_full : c->g_body, c->stream));
+  return DEC_OK;
+}
+
+dec_status put_tokens(dec_ctx* c, const int32_t* toks, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (toks[i] < 0 || toks[i] >= c->cfg.vocab)
+      return fail(&c->err, DEC_EINVAL, "token %d at row %d is outside [0, %d)", toks[i], i, c->cfg.vocab);
+  }
+  std::memcpy(c->h_tok + c->pos, toks, sizeof(int32_t) * n);
+  WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->at<int32_t>(c->L.tok) + c->pos, c->h_tok + c->pos, sizeof(int32_t) * n,
+                                        cudaMemcpyHostToDevice, c->stream));
+  return DEC_OK;
+}
+
+dec_status finish_head(dec_ctx* c, int32_t last_pos, float* d_logits, int32_t* h_next) {
+  if (d_logits)
+    WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(d_logits, c->at<float>(c->L.logits), sizeof(float) * c->cfg.vocab,
+                                          cudaMemcpyDeviceToDevice, c->stream));
+  if (h_next) {
+    WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->h_next, c->at<int32_t>(c->L.tok) + last_pos + 1, sizeof(int32_t),
+                                          cudaMemcpyDeviceToHost, c->stream));
+    WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
+    *h_next = *c->h_next;
+  }
+  return DEC_OK;
+}
+
+}  // namespace
+
+extern "C" size_t dec_workspace_bytes(const dec_config* cfg) {
+  if (!config_ok(cfg, nullptr)) return 0;
+  return make_layout(*cfg).total;
+}
+
+extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_t workspace_bytes, void* stream,
+                                 dec_ctx** out) {
+  std::string why;
+  if (!out) return fail(nullptr, DEC_EINVAL, "dec_create: NULL output handle");
+  *out = nullptr;
+  if (!config_ok(cfg, &why)) return fail(nullptr, DEC_EINVAL, "dec_create: %s", why.c_str());
+  if (!d_workspace || (reinterpret_cast<uintptr_t>(d_workspace) % kAlign))
+    return fail(nullptr, DEC_EINVAL, "dec_create: workspace must be non-NULL and 256-byte aligned");
+  const Layout L = make_layout(*cfg);
+  if (workspace_bytes < L.total)
+    return fail(nullptr, DEC_ENOMEM, "dec_create: workspace has %zu bytes, %zu needed", workspace_bytes, L.total);
+  DeviceInfo di;
+  dec_status s = device_info(&di, nullptr);
+  if (s != DEC_OK) return s;
+
+  dec_ctx* c = new (std::nothrow) dec_ctx();
+  if (!c) return fail(nullptr, DEC_ENOMEM, "dec_create: out of host memory");
+  c->cfg = *cfg;
+  c->di = di;
+  c->ws = static_cast<char*>(d_workspace);
+  c->ws_bytes = workspace_bytes;
+  c->L = L;
+  c->stream = static_cast<cudaStream_t>(stream);
+  auto bail = [&](dec_status st) {
+    dec_destroy(c);
+    return st;
+  };
+  cudaError_t e = cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaMallocHost(&c->h_tok, sizeof(int32_t) * (cfg->max_seq + 1));
+  if (e == cudaSuccess) e = cudaMallocHost(&c->h_next, sizeof(int32_t));
+  if (e != cudaSuccess) return bail(fail(nullptr, DEC_ECUDA, "dec_create: %s", cudaGetErrorString(e)));
+
+  // Rotary table: angle = p * theta^(-2i/d), evaluated in double, stored float32.
+  const int half = cfg->head_dim / 2;
+  std::vector<float> cs(static_cast<size_t>(cfg->max_seq) * half), sn(cs.size());
+  for (int i = 0; i < half; ++i) {
+    const double inv = std::pow(static_cast<double>(cfg->rope_theta), -2.0 * i / cfg->head_dim);
+    for (int p = 0; p < cfg->max_seq; ++p) {
+      const double ang = static_cast<double>(p) * inv;
+      cs[static_cast<size_t>(p) * half + i] = static_cast<float>(std::cos(ang));
+      sn[static_cast<size_t>(p) * half + i] = static_cast<float>(std::sin(ang));
+    }
+  }
+  e = cudaMemcpy(c->ws + L.rope_cos, cs.data(), cs.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(c->ws + L.rope_sin, sn.data(), sn.size() * 4, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemset(c->ws, 0, L.rope_cos);           // control, activations, partials
+  if (e == cudaSuccess) e = cudaMemset(c->ws + L.kc, 0, L.total - L.kc);  // caches
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return bail(fail(nullptr, DEC_ECUDA, "dec_create: %s", cudaGetErrorString(e)));
+
+  const int welem = static_cast<int>(dtype_bytes(cfg->wdtype));
+  const int qw = cfg->n_q * cfg->head_dim, kvw = cfg->n_kv * cfg->head_dim;
+  c->p_qkv = plan_gemv(qw + 2 * kvw, cfg->hidden, welem, 1, di.sms, di.sms);
+  c->p_o = plan_gemv(cfg->hidden, qw, welem, 1, di.sms, di.sms);
+  c->p_gu = plan_gemv(2 * cfg->inter, cfg->hidden, welem, 2, di.sms, di.sms);
+  c->p_down = plan_gemv(cfg->hidden, cfg->inter, welem, 1, di.sms, di.sms);
+  c->p_vocab = plan_gemv(cfg->vocab, cfg->hidden, welem, 1, di.sms, kArgmaxPartsMax);
+  for (const Plan* p : {&c->p_qkv, &c->p_o, &c->p_gu, &c->p_down, &c->p_vocab})
+    if (p->smem > di.smem_optin)
+      return bail(fail(nullptr, DEC_EINVAL, "dec_create: a projection needs %zu B of shared memory (max %zu)", p->smem,
+                       di.smem_optin));
+  c->attn_smem = attn_smem_bytes(cfg->n_q / cfg->n_kv, cfg->head_dim);
+  c->nsplit_max = di.sms / cfg->n_kv;
+  if (c->nsplit_max < 1) c->nsplit_max = 1;
+  if (c->nsplit_max > kSplitMax) c->nsplit_max = kSplitMax;
+  s = cfg->wdtype == DEC_F32 ? prepare_kernels<float>(c) : prepare_kernels<uint16_t>(c);
+  if (s != DEC_OK) {
+    thread_error() = c->err;
+    return bail(s);
+  }
+  *out = c;
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_load_weights: NULL context");
+  if (!w || !w->embed || !w->g_final || !w->layers) return fail(&c->err, DEC_EINVAL, "dec_load_weights: NULL pointer");
+  auto ok = [](const void* p) { return p && aligned16(p); };
+  if (!ok(w->embed) || !ok(w->g_final)) return fail(&c->err, DEC_EINVAL, "dec_load_weights: embed/g_final misaligned");
+  for (int l = 0; l < c->cfg.layers; ++l) {
+    const dec_layer_weights& x = w->layers[l];
+    const void* ps[] = {x.w_q, x.w_k, x.w_v, x.w_o, x.w_gate, x.w_up, x.w_down, x.g_in, x.g_post, x.g_q, x.g_k};
+    for (const void* p : ps)
+      if (!ok(p)) return fail(&c->err, DEC_EINVAL, "dec_load_weights: layer %d has a NULL or misaligned tensor", l);
+  }
+  c->layers.assign(w->layers, w->layers + c->cfg.layers);
+  c->w = *w;
+  c->w.layers = c->layers.data();
+  // Graphs bake in the weight pointers: drop any captured with older ones.
+  if (c->g_full) cudaGraphExecDestroy(c->g_full);
+  if (c->g_body) cudaGraphExecDestroy(c->g_body);
+  c->g_full = c->g_body = nullptr;
+  c->have_weights = true;
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_reset(dec_ctx* c) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_reset: NULL context");
+  // Earlier asynchronous copies may still read the pinned token slots.
+  WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
+  c->pos = 0;
+  WSG_CUDA_TRY(&c->err, cudaMemsetAsync(c->ws + c->L.ctrl, 0, 64 * 4, c->stream));
+  WSG_CUDA_TRY(&c->err, cudaMemsetAsync(c->ws + c->L.kc, 0, c->L.total - c->L.kc, c->stream));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_step(dec_ctx* c, int32_t token, uint32_t flags, float* d_logits, int32_t* h_next) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_step: NULL context");
+  if (flags & ~DEC_SKIP_LOGITS) return fail(&c->err, DEC_EINVAL, "dec_step: unknown flags 0x%x", flags);
+  const bool full = !(flags & DEC_SKIP_LOGITS);
+  if (!full && (d_logits || h_next))
+    return fail(&c->err, DEC_EINVAL, "dec_step: DEC_SKIP_LOGITS with a logits or token output");
+  if (!c->have_weights) return fail(&c->err, DEC_ESTATE, "dec_step: weights not loaded");
+  if (c->pos >= c->cfg.max_seq)
+    return fail(&c->err, DEC_ECAPACITY, "dec_step: position %d reached max_seq %d", c->pos, c->cfg.max_seq);
+  dec_status s = ensure_graphs(c, full);
+  if (s != DEC_OK) return s;
+  if ((s = put_tokens(c, &token, 1)) != DEC_OK) return s;
+  if ((s = run_steps(c, full, 1)) != DEC_OK) return s;
+  const int32_t p = c->pos;
+  c->pos += 1;
+  if (full) return finish_head(c, p, d_logits, h_next);
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_prefill_chunk(dec_ctx* c, const int32_t* h_tokens, int32_t n, int32_t is_last,
+                                        float* d_logits, int32_t* h_next) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_prefill_chunk: NULL context");
+  if (!h_tokens || n < 1) return fail(&c->err, DEC_EINVAL, "dec_prefill_chunk: need n >= 1 tokens");
+  if (!is_last && (d_logits || h_next))
+    return fail(&c->err, DEC_EINVAL, "dec_prefill_chunk: outputs requested from a non-final chunk");
+  if (!c->have_weights) return fail(&c->err, DEC_ESTATE, "dec_prefill_chunk: weights not loaded");
+  if (static_cast<long long>(c->pos) + n > c->cfg.max_seq)
+    return fail(&c->err, DEC_ECAPACITY, "dec_prefill_chunk: %d rows at position %d exceed max_seq %d", n, c->pos,
+                c->cfg.max_seq);
+  dec_status s = ensure_graphs(c, false);
+  if (s == DEC_OK && is_last) s = ensure_graphs(c, true);
+  if (s != DEC_OK) return s;
+  if ((s = put_tokens(c, h_tokens, n)) != DEC_OK) return s;
+  const int body = is_last ? n - 1 : n;
+  if ((s = run_steps(c, false, body)) != DEC_OK) return s;
+  const int32_t p0 = c->pos;
+  if (is_last && (s = run_steps(c, true, 1)) != DEC_OK) return s;
+  c->pos += n;
+  if (is_last) return finish_head(c, p0 + n - 1, d_logits, h_next);
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_generate(dec_ctx* c, int32_t token, int32_t n, int32_t* d_tokens_out) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_generate: NULL context");
+  if (n < 1 || !d_tokens_out) return fail(&c->err, DEC_EINVAL, "dec_generate: need n >= 1 and an output buffer");
+  if (!c->have_weights) return fail(&c->err, DEC_ESTATE, "dec_generate: weights not loaded");
+  if (static_cast<long long>(c->pos) + n > c->cfg.max_seq)
+    return fail(&c->err, DEC_ECAPACITY, "dec_generate: %d steps at position %d exceed max_seq %d", n, c->pos,
+                c->cfg.max_seq);
+  dec_status s = ensure_graphs(c, true);
+  if (s != DEC_OK) return s;
+  if ((s = put_tokens(c, &token, 1)) != DEC_OK) return s;
+  if ((s = run_steps(c, true, n)) != DEC_OK) return s;
+  WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(d_tokens_out, c->at<int32_t>(c->L.tok) + c->pos + 1, sizeof(int32_t) * n,
+                                        cudaMemcpyDeviceToDevice, c->stream));
+  c->pos += n;
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_get_kv(const dec_ctx* c, int32_t layer, const void** d_k, const void** d_v,
+                                 int32_t* n_valid) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_get_kv: NULL context");
+  if (layer < 0 || layer >= c->cfg.layers) return fail(nullptr, DEC_EINVAL, "dec_get_kv: layer %d", layer);
+  const size_t off = static_cast<size_t>(layer) * c->kv_layer_elems() * dtype_bytes(c->cfg.kvdtype);
+  if (d_k) *d_k = c->ws + c->L.kc + off;
+  if (d_v) *d_v = c->ws + c->L.vc + off;
+  if (n_valid) *n_valid = c->pos;
+  return DEC_OK;
+}
+
+extern "C" int32_t dec_position(const dec_ctx* c) { return c ? c->pos : -1; }
+
+extern "C" dec_status dec_device_errors(dec_ctx* c, int32_t clear, uint32_t* bits) {
+  if (!c || !bits) return fail(nullptr, DEC_EINVAL, "dec_device_errors: NULL argument");
+  WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
+  WSG_CUDA_TRY(&c->err, cudaMemcpy(bits, c->ws + c->L.err, sizeof(uint32_t), cudaMemcpyDeviceToHost));
+  if (clear) WSG_CUDA_TRY(&c->err, cudaMemset(c->ws + c->L.err, 0, sizeof(uint32_t)));
+  return DEC_OK;
+}
+
+extern "C" void dec_destroy(dec_ctx* c) {
+  if (!c) return;
+  if (c->stream || c->cap) cudaStreamSynchronize(c->stream);
+  if (c->g_full) cudaGraphExecDestroy(c->g_full);
+  if (c->g_body) cudaGraphExecDestroy(c->g_body);
+  if (c->cap) cudaStreamDestroy(c->cap);
+  if (c->h_tok) cudaFreeHost(c->h_tok);
+  if (c->h_next) cudaFreeHost(c->h_next);
+  delete c;
+}
+
+extern "C" const char* dec_last_error(const dec_ctx* c) {
+  if (c) return c->err.c_str();
+  return thread_error().c_str();
+}

@@ -1,0 +1,326 @@
+// Standalone matrix-vector products: gemv (float32 / bfloat16 weights) and
+// gemv_q4 (4-bit groupwise-affine weights, one or two tokens).
+//
+// "Our Kernel Benchmark Was Measuring the System Cache" measures exactly
+// these products cold: every call streams a weight matrix that is not in
+// cache. gemv uses the bulk-copy streaming engine of gemv_stream.cuh; gemv_q4
+// dequantises in registers.
+#include <cuda_fp16.h>
+
+#include <mutex>
+
+#include "common.h"
+#include "gemv_stream.cuh"
+
+namespace wsg {
+
+std::string& thread_error() {
+  static thread_local std::string s;
+  return s;
+}
+
+dec_status device_info(DeviceInfo* out, std::string* err) {
+  static std::mutex mu;
+  static DeviceInfo cache[64];
+  int dev = 0;
+  WSG_CUDA_TRY(err, cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(err, DEC_EDEVICE, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (cache[dev].device != dev) {
+    cudaDeviceProp p;
+    WSG_CUDA_TRY(err, cudaGetDeviceProperties(&p, dev));
+    if (p.major != 10 || p.minor != 3)
+      return fail(err, DEC_EDEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, p.major,
+                  p.minor);
+    cache[dev].device = dev;
+    cache[dev].sms = p.multiProcessorCount;
+    cache[dev].major = p.major;
+    cache[dev].minor = p.minor;
+    cache[dev].smem_optin = p.sharedMemPerBlockOptin;
+  }
+  *out = cache[dev];
+  return DEC_OK;
+}
+
+// Device error word of the context-free entry points.
+__device__ uint32_t g_gemv_err;
+
+namespace {
+
+constexpr int kNW = 8, kNS = 3, kSEG = 4096;
+
+__global__ void fill_zero_kernel(float* y, int n) {
+  pdl_wait();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) y[i] = 0.f;
+}
+
+// Any-alignment fallback: one warp per row, element loads, float32 accumulation,
+// lane partials reduced by a fixed shuffle tree.
+template <typename WT, typename XT>
+__global__ void gemv_plain_kernel(const WT* __restrict__ W, const XT* __restrict__ x, float* __restrict__ y, int out,
+                                  int in) {
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int warps = gridDim.x * (blockDim.x >> 5);
+  for (int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); row < out; row += warps) {
+    const WT* w = W + static_cast<size_t>(row) * in;
+    float acc = 0.f;
+    for (int j = lane; j < in; j += 32) acc = fmaf(load_f32<WT>(w, j), load_f32<XT>(x, j), acc);
+    acc = warp_sum(acc);
+    if (lane == 0) y[row] = acc;
+  }
+}
+
+// ---- 4-bit groupwise-affine GEMV ----
+//
+// Lane l of a warp handles 32-column chunks c = l, l+32, ... of R rows at a
+// time; one 16-byte load brings a chunk's 32 codes. Each code q becomes the
+// float 0.5 + q/256 with one byte permute (exponent byte 0x3F, code in the
+// third byte), so S = sum (0.5 + q/256) x = X/2 + (sum q x)/256 over the chunk
+// and the chunk's contribution s*sum(q x) + b*X equals 256 s S + (b - 128 s) X,
+// with X the chunk's column sum of x (staged once per CTA). A chunk is half of
+// a 64-column group, so it has a single (s, b).
+template <int R, int NTOK>
+__global__ void __launch_bounds__(256) gemv_q4_kernel(const uint32_t* __restrict__ codes,
+                                                      const __half* __restrict__ sc, const __half* __restrict__ bi,
+                                                      const uint16_t* __restrict__ x, float* __restrict__ y, int out,
+                                                      int in) {
+  extern __shared__ float4 q4_smem[];
+  const int nch = in >> 5;
+  float4* xs4 = q4_smem;                                     // [NTOK][8][nch]
+  float* xsum = reinterpret_cast<float*>(xs4 + NTOK * 8 * nch);  // [NTOK][nch]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  pdl_trigger();
+  pdl_wait();
+  for (int idx = tid; idx < NTOK * nch * 8; idx += blockDim.x) {
+    const int t = idx / (nch * 8), rem = idx - t * nch * 8, c = rem >> 3, k = rem & 7;
+    const uint16_t* xp = x + static_cast<size_t>(t) * in + 32 * c + 4 * k;
+    xs4[(t * 8 + k) * nch + c] = make_float4(bf16_to_f32(xp[0]), bf16_to_f32(xp[1]), bf16_to_f32(xp[2]),
+                                             bf16_to_f32(xp[3]));
+  }
+  for (int idx = tid; idx < NTOK * nch; idx += blockDim.x) {
+    const int t = idx / nch, c = idx - t * nch;
+    const uint16_t* xp = x + static_cast<size_t>(t) * in + 32 * c;
+    float s = 0.f;
+    for (int j = 0; j < 32; ++j) s += bf16_to_f32(xp[j]);
+    xsum[t * nch + c] = s;
+  }
+  __syncthreads();
+
+  const int words_per_row = in >> 3, groups_per_row = in >> 6;
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  for (int rb = (blockIdx.x * (blockDim.x >> 5) + warp) * R; rb < out; rb += warps_total * R) {
+    float acc[R][NTOK];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
+
+    for (int c = lane; c < nch; c += 32) {
+      uint4 q[R];
+      float s[R], b[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = rb + r;
+        if (row < out) {
+          const uint32_t* p = codes + static_cast<size_t>(row) * words_per_row + 4 * c;
+          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(q[r].x), "=r"(q[r].y), "=r"(q[r].z), "=r"(q[r].w)
+                       : "l"(p));
+          s[r] = __half2float(sc[static_cast<size_t>(row) * groups_per_row + (c >> 1)]);
+          b[r] = __half2float(bi[static_cast<size_t>(row) * groups_per_row + (c >> 1)]);
+        } else {
+          q[r] = make_uint4(0, 0, 0, 0);
+          s[r] = b[r] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) {
+        float xv[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 v = xs4[(t * 8 + k) * nch + c];
+          xv[4 * k] = v.x;
+          xv[4 * k + 1] = v.y;
+          xv[4 * k + 2] = v.z;
+          xv[4 * k + 3] = v.w;
+        }
+        const float X = xsum[t * nch + c];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint32_t wd[4] = {q[r].x, q[r].y, q[r].z, q[r].w};
+          float S0 = 0.f, S1 = 0.f;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t lo = wd[m] & 0x0F0F0F0Fu;         // codes 0,2,4,6 of the word
+            const uint32_t hi = (wd[m] >> 4) & 0x0F0F0F0Fu;  // codes 1,3,5,7
+            S0 = fmaf(__uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7044)), xv[8 * m + 0], S0);
+            S1 = fmaf(__uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7044)), xv[8 * m + 1], S1);
+            S0 = fmaf(__uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7144)), xv[8 * m + 2], S0);
+            S1 = fmaf(__uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7144)), xv[8 * m + 3], S1);
+            S0 = fmaf(__uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7244)), xv[8 * m + 4], S0);
+            S1 = fmaf(__uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7244)), xv[8 * m + 5], S1);
+            S0 = fmaf(__uint_as_float(__byte_perm(lo, 0x3F000000u, 0x7344)), xv[8 * m + 6], S0);
+            S1 = fmaf(__uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7344)), xv[8 * m + 7], S1);
+          }
+          const float S = S0 + S1;
+          acc[r][t] = fmaf(256.f * s[r], S, fmaf(b[r] - 128.f * s[r], X, acc[r][t]));
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) {
+        const float v = warp_sum(acc[r][t]);
+        if (lane == 0 && rb + r < out) y[static_cast<size_t>(t) * out + rb + r] = v;
+      }
+  }
+}
+
+int g_q4_rows[3] = {0, 1, 2};  // rows per warp for ntok = 1, 2 (index by ntok)
+
+template <int R, int NTOK>
+dec_status launch_q4_r(const uint32_t* codes, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
+                       int out, int in, cudaStream_t st, const DeviceInfo& di) {
+  auto kern = gemv_q4_kernel<R, NTOK>;
+  const size_t smem = static_cast<size_t>(NTOK) * (in >> 5) * (8 * sizeof(float4) + sizeof(float));
+  if (smem > di.smem_optin) return fail(nullptr, DEC_EINVAL, "gemv_q4: in=%d needs %zu B of shared memory", in, smem);
+  WSG_CUDA_TRY(nullptr, allow_smem(kern, smem));
+  int per_sm = 0;
+  WSG_CUDA_TRY(nullptr, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+  if (per_sm < 1) per_sm = 1;
+  const long long warps_needed = (static_cast<long long>(out) + R - 1) / R;
+  long long grid = static_cast<long long>(di.sms) * per_sm;
+  const long long grid_needed = (warps_needed + 7) / 8;
+  if (grid > grid_needed) grid = grid_needed;
+  if (grid < 1) grid = 1;
+  WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(static_cast<unsigned>(grid)), dim3(256), smem, st, true, codes,
+                                 reinterpret_cast<const __half*>(s), reinterpret_cast<const __half*>(b), x, y, out,
+                                 in));
+  return DEC_OK;
+}
+
+template <int NTOK>
+dec_status launch_q4(int R, const uint32_t* codes, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
+                     int out, int in, cudaStream_t st, const DeviceInfo& di) {
+  switch (R) {
+    case 1: return launch_q4_r<1, NTOK>(codes, s, b, x, y, out, in, st, di);
+    case 2: return launch_q4_r<2, NTOK>(codes, s, b, x, y, out, in, st, di);
+    case 4: return launch_q4_r<4, NTOK>(codes, s, b, x, y, out, in, st, di);
+    default: return launch_q4_r<8, NTOK>(codes, s, b, x, y, out, in, st, di);
+  }
+}
+
+template <typename WT, typename XT>
+dec_status launch_gemv(const void* W, const void* x, float* y, int out, int in, cudaStream_t st,
+                       const DeviceInfo& di) {
+  const int row_bytes_ok = (static_cast<long long>(in) * sizeof(WT)) % 16 == 0;
+  const long long row_bytes = static_cast<long long>(in) * sizeof(WT);
+  if (row_bytes_ok && aligned16(W) && row_bytes < (1ll << 30)) {
+    GemvArgs a = {};
+    a.w.base[0] = a.w.base[1] = a.w.base[2] = static_cast<const char*>(W);
+    a.w.split1 = a.w.split2 = out;
+    a.out = out;
+    a.in = in;
+    a.row_bytes = static_cast<int>(row_bytes);
+    int spr = static_cast<int>((row_bytes + kSEG - 1) / kSEG);
+    int seg = static_cast<int>(((row_bytes + spr - 1) / spr + 15) / 16 * 16);
+    spr = static_cast<int>((row_bytes + seg - 1) / seg);
+    a.seg_bytes = seg;
+    a.segs_per_row = spr;
+    a.row_unit = 1;
+    a.x = x;
+    a.err = nullptr;
+    int grid = out < di.sms ? out : di.sms;
+    int max_rows = (out + grid - 1) / grid;
+    // Keep the partial-dot array within shared memory by adding CTAs if needed.
+    while (static_cast<size_t>(max_rows) * spr * 4 > 64 * 1024) {
+      grid *= 2;
+      max_rows = (out + grid - 1) / grid;
+    }
+    const size_t smem = gemv_smem_bytes(gemv_ring_bytes<kNW, kNS, kSEG>(), in, max_rows, spr);
+    if (smem <= di.smem_optin) {
+      auto kern = gemv_stream_kernel<WT, XT, PRO_X, EPI_STORE, kNW, kNS, kSEG>;
+      uint32_t* errp = nullptr;
+      WSG_CUDA_TRY(nullptr, cudaGetSymbolAddress(reinterpret_cast<void**>(&errp), g_gemv_err));
+      a.err = errp;
+      a.y = y;
+      WSG_CUDA_TRY(nullptr, allow_smem(kern, smem));
+      WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(grid), dim3(kNW * 32), smem, st, true, a));
+      return DEC_OK;
+    }
+  }
+  const int blocks = static_cast<int>((static_cast<long long>(out) + 7) / 8);
+  const int grid = blocks < di.sms * 8 ? blocks : di.sms * 8;
+  WSG_CUDA_TRY(nullptr, launch_k(gemv_plain_kernel<WT, XT>, dim3(grid), dim3(256), 0, st, true,
+                                 static_cast<const WT*>(W), static_cast<const XT*>(x), y, out, in));
+  return DEC_OK;
+}
+
+}  // namespace
+}  // namespace wsg
+
+using namespace wsg;
+
+extern "C" dec_status gemv(int32_t wdtype, const void* d_W, const void* d_x, float* d_y, int32_t out, int32_t in,
+                           void* stream) {
+  if (out < 0 || in < 0) return fail(nullptr, DEC_EINVAL, "gemv: negative size out=%d in=%d", out, in);
+  if (wdtype != DEC_F32 && wdtype != DEC_BF16) return fail(nullptr, DEC_EINVAL, "gemv: wdtype %d", wdtype);
+  if (out == 0) return DEC_OK;
+  if (!d_y || (in > 0 && (!d_W || !d_x))) return fail(nullptr, DEC_EINVAL, "gemv: NULL pointer");
+  DeviceInfo di;
+  dec_status st = device_info(&di, nullptr);
+  if (st != DEC_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (in == 0) {
+    const int grid = (out + 255) / 256 < di.sms * 4 ? (out + 255) / 256 : di.sms * 4;
+    WSG_CUDA_TRY(nullptr, launch_k(fill_zero_kernel, dim3(grid), dim3(256), 0, s, true, d_y, out));
+    return DEC_OK;
+  }
+  if (wdtype == DEC_F32) return launch_gemv<float, float>(d_W, d_x, d_y, out, in, s, di);
+  return launch_gemv<uint16_t, uint16_t>(d_W, d_x, d_y, out, in, s, di);
+}
+
+extern "C" dec_status gemv_q4(const uint32_t* d_codes, const uint16_t* d_scale, const uint16_t* d_bias,
+                              const uint16_t* d_x, float* d_y, int32_t out, int32_t in, int32_t ntok, void* stream) {
+  if (out < 0 || in < 0) return fail(nullptr, DEC_EINVAL, "gemv_q4: negative size out=%d in=%d", out, in);
+  if (ntok != 1 && ntok != 2) return fail(nullptr, DEC_EINVAL, "gemv_q4: ntok must be 1 or 2, got %d", ntok);
+  if (in % 64) return fail(nullptr, DEC_EINVAL, "gemv_q4: in=%d is not a multiple of 64", in);
+  if (out == 0) return DEC_OK;
+  if (!d_y) return fail(nullptr, DEC_EINVAL, "gemv_q4: NULL output");
+  DeviceInfo di;
+  dec_status st = device_info(&di, nullptr);
+  if (st != DEC_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (in == 0) {
+    const long long n = static_cast<long long>(out) * ntok;
+    const int grid = static_cast<int>((n + 255) / 256 < di.sms * 4 ? (n + 255) / 256 : di.sms * 4);
+    WSG_CUDA_TRY(nullptr, launch_k(fill_zero_kernel, dim3(grid), dim3(256), 0, s, true, d_y, static_cast<int>(n)));
+    return DEC_OK;
+  }
+  if (!d_codes || !d_scale || !d_bias || !d_x) return fail(nullptr, DEC_EINVAL, "gemv_q4: NULL pointer");
+  if (!aligned16(d_codes)) return fail(nullptr, DEC_EINVAL, "gemv_q4: codes must be 16-byte aligned");
+  const int R = g_q4_rows[ntok];
+  if (ntok == 1) return launch_q4<1>(R, d_codes, d_scale, d_bias, d_x, d_y, out, in, s, di);
+  return launch_q4<2>(R, d_codes, d_scale, d_bias, d_x, d_y, out, in, s, di);
+}
+
+extern "C" int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r) {
+  if (ntok != 1 && ntok != 2) return -1;
+  if (r != 0 && r != 1 && r != 2 && r != 4 && r != 8) return -1;
+  if (r > 0) g_q4_rows[ntok] = r;
+  return g_q4_rows[ntok];
+}
+
+extern "C" dec_status gemv_device_errors(int32_t clear, uint32_t* bits) {
+  if (!bits) return fail(nullptr, DEC_EINVAL, "gemv_device_errors: NULL output");
+  WSG_CUDA_TRY(nullptr, cudaDeviceSynchronize());
+  WSG_CUDA_TRY(nullptr, cudaMemcpyFromSymbol(bits, g_gemv_err, sizeof(uint32_t)));
+  if (clear) {
+    const uint32_t z = 0;
+    WSG_CUDA_TRY(nullptr, cudaMemcpyToSymbol(g_gemv_err, &z, sizeof(uint32_t)));
+  }
+  return DEC_OK;
+}

@@ -1,0 +1,401 @@
+// Weight-streaming GEMV engine: y = W x for one activation vector.
+//
+// The matrix-vector products of the decode step read every weight exactly
+// once per token ("Our Kernel Benchmark Was Measuring the System Cache",
+// Summary: production decode streams every weight once per token), so the
+// kernel is built to keep HBM busy:
+//
+//  * one CTA per SM; each CTA owns a contiguous range of output rows, handed
+//    out in balanced units so no CTA gets more than one unit above average;
+//  * each row is cut into segments of at most SEG bytes; warp w of the CTA
+//    takes segments w, w + NW, w + 2NW, ... and streams them through its own
+//    ring of NS shared-memory slots with bulk (TMA) copies completed on
+//    mbarriers; the copies carry an L2 evict-first policy;
+//  * the first NS copies of every warp are issued before the kernel waits on
+//    its predecessor (programmatic dependent launch), so weight traffic of
+//    this kernel overlaps the tail of the previous one;
+//  * the activation vector is staged once per CTA in shared memory, with an
+//    optional fused RMSNorm prologue;
+//  * per-segment partial dots are reduced in a fixed order, so results are
+//    bit-reproducible run to run;
+//  * fused epilogues: plain store, residual add, SwiGLU on (gate, up) row
+//    pairs, and logits + two-pass lowest-ID argmax + position advance.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace wsg {
+
+enum Pro : int {
+  PRO_X = 0,           // x read from memory (XT), no norm
+  PRO_NORM = 1,        // x = RMSNorm(h) * g, h f32
+  PRO_EMBED_NORM = 2,  // h = embed[token]; x = RMSNorm(h) * g; CTA 0 stores h
+};
+
+enum Epi : int {
+  EPI_STORE = 0,   // y[row] = v
+  EPI_RESID = 1,   // y[row] += v
+  EPI_SWIGLU = 2,  // logical rows (2i, 2i+1) = (gate_i, up_i): y[i] = silu(gate_i) * up_i
+  EPI_ARGMAX = 3,  // y[row] = v (if y); greedy token of all rows -> tok[pos+1]; ctrl[0] = pos+1
+};
+
+struct RowMap {
+  const char* base[3];
+  int32_t split1, split2;  // logical rows [0,split1) -> base[0], [split1,split2) -> base[1], rest -> base[2]
+  int32_t interleave;      // nonzero: logical row 2i -> base[0] row i, 2i+1 -> base[1] row i
+};
+
+struct GemvArgs {
+  RowMap w;
+  int32_t out, in;
+  int32_t row_bytes, seg_bytes, segs_per_row, row_unit;
+  const void* x;
+  const float* norm_g;
+  float eps;
+  const void* embed;
+  const int32_t* tok;
+  int32_t* ctrl;
+  float* h_out;
+  float* y;
+  int32_t vocab;
+  float* part_val;
+  int32_t* part_idx;
+  uint32_t* counter;
+  int32_t* tok_w;
+  uint32_t* err;
+};
+
+__device__ __forceinline__ const char* row_ptr(const RowMap& m, int row, int row_bytes) {
+  if (m.interleave) return m.base[row & 1] + static_cast<size_t>(row >> 1) * row_bytes;
+  if (row < m.split1) return m.base[0] + static_cast<size_t>(row) * row_bytes;
+  if (row < m.split2) return m.base[1] + static_cast<size_t>(row - m.split1) * row_bytes;
+  return m.base[2] + static_cast<size_t>(row - m.split2) * row_bytes;
+}
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const void* p, int i);
+template <>
+__device__ __forceinline__ float load_f32<float>(const void* p, int i) {
+  return static_cast<const float*>(p)[i];
+}
+template <>
+__device__ __forceinline__ float load_f32<uint16_t>(const void* p, int i) {
+  return bf16_to_f32(static_cast<const uint16_t*>(p)[i]);
+}
+
+// Position of element i of the activation vector in the shared staging array.
+// bf16 weights read 8 columns per 16-byte load; their x is staged as two float4
+// planes (columns 8g..8g+3 in plane 0, 8g+4..8g+7 in plane 1) so that the
+// 32 lanes of a warp hit distinct banks.
+template <typename WT>
+__device__ __forceinline__ int xs_index(int i, int in);
+template <>
+__device__ __forceinline__ int xs_index<float>(int i, int) {
+  return i;
+}
+template <>
+__device__ __forceinline__ int xs_index<uint16_t>(int i, int in) {
+  const int g = i >> 3, r = i & 7;
+  return r < 4 ? 4 * g + r : 4 * ((in >> 3) + g) + (r - 4);
+}
+
+// Partial dot of one segment held in shared memory with the matching x.
+template <typename WT>
+__device__ __forceinline__ float seg_dot(const unsigned char* seg, const float* xs, int e0, int bytes, int in, int lane);
+
+template <>
+__device__ __forceinline__ float seg_dot<float>(const unsigned char* seg, const float* xs, int e0, int bytes, int,
+                                                int lane) {
+  const float4* w4 = reinterpret_cast<const float4*>(seg);
+  const float4* x4 = reinterpret_cast<const float4*>(xs + e0);
+  const int n4 = bytes >> 4;
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+  for (int i = lane; i < n4; i += 32) {
+    const float4 w = w4[i], x = x4[i];
+    a0 = fmaf(w.x, x.x, a0);
+    a1 = fmaf(w.y, x.y, a1);
+    a0 = fmaf(w.z, x.z, a0);
+    a1 = fmaf(w.w, x.w, a1);
+  }
+  return a0 + a1;
+}
+
+template <>
+__device__ __forceinline__ float seg_dot<uint16_t>(const unsigned char* seg, const float* xs, int e0, int bytes, int in,
+                                                   int lane) {
+  const uint4* w8 = reinterpret_cast<const uint4*>(seg);
+  const float4* xa = reinterpret_cast<const float4*>(xs) + (e0 >> 3);
+  const float4* xb = reinterpret_cast<const float4*>(xs) + (in >> 3) + (e0 >> 3);
+  const int n8 = bytes >> 4;
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll 4
+  for (int i = lane; i < n8; i += 32) {
+    const uint4 w = w8[i];
+    const float4 p = xa[i], q = xb[i];
+    a0 = fmaf(__uint_as_float(w.x << 16), p.x, a0);
+    a1 = fmaf(__uint_as_float(w.x & 0xFFFF0000u), p.y, a1);
+    a0 = fmaf(__uint_as_float(w.y << 16), p.z, a0);
+    a1 = fmaf(__uint_as_float(w.y & 0xFFFF0000u), p.w, a1);
+    a0 = fmaf(__uint_as_float(w.z << 16), q.x, a0);
+    a1 = fmaf(__uint_as_float(w.z & 0xFFFF0000u), q.y, a1);
+    a0 = fmaf(__uint_as_float(w.w << 16), q.z, a0);
+    a1 = fmaf(__uint_as_float(w.w & 0xFFFF0000u), q.w, a1);
+  }
+  return a0 + a1;
+}
+
+// (v, i) beats (bv, bi) under "largest value, lowest index on ties"; NaN never beats.
+__device__ __forceinline__ bool argmax_better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
+
+// Shared memory bytes the kernel needs for a given problem.
+template <int NW, int NS, int SEG>
+__host__ __device__ constexpr size_t gemv_ring_bytes() {
+  return static_cast<size_t>(NW) * NS * SEG + static_cast<size_t>(NW) * NS * 8;
+}
+
+inline size_t gemv_smem_bytes(size_t ring_bytes, int in, int max_rows, int segs_per_row) {
+  size_t b = ring_bytes;
+  b += ((static_cast<size_t>(in) * 4 + 15) / 16) * 16;                        // x staging
+  b += ((static_cast<size_t>(max_rows) * segs_per_row * 4 + 15) / 16) * 16;   // partial dots
+  b += 64 * 8;                                                               // reductions
+  return b;
+}
+
+// Row epilogues after the per-segment partial dots are complete: store,
+// residual add, or logits with the two argmax passes (the last CTA to
+// finish, detected with an atomic counter, reduces every CTA's best).
+template <int EPI>
+__device__ __forceinline__ void rows_epilogue(const GemvArgs& a, const float* part, float* red, int nrows, int spr,
+                                                int r0, int pos, int c, int G, int tid, int warp, int lane, int NT,
+                                                int NW) {
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int r = tid; r < nrows; r += NT) {
+    float v = 0.f;
+    for (int j = 0; j < spr; ++j) v += part[r * spr + j];
+    const int row = r0 + r;
+    if constexpr (EPI == EPI_STORE) a.y[row] = v;
+    if constexpr (EPI == EPI_RESID) a.y[row] += v;
+    if constexpr (EPI == EPI_ARGMAX) {
+      if (a.y) a.y[row] = v;
+      if (argmax_better(v, row, bv, bi)) {
+        bv = v;
+        bi = row;
+      }
+    }
+  }
+  if constexpr (EPI == EPI_ARGMAX) {
+  // Pass 1: this CTA's best (value, index).
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (argmax_better(ov, oi, bv, bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  int* redi = reinterpret_cast<int*>(red + 32);
+  __syncthreads();
+  if (lane == 0) {
+    red[warp] = bv;
+    redi[warp] = bi;
+  }
+  __syncthreads();
+  __shared__ int s_last;
+  if (tid == 0) {
+    for (int w = 1; w < NW; ++w)
+      if (argmax_better(red[w], redi[w], bv, bi)) {
+        bv = red[w];
+        bi = redi[w];
+      }
+    a.part_val[c] = bv;
+    a.part_idx[c] = bi;
+    __threadfence();
+    const uint32_t prev = atomicAdd(a.counter, 1u);
+    s_last = (prev == static_cast<uint32_t>(G - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  // Pass 2 (last CTA to finish): best over all CTAs, lowest index on ties.
+  __threadfence();
+  float gv = -INFINITY;
+  int gi = 0x7fffffff;
+  for (int k = tid; k < G; k += NT) {
+    const float v = __ldcg(a.part_val + k);
+    const int i = __ldcg(a.part_idx + k);
+    if (argmax_better(v, i, gv, gi)) {
+      gv = v;
+      gi = i;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, gv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, gi, o);
+    if (argmax_better(ov, oi, gv, gi)) {
+      gv = ov;
+      gi = oi;
+    }
+  }
+  __syncthreads();
+  if (lane == 0) {
+    red[warp] = gv;
+    redi[warp] = gi;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int w = 1; w < NW; ++w)
+      if (argmax_better(red[w], redi[w], gv, gi)) {
+        gv = red[w];
+        gi = redi[w];
+      }
+    if (gi == 0x7fffffff) {  // every logit was NaN
+      gi = 0;
+      atomicOr(a.err, ERR_ARGMAX_NAN);
+    }
+    a.tok_w[pos + 1] = gi;
+    a.ctrl[0] = pos + 1;
+    *a.counter = 0u;
+    __threadfence();
+  }
+  }
+}
+
+template <typename WT, typename XT, int PRO, int EPI, int NW, int NS, int SEG>
+__global__ void __launch_bounds__(NW * 32, 1) gemv_stream_kernel(const GemvArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  constexpr int NT = NW * 32;
+  unsigned char* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(NW) * NS * SEG);
+  float* xs = reinterpret_cast<float*>(smem + gemv_ring_bytes<NW, NS, SEG>());
+  float* part = xs + ((a.in + 3) & ~3);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int spr = a.segs_per_row;
+  const int nunits = a.out / a.row_unit;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int u0 = static_cast<int>(static_cast<int64_t>(c) * nunits / G);
+  const int u1 = static_cast<int>(static_cast<int64_t>(c + 1) * nunits / G);
+  const int r0 = u0 * a.row_unit;
+  const int nrows = (u1 - u0) * a.row_unit;
+  const int nseg = nrows * spr;
+  float* red = part + ((nrows * spr + 3) & ~3);
+  const int njobs = nseg > warp ? (nseg - warp + NW - 1) / NW : 0;
+
+  uint64_t* mybars = bars + warp * NS;
+  unsigned char* myring = ring + static_cast<size_t>(warp) * NS * SEG;
+  const uint64_t pol = l2_policy_evict_first();
+
+  auto issue = [&](int it) {
+    const int k = warp + it * NW;
+    const int row = r0 + k / spr, j = k % spr;
+    const int off = j * a.seg_bytes;
+    const uint32_t bytes = static_cast<uint32_t>(min(a.seg_bytes, a.row_bytes - off));
+    const int slot = it % NS;
+    mbar_arrive_expect_tx(&mybars[slot], bytes);
+    bulk_g2s(myring + static_cast<size_t>(slot) * SEG, row_ptr(a.w, row, a.row_bytes) + off, bytes, &mybars[slot], pol);
+  };
+
+  // Weights never depend on earlier kernels: start streaming them at once.
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&mybars[s], 1);
+    fence_mbar_init();
+    const int first = njobs < NS ? njobs : NS;
+    for (int it = 0; it < first; ++it) issue(it);
+  }
+  __syncwarp();
+  pdl_trigger();
+  pdl_wait();
+
+  // ---- activation vector (and fused RMSNorm) ----
+  int pos = 0;
+  if (PRO == PRO_EMBED_NORM || EPI == EPI_ARGMAX) pos = a.ctrl[0];
+  if (PRO == PRO_X) {
+    for (int i = tid; i < a.in; i += NT) xs[xs_index<WT>(i, a.in)] = load_f32<XT>(a.x, i);
+  } else {
+    const void* src = a.x;
+    bool src_is_w = false;
+    if (PRO == PRO_EMBED_NORM) {
+      int t = a.tok[pos];
+      if (t < 0 || t >= a.vocab) {
+        if (tid == 0) atomicOr(a.err, ERR_BAD_TOKEN);
+        t = 0;
+      }
+      src = static_cast<const WT*>(a.embed) + static_cast<size_t>(t) * a.in;
+      src_is_w = true;
+    }
+    float ss = 0.f;
+    for (int i = tid; i < a.in; i += NT) {
+      const float v = src_is_w ? load_f32<WT>(src, i) : static_cast<const float*>(src)[i];
+      if (PRO == PRO_EMBED_NORM && c == 0) a.h_out[i] = v;
+      xs[xs_index<WT>(i, a.in)] = v;
+      ss = fmaf(v, v, ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (warp == 0) {
+      float t = lane < NW ? red[lane] : 0.f;
+      t = warp_sum(t);
+      if (lane == 0) red[NW] = 1.0f / sqrtf(t / static_cast<float>(a.in) + a.eps);
+    }
+    __syncthreads();
+    const float inv = red[NW];
+    for (int i = tid; i < a.in; i += NT) {
+      const int k = xs_index<WT>(i, a.in);
+      xs[k] = xs[k] * inv * a.norm_g[i];
+    }
+  }
+  __syncthreads();
+
+  // ---- stream this warp's segments ----
+  int fail_it = -1;
+  for (int it = 0; it < njobs; ++it) {
+    const int slot = it % NS;
+    if (!mbar_wait(&mybars[slot], (it / NS) & 1)) {
+      fail_it = it;
+      break;
+    }
+    const int k = warp + it * NW;
+    const int j = k % spr;
+    const int off = j * a.seg_bytes;
+    const int bytes = min(a.seg_bytes, a.row_bytes - off);
+    float v = seg_dot<WT>(myring + static_cast<size_t>(slot) * SEG, xs, off / static_cast<int>(sizeof(WT)), bytes, a.in,
+                          lane);
+    v = warp_sum(v);
+    if (lane == 0) part[k] = v;
+    __syncwarp();
+    if (lane == 0 && it + NS < njobs) {
+      fence_proxy_async_smem();
+      issue(it + NS);
+    }
+  }
+  if (fail_it >= 0) {
+    if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
+    // Drain copies still in flight into this warp's ring before the CTA exits.
+    const int last = min(njobs, fail_it + NS);
+    for (int it = fail_it + 1; it < last; ++it) mbar_wait(&mybars[it % NS], (it / NS) & 1);
+  }
+  __syncthreads();
+
+  // ---- epilogue ----
+  if constexpr (EPI == EPI_SWIGLU) {
+    for (int i = tid; i < nrows / 2; i += NT) {
+      float g = 0.f, u = 0.f;
+      for (int j = 0; j < spr; ++j) g += part[(2 * i) * spr + j];
+      for (int j = 0; j < spr; ++j) u += part[(2 * i + 1) * spr + j];
+      a.y[r0 / 2 + i] = silu_f32(g) * u;
+    }
+  } else {
+    rows_epilogue<EPI>(a, part, red, nrows, spr, r0, pos, c, G, tid, warp, lane, NT, NW);
+  }
+}
+
+}  // namespace wsg

@@ -1,0 +1,114 @@
+"""Decoder: owns a workspace tensor and a dec_ctx, and marshals weights to the C ABI.
+
+PyTorch provides device memory and the stream; every step of the forward
+runs in libwsg.so's kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import binding as B
+
+_LAYER_KEYS = ("w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down", "g_in", "g_post", "g_q", "g_k")
+
+
+def to_device(a, device="cuda") -> torch.Tensor:
+    """numpy array -> device tensor; uint16 arrays are taken as bfloat16 bit patterns."""
+    if isinstance(a, torch.Tensor):
+        return a.to(device).contiguous()
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(a).to(device)
+
+
+class Decoder:
+    """Batch-1 decoder on the current CUDA device.
+
+    shape: an object with layers, hidden, inter, n_q, n_kv, head_dim, vocab,
+    eps, rope_theta. weights: dict as made by workloads.decoder_weights
+    (numpy) or the same layout of device tensors.
+    """
+
+    def __init__(self, shape, weights: dict, kv_dtype: str = "f32", max_seq: int = 4096, chunk_cap: int = 0,
+                 stream: torch.cuda.Stream | None = None):
+        wd = weights.get("wdtype", "f32")
+        self.shape = shape
+        self.cfg = B.dec_config(
+            layers=shape.layers, hidden=shape.hidden, inter=shape.inter, n_q=shape.n_q, n_kv=shape.n_kv,
+            head_dim=shape.head_dim, vocab=shape.vocab, eps=shape.eps, rope_theta=shape.rope_theta,
+            wdtype=B.DEC_F32 if wd == "f32" else B.DEC_BF16,
+            kvdtype=B.DEC_F32 if kv_dtype == "f32" else B.DEC_BF16,
+            max_seq=max_seq, chunk_cap=chunk_cap)
+        self.kv_dtype = kv_dtype
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        nbytes = B.dec_workspace_bytes(self.cfg)
+        if nbytes == 0:
+            raise B.WsgError(B.DEC_EINVAL, "invalid decoder configuration")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        self.ctx = B.dec_create(self.cfg, self.workspace, nbytes, self.stream)
+        # device copies of the weights; kept alive as long as the context
+        self.dev = {"embed": to_device(weights["embed"]), "g_final": to_device(weights["g_final"]),
+                    "layers": [{k: to_device(lw[k]) for k in _LAYER_KEYS} for lw in weights["layers"]]}
+        arr = (B.dec_layer_weights * shape.layers)()
+        for i, lw in enumerate(self.dev["layers"]):
+            for k in _LAYER_KEYS:
+                setattr(arr[i], k, lw[k].data_ptr())
+        self._layer_arr = arr
+        w = B.dec_weights(embed=self.dev["embed"].data_ptr(), g_final=self.dev["g_final"].data_ptr(),
+                          layers=ctypes.cast(arr, ctypes.POINTER(B.dec_layer_weights)))
+        B.dec_load_weights(self.ctx, w)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            B.dec_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- calls ---------------------------------------------------------------
+    def reset(self):
+        B.dec_reset(self.ctx)
+
+    @property
+    def position(self) -> int:
+        return B.dec_position(self.ctx)
+
+    def step(self, token: int, logits: torch.Tensor | None = None, skip_logits: bool = False):
+        if skip_logits:
+            return B.dec_step(self.ctx, int(token), B.DEC_SKIP_LOGITS, None, want_next=False)
+        return B.dec_step(self.ctx, int(token), 0, logits, want_next=True)
+
+    def prefill(self, tokens, is_last: bool = True, logits: torch.Tensor | None = None):
+        return B.dec_prefill_chunk(self.ctx, tokens, is_last, logits if is_last else None, want_next=is_last)
+
+    def generate(self, token: int, n: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device="cuda")
+        B.dec_generate(self.ctx, int(token), n, out)
+        return out
+
+    def kv(self, layer: int) -> tuple[torch.Tensor, torch.Tensor, int]:
+        """(K, V, n_valid): views of the cache, each [n_kv, max_seq, head_dim]."""
+        k, v, n = B.dec_get_kv(self.ctx, layer)
+        base = self.workspace.data_ptr()
+        s = self.shape
+        elem = 4 if self.kv_dtype == "f32" else 2
+        count = s.n_kv * self.cfg.max_seq * s.head_dim
+        dt = torch.float32 if self.kv_dtype == "f32" else torch.bfloat16
+
+        def view(p):
+            off = p - base
+            return self.workspace[off: off + count * elem].view(dt).view(s.n_kv, self.cfg.max_seq, s.head_dim)
+
+        return view(k), view(v), n
+
+    def device_errors(self, clear: bool = True) -> int:
+        return B.dec_device_errors(self.ctx, clear)

@@ -144,7 +144,7 @@ def bytes_per_step(s, pos):
     return 4 * (weights + kv) + 4 * s.vocab  # plus the logits write
 
 
-def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=3, min_bytes=1 << 30, ntok=1, gen=None):
+def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=5, min_bytes=1 << 30, ntok=1, gen=None):
     """Cold GB/s: cycle >= 1 GiB of distinct matrices; returns (GB/s, bytes per launch, avg launch s, launches)."""
     if dtype == "q4":
         per = out * inp // 2 + out * (inp // 64) * 4
@@ -162,8 +162,8 @@ def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=3, min_bytes=1 << 3
         x = torch.randn((ntok, inp), device="cuda", generator=gen).to(torch.bfloat16)
         y = torch.empty((ntok, out), device="cuda")
 
-        def call(i):
-            W.gemv_q4(codes[i], sc[i], bi[i], x, y, out, inp, ntok, stream)
+        def call(i, st):
+            W.gemv_q4(codes[i], sc[i], bi[i], x, y, out, inp, ntok, st)
         per_launch = per + ntok * (inp * 2 + out * 4)
     else:
         mats = [(0.02 * torch.randn((out, inp), device="cuda", generator=gen)).to(tdt) for _ in range(count)]
@@ -171,22 +171,33 @@ def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=3, min_bytes=1 << 3
         y = torch.empty(out, device="cuda")
         code = W.DEC_F32 if dtype == "f32" else W.DEC_BF16
 
-        def call(i):
-            W.gemv(code, mats[i], x, y, out, inp, stream)
+        def call(i, st):
+            W.gemv(code, mats[i], x, y, out, inp, st)
         per_launch = per + inp * (4 if dtype == "f32" else 2) + out * 4
-    for i in range(count):  # warm-up: one pass
-        call(i)
+    # One graph launches every matrix once (back to back, with the launch
+    # edges the library sets); replaying it removes host launch overhead.
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        for i in range(count):  # warm-up outside capture: lazy set-up happens here
+            call(i, cap)
+    cap.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=cap):
+        for i in range(count):
+            call(i, cap)
+    graph.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     n = rounds * count
     e0.record(stream)
     for r in range(rounds):
-        for i in range(count):
-            call(i)
+        graph.replay()
     e1.record(stream)
     torch.cuda.synchronize()
     sec = e0.elapsed_time(e1) / 1e3
     avg = sec / n
+    del graph
     if dtype == "q4":
         del codes, sc, bi
     else:

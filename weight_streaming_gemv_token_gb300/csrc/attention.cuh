@@ -94,6 +94,7 @@ __device__ __forceinline__ void norm_rope_warp(float* v, const float* g, float e
 }
 
 constexpr int kAttnWarps = 8;
+constexpr int kAttnBatch = 8;  // keys loaded per warp per round trip
 
 inline size_t attn_smem_bytes(int group, int d) {
   // qn[group][d], kn[d], vn[d], per-warp (m, l)[group] and o[group][d]
@@ -174,46 +175,54 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
     o[h] = make_float4(0, 0, 0, 0);
   }
 
-  for (int t = t0 + warp; t < t1; t += 2 * kAttnWarps) {
-    const int tb = t + kAttnWarps;
-    const bool two = tb < t1;
-    float4 k0 = make_float4(0, 0, 0, 0), v0 = k0, k1 = k0, v1 = k0;
-    if (active) {
-      if (t == pos) {
-        k0 = *reinterpret_cast<const float4*>(kn + 4 * lane);
-        v0 = *reinterpret_cast<const float4*>(vn + 4 * lane);
-      } else {
-        k0 = load4<KT>(a.kc, head_base + static_cast<size_t>(t) * d + 4 * lane);
-        v0 = load4<KT>(a.vc, head_base + static_cast<size_t>(t) * d + 4 * lane);
-      }
-      if (two) {
-        if (tb == pos) {
-          k1 = *reinterpret_cast<const float4*>(kn + 4 * lane);
-          v1 = *reinterpret_cast<const float4*>(vn + 4 * lane);
+  // Each warp takes a contiguous run of this CTA's keys and loads kAttnBatch of
+  // them at a time, so one memory round trip covers the whole batch.
+  const int per_w = (t1 - t0 + kAttnWarps - 1) / kAttnWarps;
+  const int w0 = t0 + warp * per_w;
+  const int w1 = min(t1, w0 + per_w);
+  for (int tb = w0; tb < w1; tb += kAttnBatch) {
+    float4 kk[kAttnBatch], vv[kAttnBatch];
+#pragma unroll
+    for (int u = 0; u < kAttnBatch; ++u) {
+      const int t = tb + u;
+      kk[u] = vv[u] = make_float4(0, 0, 0, 0);
+      if (t < w1 && active) {
+        if (t == pos) {
+          kk[u] = *reinterpret_cast<const float4*>(kn + 4 * lane);
+          vv[u] = *reinterpret_cast<const float4*>(vn + 4 * lane);
         } else {
-          k1 = load4<KT>(a.kc, head_base + static_cast<size_t>(tb) * d + 4 * lane);
-          v1 = load4<KT>(a.vc, head_base + static_cast<size_t>(tb) * d + 4 * lane);
+          kk[u] = load4<KT>(a.kc, head_base + static_cast<size_t>(t) * d + 4 * lane);
+          vv[u] = load4<KT>(a.vc, head_base + static_cast<size_t>(t) * d + 4 * lane);
         }
       }
     }
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
       if (h >= group) break;
-      float s0 = q[h].x * k0.x + q[h].y * k0.y + q[h].z * k0.z + q[h].w * k0.w;
-      float s1 = q[h].x * k1.x + q[h].y * k1.y + q[h].z * k1.z + q[h].w * k1.w;
-      s0 = warp_sum(s0) * a.scale;
-      s1 = warp_sum(s1) * a.scale;
-      float mn = fmaxf(m[h], s0);
-      if (two) mn = fmaxf(mn, s1);
-      const float corr = expf(m[h] - mn);
-      const float p0 = expf(s0 - mn);
-      const float p1 = two ? expf(s1 - mn) : 0.f;
-      l[h] = l[h] * corr + p0 + p1;
-      o[h].x = o[h].x * corr + p0 * v0.x + p1 * v1.x;
-      o[h].y = o[h].y * corr + p0 * v0.y + p1 * v1.y;
-      o[h].z = o[h].z * corr + p0 * v0.z + p1 * v1.z;
-      o[h].w = o[h].w * corr + p0 * v0.w + p1 * v1.w;
-      m[h] = mn;
+      float sc[kAttnBatch];
+      float mx = m[h];
+#pragma unroll
+      for (int u = 0; u < kAttnBatch; ++u) {
+        const float dot = q[h].x * kk[u].x + q[h].y * kk[u].y + q[h].z * kk[u].z + q[h].w * kk[u].w;
+        sc[u] = (tb + u < w1) ? warp_sum(dot) * a.scale : -INFINITY;
+        mx = fmaxf(mx, sc[u]);
+      }
+      const float corr = expf(m[h] - mx);
+      l[h] *= corr;
+      o[h].x *= corr;
+      o[h].y *= corr;
+      o[h].z *= corr;
+      o[h].w *= corr;
+#pragma unroll
+      for (int u = 0; u < kAttnBatch; ++u) {
+        const float p = expf(sc[u] - mx);
+        l[h] += p;
+        o[h].x = fmaf(p, vv[u].x, o[h].x);
+        o[h].y = fmaf(p, vv[u].y, o[h].y);
+        o[h].z = fmaf(p, vv[u].z, o[h].z);
+        o[h].w = fmaf(p, vv[u].w, o[h].w);
+      }
+      m[h] = mx;
     }
   }
 

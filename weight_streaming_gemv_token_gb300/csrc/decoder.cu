@@ -30,7 +30,8 @@ using namespace wsg;
 
 namespace {
 
-constexpr int kNW = 8, kNS = 3, kSEG = 4096;
+constexpr int kNW = 8, kNSMAX = 8, kRING = 12288, kSEGMAX = 4096;
+constexpr long long kL2PrefetchMax = 64ll << 20;  // whole-matrix L2 prefetch up to this size
 constexpr int kArgmaxPartsMax = 4096;
 constexpr int kSplitMax = 64;
 constexpr size_t kAlign = 256;
@@ -99,12 +100,13 @@ Layout make_layout(const dec_config& c) {
 struct Plan {  // launch shape of one decoder GEMV
   int grid = 0, seg = 0, spr = 0;
   size_t smem = 0;
+  bool l2pf = false;
 };
 
 Plan plan_gemv(int out, int in, int elem, int row_unit, int sms, int max_grid) {
   Plan p;
   const long long rb = static_cast<long long>(in) * elem;
-  int spr = static_cast<int>((rb + kSEG - 1) / kSEG);
+  int spr = static_cast<int>((rb + kSEGMAX - 1) / kSEGMAX);
   p.seg = static_cast<int>(((rb + spr - 1) / spr + 15) / 16 * 16);
   p.spr = static_cast<int>((rb + p.seg - 1) / p.seg);
   const int units = out / row_unit;
@@ -115,7 +117,8 @@ Plan plan_gemv(int out, int in, int elem, int row_unit, int sms, int max_grid) {
     p.grid *= 2;
     max_rows = (units + p.grid - 1) / p.grid * row_unit;
   }
-  p.smem = gemv_smem_bytes(gemv_ring_bytes<kNW, kNS, kSEG>(), in, max_rows, p.spr);
+  p.smem = gemv_smem_bytes(gemv_ring_bytes<kNW, kNSMAX, kRING>(), in, max_rows, p.spr);
+  p.l2pf = static_cast<long long>(out) * rb <= kL2PrefetchMax;
   return p;
 }
 
@@ -157,7 +160,7 @@ namespace {
 
 template <typename WT, int PRO, int EPI>
 dec_status launch_dec_gemv(dec_ctx* c, const Plan& p, const GemvArgs& a, cudaStream_t st, bool pdl) {
-  auto kern = gemv_stream_kernel<WT, float, PRO, EPI, kNW, kNS, kSEG>;
+  auto kern = gemv_stream_kernel<WT, float, PRO, EPI, kNW, kNSMAX, kRING>;
   WSG_CUDA_TRY(&c->err, launch_k(kern, dim3(p.grid), dim3(kNW * 32), p.smem, st, pdl, a));
   return DEC_OK;
 }
@@ -167,12 +170,12 @@ dec_status launch_dec_gemv(dec_ctx* c, const Plan& p, const GemvArgs& a, cudaStr
 template <typename WT>
 dec_status prepare_kernels(dec_ctx* c) {
   std::string* e = &c->err;
-  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_EMBED_NORM, EPI_STORE, kNW, kNS, kSEG>, c->p_qkv.smem));
-  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_STORE, kNW, kNS, kSEG>, c->p_qkv.smem));
-  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_X, EPI_RESID, kNW, kNS, kSEG>,
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_EMBED_NORM, EPI_STORE, kNW, kNSMAX, kRING>, c->p_qkv.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_STORE, kNW, kNSMAX, kRING>, c->p_qkv.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_X, EPI_RESID, kNW, kNSMAX, kRING>,
                              c->p_o.smem > c->p_down.smem ? c->p_o.smem : c->p_down.smem));
-  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_SWIGLU, kNW, kNS, kSEG>, c->p_gu.smem));
-  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_ARGMAX, kNW, kNS, kSEG>, c->p_vocab.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_SWIGLU, kNW, kNSMAX, kRING>, c->p_gu.smem));
+  WSG_CUDA_TRY(e, allow_smem(gemv_stream_kernel<WT, float, PRO_NORM, EPI_ARGMAX, kNW, kNSMAX, kRING>, c->p_vocab.smem));
   WSG_CUDA_TRY(e, allow_smem(attn_decode_kernel<float, 2>, c->attn_smem));
   WSG_CUDA_TRY(e, allow_smem(attn_decode_kernel<float, 8>, c->attn_smem));
   WSG_CUDA_TRY(e, allow_smem(attn_decode_kernel<uint16_t, 2>, c->attn_smem));
@@ -187,6 +190,7 @@ GemvArgs base_args(dec_ctx* c, const Plan& p, int out, int in) {
   a.row_bytes = in * static_cast<int>(dtype_bytes(c->cfg.wdtype));
   a.seg_bytes = p.seg;
   a.segs_per_row = p.spr;
+  a.l2_prefetch = p.l2pf;
   a.row_unit = 1;
   a.eps = c->cfg.eps;
   a.vocab = c->cfg.vocab;

@@ -47,7 +47,28 @@ __device__ uint32_t g_gemv_err;
 
 namespace {
 
-constexpr int kNW = 8, kNS = 3, kSEG = 4096;
+constexpr int kNW = 8, kNSMAX = 8, kRING = 12288, kSEGMAX = 4096;
+// Matrices up to this size are prefetched into L2 whole at kernel start.
+constexpr long long kL2PrefetchMax = 64ll << 20;
+
+// Address of the device error word on the current device (looked up once).
+uint32_t* gemv_err_ptr(int dev) {
+  static uint32_t* ptrs[64] = {};
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_gemv_err) == cudaSuccess) ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+// Lift a kernel's dynamic shared memory limit to the device maximum, once per device.
+template <typename K>
+cudaError_t smem_once(K kern, const DeviceInfo& di, bool* done) {
+  if (done[di.device]) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(di.smem_optin));
+  if (e == cudaSuccess) done[di.device] = true;
+  return e;
+}
 
 __global__ void fill_zero_kernel(float* y, int n) {
   pdl_wait();
@@ -80,6 +101,37 @@ __global__ void gemv_plain_kernel(const WT* __restrict__ W, const XT* __restrict
 // and the chunk's contribution s*sum(q x) + b*X equals 256 s S + (b - 128 s) X,
 // with X the chunk's column sum of x (staged once per CTA). A chunk is half of
 // a 64-column group, so it has a single (s, b).
+//
+// Work items of a warp are (row batch, chunk slot) pairs; the codes and scales
+// of item i+1 are loaded while item i is computed, and item 0 is loaded before
+// the kernel waits on its predecessor (programmatic dependent launch).
+template <int R>
+struct Q4Item {
+  uint4 q[R];
+  float s[R], b[R];
+};
+
+template <int R>
+__device__ __forceinline__ void q4_load(Q4Item<R>& it, const uint32_t* __restrict__ codes, const __half* __restrict__ sc,
+                                        const __half* __restrict__ bi, int rb, int c, int out, int nch,
+                                        int words_per_row, int groups_per_row) {
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const int row = rb + r;
+    if (row < out && c < nch) {
+      const uint32_t* p = codes + static_cast<size_t>(row) * words_per_row + 4 * c;
+      asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(it.q[r].x), "=r"(it.q[r].y), "=r"(it.q[r].z), "=r"(it.q[r].w)
+                   : "l"(p));
+      it.s[r] = __half2float(sc[static_cast<size_t>(row) * groups_per_row + (c >> 1)]);
+      it.b[r] = __half2float(bi[static_cast<size_t>(row) * groups_per_row + (c >> 1)]);
+    } else {
+      it.q[r] = make_uint4(0, 0, 0, 0);
+      it.s[r] = it.b[r] = 0.f;
+    }
+  }
+}
+
 template <int R, int NTOK>
 __global__ void __launch_bounds__(256) gemv_q4_kernel(const uint32_t* __restrict__ codes,
                                                       const __half* __restrict__ sc, const __half* __restrict__ bi,
@@ -87,10 +139,19 @@ __global__ void __launch_bounds__(256) gemv_q4_kernel(const uint32_t* __restrict
                                                       int in) {
   extern __shared__ float4 q4_smem[];
   const int nch = in >> 5;
-  float4* xs4 = q4_smem;                                     // [NTOK][8][nch]
+  float4* xs4 = q4_smem;                                         // [NTOK][8][nch]
   float* xsum = reinterpret_cast<float*>(xs4 + NTOK * 8 * nch);  // [NTOK][nch]
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int words_per_row = in >> 3, groups_per_row = in >> 6;
+  const int cpl = (nch + 31) >> 5;  // chunk slots per lane per row batch
+  const int warps_total = gridDim.x * (blockDim.x >> 5);
+  const int gw = blockIdx.x * (blockDim.x >> 5) + warp;
+  const int nbatch = (out + R - 1) / R;
+  const int my_batches = gw < nbatch ? (nbatch - gw + warps_total - 1) / warps_total : 0;
+  const int nitems = my_batches * cpl;
 
+  Q4Item<R> cur;
+  if (nitems > 0) q4_load<R>(cur, codes, sc, bi, gw * R, lane, out, nch, words_per_row, groups_per_row);
   pdl_trigger();
   pdl_wait();
   for (int idx = tid; idx < NTOK * nch * 8; idx += blockDim.x) {
@@ -108,48 +169,39 @@ __global__ void __launch_bounds__(256) gemv_q4_kernel(const uint32_t* __restrict
   }
   __syncthreads();
 
-  const int words_per_row = in >> 3, groups_per_row = in >> 6;
-  const int warps_total = gridDim.x * (blockDim.x >> 5);
-  for (int rb = (blockIdx.x * (blockDim.x >> 5) + warp) * R; rb < out; rb += warps_total * R) {
-    float acc[R][NTOK];
+  float acc[R][NTOK];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+  for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
+    for (int t = 0; t < NTOK; ++t) acc[r][t] = 0.f;
 
-    for (int c = lane; c < nch; c += 32) {
-      uint4 q[R];
-      float s[R], b[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int row = rb + r;
-        if (row < out) {
-          const uint32_t* p = codes + static_cast<size_t>(row) * words_per_row + 4 * c;
-          asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(q[r].x), "=r"(q[r].y), "=r"(q[r].z), "=r"(q[r].w)
-                       : "l"(p));
-          s[r] = __half2float(sc[static_cast<size_t>(row) * groups_per_row + (c >> 1)]);
-          b[r] = __half2float(bi[static_cast<size_t>(row) * groups_per_row + (c >> 1)]);
-        } else {
-          q[r] = make_uint4(0, 0, 0, 0);
-          s[r] = b[r] = 0.f;
-        }
-      }
+#pragma unroll 1
+  for (int i = 0; i < nitems; ++i) {
+    const int k = i / cpl, j = i - k * cpl;
+    const int rb = (gw + k * warps_total) * R;
+    const int c = lane + 32 * j;
+    Q4Item<R> nxt;
+    if (i + 1 < nitems) {
+      const int k2 = (i + 1) / cpl, j2 = (i + 1) - k2 * cpl;
+      q4_load<R>(nxt, codes, sc, bi, (gw + k2 * warps_total) * R, lane + 32 * j2, out, nch, words_per_row,
+                 groups_per_row);
+    }
+    if (c < nch) {
 #pragma unroll
       for (int t = 0; t < NTOK; ++t) {
         float xv[32];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float4 v = xs4[(t * 8 + k) * nch + c];
-          xv[4 * k] = v.x;
-          xv[4 * k + 1] = v.y;
-          xv[4 * k + 2] = v.z;
-          xv[4 * k + 3] = v.w;
+        for (int kk = 0; kk < 8; ++kk) {
+          const float4 v = xs4[(t * 8 + kk) * nch + c];
+          xv[4 * kk] = v.x;
+          xv[4 * kk + 1] = v.y;
+          xv[4 * kk + 2] = v.z;
+          xv[4 * kk + 3] = v.w;
         }
         const float X = xsum[t * nch + c];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-          const uint32_t wd[4] = {q[r].x, q[r].y, q[r].z, q[r].w};
+          const uint32_t wd[4] = {cur.q[r].x, cur.q[r].y, cur.q[r].z, cur.q[r].w};
           float S0 = 0.f, S1 = 0.f;
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
@@ -165,17 +217,21 @@ __global__ void __launch_bounds__(256) gemv_q4_kernel(const uint32_t* __restrict
             S1 = fmaf(__uint_as_float(__byte_perm(hi, 0x3F000000u, 0x7344)), xv[8 * m + 7], S1);
           }
           const float S = S0 + S1;
-          acc[r][t] = fmaf(256.f * s[r], S, fmaf(b[r] - 128.f * s[r], X, acc[r][t]));
+          acc[r][t] = fmaf(256.f * cur.s[r], S, fmaf(cur.b[r] - 128.f * cur.s[r], X, acc[r][t]));
         }
       }
     }
+    if (j == cpl - 1) {  // this row batch is complete
 #pragma unroll
-    for (int r = 0; r < R; ++r)
+      for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int t = 0; t < NTOK; ++t) {
-        const float v = warp_sum(acc[r][t]);
-        if (lane == 0 && rb + r < out) y[static_cast<size_t>(t) * out + rb + r] = v;
-      }
+        for (int t = 0; t < NTOK; ++t) {
+          const float v = warp_sum(acc[r][t]);
+          if (lane == 0 && rb + r < out) y[static_cast<size_t>(t) * out + rb + r] = v;
+          acc[r][t] = 0.f;
+        }
+    }
+    if (i + 1 < nitems) cur = nxt;
   }
 }
 
@@ -187,9 +243,19 @@ dec_status launch_q4_r(const uint32_t* codes, const uint16_t* s, const uint16_t*
   auto kern = gemv_q4_kernel<R, NTOK>;
   const size_t smem = static_cast<size_t>(NTOK) * (in >> 5) * (8 * sizeof(float4) + sizeof(float));
   if (smem > di.smem_optin) return fail(nullptr, DEC_EINVAL, "gemv_q4: in=%d needs %zu B of shared memory", in, smem);
-  WSG_CUDA_TRY(nullptr, allow_smem(kern, smem));
+  static bool done[64] = {};
+  WSG_CUDA_TRY(nullptr, smem_once(kern, di, done));
+  // Resident CTAs per SM, cached per (device, in).
+  static int occ_dev[64] = {}, occ_in[64] = {}, occ_val[64] = {};
   int per_sm = 0;
-  WSG_CUDA_TRY(nullptr, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+  if (occ_dev[di.device] == di.device + 1 && occ_in[di.device] == in) {
+    per_sm = occ_val[di.device];
+  } else {
+    WSG_CUDA_TRY(nullptr, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 256, smem));
+    occ_dev[di.device] = di.device + 1;
+    occ_in[di.device] = in;
+    occ_val[di.device] = per_sm;
+  }
   if (per_sm < 1) per_sm = 1;
   const long long warps_needed = (static_cast<long long>(out) + R - 1) / R;
   long long grid = static_cast<long long>(di.sms) * per_sm;
@@ -225,7 +291,7 @@ dec_status launch_gemv(const void* W, const void* x, float* y, int out, int in, 
     a.out = out;
     a.in = in;
     a.row_bytes = static_cast<int>(row_bytes);
-    int spr = static_cast<int>((row_bytes + kSEG - 1) / kSEG);
+    int spr = static_cast<int>((row_bytes + kSEGMAX - 1) / kSEGMAX);
     int seg = static_cast<int>(((row_bytes + spr - 1) / spr + 15) / 16 * 16);
     spr = static_cast<int>((row_bytes + seg - 1) / seg);
     a.seg_bytes = seg;
@@ -240,14 +306,15 @@ dec_status launch_gemv(const void* W, const void* x, float* y, int out, int in, 
       grid *= 2;
       max_rows = (out + grid - 1) / grid;
     }
-    const size_t smem = gemv_smem_bytes(gemv_ring_bytes<kNW, kNS, kSEG>(), in, max_rows, spr);
+    const size_t smem = gemv_smem_bytes(gemv_ring_bytes<kNW, kNSMAX, kRING>(), in, max_rows, spr);
     if (smem <= di.smem_optin) {
-      auto kern = gemv_stream_kernel<WT, XT, PRO_X, EPI_STORE, kNW, kNS, kSEG>;
-      uint32_t* errp = nullptr;
-      WSG_CUDA_TRY(nullptr, cudaGetSymbolAddress(reinterpret_cast<void**>(&errp), g_gemv_err));
-      a.err = errp;
+      auto kern = gemv_stream_kernel<WT, XT, PRO_X, EPI_STORE, kNW, kNSMAX, kRING>;
+      static bool done[64] = {};
+      a.err = gemv_err_ptr(di.device);
+      if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv: device error word unavailable");
       a.y = y;
-      WSG_CUDA_TRY(nullptr, allow_smem(kern, smem));
+      a.l2_prefetch = static_cast<long long>(out) * row_bytes <= kL2PrefetchMax;
+      WSG_CUDA_TRY(nullptr, smem_once(kern, di, done));
       WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(grid), dim3(kNW * 32), smem, st, true, a));
       return DEC_OK;
     }

@@ -7,13 +7,15 @@
 //
 //  * one CTA per SM; each CTA owns a contiguous range of output rows, handed
 //    out in balanced units so no CTA gets more than one unit above average;
-//  * each row is cut into segments of at most SEG bytes; warp w of the CTA
+//  * each row is cut into segments of at most a few KB; warp w of the CTA
 //    takes segments w, w + NW, w + 2NW, ... and streams them through its own
-//    ring of NS shared-memory slots with bulk (TMA) copies completed on
-//    mbarriers; the copies carry an L2 evict-first policy;
-//  * the first NS copies of every warp are issued before the kernel waits on
-//    its predecessor (programmatic dependent launch), so weight traffic of
-//    this kernel overlaps the tail of the previous one;
+//    RING-byte shared-memory ring (as many slots as segments fit, up to
+//    NSMAX) with bulk (TMA) copies completed on mbarriers; the copies carry
+//    an L2 evict-first policy;
+//  * the first copies of every warp, and for matrices that fit in L2 an L2
+//    prefetch of the CTA's whole weight slice, are issued before the kernel
+//    waits on its predecessor (programmatic dependent launch), so the weight
+//    stream of this kernel overlaps the tail and the prologue of the chain;
 //  * the activation vector is staged once per CTA in shared memory, with an
 //    optional fused RMSNorm prologue;
 //  * per-segment partial dots are reduced in a fixed order, so results are
@@ -64,6 +66,7 @@ struct GemvArgs {
   uint32_t* counter;
   int32_t* tok_w;
   uint32_t* err;
+  int32_t l2_prefetch;  // nonzero: prefetch this CTA's whole weight slice into L2 up front
 };
 
 __device__ __forceinline__ const char* row_ptr(const RowMap& m, int row, int row_bytes) {
@@ -154,9 +157,9 @@ __device__ __forceinline__ bool argmax_better(float v, int i, float bv, int bi) 
 __device__ __forceinline__ float silu_f32(float z) { return z / (1.0f + expf(-z)); }
 
 // Shared memory bytes the kernel needs for a given problem.
-template <int NW, int NS, int SEG>
+template <int NW, int NSMAX, int RING>
 __host__ __device__ constexpr size_t gemv_ring_bytes() {
-  return static_cast<size_t>(NW) * NS * SEG + static_cast<size_t>(NW) * NS * 8;
+  return static_cast<size_t>(NW) * RING + static_cast<size_t>(NW) * NSMAX * 8;
 }
 
 inline size_t gemv_smem_bytes(size_t ring_bytes, int in, int max_rows, int segs_per_row) {
@@ -268,13 +271,36 @@ __device__ __forceinline__ void rows_epilogue(const GemvArgs& a, const float* pa
   }
 }
 
-template <typename WT, typename XT, int PRO, int EPI, int NW, int NS, int SEG>
+// Issue L2 prefetches covering this CTA's weight rows [r0, r0 + nrows).
+__device__ __forceinline__ void prefetch_rows_l2(const RowMap& m, int r0, int nrows, int row_bytes) {
+  auto piece = [&](const char* p, long long bytes) {
+    for (long long off = 0; off < bytes; off += 32768)
+      bulk_prefetch_l2(p + off, static_cast<uint32_t>(bytes - off < 32768 ? bytes - off : 32768));
+  };
+  if (m.interleave) {
+    piece(m.base[0] + static_cast<size_t>(r0 >> 1) * row_bytes, static_cast<long long>(nrows >> 1) * row_bytes);
+    piece(m.base[1] + static_cast<size_t>(r0 >> 1) * row_bytes, static_cast<long long>(nrows >> 1) * row_bytes);
+    return;
+  }
+  const int r1 = r0 + nrows;
+  const int lo[3] = {0, m.split1, m.split2};
+  const int hi[3] = {m.split1, m.split2, 0x7fffffff};
+  for (int k = 0; k < 3; ++k) {
+    const int a = r0 > lo[k] ? r0 : lo[k];
+    const int b = r1 < hi[k] ? r1 : hi[k];
+    if (a < b) piece(m.base[k] + static_cast<size_t>(a - lo[k]) * row_bytes, static_cast<long long>(b - a) * row_bytes);
+  }
+}
+
+// NW warps per CTA; each warp streams its segments through a ring of RING
+// bytes cut into slots of a.seg_bytes (at most NSMAX slots).
+template <typename WT, typename XT, int PRO, int EPI, int NW, int NSMAX, int RING>
 __global__ void __launch_bounds__(NW * 32, 1) gemv_stream_kernel(const GemvArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = NW * 32;
   unsigned char* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(NW) * NS * SEG);
-  float* xs = reinterpret_cast<float*>(smem + gemv_ring_bytes<NW, NS, SEG>());
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(NW) * RING);
+  float* xs = reinterpret_cast<float*>(smem + gemv_ring_bytes<NW, NSMAX, RING>());
   float* part = xs + ((a.in + 3) & ~3);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -288,9 +314,10 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_stream_kernel(const GemvArgs 
   const int nseg = nrows * spr;
   float* red = part + ((nrows * spr + 3) & ~3);
   const int njobs = nseg > warp ? (nseg - warp + NW - 1) / NW : 0;
+  const int ns = min(NSMAX, RING / a.seg_bytes);
 
-  uint64_t* mybars = bars + warp * NS;
-  unsigned char* myring = ring + static_cast<size_t>(warp) * NS * SEG;
+  uint64_t* mybars = bars + warp * NSMAX;
+  unsigned char* myring = ring + static_cast<size_t>(warp) * RING;
   const uint64_t pol = l2_policy_evict_first();
 
   auto issue = [&](int it) {
@@ -298,18 +325,21 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_stream_kernel(const GemvArgs 
     const int row = r0 + k / spr, j = k % spr;
     const int off = j * a.seg_bytes;
     const uint32_t bytes = static_cast<uint32_t>(min(a.seg_bytes, a.row_bytes - off));
-    const int slot = it % NS;
+    const int slot = it % ns;
     mbar_arrive_expect_tx(&mybars[slot], bytes);
-    bulk_g2s(myring + static_cast<size_t>(slot) * SEG, row_ptr(a.w, row, a.row_bytes) + off, bytes, &mybars[slot], pol);
+    bulk_g2s(myring + static_cast<size_t>(slot) * a.seg_bytes, row_ptr(a.w, row, a.row_bytes) + off, bytes,
+             &mybars[slot], pol);
   };
 
-  // Weights never depend on earlier kernels: start streaming them at once.
+  // Weights never depend on earlier kernels: start streaming them at once,
+  // into this warp's ring and (for matrices that fit in L2) into L2.
   if (lane == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&mybars[s], 1);
+    for (int s = 0; s < ns; ++s) mbar_init(&mybars[s], 1);
     fence_mbar_init();
-    const int first = njobs < NS ? njobs : NS;
+    const int first = njobs < ns ? njobs : ns;
     for (int it = 0; it < first; ++it) issue(it);
   }
+  if (tid == 0 && a.l2_prefetch && nrows > 0) prefetch_rows_l2(a.w, r0, nrows, a.row_bytes);
   __syncwarp();
   pdl_trigger();
   pdl_wait();
@@ -358,8 +388,9 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_stream_kernel(const GemvArgs 
   // ---- stream this warp's segments ----
   int fail_it = -1;
   for (int it = 0; it < njobs; ++it) {
-    const int slot = it % NS;
-    if (!mbar_wait(&mybars[slot], (it / NS) & 1)) {
+    const int slot = it % ns;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&mybars[slot], (it / ns) & 1));
+    if (!ok) {
       fail_it = it;
       break;
     }
@@ -367,21 +398,21 @@ __global__ void __launch_bounds__(NW * 32, 1) gemv_stream_kernel(const GemvArgs 
     const int j = k % spr;
     const int off = j * a.seg_bytes;
     const int bytes = min(a.seg_bytes, a.row_bytes - off);
-    float v = seg_dot<WT>(myring + static_cast<size_t>(slot) * SEG, xs, off / static_cast<int>(sizeof(WT)), bytes, a.in,
-                          lane);
+    float v = seg_dot<WT>(myring + static_cast<size_t>(slot) * a.seg_bytes, xs, off / static_cast<int>(sizeof(WT)),
+                          bytes, a.in, lane);
     v = warp_sum(v);
     if (lane == 0) part[k] = v;
     __syncwarp();
-    if (lane == 0 && it + NS < njobs) {
+    if (lane == 0 && it + ns < njobs) {
       fence_proxy_async_smem();
-      issue(it + NS);
+      issue(it + ns);
     }
   }
   if (fail_it >= 0) {
     if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
     // Drain copies still in flight into this warp's ring before the CTA exits.
-    const int last = min(njobs, fail_it + NS);
-    for (int it = fail_it + 1; it < last; ++it) mbar_wait(&mybars[it % NS], (it / NS) & 1);
+    const int last = min(njobs, fail_it + ns);
+    for (int it = fail_it + 1; it < last; ++it) mbar_wait(&mybars[it % ns], (it / ns) & 1);
   }
   __syncthreads();
 

@@ -1,0 +1,93 @@
+"""Profiling driver: runs a region of interest between cudaProfilerStart/Stop.
+
+Use under ncu with --profile-from-start off, e.g.
+
+  ncu --profile-from-start off --metrics gpu__time_duration.sum --clock-control none --csv \\
+      python -m weight_streaming_gemv_token_gb300.profile_step decode --steps 1
+  ncu --profile-from-start off --set full --clock-control none -k regex:gemv_stream -c 3 -o prof \\
+      python -m weight_streaming_gemv_token_gb300.profile_step gemv --out 6144 --in 1024 --count 8
+
+decode: Qwen3-0.6B-shaped decoder with seeded random weights, a uniform
+        prompt, warm-up steps, then --steps decode steps inside the region.
+gemv:   --count distinct matrices of one shape (sized past L2 by default),
+        one warm-up pass, then one launch per matrix inside the region.
+"""
+from __future__ import annotations
+
+import argparse
+import os
+import sys
+
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def decode(args):
+    import workloads as Wl
+
+    from . import build
+    from .decoder import Decoder
+
+    build.build()
+    s = Wl.QWEN3_06B
+    w = Wl.decoder_weights(s, seed=1, wdtype=args.dtype)
+    prompt = Wl.prompt_uniform(args.prompt, s.vocab, seed=0)
+    dec = Decoder(s, w, kv_dtype=args.kv, max_seq=args.prompt + args.warmup + args.steps + 4)
+    first = dec.prefill(prompt, is_last=True)
+    out = dec.generate(first, args.warmup)
+    torch.cuda.synchronize()
+    tok = int(out[-1].item())
+    torch.cuda.profiler.start()
+    dec.generate(tok, args.steps)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    assert dec.device_errors() == 0
+
+
+def gemv(args):
+    from . import binding as B
+    from . import build
+
+    build.build()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    tdt = torch.float32 if args.dtype == "f32" else torch.bfloat16
+    per = args.out * args.inp * (4 if args.dtype == "f32" else 2)
+    count = args.count or max(2, -(-(256 << 20) // per))
+    mats = [(0.02 * torch.randn((args.out, args.inp), device="cuda", generator=g)).to(tdt) for _ in range(count)]
+    x = (0.02 * torch.randn(args.inp, device="cuda", generator=g)).to(tdt)
+    y = torch.empty(args.out, device="cuda")
+    code = B.DEC_F32 if args.dtype == "f32" else B.DEC_BF16
+    for m in mats:
+        B.gemv(code, m, x, y, args.out, args.inp, None)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    for m in mats:
+        B.gemv(code, m, x, y, args.out, args.inp, None)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    sub = ap.add_subparsers(dest="mode", required=True)
+    d = sub.add_parser("decode")
+    d.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
+    d.add_argument("--kv", default="f32", choices=["f32", "bf16"])
+    d.add_argument("--prompt", type=int, default=32)
+    d.add_argument("--warmup", type=int, default=3)
+    d.add_argument("--steps", type=int, default=1)
+    gm = sub.add_parser("gemv")
+    gm.add_argument("--out", type=int, default=6144)
+    gm.add_argument("--in", dest="inp", type=int, default=1024)
+    gm.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
+    gm.add_argument("--count", type=int, default=0)
+    args = ap.parse_args()
+    decode(args) if args.mode == "decode" else gemv(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -223,7 +223,7 @@ def gpu_arm(args):
     K, Wm = args.steps, args.warmup
     max_seq = PROMPT + 1 + Wm + K + 1 + 2 * args.e2e_steps + 8
     stream = torch.cuda.current_stream()
-    dec = Decoder(s, weights, kv_dtype="f32", max_seq=max_seq, stream=stream)
+    dec = Decoder(s, weights, kv_dtype="f32", max_seq=max_seq, stream=stream, engine=args.engine)
     dec.reset()
     first = dec.prefill(prompt, is_last=True)
     out_buf = torch.empty(max(Wm, 1) + K, dtype=torch.int32, device="cuda")
@@ -317,7 +317,7 @@ def gpu_arm(args):
                             f"after a {PROMPT}-token prompt (positions {pos0}..{pos0 + K - 1})",
                 "layers": s.layers, "hidden": s.hidden, "inter": s.inter, "heads": f"{s.n_q}q/{s.n_kv}kv",
                 "head_dim": s.head_dim, "vocab": s.vocab, "global_batch": 1, "seq_len": pos0 + K,
-                "parallelism": "replicas" if ws > 1 else "single GPU",
+                "parallelism": "replicas" if ws > 1 else "single GPU", "engine": args.engine,
                 "l2": "inputs larger than L2 (2.38 GB of weights streamed per step)",
             },
             "step_roofline": {"bytes_per_step": step_bytes, "achieved_GB/s": round(step_bytes * K / sec / 1e9, 1),
@@ -325,7 +325,7 @@ def gpu_arm(args):
                               "roofline_tokens_per_s": round(hbm * 1e9 / step_bytes, 1)},
             "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": 4, "steps": n_e2e},
-            "gpu_launches": K * (5 * s.layers + 1),
+            "gpu_launches": 1 if args.engine == "persistent" else K * (5 * s.layers + 1),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }
@@ -403,6 +403,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-sweep", action="store_true", help="skip the cold GEMV sweep")
+    ap.add_argument("--engine", default="persistent", choices=["persistent", "staged"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     args = ap.parse_args()
     if args.impl == "reference":

@@ -63,6 +63,10 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
 #define DEC_DEVERR_ARGMAX_NAN 0x2u   /* all logits NaN; token 0 was returned */
 #define DEC_DEVERR_BAD_TOKEN 0x4u    /* a token ID outside [0, vocab) was read as 0 */
 
+/* dec_config.engine */
+#define DEC_ENGINE_PERSISTENT 0 /* one cooperative launch runs whole forwards (default) */
+#define DEC_ENGINE_STAGED 1     /* five kernels per layer, replayed as a CUDA graph */
+
 /* dec_step flags */
 #define DEC_SKIP_LOGITS 0x1u /* body only: no final norm, vocabulary projection or argmax */
 
@@ -72,7 +76,12 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
  * n_q*head_dim multiples of 8; wdtype DEC_F32 or DEC_BF16; kvdtype DEC_F32
  * or DEC_BF16; max_seq >= 1 is the KV capacity in positions; chunk_cap is
  * the largest row count of one dec_prefill_chunk call that runs batched
- * (0: prompts are processed one token at a time). */
+ * (0: prompts are processed one token at a time). engine selects the
+ * execution of decode steps: DEC_ENGINE_PERSISTENT runs each call's forwards
+ * inside one persistent kernel (one CTA per SM, a producer warp streaming
+ * weights through shared memory ahead of the consumers, grid barriers
+ * between dependent stages); DEC_ENGINE_STAGED launches the per-stage
+ * kernels as a CUDA graph. Both compute the same forward. */
 typedef struct {
   int32_t layers, hidden, inter, n_q, n_kv, head_dim, vocab;
   float eps;        /* RMSNorm epsilon, e.g. 1e-6 */
@@ -81,6 +90,7 @@ typedef struct {
   int32_t kvdtype;  /* dec_dtype of the KV cache */
   int32_t max_seq;
   int32_t chunk_cap;
+  int32_t engine;   /* DEC_ENGINE_*: how steps are executed */
 } dec_config;
 
 /* One layer's tensors, device pointers, row-major [out][in] in wdtype.

@@ -22,14 +22,17 @@ def kv_to_np(t):
     return t.float().cpu().numpy().astype(np.float64) if t.dtype == torch.bfloat16 else t.cpu().numpy().astype(np.float64)
 
 
-def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every=1, max_seq=None):
+ENGINES = ["persistent", "staged"]
+
+
+def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every=1, max_seq=None, engine="persistent"):
     import torch
 
     W = lib()
     from weight_streaming_gemv_token_gb300.decoder import Decoder
 
     max_seq = max_seq or (len(prompt) + n_out + 4)
-    dec = Decoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq)
+    dec = Decoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq, engine=engine)
     ora = O.OracleDecoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq)
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
     dec.reset()
@@ -74,19 +77,22 @@ def tiny_w():
     return Wl.decoder_weights(Wl.TINY, seed=1)
 
 
-def test_tiny_fp32_every_logit_and_kv(tiny_w):
+@pytest.mark.parametrize("engine", ENGINES)
+def test_tiny_fp32_every_logit_and_kv(tiny_w, engine):
     prompt = Wl.prompt_uniform(8, Wl.TINY.vocab, seed=0)
-    toks, _ = run_and_compare(Wl.TINY, tiny_w, prompt, 8, "f32", FP32_TOL)
+    toks, _ = run_and_compare(Wl.TINY, tiny_w, prompt, 8, "f32", FP32_TOL, engine=engine)
     assert len(toks) == 8
 
 
-def test_tiny_bf16(tiny_w):
+@pytest.mark.parametrize("engine", ENGINES)
+def test_tiny_bf16(tiny_w, engine):
     w = Wl.decoder_weights(Wl.TINY, seed=1, wdtype="bf16")
     prompt = Wl.prompt_uniform(8, Wl.TINY.vocab, seed=0)
-    run_and_compare(Wl.TINY, w, prompt, 8, "bf16", LOW_TOL)
+    run_and_compare(Wl.TINY, w, prompt, 8, "bf16", LOW_TOL, engine=engine)
 
 
-def test_tiny_generate_matches_step(tiny_w):
+@pytest.mark.parametrize("engine", ENGINES)
+def test_tiny_generate_matches_step(tiny_w, engine):
     """dec_generate (device-resident loop) produces the same tokens as host-driven dec_step."""
     import torch
 
@@ -94,12 +100,12 @@ def test_tiny_generate_matches_step(tiny_w):
     from weight_streaming_gemv_token_gb300.decoder import Decoder
 
     prompt = Wl.prompt_uniform(8, Wl.TINY.vocab, seed=3)
-    a = Decoder(Wl.TINY, tiny_w, max_seq=40)
+    a = Decoder(Wl.TINY, tiny_w, max_seq=40, engine=engine)
     first = a.prefill(prompt, is_last=True)
     seq = [first]
     for _ in range(12):
         seq.append(a.step(seq[-1]))
-    b = Decoder(Wl.TINY, tiny_w, max_seq=40)
+    b = Decoder(Wl.TINY, tiny_w, max_seq=40, engine=engine)
     f2 = b.prefill(prompt[:5], is_last=False)
     assert f2 is None
     first_b = b.prefill(prompt[5:], is_last=True)
@@ -113,18 +119,29 @@ def test_tiny_generate_matches_step(tiny_w):
         assert torch.equal(ka[:, :20], kb[:, :20]) and torch.equal(va[:, :20], vb[:, :20])
 
 
-def test_tiny_ragged_geometry():
+@pytest.mark.parametrize("engine", ENGINES)
+def test_tiny_ragged_geometry(engine):
     """A geometry with 4 query heads per KV head, odd row counts and head_dim 32."""
     shape = Wl.DecoderShape(layers=3, hidden=96, inter=200, n_q=8, n_kv=2, head_dim=32, vocab=777)
     w = Wl.decoder_weights(shape, seed=9)
     prompt = Wl.prompt_uniform(5, shape.vocab, seed=4)
-    run_and_compare(shape, w, prompt, 6, "f32", FP32_TOL)
+    run_and_compare(shape, w, prompt, 6, "f32", FP32_TOL, engine=engine)
 
 
-def test_long_context_split_attention(tiny_w):
+@pytest.mark.parametrize("engine", ENGINES)
+def test_bf16_long_rows_geometry(engine):
+    """bf16 rows of 2 KB (two rows per 4 KB ring slot) and 6 KB (split rows), 8 query heads per KV head."""
+    shape = Wl.DecoderShape(layers=2, hidden=1024, inter=3072, n_q=16, n_kv=2, head_dim=64, vocab=3000)
+    w = Wl.decoder_weights(shape, seed=3, wdtype="bf16")
+    prompt = Wl.prompt_uniform(6, shape.vocab, seed=2)
+    run_and_compare(shape, w, prompt, 5, "bf16", LOW_TOL, engine=engine)
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_long_context_split_attention(tiny_w, engine):
     """Positions beyond one attention split (64 keys) exercise the split merge."""
     prompt = Wl.prompt_uniform(150, Wl.TINY.vocab, seed=5)
-    run_and_compare(Wl.TINY, tiny_w, prompt, 4, "f32", FP32_TOL, check_kv_every=2, max_seq=160)
+    run_and_compare(Wl.TINY, tiny_w, prompt, 4, "f32", FP32_TOL, check_kv_every=2, max_seq=160, engine=engine)
 
 
 @pytest.fixture(scope="module")
@@ -136,6 +153,36 @@ def qwen_f32():
 def test_qwen3_fp32_generation(qwen_f32, P, N):
     prompt = Wl.prompt_uniform(P, Wl.QWEN3_06B.vocab, seed=0)
     run_and_compare(Wl.QWEN3_06B, qwen_f32, prompt, N, "f32", FP32_TOL, check_kv_every=4, max_seq=64)
+
+
+def test_qwen3_fp32_staged_engine(qwen_f32):
+    prompt = Wl.prompt_uniform(8, Wl.QWEN3_06B.vocab, seed=0)
+    run_and_compare(Wl.QWEN3_06B, qwen_f32, prompt, 8, "f32", FP32_TOL, check_kv_every=4, max_seq=64, engine="staged")
+
+
+def test_qwen3_fp32_prefill_and_generate_one_launch(qwen_f32):
+    """The persistent engine runs a whole prompt and a whole generation in one launch each."""
+    import torch
+
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.QWEN3_06B
+    prompt = Wl.prompt_uniform(32, s.vocab, seed=0)
+    dec = Decoder(s, qwen_f32, max_seq=64)
+    first = dec.prefill(prompt, is_last=True)
+    toks = [first] + dec.generate(first, 15).cpu().tolist()
+    ora = O.OracleDecoder(s, qwen_f32, max_seq=64)
+    ref = O.generate(ora, prompt, 16, forced=toks[1:] + [0])
+    agree = sum(a == b for a, b in zip(toks, ref["tokens"]))
+    assert agree == 16, (toks, ref["tokens"])
+    for l in (0, s.layers - 1):
+        K, V, n = dec.kv(l)
+        rk, rv = ora.kv(l)
+        assert n == 32 + 15 == ora.pos
+        close(kv_to_np(K[:, :n]), rk, FP32_TOL, f"K layer {l}")
+        close(kv_to_np(V[:, :n]), rv, FP32_TOL, f"V layer {l}")
+    assert dec.device_errors() == 0
 
 
 def test_api_errors(tiny_w):

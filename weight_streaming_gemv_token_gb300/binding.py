@@ -19,6 +19,7 @@ DEC_OK, DEC_EINVAL, DEC_ESTATE, DEC_ECAPACITY, DEC_ENOMEM, DEC_ECUDA, DEC_EDEVIC
 STATUS_NAMES = {0: "DEC_OK", 1: "DEC_EINVAL", 2: "DEC_ESTATE", 3: "DEC_ECAPACITY", 4: "DEC_ENOMEM", 5: "DEC_ECUDA", 6: "DEC_EDEVICE"}
 DEC_F32, DEC_BF16, DEC_Q4G64 = 0, 1, 2
 DEC_SKIP_LOGITS = 0x1
+DEC_ENGINE_PERSISTENT, DEC_ENGINE_STAGED = 0, 1
 DEC_DEVERR_WAIT_TIMEOUT, DEC_DEVERR_ARGMAX_NAN, DEC_DEVERR_BAD_TOKEN = 0x1, 0x2, 0x4
 
 # Every symbol include/wsg.h declares.
@@ -40,6 +41,7 @@ class dec_config(ctypes.Structure):
         ("layers", c_int32), ("hidden", c_int32), ("inter", c_int32), ("n_q", c_int32), ("n_kv", c_int32),
         ("head_dim", c_int32), ("vocab", c_int32), ("eps", c_float), ("rope_theta", c_float),
         ("wdtype", c_int32), ("kvdtype", c_int32), ("max_seq", c_int32), ("chunk_cap", c_int32),
+        ("engine", c_int32),
     ]
 
 

@@ -94,6 +94,10 @@ __device__ __forceinline__ void norm_rope_warp(float* v, const float* g, float e
 }
 
 constexpr int kAttnWarps = 8;
+
+struct CtaSync {  // barrier over the whole CTA
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
 constexpr int kAttnBatch = 8;  // keys loaded per warp per round trip
 
 inline size_t attn_smem_bytes(int group, int d) {
@@ -103,20 +107,16 @@ inline size_t attn_smem_bytes(int group, int d) {
          16;
 }
 
-template <typename KT, int GMAX>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const AttnArgs a) {
-  extern __shared__ __align__(16) float asmem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+// Work of split s of key/value head g for the token at position pos, run by
+// NT threads (tid in [0, NT), NT a multiple of 32 and at least 8 warps' worth
+// of the warp-indexed work below) that sync() together. asmem: shared scratch
+// of attn_smem_bytes(); s_last: one shared int.
+template <typename KT, int GMAX, int NT, typename Sync>
+__device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s, int pos, float* asmem, int tid,
+                                                 Sync sync, int* s_last) {
+  static_assert(NT == kAttnWarps * 32, "the split layout assumes kAttnWarps warps");
+  const int warp = tid >> 5, lane = tid & 31;
   const int d = a.d, group = a.n_q / a.n_kv;
-  const int g = blockIdx.x, s = blockIdx.y;
-
-  pdl_trigger();
-  pdl_wait();
-  const int pos = a.ctrl[0];
-  if (pos < 0 || pos >= a.max_seq) {
-    if (tid == 0 && g == 0 && s == 0) atomicOr(a.err, ERR_BAD_POSITION);
-    return;
-  }
   const int n = pos + 1;
   int nsplit = (n + a.tmin - 1) / a.tmin;
   if (nsplit > a.nsplit_max) nsplit = a.nsplit_max;
@@ -137,24 +137,24 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
   const float* sn = a.rope_sin + static_cast<size_t>(pos) * (d >> 1);
   const float* kraw = a.qkv + a.n_q * d + g * d;
   const float* vraw = a.qkv + a.n_q * d + a.n_kv * d + g * d;
-  for (int i = tid; i < group * d; i += blockDim.x) qn[i] = a.qkv[(g * group) * d + i];
-  for (int i = tid; i < d; i += blockDim.x) {
-    kn[i] = kraw[i];
-    vn[i] = round_store<KT>(vraw[i]);
+  for (int i = tid; i < group * d; i += NT) qn[i] = __ldcg(a.qkv + (g * group) * d + i);
+  for (int i = tid; i < d; i += NT) {
+    kn[i] = __ldcg(kraw + i);
+    vn[i] = round_store<KT>(__ldcg(vraw + i));
   }
-  __syncthreads();
+  sync();
   for (int h = warp; h <= group; h += kAttnWarps) {
     if (h < group)
       norm_rope_warp(qn + h * d, a.g_q, a.eps, d, cs, sn, lane);
     else
       norm_rope_warp(kn, a.g_k, a.eps, d, cs, sn, lane);
   }
-  __syncthreads();
-  for (int i = tid; i < d; i += blockDim.x) kn[i] = round_store<KT>(kn[i]);
-  __syncthreads();
+  sync();
+  for (int i = tid; i < d; i += NT) kn[i] = round_store<KT>(kn[i]);
+  sync();
   const size_t head_base = static_cast<size_t>(g) * a.max_seq * d;
   if (t1 == n) {  // this CTA's range holds the current position: append to the cache
-    for (int i = tid; i < d; i += blockDim.x) {
+    for (int i = tid; i < d; i += NT) {
       store1<KT>(a.kc, head_base + static_cast<size_t>(pos) * d + i, kn[i]);
       store1<KT>(a.vc, head_base + static_cast<size_t>(pos) * d + i, vn[i]);
     }
@@ -236,9 +236,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
     }
     if (active) *reinterpret_cast<float4*>(wo + (warp * group + h) * d + 4 * lane) = o[h];
   }
-  __syncthreads();
-  const int parts = gridDim.y;
-  for (int idx = tid; idx < group * d; idx += blockDim.x) {
+  sync();
+  for (int idx = tid; idx < group * d; idx += NT) {
     const int h = idx / d, e = idx - h * d;
     float M = -INFINITY;
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w * group + h]);
@@ -259,18 +258,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
       }
     }
   }
-  (void)parts;
   if (nsplit == 1) return;
 
   // Split merge: the last CTA of this key/value head to finish combines all splits.
-  __shared__ int s_last;
   __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(a.counter + g, 1u) == static_cast<uint32_t>(nsplit - 1));
-  __syncthreads();
-  if (!s_last) return;
+  sync();
+  if (tid == 0) *s_last = (atomicAdd(a.counter + g, 1u) == static_cast<uint32_t>(nsplit - 1));
+  sync();
+  if (!*s_last) return;
   __threadfence();
-  for (int idx = tid; idx < group * d; idx += blockDim.x) {
+  for (int idx = tid; idx < group * d; idx += NT) {
     const int h = idx / d, e = idx - h * d;
     float M = -INFINITY;
     for (int k = 0; k < nsplit; ++k) {
@@ -287,6 +284,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
     a.out[(g * group + h) * d + e] = O / L;
   }
   if (tid == 0) a.counter[g] = 0u;
+}
+
+template <typename KT, int GMAX>
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const AttnArgs a) {
+  extern __shared__ __align__(16) float asmem[];
+  __shared__ int s_last;
+  pdl_trigger();
+  pdl_wait();
+  const int pos = a.ctrl[0];
+  if (pos < 0 || pos >= a.max_seq) {
+    if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, ERR_BAD_POSITION);
+    return;
+  }
+  attn_decode_body<KT, GMAX, kAttnWarps * 32>(a, blockIdx.x, blockIdx.y, pos, asmem, threadIdx.x,
+                                              CtaSync{}, &s_last);
 }
 
 }  // namespace wsg

@@ -18,6 +18,7 @@
 // replays for every step. Kernels after the first carry a programmatic
 // dependent-launch edge: each GEMV starts streaming its weights while its
 // predecessor finishes, and waits only before reading activations.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <vector>
@@ -25,6 +26,12 @@
 #include "attention.cuh"
 #include "common.h"
 #include "gemv_stream.cuh"
+#include "megakernel.cuh"
+
+namespace wsg {
+void* mk_kernel_f32(bool kv_bf16, bool group_le2);
+void* mk_kernel_bf16(bool kv_bf16, bool group_le2);
+}  // namespace wsg
 
 using namespace wsg;
 
@@ -40,7 +47,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
 
 struct Layout {
-  size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, rope_cos, rope_sin, kc, vc;
+  size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, bar, mk_layers, rope_cos, rope_sin,
+      kc, vc;
   size_t total;
 };
 
@@ -61,6 +69,7 @@ bool config_ok(const dec_config* c, std::string* why) {
   if (c->kvdtype != DEC_F32 && c->kvdtype != DEC_BF16) return bad("kvdtype must be DEC_F32 or DEC_BF16");
   if (c->max_seq < 1) return bad("max_seq must be >= 1");
   if (c->chunk_cap < 0) return bad("chunk_cap must be >= 0");
+  if (c->engine != DEC_ENGINE_PERSISTENT && c->engine != DEC_ENGINE_STAGED) return bad("unknown engine");
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("eps >= 0 and rope_theta > 0 required");
   return true;
 }
@@ -88,6 +97,8 @@ Layout make_layout(const dec_config& c) {
   L.mval = take(kArgmaxPartsMax * 4);
   L.midx = take(kArgmaxPartsMax * 4);
   L.mcnt = take(16);
+  L.bar = take(16);
+  L.mk_layers = take(static_cast<size_t>(c.layers) * sizeof(MkLayer));
   L.rope_cos = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   L.rope_sin = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   const size_t cache = static_cast<size_t>(c.layers) * kvw * c.max_seq * dtype_bytes(c.kvdtype);
@@ -147,6 +158,9 @@ struct dec_ctx {
   Plan p_qkv, p_o, p_gu, p_down, p_vocab;
   size_t attn_smem = 0;
   int nsplit_max = 1;
+  MkArgs mk{};          // persistent-engine arguments (per-call fields filled at launch)
+  size_t mk_smem = 0;
+  int mk_grid = 0;
   std::string err;
 
   template <typename T>
@@ -317,6 +331,136 @@ dec_status enqueue_step_t(dec_ctx* c, cudaStream_t st, bool full) {
   return DEC_OK;
 }
 
+
+// ---- persistent engine ----
+
+MkGeom mk_geom_for(int in, int elem) {
+  MkGeom g{};
+  g.row_bytes = in * elem;
+  if (g.row_bytes > kMkSlot) {
+    g.spr = (g.row_bytes + kMkSlot - 1) / kMkSlot;
+    g.seg_bytes = ((g.row_bytes + g.spr - 1) / g.spr + 15) / 16 * 16;
+    g.spr = (g.row_bytes + g.seg_bytes - 1) / g.seg_bytes;
+    g.rps = 1;
+  } else {
+    g.spr = 1;
+    g.seg_bytes = g.row_bytes;
+    g.rps = kMkSlot / g.row_bytes;
+  }
+  return g;
+}
+
+// Persistent kernel instance for the configuration (defined per weight dtype in
+// megakernel_f32.cu / megakernel_bf16.cu).
+void* mk_kernel(const dec_config& g) {
+  const bool g2 = g.n_q / g.n_kv <= 2;
+  return g.wdtype == DEC_F32 ? mk_kernel_f32(g.kvdtype == DEC_BF16, g2) : mk_kernel_bf16(g.kvdtype == DEC_BF16, g2);
+}
+
+// Plan the persistent engine: ring depth, staging sizes, argument template.
+dec_status plan_persistent(dec_ctx* c) {
+  const dec_config& g = c->cfg;
+  const int elem = static_cast<int>(dtype_bytes(g.wdtype));
+  const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;
+  const int G = c->di.sms;
+  MkArgs& a = c->mk;
+  a = MkArgs{};
+  a.L = g.layers;
+  a.H = g.hidden;
+  a.I = g.inter;
+  a.n_q = g.n_q;
+  a.n_kv = g.n_kv;
+  a.d = g.head_dim;
+  a.V = g.vocab;
+  a.eps = g.eps;
+  a.gq = mk_geom_for(g.hidden, elem);
+  a.go = mk_geom_for(qw, elem);
+  a.gg = mk_geom_for(g.hidden, elem);
+  a.gd = mk_geom_for(g.inter, elem);
+  a.gv = mk_geom_for(g.hidden, elem);
+  auto cdiv = [](long long x, long long y) { return static_cast<int>((x + y - 1) / y); };
+  int part = cdiv(qw + 2 * kvw, G) * a.gq.spr;
+  part = std::max(part, cdiv(g.hidden, G) * a.go.spr);
+  part = std::max(part, 2 * cdiv(g.inter, G) * a.gg.spr);
+  part = std::max(part, cdiv(g.hidden, G) * a.gd.spr);
+  part = std::max(part, cdiv(g.vocab, G) * a.gv.spr);
+  a.xs_floats = (std::max(g.hidden, std::max(qw, g.inter)) + 3) / 4 * 4;
+  a.part_floats = (part + 3) / 4 * 4;
+  const int attn_floats = static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 3) / 4);
+  if (a.xs_floats + a.part_floats < attn_floats) a.part_floats = (attn_floats - a.xs_floats + 3) / 4 * 4;
+  const size_t fixed = 2 * kMkSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats);
+  const size_t static_smem = sizeof(MkShared) + 64 * 4 + 32 * 4 + 256;
+  if (fixed + static_smem + kMkSlot > c->di.smem_optin)
+    return fail(&c->err, DEC_EINVAL, "persistent engine: staging needs %zu B of shared memory", fixed);
+  a.slots = static_cast<int>(std::min<size_t>(kMkSlotsMax, (c->di.smem_optin - fixed - static_smem) / kMkSlot));
+  c->mk_smem = static_cast<size_t>(a.slots) * kMkSlot + fixed;
+  c->mk_grid = G;
+  void* k = mk_kernel(g);
+  WSG_CUDA_TRY(&c->err, cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(c->mk_smem)));
+  int per_sm = 0;
+  WSG_CUDA_TRY(&c->err, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kMkThreads, c->mk_smem));
+  if (per_sm < 1) return fail(&c->err, DEC_EINVAL, "persistent engine: kernel does not fit on an SM");
+  a.h = c->at<float>(c->L.h);
+  a.qkv = c->at<float>(c->L.qkv);
+  a.attn = c->at<float>(c->L.attn);
+  a.act = c->at<float>(c->L.act);
+  a.logits = c->at<float>(c->L.logits);
+  a.tok = c->at<int32_t>(c->L.tok);
+  a.ctrl = c->at<int32_t>(c->L.ctrl);
+  a.err = c->at<uint32_t>(c->L.err);
+  a.mval = c->at<float>(c->L.mval);
+  a.midx = c->at<int32_t>(c->L.midx);
+  a.mcnt = c->at<uint32_t>(c->L.mcnt);
+  a.bar = c->at<uint32_t>(c->L.bar);
+  a.layers = c->at<MkLayer>(c->L.mk_layers);
+  AttnArgs& at = a.at;
+  at.qkv = a.qkv;
+  at.eps = g.eps;
+  at.rope_cos = c->at<float>(c->L.rope_cos);
+  at.rope_sin = c->at<float>(c->L.rope_sin);
+  at.ctrl = a.ctrl;
+  at.kc = c->ws + c->L.kc;
+  at.vc = c->ws + c->L.vc;
+  at.max_seq = g.max_seq;
+  at.n_q = g.n_q;
+  at.n_kv = g.n_kv;
+  at.d = g.head_dim;
+  at.out = a.attn;
+  at.part = c->at<float>(c->L.apart);
+  at.counter = c->at<uint32_t>(c->L.acnt);
+  at.nsplit_max = std::max(1, std::min(kSplitMax, G / g.n_kv));
+  at.tmin = 64;
+  at.scale = 1.0f / std::sqrt(static_cast<float>(g.head_dim));
+  at.err = a.err;
+  a.kv_layer_bytes = c->kv_layer_elems() * dtype_bytes(g.kvdtype);
+  return DEC_OK;
+}
+
+// nsteps forwards at positions pos0.. in one cooperative launch.
+dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, bool head_last) {
+  MkArgs a = c->mk;
+  a.embed = c->w.embed;
+  a.g_final = c->w.g_final;
+  a.pos0 = pos0;
+  a.nsteps = nsteps;
+  a.head_every = head_every ? 1 : 0;
+  a.head_last = head_last ? 1 : 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c->mk_grid);
+  cfg.blockDim = dim3(kMkThreads);
+  cfg.dynamicSmemBytes = c->mk_smem;
+  cfg.stream = c->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  WSG_CUDA_TRY(&c->err, cudaLaunchKernelExC(&cfg, mk_kernel(c->cfg), args));
+  return DEC_OK;
+}
+
 dec_status capture(dec_ctx* c, bool full, cudaGraphExec_t* out) {
   WSG_CUDA_TRY(&c->err, cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
   dec_status s = c->cfg.wdtype == DEC_F32 ? enqueue_step_t<float>(c, c->cap, full)
@@ -444,6 +588,7 @@ extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_
   if (c->nsplit_max < 1) c->nsplit_max = 1;
   if (c->nsplit_max > kSplitMax) c->nsplit_max = kSplitMax;
   s = cfg->wdtype == DEC_F32 ? prepare_kernels<float>(c) : prepare_kernels<uint16_t>(c);
+  if (s == DEC_OK && cfg->engine == DEC_ENGINE_PERSISTENT) s = plan_persistent(c);
   if (s != DEC_OK) {
     thread_error() = c->err;
     return bail(s);
@@ -466,6 +611,14 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
   c->layers.assign(w->layers, w->layers + c->cfg.layers);
   c->w = *w;
   c->w.layers = c->layers.data();
+  std::vector<MkLayer> tab(c->cfg.layers);
+  for (int l = 0; l < c->cfg.layers; ++l) {
+    const dec_layer_weights& x = c->layers[l];
+    tab[l] = MkLayer{x.w_q, x.w_k, x.w_v, x.w_o, x.w_gate, x.w_up, x.w_down, x.g_in, x.g_post, x.g_q, x.g_k};
+  }
+  WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->ws + c->L.mk_layers, tab.data(), tab.size() * sizeof(MkLayer),
+                                        cudaMemcpyHostToDevice, c->stream));
+  WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
   // Graphs bake in the weight pointers: drop any captured with older ones.
   if (c->g_full) cudaGraphExecDestroy(c->g_full);
   if (c->g_body) cudaGraphExecDestroy(c->g_body);
@@ -479,7 +632,8 @@ extern "C" dec_status dec_reset(dec_ctx* c) {
   // Earlier asynchronous copies may still read the pinned token slots.
   WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
   c->pos = 0;
-  WSG_CUDA_TRY(&c->err, cudaMemsetAsync(c->ws + c->L.ctrl, 0, 64 * 4, c->stream));
+  // control words, counters, activations and partials (everything before the layer table)
+  WSG_CUDA_TRY(&c->err, cudaMemsetAsync(c->ws, 0, c->L.mk_layers, c->stream));
   WSG_CUDA_TRY(&c->err, cudaMemsetAsync(c->ws + c->L.kc, 0, c->L.total - c->L.kc, c->stream));
   return DEC_OK;
 }
@@ -493,10 +647,12 @@ extern "C" dec_status dec_step(dec_ctx* c, int32_t token, uint32_t flags, float*
   if (!c->have_weights) return fail(&c->err, DEC_ESTATE, "dec_step: weights not loaded");
   if (c->pos >= c->cfg.max_seq)
     return fail(&c->err, DEC_ECAPACITY, "dec_step: position %d reached max_seq %d", c->pos, c->cfg.max_seq);
-  dec_status s = ensure_graphs(c, full);
+  const bool persistent = c->cfg.engine == DEC_ENGINE_PERSISTENT;
+  dec_status s = persistent ? DEC_OK : ensure_graphs(c, full);
   if (s != DEC_OK) return s;
   if ((s = put_tokens(c, &token, 1)) != DEC_OK) return s;
-  if ((s = run_steps(c, full, 1)) != DEC_OK) return s;
+  s = persistent ? run_persistent(c, c->pos, 1, full, false) : run_steps(c, full, 1);
+  if (s != DEC_OK) return s;
   const int32_t p = c->pos;
   c->pos += 1;
   if (full) return finish_head(c, p, d_logits, h_next);
@@ -513,14 +669,22 @@ extern "C" dec_status dec_prefill_chunk(dec_ctx* c, const int32_t* h_tokens, int
   if (static_cast<long long>(c->pos) + n > c->cfg.max_seq)
     return fail(&c->err, DEC_ECAPACITY, "dec_prefill_chunk: %d rows at position %d exceed max_seq %d", n, c->pos,
                 c->cfg.max_seq);
-  dec_status s = ensure_graphs(c, false);
-  if (s == DEC_OK && is_last) s = ensure_graphs(c, true);
+  const bool persistent = c->cfg.engine == DEC_ENGINE_PERSISTENT;
+  dec_status s = DEC_OK;
+  if (!persistent) {
+    s = ensure_graphs(c, false);
+    if (s == DEC_OK && is_last) s = ensure_graphs(c, true);
+  }
   if (s != DEC_OK) return s;
   if ((s = put_tokens(c, h_tokens, n)) != DEC_OK) return s;
-  const int body = is_last ? n - 1 : n;
-  if ((s = run_steps(c, false, body)) != DEC_OK) return s;
   const int32_t p0 = c->pos;
-  if (is_last && (s = run_steps(c, true, 1)) != DEC_OK) return s;
+  if (persistent) {
+    if ((s = run_persistent(c, p0, n, false, is_last != 0)) != DEC_OK) return s;
+  } else {
+    const int body = is_last ? n - 1 : n;
+    if ((s = run_steps(c, false, body)) != DEC_OK) return s;
+    if (is_last && (s = run_steps(c, true, 1)) != DEC_OK) return s;
+  }
   c->pos += n;
   if (is_last) return finish_head(c, p0 + n - 1, d_logits, h_next);
   return DEC_OK;
@@ -533,10 +697,12 @@ extern "C" dec_status dec_generate(dec_ctx* c, int32_t token, int32_t n, int32_t
   if (static_cast<long long>(c->pos) + n > c->cfg.max_seq)
     return fail(&c->err, DEC_ECAPACITY, "dec_generate: %d steps at position %d exceed max_seq %d", n, c->pos,
                 c->cfg.max_seq);
-  dec_status s = ensure_graphs(c, true);
+  const bool persistent = c->cfg.engine == DEC_ENGINE_PERSISTENT;
+  dec_status s = persistent ? DEC_OK : ensure_graphs(c, true);
   if (s != DEC_OK) return s;
   if ((s = put_tokens(c, &token, 1)) != DEC_OK) return s;
-  if ((s = run_steps(c, true, n)) != DEC_OK) return s;
+  s = persistent ? run_persistent(c, c->pos, n, true, false) : run_steps(c, true, n);
+  if (s != DEC_OK) return s;
   WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(d_tokens_out, c->at<int32_t>(c->L.tok) + c->pos + 1, sizeof(int32_t) * n,
                                         cudaMemcpyDeviceToDevice, c->stream));
   c->pos += n;

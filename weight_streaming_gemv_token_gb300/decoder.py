@@ -34,7 +34,7 @@ class Decoder:
     """
 
     def __init__(self, shape, weights: dict, kv_dtype: str = "f32", max_seq: int = 4096, chunk_cap: int = 0,
-                 stream: torch.cuda.Stream | None = None):
+                 stream: torch.cuda.Stream | None = None, engine: str = "persistent"):
         wd = weights.get("wdtype", "f32")
         self.shape = shape
         self.cfg = B.dec_config(
@@ -42,7 +42,8 @@ class Decoder:
             head_dim=shape.head_dim, vocab=shape.vocab, eps=shape.eps, rope_theta=shape.rope_theta,
             wdtype=B.DEC_F32 if wd == "f32" else B.DEC_BF16,
             kvdtype=B.DEC_F32 if kv_dtype == "f32" else B.DEC_BF16,
-            max_seq=max_seq, chunk_cap=chunk_cap)
+            max_seq=max_seq, chunk_cap=chunk_cap,
+            engine=B.DEC_ENGINE_PERSISTENT if engine == "persistent" else B.DEC_ENGINE_STAGED)
         self.kv_dtype = kv_dtype
         self.stream = stream if stream is not None else torch.cuda.current_stream()
         nbytes = B.dec_workspace_bytes(self.cfg)

@@ -108,7 +108,7 @@ __device__ __forceinline__ const MkGeom& mk_geom(const MkArgs& a, int st) {
 }
 
 // This CTA's rows of one stage: balanced contiguous units, cut at source boundaries.
-__device__ MkSlice mk_slice(const MkArgs& a, const MkLayer& lw, int st, int c, int G) {
+__device__ __forceinline__ MkSlice mk_slice(const MkArgs& a, const MkLayer& lw, int st, int c, int G) {
   MkSlice s;
   s.np = 0;
   const MkGeom& gm = mk_geom(a, st);

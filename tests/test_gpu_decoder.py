@@ -221,3 +221,38 @@ def test_api_errors(tiny_w):
         B.dec_step(ctx, 1)
     assert e.value.status == B.DEC_ESTATE
     B.dec_destroy(ctx)
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+@pytest.mark.parametrize("model", ["tiny", "qwen3"])
+def test_multistep_launch_is_bitwise_single_steps(engine, model, tiny_w, request):
+    """One call running many forwards equals the same forwards run one call each, bit for bit."""
+    import torch
+
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.TINY if model == "tiny" else Wl.QWEN3_06B
+    w = tiny_w if model == "tiny" else request.getfixturevalue("qwen_f32")
+    prompt = Wl.prompt_uniform(20, s.vocab, seed=7)
+    la = torch.empty(s.vocab, device="cuda")
+    lb = torch.empty(s.vocab, device="cuda")
+    a = Decoder(s, w, max_seq=40, engine=engine)
+    first_a = a.prefill(prompt, is_last=True, logits=la)
+    seq_a = [first_a] + a.generate(first_a, 9).cpu().tolist()
+    b = Decoder(s, w, max_seq=40, engine=engine)
+    for t in prompt[:-1]:
+        b.step(int(t), skip_logits=True)
+    first_b = b.step(int(prompt[-1]), logits=lb)
+    assert torch.equal(la, lb)
+    seq_b = [first_b]
+    for _ in range(9):
+        seq_b.append(b.step(seq_b[-1]))
+    assert seq_a == seq_b
+    for l in range(s.layers):
+        ka, va, na = a.kv(l)
+        kb, vb, nb = b.kv(l)
+        assert na == nb == 29
+        assert torch.equal(ka[:, :29], kb[:, :29]), f"K layer {l}"
+        assert torch.equal(va[:, :29], vb[:, :29]), f"V layer {l}"
+    assert a.device_errors() == 0 and b.device_errors() == 0

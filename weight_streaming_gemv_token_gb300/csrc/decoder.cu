@@ -388,12 +388,13 @@ dec_status plan_persistent(dec_ctx* c) {
   a.part_floats = (part + 3) / 4 * 4;
   const int attn_floats = static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 3) / 4);
   if (a.xs_floats + a.part_floats < attn_floats) a.part_floats = (attn_floats - a.xs_floats + 3) / 4 * 4;
-  const size_t fixed = 2 * kMkSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats);
-  const size_t static_smem = sizeof(MkShared) + 64 * 4 + 32 * 4 + 256;
-  if (fixed + static_smem + kMkSlot > c->di.smem_optin)
+  const size_t fixed = kMkWarps * kMkWarpSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats);
+  const size_t static_smem = 64 * 4 + 32 * 4 + 8 + 256;
+  const size_t per_slot = static_cast<size_t>(kMkWarps) * kMkSlot;  // one slot in every warp's ring
+  if (fixed + static_smem + per_slot > c->di.smem_optin)
     return fail(&c->err, DEC_EINVAL, "persistent engine: staging needs %zu B of shared memory", fixed);
-  a.slots = static_cast<int>(std::min<size_t>(kMkSlotsMax, (c->di.smem_optin - fixed - static_smem) / kMkSlot));
-  c->mk_smem = static_cast<size_t>(a.slots) * kMkSlot + fixed;
+  a.wslots = static_cast<int>(std::min<size_t>(kMkWarpSlotsMax, (c->di.smem_optin - fixed - static_smem) / per_slot));
+  c->mk_smem = static_cast<size_t>(a.wslots) * per_slot + fixed;
   c->mk_grid = G;
   void* k = mk_kernel(g);
   WSG_CUDA_TRY(&c->err, cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -6,26 +6,28 @@
 // 227 ordered dispatches. This kernel keeps the whole GPU busy inside one
 // launch: one CTA per SM, co-resident by cooperative launch.
 //
-//  * Warp 8 of each CTA is a producer. One lane streams, in order, every
-//    weight segment this CTA will need for all stages of all requested steps
-//    (QKV, O, gate/up, down of every layer, then the vocabulary slice) into a
-//    ring of 4 KB shared-memory slots with bulk copies. Weights never depend
-//    on activations, so the producer runs ahead across stage and layer
-//    boundaries, limited only by free slots; HBM keeps streaming while the
-//    consumers wait at barriers.
-//  * Warps 0-7 are consumers. Per stage they stage the activation vector (with
-//    the fused RMSNorm), take the stage's segments round-robin, reduce partial
-//    dots in a fixed order, run the fused epilogue, and meet the other CTAs at
-//    a grid barrier before the next stage reads what this one wrote.
+//  * Every weight segment (at most 4 KB) this CTA will read, over all stages
+//    of all requested steps (QKV, O, gate/up, down of every layer, then the
+//    vocabulary slice), is assigned to one of its 8 warps: segment j of a
+//    stage goes to warp j mod 8. Each warp owns a private ring of 4 KB
+//    shared-memory slots and keeps it full: lane 0 walks a cursor through the
+//    warp's future segments (across stage, layer and step boundaries) and
+//    issues a bulk copy for the next one each time a slot is consumed.
+//    Weights never depend on activations, so the rings hold the next stages'
+//    weights while the CTA waits at a barrier and HBM keeps streaming.
+//  * Per stage the CTA stages the activation vector (with the fused RMSNorm),
+//    each warp reduces its segments to partial dots, the partials are summed
+//    in a fixed order, the fused epilogue runs, and the CTAs meet at a grid
+//    barrier before the next stage reads what this one wrote.
 //  * Attention runs between QKV and O on n_kv x nsplit CTAs (the same body as
 //    the standalone attention kernel: Q/K norm, RoPE, KV append, key-parallel
 //    splits merged by the last CTA).
 //  * The head (final RMSNorm, vocabulary GEMV, two-pass argmax) writes the
 //    next token, which the next step's embedding gather reads after a barrier.
 //
-// Every wait is bounded. On a timeout the CTA raises an abort flag, the
-// producer stops issuing, the consumers wait (bounded) for the copies already
-// in flight, and the error word records the cause.
+// Every wait is bounded. On a timeout the CTA raises an abort flag, stops
+// issuing, waits (bounded) for the copies already in flight, and the error
+// word records the cause.
 #pragma once
 #include <cstdint>
 
@@ -35,11 +37,10 @@
 
 namespace wsg {
 
-constexpr int kMkConsumerWarps = 8;
-constexpr int kMkConsumers = kMkConsumerWarps * 32;
-constexpr int kMkThreads = kMkConsumers + 32;
-constexpr int kMkSlot = 4096;      // bytes per ring slot
-constexpr int kMkSlotsMax = 64;    // ring depth limit (barrier array size)
+constexpr int kMkWarps = 8;
+constexpr int kMkThreads = kMkWarps * 32;
+constexpr int kMkSlot = 4096;         // bytes per ring slot
+constexpr int kMkWarpSlotsMax = 8;    // ring slots per warp, upper bound
 
 enum : uint32_t { ERR_GRID_BARRIER_TIMEOUT = 1u << 4 };
 
@@ -77,7 +78,7 @@ struct MkArgs {
   uint32_t* bar;  // [0] grid barrier arrivals, [1] CTAs finished
   AttnArgs at;    // kc / vc point at layer 0's cache
   size_t kv_layer_bytes;
-  int32_t slots;  // ring slots in use (<= kMkSlotsMax)
+  int32_t wslots;  // ring slots per warp (<= kMkWarpSlotsMax)
   int32_t xs_floats, part_floats;
   int32_t pos0, nsteps;
   int32_t head_every, head_last;  // head on every step / on the last step
@@ -185,130 +186,153 @@ __device__ __forceinline__ MkSeg mk_seg(const MkSlice& s, const MkGeom& gm, int 
   return r;
 }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kMkConsumers) : "memory"); }
-
-struct ConsumerSync {
-  __device__ __forceinline__ void operator()() const { consumer_sync(); }
-};
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
 
-struct MkShared {
-  int abort;          // set on any timeout
-  int issued;         // segments the producer has issued
-  int producer_done;  // producer has stopped issuing
-  int s_last;
+__device__ __forceinline__ bool mk_head_on(const MkArgs& a, int step) {
+  return a.head_every || (a.head_last && step == a.nsteps - 1);
+}
+
+// Walks one warp's segments in consumption order: steps, layers, stages
+// (QKV, O, gate/up, down, then the vocabulary on head steps), segment j of a
+// stage for j = warp, warp + 8, ...
+struct MkCursor {
+  int step, layer, stage, j;
+  bool done;
+  MkSlice sl;
 };
+
+__device__ __forceinline__ void mk_cursor_settle(MkCursor& k, const MkArgs& a, int c, int G, int warp) {
+  while (true) {
+    if (k.step >= a.nsteps) {
+      k.done = true;
+      return;
+    }
+    k.sl = mk_slice(a, a.layers[k.stage == MK_VOCAB ? 0 : k.layer], k.stage, c, G);
+    k.j = warp;
+    if (k.j < k.sl.nseg) return;
+    // next stage
+    if (k.stage == MK_VOCAB) {
+      ++k.step;
+      k.layer = 0;
+      k.stage = MK_QKV;
+    } else if (k.stage == MK_DOWN) {
+      if (k.layer + 1 < a.L) {
+        ++k.layer;
+        k.stage = MK_QKV;
+      } else if (mk_head_on(a, k.step)) {
+        k.stage = MK_VOCAB;
+      } else {
+        ++k.step;
+        k.layer = 0;
+        k.stage = MK_QKV;
+      }
+    } else {
+      ++k.stage;
+    }
+  }
+}
+
+__device__ __forceinline__ void mk_cursor_next(MkCursor& k, const MkArgs& a, int c, int G, int warp) {
+  k.j += kMkWarps;
+  if (k.j < k.sl.nseg) return;
+  if (k.stage == MK_VOCAB) {
+    ++k.step;
+    k.layer = 0;
+    k.stage = MK_QKV;
+  } else if (k.stage == MK_DOWN) {
+    if (k.layer + 1 < a.L) {
+      ++k.layer;
+      k.stage = MK_QKV;
+    } else if (mk_head_on(a, k.step)) {
+      k.stage = MK_VOCAB;
+    } else {
+      ++k.step;
+      k.layer = 0;
+      k.stage = MK_QKV;
+    }
+  } else {
+    ++k.stage;
+  }
+  mk_cursor_settle(k, a, c, G, warp);
+}
 
 template <typename WT, typename KT, int GMAX>
 __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ MkShared sh;
   __shared__ float red[64];
   __shared__ int redi[32];
-  const int S = a.slots;
-  unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * kMkSlot);
-  uint64_t* empty = full + kMkSlotsMax;
-  float* xs = reinterpret_cast<float*>(empty + kMkSlotsMax);
-  float* part = xs + a.xs_floats;
-  float* ascratch = xs;  // the attention stage reuses the GEMV staging area
-
+  __shared__ int s_abort, s_last;
+  const int R = a.wslots;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
-  volatile MkShared* vsh = &sh;
+  unsigned char* myring = smem + static_cast<size_t>(warp) * R * kMkSlot;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kMkWarps) * R * kMkSlot);
+  uint64_t* mybars = bars + warp * kMkWarpSlotsMax;
+  float* xs = reinterpret_cast<float*>(bars + kMkWarps * kMkWarpSlotsMax);
+  float* part = xs + a.xs_floats;
+  float* ascratch = xs;  // the attention stage reuses the GEMV staging area
+  volatile int* vabort = &s_abort;
 
+  // ---- each warp primes its ring ----
+  MkCursor cur;
+  int issued = 0;    // lane 0: segments issued into this warp's ring
+  int consumed = 0;  // all lanes: segments consumed
+  const uint64_t pol = l2_policy_evict_first();
+  auto issue_one = [&]() {  // lane 0 only; requires issued < consumed + R
+    const MkGeom& gm = mk_geom(a, cur.stage);
+    const MkSeg sg = mk_seg(cur.sl, gm, cur.j);
+    const int slot = issued % R;
+    mbar_arrive_expect_tx(&mybars[slot], static_cast<uint32_t>(sg.bytes));
+    bulk_g2s(myring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes), &mybars[slot], pol);
+    ++issued;
+    mk_cursor_next(cur, a, c, G, warp);
+  };
   if (tid == 0) {
-    sh.abort = 0;
-    sh.issued = 0;
-    sh.producer_done = 0;
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
+    s_abort = 0;
+    s_last = 0;
+  }
+  if (lane == 0) {
+    for (int s = 0; s < R; ++s) mbar_init(&mybars[s], 1);
     fence_mbar_init();
+    cur.step = 0;
+    cur.layer = 0;
+    cur.stage = MK_QKV;
+    cur.done = false;
+    mk_cursor_settle(cur, a, c, G, warp);
+    while (!cur.done && issued < R) issue_one();
   }
   __syncthreads();
 
-  auto head_on = [&](int step) { return a.head_every || (a.head_last && step == a.nsteps - 1); };
-
-  // ------------------------------------------------------------- producer ----
-  if (warp == kMkConsumerWarps) {
-    if (lane == 0) {
-      const uint64_t pol = l2_policy_evict_first();
-      int g = 0;
-      bool stop = false;
-      auto stream_stage = [&](const MkSlice& sl, const MkGeom& gm) {
-        for (int j = 0; j < sl.nseg && !stop; ++j, ++g) {
-          const int slot = g % S;
-          if (g >= S && !mbar_wait(&empty[slot], ((g / S) - 1) & 1)) {
-            vsh->abort = 1;
-            atomicOr(a.err, ERR_MBAR_TIMEOUT);
-            stop = true;
-            break;
-          }
-          if (vsh->abort) {
-            stop = true;
-            break;
-          }
-          const MkSeg sg = mk_seg(sl, gm, j);
-          mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(sg.bytes));
-          bulk_g2s(ring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes), &full[slot],
-                   pol);
-          vsh->issued = g + 1;
-        }
-      };
-      for (int step = 0; step < a.nsteps && !stop; ++step) {
-        for (int l = 0; l < a.L && !stop; ++l) {
-          const MkLayer lw = a.layers[l];
-          for (int st = MK_QKV; st <= MK_DOWN && !stop; ++st) stream_stage(mk_slice(a, lw, st, c, G), mk_geom(a, st));
-        }
-        if (!stop && head_on(step)) stream_stage(mk_slice(a, a.layers[0], MK_VOCAB, c, G), a.gv);
-      }
-      vsh->producer_done = 1;
-    }
-    return;
-  }
-
-  // ------------------------------------------------------------- consumers ----
-  const int ctid = tid;  // 0 .. kMkConsumers-1
-  int gbase = 0;         // global index of the current stage's first segment
   uint32_t sync_target = 0;
   const int qw = a.n_q * a.d;
-  const int group = a.n_q / a.n_kv;
 
   auto grid_sync = [&]() -> bool {
-    consumer_sync();
-    if (ctid == 0) {
+    __syncthreads();
+    if (tid == 0) {
       sync_target += G;
       __threadfence();
       atomicAdd(a.bar, 1u);
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(a.bar) < sync_target) {
-        if (vsh->abort) break;
         if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
-          vsh->abort = 1;
+          *vabort = 1;
           atomicOr(a.err, ERR_GRID_BARRIER_TIMEOUT);
           break;
         }
       }
     }
-    consumer_sync();
-    return !vsh->abort;
+    __syncthreads();
+    return !*vabort;
   };
 
   // Stage the activation vector: plain copy, or RMSNorm(src) * gain.
   auto stage_x = [&](const float* src, const WT* wsrc, int in, const float* gain, bool store_h) {
     float ss = 0.f;
-    for (int i = ctid; i < in; i += kMkConsumers) {
+    for (int i = tid; i < in; i += kMkThreads) {
       const float v = wsrc ? load_f32<WT>(wsrc, i) : __ldcg(src + i);
       if (store_h) a.h[i] = v;
       xs[xs_index<WT>(i, in)] = v;
@@ -317,52 +341,51 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     if (gain) {
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
-      consumer_sync();
+      __syncthreads();
       float t = 0.f;
 #pragma unroll
-      for (int w = 0; w < kMkConsumerWarps; ++w) t += red[w];
+      for (int w = 0; w < kMkWarps; ++w) t += red[w];
       const float inv = 1.0f / sqrtf(t / static_cast<float>(in) + a.eps);
-      for (int i = ctid; i < in; i += kMkConsumers) {
+      for (int i = tid; i < in; i += kMkThreads) {
         const int k = xs_index<WT>(i, in);
         xs[k] = xs[k] * inv * gain[i];
       }
     }
-    consumer_sync();
+    __syncthreads();
   };
 
-  // Consume this CTA's segments of one stage into part[].
+  // This warp's segments of one stage, in ring order, into part[].
   auto consume = [&](const MkSlice& sl, const MkGeom& gm, int in) -> bool {
-    const int rchunks = gm.row_bytes >> 4;  // 16-byte chunks per row
-    for (int j = warp; j < sl.nseg; j += kMkConsumerWarps) {
-      const int g = gbase + j;
-      const int slot = g % S;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (g / S) & 1));
+    for (int j = warp; j < sl.nseg; j += kMkWarps) {
+      const int slot = consumed % R;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&mybars[slot], (consumed / R) & 1));
       if (!ok) {
-        if (lane == 0) {
-          vsh->abort = 1;
-          atomicOr(a.err, ERR_MBAR_TIMEOUT);
-        }
-        return false;
+        if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
+        *vabort = 1;
+        break;
       }
       const MkSeg sg = mk_seg(sl, gm, j);
-      const unsigned char* buf = ring + static_cast<size_t>(slot) * kMkSlot;
+      const unsigned char* buf = myring + static_cast<size_t>(slot) * kMkSlot;
       if (sg.nr == 1) {
         float v = seg_dot<WT>(buf, xs, sg.off / static_cast<int>(sizeof(WT)), sg.bytes, in, lane);
         v = warp_sum(v);
         if (lane == 0) part[sg.lrow * gm.spr + sg.part] = v;
       } else {
         for (int r = 0; r < sg.nr; ++r) {
-          float v = seg_dot<WT>(buf + static_cast<size_t>(r) * gm.row_bytes, xs, 0, rchunks << 4, in, lane);
+          float v = seg_dot<WT>(buf + static_cast<size_t>(r) * gm.row_bytes, xs, 0, gm.row_bytes, in, lane);
           v = warp_sum(v);
           if (lane == 0) part[sg.lrow + r] = v;
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);
+      ++consumed;
+      if (lane == 0 && !cur.done && !*vabort) {
+        fence_proxy_async_smem();
+        issue_one();
+      }
     }
-    gbase += sl.nseg;
-    consumer_sync();
-    return !vsh->abort;
+    __syncthreads();
+    return !*vabort;
   };
 
   auto row_value = [&](const MkGeom& gm, int lr) {
@@ -382,7 +405,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         if (l == 0) {
           int t = __ldcg(a.tok + pos);
           if (t < 0 || t >= a.V) {
-            if (ctid == 0) atomicOr(a.err, ERR_BAD_TOKEN);
+            if (tid == 0) atomicOr(a.err, ERR_BAD_TOKEN);
             t = 0;
           }
           stage_x(nullptr, static_cast<const WT*>(a.embed) + static_cast<size_t>(t) * a.H, a.H, lw.g_in, c == 0);
@@ -390,7 +413,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           stage_x(a.h, nullptr, a.H, lw.g_in, false);
         }
         if (!(ok = consume(sl, a.gq, a.H))) break;
-        for (int lr = ctid; lr < sl.nloc; lr += kMkConsumers) a.qkv[sl.u0 + lr] = row_value(a.gq, lr);
+        for (int lr = tid; lr < sl.nloc; lr += kMkThreads) a.qkv[sl.u0 + lr] = row_value(a.gq, lr);
         if (!(ok = grid_sync())) break;
       }
       // ---- attention (Q/K norm, RoPE, KV append, key-parallel splits) ----
@@ -401,8 +424,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         if (c < a.n_kv * at.nsplit_max)
-          attn_decode_body<KT, GMAX, kMkConsumers>(at, c % a.n_kv, c / a.n_kv, pos, ascratch, ctid, ConsumerSync{},
-                                                   &sh.s_last);
+          attn_decode_body<KT, GMAX, kMkThreads>(at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, CtaSync{}, &s_last);
         if (!(ok = grid_sync())) break;
       }
       // ---- O projection + residual ----
@@ -410,7 +432,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         const MkSlice sl = mk_slice(a, lw, MK_O, c, G);
         stage_x(a.attn, nullptr, qw, nullptr, false);
         if (!(ok = consume(sl, a.go, qw))) break;
-        for (int lr = ctid; lr < sl.nloc; lr += kMkConsumers) {
+        for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
           const int row = sl.u0 + lr;
           a.h[row] = __ldcg(a.h + row) + row_value(a.go, lr);
         }
@@ -422,7 +444,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         stage_x(a.h, nullptr, a.H, lw.g_post, false);
         if (!(ok = consume(sl, a.gg, a.H))) break;
         const int np = sl.nloc >> 1;
-        for (int i = ctid; i < np; i += kMkConsumers) a.act[sl.u0 + i] = silu_f32(row_value(a.gg, i)) * row_value(a.gg, np + i);
+        for (int i = tid; i < np; i += kMkThreads)
+          a.act[sl.u0 + i] = silu_f32(row_value(a.gg, i)) * row_value(a.gg, np + i);
         if (!(ok = grid_sync())) break;
       }
       // ---- down projection + residual ----
@@ -430,21 +453,21 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         const MkSlice sl = mk_slice(a, lw, MK_DOWN, c, G);
         stage_x(a.act, nullptr, a.I, nullptr, false);
         if (!(ok = consume(sl, a.gd, a.I))) break;
-        for (int lr = ctid; lr < sl.nloc; lr += kMkConsumers) {
+        for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
           const int row = sl.u0 + lr;
           a.h[row] = __ldcg(a.h + row) + row_value(a.gd, lr);
         }
         if (!(ok = grid_sync())) break;
       }
     }
-    if (!ok || !head_on(step)) continue;
+    if (!ok || !mk_head_on(a, step)) continue;
     // ---- head: final RMSNorm, tied vocabulary projection, two-pass argmax ----
     const MkSlice sl = mk_slice(a, a.layers[0], MK_VOCAB, c, G);
     stage_x(a.h, nullptr, a.H, a.g_final, false);
     if (!(ok = consume(sl, a.gv, a.H))) break;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int lr = ctid; lr < sl.nloc; lr += kMkConsumers) {
+    for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
       const int row = sl.u0 + lr;
       const float v = row_value(a.gv, lr);
       if (a.logits) a.logits[row] = v;
@@ -466,9 +489,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       red[warp] = bv;
       redi[warp] = bi;
     }
-    consumer_sync();
-    if (ctid == 0) {
-      for (int w = 1; w < kMkConsumerWarps; ++w)
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kMkWarps; ++w)
         if (argmax_better(red[w], redi[w], bv, bi)) {
           bv = red[w];
           bi = redi[w];
@@ -476,8 +499,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       a.mval[c] = bv;
       a.midx[c] = bi;
       __threadfence();
-      sh.s_last = atomicAdd(a.mcnt, 1u) == static_cast<uint32_t>(G - 1);
-      if (sh.s_last) {
+      if (atomicAdd(a.mcnt, 1u) == static_cast<uint32_t>(G - 1)) {
         __threadfence();
         float gv = -INFINITY;
         int gi = 0x7fffffff;
@@ -501,23 +523,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     if (step + 1 < a.nsteps) ok = grid_sync();  // the next step reads the new token
   }
 
-  // ---- drain after an abort: wait for the copies already issued ----
-  if (vsh->abort) {
-    if (ctid == 0) {
-      const uint64_t t0 = globaltimer_ns();
-      while (!vsh->producer_done && globaltimer_ns() - t0 < WSG_WAIT_LIMIT_NS) {
-      }
-      const int issued = vsh->issued;
-      for (int s = 0; s < S && s < issued; ++s) {
-        const int last = issued - 1 - ((issued - 1 - s) % S);  // last segment issued into slot s
-        mbar_wait(&full[s], (last / S) & 1);
-      }
-    }
-    consumer_sync();
+  // ---- after an abort: wait (bounded) for this warp's copies still in flight ----
+  if (*vabort && lane == 0) {
+    for (int g = consumed; g < issued; ++g) mbar_wait(&mybars[g % R], (g / R) & 1);
   }
+  __syncthreads();
 
   // ---- exit: the last CTA out resets the barrier counters and publishes the position ----
-  if (ctid == 0) {
+  if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.bar + 1, 1u) == static_cast<uint32_t>(G - 1)) {
       a.bar[0] = 0u;

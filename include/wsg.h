@@ -174,6 +174,18 @@ dec_status dec_get_kv(const dec_ctx* ctx, int32_t layer, const void** d_k, const
 /* Current position (number of valid cache entries). -1 if ctx is NULL. */
 int32_t dec_position(const dec_ctx* ctx);
 
+/* Stage tracing of the persistent engine. dec_trace_bytes: size of the
+ * trace buffer (0 for the staged engine). dec_set_trace: with a non-NULL
+ * device buffer of at least that size, every later persistent launch writes,
+ * for its first forward, one %globaltimer stamp (nanoseconds) per
+ * [cta][layer 0..layers][stage 0..4][event 0..3] as uint64. Stages 0-4 of a
+ * layer are QKV, attention, O, gate/up, down; the extra layer index `layers`
+ * holds the head (stage 0: vocabulary GEMV, stage 1 event 0: argmax done).
+ * Events: stage entry, activation vector staged, weights consumed and
+ * epilogue written, grid barrier passed. NULL turns tracing off. */
+size_t dec_trace_bytes(const dec_ctx* ctx);
+dec_status dec_set_trace(dec_ctx* ctx, uint64_t* d_trace, size_t bytes);
+
 /* Synchronizes the context's stream and returns (and, if clear != 0,
  * clears) the device error bits DEC_DEVERR_*. */
 dec_status dec_device_errors(dec_ctx* ctx, int32_t clear, uint32_t* bits);

@@ -173,7 +173,7 @@ def test_qwen3_fp32_prefill_and_generate_one_launch(qwen_f32):
     first = dec.prefill(prompt, is_last=True)
     toks = [first] + dec.generate(first, 15).cpu().tolist()
     ora = O.OracleDecoder(s, qwen_f32, max_seq=64)
-    ref = O.generate(ora, prompt, 16, forced=toks[1:] + [0])
+    ref = O.generate(ora, prompt, 16, forced=toks)
     agree = sum(a == b for a, b in zip(toks, ref["tokens"]))
     assert agree == 16, (toks, ref["tokens"])
     for l in (0, s.layers - 1):

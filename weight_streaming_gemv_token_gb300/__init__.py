@@ -24,7 +24,9 @@ from .binding import (  # noqa: F401
     dec_position,
     dec_prefill_chunk,
     dec_reset,
+    dec_set_trace,
     dec_step,
+    dec_trace_bytes,
     dec_weights,
     dec_workspace_bytes,
     gemv,

@@ -25,7 +25,8 @@ DEC_DEVERR_WAIT_TIMEOUT, DEC_DEVERR_ARGMAX_NAN, DEC_DEVERR_BAD_TOKEN = 0x1, 0x2,
 # Every symbol include/wsg.h declares.
 EXPORTED = (
     "dec_workspace_bytes", "dec_create", "dec_load_weights", "dec_reset", "dec_step", "dec_prefill_chunk",
-    "dec_generate", "dec_get_kv", "dec_position", "dec_device_errors", "dec_destroy", "dec_last_error",
+    "dec_generate", "dec_get_kv", "dec_position", "dec_trace_bytes", "dec_set_trace", "dec_device_errors",
+    "dec_destroy", "dec_last_error",
     "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors",
 )
 
@@ -75,6 +76,8 @@ def library() -> ctypes.CDLL:
             "dec_generate": (c_int32, [c_void_p, c_int32, c_int32, c_void_p]),
             "dec_get_kv": (c_int32, [c_void_p, c_int32, P(c_void_p), P(c_void_p), P(c_int32)]),
             "dec_position": (c_int32, [c_void_p]),
+            "dec_trace_bytes": (c_size_t, [c_void_p]),
+            "dec_set_trace": (c_int32, [c_void_p, c_void_p, c_size_t]),
             "dec_device_errors": (c_int32, [c_void_p, c_int32, P(c_uint32)]),
             "dec_destroy": (None, [c_void_p]),
             "dec_last_error": (ctypes.c_char_p, [c_void_p]),
@@ -162,6 +165,14 @@ def dec_get_kv(ctx: int, layer: int) -> tuple[int, int, int]:
 
 def dec_position(ctx: int) -> int:
     return library().dec_position(ctx)
+
+
+def dec_trace_bytes(ctx: int) -> int:
+    return library().dec_trace_bytes(ctx)
+
+
+def dec_set_trace(ctx: int, d_trace, nbytes: int):
+    _check(library().dec_set_trace(ctx, _ptr(d_trace), nbytes), ctx)
 
 
 def dec_device_errors(ctx: int, clear: bool = True) -> int:

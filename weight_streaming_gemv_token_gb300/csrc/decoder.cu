@@ -159,6 +159,7 @@ struct dec_ctx {
   size_t attn_smem = 0;
   int nsplit_max = 1;
   MkArgs mk{};          // persistent-engine arguments (per-call fields filled at launch)
+  uint64_t* trace = nullptr;  // caller's stage-trace buffer (persistent engine), or NULL
   size_t mk_smem = 0;
   int mk_grid = 0;
   std::string err;
@@ -384,6 +385,8 @@ dec_status plan_persistent(dec_ctx* c) {
   part = std::max(part, 2 * cdiv(g.inter, G) * a.gg.spr);
   part = std::max(part, cdiv(g.hidden, G) * a.gd.spr);
   part = std::max(part, cdiv(g.vocab, G) * a.gv.spr);
+  if (std::max(g.hidden, std::max(qw, g.inter)) > kMkMaxWidth)
+    return fail(&c->err, DEC_EINVAL, "persistent engine: widths above %d need the staged engine", kMkMaxWidth);
   a.xs_floats = (std::max(g.hidden, std::max(qw, g.inter)) + 3) / 4 * 4;
   a.part_floats = (part + 3) / 4 * 4;
   const int attn_floats = static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 3) / 4);
@@ -447,6 +450,7 @@ dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, boo
   a.nsteps = nsteps;
   a.head_every = head_every ? 1 : 0;
   a.head_last = head_last ? 1 : 0;
+  a.trace = c->trace;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c->mk_grid);
   cfg.blockDim = dim3(kMkThreads);
@@ -722,6 +726,21 @@ extern "C" dec_status dec_get_kv(const dec_ctx* c, int32_t layer, const void** d
 }
 
 extern "C" int32_t dec_position(const dec_ctx* c) { return c ? c->pos : -1; }
+
+extern "C" size_t dec_trace_bytes(const dec_ctx* c) {
+  if (!c || c->cfg.engine != DEC_ENGINE_PERSISTENT) return 0;
+  return static_cast<size_t>(c->mk_grid) * (c->cfg.layers + 1) * kMkTraceStages * kMkTraceEvents * sizeof(uint64_t);
+}
+
+extern "C" dec_status dec_set_trace(dec_ctx* c, uint64_t* d_trace, size_t bytes) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_set_trace: NULL context");
+  if (c->cfg.engine != DEC_ENGINE_PERSISTENT)
+    return fail(&c->err, DEC_EINVAL, "dec_set_trace: tracing records the persistent engine only");
+  if (d_trace && bytes < dec_trace_bytes(c))
+    return fail(&c->err, DEC_EINVAL, "dec_set_trace: buffer has %zu bytes, %zu needed", bytes, dec_trace_bytes(c));
+  c->trace = d_trace;
+  return DEC_OK;
+}
 
 extern "C" dec_status dec_device_errors(dec_ctx* c, int32_t clear, uint32_t* bits) {
   if (!c || !bits) return fail(nullptr, DEC_EINVAL, "dec_device_errors: NULL argument");

@@ -82,25 +82,42 @@ struct MkArgs {
   int32_t xs_floats, part_floats;
   int32_t pos0, nsteps;
   int32_t head_every, head_last;  // head on every step / on the last step
+  uint64_t* trace;  // optional: [G][L + 1][5][4] globaltimer stamps of the first forward
 };
 
-enum MkStage : int { MK_QKV = 0, MK_O = 1, MK_GU = 2, MK_DOWN = 3, MK_VOCAB = 4 };
+// Trace points per stage: entry, activations staged, segments consumed, barrier passed.
+constexpr int kMkTraceStages = 5, kMkTraceEvents = 4;
 
-struct MkPiece {
-  const char* base;  // first row of the piece
-  int nrows;
-  int local0;  // index of its first row among the CTA's local rows
+enum MkStageKind : int { MK_QKV = 0, MK_O = 1, MK_GU = 2, MK_DOWN = 3, MK_VOCAB = 4 };
+
+// This CTA's share of one stage type: partition units [u0, u1) (rows, or
+// gate/up row pairs), balanced so no CTA has more than one unit above average.
+struct MkRange {
+  int u0, u1;
 };
 
-struct MkSlice {
-  MkPiece p[3];
-  int np;
-  int nloc;  // local rows
-  int u0;    // first partition unit (row, or gate/up pair)
-  int nseg;
+__device__ __forceinline__ int mk_units(const MkArgs& a, int st) {
+  return st == MK_QKV ? (a.n_q + 2 * a.n_kv) * a.d : st == MK_GU ? a.I : st == MK_VOCAB ? a.V : a.H;
+}
+
+__device__ __forceinline__ MkRange mk_range(const MkArgs& a, int st, int c, int G) {
+  const long long units = mk_units(a, st);
+  return MkRange{static_cast<int>(c * units / G), static_cast<int>((c + 1) * units / G)};
+}
+
+// One stage's weight segments for this CTA: up to three contiguous row pieces
+// (QKV spans the three source matrices; gate/up streams the gate rows, then
+// the up rows, of the same units). Held in registers: pieces are chosen by
+// comparisons, never by array indexing.
+struct MkStage {
+  const char *b0, *b1, *b2;  // first row of each piece
+  int nr0, nr1, nr2;         // rows per piece
+  int l1, l2;                // local index of the first row of pieces 1 and 2 (piece 0 starts at 0)
+  int c1, c2, n;             // segments: piece 0 [0, c1), piece 1 [c1, c2), piece 2 [c2, n)
+  int u0, nloc;
 };
 
-__device__ __forceinline__ int mk_piece_segs(const MkGeom& gm, int nrows) {
+__device__ __forceinline__ int mk_segs(const MkGeom& gm, int nrows) {
   return gm.spr > 1 ? nrows * gm.spr : (nrows + gm.rps - 1) / gm.rps;
 }
 
@@ -108,42 +125,44 @@ __device__ __forceinline__ const MkGeom& mk_geom(const MkArgs& a, int st) {
   return st == MK_QKV ? a.gq : st == MK_O ? a.go : st == MK_GU ? a.gg : st == MK_DOWN ? a.gd : a.gv;
 }
 
-// This CTA's rows of one stage: balanced contiguous units, cut at source boundaries.
-__device__ __forceinline__ MkSlice mk_slice(const MkArgs& a, const MkLayer& lw, int st, int c, int G) {
-  MkSlice s;
-  s.np = 0;
+__device__ __forceinline__ MkStage mk_stage(const MkArgs& a, const MkLayer& lw, int st, MkRange r) {
   const MkGeom& gm = mk_geom(a, st);
-  const int qw = a.n_q * a.d, kvw = a.n_kv * a.d;
-  int units = st == MK_QKV ? qw + 2 * kvw : st == MK_GU ? a.I : st == MK_VOCAB ? a.V : a.H;
-  const int u0 = static_cast<int>(static_cast<int64_t>(c) * units / G);
-  const int u1 = static_cast<int>(static_cast<int64_t>(c + 1) * units / G);
-  s.u0 = u0;
-  auto add = [&](const void* base, int first_row, int nrows, int local0) {
-    if (nrows <= 0) return;
-    s.p[s.np].base = static_cast<const char*>(base) + static_cast<size_t>(first_row) * gm.row_bytes;
-    s.p[s.np].nrows = nrows;
-    s.p[s.np].local0 = local0;
-    ++s.np;
-  };
+  const size_t rb = static_cast<size_t>(gm.row_bytes);
+  MkStage s;
+  s.u0 = r.u0;
+  s.b1 = s.b2 = nullptr;
+  s.nr1 = s.nr2 = 0;
+  s.l1 = s.l2 = 0;
   if (st == MK_QKV) {
-    const int lo[3] = {0, qw, qw + kvw}, hi[3] = {qw, qw + kvw, qw + 2 * kvw};
-    const void* b[3] = {lw.wq, lw.wk, lw.wv};
-    for (int k = 0; k < 3; ++k) {
-      const int x0 = max(u0, lo[k]), x1 = min(u1, hi[k]);
-      add(b[k], x0 - lo[k], x1 - x0, x0 - u0);
-    }
-    s.nloc = u1 - u0;
+    const int qw = a.n_q * a.d, kvw = a.n_kv * a.d;
+    const int q0 = min(r.u0, qw), q1 = min(r.u1, qw);
+    const int k0 = min(max(r.u0, qw), qw + kvw), k1 = min(max(r.u1, qw), qw + kvw);
+    const int v0 = max(r.u0, qw + kvw), v1 = max(r.u1, qw + kvw);
+    s.b0 = static_cast<const char*>(lw.wq) + q0 * rb;
+    s.nr0 = q1 - q0;
+    s.b1 = static_cast<const char*>(lw.wk) + (k0 - qw) * rb;
+    s.nr1 = k1 - k0;
+    s.l1 = k0 - r.u0;
+    s.b2 = static_cast<const char*>(lw.wv) + (v0 - qw - kvw) * rb;
+    s.nr2 = v1 - v0;
+    s.l2 = v0 - r.u0;
+    s.nloc = r.u1 - r.u0;
   } else if (st == MK_GU) {
-    add(lw.wg, u0, u1 - u0, 0);
-    add(lw.wu, u0, u1 - u0, u1 - u0);
-    s.nloc = 2 * (u1 - u0);
+    s.b0 = static_cast<const char*>(lw.wg) + r.u0 * rb;
+    s.nr0 = r.u1 - r.u0;
+    s.b1 = static_cast<const char*>(lw.wu) + r.u0 * rb;
+    s.nr1 = r.u1 - r.u0;
+    s.l1 = r.u1 - r.u0;
+    s.nloc = 2 * (r.u1 - r.u0);
   } else {
     const void* b = st == MK_O ? lw.wo : st == MK_DOWN ? lw.wd : a.embed;
-    add(b, u0, u1 - u0, 0);
-    s.nloc = u1 - u0;
+    s.b0 = static_cast<const char*>(b) + r.u0 * rb;
+    s.nr0 = r.u1 - r.u0;
+    s.nloc = r.u1 - r.u0;
   }
-  s.nseg = 0;
-  for (int k = 0; k < s.np; ++k) s.nseg += mk_piece_segs(gm, s.p[k].nrows);
+  s.c1 = mk_segs(gm, s.nr0);
+  s.c2 = s.c1 + mk_segs(gm, s.nr1);
+  s.n = s.c2 + mk_segs(gm, s.nr2);
   return s;
 }
 
@@ -156,34 +175,57 @@ struct MkSeg {
   int off;   // byte offset within the row
 };
 
-__device__ __forceinline__ MkSeg mk_seg(const MkSlice& s, const MkGeom& gm, int j) {
-  int k = 0;
-  while (k + 1 < s.np) {
-    const int n = mk_piece_segs(gm, s.p[k].nrows);
-    if (j < n) break;
-    j -= n;
-    ++k;
-  }
-  const MkPiece& p = s.p[k];
+__device__ __forceinline__ MkSeg mk_seg(const MkStage& s, const MkGeom& gm, int j) {
+  const bool p0 = j < s.c1, p1 = !p0 && j < s.c2;
+  const int jj = j - (p0 ? 0 : p1 ? s.c1 : s.c2);
+  const char* base = p0 ? s.b0 : p1 ? s.b1 : s.b2;
+  const int lbase = p0 ? 0 : p1 ? s.l1 : s.l2;
   MkSeg r;
   if (gm.spr > 1) {
-    const int row = j / gm.spr, part = j - row * gm.spr;
+    const int row = jj / gm.spr, part = jj - row * gm.spr;
     r.off = part * gm.seg_bytes;
     r.bytes = min(gm.seg_bytes, gm.row_bytes - r.off);
-    r.src = p.base + static_cast<size_t>(row) * gm.row_bytes + r.off;
-    r.lrow = p.local0 + row;
+    r.src = base + static_cast<size_t>(row) * gm.row_bytes + r.off;
+    r.lrow = lbase + row;
     r.part = part;
     r.nr = 1;
   } else {
-    const int row = j * gm.rps;
-    r.nr = min(gm.rps, p.nrows - row);
+    const int nrows = p0 ? s.nr0 : p1 ? s.nr1 : s.nr2;
+    const int row = jj * gm.rps;
+    r.nr = min(gm.rps, nrows - row);
     r.off = 0;
     r.bytes = r.nr * gm.row_bytes;
-    r.src = p.base + static_cast<size_t>(row) * gm.row_bytes;
-    r.lrow = p.local0 + row;
+    r.src = base + static_cast<size_t>(row) * gm.row_bytes;
+    r.lrow = lbase + row;
     r.part = 0;
   }
   return r;
+}
+
+template <typename T>
+__device__ __forceinline__ T* ldg_ptr(T* const* p) {
+  return reinterpret_cast<T*>(__ldg(reinterpret_cast<const unsigned long long*>(p)));
+}
+
+__device__ __forceinline__ MkLayer mk_layer(const MkArgs& a, int l) {
+  const MkLayer* p = a.layers + l;
+  MkLayer w;
+  w.wq = ldg_ptr(&p->wq);
+  w.wk = ldg_ptr(&p->wk);
+  w.wv = ldg_ptr(&p->wv);
+  w.wo = ldg_ptr(&p->wo);
+  w.wg = ldg_ptr(&p->wg);
+  w.wu = ldg_ptr(&p->wu);
+  w.wd = ldg_ptr(&p->wd);
+  w.g_in = ldg_ptr(&p->g_in);
+  w.g_post = ldg_ptr(&p->g_post);
+  w.g_q = ldg_ptr(&p->g_q);
+  w.g_k = ldg_ptr(&p->g_k);
+  return w;
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
@@ -196,69 +238,8 @@ __device__ __forceinline__ bool mk_head_on(const MkArgs& a, int step) {
   return a.head_every || (a.head_last && step == a.nsteps - 1);
 }
 
-// Walks one warp's segments in consumption order: steps, layers, stages
-// (QKV, O, gate/up, down, then the vocabulary on head steps), segment j of a
-// stage for j = warp, warp + 8, ...
-struct MkCursor {
-  int step, layer, stage, j;
-  bool done;
-  MkSlice sl;
-};
-
-__device__ __forceinline__ void mk_cursor_settle(MkCursor& k, const MkArgs& a, int c, int G, int warp) {
-  while (true) {
-    if (k.step >= a.nsteps) {
-      k.done = true;
-      return;
-    }
-    k.sl = mk_slice(a, a.layers[k.stage == MK_VOCAB ? 0 : k.layer], k.stage, c, G);
-    k.j = warp;
-    if (k.j < k.sl.nseg) return;
-    // next stage
-    if (k.stage == MK_VOCAB) {
-      ++k.step;
-      k.layer = 0;
-      k.stage = MK_QKV;
-    } else if (k.stage == MK_DOWN) {
-      if (k.layer + 1 < a.L) {
-        ++k.layer;
-        k.stage = MK_QKV;
-      } else if (mk_head_on(a, k.step)) {
-        k.stage = MK_VOCAB;
-      } else {
-        ++k.step;
-        k.layer = 0;
-        k.stage = MK_QKV;
-      }
-    } else {
-      ++k.stage;
-    }
-  }
-}
-
-__device__ __forceinline__ void mk_cursor_next(MkCursor& k, const MkArgs& a, int c, int G, int warp) {
-  k.j += kMkWarps;
-  if (k.j < k.sl.nseg) return;
-  if (k.stage == MK_VOCAB) {
-    ++k.step;
-    k.layer = 0;
-    k.stage = MK_QKV;
-  } else if (k.stage == MK_DOWN) {
-    if (k.layer + 1 < a.L) {
-      ++k.layer;
-      k.stage = MK_QKV;
-    } else if (mk_head_on(a, k.step)) {
-      k.stage = MK_VOCAB;
-    } else {
-      ++k.step;
-      k.layer = 0;
-      k.stage = MK_QKV;
-    }
-  } else {
-    ++k.stage;
-  }
-  mk_cursor_settle(k, a, c, G, warp);
-}
+// Widest activation vector the staging code holds in registers (16 per thread).
+constexpr int kMkMaxWidth = 16 * kMkThreads;
 
 template <typename WT, typename KT, int GMAX>
 __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs a) {
@@ -277,19 +258,57 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   float* ascratch = xs;  // the attention stage reuses the GEMV staging area
   volatile int* vabort = &s_abort;
 
-  // ---- each warp primes its ring ----
-  MkCursor cur;
+  // ---- issue cursor (lane 0 of each warp): this warp's segments in
+  //      consumption order, steps -> layers -> QKV, O, gate/up, down -> head ----
+  int cstep = 0, clayer = 0, cst = MK_QKV, cj = 0;
+  bool cdone = false;
+  MkStage cs{};
   int issued = 0;    // lane 0: segments issued into this warp's ring
   int consumed = 0;  // all lanes: segments consumed
   const uint64_t pol = l2_policy_evict_first();
+  auto cursor_advance = [&]() {
+    if (cst == MK_VOCAB) {
+      ++cstep;
+      clayer = 0;
+      cst = MK_QKV;
+    } else if (cst == MK_DOWN) {
+      if (clayer + 1 < a.L) {
+        ++clayer;
+        cst = MK_QKV;
+      } else if (mk_head_on(a, cstep)) {
+        cst = MK_VOCAB;
+      } else {
+        ++cstep;
+        clayer = 0;
+        cst = MK_QKV;
+      }
+    } else {
+      ++cst;
+    }
+  };
+  auto cursor_settle = [&]() {  // first stage, from the current one, that has a segment for this warp
+    while (true) {
+      if (cstep >= a.nsteps) {
+        cdone = true;
+        return;
+      }
+      cs = mk_stage(a, mk_layer(a, cst == MK_VOCAB ? 0 : clayer), cst, mk_range(a, cst, c, G));
+      cj = warp;
+      if (cj < cs.n) return;
+      cursor_advance();
+    }
+  };
   auto issue_one = [&]() {  // lane 0 only; requires issued < consumed + R
-    const MkGeom& gm = mk_geom(a, cur.stage);
-    const MkSeg sg = mk_seg(cur.sl, gm, cur.j);
+    const MkSeg sg = mk_seg(cs, mk_geom(a, cst), cj);
     const int slot = issued % R;
     mbar_arrive_expect_tx(&mybars[slot], static_cast<uint32_t>(sg.bytes));
     bulk_g2s(myring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes), &mybars[slot], pol);
     ++issued;
-    mk_cursor_next(cur, a, c, G, warp);
+    cj += kMkWarps;
+    if (cj >= cs.n) {
+      cursor_advance();
+      cursor_settle();
+    }
   };
   if (tid == 0) {
     s_abort = 0;
@@ -298,12 +317,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   if (lane == 0) {
     for (int s = 0; s < R; ++s) mbar_init(&mybars[s], 1);
     fence_mbar_init();
-    cur.step = 0;
-    cur.layer = 0;
-    cur.stage = MK_QKV;
-    cur.done = false;
-    mk_cursor_settle(cur, a, c, G, warp);
-    while (!cur.done && issued < R) issue_one();
+    cursor_settle();
+    while (!cdone && issued < R) issue_one();
   }
   __syncthreads();
 
@@ -329,15 +344,25 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     return !*vabort;
   };
 
-  // Stage the activation vector: plain copy, or RMSNorm(src) * gain.
+  // Stage the activation vector: plain copy, or RMSNorm(src) * gain. Values
+  // and gains are loaded together (one memory round trip) into registers.
   auto stage_x = [&](const float* src, const WT* wsrc, int in, const float* gain, bool store_h) {
+    constexpr int K = kMkMaxWidth / kMkThreads;
+    float v[K], gn[K];
     float ss = 0.f;
-    for (int i = tid; i < in; i += kMkThreads) {
-      const float v = wsrc ? load_f32<WT>(wsrc, i) : __ldcg(src + i);
-      if (store_h) a.h[i] = v;
-      xs[xs_index<WT>(i, in)] = v;
-      ss = fmaf(v, v, ss);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = tid + k * kMkThreads;
+      v[k] = 0.f;
+      gn[k] = 1.f;
+      if (i < in) {
+        v[k] = wsrc ? load_f32<WT>(wsrc, i) : __ldcg(src + i);
+        if (gain) gn[k] = __ldg(gain + i);
+      }
     }
+#pragma unroll
+    for (int k = 0; k < K; ++k) ss = fmaf(v[k], v[k], ss);
+    float inv = 1.f;
     if (gain) {
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
@@ -345,18 +370,22 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       float t = 0.f;
 #pragma unroll
       for (int w = 0; w < kMkWarps; ++w) t += red[w];
-      const float inv = 1.0f / sqrtf(t / static_cast<float>(in) + a.eps);
-      for (int i = tid; i < in; i += kMkThreads) {
-        const int k = xs_index<WT>(i, in);
-        xs[k] = xs[k] * inv * gain[i];
+      inv = 1.0f / sqrtf(t / static_cast<float>(in) + a.eps);
+    }
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = tid + k * kMkThreads;
+      if (i < in) {
+        if (store_h) a.h[i] = v[k];
+        xs[xs_index<WT>(i, in)] = gain ? v[k] * inv * gn[k] : v[k];
       }
     }
     __syncthreads();
   };
 
   // This warp's segments of one stage, in ring order, into part[].
-  auto consume = [&](const MkSlice& sl, const MkGeom& gm, int in) -> bool {
-    for (int j = warp; j < sl.nseg; j += kMkWarps) {
+  auto consume = [&](const MkStage& sl, const MkGeom& gm, int in) -> bool {
+    for (int j = warp; j < sl.n; j += kMkWarps) {
       const int slot = consumed % R;
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&mybars[slot], (consumed / R) & 1));
       if (!ok) {
@@ -379,7 +408,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       }
       __syncwarp();
       ++consumed;
-      if (lane == 0 && !cur.done && !*vabort) {
+      if (lane == 0 && !cdone && !*vabort) {
         fence_proxy_async_smem();
         issue_one();
       }
@@ -394,14 +423,21 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     return v;
   };
 
+  auto stamp = [&](int step, int l, int st, int ev) {
+    if (a.trace && step == 0 && tid == 0)
+      a.trace[((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + st) * kMkTraceEvents + ev] =
+          globaltimer_ns();
+  };
+
   bool ok = true;
   for (int step = 0; step < a.nsteps && ok; ++step) {
     const int pos = a.pos0 + step;
     for (int l = 0; l < a.L && ok; ++l) {
-      const MkLayer lw = a.layers[l];
+      const MkLayer lw = mk_layer(a, l);
       // ---- QKV with the input RMSNorm (layer 0: of the token's embedding row) ----
       {
-        const MkSlice sl = mk_slice(a, lw, MK_QKV, c, G);
+        stamp(step, l, 0, 0);
+        const MkStage sl = mk_stage(a, lw, MK_QKV, mk_range(a, MK_QKV, c, G));
         if (l == 0) {
           int t = __ldcg(a.tok + pos);
           if (t < 0 || t >= a.V) {
@@ -412,9 +448,12 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         } else {
           stage_x(a.h, nullptr, a.H, lw.g_in, false);
         }
+        stamp(step, l, 0, 1);
         if (!(ok = consume(sl, a.gq, a.H))) break;
         for (int lr = tid; lr < sl.nloc; lr += kMkThreads) a.qkv[sl.u0 + lr] = row_value(a.gq, lr);
+        stamp(step, l, 0, 2);
         if (!(ok = grid_sync())) break;
+        stamp(step, l, 0, 3);
       }
       // ---- attention (Q/K norm, RoPE, KV append, key-parallel splits) ----
       {
@@ -423,48 +462,66 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         at.g_k = lw.g_k;
         at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
+        stamp(step, l, 1, 0);
         if (c < a.n_kv * at.nsplit_max)
           attn_decode_body<KT, GMAX, kMkThreads>(at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, CtaSync{}, &s_last);
+        stamp(step, l, 1, 2);
         if (!(ok = grid_sync())) break;
+        stamp(step, l, 1, 3);
       }
       // ---- O projection + residual ----
       {
-        const MkSlice sl = mk_slice(a, lw, MK_O, c, G);
+        stamp(step, l, 2, 0);
+        const MkStage sl = mk_stage(a, lw, MK_O, mk_range(a, MK_O, c, G));
         stage_x(a.attn, nullptr, qw, nullptr, false);
+        stamp(step, l, 2, 1);
         if (!(ok = consume(sl, a.go, qw))) break;
         for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
           const int row = sl.u0 + lr;
           a.h[row] = __ldcg(a.h + row) + row_value(a.go, lr);
         }
+        stamp(step, l, 2, 2);
         if (!(ok = grid_sync())) break;
+        stamp(step, l, 2, 3);
       }
       // ---- gate/up with the post-attention RMSNorm, SwiGLU ----
       {
-        const MkSlice sl = mk_slice(a, lw, MK_GU, c, G);
+        stamp(step, l, 3, 0);
+        const MkStage sl = mk_stage(a, lw, MK_GU, mk_range(a, MK_GU, c, G));
         stage_x(a.h, nullptr, a.H, lw.g_post, false);
+        stamp(step, l, 3, 1);
         if (!(ok = consume(sl, a.gg, a.H))) break;
         const int np = sl.nloc >> 1;
         for (int i = tid; i < np; i += kMkThreads)
           a.act[sl.u0 + i] = silu_f32(row_value(a.gg, i)) * row_value(a.gg, np + i);
+        stamp(step, l, 3, 2);
         if (!(ok = grid_sync())) break;
+        stamp(step, l, 3, 3);
       }
       // ---- down projection + residual ----
       {
-        const MkSlice sl = mk_slice(a, lw, MK_DOWN, c, G);
+        stamp(step, l, 4, 0);
+        const MkStage sl = mk_stage(a, lw, MK_DOWN, mk_range(a, MK_DOWN, c, G));
         stage_x(a.act, nullptr, a.I, nullptr, false);
+        stamp(step, l, 4, 1);
         if (!(ok = consume(sl, a.gd, a.I))) break;
         for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
           const int row = sl.u0 + lr;
           a.h[row] = __ldcg(a.h + row) + row_value(a.gd, lr);
         }
+        stamp(step, l, 4, 2);
         if (!(ok = grid_sync())) break;
+        stamp(step, l, 4, 3);
       }
     }
     if (!ok || !mk_head_on(a, step)) continue;
     // ---- head: final RMSNorm, tied vocabulary projection, two-pass argmax ----
-    const MkSlice sl = mk_slice(a, a.layers[0], MK_VOCAB, c, G);
+    stamp(step, a.L, 0, 0);
+    const MkStage sl = mk_stage(a, mk_layer(a, 0), MK_VOCAB, mk_range(a, MK_VOCAB, c, G));
     stage_x(a.h, nullptr, a.H, a.g_final, false);
+    stamp(step, a.L, 0, 1);
     if (!(ok = consume(sl, a.gv, a.H))) break;
+    stamp(step, a.L, 0, 2);
     float bv = -INFINITY;
     int bi = 0x7fffffff;
     for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
@@ -520,6 +577,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         __threadfence();
       }
     }
+    stamp(step, a.L, 1, 0);
     if (step + 1 < a.nsteps) ok = grid_sync();  // the next step reads the new token
   }
 

@@ -182,7 +182,10 @@ int32_t dec_position(const dec_ctx* ctx);
  * layer are QKV, attention, O, gate/up, down; the extra layer index `layers`
  * holds the head (stage 0: vocabulary GEMV, stage 1 event 0: argmax done).
  * Events: stage entry, activation vector staged, weights consumed and
- * epilogue written, grid barrier passed. NULL turns tracing off. */
+ * epilogue written, grid barrier passed. After that block, [512][4] uint64
+ * SM clock stamps (clock64) of the first 512 weight segments consumed by
+ * warp 0 of CTA 0: wait begins, data ready, dot reduced, next copy issued.
+ * NULL turns tracing off. */
 size_t dec_trace_bytes(const dec_ctx* ctx);
 dec_status dec_set_trace(dec_ctx* ctx, uint64_t* d_trace, size_t bytes);
 

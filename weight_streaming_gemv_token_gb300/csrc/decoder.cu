@@ -391,8 +391,9 @@ dec_status plan_persistent(dec_ctx* c) {
   a.part_floats = (part + 3) / 4 * 4;
   const int attn_floats = static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 3) / 4);
   if (a.xs_floats + a.part_floats < attn_floats) a.part_floats = (attn_floats - a.xs_floats + 3) / 4 * 4;
-  const size_t fixed = kMkWarps * kMkWarpSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats);
-  const size_t static_smem = 64 * 4 + 32 * 4 + 8 + 256;
+  const size_t fixed = kMkWarps * kMkWarpSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats) +
+                       static_cast<size_t>(g.layers) * kMkLayerPtrs * sizeof(void*);
+  const size_t static_smem = 64 * 4 + 32 * 4 + 8 + 5 * sizeof(MkStageT) + 256;
   const size_t per_slot = static_cast<size_t>(kMkWarps) * kMkSlot;  // one slot in every warp's ring
   if (fixed + static_smem + per_slot > c->di.smem_optin)
     return fail(&c->err, DEC_EINVAL, "persistent engine: staging needs %zu B of shared memory", fixed);
@@ -729,7 +730,9 @@ extern "C" int32_t dec_position(const dec_ctx* c) { return c ? c->pos : -1; }
 
 extern "C" size_t dec_trace_bytes(const dec_ctx* c) {
   if (!c || c->cfg.engine != DEC_ENGINE_PERSISTENT) return 0;
-  return static_cast<size_t>(c->mk_grid) * (c->cfg.layers + 1) * kMkTraceStages * kMkTraceEvents * sizeof(uint64_t);
+  return (static_cast<size_t>(c->mk_grid) * (c->cfg.layers + 1) * kMkTraceStages * kMkTraceEvents +
+          static_cast<size_t>(kMkTraceSegs) * kMkTraceSegEvents) *
+         sizeof(uint64_t);
 }
 
 extern "C" dec_status dec_set_trace(dec_ctx* c, uint64_t* d_trace, size_t bytes) {

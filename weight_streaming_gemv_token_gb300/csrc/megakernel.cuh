@@ -39,7 +39,8 @@ namespace wsg {
 
 constexpr int kMkWarps = 8;
 constexpr int kMkThreads = kMkWarps * 32;
-constexpr int kMkSlot = 4096;         // bytes per ring slot
+constexpr int kMkSlot = 8192;         // bytes per ring slot
+constexpr int kMkLayerPtrs = 12;      // pointers per layer in the shared layer table
 constexpr int kMkWarpSlotsMax = 8;    // ring slots per warp, upper bound
 
 enum : uint32_t { ERR_GRID_BARRIER_TIMEOUT = 1u << 4 };
@@ -87,6 +88,9 @@ struct MkArgs {
 
 // Trace points per stage: entry, activations staged, segments consumed, barrier passed.
 constexpr int kMkTraceStages = 5, kMkTraceEvents = 4;
+// Per-segment trace of warp 0 of CTA 0 (first kMkTraceSegs segments of the first
+// forward), after the stage trace: wait begins, data ready, dot reduced, next copy issued.
+constexpr int kMkTraceSegs = 512, kMkTraceSegEvents = 4;
 
 enum MkStageKind : int { MK_QKV = 0, MK_O = 1, MK_GU = 2, MK_DOWN = 3, MK_VOCAB = 4 };
 
@@ -125,12 +129,21 @@ __device__ __forceinline__ const MkGeom& mk_geom(const MkArgs& a, int st) {
   return st == MK_QKV ? a.gq : st == MK_O ? a.go : st == MK_GU ? a.gg : st == MK_DOWN ? a.gd : a.gv;
 }
 
-__device__ __forceinline__ MkStage mk_stage(const MkArgs& a, const MkLayer& lw, int st, MkRange r) {
+// Stage geometry of this CTA with tensors named by index into a layer's
+// pointer table (0 wq, 1 wk, 2 wv, 3 wo, 4 wg, 5 wu, 6 wd; 7: the embedding),
+// so it is computed once per launch and combined with any layer's pointers.
+struct MkStageT {
+  int t0, t1, t2;        // tensor of each piece
+  int row0, row1, row2;  // first row of each piece within its tensor
+  int nr0, nr1, nr2, l1, l2, c1, c2, n, u0, nloc;
+};
+
+__device__ __forceinline__ MkStageT mk_stage_t(const MkArgs& a, int st, MkRange r) {
   const MkGeom& gm = mk_geom(a, st);
-  const size_t rb = static_cast<size_t>(gm.row_bytes);
-  MkStage s;
+  MkStageT s;
   s.u0 = r.u0;
-  s.b1 = s.b2 = nullptr;
+  s.t1 = s.t2 = 0;
+  s.row1 = s.row2 = 0;
   s.nr1 = s.nr2 = 0;
   s.l1 = s.l2 = 0;
   if (st == MK_QKV) {
@@ -138,31 +151,39 @@ __device__ __forceinline__ MkStage mk_stage(const MkArgs& a, const MkLayer& lw, 
     const int q0 = min(r.u0, qw), q1 = min(r.u1, qw);
     const int k0 = min(max(r.u0, qw), qw + kvw), k1 = min(max(r.u1, qw), qw + kvw);
     const int v0 = max(r.u0, qw + kvw), v1 = max(r.u1, qw + kvw);
-    s.b0 = static_cast<const char*>(lw.wq) + q0 * rb;
-    s.nr0 = q1 - q0;
-    s.b1 = static_cast<const char*>(lw.wk) + (k0 - qw) * rb;
-    s.nr1 = k1 - k0;
-    s.l1 = k0 - r.u0;
-    s.b2 = static_cast<const char*>(lw.wv) + (v0 - qw - kvw) * rb;
-    s.nr2 = v1 - v0;
-    s.l2 = v0 - r.u0;
+    s.t0 = 0, s.row0 = q0, s.nr0 = q1 - q0;
+    s.t1 = 1, s.row1 = k0 - qw, s.nr1 = k1 - k0, s.l1 = k0 - r.u0;
+    s.t2 = 2, s.row2 = v0 - qw - kvw, s.nr2 = v1 - v0, s.l2 = v0 - r.u0;
     s.nloc = r.u1 - r.u0;
   } else if (st == MK_GU) {
-    s.b0 = static_cast<const char*>(lw.wg) + r.u0 * rb;
-    s.nr0 = r.u1 - r.u0;
-    s.b1 = static_cast<const char*>(lw.wu) + r.u0 * rb;
-    s.nr1 = r.u1 - r.u0;
-    s.l1 = r.u1 - r.u0;
+    s.t0 = 4, s.row0 = r.u0, s.nr0 = r.u1 - r.u0;
+    s.t1 = 5, s.row1 = r.u0, s.nr1 = r.u1 - r.u0, s.l1 = r.u1 - r.u0;
     s.nloc = 2 * (r.u1 - r.u0);
   } else {
-    const void* b = st == MK_O ? lw.wo : st == MK_DOWN ? lw.wd : a.embed;
-    s.b0 = static_cast<const char*>(b) + r.u0 * rb;
+    s.t0 = st == MK_O ? 3 : st == MK_DOWN ? 6 : 7;
+    s.row0 = r.u0;
     s.nr0 = r.u1 - r.u0;
     s.nloc = r.u1 - r.u0;
   }
   s.c1 = mk_segs(gm, s.nr0);
   s.c2 = s.c1 + mk_segs(gm, s.nr1);
   s.n = s.c2 + mk_segs(gm, s.nr2);
+  return s;
+}
+
+// Bind a stage template to one layer's tensors (lp: that layer's pointer table).
+__device__ __forceinline__ MkStage mk_bind(const MkStageT& t, const MkGeom& gm, const void* const* lp,
+                                          const void* embed) {
+  auto ptr = [&](int id) { return static_cast<const char*>(id == 7 ? embed : lp[id]); };
+  const size_t rb = static_cast<size_t>(gm.row_bytes);
+  MkStage s;
+  s.b0 = ptr(t.t0) + t.row0 * rb;
+  s.b1 = ptr(t.t1) + t.row1 * rb;
+  s.b2 = ptr(t.t2) + t.row2 * rb;
+  s.nr0 = t.nr0, s.nr1 = t.nr1, s.nr2 = t.nr2;
+  s.l1 = t.l1, s.l2 = t.l2;
+  s.c1 = t.c1, s.c2 = t.c2, s.n = t.n;
+  s.u0 = t.u0, s.nloc = t.nloc;
   return s;
 }
 
@@ -202,28 +223,6 @@ __device__ __forceinline__ MkSeg mk_seg(const MkStage& s, const MkGeom& gm, int 
   return r;
 }
 
-template <typename T>
-__device__ __forceinline__ T* ldg_ptr(T* const* p) {
-  return reinterpret_cast<T*>(__ldg(reinterpret_cast<const unsigned long long*>(p)));
-}
-
-__device__ __forceinline__ MkLayer mk_layer(const MkArgs& a, int l) {
-  const MkLayer* p = a.layers + l;
-  MkLayer w;
-  w.wq = ldg_ptr(&p->wq);
-  w.wk = ldg_ptr(&p->wk);
-  w.wv = ldg_ptr(&p->wv);
-  w.wo = ldg_ptr(&p->wo);
-  w.wg = ldg_ptr(&p->wg);
-  w.wu = ldg_ptr(&p->wu);
-  w.wd = ldg_ptr(&p->wd);
-  w.g_in = ldg_ptr(&p->g_in);
-  w.g_post = ldg_ptr(&p->g_post);
-  w.g_q = ldg_ptr(&p->g_q);
-  w.g_k = ldg_ptr(&p->g_k);
-  return w;
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -247,6 +246,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   __shared__ float red[64];
   __shared__ int redi[32];
   __shared__ int s_abort, s_last;
+  __shared__ MkStageT s_stage[5];
   const int R = a.wslots;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
@@ -256,7 +256,33 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   float* xs = reinterpret_cast<float*>(bars + kMkWarps * kMkWarpSlotsMax);
   float* part = xs + a.xs_floats;
   float* ascratch = xs;  // the attention stage reuses the GEMV staging area
+  const void** lptr = reinterpret_cast<const void**>(part + a.part_floats);  // [L][kMkLayerPtrs]
   volatile int* vabort = &s_abort;
+
+  // Per-launch tables: every layer's tensor pointers, this CTA's stage geometry.
+  for (int i = tid; i < a.L * kMkLayerPtrs; i += kMkThreads) {
+    const int l = i / kMkLayerPtrs, k = i - l * kMkLayerPtrs;
+    const MkLayer* p = a.layers + l;
+    const void* v = nullptr;
+    switch (k) {
+      case 0: v = p->wq; break;
+      case 1: v = p->wk; break;
+      case 2: v = p->wv; break;
+      case 3: v = p->wo; break;
+      case 4: v = p->wg; break;
+      case 5: v = p->wu; break;
+      case 6: v = p->wd; break;
+      case 7: v = p->g_in; break;
+      case 8: v = p->g_post; break;
+      case 9: v = p->g_q; break;
+      case 10: v = p->g_k; break;
+      default: break;
+    }
+    lptr[i] = v;
+  }
+  if (tid < 5) s_stage[tid] = mk_stage_t(a, tid, mk_range(a, tid, c, G));
+  __syncthreads();
+  auto layer_ptrs = [&](int l) { return lptr + l * kMkLayerPtrs; };
 
   // ---- issue cursor (lane 0 of each warp): this warp's segments in
   //      consumption order, steps -> layers -> QKV, O, gate/up, down -> head ----
@@ -292,7 +318,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         cdone = true;
         return;
       }
-      cs = mk_stage(a, mk_layer(a, cst == MK_VOCAB ? 0 : clayer), cst, mk_range(a, cst, c, G));
+      cs = mk_bind(s_stage[cst], mk_geom(a, cst), layer_ptrs(cst == MK_VOCAB ? 0 : clayer), a.embed);
       cj = warp;
       if (cj < cs.n) return;
       cursor_advance();
@@ -384,10 +410,18 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   };
 
   // This warp's segments of one stage, in ring order, into part[].
+  uint64_t* segtrace = nullptr;
+  if (a.trace && c == 0 && warp == 0)
+    segtrace = a.trace + static_cast<size_t>(G) * (a.L + 1) * kMkTraceStages * kMkTraceEvents;
+  auto segstamp = [&](int ev) {
+    if (segtrace && lane == 0 && consumed < kMkTraceSegs) segtrace[consumed * kMkTraceSegEvents + ev] = clock64();
+  };
   auto consume = [&](const MkStage& sl, const MkGeom& gm, int in) -> bool {
     for (int j = warp; j < sl.n; j += kMkWarps) {
       const int slot = consumed % R;
+      segstamp(0);
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&mybars[slot], (consumed / R) & 1));
+      segstamp(1);
       if (!ok) {
         if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
         *vabort = 1;
@@ -400,18 +434,30 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         v = warp_sum(v);
         if (lane == 0) part[sg.lrow * gm.spr + sg.part] = v;
       } else {
-        for (int r = 0; r < sg.nr; ++r) {
-          float v = seg_dot<WT>(buf + static_cast<size_t>(r) * gm.row_bytes, xs, 0, gm.row_bytes, in, lane);
-          v = warp_sum(v);
-          if (lane == 0) part[sg.lrow + r] = v;
+        // several whole rows: all lane partials first, then one interleaved reduction
+        float v[4];
+        for (int r0 = 0; r0 < sg.nr; r0 += 4) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+            v[r] = (r0 + r < sg.nr)
+                       ? seg_dot<WT>(buf + static_cast<size_t>(r0 + r) * gm.row_bytes, xs, 0, gm.row_bytes, in, lane)
+                       : 0.f;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
+          if (lane == 0)
+            for (int r = 0; r < 4 && r0 + r < sg.nr; ++r) part[sg.lrow + r0 + r] = v[r];
         }
       }
       __syncwarp();
-      ++consumed;
+      segstamp(2);
       if (lane == 0 && !cdone && !*vabort) {
         fence_proxy_async_smem();
         issue_one();
       }
+      segstamp(3);
+      ++consumed;
     }
     __syncthreads();
     return !*vabort;
@@ -433,11 +479,16 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   for (int step = 0; step < a.nsteps && ok; ++step) {
     const int pos = a.pos0 + step;
     for (int l = 0; l < a.L && ok; ++l) {
-      const MkLayer lw = mk_layer(a, l);
+      const void* const* lp = layer_ptrs(l);
+      MkLayer lw;
+      lw.g_in = static_cast<const float*>(lp[7]);
+      lw.g_post = static_cast<const float*>(lp[8]);
+      lw.g_q = static_cast<const float*>(lp[9]);
+      lw.g_k = static_cast<const float*>(lp[10]);
       // ---- QKV with the input RMSNorm (layer 0: of the token's embedding row) ----
       {
         stamp(step, l, 0, 0);
-        const MkStage sl = mk_stage(a, lw, MK_QKV, mk_range(a, MK_QKV, c, G));
+        const MkStage sl = mk_bind(s_stage[MK_QKV], a.gq, lp, a.embed);
         if (l == 0) {
           int t = __ldcg(a.tok + pos);
           if (t < 0 || t >= a.V) {
@@ -472,7 +523,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       // ---- O projection + residual ----
       {
         stamp(step, l, 2, 0);
-        const MkStage sl = mk_stage(a, lw, MK_O, mk_range(a, MK_O, c, G));
+        const MkStage sl = mk_bind(s_stage[MK_O], a.go, lp, a.embed);
         stage_x(a.attn, nullptr, qw, nullptr, false);
         stamp(step, l, 2, 1);
         if (!(ok = consume(sl, a.go, qw))) break;
@@ -487,7 +538,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       // ---- gate/up with the post-attention RMSNorm, SwiGLU ----
       {
         stamp(step, l, 3, 0);
-        const MkStage sl = mk_stage(a, lw, MK_GU, mk_range(a, MK_GU, c, G));
+        const MkStage sl = mk_bind(s_stage[MK_GU], a.gg, lp, a.embed);
         stage_x(a.h, nullptr, a.H, lw.g_post, false);
         stamp(step, l, 3, 1);
         if (!(ok = consume(sl, a.gg, a.H))) break;
@@ -501,7 +552,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       // ---- down projection + residual ----
       {
         stamp(step, l, 4, 0);
-        const MkStage sl = mk_stage(a, lw, MK_DOWN, mk_range(a, MK_DOWN, c, G));
+        const MkStage sl = mk_bind(s_stage[MK_DOWN], a.gd, lp, a.embed);
         stage_x(a.act, nullptr, a.I, nullptr, false);
         stamp(step, l, 4, 1);
         if (!(ok = consume(sl, a.gd, a.I))) break;
@@ -517,7 +568,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     if (!ok || !mk_head_on(a, step)) continue;
     // ---- head: final RMSNorm, tied vocabulary projection, two-pass argmax ----
     stamp(step, a.L, 0, 0);
-    const MkStage sl = mk_stage(a, mk_layer(a, 0), MK_VOCAB, mk_range(a, MK_VOCAB, c, G));
+    const MkStage sl = mk_bind(s_stage[MK_VOCAB], a.gv, layer_ptrs(0), a.embed);
     stage_x(a.h, nullptr, a.H, a.g_final, false);
     stamp(step, a.L, 0, 1);
     if (!(ok = consume(sl, a.gv, a.H))) break;

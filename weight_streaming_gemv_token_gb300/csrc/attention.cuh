@@ -107,6 +107,22 @@ inline size_t attn_smem_bytes(int group, int d) {
          16;
 }
 
+// Key range [t0, t1) of split s for the token at position pos (keys 0..pos);
+// false if split s has no keys. Splits hold at least tmin keys where possible
+// and number at most nsplit_max.
+__device__ __forceinline__ bool attn_split_range(const AttnArgs& a, int s, int pos, int* t0, int* t1, int* nsplit_out) {
+  const int n = pos + 1;
+  int nsplit = (n + a.tmin - 1) / a.tmin;
+  if (nsplit > a.nsplit_max) nsplit = a.nsplit_max;
+  const int per = (n + nsplit - 1) / nsplit;
+  nsplit = (n + per - 1) / per;
+  *nsplit_out = nsplit;
+  if (s >= nsplit) return false;
+  *t0 = s * per;
+  *t1 = min(n, *t0 + per);
+  return true;
+}
+
 // Work of split s of key/value head g for the token at position pos, run by
 // NT threads (tid in [0, NT), NT a multiple of 32 and at least 8 warps' worth
 // of the warp-indexed work below) that sync() together. asmem: shared scratch
@@ -118,12 +134,8 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
   const int warp = tid >> 5, lane = tid & 31;
   const int d = a.d, group = a.n_q / a.n_kv;
   const int n = pos + 1;
-  int nsplit = (n + a.tmin - 1) / a.tmin;
-  if (nsplit > a.nsplit_max) nsplit = a.nsplit_max;
-  const int per = (n + nsplit - 1) / nsplit;
-  nsplit = (n + per - 1) / per;
-  if (s >= nsplit) return;
-  const int t0 = s * per, t1 = min(n, t0 + per);
+  int t0, t1, nsplit;
+  if (!attn_split_range(a, s, pos, &t0, &t1, &nsplit)) return;
 
   float* qn = asmem;                       // [group][d]
   float* kn = qn + group * d;              // [d]

@@ -149,6 +149,63 @@ __device__ __forceinline__ float seg_dot<uint16_t>(const unsigned char* seg, con
   return a0 + a1;
 }
 
+// Dots of nr (<= 4) consecutive whole rows held in shared memory with the same
+// x: each x chunk is read from shared memory once for all rows. Lane partials
+// are returned in v[0..3] (zero past nr).
+template <typename WT>
+__device__ __forceinline__ void rows_dot(const unsigned char* seg, int row_bytes, int nr, const float* xs, int in,
+                                         int lane, float (&v)[4]);
+
+template <>
+__device__ __forceinline__ void rows_dot<float>(const unsigned char* seg, int row_bytes, int nr, const float* xs, int,
+                                                int lane, float (&v)[4]) {
+  const int n4 = row_bytes >> 4;
+  const float4* x4 = reinterpret_cast<const float4*>(xs);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) v[r] = 0.f;
+#pragma unroll 2
+  for (int i = lane; i < n4; i += 32) {
+    const float4 x = x4[i];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      if (r < nr) {
+        const float4 w = reinterpret_cast<const float4*>(seg + static_cast<size_t>(r) * row_bytes)[i];
+        v[r] = fmaf(w.x, x.x, fmaf(w.y, x.y, fmaf(w.z, x.z, fmaf(w.w, x.w, v[r]))));
+      }
+    }
+  }
+}
+
+template <>
+__device__ __forceinline__ void rows_dot<uint16_t>(const unsigned char* seg, int row_bytes, int nr, const float* xs,
+                                                   int in, int lane, float (&v)[4]) {
+  const int n8 = row_bytes >> 4;
+  const float4* xa = reinterpret_cast<const float4*>(xs);
+  const float4* xb = reinterpret_cast<const float4*>(xs) + (in >> 3);
+#pragma unroll
+  for (int r = 0; r < 4; ++r) v[r] = 0.f;
+#pragma unroll 2
+  for (int i = lane; i < n8; i += 32) {
+    const float4 p = xa[i], q = xb[i];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      if (r < nr) {
+        const uint4 w = reinterpret_cast<const uint4*>(seg + static_cast<size_t>(r) * row_bytes)[i];
+        float t = v[r];
+        t = fmaf(__uint_as_float(w.x << 16), p.x, t);
+        t = fmaf(__uint_as_float(w.x & 0xFFFF0000u), p.y, t);
+        t = fmaf(__uint_as_float(w.y << 16), p.z, t);
+        t = fmaf(__uint_as_float(w.y & 0xFFFF0000u), p.w, t);
+        t = fmaf(__uint_as_float(w.z << 16), q.x, t);
+        t = fmaf(__uint_as_float(w.z & 0xFFFF0000u), q.y, t);
+        t = fmaf(__uint_as_float(w.w << 16), q.z, t);
+        t = fmaf(__uint_as_float(w.w & 0xFFFF0000u), q.w, t);
+        v[r] = t;
+      }
+    }
+  }
+}
+
 // (v, i) beats (bv, bi) under "largest value, lowest index on ties"; NaN never beats.
 __device__ __forceinline__ bool argmax_better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);

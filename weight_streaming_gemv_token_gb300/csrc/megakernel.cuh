@@ -355,8 +355,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     __syncthreads();
     if (tid == 0) {
       sync_target += G;
-      __threadfence();
-      atomicAdd(a.bar, 1u);
+      // release: this CTA's writes (ordered before by __syncthreads) become
+      // visible to every CTA that acquires the count
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.bar) : "memory");
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(a.bar) < sync_target) {
         if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
@@ -434,14 +435,11 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         v = warp_sum(v);
         if (lane == 0) part[sg.lrow * gm.spr + sg.part] = v;
       } else {
-        // several whole rows: all lane partials first, then one interleaved reduction
+        // several whole rows: all lane partials first (each x chunk read once),
+        // then one interleaved reduction
         float v[4];
         for (int r0 = 0; r0 < sg.nr; r0 += 4) {
-#pragma unroll
-          for (int r = 0; r < 4; ++r)
-            v[r] = (r0 + r < sg.nr)
-                       ? seg_dot<WT>(buf + static_cast<size_t>(r0 + r) * gm.row_bytes, xs, 0, gm.row_bytes, in, lane)
-                       : 0.f;
+          rows_dot<WT>(buf + static_cast<size_t>(r0) * gm.row_bytes, gm.row_bytes, min(4, sg.nr - r0), xs, in, lane, v);
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
@@ -452,10 +450,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       }
       __syncwarp();
       segstamp(2);
-      if (lane == 0 && !cdone && !*vabort) {
-        fence_proxy_async_smem();
-        issue_one();
-      }
+      // The slot's data reached registers before the shuffles above, so the
+      // next bulk copy into it cannot race with these reads.
+      if (lane == 0 && !cdone && !*vabort) issue_one();
       segstamp(3);
       ++consumed;
     }
@@ -500,6 +497,22 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           stage_x(a.h, nullptr, a.H, lw.g_in, false);
         }
         stamp(step, l, 0, 1);
+        // Keys and values before pos do not depend on this token: pull this
+        // CTA's attention range of them into L2 while QKV runs.
+        if (tid == 0 && c < a.n_kv * a.at.nsplit_max) {
+          int t0, t1, ns;
+          if (attn_split_range(a.at, c / a.n_kv, pos, &t0, &t1, &ns)) {
+            t1 = min(t1, pos);
+            if (t1 > t0) {
+              const size_t eb = a.kv_layer_bytes / (static_cast<size_t>(a.n_kv) * a.at.max_seq * a.d);
+              const size_t off = static_cast<size_t>(l) * a.kv_layer_bytes +
+                                 ((static_cast<size_t>(c % a.n_kv) * a.at.max_seq + t0) * a.d) * eb;
+              const uint32_t bytes = static_cast<uint32_t>(static_cast<size_t>(t1 - t0) * a.d * eb);
+              bulk_prefetch_l2(static_cast<const char*>(a.at.kc) + off, bytes);
+              bulk_prefetch_l2(static_cast<const char*>(a.at.vc) + off, bytes);
+            }
+          }
+        }
         if (!(ok = consume(sl, a.gq, a.H))) break;
         for (int lr = tid; lr < sl.nloc; lr += kMkThreads) a.qkv[sl.u0 + lr] = row_value(a.gq, lr);
         stamp(step, l, 0, 2);

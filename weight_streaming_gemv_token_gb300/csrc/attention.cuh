@@ -127,7 +127,7 @@ __device__ __forceinline__ bool attn_split_range(const AttnArgs& a, int s, int p
 // NT threads (tid in [0, NT), NT a multiple of 32 and at least 8 warps' worth
 // of the warp-indexed work below) that sync() together. asmem: shared scratch
 // of attn_smem_bytes(); s_last: one shared int.
-template <typename KT, int GMAX, int NT, typename Sync>
+template <typename KT, int GMAX, int NT, typename Sync, int BATCH = kAttnBatch>
 __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s, int pos, float* asmem, int tid,
                                                  Sync sync, int* s_last) {
   static_assert(NT == kAttnWarps * 32, "the split layout assumes kAttnWarps warps");
@@ -187,15 +187,15 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     o[h] = make_float4(0, 0, 0, 0);
   }
 
-  // Each warp takes a contiguous run of this CTA's keys and loads kAttnBatch of
+  // Each warp takes a contiguous run of this CTA's keys and loads BATCH of
   // them at a time, so one memory round trip covers the whole batch.
   const int per_w = (t1 - t0 + kAttnWarps - 1) / kAttnWarps;
   const int w0 = t0 + warp * per_w;
   const int w1 = min(t1, w0 + per_w);
-  for (int tb = w0; tb < w1; tb += kAttnBatch) {
-    float4 kk[kAttnBatch], vv[kAttnBatch];
+  for (int tb = w0; tb < w1; tb += BATCH) {
+    float4 kk[BATCH], vv[BATCH];
 #pragma unroll
-    for (int u = 0; u < kAttnBatch; ++u) {
+    for (int u = 0; u < BATCH; ++u) {
       const int t = tb + u;
       kk[u] = vv[u] = make_float4(0, 0, 0, 0);
       if (t < w1 && active) {
@@ -211,10 +211,10 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
       if (h >= group) break;
-      float sc[kAttnBatch];
+      float sc[BATCH];
       float mx = m[h];
 #pragma unroll
-      for (int u = 0; u < kAttnBatch; ++u) {
+      for (int u = 0; u < BATCH; ++u) {
         const float dot = q[h].x * kk[u].x + q[h].y * kk[u].y + q[h].z * kk[u].z + q[h].w * kk[u].w;
         sc[u] = (tb + u < w1) ? warp_sum(dot) * a.scale : -INFINITY;
         mx = fmaxf(mx, sc[u]);
@@ -226,7 +226,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
       o[h].z *= corr;
       o[h].w *= corr;
 #pragma unroll
-      for (int u = 0; u < kAttnBatch; ++u) {
+      for (int u = 0; u < BATCH; ++u) {
         const float p = expf(sc[u] - mx);
         l[h] += p;
         o[h].x = fmaf(p, vv[u].x, o[h].x);

@@ -391,7 +391,7 @@ dec_status plan_persistent(dec_ctx* c) {
   a.part_floats = (part + 3) / 4 * 4;
   const int attn_floats = static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 3) / 4);
   if (a.xs_floats + a.part_floats < attn_floats) a.part_floats = (attn_floats - a.xs_floats + 3) / 4 * 4;
-  const size_t fixed = kMkWarps * kMkWarpSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats) +
+  const size_t fixed = 2 * kMkWarps * kMkWarpSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats) +
                        static_cast<size_t>(g.layers) * kMkLayerPtrs * sizeof(void*);
   const size_t static_smem = 64 * 4 + 32 * 4 + 8 + 5 * sizeof(MkStageT) + 256;
   const size_t per_slot = static_cast<size_t>(kMkWarps) * kMkSlot;  // one slot in every warp's ring

@@ -6,15 +6,16 @@
 // 227 ordered dispatches. This kernel keeps the whole GPU busy inside one
 // launch: one CTA per SM, co-resident by cooperative launch.
 //
-//  * Every weight segment (at most 4 KB) this CTA will read, over all stages
+//  * Every weight segment (at most 8 KB) this CTA will read, over all stages
 //    of all requested steps (QKV, O, gate/up, down of every layer, then the
-//    vocabulary slice), is assigned to one of its 8 warps: segment j of a
-//    stage goes to warp j mod 8. Each warp owns a private ring of 4 KB
-//    shared-memory slots and keeps it full: lane 0 walks a cursor through the
-//    warp's future segments (across stage, layer and step boundaries) and
-//    issues a bulk copy for the next one each time a slot is consumed.
-//    Weights never depend on activations, so the rings hold the next stages'
-//    weights while the CTA waits at a barrier and HBM keeps streaming.
+//    vocabulary slice), is assigned to one of its 8 consumer warps: segment j
+//    of a stage goes to warp j mod 8. Each consumer warp owns a private ring
+//    of shared-memory slots. Lane w of a ninth, producer warp walks a cursor
+//    through consumer w's future segments (across stage, layer and step
+//    boundaries) and issues a bulk copy into ring w whenever a slot is free
+//    (full/empty mbarrier pair per slot). Weights never depend on
+//    activations, so the rings hold the next stages' weights while the
+//    consumers wait at a barrier, and HBM keeps streaming.
 //  * Per stage the CTA stages the activation vector (with the fused RMSNorm),
 //    each warp reduces its segments to partial dots, the partials are summed
 //    in a fixed order, the fused epilogue runs, and the CTAs meet at a grid
@@ -37,8 +38,9 @@
 
 namespace wsg {
 
-constexpr int kMkWarps = 8;
-constexpr int kMkThreads = kMkWarps * 32;
+constexpr int kMkWarps = 8;                      // consumer warps
+constexpr int kMkConsumers = kMkWarps * 32;
+constexpr int kMkThreads = kMkConsumers + 32;    // plus one producer warp
 constexpr int kMkSlot = 8192;         // bytes per ring slot
 constexpr int kMkLayerPtrs = 12;      // pointers per layer in the shared layer table
 constexpr int kMkWarpSlotsMax = 8;    // ring slots per warp, upper bound
@@ -238,7 +240,13 @@ __device__ __forceinline__ bool mk_head_on(const MkArgs& a, int step) {
 }
 
 // Widest activation vector the staging code holds in registers (16 per thread).
-constexpr int kMkMaxWidth = 16 * kMkThreads;
+constexpr int kMkMaxWidth = 16 * kMkConsumers;
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kMkConsumers) : "memory"); }
+
+struct ConsumerSync {  // barrier over the consumer warps only
+  __device__ __forceinline__ void operator()() const { consumer_sync(); }
+};
 
 template <typename WT, typename KT, int GMAX>
 __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs a) {
@@ -250,16 +258,16 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   const int R = a.wslots;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
-  unsigned char* myring = smem + static_cast<size_t>(warp) * R * kMkSlot;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kMkWarps) * R * kMkSlot);
-  uint64_t* mybars = bars + warp * kMkWarpSlotsMax;
-  float* xs = reinterpret_cast<float*>(bars + kMkWarps * kMkWarpSlotsMax);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kMkWarps) * R * kMkSlot);
+  uint64_t* empty = full + kMkWarps * kMkWarpSlotsMax;
+  float* xs = reinterpret_cast<float*>(empty + kMkWarps * kMkWarpSlotsMax);
   float* part = xs + a.xs_floats;
   float* ascratch = xs;  // the attention stage reuses the GEMV staging area
   const void** lptr = reinterpret_cast<const void**>(part + a.part_floats);  // [L][kMkLayerPtrs]
   volatile int* vabort = &s_abort;
+  auto ring_of = [&](int w) { return smem + static_cast<size_t>(w) * R * kMkSlot; };
 
-  // Per-launch tables: every layer's tensor pointers, this CTA's stage geometry.
+  // ---- per-launch tables: every layer's tensor pointers, this CTA's stage geometry ----
   for (int i = tid; i < a.L * kMkLayerPtrs; i += kMkThreads) {
     const int l = i / kMkLayerPtrs, k = i - l * kMkLayerPtrs;
     const MkLayer* p = a.layers + l;
@@ -281,82 +289,104 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     lptr[i] = v;
   }
   if (tid < 5) s_stage[tid] = mk_stage_t(a, tid, mk_range(a, tid, c, G));
-  __syncthreads();
-  auto layer_ptrs = [&](int l) { return lptr + l * kMkLayerPtrs; };
-
-  // ---- issue cursor (lane 0 of each warp): this warp's segments in
-  //      consumption order, steps -> layers -> QKV, O, gate/up, down -> head ----
-  int cstep = 0, clayer = 0, cst = MK_QKV, cj = 0;
-  bool cdone = false;
-  MkStage cs{};
-  int issued = 0;    // lane 0: segments issued into this warp's ring
-  int consumed = 0;  // all lanes: segments consumed
-  const uint64_t pol = l2_policy_evict_first();
-  auto cursor_advance = [&]() {
-    if (cst == MK_VOCAB) {
-      ++cstep;
-      clayer = 0;
-      cst = MK_QKV;
-    } else if (cst == MK_DOWN) {
-      if (clayer + 1 < a.L) {
-        ++clayer;
-        cst = MK_QKV;
-      } else if (mk_head_on(a, cstep)) {
-        cst = MK_VOCAB;
-      } else {
-        ++cstep;
-        clayer = 0;
-        cst = MK_QKV;
-      }
-    } else {
-      ++cst;
-    }
-  };
-  auto cursor_settle = [&]() {  // first stage, from the current one, that has a segment for this warp
-    while (true) {
-      if (cstep >= a.nsteps) {
-        cdone = true;
-        return;
-      }
-      cs = mk_bind(s_stage[cst], mk_geom(a, cst), layer_ptrs(cst == MK_VOCAB ? 0 : clayer), a.embed);
-      cj = warp;
-      if (cj < cs.n) return;
-      cursor_advance();
-    }
-  };
-  auto issue_one = [&]() {  // lane 0 only; requires issued < consumed + R
-    const MkSeg sg = mk_seg(cs, mk_geom(a, cst), cj);
-    const int slot = issued % R;
-    mbar_arrive_expect_tx(&mybars[slot], static_cast<uint32_t>(sg.bytes));
-    bulk_g2s(myring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes), &mybars[slot], pol);
-    ++issued;
-    cj += kMkWarps;
-    if (cj >= cs.n) {
-      cursor_advance();
-      cursor_settle();
-    }
-  };
   if (tid == 0) {
     s_abort = 0;
     s_last = 0;
   }
-  if (lane == 0) {
-    for (int s = 0; s < R; ++s) mbar_init(&mybars[s], 1);
+  if (tid < kMkWarps * R) {
+    const int w = tid / R, s = tid - w * R;
+    mbar_init(&full[w * kMkWarpSlotsMax + s], 1);
+    mbar_init(&empty[w * kMkWarpSlotsMax + s], 1);
     fence_mbar_init();
-    cursor_settle();
-    while (!cdone && issued < R) issue_one();
   }
   __syncthreads();
+  auto layer_ptrs = [&](int l) { return lptr + l * kMkLayerPtrs; };
 
+  // ------------------------------------------------------------------ producer ----
+  if (warp == kMkWarps) {
+    if (lane < kMkWarps) {
+      const int w = lane;
+      uint64_t* wfull = full + w * kMkWarpSlotsMax;
+      uint64_t* wempty = empty + w * kMkWarpSlotsMax;
+      unsigned char* wring = ring_of(w);
+      const uint64_t pol = l2_policy_evict_first();
+      int cstep = 0, clayer = 0, cst = MK_QKV, cj = 0;
+      bool cdone = false;
+      MkStage cs{};
+      auto advance = [&]() {
+        if (cst == MK_VOCAB) {
+          ++cstep;
+          clayer = 0;
+          cst = MK_QKV;
+        } else if (cst == MK_DOWN) {
+          if (clayer + 1 < a.L) {
+            ++clayer;
+            cst = MK_QKV;
+          } else if (mk_head_on(a, cstep)) {
+            cst = MK_VOCAB;
+          } else {
+            ++cstep;
+            clayer = 0;
+            cst = MK_QKV;
+          }
+        } else {
+          ++cst;
+        }
+      };
+      auto settle = [&]() {  // first stage, from the current one, with a segment for consumer w
+        while (true) {
+          if (cstep >= a.nsteps) {
+            cdone = true;
+            return;
+          }
+          cs = mk_bind(s_stage[cst], mk_geom(a, cst), layer_ptrs(cst == MK_VOCAB ? 0 : clayer), a.embed);
+          cj = w;
+          if (cj < cs.n) return;
+          advance();
+        }
+      };
+      settle();
+      int issued = 0;
+      while (!cdone) {
+        const int slot = issued % R;
+        if (issued >= R && !mbar_wait(&wempty[slot], ((issued / R) - 1) & 1)) {
+          *vabort = 1;
+          atomicOr(a.err, ERR_MBAR_TIMEOUT);
+          break;
+        }
+        if (*vabort) break;
+        const MkSeg sg = mk_seg(cs, mk_geom(a, cst), cj);
+        mbar_arrive_expect_tx(&wfull[slot], static_cast<uint32_t>(sg.bytes));
+        bulk_g2s(wring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes), &wfull[slot],
+                 pol);
+        ++issued;
+        cj += kMkWarps;
+        if (cj >= cs.n) {
+          advance();
+          settle();
+        }
+      }
+      // After an abort: wait (bounded) until the copies already issued have landed.
+      if (*vabort)
+        for (int n = max(0, issued - R); n < issued; ++n) mbar_wait(&wfull[n % R], (n / R) & 1);
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers ----
+  uint64_t* mfull = full + warp * kMkWarpSlotsMax;
+  uint64_t* mempty = empty + warp * kMkWarpSlotsMax;
+  const unsigned char* myring = ring_of(warp);
+  int consumed = 0;
   uint32_t sync_target = 0;
   const int qw = a.n_q * a.d;
 
   auto grid_sync = [&]() -> bool {
-    __syncthreads();
+    consumer_sync();
     if (tid == 0) {
       sync_target += G;
-      // release: this CTA's writes (ordered before by __syncthreads) become
-      // visible to every CTA that acquires the count
+      // release: the consumers' writes (ordered before by the named barrier)
+      // become visible to every CTA that acquires the count
       asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.bar) : "memory");
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(a.bar) < sync_target) {
@@ -367,19 +397,19 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         }
       }
     }
-    __syncthreads();
+    consumer_sync();
     return !*vabort;
   };
 
   // Stage the activation vector: plain copy, or RMSNorm(src) * gain. Values
   // and gains are loaded together (one memory round trip) into registers.
   auto stage_x = [&](const float* src, const WT* wsrc, int in, const float* gain, bool store_h) {
-    constexpr int K = kMkMaxWidth / kMkThreads;
+    constexpr int K = kMkMaxWidth / kMkConsumers;
     float v[K], gn[K];
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      const int i = tid + k * kMkThreads;
+      const int i = tid + k * kMkConsumers;
       v[k] = 0.f;
       gn[k] = 1.f;
       if (i < in) {
@@ -393,7 +423,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     if (gain) {
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
-      __syncthreads();
+      consumer_sync();
       float t = 0.f;
 #pragma unroll
       for (int w = 0; w < kMkWarps; ++w) t += red[w];
@@ -401,27 +431,28 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     }
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      const int i = tid + k * kMkThreads;
+      const int i = tid + k * kMkConsumers;
       if (i < in) {
         if (store_h) a.h[i] = v[k];
         xs[xs_index<WT>(i, in)] = gain ? v[k] * inv * gn[k] : v[k];
       }
     }
-    __syncthreads();
+    consumer_sync();
   };
 
-  // This warp's segments of one stage, in ring order, into part[].
   uint64_t* segtrace = nullptr;
   if (a.trace && c == 0 && warp == 0)
     segtrace = a.trace + static_cast<size_t>(G) * (a.L + 1) * kMkTraceStages * kMkTraceEvents;
   auto segstamp = [&](int ev) {
     if (segtrace && lane == 0 && consumed < kMkTraceSegs) segtrace[consumed * kMkTraceSegEvents + ev] = clock64();
   };
+
+  // This warp's segments of one stage, in ring order, into part[].
   auto consume = [&](const MkStage& sl, const MkGeom& gm, int in) -> bool {
     for (int j = warp; j < sl.n; j += kMkWarps) {
       const int slot = consumed % R;
       segstamp(0);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&mybars[slot], (consumed / R) & 1));
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&mfull[slot], (consumed / R) & 1));
       segstamp(1);
       if (!ok) {
         if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
@@ -448,15 +479,15 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
             for (int r = 0; r < 4 && r0 + r < sg.nr; ++r) part[sg.lrow + r0 + r] = v[r];
         }
       }
-      __syncwarp();
       segstamp(2);
-      // The slot's data reached registers before the shuffles above, so the
-      // next bulk copy into it cannot race with these reads.
-      if (lane == 0 && !cdone && !*vabort) issue_one();
+      // The slot's data reached registers before the shuffles above; hand the
+      // slot back to the producer.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mempty[slot]);
       segstamp(3);
       ++consumed;
     }
-    __syncthreads();
+    consumer_sync();
     return !*vabort;
   };
 
@@ -477,11 +508,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     const int pos = a.pos0 + step;
     for (int l = 0; l < a.L && ok; ++l) {
       const void* const* lp = layer_ptrs(l);
-      MkLayer lw;
-      lw.g_in = static_cast<const float*>(lp[7]);
-      lw.g_post = static_cast<const float*>(lp[8]);
-      lw.g_q = static_cast<const float*>(lp[9]);
-      lw.g_k = static_cast<const float*>(lp[10]);
+      const float* g_in = static_cast<const float*>(lp[7]);
+      const float* g_post = static_cast<const float*>(lp[8]);
       // ---- QKV with the input RMSNorm (layer 0: of the token's embedding row) ----
       {
         stamp(step, l, 0, 0);
@@ -492,9 +520,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
             if (tid == 0) atomicOr(a.err, ERR_BAD_TOKEN);
             t = 0;
           }
-          stage_x(nullptr, static_cast<const WT*>(a.embed) + static_cast<size_t>(t) * a.H, a.H, lw.g_in, c == 0);
+          stage_x(nullptr, static_cast<const WT*>(a.embed) + static_cast<size_t>(t) * a.H, a.H, g_in, c == 0);
         } else {
-          stage_x(a.h, nullptr, a.H, lw.g_in, false);
+          stage_x(a.h, nullptr, a.H, g_in, false);
         }
         stamp(step, l, 0, 1);
         // Keys and values before pos do not depend on this token: pull this
@@ -514,7 +542,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           }
         }
         if (!(ok = consume(sl, a.gq, a.H))) break;
-        for (int lr = tid; lr < sl.nloc; lr += kMkThreads) a.qkv[sl.u0 + lr] = row_value(a.gq, lr);
+        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) a.qkv[sl.u0 + lr] = row_value(a.gq, lr);
         stamp(step, l, 0, 2);
         if (!(ok = grid_sync())) break;
         stamp(step, l, 0, 3);
@@ -522,13 +550,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       // ---- attention (Q/K norm, RoPE, KV append, key-parallel splits) ----
       {
         AttnArgs at = a.at;
-        at.g_q = lw.g_q;
-        at.g_k = lw.g_k;
+        at.g_q = static_cast<const float*>(lp[9]);
+        at.g_k = static_cast<const float*>(lp[10]);
         at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         stamp(step, l, 1, 0);
         if (c < a.n_kv * at.nsplit_max)
-          attn_decode_body<KT, GMAX, kMkThreads>(at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, CtaSync{}, &s_last);
+          attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, 4>(at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid,
+                                                                    ConsumerSync{}, &s_last);
         stamp(step, l, 1, 2);
         if (!(ok = grid_sync())) break;
         stamp(step, l, 1, 3);
@@ -540,7 +569,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         stage_x(a.attn, nullptr, qw, nullptr, false);
         stamp(step, l, 2, 1);
         if (!(ok = consume(sl, a.go, qw))) break;
-        for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
+        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
           const int row = sl.u0 + lr;
           a.h[row] = __ldcg(a.h + row) + row_value(a.go, lr);
         }
@@ -552,11 +581,11 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       {
         stamp(step, l, 3, 0);
         const MkStage sl = mk_bind(s_stage[MK_GU], a.gg, lp, a.embed);
-        stage_x(a.h, nullptr, a.H, lw.g_post, false);
+        stage_x(a.h, nullptr, a.H, g_post, false);
         stamp(step, l, 3, 1);
         if (!(ok = consume(sl, a.gg, a.H))) break;
         const int np = sl.nloc >> 1;
-        for (int i = tid; i < np; i += kMkThreads)
+        for (int i = tid; i < np; i += kMkConsumers)
           a.act[sl.u0 + i] = silu_f32(row_value(a.gg, i)) * row_value(a.gg, np + i);
         stamp(step, l, 3, 2);
         if (!(ok = grid_sync())) break;
@@ -569,7 +598,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         stage_x(a.act, nullptr, a.I, nullptr, false);
         stamp(step, l, 4, 1);
         if (!(ok = consume(sl, a.gd, a.I))) break;
-        for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
+        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
           const int row = sl.u0 + lr;
           a.h[row] = __ldcg(a.h + row) + row_value(a.gd, lr);
         }
@@ -588,7 +617,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     stamp(step, a.L, 0, 2);
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int lr = tid; lr < sl.nloc; lr += kMkThreads) {
+    for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
       const int row = sl.u0 + lr;
       const float v = row_value(a.gv, lr);
       if (a.logits) a.logits[row] = v;
@@ -610,7 +639,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       red[warp] = bv;
       redi[warp] = bi;
     }
-    __syncthreads();
+    consumer_sync();
     if (tid == 0) {
       for (int w = 1; w < kMkWarps; ++w)
         if (argmax_better(red[w], redi[w], bv, bi)) {
@@ -645,13 +674,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     if (step + 1 < a.nsteps) ok = grid_sync();  // the next step reads the new token
   }
 
-  // ---- after an abort: wait (bounded) for this warp's copies still in flight ----
-  if (*vabort && lane == 0) {
-    for (int g = consumed; g < issued; ++g) mbar_wait(&mybars[g % R], (g / R) & 1);
-  }
-  __syncthreads();
-
   // ---- exit: the last CTA out resets the barrier counters and publishes the position ----
+  consumer_sync();
   if (tid == 0) {
     __threadfence();
     if (atomicAdd(a.bar + 1, 1u) == static_cast<uint32_t>(G - 1)) {

@@ -304,72 +304,91 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
 
   // ------------------------------------------------------------------ producer ----
   if (warp == kMkWarps) {
-    if (lane < kMkWarps) {
-      const int w = lane;
-      uint64_t* wfull = full + w * kMkWarpSlotsMax;
-      uint64_t* wempty = empty + w * kMkWarpSlotsMax;
-      unsigned char* wring = ring_of(w);
-      const uint64_t pol = l2_policy_evict_first();
-      int cstep = 0, clayer = 0, cst = MK_QKV, cj = 0;
-      bool cdone = false;
-      MkStage cs{};
-      auto advance = [&]() {
-        if (cst == MK_VOCAB) {
+    // Lane w feeds consumer warp w's ring. The warp stays converged: every
+    // pass, each lane tests (without blocking) whether its next slot is free,
+    // and all lanes that can issue do so together.
+    const int w = lane;
+    uint64_t* wfull = full + (w < kMkWarps ? w : 0) * kMkWarpSlotsMax;
+    uint64_t* wempty = empty + (w < kMkWarps ? w : 0) * kMkWarpSlotsMax;
+    unsigned char* wring = ring_of(w < kMkWarps ? w : 0);
+    const uint64_t pol = l2_policy_evict_first();
+    int cstep = 0, clayer = 0, cst = MK_QKV, cj = 0;
+    bool cdone = w >= kMkWarps;
+    MkStage cs{};
+    auto advance = [&]() {
+      if (cst == MK_VOCAB) {
+        ++cstep;
+        clayer = 0;
+        cst = MK_QKV;
+      } else if (cst == MK_DOWN) {
+        if (clayer + 1 < a.L) {
+          ++clayer;
+          cst = MK_QKV;
+        } else if (mk_head_on(a, cstep)) {
+          cst = MK_VOCAB;
+        } else {
           ++cstep;
           clayer = 0;
           cst = MK_QKV;
-        } else if (cst == MK_DOWN) {
-          if (clayer + 1 < a.L) {
-            ++clayer;
-            cst = MK_QKV;
-          } else if (mk_head_on(a, cstep)) {
-            cst = MK_VOCAB;
-          } else {
-            ++cstep;
-            clayer = 0;
-            cst = MK_QKV;
-          }
-        } else {
-          ++cst;
         }
-      };
-      auto settle = [&]() {  // first stage, from the current one, with a segment for consumer w
-        while (true) {
-          if (cstep >= a.nsteps) {
-            cdone = true;
-            return;
-          }
-          cs = mk_bind(s_stage[cst], mk_geom(a, cst), layer_ptrs(cst == MK_VOCAB ? 0 : clayer), a.embed);
-          cj = w;
-          if (cj < cs.n) return;
-          advance();
+      } else {
+        ++cst;
+      }
+    };
+    auto settle = [&]() {  // first stage, from the current one, with a segment for consumer w
+      while (true) {
+        if (cstep >= a.nsteps) {
+          cdone = true;
+          return;
         }
-      };
-      settle();
-      int issued = 0;
-      while (!cdone) {
+        cs = mk_bind(s_stage[cst], mk_geom(a, cst), layer_ptrs(cst == MK_VOCAB ? 0 : clayer), a.embed);
+        cj = w;
+        if (cj < cs.n) return;
+        advance();
+      }
+    };
+    if (!cdone) settle();
+    int issued = 0;
+    uint64_t idle_since = 0;
+    while (__any_sync(0xffffffffu, !cdone)) {
+      bool can = false;
+      if (!cdone) {
         const int slot = issued % R;
-        if (issued >= R && !mbar_wait(&wempty[slot], ((issued / R) - 1) & 1)) {
-          *vabort = 1;
-          atomicOr(a.err, ERR_MBAR_TIMEOUT);
-          break;
-        }
-        if (*vabort) break;
-        const MkSeg sg = mk_seg(cs, mk_geom(a, cst), cj);
-        mbar_arrive_expect_tx(&wfull[slot], static_cast<uint32_t>(sg.bytes));
-        bulk_g2s(wring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes), &wfull[slot],
-                 pol);
-        ++issued;
-        cj += kMkWarps;
-        if (cj >= cs.n) {
-          advance();
-          settle();
+        can = issued < R || mbar_test(&wempty[slot], ((issued / R) - 1) & 1);
+        if (can) {
+          const MkSeg sg = mk_seg(cs, mk_geom(a, cst), cj);
+          mbar_arrive_expect_tx(&wfull[slot], static_cast<uint32_t>(sg.bytes));
+          bulk_g2s(wring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes),
+                   &wfull[slot], pol);
+          ++issued;
+          cj += kMkWarps;
+          if (cj >= cs.n) {
+            advance();
+            settle();
+          }
         }
       }
-      // After an abort: wait (bounded) until the copies already issued have landed.
-      if (*vabort)
-        for (int n = max(0, issued - R); n < issued; ++n) mbar_wait(&wfull[n % R], (n / R) & 1);
+      if (__any_sync(0xffffffffu, can)) {
+        idle_since = 0;
+        continue;
+      }
+      // nothing to issue this pass: back off, bounded
+      if (*vabort) break;
+      const uint64_t now = globaltimer_ns();
+      if (idle_since == 0) {
+        idle_since = now;
+      } else if (now - idle_since > WSG_WAIT_LIMIT_NS) {
+        if (lane == 0) {
+          *vabort = 1;
+          atomicOr(a.err, ERR_MBAR_TIMEOUT);
+        }
+        break;
+      }
+      __nanosleep(64);
     }
+    // After an abort: wait (bounded) until the copies already issued have landed.
+    if (*vabort && w < kMkWarps)
+      for (int n = max(0, issued - R); n < issued; ++n) mbar_wait(&wfull[n % R], (n / R) & 1);
     return;
   }
 

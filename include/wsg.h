@@ -232,6 +232,30 @@ int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r);
  * on the current device; synchronizes the device. */
 dec_status gemv_device_errors(int32_t clear, uint32_t* bits);
 
+/* Greedy head for callers that cannot allocate device memory (the pages have
+ * no counterpart of this call). Some callers cannot call cudaMalloc: code
+ * running inside a host framework that owns every device allocation, or a
+ * generation loop that must not risk the device synchronisation an
+ * allocation can cause. This call computes x = RMSNorm(h) * gain (eps as
+ * given), logits = E x and the greedy token (lowest ID among equal maxima)
+ * with the same kernel as the decoder's head, but keeps that kernel's
+ * scratch (per-CTA argmax partials, a counter, a position word) in a
+ * fixed 8448-byte device array inside the library instead of a workspace.
+ * wdtype DEC_F32 or DEC_BF16: d_embed [vocab][hidden] in that dtype (16-byte
+ * aligned, rows a multiple of 16 bytes); d_h and d_gain float32 [hidden];
+ * d_logits float32 [vocab] or NULL; d_token receives the int32 token.
+ * Limits: at most 1024 CTAs of argmax partials (vocab x hidden beyond that is
+ * rejected with DEC_EINVAL) and hidden small enough for the shared-memory
+ * staging. The array persists on every device that loaded the library until
+ * exit and is shared by all calls: calls that overlap on the GPU (other
+ * streams, other threads) race on it and must be serialised by the caller.
+ * The first call on a device looks up the array's address and sets the
+ * kernel's shared-memory limit; make that first call before any stream
+ * capture. Allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine). Errors: DEC_EINVAL, DEC_EDEVICE, DEC_ECUDA. */
+dec_status greedy_head_noalloc(int32_t wdtype, const void* d_embed, const float* d_h, const float* d_gain, float eps,
+                               int32_t vocab, int32_t hidden, float* d_logits, int32_t* d_token, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -33,5 +33,6 @@ from .binding import (  # noqa: F401
     gemv_device_errors,
     gemv_q4,
     gemv_q4_rows_per_warp,
+    greedy_head_noalloc,
     library,
 )

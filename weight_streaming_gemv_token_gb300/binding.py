@@ -27,7 +27,7 @@ EXPORTED = (
     "dec_workspace_bytes", "dec_create", "dec_load_weights", "dec_reset", "dec_step", "dec_prefill_chunk",
     "dec_generate", "dec_get_kv", "dec_position", "dec_trace_bytes", "dec_set_trace", "dec_device_errors",
     "dec_destroy", "dec_last_error",
-    "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors",
+    "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors", "greedy_head_noalloc",
 )
 
 
@@ -85,6 +85,8 @@ def library() -> ctypes.CDLL:
             "gemv_q4": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]),
             "gemv_q4_rows_per_warp": (c_int32, [c_int32, c_int32]),
             "gemv_device_errors": (c_int32, [c_int32, P(c_uint32)]),
+            "greedy_head_noalloc": (c_int32, [c_int32, c_void_p, c_void_p, c_void_p, c_float, c_int32, c_int32,
+                                              c_void_p, c_void_p, c_void_p]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -209,3 +211,9 @@ def gemv_device_errors(clear: bool = True) -> int:
     bits = c_uint32()
     _check(library().gemv_device_errors(int(clear), ctypes.byref(bits)))
     return bits.value
+
+
+def greedy_head_noalloc(wdtype: int, embed, h, gain, eps: float, vocab: int, hidden: int, logits, token, stream=None):
+    """Final RMSNorm, tied vocabulary GEMV and greedy argmax with no device allocation (library-held scratch)."""
+    _check(library().greedy_head_noalloc(wdtype, _ptr(embed), _ptr(h), _ptr(gain), eps, vocab, hidden, _ptr(logits),
+                                         _ptr(token), _stream(stream)))

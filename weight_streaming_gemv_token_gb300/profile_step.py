@@ -7,8 +7,10 @@ Use under ncu with --profile-from-start off, e.g.
   ncu --profile-from-start off --set full --clock-control none -k regex:gemv_stream -c 3 -o prof \\
       python -m weight_streaming_gemv_token_gb300.profile_step gemv --out 6144 --in 1024 --count 8
 
-decode: Qwen3-0.6B-shaped decoder with seeded random weights, a uniform
-        prompt, warm-up steps, then --steps decode steps inside the region.
+decode: Qwen3-0.6B-shaped decoder (optionally fewer layers / a smaller
+        vocabulary, for captures that must stay small) with seeded random
+        weights, a uniform prompt, warm-up steps, then --steps decode steps
+        inside the region.
 gemv:   --count distinct matrices of one shape (sized past L2 by default),
         one warm-up pass, then one launch per matrix inside the region.
 """
@@ -33,9 +35,13 @@ def decode(args):
 
     build.build()
     s = Wl.QWEN3_06B
+    if args.layers or args.vocab:
+        import dataclasses
+
+        s = dataclasses.replace(s, layers=args.layers or s.layers, vocab=args.vocab or s.vocab)
     w = Wl.decoder_weights(s, seed=1, wdtype=args.dtype)
     prompt = Wl.prompt_uniform(args.prompt, s.vocab, seed=0)
-    dec = Decoder(s, w, kv_dtype=args.kv, max_seq=args.prompt + args.warmup + args.steps + 4)
+    dec = Decoder(s, w, kv_dtype=args.kv, max_seq=args.prompt + args.warmup + args.steps + 4, engine=args.engine)
     first = dec.prefill(prompt, is_last=True)
     out = dec.generate(first, args.warmup)
     torch.cuda.synchronize()
@@ -80,6 +86,9 @@ def main():
     d.add_argument("--prompt", type=int, default=32)
     d.add_argument("--warmup", type=int, default=3)
     d.add_argument("--steps", type=int, default=1)
+    d.add_argument("--layers", type=int, default=0, help="fewer layers than the Qwen3-0.6B shape (0: 28)")
+    d.add_argument("--vocab", type=int, default=0, help="smaller vocabulary (0: 151936)")
+    d.add_argument("--engine", default="persistent", choices=["persistent", "staged"])
     gm = sub.add_parser("gemv")
     gm.add_argument("--out", type=int, default=6144)
     gm.add_argument("--in", dest="inp", type=int, default=1024)

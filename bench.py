@@ -42,6 +42,12 @@ sys.path.insert(0, ROOT)
 import workloads as Wl  # noqa: E402
 
 METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
+
+# DRAM traffic of the persistent decode kernel per algorithmic byte, from ncu on a
+# 4-layer / 32768-vocabulary case of the same widths (profiles/decode_megakernel_small_full.md):
+# (387,255,808 read + 3,407,872 written) / 387,186,688 algorithmic bytes. Set to None when
+# the kernel changes until it is measured again.
+MK_TRAFFIC_PER_ALG_BYTE = (387255808 + 3407872) / 387186688
 PROMPT = 32
 
 
@@ -276,9 +282,20 @@ def gpu_arm(args):
     if rank == 0:
         gen = torch.Generator(device="cuda")
         gen.manual_seed(1234)
-        # dominant kernel: the streaming GEMV at the gate/up shape, cold
+        if args.engine == "persistent":
+            # the dominant (only) kernel of the timed region: one persistent launch for all K steps
+            achieved = step_bytes * K / sec / 1e9
+            extra["roofline"] = {
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(achieved / hbm, 4),
+                "traffic": (round(MK_TRAFFIC_PER_ALG_BYTE * step_bytes * K) if MK_TRAFFIC_PER_ALG_BYTE else None),
+                "peak_kind": peak_kind, "kernel": "decode_megakernel<float,float,2> (one cooperative launch, K steps)",
+                "bytes_per_launch": step_bytes * K, "launch_us": round(sec * 1e6, 1), "launches": 1,
+                "traffic_source": "ncu dram bytes of a 4-layer/32768-vocab case of the same widths, scaled by "
+                                  "algorithmic bytes (profiles/decode_megakernel_small_full.md)"}
+        # the streaming GEMV engine alone at the gate/up shape, cold
         gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", 6144, 1024, stream, gen=gen)
-        extra["roofline"] = {
+        extra["roofline" if args.engine != "persistent" else "gemv_roofline"] = {
             "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
             "traffic": None, "peak_kind": peak_kind,
             "kernel": "gemv_stream_kernel<f32> 6144x1024 (gate/up shape), standalone gemv entry, cold round-robin",

@@ -297,7 +297,9 @@ def gpu_arm(args):
         gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", 6144, 1024, stream, gen=gen)
         extra["roofline" if args.engine != "persistent" else "gemv_roofline"] = {
             "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-            "traffic": None, "peak_kind": peak_kind,
+            # ncu dram__bytes_read+write per launch of this kernel on this shape (no writes; 3 launches,
+            # 25,203,456-25,204,992 B); see profiles/gemv_stream_f32_6144x1024_full.md
+            "traffic": 25204224, "peak_kind": peak_kind,
             "kernel": "gemv_stream_kernel<f32> 6144x1024 (gate/up shape), standalone gemv entry, cold round-robin",
             "bytes_per_launch": per_launch, "avg_launch_us": round(avg * 1e6, 3), "launches": launches}
         if not args.no_sweep:

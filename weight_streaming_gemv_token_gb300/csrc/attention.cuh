@@ -127,9 +127,22 @@ __device__ __forceinline__ bool attn_split_range(const AttnArgs& a, int s, int p
 // NT threads (tid in [0, NT), NT a multiple of 32 and at least 8 warps' worth
 // of the warp-indexed work below) that sync() together. asmem: shared scratch
 // of attn_smem_bytes(); s_last: one shared int.
-template <typename KT, int GMAX, int NT, typename Sync, int BATCH = kAttnBatch>
+// How the attention body reads the raw q/k/v projections and writes its
+// output: directly from / to the buffers of AttnArgs (kernel-boundary
+// ordering), or through another exchange (see the persistent kernel).
+struct AttnPlainIo {
+  const float* qkv;
+  float* out;
+  __device__ __forceinline__ float load_qkv(int i) const { return __ldcg(qkv + i); }
+  __device__ __forceinline__ void acquire() const {}
+  __device__ __forceinline__ void store_out(int i, float v) const { out[i] = v; }
+  // Called by thread 0 after the CTA appended position pos of head g and synced.
+  __device__ __forceinline__ void publish_kv(int, int) const {}
+};
+
+template <typename KT, int GMAX, int NT, typename Sync, int BATCH = kAttnBatch, typename Io = AttnPlainIo>
 __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s, int pos, float* asmem, int tid,
-                                                 Sync sync, int* s_last) {
+                                                 Sync sync, int* s_last, Io io = Io{}) {
   static_assert(NT == kAttnWarps * 32, "the split layout assumes kAttnWarps warps");
   const int warp = tid >> 5, lane = tid & 31;
   const int d = a.d, group = a.n_q / a.n_kv;
@@ -147,13 +160,14 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
   // Current token: raw projections -> RMSNorm -> RoPE (q, k); v as is.
   const float* cs = a.rope_cos + static_cast<size_t>(pos) * (d >> 1);
   const float* sn = a.rope_sin + static_cast<size_t>(pos) * (d >> 1);
-  const float* kraw = a.qkv + a.n_q * d + g * d;
-  const float* vraw = a.qkv + a.n_q * d + a.n_kv * d + g * d;
-  for (int i = tid; i < group * d; i += NT) qn[i] = __ldcg(a.qkv + (g * group) * d + i);
+  const int kraw = a.n_q * d + g * d;
+  const int vraw = a.n_q * d + a.n_kv * d + g * d;
+  for (int i = tid; i < group * d; i += NT) qn[i] = io.load_qkv((g * group) * d + i);
   for (int i = tid; i < d; i += NT) {
-    kn[i] = __ldcg(kraw + i);
-    vn[i] = round_store<KT>(__ldcg(vraw + i));
+    kn[i] = io.load_qkv(kraw + i);
+    vn[i] = round_store<KT>(io.load_qkv(vraw + i));
   }
+  io.acquire();
   sync();
   for (int h = warp; h <= group; h += kAttnWarps) {
     if (h < group)
@@ -249,6 +263,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     if (active) *reinterpret_cast<float4*>(wo + (warp * group + h) * d + 4 * lane) = o[h];
   }
   sync();
+  if (tid == 0 && t1 == n) io.publish_kv(g, pos);
   for (int idx = tid; idx < group * d; idx += NT) {
     const int h = idx / d, e = idx - h * d;
     float M = -INFINITY;
@@ -260,7 +275,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
       O += wo[(w * group + h) * d + e] * f;
     }
     if (nsplit == 1) {
-      a.out[(g * group + h) * d + e] = O / L;
+      io.store_out((g * group + h) * d + e, O / L);
     } else {
       float* p = a.part + ((static_cast<size_t>(g) * a.nsplit_max + s) * group + h) * (d + 2);
       p[e] = O;
@@ -293,7 +308,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
       L += __ldcg(p + d + 1) * f;
       O += __ldcg(p + e) * f;
     }
-    a.out[(g * group + h) * d + e] = O / L;
+    io.store_out((g * group + h) * d + e, O / L);
   }
   if (tid == 0) a.counter[g] = 0u;
 }
@@ -309,8 +324,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, ERR_BAD_POSITION);
     return;
   }
-  attn_decode_body<KT, GMAX, kAttnWarps * 32>(a, blockIdx.x, blockIdx.y, pos, asmem, threadIdx.x,
-                                              CtaSync{}, &s_last);
+  attn_decode_body<KT, GMAX, kAttnWarps * 32>(a, blockIdx.x, blockIdx.y, pos, asmem, threadIdx.x, CtaSync{}, &s_last,
+                                              AttnPlainIo{a.qkv, a.out});
 }
 
 }  // namespace wsg

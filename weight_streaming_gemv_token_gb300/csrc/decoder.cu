@@ -47,8 +47,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
 
 struct Layout {
-  size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, bar, mk_layers, rope_cos, rope_sin,
-      kc, vc;
+  size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn, ll_act,
+      ll_tok, kv_ready, mk_layers, rope_cos, rope_sin, kc, vc;
   size_t total;
 };
 
@@ -97,7 +97,13 @@ Layout make_layout(const dec_config& c) {
   L.mval = take(kArgmaxPartsMax * 4);
   L.midx = take(kArgmaxPartsMax * 4);
   L.mcnt = take(16);
-  L.bar = take(16);
+  // persistent-engine exchange words (64-bit tag/value) and per-head cache positions
+  L.ll_h = take(static_cast<size_t>(c.hidden) * 8);
+  L.ll_qkv = take((qw + 2 * kvw) * 8);
+  L.ll_attn = take(qw * 8);
+  L.ll_act = take(static_cast<size_t>(c.inter) * 8);
+  L.ll_tok = take(8);
+  L.kv_ready = take(static_cast<size_t>(c.layers) * c.n_kv * 4);
   L.mk_layers = take(static_cast<size_t>(c.layers) * sizeof(MkLayer));
   L.rope_cos = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   L.rope_sin = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
@@ -160,6 +166,7 @@ struct dec_ctx {
   int nsplit_max = 1;
   MkArgs mk{};          // persistent-engine arguments (per-call fields filled at launch)
   uint64_t* trace = nullptr;  // caller's stage-trace buffer (persistent engine), or NULL
+  uint32_t epoch = 0;         // tag prefix of the last persistent launch (1..4095)
   size_t mk_smem = 0;
   int mk_grid = 0;
   std::string err;
@@ -389,10 +396,11 @@ dec_status plan_persistent(dec_ctx* c) {
     return fail(&c->err, DEC_EINVAL, "persistent engine: widths above %d need the staged engine", kMkMaxWidth);
   a.xs_floats = (std::max(g.hidden, std::max(qw, g.inter)) + 3) / 4 * 4;
   a.part_floats = (part + 3) / 4 * 4;
+  a.hown_floats = (cdiv(g.hidden, G) + 3) / 4 * 4;
   const int attn_floats = static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 3) / 4);
   if (a.xs_floats + a.part_floats < attn_floats) a.part_floats = (attn_floats - a.xs_floats + 3) / 4 * 4;
   const size_t fixed = 2 * kMkWarps * kMkWarpSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats) +
-                       static_cast<size_t>(g.layers) * kMkLayerPtrs * sizeof(void*);
+                       static_cast<size_t>(g.layers) * kMkLayerPtrs * sizeof(void*) + 4 * static_cast<size_t>(a.hown_floats);
   const size_t static_smem = 64 * 4 + 32 * 4 + 8 + 5 * sizeof(MkStageT) + 256;
   const size_t per_slot = static_cast<size_t>(kMkWarps) * kMkSlot;  // one slot in every warp's ring
   if (fixed + static_smem + per_slot > c->di.smem_optin)
@@ -417,7 +425,12 @@ dec_status plan_persistent(dec_ctx* c) {
   a.mval = c->at<float>(c->L.mval);
   a.midx = c->at<int32_t>(c->L.midx);
   a.mcnt = c->at<uint32_t>(c->L.mcnt);
-  a.bar = c->at<uint32_t>(c->L.bar);
+  a.ll_h = c->at<uint64_t>(c->L.ll_h);
+  a.ll_qkv = c->at<uint64_t>(c->L.ll_qkv);
+  a.ll_attn = c->at<uint64_t>(c->L.ll_attn);
+  a.ll_act = c->at<uint64_t>(c->L.ll_act);
+  a.ll_tok = c->at<uint64_t>(c->L.ll_tok);
+  a.kv_ready = c->at<uint32_t>(c->L.kv_ready);
   a.layers = c->at<MkLayer>(c->L.mk_layers);
   AttnArgs& at = a.at;
   at.qkv = a.qkv;
@@ -452,6 +465,10 @@ dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, boo
   a.head_every = head_every ? 1 : 0;
   a.head_last = head_last ? 1 : 0;
   a.trace = c->trace;
+  c->epoch = c->epoch % 4095 + 1;  // exchange tags never repeat between consecutive launches
+  a.epoch = c->epoch;
+  if (static_cast<long long>(nsteps) * (c->cfg.layers + 1) * 5 + 1 >= (1ll << 20))
+    return fail(&c->err, DEC_EINVAL, "persistent engine: %d steps exceed one launch's tag space", nsteps);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c->mk_grid);
   cfg.blockDim = dim3(kMkThreads);

@@ -18,13 +18,19 @@
 //    consumers wait at a barrier, and HBM keeps streaming.
 //  * Per stage the CTA stages the activation vector (with the fused RMSNorm),
 //    each warp reduces its segments to partial dots, the partials are summed
-//    in a fixed order, the fused epilogue runs, and the CTAs meet at a grid
-//    barrier before the next stage reads what this one wrote.
+//    in a fixed order and the fused epilogue writes the outputs. Stages hand
+//    data to each other through exchange words: 64-bit (tag, value) pairs
+//    written in one store. A reader polls the words it needs until they carry
+//    the tag of the producing stage, so readiness and data arrive together
+//    and no grid-wide barrier is needed. Each buffer's next version can only
+//    be written after every reader of the current version has read it (the
+//    forward's own data dependencies order them), and a CTA with no rows in a
+//    stage reads nothing for it.
 //  * Attention runs between QKV and O on n_kv x nsplit CTAs (the same body as
 //    the standalone attention kernel: Q/K norm, RoPE, KV append, key-parallel
 //    splits merged by the last CTA).
-//  * The head (final RMSNorm, vocabulary GEMV, two-pass argmax) writes the
-//    next token, which the next step's embedding gather reads after a barrier.
+//  * The head (final RMSNorm, vocabulary GEMV, two-pass argmax) publishes the
+//    next token as an exchange word for the next step's embedding gather.
 //
 // Every wait is bounded. On a timeout the CTA raises an abort flag, stops
 // issuing, waits (bounded) for the copies already in flight, and the error
@@ -45,7 +51,7 @@ constexpr int kMkSlot = 8192;         // bytes per ring slot
 constexpr int kMkLayerPtrs = 12;      // pointers per layer in the shared layer table
 constexpr int kMkWarpSlotsMax = 8;    // ring slots per warp, upper bound
 
-enum : uint32_t { ERR_GRID_BARRIER_TIMEOUT = 1u << 4 };
+enum : uint32_t { ERR_EXCHANGE_TIMEOUT = 1u << 4 };
 
 struct MkLayer {
   const void *wq, *wk, *wv, *wo, *wg, *wu, *wd;
@@ -78,11 +84,19 @@ struct MkArgs {
   float* mval;
   int32_t* midx;
   uint32_t* mcnt;
-  uint32_t* bar;  // [0] grid barrier arrivals, [1] CTAs finished
-  AttnArgs at;    // kc / vc point at layer 0's cache
+  // Cross-CTA exchanges: 64-bit (tag, value) words, each written in one store,
+  // so a reader that sees the expected tag also has the value.
+  uint64_t* ll_h;     // residual stream [H]
+  uint64_t* ll_qkv;   // raw q, k, v [(n_q + 2 n_kv) d]
+  uint64_t* ll_attn;  // attention output [n_q d]
+  uint64_t* ll_act;   // SwiGLU activations [I]
+  uint64_t* ll_tok;   // next token [1]
+  uint32_t* kv_ready; // [L][n_kv]: positions appended to the cache (release-stored)
+  uint32_t epoch;     // per-launch tag prefix (nonzero; 12 bits)
+  AttnArgs at;        // kc / vc point at layer 0's cache
   size_t kv_layer_bytes;
   int32_t wslots;  // ring slots per warp (<= kMkWarpSlotsMax)
-  int32_t xs_floats, part_floats;
+  int32_t xs_floats, part_floats, hown_floats;
   int32_t pos0, nsteps;
   int32_t head_every, head_last;  // head on every step / on the last step
   uint64_t* trace;  // optional: [G][L + 1][5][4] globaltimer stamps of the first forward
@@ -242,6 +256,87 @@ __device__ __forceinline__ bool mk_head_on(const MkArgs& a, int step) {
 // Widest activation vector the staging code holds in registers (16 per thread).
 constexpr int kMkMaxWidth = 16 * kMkConsumers;
 
+// ---- flag-in-data exchange ----
+__device__ __forceinline__ uint32_t mk_tag(const MkArgs& a, int step, int l, int st) {
+  return (a.epoch << 20) | static_cast<uint32_t>((step * (a.L + 1) + l) * 5 + st + 1);
+}
+
+__device__ __forceinline__ void ll_store(uint64_t* p, float v, uint32_t tag) {
+  const uint64_t w = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+// Release store: this thread's earlier writes (and, through a CTA barrier,
+// the CTA's) are visible to whoever reads the tag.
+__device__ __forceinline__ void ll_store_release(uint64_t* p, float v, uint32_t tag) {
+  const uint64_t w = (static_cast<uint64_t>(tag) << 32) | __float_as_uint(v);
+  asm volatile("st.release.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ll_load(const uint64_t* p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Value of an exchange word once its tag is `tag`; bounded poll. On timeout
+// raises the abort flag, records the error and returns 0.
+__device__ __forceinline__ float ll_wait(const uint64_t* p, uint32_t tag, uint64_t w, volatile int* abort,
+                                         uint32_t* err) {
+  if (static_cast<uint32_t>(w >> 32) == tag) return __uint_as_float(static_cast<uint32_t>(w));
+  const uint64_t t0 = globaltimer_ns();
+  for (int it = 0;; ++it) {
+    w = ll_load(p);
+    if (static_cast<uint32_t>(w >> 32) == tag) return __uint_as_float(static_cast<uint32_t>(w));
+    if ((it & 63) == 63) {
+      if (*abort) return 0.f;
+      if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+        *abort = 1;
+        atomicOr(err, ERR_EXCHANGE_TIMEOUT);
+        return 0.f;
+      }
+    }
+  }
+}
+
+// Attention input/output through the exchange words; the cache rows this CTA
+// appends are published with a release store of the per-head position count.
+struct AttnLlIo {
+  const uint64_t* qkv;
+  uint64_t* out;
+  uint32_t* kv_ready;  // this layer's [n_kv]
+  uint32_t tag_in, tag_out;
+  volatile int* abort;
+  uint32_t* err;
+  __device__ __forceinline__ float load_qkv(int i) const { return ll_wait(qkv + i, tag_in, ll_load(qkv + i), abort, err); }
+  __device__ __forceinline__ void acquire() const { fence_acq_rel_gpu(); }
+  __device__ __forceinline__ void store_out(int i, float v) const { ll_store_release(out + i, v, tag_out); }
+  __device__ __forceinline__ void publish_kv(int g, int pos) const {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(kv_ready + g), "r"(static_cast<uint32_t>(pos + 1))
+                 : "memory");
+  }
+};
+
+// Bounded wait until *p >= v, with acquire semantics.
+__device__ __forceinline__ bool wait_at_least(const uint32_t* p, uint32_t v, volatile int* abort, uint32_t* err) {
+  const uint64_t t0 = globaltimer_ns();
+  for (int it = 0;; ++it) {
+    uint32_t x;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
+    if (x >= v) return true;
+    if ((it & 63) == 63) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+        *abort = 1;
+        atomicOr(err, ERR_EXCHANGE_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kMkConsumers) : "memory"); }
 
 struct ConsumerSync {  // barrier over the consumer warps only
@@ -396,48 +491,36 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   uint64_t* mfull = full + warp * kMkWarpSlotsMax;
   uint64_t* mempty = empty + warp * kMkWarpSlotsMax;
   const unsigned char* myring = ring_of(warp);
+  float* hown = reinterpret_cast<float*>(lptr + a.L * kMkLayerPtrs);  // this CTA's rows of h
   int consumed = 0;
-  uint32_t sync_target = 0;
   const int qw = a.n_q * a.d;
+  const MkRange rH = mk_range(a, MK_O, c, G);  // O and down own the same rows of h
 
-  auto grid_sync = [&]() -> bool {
-    consumer_sync();
-    if (tid == 0) {
-      sync_target += G;
-      // release: the consumers' writes (ordered before by the named barrier)
-      // become visible to every CTA that acquires the count
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(a.bar) : "memory");
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_gpu(a.bar) < sync_target) {
-        if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
-          *vabort = 1;
-          atomicOr(a.err, ERR_GRID_BARRIER_TIMEOUT);
-          break;
-        }
+  // Stage an activation vector from exchange words (tag `tag`) into xs:
+  // plain copy, or RMSNorm * gain. All loads are issued first, then only the
+  // words not yet carrying the tag are polled.
+  auto stage_ll = [&](const uint64_t* src, uint32_t tag, int in, const float* gain) {
+    constexpr int K = kMkMaxWidth / kMkConsumers;
+    uint64_t wv[K];
+    float gn[K];
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = tid + k * kMkConsumers;
+      wv[k] = 0;
+      gn[k] = 1.f;
+      if (i < in) {
+        wv[k] = ll_load(src + i);
+        if (gain) gn[k] = __ldg(gain + i);
       }
     }
-    consumer_sync();
-    return !*vabort;
-  };
-
-  // Stage the activation vector: plain copy, or RMSNorm(src) * gain. Values
-  // and gains are loaded together (one memory round trip) into registers.
-  auto stage_x = [&](const float* src, const WT* wsrc, int in, const float* gain, bool store_h) {
-    constexpr int K = kMkMaxWidth / kMkConsumers;
-    float v[K], gn[K];
+    float v[K];
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int i = tid + k * kMkConsumers;
-      v[k] = 0.f;
-      gn[k] = 1.f;
-      if (i < in) {
-        v[k] = wsrc ? load_f32<WT>(wsrc, i) : __ldcg(src + i);
-        if (gain) gn[k] = __ldg(gain + i);
-      }
+      v[k] = i < in ? ll_wait(src + i, tag, wv[k], vabort, a.err) : 0.f;
+      ss = fmaf(v[k], v[k], ss);
     }
-#pragma unroll
-    for (int k = 0; k < K; ++k) ss = fmaf(v[k], v[k], ss);
     float inv = 1.f;
     if (gain) {
       ss = warp_sum(ss);
@@ -451,10 +534,35 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int i = tid + k * kMkConsumers;
-      if (i < in) {
-        if (store_h) a.h[i] = v[k];
-        xs[xs_index<WT>(i, in)] = gain ? v[k] * inv * gn[k] : v[k];
-      }
+      if (i < in) xs[xs_index<WT>(i, in)] = gain ? v[k] * inv * gn[k] : v[k];
+    }
+    consumer_sync();
+  };
+
+  // Layer 0: RMSNorm of the token's embedding row.
+  auto stage_embed = [&](int t, const float* gain) {
+    constexpr int K = kMkMaxWidth / kMkConsumers;
+    const WT* row = static_cast<const WT*>(a.embed) + static_cast<size_t>(t) * a.H;
+    float v[K], gn[K];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = tid + k * kMkConsumers;
+      v[k] = i < a.H ? load_f32<WT>(row, i) : 0.f;
+      gn[k] = i < a.H ? __ldg(gain + i) : 1.f;
+      ss = fmaf(v[k], v[k], ss);
+    }
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    consumer_sync();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMkWarps; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / static_cast<float>(a.H) + a.eps);
+#pragma unroll
+    for (int k = 0; k < K; ++k) {
+      const int i = tid + k * kMkConsumers;
+      if (i < a.H) xs[xs_index<WT>(i, a.H)] = v[k] * inv * gn[k];
     }
     consumer_sync();
   };
@@ -516,16 +624,42 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     return v;
   };
 
+  // Trace events per stage: 0 entry, 1 inputs staged, 2 outputs published.
   auto stamp = [&](int step, int l, int st, int ev) {
     if (a.trace && step == 0 && tid == 0)
       a.trace[((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + st) * kMkTraceEvents + ev] =
           globaltimer_ns();
   };
 
+  const bool attn_cta = c < a.n_kv * a.at.nsplit_max;
   bool ok = true;
   for (int step = 0; step < a.nsteps && ok; ++step) {
     const int pos = a.pos0 + step;
-    for (int l = 0; l < a.L && ok; ++l) {
+    // The token: written by the host before the launch, or published by the
+    // previous step's head.
+    int tok;
+    if (step > 0 && a.head_every) {
+      const uint64_t* p = a.ll_tok;
+      tok = __float_as_int(ll_wait(p, mk_tag(a, step - 1, a.L, 0), ll_load(p), vabort, a.err));
+    } else {
+      tok = __ldcg(a.tok + pos);
+    }
+    if (tok < 0 || tok >= a.V) {
+      if (tid == 0) atomicOr(a.err, ERR_BAD_TOKEN);
+      tok = 0;
+    }
+    if (step > 0 && !a.head_every) {
+      // Body-only steps take their token from the host, so nothing else would
+      // order this step's writes after the previous step's reads: read the
+      // previous step's final residual words (written by every CTA that owns
+      // rows of h) before writing anything.
+      for (int i = tid; i < a.H; i += kMkConsumers) {
+        const uint64_t* p = a.ll_h + i;
+        ll_wait(p, mk_tag(a, step - 1, a.L - 1, MK_DOWN), ll_load(p), vabort, a.err);
+      }
+      consumer_sync();
+    }
+    for (int l = 0; l < a.L && ok && !*vabort; ++l) {
       const void* const* lp = layer_ptrs(l);
       const float* g_in = static_cast<const float*>(lp[7]);
       const float* g_post = static_cast<const float*>(lp[8]);
@@ -533,20 +667,19 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       {
         stamp(step, l, 0, 0);
         const MkStage sl = mk_bind(s_stage[MK_QKV], a.gq, lp, a.embed);
-        if (l == 0) {
-          int t = __ldcg(a.tok + pos);
-          if (t < 0 || t >= a.V) {
-            if (tid == 0) atomicOr(a.err, ERR_BAD_TOKEN);
-            t = 0;
-          }
-          stage_x(nullptr, static_cast<const WT*>(a.embed) + static_cast<size_t>(t) * a.H, a.H, g_in, c == 0);
-        } else {
-          stage_x(a.h, nullptr, a.H, g_in, false);
+        if (sl.nloc > 0) {
+          if (l == 0)
+            stage_embed(tok, g_in);
+          else
+            stage_ll(a.ll_h, mk_tag(a, step, l - 1, MK_DOWN), a.H, g_in);
         }
         stamp(step, l, 0, 1);
-        // Keys and values before pos do not depend on this token: pull this
+        // Keys and values before pos do not depend on this token: make sure the
+        // rows of earlier positions are published (acquire) and pull this
         // CTA's attention range of them into L2 while QKV runs.
-        if (tid == 0 && c < a.n_kv * a.at.nsplit_max) {
+        if (tid == 0 && attn_cta && pos > 0)
+          wait_at_least(a.kv_ready + l * a.n_kv + c % a.n_kv, static_cast<uint32_t>(pos), vabort, a.err);
+        if (tid == 0 && attn_cta) {
           int t0, t1, ns;
           if (attn_split_range(a.at, c / a.n_kv, pos, &t0, &t1, &ns)) {
             t1 = min(t1, pos);
@@ -561,76 +694,80 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           }
         }
         if (!(ok = consume(sl, a.gq, a.H))) break;
-        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) a.qkv[sl.u0 + lr] = row_value(a.gq, lr);
+        const uint32_t tg = mk_tag(a, step, l, MK_QKV);
+        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) ll_store(a.ll_qkv + sl.u0 + lr, row_value(a.gq, lr), tg);
         stamp(step, l, 0, 2);
-        if (!(ok = grid_sync())) break;
-        stamp(step, l, 0, 3);
       }
       // ---- attention (Q/K norm, RoPE, KV append, key-parallel splits) ----
-      {
+      if (attn_cta) {
+        consumer_sync();  // the attention scratch overlaps the staging area the QKV epilogue read
         AttnArgs at = a.at;
         at.g_q = static_cast<const float*>(lp[9]);
         at.g_k = static_cast<const float*>(lp[10]);
         at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         stamp(step, l, 1, 0);
-        if (c < a.n_kv * at.nsplit_max)
-          attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, 4>(at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid,
-                                                                    ConsumerSync{}, &s_last);
+        attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, 4, AttnLlIo>(
+            at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
+            AttnLlIo{a.ll_qkv, a.ll_attn, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV), mk_tag(a, step, l, 1),
+                     vabort, a.err});
         stamp(step, l, 1, 2);
-        if (!(ok = grid_sync())) break;
-        stamp(step, l, 1, 3);
+        consumer_sync();
       }
       // ---- O projection + residual ----
       {
         stamp(step, l, 2, 0);
         const MkStage sl = mk_bind(s_stage[MK_O], a.go, lp, a.embed);
-        stage_x(a.attn, nullptr, qw, nullptr, false);
+        if (sl.nloc > 0) stage_ll(a.ll_attn, mk_tag(a, step, l, 1), qw, nullptr);
         stamp(step, l, 2, 1);
         if (!(ok = consume(sl, a.go, qw))) break;
+        const uint32_t tg = mk_tag(a, step, l, MK_O);
         for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
           const int row = sl.u0 + lr;
-          a.h[row] = __ldcg(a.h + row) + row_value(a.go, lr);
+          const float prev = l == 0 ? load_f32<WT>(static_cast<const WT*>(a.embed) + static_cast<size_t>(tok) * a.H, row)
+                                    : hown[lr];
+          const float hn = prev + row_value(a.go, lr);
+          hown[lr] = hn;
+          ll_store(a.ll_h + row, hn, tg);
         }
         stamp(step, l, 2, 2);
-        if (!(ok = grid_sync())) break;
-        stamp(step, l, 2, 3);
       }
       // ---- gate/up with the post-attention RMSNorm, SwiGLU ----
       {
         stamp(step, l, 3, 0);
         const MkStage sl = mk_bind(s_stage[MK_GU], a.gg, lp, a.embed);
-        stage_x(a.h, nullptr, a.H, g_post, false);
+        if (sl.nloc > 0) stage_ll(a.ll_h, mk_tag(a, step, l, MK_O), a.H, g_post);
         stamp(step, l, 3, 1);
         if (!(ok = consume(sl, a.gg, a.H))) break;
         const int np = sl.nloc >> 1;
+        const uint32_t tg = mk_tag(a, step, l, MK_GU);
         for (int i = tid; i < np; i += kMkConsumers)
-          a.act[sl.u0 + i] = silu_f32(row_value(a.gg, i)) * row_value(a.gg, np + i);
+          ll_store(a.ll_act + sl.u0 + i, silu_f32(row_value(a.gg, i)) * row_value(a.gg, np + i), tg);
         stamp(step, l, 3, 2);
-        if (!(ok = grid_sync())) break;
-        stamp(step, l, 3, 3);
       }
       // ---- down projection + residual ----
       {
         stamp(step, l, 4, 0);
         const MkStage sl = mk_bind(s_stage[MK_DOWN], a.gd, lp, a.embed);
-        stage_x(a.act, nullptr, a.I, nullptr, false);
+        if (sl.nloc > 0) stage_ll(a.ll_act, mk_tag(a, step, l, MK_GU), a.I, nullptr);
         stamp(step, l, 4, 1);
         if (!(ok = consume(sl, a.gd, a.I))) break;
+        const uint32_t tg = mk_tag(a, step, l, MK_DOWN);
         for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
-          const int row = sl.u0 + lr;
-          a.h[row] = __ldcg(a.h + row) + row_value(a.gd, lr);
+          const float hn = hown[lr] + row_value(a.gd, lr);
+          hown[lr] = hn;
+          ll_store(a.ll_h + sl.u0 + lr, hn, tg);
         }
         stamp(step, l, 4, 2);
-        if (!(ok = grid_sync())) break;
-        stamp(step, l, 4, 3);
       }
+      consumer_sync();  // hown is rewritten by the next layer's O stage
     }
-    if (!ok || !mk_head_on(a, step)) continue;
+    (void)rH;
+    if (!ok || *vabort || !mk_head_on(a, step)) continue;
     // ---- head: final RMSNorm, tied vocabulary projection, two-pass argmax ----
     stamp(step, a.L, 0, 0);
     const MkStage sl = mk_bind(s_stage[MK_VOCAB], a.gv, layer_ptrs(0), a.embed);
-    stage_x(a.h, nullptr, a.H, a.g_final, false);
+    if (sl.nloc > 0) stage_ll(a.ll_h, mk_tag(a, step, a.L - 1, MK_DOWN), a.H, a.g_final);
     stamp(step, a.L, 0, 1);
     if (!(ok = consume(sl, a.gv, a.H))) break;
     stamp(step, a.L, 0, 2);
@@ -686,24 +823,15 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         }
         a.tok[pos + 1] = gi;
         *a.mcnt = 0u;
-        __threadfence();
+        ll_store_release(a.ll_tok, __int_as_float(gi), mk_tag(a, step, a.L, 0));
       }
     }
     stamp(step, a.L, 1, 0);
-    if (step + 1 < a.nsteps) ok = grid_sync();  // the next step reads the new token
+    consumer_sync();
   }
 
-  // ---- exit: the last CTA out resets the barrier counters and publishes the position ----
-  consumer_sync();
-  if (tid == 0) {
-    __threadfence();
-    if (atomicAdd(a.bar + 1, 1u) == static_cast<uint32_t>(G - 1)) {
-      a.bar[0] = 0u;
-      a.bar[1] = 0u;
-      a.ctrl[0] = a.pos0 + a.nsteps;
-      __threadfence();
-    }
-  }
+  // ---- exit: publish the position for the host-side mirror ----
+  if (tid == 0 && c == 0) a.ctrl[0] = a.pos0 + a.nsteps;
 }
 
 }  // namespace wsg

@@ -513,12 +513,38 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         if (gain) gn[k] = __ldg(gain + i);
       }
     }
+    // Poll in rounds: every round reloads all of this thread's words that do
+    // not yet carry the tag, together (one round trip per round).
+    {
+      const uint64_t t0 = globaltimer_ns();
+      for (int round = 0;; ++round) {
+        bool stale = false;
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const int i = tid + k * kMkConsumers;
+          if (i < in && static_cast<uint32_t>(wv[k] >> 32) != tag) stale = true;
+        }
+        if (!stale) break;
+        if ((round & 63) == 63) {
+          if (*vabort) break;
+          if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+            *vabort = 1;
+            atomicOr(a.err, ERR_EXCHANGE_TIMEOUT);
+            break;
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+          const int i = tid + k * kMkConsumers;
+          if (i < in && static_cast<uint32_t>(wv[k] >> 32) != tag) wv[k] = ll_load(src + i);
+        }
+      }
+    }
     float v[K];
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      const int i = tid + k * kMkConsumers;
-      v[k] = i < in ? ll_wait(src + i, tag, wv[k], vabort, a.err) : 0.f;
+      v[k] = __uint_as_float(static_cast<uint32_t>(wv[k]));
       ss = fmaf(v[k], v[k], ss);
     }
     float inv = 1.f;

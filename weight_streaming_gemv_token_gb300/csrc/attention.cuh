@@ -134,6 +134,16 @@ struct AttnPlainIo {
   const float* qkv;
   float* out;
   __device__ __forceinline__ float load_qkv(int i) const { return __ldcg(qkv + i); }
+  // q of this head group into qn[group*d], k and v of head g into kn[d], vn[d]
+  // (elements tid, tid + nt, ...).
+  __device__ __forceinline__ void load_all(float* qn, float* kn, float* vn, int qbase, int kbase, int vbase, int nq_el,
+                                           int d, int tid, int nt) const {
+    for (int i = tid; i < nq_el; i += nt) qn[i] = __ldcg(qkv + qbase + i);
+    for (int i = tid; i < d; i += nt) {
+      kn[i] = __ldcg(qkv + kbase + i);
+      vn[i] = __ldcg(qkv + vbase + i);
+    }
+  }
   __device__ __forceinline__ void acquire() const {}
   __device__ __forceinline__ void store_out(int i, float v) const { out[i] = v; }
   // Called by thread 0 after the CTA appended position pos of head g and synced.
@@ -162,11 +172,8 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
   const float* sn = a.rope_sin + static_cast<size_t>(pos) * (d >> 1);
   const int kraw = a.n_q * d + g * d;
   const int vraw = a.n_q * d + a.n_kv * d + g * d;
-  for (int i = tid; i < group * d; i += NT) qn[i] = io.load_qkv((g * group) * d + i);
-  for (int i = tid; i < d; i += NT) {
-    kn[i] = io.load_qkv(kraw + i);
-    vn[i] = round_store<KT>(io.load_qkv(vraw + i));
-  }
+  io.load_all(qn, kn, vn, (g * group) * d, kraw, vraw, group * d, d, tid, NT);
+  for (int i = tid; i < d; i += NT) vn[i] = round_store<KT>(vn[i]);
   io.acquire();
   sync();
   for (int h = warp; h <= group; h += kAttnWarps) {

@@ -311,6 +311,47 @@ struct AttnLlIo {
   volatile int* abort;
   uint32_t* err;
   __device__ __forceinline__ float load_qkv(int i) const { return ll_wait(qkv + i, tag_in, ll_load(qkv + i), abort, err); }
+  // All of this thread's q/k/v words requested together, then polled in rounds.
+  __device__ __forceinline__ void load_all(float* qn, float* kn, float* vn, int qbase, int kbase, int vbase, int nq_el,
+                                           int d, int tid, int nt) const {
+    constexpr int NQ = 4;  // q elements per thread: group * d <= 8 * 128 over 256 threads
+    uint64_t w[NQ + 2];
+    int at[NQ + 2];
+#pragma unroll
+    for (int k = 0; k < NQ; ++k) {
+      const int i = tid + k * nt;
+      at[k] = i < nq_el ? qbase + i : -1;
+    }
+    at[NQ] = tid < d ? kbase + tid : -1;
+    at[NQ + 1] = tid < d ? vbase + tid : -1;
+#pragma unroll
+    for (int k = 0; k < NQ + 2; ++k) w[k] = at[k] >= 0 ? ll_load(qkv + at[k]) : (static_cast<uint64_t>(tag_in) << 32);
+    const uint64_t t0 = globaltimer_ns();
+    for (int round = 0;; ++round) {
+      bool stale = false;
+#pragma unroll
+      for (int k = 0; k < NQ + 2; ++k) stale |= static_cast<uint32_t>(w[k] >> 32) != tag_in;
+      if (!stale) break;
+      if ((round & 63) == 63) {
+        if (*abort) break;
+        if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+          *abort = 1;
+          atomicOr(err, ERR_EXCHANGE_TIMEOUT);
+          break;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < NQ + 2; ++k)
+        if (static_cast<uint32_t>(w[k] >> 32) != tag_in) w[k] = ll_load(qkv + at[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < NQ; ++k)
+      if (at[k] >= 0) qn[tid + k * nt] = __uint_as_float(static_cast<uint32_t>(w[k]));
+    if (tid < d) {
+      kn[tid] = __uint_as_float(static_cast<uint32_t>(w[NQ]));
+      vn[tid] = __uint_as_float(static_cast<uint32_t>(w[NQ + 1]));
+    }
+  }
   __device__ __forceinline__ void acquire() const { fence_acq_rel_gpu(); }
   __device__ __forceinline__ void store_out(int i, float v) const { ll_store_release(out + i, v, tag_out); }
   __device__ __forceinline__ void publish_kv(int g, int pos) const {

@@ -182,7 +182,8 @@ int32_t dec_position(const dec_ctx* ctx);
  * layer are QKV, attention, O, gate/up, down; the extra layer index `layers`
  * holds the head (stage 0: vocabulary GEMV, stage 1 event 0: argmax done).
  * Events: 0 stage entry, 1 inputs received and staged (includes waiting
- * for the producing stage), 2 outputs published, 3 unused. After that block, [512][4] uint64
+ * for the producing stage), 2 outputs published, 3 unused (attention: key
+ * loop done). After that block, [512][4] uint64
  * SM clock stamps (clock64) of the first 512 weight segments consumed by
  * warp 0 of CTA 0: wait begins, data ready, dot reduced, next copy issued.
  * NULL turns tracing off. */

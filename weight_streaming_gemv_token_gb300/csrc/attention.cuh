@@ -75,9 +75,12 @@ __device__ __forceinline__ void store1<uint16_t>(void* base, size_t idx, float v
 }
 
 // RMSNorm over d elements held in shared memory, then RoPE at position pos,
-// in place; one warp.
+// in place; one warp. g, cs, sn: the gain and the cos/sin row, in shared memory.
+// With round_k the result is also rounded to the cache's element type (the
+// key is stored, and attended to, at that precision).
+template <typename KT>
 __device__ __forceinline__ void norm_rope_warp(float* v, const float* g, float eps, int d, const float* cs,
-                                               const float* sn, int lane) {
+                                               const float* sn, int lane, bool round_k) {
   float ss = 0.f;
   for (int e = lane; e < d; e += 32) ss = fmaf(v[e], v[e], ss);
   ss = warp_sum(ss);
@@ -87,8 +90,13 @@ __device__ __forceinline__ void norm_rope_warp(float* v, const float* g, float e
   const int half = d >> 1;
   for (int i = lane; i < half; i += 32) {
     const float a = v[i], b = v[i + half], c = cs[i], s = sn[i];
-    v[i] = a * c - b * s;
-    v[i + half] = a * s + b * c;
+    float lo = a * c - b * s, hi = a * s + b * c;
+    if (round_k) {
+      lo = round_store<KT>(lo);
+      hi = round_store<KT>(hi);
+    }
+    v[i] = lo;
+    v[i + half] = hi;
   }
   __syncwarp();
 }
@@ -101,9 +109,10 @@ struct CtaSync {  // barrier over the whole CTA
 constexpr int kAttnBatch = 8;  // keys loaded per warp per round trip
 
 inline size_t attn_smem_bytes(int group, int d) {
-  // qn[group][d], kn[d], vn[d], per-warp (m, l)[group] and o[group][d]
+  // qn[group][d], kn[d], vn[d], per-warp (m, l)[group] and o[group][d], then
+  // the tables gain_q[d], gain_k[d], cos[d/2], sin[d/2]
   return sizeof(float) * (static_cast<size_t>(group) * d + 2 * d + kAttnWarps * group * 2 +
-                          static_cast<size_t>(kAttnWarps) * group * d) +
+                          static_cast<size_t>(kAttnWarps) * group * d + 3 * static_cast<size_t>(d)) +
          16;
 }
 
@@ -123,17 +132,14 @@ __device__ __forceinline__ bool attn_split_range(const AttnArgs& a, int s, int p
   return true;
 }
 
-// Work of split s of key/value head g for the token at position pos, run by
-// NT threads (tid in [0, NT), NT a multiple of 32 and at least 8 warps' worth
-// of the warp-indexed work below) that sync() together. asmem: shared scratch
-// of attn_smem_bytes(); s_last: one shared int.
 // How the attention body reads the raw q/k/v projections and writes its
 // output: directly from / to the buffers of AttnArgs (kernel-boundary
-// ordering), or through another exchange (see the persistent kernel).
+// ordering; splits merged by the last CTA to finish), or through another
+// exchange (see the persistent kernel).
 struct AttnPlainIo {
+  static constexpr bool kPolledMerge = false;
   const float* qkv;
   float* out;
-  __device__ __forceinline__ float load_qkv(int i) const { return __ldcg(qkv + i); }
   // q of this head group into qn[group*d], k and v of head g into kn[d], vn[d]
   // (elements tid, tid + nt, ...).
   __device__ __forceinline__ void load_all(float* qn, float* kn, float* vn, int qbase, int kbase, int vbase, int nq_el,
@@ -144,10 +150,16 @@ struct AttnPlainIo {
       vn[i] = __ldcg(qkv + vbase + i);
     }
   }
-  __device__ __forceinline__ void acquire() const {}
   __device__ __forceinline__ void store_out(int i, float v) const { out[i] = v; }
-  // Called by thread 0 after the CTA appended position pos of head g and synced.
+  // Called by one thread, after a CTA barrier that follows the cache append
+  // of position pos of head g.
   __device__ __forceinline__ void publish_kv(int, int) const {}
+  // Trace hook (thread 0): 1 = current q/k/v received by the CTA, 3 = key loop done.
+  __device__ __forceinline__ void mark(int) const {}
+  // Polled split merge (unused here).
+  __device__ __forceinline__ void store_part(size_t, float) const {}
+  template <int KC>
+  __device__ __forceinline__ void poll_parts(size_t, size_t, int, int, int, float*, float*, float*) const {}
 };
 
 template <typename KT, int GMAX, int NT, typename Sync, int BATCH = kAttnBatch, typename Io = AttnPlainIo>
@@ -155,7 +167,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
                                                  Sync sync, int* s_last, Io io = Io{}) {
   static_assert(NT == kAttnWarps * 32, "the split layout assumes kAttnWarps warps");
   const int warp = tid >> 5, lane = tid & 31;
-  const int d = a.d, group = a.n_q / a.n_kv;
+  const int d = a.d, group = a.n_q / a.n_kv, half = d >> 1;
   const int n = pos + 1;
   int t0, t1, nsplit;
   if (!attn_split_range(a, s, pos, &t0, &t1, &nsplit)) return;
@@ -166,26 +178,56 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
   float* wm = vn + d;                      // [warps][group]
   float* wl = wm + kAttnWarps * group;     // [warps][group]
   float* wo = wl + kAttnWarps * group;     // [warps][group][d]
+  float* tab = wo + kAttnWarps * group * d;  // gain_q[d], gain_k[d], cos[d/2], sin[d/2]
 
-  // Current token: raw projections -> RMSNorm -> RoPE (q, k); v as is.
-  const float* cs = a.rope_cos + static_cast<size_t>(pos) * (d >> 1);
-  const float* sn = a.rope_sin + static_cast<size_t>(pos) * (d >> 1);
   const int kraw = a.n_q * d + g * d;
   const int vraw = a.n_q * d + a.n_kv * d + g * d;
+  // Each lane owns 4 consecutive elements [4 lane, 4 lane + 4) of a head vector;
+  // each warp takes a contiguous run of this CTA's keys, BATCH at a time, the
+  // next batch in flight while the current one is scored.
+  const bool active = 4 * lane < d;
+  const int per_w = (t1 - t0 + kAttnWarps - 1) / kAttnWarps;
+  const int w0 = t0 + warp * per_w;
+  const int w1 = min(t1, w0 + per_w);
+  const size_t head_base = static_cast<size_t>(g) * a.max_seq * d;
+  auto fetch = [&](int tb, float4* kk, float4* vv) {
+#pragma unroll
+    for (int u = 0; u < BATCH; ++u) {
+      const int t = tb + u;
+      kk[u] = vv[u] = make_float4(0, 0, 0, 0);
+      if (t < w1 && active && t != pos) {
+        kk[u] = load4<KT>(a.kc, head_base + static_cast<size_t>(t) * d + 4 * lane);
+        vv[u] = load4<KT>(a.vc, head_base + static_cast<size_t>(t) * d + 4 * lane);
+      }
+    }
+  };
+  // Nothing below depends on this token until its q/k/v arrive: the gains,
+  // the RoPE row and the first batch of cached keys/values are requested
+  // before waiting for them.
+  float tv[2];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int i = tid + k * NT;
+    const float* cs = a.rope_cos + static_cast<size_t>(pos) * half;
+    const float* sn = a.rope_sin + static_cast<size_t>(pos) * half;
+    tv[k] = i < d ? __ldg(a.g_q + i)
+                  : i < 2 * d ? __ldg(a.g_k + i - d)
+                              : i < 2 * d + half ? __ldg(cs + i - 2 * d) : i < 3 * d ? __ldg(sn + i - 2 * d - half) : 0.f;
+  }
+  float4 nk[BATCH], nv[BATCH];
+  fetch(w0, nk, nv);
   io.load_all(qn, kn, vn, (g * group) * d, kraw, vraw, group * d, d, tid, NT);
   for (int i = tid; i < d; i += NT) vn[i] = round_store<KT>(vn[i]);
-  io.acquire();
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+    if (tid + k * NT < 3 * d) tab[tid + k * NT] = tv[k];
   sync();
-  for (int h = warp; h <= group; h += kAttnWarps) {
-    if (h < group)
-      norm_rope_warp(qn + h * d, a.g_q, a.eps, d, cs, sn, lane);
-    else
-      norm_rope_warp(kn, a.g_k, a.eps, d, cs, sn, lane);
-  }
+  if (tid == 0) io.mark(1);
+  // Current token: RMSNorm -> RoPE of each q head and of k (k rounded to the cache type).
+  for (int h = warp; h <= group; h += kAttnWarps)
+    norm_rope_warp<KT>(h < group ? qn + h * d : kn, h < group ? tab : tab + d, a.eps, d, tab + 2 * d, tab + 2 * d + half,
+                       lane, h == group);
   sync();
-  for (int i = tid; i < d; i += NT) kn[i] = round_store<KT>(kn[i]);
-  sync();
-  const size_t head_base = static_cast<size_t>(g) * a.max_seq * d;
   if (t1 == n) {  // this CTA's range holds the current position: append to the cache
     for (int i = tid; i < d; i += NT) {
       store1<KT>(a.kc, head_base + static_cast<size_t>(pos) * d + i, kn[i]);
@@ -193,8 +235,6 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     }
   }
 
-  // Each lane owns 4 consecutive elements [4 lane, 4 lane + 4) of a head vector.
-  const bool active = 4 * lane < d;
   float4 q[GMAX];
 #pragma unroll
   for (int h = 0; h < GMAX; ++h)
@@ -208,27 +248,18 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     o[h] = make_float4(0, 0, 0, 0);
   }
 
-  // Each warp takes a contiguous run of this CTA's keys and loads BATCH of
-  // them at a time, so one memory round trip covers the whole batch.
-  const int per_w = (t1 - t0 + kAttnWarps - 1) / kAttnWarps;
-  const int w0 = t0 + warp * per_w;
-  const int w1 = min(t1, w0 + per_w);
   for (int tb = w0; tb < w1; tb += BATCH) {
     float4 kk[BATCH], vv[BATCH];
 #pragma unroll
     for (int u = 0; u < BATCH; ++u) {
-      const int t = tb + u;
-      kk[u] = vv[u] = make_float4(0, 0, 0, 0);
-      if (t < w1 && active) {
-        if (t == pos) {
-          kk[u] = *reinterpret_cast<const float4*>(kn + 4 * lane);
-          vv[u] = *reinterpret_cast<const float4*>(vn + 4 * lane);
-        } else {
-          kk[u] = load4<KT>(a.kc, head_base + static_cast<size_t>(t) * d + 4 * lane);
-          vv[u] = load4<KT>(a.vc, head_base + static_cast<size_t>(t) * d + 4 * lane);
-        }
+      kk[u] = nk[u];
+      vv[u] = nv[u];
+      if (tb + u == pos && tb + u < w1 && active) {  // the current token: from shared memory
+        kk[u] = *reinterpret_cast<const float4*>(kn + 4 * lane);
+        vv[u] = *reinterpret_cast<const float4*>(vn + 4 * lane);
       }
     }
+    if (tb + BATCH < w1) fetch(tb + BATCH, nk, nv);
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
       if (h >= group) break;
@@ -259,6 +290,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     }
   }
 
+  if (tid == 0) io.mark(3);
   // Merge the warps of this CTA.
 #pragma unroll
   for (int h = 0; h < GMAX; ++h) {
@@ -270,7 +302,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     if (active) *reinterpret_cast<float4*>(wo + (warp * group + h) * d + 4 * lane) = o[h];
   }
   sync();
-  if (tid == 0 && t1 == n) io.publish_kv(g, pos);
+  const bool merger = Io::kPolledMerge && nsplit > 1 && s == 0;
   for (int idx = tid; idx < group * d; idx += NT) {
     const int h = idx / d, e = idx - h * d;
     float M = -INFINITY;
@@ -281,10 +313,40 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
       L += wl[w * group + h] * f;
       O += wo[(w * group + h) * d + e] * f;
     }
+    const size_t pbase = ((static_cast<size_t>(g) * a.nsplit_max) * group + h) * (d + 2);  // split 0 of (g, h)
+    const size_t pstride = static_cast<size_t>(group) * (d + 2);                       // next split
     if (nsplit == 1) {
       io.store_out((g * group + h) * d + e, O / L);
+    } else if constexpr (Io::kPolledMerge) {
+      if (!merger) {
+        // (O, M, L) of this split as exchange words; split 0 merges them
+        const size_t pb = pbase + s * pstride;
+        io.store_part(pb + e, O);
+        if (e == 0) {
+          io.store_part(pb + d, M);
+          io.store_part(pb + d + 1, L);
+        }
+      } else {
+        // split 0: fold in the other splits in order, a few at a time (their
+        // words requested together, then polled)
+        constexpr int KC = 4;
+        for (int k0 = 1; k0 < nsplit; k0 += KC) {
+          float ov[KC], mv[KC], lv[KC];
+          io.template poll_parts<KC>(pbase + k0 * pstride, pstride, min(KC, nsplit - k0), e, d, ov, mv, lv);
+#pragma unroll
+          for (int k = 0; k < KC; ++k) {
+            if (k0 + k >= nsplit) break;
+            const float Mn = fmaxf(M, mv[k]);
+            const float fa = expf(M - Mn), fb = expf(mv[k] - Mn);
+            L = L * fa + lv[k] * fb;
+            O = O * fa + ov[k] * fb;
+            M = Mn;
+          }
+        }
+        io.store_out((g * group + h) * d + e, O / L);
+      }
     } else {
-      float* p = a.part + ((static_cast<size_t>(g) * a.nsplit_max + s) * group + h) * (d + 2);
+      float* p = a.part + pbase + s * pstride;
       p[e] = O;
       if (e == 0) {
         p[d] = M;
@@ -292,7 +354,9 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
       }
     }
   }
-  if (nsplit == 1) return;
+  // The appended row was written before the barrier above.
+  if (tid == NT - 1 && t1 == n) io.publish_kv(g, pos);
+  if (nsplit == 1 || Io::kPolledMerge) return;
 
   // Split merge: the last CTA of this key/value head to finish combines all splits.
   __threadfence();
@@ -331,7 +395,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, ERR_BAD_POSITION);
     return;
   }
-  attn_decode_body<KT, GMAX, kAttnWarps * 32>(a, blockIdx.x, blockIdx.y, pos, asmem, threadIdx.x, CtaSync{}, &s_last,
+  attn_decode_body<KT, GMAX, kAttnWarps * 32, CtaSync, GMAX <= 2 ? kAttnBatch : kAttnBatch / 2>(a, blockIdx.x, blockIdx.y, pos, asmem, threadIdx.x, CtaSync{}, &s_last,
                                               AttnPlainIo{a.qkv, a.out});
 }
 

@@ -48,7 +48,7 @@ size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
 
 struct Layout {
   size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn, ll_act,
-      ll_tok, kv_ready, mk_layers, rope_cos, rope_sin, kc, vc;
+      ll_tok, ll_apart, kv_ready, mk_layers, rope_cos, rope_sin, kc, vc;
   size_t total;
 };
 
@@ -103,6 +103,7 @@ Layout make_layout(const dec_config& c) {
   L.ll_attn = take(qw * 8);
   L.ll_act = take(static_cast<size_t>(c.inter) * 8);
   L.ll_tok = take(8);
+  L.ll_apart = take(static_cast<size_t>(c.n_kv) * kSplitMax * group * (c.head_dim + 2) * 8);
   L.kv_ready = take(static_cast<size_t>(c.layers) * c.n_kv * 4);
   L.mk_layers = take(static_cast<size_t>(c.layers) * sizeof(MkLayer));
   L.rope_cos = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
@@ -430,6 +431,7 @@ dec_status plan_persistent(dec_ctx* c) {
   a.ll_attn = c->at<uint64_t>(c->L.ll_attn);
   a.ll_act = c->at<uint64_t>(c->L.ll_act);
   a.ll_tok = c->at<uint64_t>(c->L.ll_tok);
+  a.ll_apart = c->at<uint64_t>(c->L.ll_apart);
   a.kv_ready = c->at<uint32_t>(c->L.kv_ready);
   a.layers = c->at<MkLayer>(c->L.mk_layers);
   AttnArgs& at = a.at;

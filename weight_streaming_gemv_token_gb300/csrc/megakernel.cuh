@@ -91,6 +91,7 @@ struct MkArgs {
   uint64_t* ll_attn;  // attention output [n_q d]
   uint64_t* ll_act;   // SwiGLU activations [I]
   uint64_t* ll_tok;   // next token [1]
+  uint64_t* ll_apart; // attention split partials [n_kv][nsplit_max][group][d + 2]
   uint32_t* kv_ready; // [L][n_kv]: positions appended to the cache (release-stored)
   uint32_t epoch;     // per-launch tag prefix (nonzero; 12 bits)
   AttnArgs at;        // kc / vc point at layer 0's cache
@@ -303,34 +304,34 @@ __device__ __forceinline__ float ll_wait(const uint64_t* p, uint32_t tag, uint64
 
 // Attention input/output through the exchange words; the cache rows this CTA
 // appends are published with a release store of the per-head position count.
+// Splits of one head hand their partial (O, M, L) to split 0 as exchange words.
 struct AttnLlIo {
+  static constexpr bool kPolledMerge = true;
   const uint64_t* qkv;
   uint64_t* out;
+  uint64_t* part;      // [n_kv][nsplit_max][group][d + 2] partial words
   uint32_t* kv_ready;  // this layer's [n_kv]
   uint32_t tag_in, tag_out;
   volatile int* abort;
   uint32_t* err;
-  __device__ __forceinline__ float load_qkv(int i) const { return ll_wait(qkv + i, tag_in, ll_load(qkv + i), abort, err); }
-  // All of this thread's q/k/v words requested together, then polled in rounds.
-  __device__ __forceinline__ void load_all(float* qn, float* kn, float* vn, int qbase, int kbase, int vbase, int nq_el,
-                                           int d, int tid, int nt) const {
-    constexpr int NQ = 4;  // q elements per thread: group * d <= 8 * 128 over 256 threads
-    uint64_t w[NQ + 2];
-    int at[NQ + 2];
+  uint64_t* trace_slot;  // this CTA's [4] stamps of the stage, or NULL
+  __device__ __forceinline__ void mark(int ev) const {
+    if (trace_slot) trace_slot[ev] = globaltimer_ns();
+  }
+  // Poll the N words addr(0..N) (nullptr: none) until each carries `tag`;
+  // all stale words are reloaded together, one round trip per round.
+  template <int N, typename Addr>
+  __device__ __forceinline__ void poll(Addr addr, uint32_t tag, uint64_t* w) const {
 #pragma unroll
-    for (int k = 0; k < NQ; ++k) {
-      const int i = tid + k * nt;
-      at[k] = i < nq_el ? qbase + i : -1;
+    for (int k = 0; k < N; ++k) {
+      const uint64_t* p = addr(k);
+      w[k] = p ? ll_load(p) : (static_cast<uint64_t>(tag) << 32);
     }
-    at[NQ] = tid < d ? kbase + tid : -1;
-    at[NQ + 1] = tid < d ? vbase + tid : -1;
-#pragma unroll
-    for (int k = 0; k < NQ + 2; ++k) w[k] = at[k] >= 0 ? ll_load(qkv + at[k]) : (static_cast<uint64_t>(tag_in) << 32);
     const uint64_t t0 = globaltimer_ns();
     for (int round = 0;; ++round) {
       bool stale = false;
 #pragma unroll
-      for (int k = 0; k < NQ + 2; ++k) stale |= static_cast<uint32_t>(w[k] >> 32) != tag_in;
+      for (int k = 0; k < N; ++k) stale |= static_cast<uint32_t>(w[k] >> 32) != tag;
       if (!stale) break;
       if ((round & 63) == 63) {
         if (*abort) break;
@@ -341,19 +342,50 @@ struct AttnLlIo {
         }
       }
 #pragma unroll
-      for (int k = 0; k < NQ + 2; ++k)
-        if (static_cast<uint32_t>(w[k] >> 32) != tag_in) w[k] = ll_load(qkv + at[k]);
+      for (int k = 0; k < N; ++k)
+        if (static_cast<uint32_t>(w[k] >> 32) != tag) w[k] = ll_load(addr(k));
     }
+  }
+  // q of the head group, k and v of head g.
+  __device__ __forceinline__ void load_all(float* qn, float* kn, float* vn, int qbase, int kbase, int vbase, int nq_el,
+                                           int d, int tid, int nt) const {
+    constexpr int NQ = 4;  // q elements per thread: group * d <= 8 * 128 over 256 threads
+    uint64_t w[NQ + 2];
+    poll<NQ + 2>(
+        [&](int k) -> const uint64_t* {
+          if (k < NQ) return tid + k * nt < nq_el ? qkv + qbase + tid + k * nt : nullptr;
+          return tid < d ? qkv + (k == NQ ? kbase : vbase) + tid : nullptr;
+        },
+        tag_in, w);
 #pragma unroll
     for (int k = 0; k < NQ; ++k)
-      if (at[k] >= 0) qn[tid + k * nt] = __uint_as_float(static_cast<uint32_t>(w[k]));
+      if (tid + k * nt < nq_el) qn[tid + k * nt] = __uint_as_float(static_cast<uint32_t>(w[k]));
     if (tid < d) {
       kn[tid] = __uint_as_float(static_cast<uint32_t>(w[NQ]));
       vn[tid] = __uint_as_float(static_cast<uint32_t>(w[NQ + 1]));
     }
   }
-  __device__ __forceinline__ void acquire() const { fence_acq_rel_gpu(); }
-  __device__ __forceinline__ void store_out(int i, float v) const { ll_store_release(out + i, v, tag_out); }
+  __device__ __forceinline__ void store_out(int i, float v) const { ll_store(out + i, v, tag_out); }
+  __device__ __forceinline__ void store_part(size_t i, float v) const { ll_store(part + i, v, tag_out); }
+  // Splits k < cnt at base + k * stride: element e of O, then M and L.
+  template <int KC>
+  __device__ __forceinline__ void poll_parts(size_t base, size_t stride, int cnt, int e, int d, float* ov, float* mv,
+                                             float* lv) const {
+    uint64_t w[3 * KC];
+    const uint64_t* p0 = part + base;
+    poll<3 * KC>(
+        [&](int j) -> const uint64_t* {
+          const int k = j / 3, r = j - 3 * k;
+          return k < cnt ? p0 + k * stride + (r == 0 ? e : d + r - 1) : nullptr;
+        },
+        tag_out, w);
+#pragma unroll
+    for (int k = 0; k < KC; ++k) {
+      ov[k] = __uint_as_float(static_cast<uint32_t>(w[3 * k]));
+      mv[k] = __uint_as_float(static_cast<uint32_t>(w[3 * k + 1]));
+      lv[k] = __uint_as_float(static_cast<uint32_t>(w[3 * k + 2]));
+    }
+  }
   __device__ __forceinline__ void publish_kv(int g, int pos) const {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(kv_ready + g), "r"(static_cast<uint32_t>(pos + 1))
                  : "memory");
@@ -774,10 +806,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         stamp(step, l, 1, 0);
-        attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, 4, AttnLlIo>(
+        attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? 4 : 2), AttnLlIo>(
             at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
-            AttnLlIo{a.ll_qkv, a.ll_attn, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV), mk_tag(a, step, l, 1),
-                     vabort, a.err});
+            AttnLlIo{a.ll_qkv, a.ll_attn, a.ll_apart, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV),
+                     mk_tag(a, step, l, 1),
+                     vabort, a.err,
+                     (a.trace && step == 0)
+                         ? a.trace + ((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + 1) * kMkTraceEvents
+                         : nullptr});
         stamp(step, l, 1, 2);
         consumer_sync();
       }

@@ -18,9 +18,13 @@
 // replays for every step. Kernels after the first carry a programmatic
 // dependent-launch edge: each GEMV starts streaming its weights while its
 // predecessor finishes, and waits only before reading activations.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <mutex>
 #include <vector>
 
 #include "attention.cuh"
@@ -48,7 +52,7 @@ size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
 
 struct Layout {
   size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn, ll_act,
-      ll_tok, ll_apart, kv_ready, mk_layers, rope_cos, rope_sin, kc, vc;
+      ll_tok, ll_apart, kv_ready, mk_layers, mk_maps, rope_cos, rope_sin, kc, vc;
   size_t total;
 };
 
@@ -106,6 +110,7 @@ Layout make_layout(const dec_config& c) {
   L.ll_apart = take(static_cast<size_t>(c.n_kv) * kSplitMax * group * (c.head_dim + 2) * 8);
   L.kv_ready = take(static_cast<size_t>(c.layers) * c.n_kv * 4);
   L.mk_layers = take(static_cast<size_t>(c.layers) * sizeof(MkLayer));
+  L.mk_maps = take((static_cast<size_t>(c.layers) * kMkMapsPerLayer + 1) * kMkMapBytes);
   L.rope_cos = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   L.rope_sin = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   const size_t cache = static_cast<size_t>(c.layers) * kvw * c.max_seq * dtype_bytes(c.kvdtype);
@@ -343,20 +348,114 @@ dec_status enqueue_step_t(dec_ctx* c, cudaStream_t st, bool full) {
 
 // ---- persistent engine ----
 
-MkGeom mk_geom_for(int in, int elem) {
-  MkGeom g{};
-  g.row_bytes = in * elem;
-  if (g.row_bytes > kMkSlot) {
-    g.spr = (g.row_bytes + kMkSlot - 1) / kMkSlot;
-    g.seg_bytes = ((g.row_bytes + g.spr - 1) / g.spr + 15) / 16 * 16;
-    g.spr = (g.row_bytes + g.seg_bytes - 1) / g.seg_bytes;
-    g.rps = 1;
+// Rows of each piece of stage st for CTA c of G (the kernel's partition,
+// mirrored on the host to plan box heights and partial capacity).
+void mk_pieces(const dec_config& g, int st, int c, int G, int nr[3]) {
+  const long long qw = static_cast<long long>(g.n_q) * g.head_dim, kvw = static_cast<long long>(g.n_kv) * g.head_dim;
+  const long long units = st == MK_QKV ? qw + 2 * kvw : st == MK_GU ? g.inter : st == MK_VOCAB ? g.vocab : g.hidden;
+  const long long u0 = c * units / G, u1 = (c + 1) * units / G;
+  nr[0] = nr[1] = nr[2] = 0;
+  if (st == MK_QKV) {
+    auto clampr = [](long long x, long long lo, long long hi) { return std::min(std::max(x, lo), hi); };
+    nr[0] = static_cast<int>(clampr(u1, 0, qw) - clampr(u0, 0, qw));
+    nr[1] = static_cast<int>(clampr(u1, qw, qw + kvw) - clampr(u0, qw, qw + kvw));
+    nr[2] = static_cast<int>(std::max(u1, qw + kvw) - std::max(u0, qw + kvw));
+  } else if (st == MK_GU) {
+    nr[0] = nr[1] = static_cast<int>(u1 - u0);
   } else {
-    g.spr = 1;
-    g.seg_bytes = g.row_bytes;
-    g.rps = kMkSlot / g.row_bytes;
+    nr[0] = static_cast<int>(u1 - u0);
   }
-  return g;
+}
+
+// Split-K geometry of stage st (input width `in`): 8 column parts (16 when a
+// part would exceed 256 columns, the TMA box limit), each 16-byte aligned;
+// R rows per box chosen to minimise the busiest CTA's streamed bytes plus a
+// fixed cost per box (a copy of a few KB runs below the streaming rate of
+// larger ones); boxes fit one ring slot.
+MkGeom mk_geom_for(const dec_config& g, int st, int in, int elem, int G) {
+  MkGeom m{};
+  const int align = 16 / elem;
+  auto width = [&](int parts) {
+    const int cw = (in + parts - 1) / parts;
+    return (cw + align - 1) / align * align;
+  };
+  m.pw = 1;
+  m.cw = width(kMkWarps);
+  if (m.cw > 256) {
+    m.pw = 2;
+    m.cw = width(2 * kMkWarps);
+  }
+  m.kc = (m.cw + 127) / 128;
+  // rows per box: the consumer holds at most 16 (f32) / 32 (bf16) 4-element
+  // weight groups per lane, i.e. that many rows of a one-chunk part
+  const int rmax = std::min((elem == 4 ? 16 : 32) / m.kc, kMkSlot / (m.cw * elem));
+  constexpr long long kBoxCost = 2048;
+  long long best = -1;
+  for (int R = 1; R <= rmax; ++R) {
+    long long worst = 0;
+    for (int c = 0; c < G; ++c) {
+      int nr[3];
+      mk_pieces(g, st, c, G, nr);
+      long long cost = 0;
+      for (int p = 0; p < 3; ++p)
+        cost += static_cast<long long>((nr[p] + R - 1) / R) * (static_cast<long long>(R) * m.cw * elem + kBoxCost);
+      worst = std::max(worst, cost);
+    }
+    if (best < 0 || worst <= best) {
+      best = worst;
+      m.R = R;
+    }
+  }
+  m.box_bytes = m.R * m.cw * elem;
+  return m;
+}
+
+// Most row groups x R over the CTAs (shared partial rows the stage needs in one chunk).
+int mk_group_rows(const dec_config& g, int st, const MkGeom& m, int G) {
+  int most = 0;
+  for (int c = 0; c < G; ++c) {
+    int nr[3];
+    mk_pieces(g, st, c, G, nr);
+    int ng = 0;
+    for (int p = 0; p < 3; ++p) ng += (nr[p] + m.R - 1) / m.R;
+    most = std::max(most, ng * m.R);
+  }
+  return most;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Tensor map of a row-major [rows][in] weight matrix with boxes of m.R rows x m.cw columns.
+dec_status encode_map(CUtensorMap* out, const void* base, int rows, int in, int wdtype, const MkGeom& m,
+                      std::string* err) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(err, DEC_ECUDA, "cuTensorMapEncodeTiled is not available");
+  const int elem = static_cast<int>(dtype_bytes(wdtype));
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(in), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(in) * elem};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(m.cw), static_cast<cuuint32_t>(m.R)};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r =
+      enc(out, wdtype == DEC_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(err, DEC_EINVAL, "cuTensorMapEncodeTiled failed (%d) for a %d x %d matrix, box %d x %d", static_cast<int>(r),
+                rows, in, m.R, m.cw);
+  return DEC_OK;
 }
 
 // Persistent kernel instance for the configuration (defined per weight dtype in
@@ -382,32 +481,37 @@ dec_status plan_persistent(dec_ctx* c) {
   a.d = g.head_dim;
   a.V = g.vocab;
   a.eps = g.eps;
-  a.gq = mk_geom_for(g.hidden, elem);
-  a.go = mk_geom_for(qw, elem);
-  a.gg = mk_geom_for(g.hidden, elem);
-  a.gd = mk_geom_for(g.inter, elem);
-  a.gv = mk_geom_for(g.hidden, elem);
-  auto cdiv = [](long long x, long long y) { return static_cast<int>((x + y - 1) / y); };
-  int part = cdiv(qw + 2 * kvw, G) * a.gq.spr;
-  part = std::max(part, cdiv(g.hidden, G) * a.go.spr);
-  part = std::max(part, 2 * cdiv(g.inter, G) * a.gg.spr);
-  part = std::max(part, cdiv(g.hidden, G) * a.gd.spr);
-  part = std::max(part, cdiv(g.vocab, G) * a.gv.spr);
   if (std::max(g.hidden, std::max(qw, g.inter)) > kMkMaxWidth)
     return fail(&c->err, DEC_EINVAL, "persistent engine: widths above %d need the staged engine", kMkMaxWidth);
-  a.xs_floats = (std::max(g.hidden, std::max(qw, g.inter)) + 3) / 4 * 4;
-  a.part_floats = (part + 3) / 4 * 4;
+  a.gq = mk_geom_for(g, MK_QKV, g.hidden, elem, G);
+  a.go = mk_geom_for(g, MK_O, qw, elem, G);
+  a.gg = mk_geom_for(g, MK_GU, g.hidden, elem, G);
+  a.gd = mk_geom_for(g, MK_DOWN, g.inter, elem, G);
+  a.gv = mk_geom_for(g, MK_VOCAB, g.hidden, elem, G);
+  (void)kvw;
+  auto cdiv = [](long long x, long long y) { return static_cast<int>((x + y - 1) / y); };
+  // Shared partials: every layer stage in one chunk; the vocabulary in chunks.
+  int prows = kMkPartRows;
+  prows = std::max(prows, mk_group_rows(g, MK_QKV, a.gq, G));
+  prows = std::max(prows, mk_group_rows(g, MK_O, a.go, G));
+  prows = std::max(prows, mk_group_rows(g, MK_GU, a.gg, G));
+  prows = std::max(prows, mk_group_rows(g, MK_DOWN, a.gd, G));
+  for (MkGeom* m : {&a.gq, &a.go, &a.gg, &a.gd, &a.gv}) m->gchunk = std::max(1, prows / m->R);
+  a.part_floats = prows * kMkWarps;
+  // staging of one activation vector; the attention scratch shares it
+  a.xs_floats = std::max(static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 15) / 16 * 4),
+                         (std::max(g.hidden, std::max(qw, g.inter)) + 3) / 4 * 4);
   a.hown_floats = (cdiv(g.hidden, G) + 3) / 4 * 4;
-  const int attn_floats = static_cast<int>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 3) / 4);
-  if (a.xs_floats + a.part_floats < attn_floats) a.part_floats = (attn_floats - a.xs_floats + 3) / 4 * 4;
-  const size_t fixed = 2 * kMkWarps * kMkWarpSlotsMax * sizeof(uint64_t) + 4 * static_cast<size_t>(a.xs_floats + a.part_floats) +
+  const size_t fixed = 2 * kMkWarps * kMkQ * sizeof(uint64_t) +  // full and empty barriers
+                       4 * static_cast<size_t>(a.xs_floats + a.part_floats) +
                        static_cast<size_t>(g.layers) * kMkLayerPtrs * sizeof(void*) + 4 * static_cast<size_t>(a.hown_floats);
   const size_t static_smem = 64 * 4 + 32 * 4 + 8 + 5 * sizeof(MkStageT) + 256;
-  const size_t per_slot = static_cast<size_t>(kMkWarps) * kMkSlot;  // one slot in every warp's ring
-  if (fixed + static_smem + per_slot > c->di.smem_optin)
+  if (fixed + static_smem + static_cast<size_t>(kMkWarps) * kMkSlot > c->di.smem_optin)
     return fail(&c->err, DEC_EINVAL, "persistent engine: staging needs %zu B of shared memory", fixed);
-  a.wslots = static_cast<int>(std::min<size_t>(kMkWarpSlotsMax, (c->di.smem_optin - fixed - static_smem) / per_slot));
-  c->mk_smem = static_cast<size_t>(a.wslots) * per_slot + fixed;
+  // every warp's ring: what is left, in 128-byte units, at most 8 slots' worth
+  const size_t ring = std::min<size_t>(8 * kMkSlot, (c->di.smem_optin - fixed - static_smem) / kMkWarps / 128 * 128);
+  a.ring_bytes = static_cast<int>(ring);
+  c->mk_smem = static_cast<size_t>(kMkWarps) * ring + fixed;
   c->mk_grid = G;
   void* k = mk_kernel(g);
   WSG_CUDA_TRY(&c->err, cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -415,6 +519,14 @@ dec_status plan_persistent(dec_ctx* c) {
   int per_sm = 0;
   WSG_CUDA_TRY(&c->err, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kMkThreads, c->mk_smem));
   if (per_sm < 1) return fail(&c->err, DEC_EINVAL, "persistent engine: kernel does not fit on an SM");
+  // The warpgroups re-split the registers the block is launched with
+  // (setmaxnreg); the new split must fit in them, or the raise would wait forever.
+  cudaFuncAttributes fa{};
+  WSG_CUDA_TRY(&c->err, cudaFuncGetAttributes(&fa, k));
+  if (static_cast<long long>(fa.numRegs) * kMkThreads <
+      static_cast<long long>(kMkConsumerRegs) * kMkConsumers + static_cast<long long>(kMkProducerRegs) * 128)
+    return fail(&c->err, DEC_EINVAL, "persistent engine: launched with %d registers per thread, too few for the split",
+                fa.numRegs);
   a.h = c->at<float>(c->L.h);
   a.qkv = c->at<float>(c->L.qkv);
   a.attn = c->at<float>(c->L.attn);
@@ -434,6 +546,7 @@ dec_status plan_persistent(dec_ctx* c) {
   a.ll_apart = c->at<uint64_t>(c->L.ll_apart);
   a.kv_ready = c->at<uint32_t>(c->L.kv_ready);
   a.layers = c->at<MkLayer>(c->L.mk_layers);
+  a.maps = c->ws + c->L.mk_maps;
   AttnArgs& at = a.at;
   at.qkv = a.qkv;
   at.eps = g.eps;
@@ -643,6 +756,34 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
   }
   WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->ws + c->L.mk_layers, tab.data(), tab.size() * sizeof(MkLayer),
                                         cudaMemcpyHostToDevice, c->stream));
+  std::vector<CUtensorMap> maps;
+  if (c->cfg.engine == DEC_ENGINE_PERSISTENT) {
+    // Tiled-copy descriptors of every weight matrix for the persistent engine.
+    const dec_config& g = c->cfg;
+    const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;
+    maps.resize(static_cast<size_t>(g.layers) * kMkMapsPerLayer + 1);
+    for (int l = 0; l < g.layers; ++l) {
+      const dec_layer_weights& x = c->layers[l];
+      CUtensorMap* m = maps.data() + static_cast<size_t>(l) * kMkMapsPerLayer;
+      const struct {
+        const void* p;
+        int rows, in;
+        const MkGeom* gm;
+      } t[kMkMapsPerLayer] = {{x.w_q, qw, g.hidden, &c->mk.gq},     {x.w_k, kvw, g.hidden, &c->mk.gq},
+                              {x.w_v, kvw, g.hidden, &c->mk.gq},    {x.w_o, g.hidden, qw, &c->mk.go},
+                              {x.w_gate, g.inter, g.hidden, &c->mk.gg}, {x.w_up, g.inter, g.hidden, &c->mk.gg},
+                              {x.w_down, g.hidden, g.inter, &c->mk.gd}};
+      for (int k = 0; k < kMkMapsPerLayer; ++k) {
+        const dec_status st = encode_map(m + k, t[k].p, t[k].rows, t[k].in, g.wdtype, *t[k].gm, &c->err);
+        if (st != DEC_OK) return st;
+      }
+    }
+    const dec_status st = encode_map(maps.data() + maps.size() - 1, c->w.embed, g.vocab, g.hidden, g.wdtype, c->mk.gv, &c->err);
+    if (st != DEC_OK) return st;
+    static_assert(sizeof(CUtensorMap) == kMkMapBytes, "tensor map size");
+    WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->ws + c->L.mk_maps, maps.data(), maps.size() * sizeof(CUtensorMap),
+                                          cudaMemcpyHostToDevice, c->stream));
+  }
   WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
   // Graphs bake in the weight pointers: drop any captured with older ones.
   if (c->g_full) cudaGraphExecDestroy(c->g_full);

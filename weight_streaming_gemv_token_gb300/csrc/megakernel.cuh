@@ -6,29 +6,42 @@
 // 227 ordered dispatches. This kernel keeps the whole GPU busy inside one
 // launch: one CTA per SM, co-resident by cooperative launch.
 //
-//  * Every weight segment (at most 8 KB) this CTA will read, over all stages
-//    of all requested steps (QKV, O, gate/up, down of every layer, then the
-//    vocabulary slice), is assigned to one of its 8 consumer warps: segment j
-//    of a stage goes to warp j mod 8. Each consumer warp owns a private ring
-//    of shared-memory slots. Lane w of a ninth, producer warp walks a cursor
-//    through consumer w's future segments (across stage, layer and step
-//    boundaries) and issues a bulk copy into ring w whenever a slot is free
-//    (full/empty mbarrier pair per slot). Weights never depend on
+//  * GEMV stages (QKV, O, gate/up, down of every layer, then the vocabulary
+//    slice) give each CTA a contiguous range of output rows and split every
+//    row's columns across the CTA's 8 consumer warps (split-K): warp w owns
+//    the column parts w (and w + 8) of every row, holds the matching
+//    activation elements in registers for the whole stage, and reads only
+//    weights from shared memory. All warps get the same work, whatever the
+//    row count.
+//  * Weights arrive as tiled TMA boxes (R rows x one column part) through a
+//    private byte ring per consumer warp. Lane w of a producer warp walks a
+//    cursor through consumer w's future boxes (across stage, layer and step
+//    boundaries) and issues each box as soon as the ring has room for it
+//    (full/empty mbarrier per box in flight; a box never straddles the ring's
+//    end). The consumer derives each box's ring offset from the same
+//    placement rule, so no offsets are exchanged. Weights never depend on
 //    activations, so the rings hold the next stages' weights while the
-//    consumers wait at a barrier, and HBM keeps streaming.
-//  * Per stage the CTA stages the activation vector (with the fused RMSNorm),
-//    each warp reduces its segments to partial dots, the partials are summed
-//    in a fixed order and the fused epilogue writes the outputs. Stages hand
-//    data to each other through exchange words: 64-bit (tag, value) pairs
-//    written in one store. A reader polls the words it needs until they carry
-//    the tag of the producing stage, so readiness and data arrive together
-//    and no grid-wide barrier is needed. Each buffer's next version can only
-//    be written after every reader of the current version has read it (the
-//    forward's own data dependencies order them), and a CTA with no rows in a
-//    stage reads nothing for it.
+//    consumers wait for their inputs, and HBM keeps streaming. The producer
+//    sits in a warpgroup of its own that gives registers back (setmaxnreg),
+//    so the consumer warps run with 224 registers per thread; a tiled copy
+//    that waits for room in the copy engine never stalls a consumer.
+//  * Per box, every lane accumulates its column chunk into one partial per
+//    row; a butterfly reduce-scatter turns the R lane partials into row sums
+//    (16 or 32 rows in log2(32) shuffle steps), the 8 warp partials of a row
+//    meet in shared memory and are added in a fixed order, so results are
+//    bit-reproducible. Fused epilogues store the outputs.
+//  * Stages hand data to each other through exchange words: 64-bit
+//    (tag, value) pairs written in one store. A reader polls the words it
+//    needs until they carry the tag of the producing stage, so readiness and
+//    data arrive together and no grid-wide barrier is needed. Each buffer's
+//    next version can only be written after every reader of the current
+//    version has read it (the forward's own data dependencies order them), and
+//    a CTA with no rows in a stage reads nothing for it. Each thread polls
+//    exactly the activation elements its lane multiplies, and the input
+//    RMSNorm is applied to them in registers.
 //  * Attention runs between QKV and O on n_kv x nsplit CTAs (the same body as
 //    the standalone attention kernel: Q/K norm, RoPE, KV append, key-parallel
-//    splits merged by the last CTA).
+//    splits, here merged by split 0 from exchange words).
 //  * The head (final RMSNorm, vocabulary GEMV, two-pass argmax) publishes the
 //    next token as an exchange word for the next step's embedding gather.
 //
@@ -37,6 +50,7 @@
 // word records the cause.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 
 #include "attention.cuh"
 #include "gemv_stream.cuh"
@@ -46,10 +60,16 @@ namespace wsg {
 
 constexpr int kMkWarps = 8;                      // consumer warps
 constexpr int kMkConsumers = kMkWarps * 32;
-constexpr int kMkThreads = kMkConsumers + 32;    // plus one producer warp
+constexpr int kMkThreads = kMkConsumers + 128;   // plus a producer warpgroup (one active warp)
+constexpr int kMkProducerRegs = 56;   // registers per thread after setmaxnreg: producer warpgroup
+constexpr int kMkConsumerRegs = 224;  // consumer warpgroups (2 x 128 x 224 + 128 x 56 = 384 x 168)
 constexpr int kMkSlot = 8192;         // bytes per ring slot
 constexpr int kMkLayerPtrs = 12;      // pointers per layer in the shared layer table
-constexpr int kMkWarpSlotsMax = 8;    // ring slots per warp, upper bound
+constexpr int kMkQ = 8;               // boxes in flight per warp, at most (one mbarrier each)
+constexpr int kMkMapsPerLayer = 7;    // tensor maps per layer: wq wk wv wo wg wu wd
+constexpr int kMkMapBytes = 128;      // one CUtensorMap
+constexpr int kMkXr = 4;              // float4 of x per lane: parts per warp (<= 2) x 128-column chunks (<= 2)
+constexpr int kMkPartRows = 256;      // row capacity of the shared partials of one epilogue chunk (at least)
 
 enum : uint32_t { ERR_EXCHANGE_TIMEOUT = 1u << 4 };
 
@@ -58,16 +78,22 @@ struct MkLayer {
   const float *g_in, *g_post, *g_q, *g_k;
 };
 
-// Streaming geometry of one matrix shape.
+// Split-K streaming geometry of one matrix shape. The columns are cut into
+// 8 * pw parts of cw columns (the last ones may reach past the row end: the
+// copies fill zeros there); warp w owns parts w and, when pw == 2, w + 8.
+// Boxes of R rows x cw columns stream through the warps' rings.
 struct MkGeom {
-  int32_t row_bytes;  // in * sizeof(weight)
-  int32_t spr;        // segments per row (> 1 when a row is longer than a slot)
-  int32_t seg_bytes;  // bytes per segment of a split row (multiple of 16)
-  int32_t rps;        // whole rows per segment when spr == 1
+  int32_t cw;         // columns per part (weights: a multiple of 16 bytes)
+  int32_t pw;         // parts per warp: 1 or 2
+  int32_t kc;         // 128-column chunks of a part: 1 or 2 (a lane covers 4 columns of each)
+  int32_t R;          // rows per box
+  int32_t box_bytes;  // R * cw * element size
+  int32_t gchunk;     // row groups per epilogue chunk
 };
 
 struct MkArgs {
   const MkLayer* layers;  // device array [L]
+  const void* maps;       // tensor maps [L][7] then the embedding's (128 bytes each, 64-byte aligned)
   const void* embed;
   const float* g_final;
   int32_t L, H, I, n_q, n_kv, d, V;
@@ -96,7 +122,7 @@ struct MkArgs {
   uint32_t epoch;     // per-launch tag prefix (nonzero; 12 bits)
   AttnArgs at;        // kc / vc point at layer 0's cache
   size_t kv_layer_bytes;
-  int32_t wslots;  // ring slots per warp (<= kMkWarpSlotsMax)
+  int32_t ring_bytes;  // bytes of each warp's ring (a multiple of 128, at least one slot)
   int32_t xs_floats, part_floats, hown_floats;
   int32_t pos0, nsteps;
   int32_t head_every, head_last;  // head on every step / on the last step
@@ -105,8 +131,8 @@ struct MkArgs {
 
 // Trace points per stage: entry, activations staged, segments consumed, barrier passed.
 constexpr int kMkTraceStages = 5, kMkTraceEvents = 4;
-// Per-segment trace of warp 0 of CTA 0 (first kMkTraceSegs segments of the first
-// forward), after the stage trace: wait begins, data ready, dot reduced, next copy issued.
+// Per-box trace of warp 0 of CTA 0 (first kMkTraceSegs boxes of the first
+// forward), after the stage trace: wait begins, data ready, dot done, box released.
 constexpr int kMkTraceSegs = 512, kMkTraceSegEvents = 4;
 
 enum MkStageKind : int { MK_QKV = 0, MK_O = 1, MK_GU = 2, MK_DOWN = 3, MK_VOCAB = 4 };
@@ -126,33 +152,22 @@ __device__ __forceinline__ MkRange mk_range(const MkArgs& a, int st, int c, int 
   return MkRange{static_cast<int>(c * units / G), static_cast<int>((c + 1) * units / G)};
 }
 
-// One stage's weight segments for this CTA: up to three contiguous row pieces
-// (QKV spans the three source matrices; gate/up streams the gate rows, then
-// the up rows, of the same units). Held in registers: pieces are chosen by
-// comparisons, never by array indexing.
-struct MkStage {
-  const char *b0, *b1, *b2;  // first row of each piece
-  int nr0, nr1, nr2;         // rows per piece
-  int l1, l2;                // local index of the first row of pieces 1 and 2 (piece 0 starts at 0)
-  int c1, c2, n;             // segments: piece 0 [0, c1), piece 1 [c1, c2), piece 2 [c2, n)
-  int u0, nloc;
-};
-
-__device__ __forceinline__ int mk_segs(const MkGeom& gm, int nrows) {
-  return gm.spr > 1 ? nrows * gm.spr : (nrows + gm.rps - 1) / gm.rps;
-}
-
 __device__ __forceinline__ const MkGeom& mk_geom(const MkArgs& a, int st) {
   return st == MK_QKV ? a.gq : st == MK_O ? a.go : st == MK_GU ? a.gg : st == MK_DOWN ? a.gd : a.gv;
 }
 
-// Stage geometry of this CTA with tensors named by index into a layer's
-// pointer table (0 wq, 1 wk, 2 wv, 3 wo, 4 wg, 5 wu, 6 wd; 7: the embedding),
-// so it is computed once per launch and combined with any layer's pointers.
+// One stage's rows for this CTA: up to three contiguous row pieces (QKV spans
+// the three source matrices; gate/up takes the gate rows, then the up rows,
+// of the same units), each cut into row groups of R rows (one box per group
+// and column part). Tensors are named by index: 0 wq, 1 wk, 2 wv, 3 wo,
+// 4 wg, 5 wu, 6 wd, 7 the embedding; computed once per launch.
 struct MkStageT {
   int t0, t1, t2;        // tensor of each piece
   int row0, row1, row2;  // first row of each piece within its tensor
-  int nr0, nr1, nr2, l1, l2, c1, c2, n, u0, nloc;
+  int nr0, nr1, nr2;     // rows per piece
+  int l1, l2;            // local index of the first row of pieces 1 and 2 (piece 0 starts at 0)
+  int g1, g2, ng;        // row groups: piece 0 [0, g1), piece 1 [g1, g2), piece 2 [g2, ng)
+  int u0, nloc;
 };
 
 __device__ __forceinline__ MkStageT mk_stage_t(const MkArgs& a, int st, MkRange r) {
@@ -162,7 +177,6 @@ __device__ __forceinline__ MkStageT mk_stage_t(const MkArgs& a, int st, MkRange 
   s.t1 = s.t2 = 0;
   s.row1 = s.row2 = 0;
   s.nr1 = s.nr2 = 0;
-  s.l1 = s.l2 = 0;
   if (st == MK_QKV) {
     const int qw = a.n_q * a.d, kvw = a.n_kv * a.d;
     const int q0 = min(r.u0, qw), q1 = min(r.u1, qw);
@@ -176,85 +190,137 @@ __device__ __forceinline__ MkStageT mk_stage_t(const MkArgs& a, int st, MkRange 
     s.t0 = 4, s.row0 = r.u0, s.nr0 = r.u1 - r.u0;
     s.t1 = 5, s.row1 = r.u0, s.nr1 = r.u1 - r.u0, s.l1 = r.u1 - r.u0;
     s.nloc = 2 * (r.u1 - r.u0);
+    s.l2 = s.nloc;
   } else {
     s.t0 = st == MK_O ? 3 : st == MK_DOWN ? 6 : 7;
     s.row0 = r.u0;
     s.nr0 = r.u1 - r.u0;
     s.nloc = r.u1 - r.u0;
+    s.l1 = s.l2 = s.nloc;
   }
-  s.c1 = mk_segs(gm, s.nr0);
-  s.c2 = s.c1 + mk_segs(gm, s.nr1);
-  s.n = s.c2 + mk_segs(gm, s.nr2);
+  auto groups = [&](int n) { return (n + gm.R - 1) / gm.R; };
+  s.g1 = groups(s.nr0);
+  s.g2 = s.g1 + groups(s.nr1);
+  s.ng = s.g2 + groups(s.nr2);
   return s;
 }
 
-// Bind a stage template to one layer's tensors (lp: that layer's pointer table).
-__device__ __forceinline__ MkStage mk_bind(const MkStageT& t, const MkGeom& gm, const void* const* lp,
-                                          const void* embed) {
-  auto ptr = [&](int id) { return static_cast<const char*>(id == 7 ? embed : lp[id]); };
-  const size_t rb = static_cast<size_t>(gm.row_bytes);
-  MkStage s;
-  s.b0 = ptr(t.t0) + t.row0 * rb;
-  s.b1 = ptr(t.t1) + t.row1 * rb;
-  s.b2 = ptr(t.t2) + t.row2 * rb;
-  s.nr0 = t.nr0, s.nr1 = t.nr1, s.nr2 = t.nr2;
-  s.l1 = t.l1, s.l2 = t.l2;
-  s.c1 = t.c1, s.c2 = t.c2, s.n = t.n;
-  s.u0 = t.u0, s.nloc = t.nloc;
-  return s;
-}
-
-struct MkSeg {
-  const char* src;
-  int bytes;
-  int lrow;  // first local row
-  int part;  // segment index within its row (split rows)
-  int nr;    // rows in this segment
-  int off;   // byte offset within the row
+// Row group rg of a stage: its tensor, first row in that tensor, rows, and
+// the local index of its first row.
+struct MkGroup {
+  int t, y, nr, lrow;
 };
 
-__device__ __forceinline__ MkSeg mk_seg(const MkStage& s, const MkGeom& gm, int j) {
-  const bool p0 = j < s.c1, p1 = !p0 && j < s.c2;
-  const int jj = j - (p0 ? 0 : p1 ? s.c1 : s.c2);
-  const char* base = p0 ? s.b0 : p1 ? s.b1 : s.b2;
-  const int lbase = p0 ? 0 : p1 ? s.l1 : s.l2;
-  MkSeg r;
-  if (gm.spr > 1) {
-    const int row = jj / gm.spr, part = jj - row * gm.spr;
-    r.off = part * gm.seg_bytes;
-    r.bytes = min(gm.seg_bytes, gm.row_bytes - r.off);
-    r.src = base + static_cast<size_t>(row) * gm.row_bytes + r.off;
-    r.lrow = lbase + row;
-    r.part = part;
-    r.nr = 1;
-  } else {
-    const int nrows = p0 ? s.nr0 : p1 ? s.nr1 : s.nr2;
-    const int row = jj * gm.rps;
-    r.nr = min(gm.rps, nrows - row);
-    r.off = 0;
-    r.bytes = r.nr * gm.row_bytes;
-    r.src = base + static_cast<size_t>(row) * gm.row_bytes;
-    r.lrow = lbase + row;
-    r.part = 0;
+__device__ __forceinline__ MkGroup mk_group(const MkStageT& s, int R, int rg) {
+  const bool p0 = rg < s.g1, p1 = !p0 && rg < s.g2;
+  const int gl = rg - (p0 ? 0 : p1 ? s.g1 : s.g2);
+  MkGroup g;
+  g.t = p0 ? s.t0 : p1 ? s.t1 : s.t2;
+  g.y = (p0 ? s.row0 : p1 ? s.row1 : s.row2) + gl * R;
+  g.nr = min(R, (p0 ? s.nr0 : p1 ? s.nr1 : s.nr2) - gl * R);
+  g.lrow = (p0 ? 0 : p1 ? s.l1 : s.l2) + gl * R;
+  return g;
+}
+
+// Slot of local row lr among the partials of the chunk that starts at row group cg.
+__device__ __forceinline__ int mk_slot(const MkStageT& s, int R, int cg, int lr) {
+  const bool p0 = lr < s.l1, p1 = !p0 && lr < s.l2;
+  const int q = lr - (p0 ? 0 : p1 ? s.l1 : s.l2);
+  const int rg = (p0 ? 0 : p1 ? s.g1 : s.g2) + q / R;
+  return (rg - cg) * R + q % R;
+}
+
+__device__ __forceinline__ const void* mk_map(const MkArgs& a, int layer, int t) {
+  const int i = t == 7 ? a.L * kMkMapsPerLayer : layer * kMkMapsPerLayer + t;
+  return static_cast<const char*>(a.maps) + static_cast<size_t>(i) * kMkMapBytes;
+}
+
+// Raw weight words of four consecutive elements (f32: float4, bf16: uint2).
+template <typename WT>
+struct MkW4;
+template <>
+struct MkW4<float> {
+  using T = float4;
+  __device__ __forceinline__ static T zero() { return make_float4(0, 0, 0, 0); }
+  __device__ __forceinline__ static T lds(const unsigned char* buf, int i) {
+    return *reinterpret_cast<const float4*>(buf + static_cast<size_t>(i) * 4);
   }
-  return r;
+  __device__ __forceinline__ static float dot(const T& w, const float4& x, float acc) {
+    return fmaf(w.x, x.x, fmaf(w.y, x.y, fmaf(w.z, x.z, fmaf(w.w, x.w, acc))));
+  }
+};
+template <>
+struct MkW4<uint16_t> {
+  using T = uint2;
+  __device__ __forceinline__ static T zero() { return make_uint2(0, 0); }
+  __device__ __forceinline__ static T lds(const unsigned char* buf, int i) {
+    return *reinterpret_cast<const uint2*>(buf + static_cast<size_t>(i) * 2);
+  }
+  __device__ __forceinline__ static float dot(const T& w, const float4& x, float acc) {
+    return fmaf(__uint_as_float(w.x << 16), x.x,
+                fmaf(__uint_as_float(w.x & 0xFFFF0000u), x.y,
+                     fmaf(__uint_as_float(w.y << 16), x.z, fmaf(__uint_as_float(w.y & 0xFFFF0000u), x.w, acc))));
+  }
+};
+
+// Four consecutive elements at index i of a global row (16-byte aligned for
+// f32, 8-byte for bf16).
+template <typename WT>
+__device__ __forceinline__ float4 ldg4(const void* row, int i);
+template <>
+__device__ __forceinline__ float4 ldg4<float>(const void* row, int i) {
+  return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(row) + i));
+}
+template <>
+__device__ __forceinline__ float4 ldg4<uint16_t>(const void* row, int i) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(row) + i));
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// Butterfly reduce-scatter of N (4, 8, 16 or 32) per-lane values over the warp:
+// at each step a lane keeps half of its values and adds the partner's copy of
+// them; the remaining steps are plain sums. Returns the full 32-lane sum of
+// value lane >> (5 - log2 N), held by every lane of that group.
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&a)[N], int lane) {
+  static_assert(N == 4 || N == 8 || N == 16 || N == 32, "4 to 32 rows per box, a power of two");
+  int o = 16;
+#pragma unroll
+  for (int m = N; m > 1; m >>= 1, o >>= 1) {
+    const bool hi = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < m / 2; ++i) {
+      const float send = hi ? a[i] : a[i + m / 2];
+      const float keep = hi ? a[i + m / 2] : a[i];
+      a[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float v = a[0];
+#pragma unroll
+  for (int r = 32 / N / 2; r > 0; r >>= 1) v += __shfl_xor_sync(0xffffffffu, v, r);
+  return v;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
+// Warpgroup-wide register reallocation (every thread of the warpgroup executes it).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 __device__ __forceinline__ bool mk_head_on(const MkArgs& a, int step) {
   return a.head_every || (a.head_last && step == a.nsteps - 1);
 }
 
-// Widest activation vector the staging code holds in registers (16 per thread).
+// Widest activation vector a stage can take (16 elements per consumer thread).
 constexpr int kMkMaxWidth = 16 * kMkConsumers;
 
 // ---- flag-in-data exchange ----
@@ -416,6 +482,18 @@ struct ConsumerSync {  // barrier over the consumer warps only
   __device__ __forceinline__ void operator()() const { consumer_sync(); }
 };
 
+// Issue cursor of one warp's ring: the next box to request, walking the
+// stages of every layer of every step (and the head where it runs) in the
+// order the warp consumes them. The current stage's rows are copied to
+// registers when the cursor enters it.
+struct MkCursor {
+  int step, layer, st;  // stage being issued
+  int j, n;             // next box of the stage, boxes in the stage
+  int t0, t1, t2, row0, row1, row2, g1, g2;
+  int pw, cw, R, box_bytes;
+  bool done;
+};
+
 template <typename WT, typename KT, int GMAX>
 __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -423,31 +501,25 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   __shared__ int redi[32];
   __shared__ int s_abort, s_last;
   __shared__ MkStageT s_stage[5];
-  const int R = a.wslots;
+  const uint32_t RB = static_cast<uint32_t>(a.ring_bytes);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kMkWarps) * R * kMkSlot);
-  uint64_t* empty = full + kMkWarps * kMkWarpSlotsMax;
-  float* xs = reinterpret_cast<float*>(empty + kMkWarps * kMkWarpSlotsMax);
-  float* part = xs + a.xs_floats;
-  float* ascratch = xs;  // the attention stage reuses the GEMV staging area
+  // per consumer warp: ring bytes; after all rings, kMkQ full and kMkQ empty
+  // barriers per warp (one pair per box in flight)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(kMkWarps) * RB);
+  uint64_t* empty = full + kMkWarps * kMkQ;
+  float* xs = reinterpret_cast<float*>(empty + kMkWarps * kMkQ);
+  float* part = xs + a.xs_floats;  // [rows of an epilogue chunk][8 warps]
+  float* ascratch = xs;            // attention scratch
   const void** lptr = reinterpret_cast<const void**>(part + a.part_floats);  // [L][kMkLayerPtrs]
   volatile int* vabort = &s_abort;
-  auto ring_of = [&](int w) { return smem + static_cast<size_t>(w) * R * kMkSlot; };
 
-  // ---- per-launch tables: every layer's tensor pointers, this CTA's stage geometry ----
+  // ---- per-launch tables: every layer's tensor pointers, this CTA's stage rows ----
   for (int i = tid; i < a.L * kMkLayerPtrs; i += kMkThreads) {
     const int l = i / kMkLayerPtrs, k = i - l * kMkLayerPtrs;
     const MkLayer* p = a.layers + l;
     const void* v = nullptr;
     switch (k) {
-      case 0: v = p->wq; break;
-      case 1: v = p->wk; break;
-      case 2: v = p->wv; break;
-      case 3: v = p->wo; break;
-      case 4: v = p->wg; break;
-      case 5: v = p->wu; break;
-      case 6: v = p->wd; break;
       case 7: v = p->g_in; break;
       case 8: v = p->g_post; break;
       case 9: v = p->g_q; break;
@@ -461,86 +533,130 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     s_abort = 0;
     s_last = 0;
   }
-  if (tid < kMkWarps * R) {
-    const int w = tid / R, s = tid - w * R;
-    mbar_init(&full[w * kMkWarpSlotsMax + s], 1);
-    mbar_init(&empty[w * kMkWarpSlotsMax + s], 1);
+  if (tid < kMkWarps * kMkQ) {
+    mbar_init(&full[tid], 1);
+    mbar_init(&empty[tid], 1);
     fence_mbar_init();
   }
   __syncthreads();
   auto layer_ptrs = [&](int l) { return lptr + l * kMkLayerPtrs; };
 
-  // ------------------------------------------------------------------ producer ----
-  if (warp == kMkWarps) {
-    // Lane w feeds consumer warp w's ring. The warp stays converged: every
-    // pass, each lane tests (without blocking) whether its next slot is free,
-    // and all lanes that can issue do so together.
-    const int w = lane;
-    uint64_t* wfull = full + (w < kMkWarps ? w : 0) * kMkWarpSlotsMax;
-    uint64_t* wempty = empty + (w < kMkWarps ? w : 0) * kMkWarpSlotsMax;
-    unsigned char* wring = ring_of(w < kMkWarps ? w : 0);
-    const uint64_t pol = l2_policy_evict_first();
-    int cstep = 0, clayer = 0, cst = MK_QKV, cj = 0;
-    bool cdone = w >= kMkWarps;
-    MkStage cs{};
-    auto advance = [&]() {
-      if (cst == MK_VOCAB) {
-        ++cstep;
-        clayer = 0;
-        cst = MK_QKV;
-      } else if (cst == MK_DOWN) {
-        if (clayer + 1 < a.L) {
-          ++clayer;
-          cst = MK_QKV;
-        } else if (mk_head_on(a, cstep)) {
-          cst = MK_VOCAB;
-        } else {
-          ++cstep;
-          clayer = 0;
-          cst = MK_QKV;
-        }
+  // Issue cursor over the stages, in the order the consumers run them; the
+  // current stage's rows are copied to registers when the cursor enters it.
+  MkCursor cur;
+  cur.step = 0;
+  cur.layer = 0;
+  cur.st = MK_QKV;
+  cur.done = false;
+  auto cur_next_stage = [&]() {
+    if (cur.st == MK_VOCAB) {
+      ++cur.step;
+      cur.layer = 0;
+      cur.st = MK_QKV;
+    } else if (cur.st == MK_DOWN) {
+      if (cur.layer + 1 < a.L) {
+        ++cur.layer;
+        cur.st = MK_QKV;
+      } else if (mk_head_on(a, cur.step)) {
+        cur.st = MK_VOCAB;
       } else {
-        ++cst;
+        ++cur.step;
+        cur.layer = 0;
+        cur.st = MK_QKV;
       }
-    };
-    auto settle = [&]() {  // first stage, from the current one, with a segment for consumer w
-      while (true) {
-        if (cstep >= a.nsteps) {
-          cdone = true;
-          return;
-        }
-        cs = mk_bind(s_stage[cst], mk_geom(a, cst), layer_ptrs(cst == MK_VOCAB ? 0 : clayer), a.embed);
-        cj = w;
-        if (cj < cs.n) return;
-        advance();
+    } else {
+      ++cur.st;
+    }
+  };
+  auto cur_settle = [&]() {  // first stage, from the current one, with boxes for this CTA
+    while (true) {
+      if (cur.step >= a.nsteps) {
+        cur.done = true;
+        return;
       }
-    };
-    if (!cdone) settle();
-    int issued = 0;
+      const MkStageT& t = s_stage[cur.st];
+      const MkGeom& gm = mk_geom(a, cur.st);
+      cur.j = 0;
+      cur.n = t.ng * gm.pw;
+      if (cur.n > 0) {
+        cur.t0 = t.t0, cur.t1 = t.t1, cur.t2 = t.t2;
+        cur.row0 = t.row0, cur.row1 = t.row1, cur.row2 = t.row2;
+        cur.g1 = t.g1, cur.g2 = t.g2;
+        cur.pw = gm.pw, cur.cw = gm.cw, cur.R = gm.R, cur.box_bytes = gm.box_bytes;
+        return;
+      }
+      cur_next_stage();
+    }
+  };
+
+  // ------------------------------------------------------------------ producer ----
+  if (warp >= kMkWarps) {
+    setmaxnreg_dec<kMkProducerRegs>();
+    if (warp > kMkWarps) return;  // the rest of the warpgroup only gives its registers back
+    // Lane w feeds consumer warp w's ring. Boxes sit at increasing virtual
+    // byte offsets (skipping the ring's tail where a box would straddle its
+    // end); a box may be issued when at most kMkQ boxes are in flight and it
+    // ends within RB bytes of the start of the oldest box not yet released.
+    // The warp stays converged: every pass, each lane retires the boxes its
+    // consumer has released (non-blocking tests) and issues what fits.
+    const int w = lane;
+    const bool active = w < kMkWarps;
+    uint64_t* wfull = full + (active ? w : 0) * kMkQ;
+    uint64_t* wempty = empty + (active ? w : 0) * kMkQ;
+    unsigned char* wring = smem + static_cast<size_t>(active ? w : 0) * RB;
+    const uint64_t pol = l2_policy_evict_first();
+    if (active) cur_settle();
+    cur.done = cur.done || !active;
+    uint32_t vhead = 0, phead = 0;  // virtual and ring offset of the next box
+    uint32_t qv[kMkQ];              // virtual offsets of the boxes in flight, oldest first
+#pragma unroll
+    for (int i = 0; i < kMkQ; ++i) qv[i] = 0;
+    int issued = 0, retired = 0;
     uint64_t idle_since = 0;
-    while (__any_sync(0xffffffffu, !cdone)) {
-      bool can = false;
-      if (!cdone) {
-        const int slot = issued % R;
-        can = issued < R || mbar_test(&wempty[slot], ((issued / R) - 1) & 1);
-        if (can) {
-          const MkSeg sg = mk_seg(cs, mk_geom(a, cst), cj);
-          mbar_arrive_expect_tx(&wfull[slot], static_cast<uint32_t>(sg.bytes));
-          bulk_g2s(wring + static_cast<size_t>(slot) * kMkSlot, sg.src, static_cast<uint32_t>(sg.bytes),
-                   &wfull[slot], pol);
-          ++issued;
-          cj += kMkWarps;
-          if (cj >= cs.n) {
-            advance();
-            settle();
-          }
+    while (__any_sync(0xffffffffu, !cur.done || retired < issued)) {
+      bool progress = false;
+      // retire released boxes
+      while (retired < issued && mbar_test(&wempty[retired % kMkQ], (retired / kMkQ) & 1)) {
+#pragma unroll
+        for (int i = 0; i + 1 < kMkQ; ++i) qv[i] = qv[i + 1];
+        ++retired;
+        progress = true;
+      }
+      // issue what fits
+      while (!cur.done && issued - retired < kMkQ) {
+        const uint32_t B = (static_cast<uint32_t>(cur.box_bytes) + 127u) & ~127u;
+        uint32_t v = vhead, ph = phead;
+        if (ph + B > RB) {
+          v += RB - ph;
+          ph = 0;
+        }
+        const int n = issued - retired;
+        if (n > 0 && v + B - qv[0] > RB) break;  // not free yet
+        const int rg = cur.pw == 2 ? (cur.j >> 1) : cur.j, pj = cur.j - rg * cur.pw;
+        const bool p0 = rg < cur.g1, p1 = !p0 && rg < cur.g2;
+        const int gl = rg - (p0 ? 0 : p1 ? cur.g1 : cur.g2);
+        const int t = p0 ? cur.t0 : p1 ? cur.t1 : cur.t2;
+        const int y = (p0 ? cur.row0 : p1 ? cur.row1 : cur.row2) + gl * cur.R;
+        const int q = issued % kMkQ;
+        mbar_arrive_expect_tx(&wfull[q], static_cast<uint32_t>(cur.box_bytes));
+        tma_load_2d(wring + ph, mk_map(a, cur.layer, t), (w + kMkWarps * pj) * cur.cw, y, &wfull[q], pol);
+#pragma unroll
+        for (int i = 0; i < kMkQ; ++i)
+          if (i == n) qv[i] = v;
+        vhead = v + B;
+        phead = ph + B;
+        ++issued;
+        progress = true;
+        if (++cur.j >= cur.n) {
+          cur_next_stage();
+          cur_settle();
         }
       }
-      if (__any_sync(0xffffffffu, can)) {
+      if (__any_sync(0xffffffffu, progress)) {
         idle_since = 0;
         continue;
       }
-      // nothing to issue this pass: back off, bounded
+      // nothing to do this pass: back off, bounded
       if (*vabort) break;
       const uint64_t now = globaltimer_ns();
       if (idle_since == 0) {
@@ -555,48 +671,64 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       __nanosleep(64);
     }
     // After an abort: wait (bounded) until the copies already issued have landed.
-    if (*vabort && w < kMkWarps)
-      for (int n = max(0, issued - R); n < issued; ++n) mbar_wait(&wfull[n % R], (n / R) & 1);
+    if (*vabort && active)
+      for (int k = max(retired, issued - kMkQ); k < issued; ++k) mbar_wait(&wfull[k % kMkQ], (k / kMkQ) & 1);
     return;
   }
 
   // ------------------------------------------------------------------ consumers ----
-  uint64_t* mfull = full + warp * kMkWarpSlotsMax;
-  uint64_t* mempty = empty + warp * kMkWarpSlotsMax;
-  const unsigned char* myring = ring_of(warp);
-  float* hown = reinterpret_cast<float*>(lptr + a.L * kMkLayerPtrs);  // this CTA's rows of h
+  setmaxnreg_inc<kMkConsumerRegs>();
+  uint64_t* mfull = full + warp * kMkQ;
+  uint64_t* mempty = empty + warp * kMkQ;
+  const unsigned char* myring = smem + static_cast<size_t>(warp) * RB;
+  // Ring position of the next box to read: its barrier, phase parity, and the
+  // ring offset where the previous box ended (the producer's placement rule).
+  int cq = 0;
+  uint32_t cph = 0, chead = 0;
   int consumed = 0;
-  const int qw = a.n_q * a.d;
-  const MkRange rH = mk_range(a, MK_O, c, G);  // O and down own the same rows of h
+  float* hown = reinterpret_cast<float*>(lptr + a.L * kMkLayerPtrs);  // this CTA's rows of h
 
-  // Stage an activation vector from exchange words (tag `tag`) into xs:
-  // plain copy, or RMSNorm * gain. All loads are issued first, then only the
-  // words not yet carrying the tag are polled.
-  auto stage_ll = [&](const uint64_t* src, uint32_t tag, int in, const float* gain) {
+  const int qw = a.n_q * a.d;
+
+  // Input column of this thread's x register q (part q / 2 of its warp,
+  // 128-column chunk q % 2), or -1.
+  auto xcol = [&](const MkGeom& gm, int q, int in) {
+    const int j = q >> 1, k = q & 1, off = 4 * lane + 128 * k;
+    const int col = (warp + kMkWarps * j) * gm.cw + off;
+    return (j < gm.pw && k < gm.kc && off < gm.cw && col < in) ? col : -1;
+  };
+  // CTA-wide RMSNorm scale from per-thread sums of squares.
+  auto norm_scale = [&](float ss, int in) {
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    consumer_sync();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMkWarps; ++w) t += red[w];
+    return 1.0f / sqrtf(t / static_cast<float>(in) + a.eps);
+  };
+
+  // Stage the activation vector from exchange words (tag `tag`) into this
+  // thread's x registers: plain, or RMSNorm * gain. Threads poll the words
+  // coalesced (thread t: words t, t + 256, ...; all requested first, then only
+  // the stale ones reloaded together, one round trip per round), pass them
+  // through shared memory, and after one barrier each lane picks up the
+  // elements its warp's column parts need.
+  auto stage_x = [&](const uint64_t* src, uint32_t tag, int in, const float* gain, const MkGeom& gm,
+                     float4 (&xr)[kMkXr]) {
     constexpr int K = kMkMaxWidth / kMkConsumers;
     uint64_t wv[K];
-    float gn[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int i = tid + k * kMkConsumers;
-      wv[k] = 0;
-      gn[k] = 1.f;
-      if (i < in) {
-        wv[k] = ll_load(src + i);
-        if (gain) gn[k] = __ldg(gain + i);
-      }
+      wv[k] = i < in ? ll_load(src + i) : (static_cast<uint64_t>(tag) << 32);
     }
-    // Poll in rounds: every round reloads all of this thread's words that do
-    // not yet carry the tag, together (one round trip per round).
     {
       const uint64_t t0 = globaltimer_ns();
       for (int round = 0;; ++round) {
         bool stale = false;
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-          const int i = tid + k * kMkConsumers;
-          if (i < in && static_cast<uint32_t>(wv[k] >> 32) != tag) stale = true;
-        }
+        for (int k = 0; k < K; ++k) stale |= static_cast<uint32_t>(wv[k] >> 32) != tag;
         if (!stale) break;
         if ((round & 63) == 63) {
           if (*vabort) break;
@@ -607,63 +739,68 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           }
         }
 #pragma unroll
-        for (int k = 0; k < K; ++k) {
-          const int i = tid + k * kMkConsumers;
-          if (i < in && static_cast<uint32_t>(wv[k] >> 32) != tag) wv[k] = ll_load(src + i);
-        }
+        for (int k = 0; k < K; ++k)
+          if (static_cast<uint32_t>(wv[k] >> 32) != tag) wv[k] = ll_load(src + tid + k * kMkConsumers);
       }
     }
-    float v[K];
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < K; ++k) {
-      v[k] = __uint_as_float(static_cast<uint32_t>(wv[k]));
-      ss = fmaf(v[k], v[k], ss);
+      const int i = tid + k * kMkConsumers;
+      if (i < in) {
+        const float v = __uint_as_float(static_cast<uint32_t>(wv[k]));
+        xs[i] = v;
+        ss = fmaf(v, v, ss);
+      }
     }
-    float inv = 1.f;
     if (gain) {
       ss = warp_sum(ss);
       if (lane == 0) red[warp] = ss;
-      consumer_sync();
+    }
+    consumer_sync();
+    float inv = 1.f;
+    if (gain) {
       float t = 0.f;
 #pragma unroll
       for (int w = 0; w < kMkWarps; ++w) t += red[w];
       inv = 1.0f / sqrtf(t / static_cast<float>(in) + a.eps);
     }
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int i = tid + k * kMkConsumers;
-      if (i < in) xs[xs_index<WT>(i, in)] = gain ? v[k] * inv * gn[k] : v[k];
+    for (int q = 0; q < kMkXr; ++q) {
+      const int col = xcol(gm, q, in);
+      xr[q] = make_float4(0, 0, 0, 0);
+      if (col >= 0) {
+        const float4 v = *reinterpret_cast<const float4*>(xs + col);
+        if (gain) {
+          const float4 g = __ldg(reinterpret_cast<const float4*>(gain + col));
+          xr[q] = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
+        } else {
+          xr[q] = v;
+        }
+      }
     }
-    consumer_sync();
   };
 
   // Layer 0: RMSNorm of the token's embedding row.
-  auto stage_embed = [&](int t, const float* gain) {
-    constexpr int K = kMkMaxWidth / kMkConsumers;
+  auto stage_embed = [&](int t, const float* gain, const MkGeom& gm, float4 (&xr)[kMkXr]) __attribute__((always_inline)) {
     const WT* row = static_cast<const WT*>(a.embed) + static_cast<size_t>(t) * a.H;
-    float v[K], gn[K];
     float ss = 0.f;
+    float4 gv[kMkXr];
 #pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int i = tid + k * kMkConsumers;
-      v[k] = i < a.H ? load_f32<WT>(row, i) : 0.f;
-      gn[k] = i < a.H ? __ldg(gain + i) : 1.f;
-      ss = fmaf(v[k], v[k], ss);
+    for (int q = 0; q < kMkXr; ++q) {
+      const int col = xcol(gm, q, a.H);
+      xr[q] = col >= 0 ? ldg4<WT>(row, col) : make_float4(0, 0, 0, 0);
+      gv[q] = col >= 0 ? __ldg(reinterpret_cast<const float4*>(gain + col)) : make_float4(0, 0, 0, 0);
+      ss = fmaf(xr[q].x, xr[q].x, fmaf(xr[q].y, xr[q].y, fmaf(xr[q].z, xr[q].z, fmaf(xr[q].w, xr[q].w, ss))));
     }
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    consumer_sync();
-    float tot = 0.f;
+    const float inv = norm_scale(ss, a.H);
 #pragma unroll
-    for (int w = 0; w < kMkWarps; ++w) tot += red[w];
-    const float inv = 1.0f / sqrtf(tot / static_cast<float>(a.H) + a.eps);
-#pragma unroll
-    for (int k = 0; k < K; ++k) {
-      const int i = tid + k * kMkConsumers;
-      if (i < a.H) xs[xs_index<WT>(i, a.H)] = v[k] * inv * gn[k];
+    for (int q = 0; q < kMkXr; ++q) {
+      xr[q].x = xr[q].x * inv * gv[q].x;
+      xr[q].y = xr[q].y * inv * gv[q].y;
+      xr[q].z = xr[q].z * inv * gv[q].z;
+      xr[q].w = xr[q].w * inv * gv[q].w;
     }
-    consumer_sync();
   };
 
   uint64_t* segtrace = nullptr;
@@ -673,54 +810,97 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     if (segtrace && lane == 0 && consumed < kMkTraceSegs) segtrace[consumed * kMkTraceSegEvents + ev] = clock64();
   };
 
-  // This warp's segments of one stage, in ring order, into part[].
-  auto consume = [&](const MkStage& sl, const MkGeom& gm, int in) -> bool {
-    for (int j = warp; j < sl.n; j += kMkWarps) {
-      const int slot = consumed % R;
-      segstamp(0);
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(&mfull[slot], (consumed / R) & 1));
-      segstamp(1);
-      if (!ok) {
-        if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
-        *vabort = 1;
-        break;
-      }
-      const MkSeg sg = mk_seg(sl, gm, j);
-      const unsigned char* buf = myring + static_cast<size_t>(slot) * kMkSlot;
-      if (sg.nr == 1) {
-        float v = seg_dot<WT>(buf, xs, sg.off / static_cast<int>(sizeof(WT)), sg.bytes, in, lane);
-        v = warp_sum(v);
-        if (lane == 0) part[sg.lrow * gm.spr + sg.part] = v;
-      } else {
-        // several whole rows: all lane partials first (each x chunk read once),
-        // then one interleaved reduction
-        float v[4];
-        for (int r0 = 0; r0 < sg.nr; r0 += 4) {
-          rows_dot<WT>(buf + static_cast<size_t>(r0) * gm.row_bytes, gm.row_bytes, min(4, sg.nr - r0), xs, in, lane, v);
+  // Sum of the 8 warp partials of local row lr (chunk starting at row group cg).
+  auto row_value = [&](const MkStageT& st, const MkGeom& gm, int cg, int lr) {
+    const float* p = part + mk_slot(st, gm.R, cg, lr) * kMkWarps;
+    float v = p[0];
 #pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) v[r] += __shfl_xor_sync(0xffffffffu, v[r], o);
-          if (lane == 0)
-            for (int r = 0; r < 4 && r0 + r < sg.nr; ++r) part[sg.lrow + r0 + r] = v[r];
-        }
-      }
-      segstamp(2);
-      // The slot's data reached registers before the shuffles above; hand the
-      // slot back to the producer.
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&mempty[slot]);
-      segstamp(3);
-      ++consumed;
-    }
-    consumer_sync();
-    return !*vabort;
+    for (int w = 1; w < kMkWarps; ++w) v += p[w];
+    return v;
   };
 
-  auto row_value = [&](const MkGeom& gm, int lr) {
-    float v = 0.f;
-    for (int k = 0; k < gm.spr; ++k) v += part[lr * gm.spr + k];
-    return v;
+
+  // This warp's boxes of one stage, in ring order: lane partials per row,
+  // reduce-scatter, warp partials into part[]; after each chunk of row groups
+  // the epilogue epi(cg, ce) reads the row sums of groups [cg, ce). KC
+  // (128-column chunks per part) is a template constant so every register
+  // array is indexed statically; the stage's piece sizes are copied to
+  // registers once, so the loop reads shared memory only for weights and the
+  // ring barriers. After a failed wait the warp skips its data work but keeps
+  // every barrier of the stage, so the CTA leaves the stage together at the
+  // next chunk boundary.
+  auto consume_kc = [&](auto kc_tag, const MkStageT& st, const MkGeom& gm, const float4(&xr)[kMkXr],
+                        auto&& epi) -> bool {
+    constexpr int KC = decltype(kc_tag)::value;
+    constexpr int RM = 16 * static_cast<int>(4 / sizeof(WT)) / KC;  // rows per box, at most
+    constexpr int kSh = RM == 32 ? 0 : RM == 16 ? 1 : RM == 8 ? 2 : 3;
+    using W = MkW4<WT>;
+    const int R = gm.R, pw = gm.pw, cw = gm.cw, gchunk = gm.gchunk;
+    const int ng = st.ng, g1 = st.g1, g2 = st.g2, nr0 = st.nr0, nr1 = st.nr1, nr2 = st.nr2;
+    bool ok = true;
+    for (int cg = 0; cg < ng; cg += gchunk) {
+      const int ce = min(ng, cg + gchunk);
+      for (int rg = cg; rg < ce; ++rg) {
+        const bool p0 = rg < g1, p1 = !p0 && rg < g2;
+        const int nr = min(R, (p0 ? nr0 : p1 ? nr1 : nr2) - (rg - (p0 ? 0 : p1 ? g1 : g2)) * R);
+        float acc[RM];
+#pragma unroll
+        for (int r = 0; r < RM; ++r) acc[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          if (j >= pw) break;
+          if (ok) {
+            segstamp(0);
+            ok = __all_sync(0xffffffffu, mbar_wait(&mfull[cq], cph));
+            segstamp(1);
+            if (!ok) {
+              if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
+              *vabort = 1;
+            }
+          }
+          if (ok) {
+            const uint32_t B = (static_cast<uint32_t>(gm.box_bytes) + 127u) & ~127u;
+            const uint32_t boff = chead + B > RB ? 0u : chead;
+            chead = boff + B;
+            const unsigned char* buf = myring + boff;
+#pragma unroll
+            for (int k = 0; k < KC; ++k) {
+              const int off = 4 * lane + 128 * k;
+              if (off < cw) {
+                const float4 x = xr[2 * j + k];
+#pragma unroll
+                for (int r = 0; r < RM; ++r)
+                  if (r < nr) acc[r] = W::dot(W::lds(buf, r * cw + off), x, acc[r]);
+              }
+            }
+            segstamp(2);
+            // every lane's reads of the box completed (their values are in
+            // registers): release its bytes to the producer
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mempty[cq]);
+            segstamp(3);
+            ++consumed;
+            if (++cq == kMkQ) {
+              cq = 0;
+              cph ^= 1u;
+            }
+          }
+        }
+        const float v = reduce_scatter<RM>(acc, lane);
+        const int r = lane >> kSh;
+        if (ok && (lane & ((1 << kSh) - 1)) == 0 && r < nr) part[((rg - cg) * R + r) * kMkWarps + warp] = v;
+      }
+      consumer_sync();
+      if (*vabort) return false;
+      epi(cg, ce);
+      consumer_sync();
+    }
+    return !*vabort;
+  };
+  auto consume = [&](const MkStageT& st, const MkGeom& gm, const float4(&xr)[kMkXr], auto&& epi)
+                     __attribute__((always_inline)) -> bool {
+    if (gm.kc == 1) return consume_kc(std::integral_constant<int, 1>{}, st, gm, xr, epi);
+    return consume_kc(std::integral_constant<int, 2>{}, st, gm, xr, epi);
   };
 
   // Trace events per stage: 0 entry, 1 inputs staged, 2 outputs published.
@@ -732,6 +912,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
 
   const bool attn_cta = c < a.n_kv * a.at.nsplit_max;
   bool ok = true;
+  float4 xr[kMkXr];
   for (int step = 0; step < a.nsteps && ok; ++step) {
     const int pos = a.pos0 + step;
     // The token: written by the host before the launch, or published by the
@@ -765,12 +946,12 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       // ---- QKV with the input RMSNorm (layer 0: of the token's embedding row) ----
       {
         stamp(step, l, 0, 0);
-        const MkStage sl = mk_bind(s_stage[MK_QKV], a.gq, lp, a.embed);
-        if (sl.nloc > 0) {
+        const MkStageT& st = s_stage[MK_QKV];
+        if (st.nloc > 0) {
           if (l == 0)
-            stage_embed(tok, g_in);
+            stage_embed(tok, g_in, a.gq, xr);
           else
-            stage_ll(a.ll_h, mk_tag(a, step, l - 1, MK_DOWN), a.H, g_in);
+            stage_x(a.ll_h, mk_tag(a, step, l - 1, MK_DOWN), a.H, g_in, a.gq, xr);
         }
         stamp(step, l, 0, 1);
         // Keys and values before pos do not depend on this token: make sure the
@@ -792,14 +973,16 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
             }
           }
         }
-        if (!(ok = consume(sl, a.gq, a.H))) break;
         const uint32_t tg = mk_tag(a, step, l, MK_QKV);
-        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) ll_store(a.ll_qkv + sl.u0 + lr, row_value(a.gq, lr), tg);
+        if (!(ok = consume(st, a.gq, xr, [&](int cg, int) {
+              for (int lr = tid; lr < st.nloc; lr += kMkConsumers)
+                ll_store(a.ll_qkv + st.u0 + lr, row_value(st, a.gq, cg, lr), tg);
+            })))
+          break;
         stamp(step, l, 0, 2);
       }
       // ---- attention (Q/K norm, RoPE, KV append, key-parallel splits) ----
       if (attn_cta) {
-        consumer_sync();  // the attention scratch overlaps the staging area the QKV epilogue read
         AttnArgs at = a.at;
         at.g_q = static_cast<const float*>(lp[9]);
         at.g_k = static_cast<const float*>(lp[10]);
@@ -809,82 +992,90 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? 4 : 2), AttnLlIo>(
             at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
             AttnLlIo{a.ll_qkv, a.ll_attn, a.ll_apart, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV),
-                     mk_tag(a, step, l, 1),
-                     vabort, a.err,
+                     mk_tag(a, step, l, 1), vabort, a.err,
                      (a.trace && step == 0)
                          ? a.trace + ((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + 1) * kMkTraceEvents
                          : nullptr});
         stamp(step, l, 1, 2);
-        consumer_sync();
+        consumer_sync();  // the attention scratch is reused by the next layer's attention
       }
       // ---- O projection + residual ----
       {
         stamp(step, l, 2, 0);
-        const MkStage sl = mk_bind(s_stage[MK_O], a.go, lp, a.embed);
-        if (sl.nloc > 0) stage_ll(a.ll_attn, mk_tag(a, step, l, 1), qw, nullptr);
+        const MkStageT& st = s_stage[MK_O];
+        if (st.nloc > 0) stage_x(a.ll_attn, mk_tag(a, step, l, 1), qw, nullptr, a.go, xr);
         stamp(step, l, 2, 1);
-        if (!(ok = consume(sl, a.go, qw))) break;
         const uint32_t tg = mk_tag(a, step, l, MK_O);
-        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
-          const int row = sl.u0 + lr;
-          const float prev = l == 0 ? load_f32<WT>(static_cast<const WT*>(a.embed) + static_cast<size_t>(tok) * a.H, row)
-                                    : hown[lr];
-          const float hn = prev + row_value(a.go, lr);
-          hown[lr] = hn;
-          ll_store(a.ll_h + row, hn, tg);
-        }
+        if (!(ok = consume(st, a.go, xr, [&](int cg, int) {
+              for (int lr = tid; lr < st.nloc; lr += kMkConsumers) {
+                const int row = st.u0 + lr;
+                const float prev =
+                    l == 0 ? load_f32<WT>(static_cast<const WT*>(a.embed) + static_cast<size_t>(tok) * a.H, row)
+                           : hown[lr];
+                const float hn = prev + row_value(st, a.go, cg, lr);
+                hown[lr] = hn;
+                ll_store(a.ll_h + row, hn, tg);
+              }
+            })))
+          break;
         stamp(step, l, 2, 2);
       }
       // ---- gate/up with the post-attention RMSNorm, SwiGLU ----
       {
         stamp(step, l, 3, 0);
-        const MkStage sl = mk_bind(s_stage[MK_GU], a.gg, lp, a.embed);
-        if (sl.nloc > 0) stage_ll(a.ll_h, mk_tag(a, step, l, MK_O), a.H, g_post);
+        const MkStageT& st = s_stage[MK_GU];
+        if (st.nloc > 0) stage_x(a.ll_h, mk_tag(a, step, l, MK_O), a.H, g_post, a.gg, xr);
         stamp(step, l, 3, 1);
-        if (!(ok = consume(sl, a.gg, a.H))) break;
-        const int np = sl.nloc >> 1;
         const uint32_t tg = mk_tag(a, step, l, MK_GU);
-        for (int i = tid; i < np; i += kMkConsumers)
-          ll_store(a.ll_act + sl.u0 + i, silu_f32(row_value(a.gg, i)) * row_value(a.gg, np + i), tg);
+        if (!(ok = consume(st, a.gg, xr, [&](int cg, int) {
+              const int np = st.nloc >> 1;
+              for (int i = tid; i < np; i += kMkConsumers)
+                ll_store(a.ll_act + st.u0 + i,
+                         silu_f32(row_value(st, a.gg, cg, i)) * row_value(st, a.gg, cg, np + i), tg);
+            })))
+          break;
         stamp(step, l, 3, 2);
       }
       // ---- down projection + residual ----
       {
         stamp(step, l, 4, 0);
-        const MkStage sl = mk_bind(s_stage[MK_DOWN], a.gd, lp, a.embed);
-        if (sl.nloc > 0) stage_ll(a.ll_act, mk_tag(a, step, l, MK_GU), a.I, nullptr);
+        const MkStageT& st = s_stage[MK_DOWN];
+        if (st.nloc > 0) stage_x(a.ll_act, mk_tag(a, step, l, MK_GU), a.I, nullptr, a.gd, xr);
         stamp(step, l, 4, 1);
-        if (!(ok = consume(sl, a.gd, a.I))) break;
         const uint32_t tg = mk_tag(a, step, l, MK_DOWN);
-        for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
-          const float hn = hown[lr] + row_value(a.gd, lr);
-          hown[lr] = hn;
-          ll_store(a.ll_h + sl.u0 + lr, hn, tg);
-        }
+        if (!(ok = consume(st, a.gd, xr, [&](int cg, int) {
+              for (int lr = tid; lr < st.nloc; lr += kMkConsumers) {
+                const float hn = hown[lr] + row_value(st, a.gd, cg, lr);
+                hown[lr] = hn;
+                ll_store(a.ll_h + st.u0 + lr, hn, tg);
+              }
+            })))
+          break;
         stamp(step, l, 4, 2);
       }
-      consumer_sync();  // hown is rewritten by the next layer's O stage
     }
-    (void)rH;
     if (!ok || *vabort || !mk_head_on(a, step)) continue;
     // ---- head: final RMSNorm, tied vocabulary projection, two-pass argmax ----
     stamp(step, a.L, 0, 0);
-    const MkStage sl = mk_bind(s_stage[MK_VOCAB], a.gv, layer_ptrs(0), a.embed);
-    if (sl.nloc > 0) stage_ll(a.ll_h, mk_tag(a, step, a.L - 1, MK_DOWN), a.H, a.g_final);
+    const MkStageT& st = s_stage[MK_VOCAB];
+    if (st.nloc > 0) stage_x(a.ll_h, mk_tag(a, step, a.L - 1, MK_DOWN), a.H, a.g_final, a.gv, xr);
     stamp(step, a.L, 0, 1);
-    if (!(ok = consume(sl, a.gv, a.H))) break;
-    stamp(step, a.L, 0, 2);
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int lr = tid; lr < sl.nloc; lr += kMkConsumers) {
-      const int row = sl.u0 + lr;
-      const float v = row_value(a.gv, lr);
-      if (a.logits) a.logits[row] = v;
-      if (argmax_better(v, row, bv, bi)) {
-        bv = v;
-        bi = row;
-      }
-    }
+    if (!(ok = consume(st, a.gv, xr, [&](int cg, int ce) {
+          const int r0 = cg * a.gv.R, r1 = min(st.nloc, ce * a.gv.R);
+          for (int lr = r0 + tid; lr < r1; lr += kMkConsumers) {
+            const int row = st.u0 + lr;
+            const float v = row_value(st, a.gv, cg, lr);
+            if (a.logits) a.logits[row] = v;
+            if (argmax_better(v, row, bv, bi)) {
+              bv = v;
+              bi = row;
+            }
+          }
+        })))
+      break;
+    stamp(step, a.L, 0, 2);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);

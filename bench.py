@@ -45,9 +45,10 @@ METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 
 # DRAM traffic of the persistent decode kernel per algorithmic byte, from ncu on a
 # 4-layer / 32768-vocabulary case of the same widths (profiles/decode_megakernel_small_full.md):
-# (387,255,808 read + 3,407,872 written) / 387,186,688 algorithmic bytes. Set to None when
-# the kernel changes until it is measured again.
-MK_TRAFFIC_PER_ALG_BYTE = (387255808 + 3407872) / 387186688
+# (392,428,032 read + 2,843,392 written) / 387,186,688 algorithmic bytes; the excess is the
+# rows a tiled box reads past a CTA's row range. Set to None when the kernel changes until it
+# is measured again.
+MK_TRAFFIC_PER_ALG_BYTE = (392428032 + 2843392) / 387186688
 PROMPT = 32
 
 

@@ -257,6 +257,20 @@ dec_status gemv_device_errors(int32_t clear, uint32_t* bits);
 dec_status greedy_head_noalloc(int32_t wdtype, const void* d_embed, const float* d_h, const float* d_gain, float eps,
                                int32_t vocab, int32_t hidden, float* d_logits, int32_t* d_token, void* stream);
 
+/* Chunked-prefill projection GEMM as a standalone call ("Megakernels",
+ * "Chunked prefill for long prompts": a chunk of prompt rows turns each
+ * projection into a dense matrix product, run on the tensor cores):
+ * C[m][n] = sum_k A[m][k] * W[n][k] for m < M, n < N (accumulate != 0:
+ * C[m][n] += that sum). A [M][K] and W [N][K] are bfloat16, row-major,
+ * 16-byte aligned (W is a weight matrix in the decoder's [out][in] layout);
+ * C is float32 with row stride ldc >= N. Products are exact in FP32 and
+ * accumulated in FP32 (tcgen05 tensor cores, tiles of 128 x 128 x 64).
+ * K must be a multiple of 8. Asynchronous on `stream`; device errors (a
+ * bounded wait that gave up) are reported by gemv_device_errors.
+ * Errors: DEC_EINVAL (sizes, alignment), DEC_EDEVICE, DEC_ECUDA. */
+dec_status gemm_bf16(const uint16_t* d_A, const uint16_t* d_W, float* d_C, int32_t M, int32_t N, int32_t K,
+                     int32_t ldc, int32_t accumulate, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

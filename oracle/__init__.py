@@ -14,6 +14,7 @@ from .primitives import (  # noqa: F401
     gemv,
     gemv_q4,
     gqa_decode_attention,
+    project_rows,
     q4_dequant,
     q4_unpack,
     rmsnorm,

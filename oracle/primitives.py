@@ -141,6 +141,15 @@ def gemv(W, x) -> np.ndarray:
     return widen(W) @ widen(x)
 
 
+def project_rows(A, W) -> np.ndarray:
+    """Rows of a prompt chunk through one projection: C[m] = W A[m] for every
+    row, i.e. C = A W^T with A [rows, in] and W [out, in], accumulated in
+    float64 ("Megakernels", "Chunked prefill for long prompts": the chunk's
+    rows go through each projection together).
+    """
+    return widen(A) @ widen(W).T
+
+
 def q4_unpack(packed) -> np.ndarray:
     """uint4 codes [out, in] from words [out, in/8]; code j of word w is bits [4j, 4j+4), column 8w+j."""
     packed = np.asarray(packed, dtype=np.uint32)

@@ -301,3 +301,24 @@ def test_weights_draw_order_is_stable():
     assert a["embed"].shape == (512, 64)
     g = a["layers"][0]["g_in"]
     assert abs(g.mean() - 1.0) < 0.05 and 0.05 < g.std() < 0.15
+
+
+def test_project_rows_is_a_gemv_per_row_and_brute_force():
+    """The chunk projection is the GEMV applied to every row (the definition),
+    and on a tiny case equals the explicit triple loop."""
+    rng = np.random.default_rng(5)
+    A = rng.standard_normal((7, 13)).astype(np.float32)
+    W = rng.standard_normal((5, 13)).astype(np.float32)
+    C = O.project_rows(A, W)
+    assert C.shape == (7, 5)
+    for m in range(7):  # same sums, float64 summation order aside
+        np.testing.assert_allclose(C[m], O.gemv(W, A[m]), rtol=1e-13, atol=1e-13)
+    brute = np.zeros((7, 5))
+    for m in range(7):
+        for n in range(5):
+            brute[m, n] = sum(float(A[m, k]) * float(W[n, k]) for k in range(13))
+    np.testing.assert_allclose(C, brute, rtol=1e-12, atol=1e-12)
+    # orientation: a unit row of A picks a column of W
+    e = np.zeros((1, 13), np.float32)
+    e[0, 4] = 1.0
+    np.testing.assert_array_equal(O.project_rows(e, W)[0], W[:, 4].astype(np.float64))

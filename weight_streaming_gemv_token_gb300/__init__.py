@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     dec_trace_bytes,
     dec_weights,
     dec_workspace_bytes,
+    gemm_bf16,
     gemv,
     gemv_device_errors,
     gemv_q4,

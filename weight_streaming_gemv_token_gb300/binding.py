@@ -27,7 +27,7 @@ EXPORTED = (
     "dec_workspace_bytes", "dec_create", "dec_load_weights", "dec_reset", "dec_step", "dec_prefill_chunk",
     "dec_generate", "dec_get_kv", "dec_position", "dec_trace_bytes", "dec_set_trace", "dec_device_errors",
     "dec_destroy", "dec_last_error",
-    "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors", "greedy_head_noalloc",
+    "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors", "greedy_head_noalloc", "gemm_bf16",
 )
 
 
@@ -85,6 +85,7 @@ def library() -> ctypes.CDLL:
             "gemv_q4": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]),
             "gemv_q4_rows_per_warp": (c_int32, [c_int32, c_int32]),
             "gemv_device_errors": (c_int32, [c_int32, P(c_uint32)]),
+            "gemm_bf16": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
             "greedy_head_noalloc": (c_int32, [c_int32, c_void_p, c_void_p, c_void_p, c_float, c_int32, c_int32,
                                               c_void_p, c_void_p, c_void_p]),
         }
@@ -217,3 +218,9 @@ def greedy_head_noalloc(wdtype: int, embed, h, gain, eps: float, vocab: int, hid
     """Final RMSNorm, tied vocabulary GEMV and greedy argmax with no device allocation (library-held scratch)."""
     _check(library().greedy_head_noalloc(wdtype, _ptr(embed), _ptr(h), _ptr(gain), eps, vocab, hidden, _ptr(logits),
                                          _ptr(token), _stream(stream)))
+
+
+def gemm_bf16(A, W, C, M: int, N: int, K: int, ldc: int | None = None, accumulate: bool = False, stream=None):
+    """C[M][N] (=, or += with accumulate) A[M][K] . W[N][K]^T, bfloat16 operands, FP32 accumulation (tensor cores)."""
+    _check(library().gemm_bf16(_ptr(A), _ptr(W), _ptr(C), M, N, K, N if ldc is None else ldc, int(bool(accumulate)),
+                               _stream(stream)))

@@ -71,4 +71,14 @@ cudaError_t allow_smem(K kern, size_t bytes) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Device error word of the context-free entry points on device `dev`.
+uint32_t* context_free_err_ptr(int dev);
+
+// Tiled TMA descriptor (CUtensorMap, 128 bytes, opaque here) of a row-major
+// [rows][cols] matrix of `elem`-byte elements (2: bfloat16, 4: float32) with
+// boxes of box_rows x box_cols; swizzle128 selects the 128-byte swizzle
+// (box_cols * elem must then be 128). Elements outside the matrix read as 0.
+dec_status encode_map_2d(void* out, const void* base, long long rows, long long cols, int elem, int box_cols,
+                         int box_rows, bool swizzle128, std::string* err);
+
 }  // namespace wsg

@@ -24,7 +24,6 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
-#include <mutex>
 #include <vector>
 
 #include "attention.cuh"
@@ -423,39 +422,10 @@ int mk_group_rows(const dec_config& g, int st, const MkGeom& m, int G) {
   return most;
 }
 
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
-// against the driver library).
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
 // Tensor map of a row-major [rows][in] weight matrix with boxes of m.R rows x m.cw columns.
 dec_status encode_map(CUtensorMap* out, const void* base, int rows, int in, int wdtype, const MkGeom& m,
                       std::string* err) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return fail(err, DEC_ECUDA, "cuTensorMapEncodeTiled is not available");
-  const int elem = static_cast<int>(dtype_bytes(wdtype));
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(in), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(in) * elem};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(m.cw), static_cast<cuuint32_t>(m.R)};
-  cuuint32_t estr[2] = {1, 1};
-  const CUresult r =
-      enc(out, wdtype == DEC_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS)
-    return fail(err, DEC_EINVAL, "cuTensorMapEncodeTiled failed (%d) for a %d x %d matrix, box %d x %d", static_cast<int>(r),
-                rows, in, m.R, m.cw);
-  return DEC_OK;
+  return encode_map_2d(out, base, rows, in, static_cast<int>(dtype_bytes(wdtype)), m.cw, m.R, false, err);
 }
 
 // Persistent kernel instance for the configuration (defined per weight dtype in

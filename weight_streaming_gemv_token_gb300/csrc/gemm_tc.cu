@@ -1,0 +1,66 @@
+// Host side of the tensor-core projection GEMM (gemm_tc.cuh): launch helper
+// used by the chunked prefill, and the standalone gemm_bf16 entry point.
+#include <cuda.h>
+
+#include "common.h"
+#include "gemm_tc.cuh"
+#include "gemm_tc_host.h"
+
+namespace wsg {
+
+dec_status launch_gemm_bf16(const void* mapA, const void* mapB, float* C, int ldc, int col0, int M, int N, int K,
+                            bool accumulate, uint32_t* err, cudaStream_t st, std::string* where) {
+  static bool ready[64] = {};
+  DeviceInfo di;
+  dec_status s = device_info(&di, where);
+  if (s != DEC_OK) return s;
+  if (!ready[di.device]) {
+    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kTcSmemBytes)));
+    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kTcSmemBytes)));
+    ready[di.device] = true;
+  }
+  TcArgs a;
+  a.C = C;
+  a.ldc = ldc;
+  a.col0 = col0;
+  a.M = M;
+  a.N = N;
+  a.K = K;
+  a.err = err;
+  const dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
+  const CUtensorMap& ma = *static_cast<const CUtensorMap*>(mapA);
+  const CUtensorMap& mb = *static_cast<const CUtensorMap*>(mapB);
+  if (accumulate)
+    gemm_bf16_tc_kernel<TC_ADD><<<grid, kTcThreads, kTcSmemBytes, st>>>(ma, mb, a);
+  else
+    gemm_bf16_tc_kernel<TC_STORE><<<grid, kTcThreads, kTcSmemBytes, st>>>(ma, mb, a);
+  WSG_CUDA_TRY(where, cudaGetLastError());
+  return DEC_OK;
+}
+
+dec_status encode_gemm_operand(void* out, const void* base, long long rows, int K, std::string* err) {
+  return encode_map_2d(out, base, rows, K, 2, kTcBK, kTcBM, true, err);
+}
+
+}  // namespace wsg
+
+using namespace wsg;
+
+extern "C" dec_status gemm_bf16(const uint16_t* d_A, const uint16_t* d_W, float* d_C, int32_t M, int32_t N, int32_t K,
+                                int32_t ldc, int32_t accumulate, void* stream) {
+  if (!d_A || !d_W || !d_C) return fail(nullptr, DEC_EINVAL, "gemm_bf16: NULL pointer");
+  if (M < 1 || N < 1 || K < 1) return fail(nullptr, DEC_EINVAL, "gemm_bf16: M, N, K must be >= 1");
+  if (K % 8) return fail(nullptr, DEC_EINVAL, "gemm_bf16: K must be a multiple of 8 (16-byte rows)");
+  if (ldc < N) return fail(nullptr, DEC_EINVAL, "gemm_bf16: ldc %d < N %d", ldc, N);
+  if (!aligned16(d_A) || !aligned16(d_W)) return fail(nullptr, DEC_EINVAL, "gemm_bf16: A and W must be 16-byte aligned");
+  DeviceInfo di;
+  dec_status s = device_info(&di, nullptr);
+  if (s != DEC_OK) return s;
+  alignas(64) unsigned char ma[128], mb[128];
+  if ((s = encode_gemm_operand(ma, d_A, M, K, nullptr)) != DEC_OK) return s;
+  if ((s = encode_gemm_operand(mb, d_W, N, K, nullptr)) != DEC_OK) return s;
+  return launch_gemm_bf16(ma, mb, d_C, ldc, 0, M, N, K, accumulate != 0, context_free_err_ptr(di.device),
+                          static_cast<cudaStream_t>(stream), nullptr);
+}

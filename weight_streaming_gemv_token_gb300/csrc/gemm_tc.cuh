@@ -1,0 +1,204 @@
+// Tensor-core GEMM for the chunked-prefill projections ("Megakernels",
+// "Chunked prefill for long prompts": the chunk's rows turn every projection
+// into a dense matrix product): C[M][N] (float32) = A[M][K] . W[N][K]^T, or
+// C += that product, with A (activation rows) and W (weights, row-major
+// [out][in]) in bfloat16 and FP32 accumulation.
+//
+// One CTA computes one 128 x 128 tile of C with tcgen05.mma (cta_group::1,
+// kind::f16, BF16 inputs, FP32 accumulator in tensor memory):
+//  * a TMA thread streams 128 x 64 tiles of A and W (128-byte swizzle) into a
+//    4-stage shared-memory ring (full mbarrier per stage, completed by the
+//    copies' transaction bytes);
+//  * an MMA thread issues four K = 16 MMAs per stage from shared-memory
+//    descriptors and releases the stage with tcgen05.commit on its empty
+//    mbarrier; a final commit signals the accumulator complete;
+//  * all four warps then read their 32 TMEM lanes (rows) with tcgen05.ld and
+//    store (or add) their rows of C.
+// Rows of A past M and columns of K past K read as zeros (the tensor maps'
+// bounds), so any M, N and K (K % 8 == 0) work. Every wait is bounded; on a
+// timeout the CTA records an error bit, skips the accumulator read, frees its
+// tensor memory and returns.
+#pragma once
+#include <cuda.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace wsg {
+
+constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64, kTcStages = 4, kTcThreads = 128;
+constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
+constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;  // 16 KB
+constexpr uint32_t kTcStageBytes = kTcABytes + kTcBBytes;
+constexpr uint32_t kTcTmemCols = kTcBN;  // FP32 accumulator: 128 lanes x 128 columns
+constexpr size_t kTcSmemBytes = kTcStages * kTcStageBytes + 1024;  // plus alignment slack
+
+enum : uint32_t { ERR_TC_TIMEOUT = 1u << 5 };
+
+enum TcEpi : int { TC_STORE = 0, TC_ADD = 1 };
+
+struct TcArgs {
+  float* C;
+  int32_t ldc;   // row stride of C in elements
+  int32_t col0;  // column of C where this product's column 0 goes
+  int32_t M, N, K;
+  uint32_t* err;
+};
+
+// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle:
+// rows of 128 bytes, 8-row groups 1024 bytes apart, descriptor version 1.
+__device__ __forceinline__ uint64_t tc_desc_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>(1) << 16;            // leading byte offset (unused with this swizzle)
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;    // stride byte offset: one 8-row group
+  d |= static_cast<uint64_t>(1) << 46;            // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;            // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: FP32 accumulator, BF16 A and B, both
+// K-major, N and M as encoded by the instruction (N >> 3, M >> 4).
+constexpr uint32_t tc_idesc(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d_map(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
+                        const TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char tc_raw[];
+  unsigned char* tsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], done;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kTcBN, m0 = blockIdx.y * kTcBM;
+  const int KB = (a.K + kTcBK - 1) / kTcBK;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(&done, 1);
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                 "n"(kTcTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (warp == 0 && lane == 0) {
+    // ---- TMA: A and W tiles of every K block into the stage ring ----
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % kTcStages;
+      if (kb >= kTcStages && !mbar_wait(&empty[s], ((kb / kTcStages) - 1) & 1)) {
+        s_fail = 1;
+        atomicOr(a.err, ERR_TC_TIMEOUT);
+        break;
+      }
+      unsigned char* st = tsm + static_cast<size_t>(s) * kTcStageBytes;
+      mbar_arrive_expect_tx(&full[s], kTcStageBytes);
+      tma_load_2d_map(st, &mapA, kb * kTcBK, m0, &full[s]);
+      tma_load_2d_map(st + kTcABytes, &mapB, kb * kTcBK, n0, &full[s]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---- MMA: four K = 16 steps per stage, accumulator in TMEM ----
+    constexpr uint32_t idesc = tc_idesc(kTcBM, kTcBN);
+    bool ok = true;
+    for (int kb = 0; kb < KB; ++kb) {
+      const int s = kb % kTcStages;
+      if (!mbar_wait(&full[s], (kb / kTcStages) & 1)) {
+        s_fail = 1;
+        atomicOr(a.err, ERR_TC_TIMEOUT);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t sa = smem_u32(tsm + static_cast<size_t>(s) * kTcStageBytes);
+      const uint32_t sb = sa + kTcABytes;
+#pragma unroll
+      for (int kk = 0; kk < kTcBK / 16; ++kk) {
+        const uint64_t da = tc_desc_sw128(sa + kk * 32), db = tc_desc_sw128(sb + kk * 32);
+        const uint32_t acc = (kb | kk) != 0;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+            "l"(da), "l"(db), "r"(idesc), "r"(acc)
+            : "memory");
+      }
+      // the stage's shared memory is free once these MMAs have read it
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_u32(&empty[s]))
+                   : "memory");
+    }
+    if (ok)
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_u32(&done))
+                   : "memory");
+  }
+
+  // ---- epilogue: warp w holds rows 32w..32w+31 of the tile in its TMEM lanes ----
+  __syncwarp();
+  const bool have = mbar_wait(&done, 0);
+  if (!have && lane == 0) atomicOr(a.err, ERR_TC_TIMEOUT);
+  tc_fence_after();
+  const int row = m0 + warp * 32 + lane;
+  if (__all_sync(0xffffffffu, have)) {
+#pragma unroll 1
+    for (int c0 = 0; c0 < kTcBN; c0 += 32) {
+      uint32_t v[32];
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c0);
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+          "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+          : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+            "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+            "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+            "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+          : "r"(taddr));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      if (row < a.M) {
+        float* crow = a.C + static_cast<size_t>(row) * a.ldc + a.col0;
+        const int nb = n0 + c0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int col = nb + j;
+          if (col < a.N) {
+            const float x = __uint_as_float(v[j]);
+            if (EPI == TC_ADD)
+              crow[col] += x;
+            else
+              crow[col] = x;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcTmemCols) : "memory");
+}
+
+}  // namespace wsg

@@ -45,14 +45,8 @@ dec_status device_info(DeviceInfo* out, std::string* err) {
 // Device error word of the context-free entry points.
 __device__ uint32_t g_gemv_err;
 
-namespace {
-
-constexpr int kNW = 8, kNSMAX = 8, kRING = 12288, kSEGMAX = 4096;
-// Matrices up to this size are prefetched into L2 whole at kernel start.
-constexpr long long kL2PrefetchMax = 64ll << 20;
-
-// Address of the device error word on the current device (looked up once).
-uint32_t* gemv_err_ptr(int dev) {
+// Address of the device error word on device `dev` (looked up once).
+uint32_t* context_free_err_ptr(int dev) {
   static uint32_t* ptrs[64] = {};
   if (!ptrs[dev]) {
     void* p = nullptr;
@@ -60,6 +54,14 @@ uint32_t* gemv_err_ptr(int dev) {
   }
   return ptrs[dev];
 }
+
+namespace {
+
+constexpr int kNW = 8, kNSMAX = 8, kRING = 12288, kSEGMAX = 4096;
+// Matrices up to this size are prefetched into L2 whole at kernel start.
+constexpr long long kL2PrefetchMax = 64ll << 20;
+
+uint32_t* gemv_err_ptr(int dev) { return context_free_err_ptr(dev); }
 
 // Lift a kernel's dynamic shared memory limit to the device maximum, once per device.
 template <typename K>

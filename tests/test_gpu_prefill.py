@@ -1,0 +1,122 @@
+"""Chunked prefill (tensor-core projections, causal attention over cache + chunk)
+against the oracle's tokenwise forward, through the C ABI.
+
+The chunked path computes the same forward as tokenwise prefill ("Megakernels",
+"Chunked prefill for long prompts"): its projections are BF16 tensor-core
+products whose activation operand is a bfloat16 value plus remainder pair, so
+the rows keep float32 precision and the oracle is the plain forward (batched
+over the prompt rows). Checked: the first output's logits and token, every KV
+entry of every layer after the prompt, and a few decode steps after it (which
+read the cache the chunks wrote), with BF16 weights and KV.
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as Wl
+
+from gpu_util import LOW_TOL, close, lib
+from test_gpu_decoder import kv_to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def check_token(got_logits, ref_logits, tok, tol, what):
+    own, ok = O.argmax_lowest(got_logits)
+    assert ok and tok == own, f"{what}: GPU token {tok} is not the argmax {own} of its own logits"
+    srt = np.sort(ref_logits)[::-1]
+    ref_tok, _ = O.argmax_lowest(ref_logits)
+    if srt[0] - srt[1] > 2 * (tol + tol * abs(srt[0])):
+        assert tok == ref_tok, f"{what}: GPU {tok} vs oracle {ref_tok}"
+
+
+def run_chunked(shape, weights, prompt, chunk, n_out, engine, kv_every=1):
+    import torch
+
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    max_seq = len(prompt) + n_out + 4
+    dec = Decoder(shape, weights, kv_dtype="bf16", max_seq=max_seq, chunk_cap=chunk, engine=engine)
+    ora = O.OracleDecoder(shape, weights, kv_dtype="bf16", max_seq=max_seq)
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    # GPU: the prompt in chunks of `chunk` rows; oracle: token by token
+    for c0 in range(0, len(prompt), chunk):
+        part = [int(t) for t in prompt[c0:c0 + chunk]]
+        last = c0 + chunk >= len(prompt)
+        nxt = dec.prefill(part, is_last=last, logits=logits if last else None)
+    ref = ora.prefill(prompt)["logits"][len(prompt) - 1]
+    got = logits.cpu().numpy()
+    close(got, ref, LOW_TOL, "first output logits")
+    check_token(got, ref, nxt, LOW_TOL, "first output")
+    assert dec.position == len(prompt)
+    for l in range(shape.layers):
+        K, V, n = dec.kv(l)
+        assert n == len(prompt)
+        rk, rv = ora.kv(l)
+        close(kv_to_np(K[:, :n]), rk, LOW_TOL, f"K layer {l} after the prompt")
+        close(kv_to_np(V[:, :n]), rv, LOW_TOL, f"V layer {l} after the prompt")
+    # decode after the chunks: the oracle continues on the GPU's tokens
+    cur = nxt
+    for j in range(n_out):
+        tok = dec.step(cur, logits=logits)
+        ref = ora.step(cur)
+        got = logits.cpu().numpy()
+        close(got, ref, LOW_TOL, f"decode step {j} logits")
+        check_token(got, ref, tok, LOW_TOL, f"decode step {j}")
+        cur = tok
+    if n_out:
+        for l in range(0, shape.layers, kv_every):
+            K, V, n = dec.kv(l)
+            rk, rv = ora.kv(l)
+            close(kv_to_np(K[:, :n]), rk, LOW_TOL, f"K layer {l} after decode")
+            close(kv_to_np(V[:, :n]), rv, LOW_TOL, f"V layer {l} after decode")
+    assert dec.device_errors() == 0
+    dec.close()
+
+
+@pytest.fixture(scope="module")
+def tiny_bf16():
+    return Wl.decoder_weights(Wl.TINY, seed=1, wdtype="bf16")
+
+
+@pytest.mark.parametrize("engine", ["persistent", "staged"])
+@pytest.mark.parametrize("chunk", [64, 128])
+def test_tiny_chunked_prefill(tiny_bf16, engine, chunk):
+    """150 prompt rows in chunks of 64 (64 + 64 + 22) or of 128 (128 + 22); then decode
+    steps that read the cache the chunks wrote."""
+    prompt = Wl.prompt_uniform(150, Wl.TINY.vocab, seed=0)
+    run_chunked(Wl.TINY, tiny_bf16, prompt, chunk, 4, engine)
+
+
+def test_ragged_geometry_chunked_prefill():
+    """4 query heads per KV head, head_dim 32, widths that are not multiples of the tiles."""
+    shape = Wl.DecoderShape(layers=3, hidden=96, inter=200, n_q=8, n_kv=2, head_dim=32, vocab=777)
+    w = Wl.decoder_weights(shape, seed=9, wdtype="bf16")
+    prompt = Wl.prompt_zipf(77, shape.vocab, seed=0)
+    run_chunked(shape, w, prompt, 32, 3, "persistent")
+
+
+def test_single_row_chunks():
+    """Chunks of one row: the causal attention sees only the cache."""
+    w = Wl.decoder_weights(Wl.TINY, seed=2, wdtype="bf16")
+    prompt = Wl.prompt_uniform(5, Wl.TINY.vocab, seed=1)
+    run_chunked(Wl.TINY, w, prompt, 1, 2, "persistent")
+
+
+@pytest.mark.slow
+def test_qwen3_bf16_chunked_prefill():
+    """The Qwen3-0.6B shape (BF16 weights and KV), a 300-token Zipf prompt in chunks of 128."""
+    w = Wl.decoder_weights(Wl.QWEN3_06B, seed=1, wdtype="bf16")
+    prompt = Wl.prompt_zipf(300, Wl.QWEN3_06B.vocab, seed=0)
+    run_chunked(Wl.QWEN3_06B, w, prompt, 128, 2, "persistent", kv_every=7)
+
+
+def test_chunked_prefill_needs_bf16_weights():
+    lib()
+    import weight_streaming_gemv_token_gb300 as W
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    w = Wl.decoder_weights(Wl.TINY, seed=1)
+    with pytest.raises(W.WsgError):
+        Decoder(Wl.TINY, w, kv_dtype="f32", max_seq=64, chunk_cap=64)

@@ -156,3 +156,4 @@ def test_regression_golden_tokens(tiny_weights, golden_dir):
     out = O.generate(m, W.prompt_uniform(8, W.TINY.vocab, seed=0), 8)
     assert out["tokens"] == [int(t) for t in ref["tokens"]]
     np.testing.assert_allclose(out["logits"][0][:16], ref["logits0_head"], rtol=1e-12)
+

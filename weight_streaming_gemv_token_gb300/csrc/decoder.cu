@@ -29,7 +29,9 @@
 #include "attention.cuh"
 #include "common.h"
 #include "gemv_stream.cuh"
+#include "gemm_tc_host.h"
 #include "megakernel.cuh"
+#include "prefill.cuh"
 
 namespace wsg {
 void* mk_kernel_f32(bool kv_bf16, bool group_le2);
@@ -52,6 +54,9 @@ size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
 struct Layout {
   size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn, ll_act,
       ll_tok, ll_apart, kv_ready, mk_layers, mk_maps, rope_cos, rope_sin, kc, vc;
+  // chunked prefill (chunk_cap > 0): rows padded to a multiple of 128
+  size_t pf_x, pf_ah, pf_ah2, pf_qkv, pf_ao, pf_ao2, pf_gu, pf_ai, pf_ai2;  // *2: bfloat16 remainders
+  int pf_rows;
   size_t total;
 };
 
@@ -72,6 +77,8 @@ bool config_ok(const dec_config* c, std::string* why) {
   if (c->kvdtype != DEC_F32 && c->kvdtype != DEC_BF16) return bad("kvdtype must be DEC_F32 or DEC_BF16");
   if (c->max_seq < 1) return bad("max_seq must be >= 1");
   if (c->chunk_cap < 0) return bad("chunk_cap must be >= 0");
+  if (c->chunk_cap > 0 && c->wdtype != DEC_BF16)
+    return bad("batched prefill (chunk_cap > 0) runs bfloat16 tensor-core projections: wdtype must be DEC_BF16");
   if (c->engine != DEC_ENGINE_PERSISTENT && c->engine != DEC_ENGINE_STAGED) return bad("unknown engine");
   if (!(c->eps >= 0.f) || !(c->rope_theta > 0.f)) return bad("eps >= 0 and rope_theta > 0 required");
   return true;
@@ -112,6 +119,19 @@ Layout make_layout(const dec_config& c) {
   L.mk_maps = take((static_cast<size_t>(c.layers) * kMkMapsPerLayer + 1) * kMkMapBytes);
   L.rope_cos = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   L.rope_sin = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
+  L.pf_rows = c.chunk_cap > 0 ? (c.chunk_cap + 127) / 128 * 128 : 0;
+  {
+    const size_t R = static_cast<size_t>(L.pf_rows);
+    L.pf_x = take(R * c.hidden * 4);
+    L.pf_ah = take(R * c.hidden * 2);
+    L.pf_ah2 = take(R * c.hidden * 2);
+    L.pf_qkv = take(R * (qw + 2 * kvw) * 4);
+    L.pf_ao = take(R * qw * 2);
+    L.pf_ao2 = take(R * qw * 2);
+    L.pf_gu = take(R * 2 * c.inter * 4);
+    L.pf_ai = take(R * c.inter * 2);
+    L.pf_ai2 = take(R * c.inter * 2);
+  }
   const size_t cache = static_cast<size_t>(c.layers) * kvw * c.max_seq * dtype_bytes(c.kvdtype);
   L.kc = take(cache);
   L.vc = take(cache);
@@ -174,6 +194,14 @@ struct dec_ctx {
   uint32_t epoch = 0;         // tag prefix of the last persistent launch (1..4095)
   size_t mk_smem = 0;
   int mk_grid = 0;
+  // chunked prefill: tensor maps of the GEMM operands (activation rows: normed
+  // input, attention output, SwiGLU output, then their bfloat16 remainders;
+  // weights: 7 per layer)
+  struct alignas(64) Map128 {
+    unsigned char b[128];
+  };
+  Map128 pf_amap[6];
+  std::vector<Map128> pf_wmap;
   std::string err;
 
   template <typename T>
@@ -344,6 +372,99 @@ dec_status enqueue_step_t(dec_ctx* c, cudaStream_t st, bool full) {
   return DEC_OK;
 }
 
+
+// ---- chunked prefill ----
+
+// Rows p0..p0+n-1 (tokens already in the token stream) through every layer
+// together: per-row kernels (prefill.cuh) between tensor-core GEMMs over the
+// chunk's rows (gemm_tc.cuh); the last row optionally through the head.
+template <typename KT>
+dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
+  const dec_config& g = c->cfg;
+  const Layout& L = c->L;
+  const int H = g.hidden, I = g.inter, d = g.head_dim;
+  const int qw = g.n_q * d, kvw = g.n_kv * d, W = qw + 2 * kvw;
+  const int group = g.n_q / g.n_kv;
+  cudaStream_t st = c->stream;
+  float* X = c->at<float>(L.pf_x);
+  uint16_t* AH = c->at<uint16_t>(L.pf_ah);
+  uint16_t* AH2 = c->at<uint16_t>(L.pf_ah2);
+  float* QKV = c->at<float>(L.pf_qkv);
+  uint16_t* AO = c->at<uint16_t>(L.pf_ao);
+  uint16_t* AO2 = c->at<uint16_t>(L.pf_ao2);
+  float* GU = c->at<float>(L.pf_gu);
+  uint16_t* AI = c->at<uint16_t>(L.pf_ai);
+  uint16_t* AI2 = c->at<uint16_t>(L.pf_ai2);
+  uint32_t* err = c->at<uint32_t>(L.err);
+  const float* rc = c->at<float>(L.rope_cos);
+  const float* rs = c->at<float>(L.rope_sin);
+  dec_status s;
+  // C[:, col0..col0+N) (=, or +=) rows . W^T with operand maps `amap` and
+  // amap + 3 (value and remainder of: 0 normed input, 1 attention output,
+  // 2 SwiGLU output) and weight map `wm`
+  auto gemm = [&](int amap, int wm, float* C, int ldc, int col0, int N, int K, bool acc) {
+    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, c->pf_wmap[wm].b, C, ldc, col0, n, N, K, acc,
+                            err, st, &c->err);
+  };
+  pf_embed_norm_kernel<uint16_t><<<n, kPfThreads, 0, st>>>(c->at<int32_t>(L.tok), p0, c->w.embed, g.vocab,
+                                                           c->layers[0].g_in, g.eps, H, X, AH, AH2, err);
+  WSG_CUDA_TRY(&c->err, cudaGetLastError());
+  for (int l = 0; l < g.layers; ++l) {
+    const dec_layer_weights& lw = c->layers[l];
+    const int wm = l * kMkMapsPerLayer;
+    if (l > 0) {
+      pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_in, g.eps, H, AH, AH2);
+      WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    }
+    if ((s = gemm(0, wm + 0, QKV, W, 0, qw, H, false)) != DEC_OK) return s;
+    if ((s = gemm(0, wm + 1, QKV, W, qw, kvw, H, false)) != DEC_OK) return s;
+    if ((s = gemm(0, wm + 2, QKV, W, qw + kvw, kvw, H, false)) != DEC_OK) return s;
+    const size_t off = static_cast<size_t>(l) * c->kv_layer_elems() * dtype_bytes(g.kvdtype);
+    void* kc = c->ws + L.kc + off;
+    void* vc = c->ws + L.vc + off;
+    pf_qk_rope_kv_kernel<KT><<<dim3(n, (g.n_q + 2 * g.n_kv + 3) / 4), 128, 0, st>>>(
+        QKV, p0, g.n_q, g.n_kv, d, lw.g_q, lw.g_k, g.eps, rc, rs, kc, vc, g.max_seq);
+    WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    auto ak = group <= 2 ? pf_attn_kernel<KT, 2> : pf_attn_kernel<KT, 8>;
+    ak<<<dim3(g.n_kv, (n + kPfAttnRows - 1) / kPfAttnRows), kPfAttnRows * 32, 0, st>>>(
+        QKV, n, p0, g.n_q, g.n_kv, d, kc, vc, g.max_seq, 1.0f / std::sqrt(static_cast<float>(d)), AO, AO2);
+    WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    if ((s = gemm(1, wm + 3, X, H, 0, H, qw, true)) != DEC_OK) return s;  // O projection + residual
+    pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_post, g.eps, H, AH, AH2);
+    WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    if ((s = gemm(0, wm + 4, GU, 2 * I, 0, I, H, false)) != DEC_OK) return s;
+    if ((s = gemm(0, wm + 5, GU, 2 * I, I, I, H, false)) != DEC_OK) return s;
+    pf_swiglu_kernel<<<std::min(4 * c->di.sms, (n * I + 255) / 256), 256, 0, st>>>(GU, n, I, AI, AI2);
+    WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    if ((s = gemm(2, wm + 6, X, H, 0, H, I, true)) != DEC_OK) return s;  // down projection + residual
+  }
+  // Position word (the head's position, or the next one) and, for the
+  // persistent engine, the appended cache rows published to its readers.
+  uint32_t* kvr = g.engine == DEC_ENGINE_PERSISTENT ? c->at<uint32_t>(L.kv_ready) : nullptr;
+  pf_control_kernel<<<1, 256, 0, st>>>(c->at<int32_t>(L.ctrl), is_last ? p0 + n - 1 : p0 + n, kvr,
+                                       g.layers * g.n_kv, static_cast<uint32_t>(p0 + n));
+  WSG_CUDA_TRY(&c->err, cudaGetLastError());
+  if (is_last) {
+    pf_copy_row_kernel<<<1, 256, 0, st>>>(X + static_cast<size_t>(n - 1) * H, c->at<float>(L.h), H);
+    WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    GemvArgs a = base_args(c, c->p_vocab, g.vocab, H);
+    a.w = single(c->w.embed, g.vocab);
+    a.x = c->at<float>(L.h);
+    a.norm_g = c->w.g_final;
+    a.y = c->at<float>(L.logits);
+    a.part_val = c->at<float>(L.mval);
+    a.part_idx = c->at<int32_t>(L.midx);
+    a.counter = c->at<uint32_t>(L.mcnt);
+    a.tok_w = c->at<int32_t>(L.tok);
+    if ((s = launch_dec_gemv<uint16_t, PRO_NORM, EPI_ARGMAX>(c, c->p_vocab, a, st, false)) != DEC_OK) return s;
+  }
+  return DEC_OK;
+}
+
+dec_status run_chunk_prefill(dec_ctx* c, int p0, int n, bool is_last) {
+  return c->cfg.kvdtype == DEC_F32 ? run_chunk_prefill_t<float>(c, p0, n, is_last)
+                                   : run_chunk_prefill_t<uint16_t>(c, p0, n, is_last);
+}
 
 // ---- persistent engine ----
 
@@ -692,6 +813,20 @@ extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_
       return bail(fail(nullptr, DEC_EINVAL, "dec_create: a projection needs %zu B of shared memory (max %zu)", p->smem,
                        di.smem_optin));
   c->attn_smem = attn_smem_bytes(cfg->n_q / cfg->n_kv, cfg->head_dim);
+  if (L.pf_rows > 0) {
+    const dec_status ms[6] = {
+        encode_gemm_operand(c->pf_amap[0].b, c->ws + L.pf_ah, L.pf_rows, cfg->hidden, &c->err),
+        encode_gemm_operand(c->pf_amap[1].b, c->ws + L.pf_ao, L.pf_rows, qw, &c->err),
+        encode_gemm_operand(c->pf_amap[2].b, c->ws + L.pf_ai, L.pf_rows, cfg->inter, &c->err),
+        encode_gemm_operand(c->pf_amap[3].b, c->ws + L.pf_ah2, L.pf_rows, cfg->hidden, &c->err),
+        encode_gemm_operand(c->pf_amap[4].b, c->ws + L.pf_ao2, L.pf_rows, qw, &c->err),
+        encode_gemm_operand(c->pf_amap[5].b, c->ws + L.pf_ai2, L.pf_rows, cfg->inter, &c->err)};
+    for (dec_status m : ms)
+      if (m != DEC_OK) {
+        thread_error() = c->err;
+        return bail(m);
+      }
+  }
   c->nsplit_max = di.sms / cfg->n_kv;
   if (c->nsplit_max < 1) c->nsplit_max = 1;
   if (c->nsplit_max > kSplitMax) c->nsplit_max = kSplitMax;
@@ -754,6 +889,26 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
     WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->ws + c->L.mk_maps, maps.data(), maps.size() * sizeof(CUtensorMap),
                                           cudaMemcpyHostToDevice, c->stream));
   }
+  if (c->L.pf_rows > 0) {
+    // Tensor-core GEMM operand maps of every weight matrix (chunked prefill).
+    const dec_config& g = c->cfg;
+    const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;
+    c->pf_wmap.resize(static_cast<size_t>(g.layers) * kMkMapsPerLayer);
+    for (int l = 0; l < g.layers; ++l) {
+      const dec_layer_weights& x = c->layers[l];
+      const struct {
+        const void* p;
+        int rows, K;
+      } t[kMkMapsPerLayer] = {{x.w_q, qw, g.hidden},    {x.w_k, kvw, g.hidden},      {x.w_v, kvw, g.hidden},
+                              {x.w_o, g.hidden, qw},    {x.w_gate, g.inter, g.hidden}, {x.w_up, g.inter, g.hidden},
+                              {x.w_down, g.hidden, g.inter}};
+      for (int k = 0; k < kMkMapsPerLayer; ++k) {
+        const dec_status st =
+            encode_gemm_operand(c->pf_wmap[static_cast<size_t>(l) * kMkMapsPerLayer + k].b, t[k].p, t[k].rows, t[k].K, &c->err);
+        if (st != DEC_OK) return st;
+      }
+    }
+  }
   WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
   // Graphs bake in the weight pointers: drop any captured with older ones.
   if (c->g_full) cudaGraphExecDestroy(c->g_full);
@@ -805,6 +960,15 @@ extern "C" dec_status dec_prefill_chunk(dec_ctx* c, const int32_t* h_tokens, int
   if (static_cast<long long>(c->pos) + n > c->cfg.max_seq)
     return fail(&c->err, DEC_ECAPACITY, "dec_prefill_chunk: %d rows at position %d exceed max_seq %d", n, c->pos,
                 c->cfg.max_seq);
+  if (c->cfg.chunk_cap > 0 && n <= c->cfg.chunk_cap) {  // batched: tensor-core projections
+    dec_status s = put_tokens(c, h_tokens, n);
+    if (s != DEC_OK) return s;
+    const int32_t p0 = c->pos;
+    if ((s = run_chunk_prefill(c, p0, n, is_last != 0)) != DEC_OK) return s;
+    c->pos += n;
+    if (is_last) return finish_head(c, p0 + n - 1, d_logits, h_next);
+    return DEC_OK;
+  }
   const bool persistent = c->cfg.engine == DEC_ENGINE_PERSISTENT;
   dec_status s = DEC_OK;
   if (!persistent) {

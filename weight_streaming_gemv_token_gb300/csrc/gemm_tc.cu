@@ -8,17 +8,25 @@
 
 namespace wsg {
 
-dec_status launch_gemm_bf16(const void* mapA, const void* mapB, float* C, int ldc, int col0, int M, int N, int K,
-                            bool accumulate, uint32_t* err, cudaStream_t st, std::string* where) {
+dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* mapB, float* C, int ldc, int col0, int M,
+                            int N, int K, bool accumulate, uint32_t* err, cudaStream_t st, std::string* where) {
   static bool ready[64] = {};
   DeviceInfo di;
   dec_status s = device_info(&di, where);
   if (s != DEC_OK) return s;
   if (!ready[di.device]) {
-    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kTcSmemBytes)));
-    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kTcSmemBytes)));
+    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(tc_smem_bytes<false>())));
+    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(tc_smem_bytes<false>())));
+    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(tc_smem_bytes<true>())));
+    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD, true>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(tc_smem_bytes<true>())));
     ready[di.device] = true;
   }
   TcArgs a;
@@ -31,11 +39,19 @@ dec_status launch_gemm_bf16(const void* mapA, const void* mapB, float* C, int ld
   a.err = err;
   const dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
   const CUtensorMap& ma = *static_cast<const CUtensorMap*>(mapA);
+  const CUtensorMap& ma2 = *static_cast<const CUtensorMap*>(mapA2 ? mapA2 : mapA);
   const CUtensorMap& mb = *static_cast<const CUtensorMap*>(mapB);
-  if (accumulate)
-    gemm_bf16_tc_kernel<TC_ADD><<<grid, kTcThreads, kTcSmemBytes, st>>>(ma, mb, a);
-  else
-    gemm_bf16_tc_kernel<TC_STORE><<<grid, kTcThreads, kTcSmemBytes, st>>>(ma, mb, a);
+  if (mapA2) {
+    if (accumulate)
+      gemm_bf16_tc_kernel<TC_ADD, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb, a);
+    else
+      gemm_bf16_tc_kernel<TC_STORE, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb, a);
+  } else {
+    if (accumulate)
+      gemm_bf16_tc_kernel<TC_ADD, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb, a);
+    else
+      gemm_bf16_tc_kernel<TC_STORE, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb, a);
+  }
   WSG_CUDA_TRY(where, cudaGetLastError());
   return DEC_OK;
 }
@@ -61,6 +77,6 @@ extern "C" dec_status gemm_bf16(const uint16_t* d_A, const uint16_t* d_W, float*
   alignas(64) unsigned char ma[128], mb[128];
   if ((s = encode_gemm_operand(ma, d_A, M, K, nullptr)) != DEC_OK) return s;
   if ((s = encode_gemm_operand(mb, d_W, N, K, nullptr)) != DEC_OK) return s;
-  return launch_gemm_bf16(ma, mb, d_C, ldc, 0, M, N, K, accumulate != 0, context_free_err_ptr(di.device),
+  return launch_gemm_bf16(ma, nullptr, mb, d_C, ldc, 0, M, N, K, accumulate != 0, context_free_err_ptr(di.device),
                           static_cast<cudaStream_t>(stream), nullptr);
 }

@@ -14,6 +14,11 @@
 //    mbarrier; a final commit signals the accumulator complete;
 //  * all four warps then read their 32 TMEM lanes (rows) with tcgen05.ld and
 //    store (or add) their rows of C.
+// With SPLIT the activation operand comes as two bfloat16 matrices, A = hi +
+// lo (hi the nearest bfloat16 of a float32 value, lo the nearest bfloat16 of
+// the remainder), and both products go into the same accumulator: the rows
+// keep about 16 mantissa bits, so the product matches float32 activations
+// times bfloat16 weights to ~2^-17 relative per term.
 // Rows of A past M and columns of K past K read as zeros (the tensor maps'
 // bounds), so any M, N and K (K % 8 == 0) work. Every wait is bounded; on a
 // timeout the CTA records an error bit, skips the accumulator read, frees its
@@ -30,9 +35,16 @@ namespace wsg {
 constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64, kTcStages = 4, kTcThreads = 128;
 constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
 constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;  // 16 KB
-constexpr uint32_t kTcStageBytes = kTcABytes + kTcBBytes;
 constexpr uint32_t kTcTmemCols = kTcBN;  // FP32 accumulator: 128 lanes x 128 columns
-constexpr size_t kTcSmemBytes = kTcStages * kTcStageBytes + 1024;  // plus alignment slack
+// stage: A tile (and with SPLIT the A-remainder tile), then the W tile
+template <bool SPLIT>
+constexpr uint32_t tc_stage_bytes() {
+  return (SPLIT ? 2 : 1) * kTcABytes + kTcBBytes;
+}
+template <bool SPLIT>
+constexpr size_t tc_smem_bytes() {
+  return kTcStages * tc_stage_bytes<SPLIT>() + 1024;  // plus alignment slack
+}
 
 enum : uint32_t { ERR_TC_TIMEOUT = 1u << 5 };
 
@@ -75,10 +87,12 @@ __device__ __forceinline__ void tma_load_2d_map(void* dst, const CUtensorMap* ma
       : "memory");
 }
 
-template <int EPI>
+template <int EPI, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-                        const TcArgs a) {
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
+                        const __grid_constant__ CUtensorMap mapB, const TcArgs a) {
+  constexpr uint32_t kStage = tc_stage_bytes<SPLIT>();
+  constexpr uint32_t kBOff = (SPLIT ? 2 : 1) * kTcABytes;  // W tile offset within a stage
   extern __shared__ __align__(1024) unsigned char tc_raw[];
   unsigned char* tsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], done;
@@ -117,10 +131,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         atomicOr(a.err, ERR_TC_TIMEOUT);
         break;
       }
-      unsigned char* st = tsm + static_cast<size_t>(s) * kTcStageBytes;
-      mbar_arrive_expect_tx(&full[s], kTcStageBytes);
+      unsigned char* st = tsm + static_cast<size_t>(s) * kStage;
+      mbar_arrive_expect_tx(&full[s], kStage);
       tma_load_2d_map(st, &mapA, kb * kTcBK, m0, &full[s]);
-      tma_load_2d_map(st + kTcABytes, &mapB, kb * kTcBK, n0, &full[s]);
+      if (SPLIT) tma_load_2d_map(st + kTcABytes, &mapA2, kb * kTcBK, m0, &full[s]);
+      tma_load_2d_map(st + kBOff, &mapB, kb * kTcBK, n0, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA: four K = 16 steps per stage, accumulator in TMEM ----
@@ -135,17 +150,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t sa = smem_u32(tsm + static_cast<size_t>(s) * kTcStageBytes);
-      const uint32_t sb = sa + kTcABytes;
+      const uint32_t sa = smem_u32(tsm + static_cast<size_t>(s) * kStage);
+      const uint32_t sb = sa + kBOff;
 #pragma unroll
       for (int kk = 0; kk < kTcBK / 16; ++kk) {
-        const uint64_t da = tc_desc_sw128(sa + kk * 32), db = tc_desc_sw128(sb + kk * 32);
-        const uint32_t acc = (kb | kk) != 0;
-        asm volatile(
-            "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-            "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-            "l"(da), "l"(db), "r"(idesc), "r"(acc)
-            : "memory");
+        const uint64_t db = tc_desc_sw128(sb + kk * 32);
+#pragma unroll
+        for (int part = 0; part < (SPLIT ? 2 : 1); ++part) {
+          const uint64_t da = tc_desc_sw128(sa + part * kTcABytes + kk * 32);
+          const uint32_t acc = (kb | kk | part) != 0;
+          asm volatile(
+              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
+              "l"(da), "l"(db), "r"(idesc), "r"(acc)
+              : "memory");
+        }
       }
       // the stage's shared memory is free once these MMAs have read it
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(

@@ -52,6 +52,16 @@ MK_TRAFFIC_PER_ALG_BYTE = (392428032 + 2843392) / 387186688
 PROMPT = 32
 
 
+def measured_bf16_tflops():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"])
+    return 1900.0
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -213,6 +223,86 @@ def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=5, min_bytes=1 << 3
     return per_launch / avg / 1e9, per_launch, avg, n
 
 
+def prefill_config(W, torch, hbm, tflops_peak):
+    """BF16 Qwen3-0.6B shape with chunked prefill (tensor-core projections): the
+    chunk size is tuned on a 2048-token Zipf(1.1) prompt with 8 outputs, then a
+    held-out 4096-token prompt (a different seed) decodes 1024 outputs at that
+    chunk size. TTFT = prompt rows in + first token read back (wall clock)."""
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.QWEN3_06B
+    w = Wl.decoder_weights(s, seed=1, wdtype="bf16")
+
+    def ttft(dec, prompt, chunk):
+        dec.reset()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for c0 in range(0, len(prompt), chunk):
+            last = c0 + chunk >= len(prompt)
+            nxt = dec.prefill([int(t) for t in prompt[c0:c0 + chunk]], is_last=last)
+        return time.perf_counter() - t0, nxt
+
+    tuning = {}
+    prompt = Wl.prompt_zipf(2048, s.vocab, seed=0)
+    for chunk in (128, 256, 512, 1024):
+        dec = Decoder(s, w, kv_dtype="bf16", max_seq=2048 + 16, chunk_cap=chunk)
+        ttft(dec, prompt, chunk)  # warm-up (lazy set-up)
+        runs = [ttft(dec, prompt, chunk)[0] for _ in range(3)]
+        dec.generate(ttft(dec, prompt, chunk)[1], 7)
+        torch.cuda.synchronize()
+        assert dec.device_errors() == 0
+        tuning[chunk] = round(statistics.median(runs) * 1e3, 2)
+        dec.close()
+    best = min(tuning, key=lambda c: (tuning[c], c))  # exact ties go to the smaller chunk
+    P, N = 4096, 1024
+    prompt = Wl.prompt_zipf(P, s.vocab, seed=2)
+    dec = Decoder(s, w, kv_dtype="bf16", max_seq=P + N + 8, chunk_cap=best)
+    ttft(dec, prompt[:best], best)
+    t_first, first = ttft(dec, prompt, best)
+    out = torch.empty(N - 1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    dec.generate(first, N - 1, out)
+    torch.cuda.synchronize()
+    t_dec = time.perf_counter() - t0
+    assert dec.device_errors() == 0
+    dec.close()
+    H, I, d = s.hidden, s.inter, s.head_dim
+    per_layer = (s.q_width + 2 * s.kv_width) * H + H * s.q_width + 2 * I * H + H * I
+    proj_flops = 2.0 * s.layers * per_layer * P
+    attn_flops = 2.0 * 2 * s.layers * s.n_q * d * (P * (P + 1) / 2)
+    mid = P + N // 2
+    dec_bytes = 2 * (s.layers * per_layer + s.vocab * H) + 2 * s.layers * 2 * s.kv_width * (mid + 1) + 4 * s.vocab
+    rate = (N - 1) / t_dec
+    # the projection GEMM alone on one chunk of the chosen size (gate/up shape), timed on the device
+    A = (torch.randn((best, H), device="cuda") * 0.5).to(torch.bfloat16)
+    Wg = (0.02 * torch.randn((2 * I, H), device="cuda")).to(torch.bfloat16)
+    C = torch.empty((best, 2 * I), device="cuda")
+    st = torch.cuda.current_stream()
+    for _ in range(3):
+        W.gemm_bf16(A, Wg, C, best, 2 * I, H, stream=st)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(st)
+    for _ in range(50):
+        W.gemm_bf16(A, Wg, C, best, 2 * I, H, stream=st)
+    e1.record(st)
+    torch.cuda.synchronize()
+    g_sec = e0.elapsed_time(e1) / 1e3 / 50
+    g_tflops = 2.0 * best * 2 * I * H / g_sec / 1e12
+    return {
+        "workload": "Qwen3-0.6B-shaped decoder, BF16 weights and KV cache, chunked prefill (tcgen05 projections), "
+                    "Zipf(1.1) prompts: chunk tuned on 2048 tokens / 8 outputs, held-out 4096 tokens / 1024 outputs",
+        "tuning_ttft_ms": tuning, "chunk": best,
+        "held_out": {"prompt": P, "outputs": N, "ttft_ms": round(t_first * 1e3, 2),
+                     "decode_tokens_per_s": round(rate, 1), "total_s": round(t_first + t_dec, 3),
+                     "decode_step_roofline_frac": round(dec_bytes * rate / 1e9 / hbm, 4),
+                     "prefill_tflops_algorithmic": round((proj_flops + attn_flops) / t_first / 1e12, 2)},
+        "gemm": {"shape": f"{best}x{2 * I}x{H} (chunk rows x gate/up rows x hidden)", "us": round(g_sec * 1e6, 2),
+                 "tflops_algorithmic": round(g_tflops, 1), "peak": tflops_peak, "frac": round(g_tflops / tflops_peak, 4),
+                 "note": "activation operand as bfloat16 value + remainder: 2 MMAs per product"},
+    }
+
+
 def gpu_arm(args):
     import torch
 
@@ -325,6 +415,8 @@ def gpu_arm(args):
                     sweep[f"q4 ntok={ntok} {o}x{i}"] = {"GB/s": round(g, 1), "frac": round(g / hbm, 4),
                                                        "us": round(a * 1e6, 3), "rows_per_warp": best[0]}
             extra["gemv_cold"] = sweep
+        if not args.no_prefill:
+            extra["prefill"] = prefill_config(W, torch, hbm, measured_bf16_tflops())
 
     if rank == 0:
         cpu = None if args.no_cpu else cpu_baseline_sample(weights, prompt, budget_s=args.cpu_seconds)
@@ -425,6 +517,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="skip the cold GEMV sweep")
     ap.add_argument("--engine", default="persistent", choices=["persistent", "staged"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the BF16 chunked-prefill configuration")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = args.steps if args.steps is not None else 5

@@ -425,9 +425,25 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     pf_qk_rope_kv_kernel<KT><<<dim3(n, (g.n_q + 2 * g.n_kv + 3) / 4), 128, 0, st>>>(
         QKV, p0, g.n_q, g.n_kv, d, lw.g_q, lw.g_k, g.eps, rc, rs, kc, vc, g.max_seq);
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
-    auto ak = group <= 2 ? pf_attn_kernel<KT, 2> : pf_attn_kernel<KT, 8>;
-    ak<<<dim3(g.n_kv, (n + kPfAttnRows - 1) / kPfAttnRows), kPfAttnRows * 32, 0, st>>>(
-        QKV, n, p0, g.n_q, g.n_kv, d, kc, vc, g.max_seq, 1.0f / std::sqrt(static_cast<float>(d)), AO, AO2);
+    const float scale = 1.0f / std::sqrt(static_cast<float>(d));
+    bool tc = false;
+    if constexpr (sizeof(KT) == 2) {  // bfloat16 cache: tensor-core attention
+      void (*tk)(const float*, int, int, int, int, const uint16_t*, const uint16_t*, int, float, uint16_t*, uint16_t*) =
+          d == 128 ? pf_attn_tc_kernel<128> : d == 64 ? pf_attn_tc_kernel<64> : d == 32 ? pf_attn_tc_kernel<32>
+                                                                            : d == 16 ? pf_attn_tc_kernel<16> : nullptr;
+      if (tk && 16 % group == 0) {
+        const int rows_per_block = kPfTcWarps * (16 / group);
+        tk<<<dim3(g.n_kv, (n + rows_per_block - 1) / rows_per_block), kPfTcWarps * 32, 0, st>>>(
+            QKV, n, p0, g.n_q, g.n_kv, static_cast<const uint16_t*>(kc), static_cast<const uint16_t*>(vc), g.max_seq,
+            scale, AO, AO2);
+        tc = true;
+      }
+    }
+    if (!tc) {
+      auto ak = group <= 2 ? pf_attn_kernel<KT, 2> : pf_attn_kernel<KT, 8>;
+      ak<<<dim3(g.n_kv, (n + kPfAttnRows - 1) / kPfAttnRows), kPfAttnRows * 32, 0, st>>>(
+          QKV, n, p0, g.n_q, g.n_kv, d, kc, vc, g.max_seq, scale, AO, AO2);
+    }
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     if ((s = gemm(1, wm + 3, X, H, 0, H, qw, true)) != DEC_OK) return s;  // O projection + residual
     pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_post, g.eps, H, AH, AH2);

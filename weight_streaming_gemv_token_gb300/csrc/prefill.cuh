@@ -239,6 +239,197 @@ __global__ void __launch_bounds__(kPfAttnRows * 32) pf_attn_kernel(const float* 
   }
 }
 
+// ---- causal attention on the tensor cores (bfloat16 cache) ----
+//
+// Flash-attention form with warp-level BF16 MMAs (m16n8k16, FP32
+// accumulation): a warp owns 16 query vectors, the group's query heads of
+// 16/group consecutive chunk rows (vector v = row * group + head), all on key
+// head g. For each tile of 64 keys (staged by the block: keys row-major,
+// values transposed, zero past the last key any row needs) the warp forms
+// S = Q K^T, masks keys past each row's position, updates the running max and
+// sum, and accumulates O += P V. Q and P enter the MMAs as bfloat16 value +
+// remainder pairs (two MMAs each), keys and values are the cache's bfloat16,
+// so scores and outputs keep float32 precision. Needs head_dim % 16 == 0 and
+// n_q / n_kv dividing 16.
+constexpr int kPfTcWarps = 4, kPfTcKeys = 64;
+
+__device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two floats as a packed bfloat16 pair (low half: x) for value and remainder.
+__device__ __forceinline__ void pack_split(float x, float y, uint32_t* hi, uint32_t* lo) {
+  const uint16_t hx = f32_to_bf16_rn(x), hy = f32_to_bf16_rn(y);
+  const uint16_t lx = f32_to_bf16_rn(x - bf16_to_f32(hx)), ly = f32_to_bf16_rn(y - bf16_to_f32(hy));
+  *hi = static_cast<uint32_t>(hx) | (static_cast<uint32_t>(hy) << 16);
+  *lo = static_cast<uint32_t>(lx) | (static_cast<uint32_t>(ly) << 16);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfTcWarps * 32) pf_attn_tc_kernel(const float* qkv, int n, int p0, int n_q, int n_kv,
+                                                                      const uint16_t* kc, const uint16_t* vc,
+                                                                      int max_seq, float scale, uint16_t* AO,
+                                                                      uint16_t* AO2) {
+  constexpr int KS = D / 16;  // k-steps of S = Q K^T
+  constexpr int NT = D / 8;   // n-tiles of O
+  __shared__ __align__(16) uint16_t Ks[kPfTcKeys][D + 8];
+  __shared__ __align__(16) uint16_t Vt[D][kPfTcKeys + 8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const int g = blockIdx.x;
+  const int group = n_q / n_kv, rpw = 16 / group;  // rows per warp
+  const int r0 = blockIdx.y * kPfTcWarps * rpw;
+  const int rw = r0 + warp * rpw;                 // first row of this warp
+  const int W = (n_q + 2 * n_kv) * D;
+  const int blk_rows = min(n - r0, kPfTcWarps * rpw);
+  const int pmax = p0 + r0 + blk_rows - 1;         // last key any row of the block sees
+  const int pmax_w = p0 + min(n, rw + rpw) - 1;     // ... and of this warp
+  // this thread's two query vectors: rows of the C fragments
+  const int v0 = gid, v1 = gid + 8;
+  const int row0 = rw + v0 / group, row1 = rw + v1 / group;
+  const int pos0 = p0 + row0, pos1 = p0 + row1;
+  const size_t kv_base = static_cast<size_t>(g) * max_seq * D;
+
+  // Q fragments (value and remainder), zero for rows past the chunk
+  uint32_t qh[KS][4], ql[KS][4];
+  {
+    auto qptr = [&](int v) -> const float* {
+      const int row = rw + v / group;
+      return row < n ? qkv + static_cast<size_t>(row) * W + (g * group + v % group) * D : nullptr;
+    };
+    const float* q0 = qptr(v0);
+    const float* q1 = qptr(v1);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int c = ks * 16 + 2 * tig;
+      pack_split(q0 ? q0[c] : 0.f, q0 ? q0[c + 1] : 0.f, &qh[ks][0], &ql[ks][0]);
+      pack_split(q1 ? q1[c] : 0.f, q1 ? q1[c + 1] : 0.f, &qh[ks][1], &ql[ks][1]);
+      pack_split(q0 ? q0[c + 8] : 0.f, q0 ? q0[c + 9] : 0.f, &qh[ks][2], &ql[ks][2]);
+      pack_split(q1 ? q1[c + 8] : 0.f, q1 ? q1[c + 9] : 0.f, &qh[ks][3], &ql[ks][3]);
+    }
+  }
+  float o[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  for (int t0 = 0; t0 <= pmax; t0 += kPfTcKeys) {
+    __syncthreads();
+    // stage keys t0.. (row-major) and values (transposed); zero past pmax
+    for (int i = threadIdx.x; i < kPfTcKeys * (D / 8); i += kPfTcWarps * 32) {
+      const int kk = i / (D / 8), e = (i - kk * (D / 8)) * 8;
+      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+      if (t0 + kk <= pmax) {
+        const size_t at = kv_base + static_cast<size_t>(t0 + kk) * D + e;
+        kv = __ldg(reinterpret_cast<const uint4*>(kc + at));
+        vv = __ldg(reinterpret_cast<const uint4*>(vc + at));
+      }
+      *reinterpret_cast<uint4*>(&Ks[kk][e]) = kv;
+      const uint16_t* vh = reinterpret_cast<const uint16_t*>(&vv);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) Vt[e + u][kk] = vh[u];
+    }
+    __syncthreads();
+    if (t0 > pmax_w) continue;  // no row of this warp sees these keys
+    // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
+    float sc[kPfTcKeys / 8][4];
+#pragma unroll
+    for (int j = 0; j < kPfTcKeys / 8; ++j) {
+      sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
+      const uint16_t* krow = &Ks[j * 8 + gid][0];
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks * 16 + 2 * tig);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(krow + ks * 16 + 8 + 2 * tig);
+        mma_bf16_16816(sc[j], qh[ks][0], qh[ks][1], qh[ks][2], qh[ks][3], b0, b1);
+        mma_bf16_16816(sc[j], ql[ks][0], ql[ks][1], ql[ks][2], ql[ks][3], b0, b1);
+      }
+    }
+    // mask, scale, running max
+    float mx0 = m0, mx1 = m1;
+#pragma unroll
+    for (int j = 0; j < kPfTcKeys / 8; ++j) {
+      const int t = t0 + j * 8 + 2 * tig;
+      sc[j][0] = t <= pos0 ? sc[j][0] * scale : -INFINITY;
+      sc[j][1] = t + 1 <= pos0 ? sc[j][1] * scale : -INFINITY;
+      sc[j][2] = t <= pos1 ? sc[j][2] * scale : -INFINITY;
+      sc[j][3] = t + 1 <= pos1 ? sc[j][3] * scale : -INFINITY;
+      mx0 = fmaxf(mx0, fmaxf(sc[j][0], sc[j][1]));
+      mx1 = fmaxf(mx1, fmaxf(sc[j][2], sc[j][3]));
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+    // rows with no visible key yet keep max -inf: use 0 as the reference so exp() gives 0
+    const float ref0 = mx0 == -INFINITY ? 0.f : mx0, ref1 = mx1 == -INFINITY ? 0.f : mx1;
+    const float c0 = expf(m0 - ref0), c1 = expf(m1 - ref1);
+    m0 = mx0;
+    m1 = mx1;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int j = 0; j < kPfTcKeys / 8; ++j) {
+      sc[j][0] = expf(sc[j][0] - ref0);
+      sc[j][1] = expf(sc[j][1] - ref0);
+      sc[j][2] = expf(sc[j][2] - ref1);
+      sc[j][3] = expf(sc[j][3] - ref1);
+      s0 += sc[j][0] + sc[j][1];
+      s1 += sc[j][2] + sc[j][3];
+    }
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    l0 = l0 * c0 + s0;
+    l1 = l1 * c1 + s1;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      o[j][0] *= c0;
+      o[j][1] *= c0;
+      o[j][2] *= c1;
+      o[j][3] *= c1;
+    }
+    // O += P V: 4 k-steps of 16 keys; P from the score fragments (value + remainder)
+#pragma unroll
+    for (int kk = 0; kk < kPfTcKeys / 16; ++kk) {
+      uint32_t ah[4], al[4];
+      pack_split(sc[2 * kk][0], sc[2 * kk][1], &ah[0], &al[0]);
+      pack_split(sc[2 * kk][2], sc[2 * kk][3], &ah[1], &al[1]);
+      pack_split(sc[2 * kk + 1][0], sc[2 * kk + 1][1], &ah[2], &al[2]);
+      pack_split(sc[2 * kk + 1][2], sc[2 * kk + 1][3], &ah[3], &al[3]);
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const uint16_t* vrow = &Vt[j * 8 + gid][0];
+        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vrow + kk * 16 + 2 * tig);
+        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vrow + kk * 16 + 8 + 2 * tig);
+        mma_bf16_16816(o[j], ah[0], ah[1], ah[2], ah[3], b0, b1);
+        mma_bf16_16816(o[j], al[0], al[1], al[2], al[3], b0, b1);
+      }
+    }
+  }
+  // O / L as value and remainder
+  const float i0 = 1.0f / l0, i1 = 1.0f / l1;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int c = j * 8 + 2 * tig;
+    if (row0 < n) {
+      const size_t at = static_cast<size_t>(row0) * n_q * D + (g * group + v0 % group) * D + c;
+      pf_split(o[j][0] * i0, AO, AO2, at);
+      pf_split(o[j][1] * i0, AO, AO2, at + 1);
+    }
+    if (row1 < n) {
+      const size_t at = static_cast<size_t>(row1) * n_q * D + (g * group + v1 % group) * D + c;
+      pf_split(o[j][2] * i1, AO, AO2, at);
+      pf_split(o[j][3] * i1, AO, AO2, at + 1);
+    }
+  }
+}
+
 // (AI, AI2)[r][j] = silu(GU[r][j]) * GU[r][I + j] as value and remainder.
 __global__ void pf_swiglu_kernel(const float* GU, int n, int I, uint16_t* AI, uint16_t* AI2) {
   const size_t total = static_cast<size_t>(n) * I;

@@ -200,15 +200,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (row < a.M) {
         float* crow = a.C + static_cast<size_t>(row) * a.ldc + a.col0;
         const int nb = n0 + c0;
+        if (nb + 32 <= a.N && ((reinterpret_cast<uintptr_t>(crow + nb) & 15u) == 0)) {
+          // the row's 32 columns in 16-byte pieces
+          float4* c4 = reinterpret_cast<float4*>(crow + nb);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int col = nb + j;
-          if (col < a.N) {
-            const float x = __uint_as_float(v[j]);
-            if (EPI == TC_ADD)
-              crow[col] += x;
-            else
-              crow[col] = x;
+          for (int j = 0; j < 8; ++j) {
+            float4 x = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                   __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            if (EPI == TC_ADD) {
+              const float4 y = c4[j];
+              x.x += y.x;
+              x.y += y.y;
+              x.z += y.z;
+              x.w += y.w;
+            }
+            c4[j] = x;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = nb + j;
+            if (col < a.N) {
+              const float x = __uint_as_float(v[j]);
+              if (EPI == TC_ADD)
+                crow[col] += x;
+              else
+                crow[col] = x;
+            }
           }
         }
       }

@@ -13,6 +13,9 @@ decode: Qwen3-0.6B-shaped decoder (optionally fewer layers / a smaller
         inside the region.
 gemv:   --count distinct matrices of one shape (sized past L2 by default),
         one warm-up pass, then one launch per matrix inside the region.
+prefill: BF16 Qwen3-0.6B-shaped decoder (optionally fewer layers) with chunked
+        prefill: a --prompt-token Zipf(1.1) prompt in chunks of --chunk rows,
+        one untimed pass, then the whole prompt again inside the region.
 """
 from __future__ import annotations
 
@@ -77,6 +80,37 @@ def gemv(args):
     torch.cuda.profiler.stop()
 
 
+def prefill(args):
+    import dataclasses
+
+    import workloads as Wl
+
+    from . import build
+    from .decoder import Decoder
+
+    build.build()
+    s = Wl.QWEN3_06B
+    if args.layers:
+        s = dataclasses.replace(s, layers=args.layers)
+    w = Wl.decoder_weights(s, seed=1, wdtype="bf16")
+    prompt = Wl.prompt_zipf(args.prompt, s.vocab, seed=0)
+    dec = Decoder(s, w, kv_dtype="bf16", max_seq=args.prompt + 8, chunk_cap=args.chunk)
+
+    def run():
+        dec.reset()
+        for c0 in range(0, args.prompt, args.chunk):
+            last = c0 + args.chunk >= args.prompt
+            dec.prefill([int(t) for t in prompt[c0:c0 + args.chunk]], is_last=last)
+
+    run()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    run()
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    assert dec.device_errors() == 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="mode", required=True)
@@ -94,8 +128,12 @@ def main():
     gm.add_argument("--in", dest="inp", type=int, default=1024)
     gm.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
     gm.add_argument("--count", type=int, default=0)
+    pf = sub.add_parser("prefill")
+    pf.add_argument("--prompt", type=int, default=4096)
+    pf.add_argument("--chunk", type=int, default=1024)
+    pf.add_argument("--layers", type=int, default=0, help="fewer layers than the Qwen3-0.6B shape (0: 28)")
     args = ap.parse_args()
-    decode(args) if args.mode == "decode" else gemv(args)
+    {"decode": decode, "gemv": gemv, "prefill": prefill}[args.mode](args)
 
 
 if __name__ == "__main__":

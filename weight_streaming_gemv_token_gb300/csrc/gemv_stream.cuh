@@ -352,7 +352,7 @@ __device__ __forceinline__ void prefetch_rows_l2(const RowMap& m, int r0, int nr
 // NW warps per CTA; each warp streams its segments through a ring of RING
 // bytes cut into slots of a.seg_bytes (at most NSMAX slots).
 template <typename WT, typename XT, int PRO, int EPI, int NW, int NSMAX, int RING>
-__global__ void __launch_bounds__(NW * 32, 1) gemv_stream_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(NW * 32, 2) gemv_stream_kernel(const GemvArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int NT = NW * 32;
   unsigned char* ring = smem;

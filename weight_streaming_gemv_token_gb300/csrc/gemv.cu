@@ -7,10 +7,12 @@
 // dequantises in registers.
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "common.h"
 #include "gemv_stream.cuh"
+#include "gemv_tma.cuh"
 
 namespace wsg {
 
@@ -37,6 +39,7 @@ dec_status device_info(DeviceInfo* out, std::string* err) {
     cache[dev].major = p.major;
     cache[dev].minor = p.minor;
     cache[dev].smem_optin = p.sharedMemPerBlockOptin;
+    cache[dev].smem_per_sm = p.sharedMemPerMultiprocessor;
   }
   *out = cache[dev];
   return DEC_OK;
@@ -281,9 +284,94 @@ dec_status launch_q4(int R, const uint32_t* codes, const uint16_t* s, const uint
   }
 }
 
+// Split-K geometry of one matrix for gemv_tma_kernel (the persistent decode
+// kernel's rules): 8 column parts (16 when a part would exceed 256 columns),
+// 16-byte aligned; R rows per box minimising the busiest CTA's bytes plus a
+// fixed cost per box; boxes fit one 8 KB slot.
+MkGeom plan_gemv_tma(int out, int in, int elem, int G) {
+  MkGeom m{};
+  const int align = 16 / elem;
+  auto width = [&](int parts) {
+    const int cw = (in + parts - 1) / parts;
+    return (cw + align - 1) / align * align;
+  };
+  m.pw = 1;
+  m.cw = width(kGtWarps);
+  if (m.cw > 256) {
+    m.pw = 2;
+    m.cw = width(2 * kGtWarps);
+  }
+  m.kc = (m.cw + 127) / 128;
+  const int rmax = std::min((elem == 4 ? 16 : 32) / m.kc, kMkSlot / (m.cw * elem));
+  const int lo = out / G, hi = (out + G - 1) / G;  // rows of the CTAs
+  long long best = -1;
+  for (int R = 1; R <= rmax; ++R) {
+    long long worst = 0;
+    for (int nr : {lo, hi})
+      worst = std::max(worst, static_cast<long long>((nr + R - 1) / R) * (static_cast<long long>(R) * m.cw * elem + 2048));
+    if (best < 0 || worst <= best) {
+      best = worst;
+      m.R = R;
+    }
+  }
+  m.box_bytes = m.R * m.cw * elem;
+  m.gchunk = std::max(1, kGtPartRows / m.R);
+  return m;
+}
+
+template <typename WT>
+dec_status launch_gemv_tma(const void* W, const void* x, float* y, int out, int in, cudaStream_t st,
+                           const DeviceInfo& di, bool* used) {
+  *used = false;
+  const int elem = static_cast<int>(sizeof(WT));
+  if (in > kMkMaxWidth || (in * elem) % 16 || !aligned16(W) ||
+      (reinterpret_cast<uintptr_t>(x) % (4 * elem)) != 0)
+    return DEC_OK;
+  const int G = out < di.sms ? out : di.sms;
+  const MkGeom gm = plan_gemv_tma(out, in, elem, G);
+  // shared memory: byte rings, then full/empty barriers, then the partials;
+  // sized for two CTAs per SM when the rings still hold a slot each
+  const size_t fixed = 2 * static_cast<size_t>(kGtWarps) * kGtQ * 8 + static_cast<size_t>(kGtPartRows) * kGtWarps * 4;
+  size_t per_cta = di.smem_per_sm / 2 - 1024 - 256;
+  if (per_cta < fixed + static_cast<size_t>(kGtWarps) * kMkSlot) per_cta = di.smem_optin - 256;
+  size_t ring = (per_cta - fixed) / kGtWarps / 128 * 128;
+  if (ring > 8 * static_cast<size_t>(kMkSlot)) ring = 8 * static_cast<size_t>(kMkSlot);
+  if (ring < static_cast<size_t>(kMkSlot)) return DEC_OK;
+  const size_t smem = static_cast<size_t>(kGtWarps) * ring + fixed;
+  alignas(64) CUtensorMap map;
+  dec_status s = encode_map_2d(&map, W, out, in, elem, gm.cw, gm.R, false, nullptr);
+  if (s != DEC_OK) return s;
+  static bool lifted[64] = {};
+  auto kern = gemv_tma_kernel<WT>;
+  if (!lifted[di.device]) {  // dynamic limit: the device maximum minus the kernel's static shared memory
+    cudaFuncAttributes fa{};
+    WSG_CUDA_TRY(nullptr, cudaFuncGetAttributes(&fa, kern));
+    WSG_CUDA_TRY(nullptr, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(di.smem_optin - fa.sharedSizeBytes)));
+    lifted[di.device] = true;
+  }
+  GtArgs a;
+  a.x = x;
+  a.y = y;
+  a.out = out;
+  a.in = in;
+  a.gm = gm;
+  a.ring_bytes = static_cast<int>(ring);
+  a.err = gemv_err_ptr(di.device);
+  if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv: device error word unavailable");
+  WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(G), dim3(kGtThreads), smem, st, true, map, a));
+  *used = true;
+  return DEC_OK;
+}
+
 template <typename WT, typename XT>
 dec_status launch_gemv(const void* W, const void* x, float* y, int out, int in, cudaStream_t st,
                        const DeviceInfo& di) {
+  {
+    bool used = false;
+    const dec_status s = launch_gemv_tma<WT>(W, x, y, out, in, st, di, &used);
+    if (s != DEC_OK || used) return s;
+  }
   const int row_bytes_ok = (static_cast<long long>(in) * sizeof(WT)) % 16 == 0;
   const long long row_bytes = static_cast<long long>(in) * sizeof(WT);
   if (row_bytes_ok && aligned16(W) && row_bytes < (1ll << 30)) {

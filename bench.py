@@ -49,6 +49,10 @@ METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 # rows a tiled box reads past a CTA's row range. Set to None when the kernel changes until it
 # is measured again.
 MK_TRAFFIC_PER_ALG_BYTE = (392428032 + 2843392) / 387186688
+# DRAM bytes (read + written) per launch of the standalone gemv kernel at 6144x1024 f32, from ncu
+# (profiles/gemv_tma_f32_6144x1024.md: 25,221,376-25,227,264 B read, 0 written over 8 launches);
+# None until measured for the current kernel.
+GEMV_TRAFFIC = 25221632
 PROMPT = 32
 
 
@@ -388,10 +392,10 @@ def gpu_arm(args):
         gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", 6144, 1024, stream, gen=gen)
         extra["roofline" if args.engine != "persistent" else "gemv_roofline"] = {
             "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
-            # ncu dram__bytes_read+write per launch of this kernel on this shape (no writes; 3 launches,
-            # 25,203,456-25,204,992 B); see profiles/gemv_stream_f32_6144x1024_full.md
-            "traffic": 25204224, "peak_kind": peak_kind,
-            "kernel": "gemv_stream_kernel<f32> 6144x1024 (gate/up shape), standalone gemv entry, cold round-robin",
+            # ncu dram__bytes_read+write per launch of this kernel on this shape; None until measured
+            # for the current kernel (profiles/gemv_tma_f32_6144x1024.md)
+            "traffic": GEMV_TRAFFIC, "peak_kind": peak_kind,
+            "kernel": "gemv_tma_kernel<f32> 6144x1024 (gate/up shape), standalone gemv entry, cold round-robin",
             "bytes_per_launch": per_launch, "avg_launch_us": round(avg * 1e6, 3), "launches": launches}
         if not args.no_sweep:
             sweep = {}

@@ -72,7 +72,7 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
 
 /* Decoder geometry and storage ("Megakernels", "What runs in the DSL").
  * Requirements: layers, hidden, inter, n_q, n_kv, head_dim, vocab > 0;
- * n_q % n_kv == 0; head_dim a multiple of 4 and <= 128; hidden, inter and
+ * n_q % n_kv == 0; head_dim a multiple of 8 and <= 128; hidden, inter and
  * n_q*head_dim multiples of 8; wdtype DEC_F32 or DEC_BF16; kvdtype DEC_F32
  * or DEC_BF16; max_seq >= 1 is the KV capacity in positions; chunk_cap is
  * the largest row count of one dec_prefill_chunk call that runs batched

@@ -15,6 +15,7 @@
 // workspace, an atomic counter that the last CTA resets), with no spinning.
 #pragma once
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -48,6 +49,38 @@ __device__ __forceinline__ float4 load4<float>(const void* base, size_t idx) {
 template <>
 __device__ __forceinline__ float4 load4<uint16_t>(const void* base, size_t idx) {
   const uint2 u = __ldcg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + idx));
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xFFFF0000u));
+}
+
+// The elements of a 16-byte piece of a cache row, and of 4 elements of a
+// value row, as floats.
+template <typename KT>
+__device__ __forceinline__ void unpack_piece(const uint4& u, float* f);
+template <>
+__device__ __forceinline__ void unpack_piece<float>(const uint4& u, float* f) {
+  f[0] = __uint_as_float(u.x);
+  f[1] = __uint_as_float(u.y);
+  f[2] = __uint_as_float(u.z);
+  f[3] = __uint_as_float(u.w);
+}
+template <>
+__device__ __forceinline__ void unpack_piece<uint16_t>(const uint4& u, float* f) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <typename KT, typename R>
+__device__ __forceinline__ float4 unpack_row(const R& u);
+template <>
+__device__ __forceinline__ float4 unpack_row<float, uint4>(const uint4& u) {
+  return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+template <>
+__device__ __forceinline__ float4 unpack_row<uint16_t, uint2>(const uint2& u) {
   return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xFFFF0000u), __uint_as_float(u.y << 16),
                      __uint_as_float(u.y & 0xFFFF0000u));
 }
@@ -106,7 +139,11 @@ constexpr int kAttnWarps = 8;
 struct CtaSync {  // barrier over the whole CTA
   __device__ __forceinline__ void operator()() const { __syncthreads(); }
 };
-constexpr int kAttnBatch = 8;  // keys loaded per warp per round trip
+// Keys one warp scores per round trip (a chunk): every load of a chunk, its
+// key rows and value rows, is issued at once; the rows then take 64 + 64
+// registers per lane for 128-element heads.
+template <typename KT>
+constexpr int kAttnChunk = sizeof(KT) == 2 ? 32 : 16;
 
 inline size_t attn_smem_bytes(int group, int d) {
   // qn[group][d], kn[d], vn[d], per-warp (m, l)[group] and o[group][d], then
@@ -162,7 +199,7 @@ struct AttnPlainIo {
   __device__ __forceinline__ void poll_parts(size_t, size_t, int, int, int, float*, float*, float*) const {}
 };
 
-template <typename KT, int GMAX, int NT, typename Sync, int BATCH = kAttnBatch, typename Io = AttnPlainIo>
+template <typename KT, int GMAX, int NT, typename Sync, int CK = kAttnChunk<KT>, typename Io = AttnPlainIo>
 __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s, int pos, float* asmem, int tid,
                                                  Sync sync, int* s_last, Io io = Io{}) {
   static_assert(NT == kAttnWarps * 32, "the split layout assumes kAttnWarps warps");
@@ -182,27 +219,56 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
 
   const int kraw = a.n_q * d + g * d;
   const int vraw = a.n_q * d + a.n_kv * d + g * d;
-  // Each lane owns 4 consecutive elements [4 lane, 4 lane + 4) of a head vector;
-  // each warp takes a contiguous run of this CTA's keys, BATCH at a time, the
-  // next batch in flight while the current one is scored.
+  // Each warp takes a contiguous run of this CTA's keys, CK at a time.
+  // Scores: 4 lanes per key, 8 keys per pass; lane (4 kq + sub) reads the
+  // 16-byte pieces sub, sub + 4, ... of its key's row (a key's 4 lanes read
+  // 64 contiguous bytes per load), dots them with q from shared memory, and
+  // two shuffles add the 4 partial dots. Values: lane owns the 4 elements
+  // [4 lane, 4 lane + 4) of every value row (one coalesced row per load),
+  // weighted by the key's probability, shuffled from the key's lanes.
+  static_assert(CK % 8 == 0, "a chunk is whole passes of 8 keys");
+  constexpr int PE = 16 / static_cast<int>(sizeof(KT));  // elements per 16-byte piece
+  constexpr int NPL = 128 / PE / 4;                        // pieces per lane per row (d <= 128)
+  constexpr int NPASS = CK / 8;
+  using VRow = typename std::conditional<sizeof(KT) == 2, uint2, uint4>::type;  // 4 elements
   const bool active = 4 * lane < d;
+  const int kq = lane >> 2, sub = lane & 3;
+  const int npieces = d / PE;
   const int per_w = (t1 - t0 + kAttnWarps - 1) / kAttnWarps;
   const int w0 = t0 + warp * per_w;
   const int w1 = min(t1, w0 + per_w);
   const size_t head_base = static_cast<size_t>(g) * a.max_seq * d;
-  auto fetch = [&](int tb, float4* kk, float4* vv) {
+  const unsigned char* kbytes = static_cast<const unsigned char*>(a.kc) + head_base * sizeof(KT);
+  const unsigned char* vbytes = static_cast<const unsigned char*>(a.vc) + head_base * sizeof(KT);
+  const size_t row_bytes = static_cast<size_t>(d) * sizeof(KT);
+  uint4 kr[NPASS][NPL];
+  VRow vr[CK];
+  // The current position's row is not read from the cache (it is written by
+  // this kernel): its key and value come from shared memory instead.
+  auto issue = [&](int cb) {
 #pragma unroll
-    for (int u = 0; u < BATCH; ++u) {
-      const int t = tb + u;
-      kk[u] = vv[u] = make_float4(0, 0, 0, 0);
-      if (t < w1 && active && t != pos) {
-        kk[u] = load4<KT>(a.kc, head_base + static_cast<size_t>(t) * d + 4 * lane);
-        vv[u] = load4<KT>(a.vc, head_base + static_cast<size_t>(t) * d + 4 * lane);
+    for (int ps = 0; ps < NPASS; ++ps) {
+      const int t = cb + ps * 8 + kq;
+      const bool ok = t < w1 && t != pos;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int pc = i * 4 + sub;
+        kr[ps][i] = (ok && pc < npieces)
+                        ? __ldcg(reinterpret_cast<const uint4*>(kbytes + static_cast<size_t>(t) * row_bytes) + pc)
+                        : make_uint4(0, 0, 0, 0);
       }
+    }
+#pragma unroll
+    for (int j = 0; j < CK; ++j) {
+      const int t = cb + j;
+      VRow z{};
+      vr[j] = (t < w1 && t != pos && active)
+                  ? __ldcg(reinterpret_cast<const VRow*>(vbytes + static_cast<size_t>(t) * row_bytes) + lane)
+                  : z;
     }
   };
   // Nothing below depends on this token until its q/k/v arrive: the gains,
-  // the RoPE row and the first batch of cached keys/values are requested
+  // the RoPE row and the first chunk of cached keys/values are requested
   // before waiting for them.
   float tv[2];
 #pragma unroll
@@ -214,8 +280,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
                   : i < 2 * d ? __ldg(a.g_k + i - d)
                               : i < 2 * d + half ? __ldg(cs + i - 2 * d) : i < 3 * d ? __ldg(sn + i - 2 * d - half) : 0.f;
   }
-  float4 nk[BATCH], nv[BATCH];
-  fetch(w0, nk, nv);
+  if (w0 < w1) issue(w0);
   io.load_all(qn, kn, vn, (g * group) * d, kraw, vraw, group * d, d, tid, NT);
   for (int i = tid; i < d; i += NT) vn[i] = round_store<KT>(vn[i]);
 #pragma unroll
@@ -235,10 +300,6 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     }
   }
 
-  float4 q[GMAX];
-#pragma unroll
-  for (int h = 0; h < GMAX; ++h)
-    q[h] = (h < group && active) ? *reinterpret_cast<const float4*>(qn + h * d + 4 * lane) : make_float4(0, 0, 0, 0);
   float m[GMAX], l[GMAX];
   float4 o[GMAX];
 #pragma unroll
@@ -248,45 +309,97 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
     o[h] = make_float4(0, 0, 0, 0);
   }
 
-  for (int tb = w0; tb < w1; tb += BATCH) {
-    float4 kk[BATCH], vv[BATCH];
+  for (int cb = w0; cb < w1; cb += CK) {
+    if (cb != w0) issue(cb);
+    // scores of this lane's key in every pass, for every head
+    float sc[NPASS][GMAX];
 #pragma unroll
-    for (int u = 0; u < BATCH; ++u) {
-      kk[u] = nk[u];
-      vv[u] = nv[u];
-      if (tb + u == pos && tb + u < w1 && active) {  // the current token: from shared memory
-        kk[u] = *reinterpret_cast<const float4*>(kn + 4 * lane);
-        vv[u] = *reinterpret_cast<const float4*>(vn + 4 * lane);
+    for (int ps = 0; ps < NPASS; ++ps) {
+      const int t = cb + ps * 8 + kq;
+      const bool cur = t == pos;
+      float acc[GMAX];
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+#pragma unroll
+      for (int i = 0; i < NPL; ++i) {
+        const int pc = i * 4 + sub;
+        if (pc < npieces) {
+          float kf[PE];
+          unpack_piece<KT>(kr[ps][i], kf);
+          if (cur) {
+#pragma unroll
+            for (int e = 0; e < PE; e += 4) {
+              const float4 c4 = *reinterpret_cast<const float4*>(kn + pc * PE + e);
+              kf[e] = c4.x;
+              kf[e + 1] = c4.y;
+              kf[e + 2] = c4.z;
+              kf[e + 3] = c4.w;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < GMAX; ++h) {
+            if (h >= group) break;
+#pragma unroll
+            for (int e = 0; e < PE; e += 4) {
+              const float4 q4 = *reinterpret_cast<const float4*>(qn + h * d + pc * PE + e);
+              acc[h] = fmaf(q4.x, kf[e], acc[h]);
+              acc[h] = fmaf(q4.y, kf[e + 1], acc[h]);
+              acc[h] = fmaf(q4.z, kf[e + 2], acc[h]);
+              acc[h] = fmaf(q4.w, kf[e + 3], acc[h]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 1);
+        acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], 2);
+        sc[ps][h] = t < w1 ? acc[h] * a.scale : -INFINITY;
       }
     }
-    if (tb + BATCH < w1) fetch(tb + BATCH, nk, nv);
+    // online softmax over the chunk; pr = this lane's key's probability per pass
+    float pr[NPASS][GMAX];
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
       if (h >= group) break;
-      float sc[BATCH];
-      float mx = m[h];
+      float mx = sc[0][h];
 #pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        const float dot = q[h].x * kk[u].x + q[h].y * kk[u].y + q[h].z * kk[u].z + q[h].w * kk[u].w;
-        sc[u] = (tb + u < w1) ? warp_sum(dot) * a.scale : -INFINITY;
-        mx = fmaxf(mx, sc[u]);
+      for (int ps = 1; ps < NPASS; ++ps) mx = fmaxf(mx, sc[ps][h]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mn = fmaxf(m[h], mx);
+      const float corr = expf(m[h] - mn);
+      float ls = 0.f;
+#pragma unroll
+      for (int ps = 0; ps < NPASS; ++ps) {
+        pr[ps][h] = expf(sc[ps][h] - mn);
+        ls += pr[ps][h];
       }
-      const float corr = expf(m[h] - mx);
-      l[h] *= corr;
+      ls += __shfl_xor_sync(0xffffffffu, ls, 4);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 8);
+      ls += __shfl_xor_sync(0xffffffffu, ls, 16);
+      l[h] = fmaf(l[h], corr, ls);
       o[h].x *= corr;
       o[h].y *= corr;
       o[h].z *= corr;
       o[h].w *= corr;
+      m[h] = mn;
+    }
 #pragma unroll
-      for (int u = 0; u < BATCH; ++u) {
-        const float p = expf(sc[u] - mx);
-        l[h] += p;
-        o[h].x = fmaf(p, vv[u].x, o[h].x);
-        o[h].y = fmaf(p, vv[u].y, o[h].y);
-        o[h].z = fmaf(p, vv[u].z, o[h].z);
-        o[h].w = fmaf(p, vv[u].w, o[h].w);
+    for (int j = 0; j < CK; ++j) {
+      if (cb + j >= w1) break;
+      float4 v = unpack_row<KT>(vr[j]);
+      if (cb + j == pos && active) v = *reinterpret_cast<const float4*>(vn + 4 * lane);
+#pragma unroll
+      for (int h = 0; h < GMAX; ++h) {
+        if (h >= group) break;
+        const float pj = __shfl_sync(0xffffffffu, pr[j >> 3][h], (j & 7) * 4);
+        o[h].x = fmaf(pj, v.x, o[h].x);
+        o[h].y = fmaf(pj, v.y, o[h].y);
+        o[h].z = fmaf(pj, v.z, o[h].z);
+        o[h].w = fmaf(pj, v.w, o[h].w);
       }
-      m[h] = mx;
     }
   }
 
@@ -395,7 +508,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, ERR_BAD_POSITION);
     return;
   }
-  attn_decode_body<KT, GMAX, kAttnWarps * 32, CtaSync, GMAX <= 2 ? kAttnBatch : kAttnBatch / 2>(a, blockIdx.x, blockIdx.y, pos, asmem, threadIdx.x, CtaSync{}, &s_last,
+  if (threadIdx.x == 0) {  // this CTA's cached rows (before pos) into L2 at once
+    int t0, t1, ns;
+    if (attn_split_range(a, blockIdx.y, pos, &t0, &t1, &ns) && min(t1, pos) > t0) {
+      const size_t rb = static_cast<size_t>(a.d) * sizeof(KT);
+      const size_t off = (static_cast<size_t>(blockIdx.x) * a.max_seq + t0) * rb;
+      const uint32_t bytes = static_cast<uint32_t>((min(t1, pos) - t0) * rb);
+      bulk_prefetch_l2(static_cast<const char*>(a.kc) + off, bytes);
+      bulk_prefetch_l2(static_cast<const char*>(a.vc) + off, bytes);
+    }
+  }
+  attn_decode_body<KT, GMAX, kAttnWarps * 32, CtaSync, GMAX <= 2 ? kAttnChunk<KT> : kAttnChunk<KT> / 2>(a, blockIdx.x, blockIdx.y, pos, asmem, threadIdx.x, CtaSync{}, &s_last,
                                               AttnPlainIo{a.qkv, a.out});
 }
 

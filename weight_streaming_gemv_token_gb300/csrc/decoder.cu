@@ -70,7 +70,7 @@ bool config_ok(const dec_config* c, std::string* why) {
     return bad("every geometry field must be positive");
   if (c->n_q % c->n_kv) return bad("n_q must be a multiple of n_kv");
   if (c->n_q / c->n_kv > 8) return bad("at most 8 query heads per key/value head");
-  if (c->head_dim % 4 || c->head_dim > 128) return bad("head_dim must be a multiple of 4 and <= 128");
+  if (c->head_dim % 8 || c->head_dim > 128) return bad("head_dim must be a multiple of 8 and <= 128");
   if (c->hidden % 8 || c->inter % 8 || (c->n_q * c->head_dim) % 8)
     return bad("hidden, inter and n_q*head_dim must be multiples of 8");
   if (c->wdtype != DEC_F32 && c->wdtype != DEC_BF16) return bad("wdtype must be DEC_F32 or DEC_BF16");

@@ -989,7 +989,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         stamp(step, l, 1, 0);
-        attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? 4 : 2), AttnLlIo>(
+        attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? kAttnChunk<KT> / 2 : 8), AttnLlIo>(
             at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
             AttnLlIo{a.ll_qkv, a.ll_attn, a.ll_apart, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV),
                      mk_tag(a, step, l, 1), vabort, a.err,

@@ -44,8 +44,15 @@ def decode(args):
         s = dataclasses.replace(s, layers=args.layers or s.layers, vocab=args.vocab or s.vocab)
     w = Wl.decoder_weights(s, seed=1, wdtype=args.dtype)
     prompt = Wl.prompt_uniform(args.prompt, s.vocab, seed=0)
-    dec = Decoder(s, w, kv_dtype=args.kv, max_seq=args.prompt + args.warmup + args.steps + 4, engine=args.engine)
-    first = dec.prefill(prompt, is_last=True)
+    dec = Decoder(s, w, kv_dtype=args.kv, max_seq=args.prompt + args.warmup + args.steps + 4, engine=args.engine,
+                  chunk_cap=args.chunk)
+    if args.chunk:
+        for c0 in range(0, args.prompt - args.chunk, args.chunk):
+            dec.prefill([int(t) for t in prompt[c0:c0 + args.chunk]], is_last=False)
+        c0 = (args.prompt - 1) // args.chunk * args.chunk
+        first = dec.prefill([int(t) for t in prompt[c0:]], is_last=True)
+    else:
+        first = dec.prefill(prompt, is_last=True)
     out = dec.generate(first, args.warmup)
     torch.cuda.synchronize()
     tok = int(out[-1].item())
@@ -123,6 +130,7 @@ def main():
     d.add_argument("--layers", type=int, default=0, help="fewer layers than the Qwen3-0.6B shape (0: 28)")
     d.add_argument("--vocab", type=int, default=0, help="smaller vocabulary (0: 151936)")
     d.add_argument("--engine", default="persistent", choices=["persistent", "staged"])
+    d.add_argument("--chunk", type=int, default=0, help="prefill the prompt in chunks of this many rows (bf16 only)")
     gm = sub.add_parser("gemv")
     gm.add_argument("--out", type=int, default=6144)
     gm.add_argument("--in", dest="inp", type=int, default=1024)

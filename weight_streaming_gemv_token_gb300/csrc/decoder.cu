@@ -522,9 +522,9 @@ MkGeom mk_geom_for(const dec_config& g, int st, int in, int elem, int G) {
     m.cw = width(2 * kMkWarps);
   }
   m.kc = (m.cw + 127) / 128;
-  // rows per box: the consumer holds at most 16 (f32) / 32 (bf16) 4-element
-  // weight groups per lane, i.e. that many rows of a one-chunk part
-  const int rmax = std::min((elem == 4 ? 16 : 32) / m.kc, kMkSlot / (m.cw * elem));
+  // rows per box: the consumer unrolls over at most kMkRowsMax rows of a
+  // one-chunk part (its code stays small enough to stay in the instruction cache)
+  const int rmax = std::min(kMkRowsMax / m.kc, kMkSlot / (m.cw * elem));
   constexpr long long kBoxCost = 2048;
   long long best = -1;
   for (int R = 1; R <= rmax; ++R) {

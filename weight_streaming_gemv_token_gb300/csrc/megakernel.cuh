@@ -69,6 +69,7 @@ constexpr int kMkQ = 8;               // boxes in flight per warp, at most (one 
 constexpr int kMkMapsPerLayer = 7;    // tensor maps per layer: wq wk wv wo wg wu wd
 constexpr int kMkMapBytes = 128;      // one CUtensorMap
 constexpr int kMkXr = 4;              // float4 of x per lane: parts per warp (<= 2) x 128-column chunks (<= 2)
+constexpr int kMkRowsMax = 16;       // rows of one-chunk part per box (the consumer unrolls over them)
 constexpr int kMkPartRows = 256;      // row capacity of the shared partials of one epilogue chunk (at least)
 
 enum : uint32_t { ERR_EXCHANGE_TIMEOUT = 1u << 4 };
@@ -832,7 +833,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   auto consume_kc = [&](auto kc_tag, const MkStageT& st, const MkGeom& gm, const float4(&xr)[kMkXr],
                         auto&& epi) -> bool {
     constexpr int KC = decltype(kc_tag)::value;
-    constexpr int RM = 16 * static_cast<int>(4 / sizeof(WT)) / KC;  // rows per box, at most
+    constexpr int RM = kMkRowsMax / KC;  // rows per box, at most
     constexpr int kSh = RM == 32 ? 0 : RM == 16 ? 1 : RM == 8 ? 2 : 3;
     using W = MkW4<WT>;
     const int R = gm.R, pw = gm.pw, cw = gm.cw, gchunk = gm.gchunk;

@@ -944,23 +944,55 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       const void* const* lp = layer_ptrs(l);
       const float* g_in = static_cast<const float*>(lp[7]);
       const float* g_post = static_cast<const float*>(lp[8]);
-      // ---- QKV with the input RMSNorm (layer 0: of the token's embedding row) ----
-      {
-        stamp(step, l, 0, 0);
-        const MkStageT& st = s_stage[MK_QKV];
-        if (st.nloc > 0) {
-          if (l == 0)
-            stage_embed(tok, g_in, a.gq, xr);
-          else
-            stage_x(a.ll_h, mk_tag(a, step, l - 1, MK_DOWN), a.H, g_in, a.gq, xr);
+      // The four projections of the layer run through one copy of the staging,
+      // consume and epilogue code (a loop over the stage kind, its inputs and
+      // epilogue picked at run time): five unrolled copies of the consumer's
+      // dot loop do not stay in the instruction cache together.
+      for (int sid = MK_QKV; sid <= MK_DOWN; ++sid) {
+        if (sid == MK_O && attn_cta) {
+          // ---- attention (Q/K norm, RoPE, KV append, key-parallel splits) ----
+          AttnArgs at = a.at;
+          at.g_q = static_cast<const float*>(lp[9]);
+          at.g_k = static_cast<const float*>(lp[10]);
+          at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
+          at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
+          stamp(step, l, 1, 0);
+          attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? kAttnChunk<KT> / 2 : 8), AttnLlIo>(
+              at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
+              AttnLlIo{a.ll_qkv, a.ll_attn, a.ll_apart, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV),
+                       mk_tag(a, step, l, 1), vabort, a.err,
+                       (a.trace && step == 0)
+                           ? a.trace + ((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + 1) * kMkTraceEvents
+                           : nullptr});
+          stamp(step, l, 1, 2);
+          consumer_sync();  // the attention scratch is reused by the next layer's attention
         }
-        stamp(step, l, 0, 1);
-        // Keys and values before pos do not depend on this token: make sure the
-        // rows of earlier positions are published (acquire) and pull this
-        // CTA's attention range of them into L2 while QKV runs.
-        if (tid == 0 && attn_cta && pos > 0)
-          wait_at_least(a.kv_ready + l * a.n_kv + c % a.n_kv, static_cast<uint32_t>(pos), vabort, a.err);
-        if (tid == 0 && attn_cta) {
+        const int ts = sid == MK_QKV ? 0 : sid + 1;  // trace stage (1 is attention)
+        const MkStageT& st = s_stage[sid];
+        const MkGeom& gm = sid == MK_QKV ? a.gq : sid == MK_O ? a.go : sid == MK_GU ? a.gg : a.gd;
+        stamp(step, l, ts, 0);
+        if (st.nloc > 0) {
+          if (sid == MK_QKV && l == 0) {
+            stage_embed(tok, g_in, gm, xr);  // the token's embedding row, with the input RMSNorm
+          } else {
+            // QKV: previous layer's residual (input RMSNorm); O: attention output;
+            // GU: residual after attention (post-attention RMSNorm); DOWN: SwiGLU output
+            const uint64_t* src = sid == MK_QKV ? a.ll_h : sid == MK_O ? a.ll_attn : sid == MK_GU ? a.ll_h : a.ll_act;
+            const uint32_t tin = sid == MK_QKV ? mk_tag(a, step, l - 1, MK_DOWN)
+                                 : sid == MK_O  ? mk_tag(a, step, l, 1)
+                                 : sid == MK_GU ? mk_tag(a, step, l, MK_O)
+                                                : mk_tag(a, step, l, MK_GU);
+            const int n = sid == MK_O ? qw : sid == MK_DOWN ? a.I : a.H;
+            const float* gain = sid == MK_QKV ? g_in : sid == MK_GU ? g_post : nullptr;
+            stage_x(src, tin, n, gain, gm, xr);
+          }
+        }
+        stamp(step, l, ts, 1);
+        if (sid == MK_QKV && tid == 0 && attn_cta) {
+          // Keys and values before pos do not depend on this token: make sure the
+          // rows of earlier positions are published (acquire) and pull this
+          // CTA's attention range of them into L2 while QKV runs.
+          if (pos > 0) wait_at_least(a.kv_ready + l * a.n_kv + c % a.n_kv, static_cast<uint32_t>(pos), vabort, a.err);
           int t0, t1, ns;
           if (attn_split_range(a.at, c / a.n_kv, pos, &t0, &t1, &ns)) {
             t1 = min(t1, pos);
@@ -974,85 +1006,30 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
             }
           }
         }
-        const uint32_t tg = mk_tag(a, step, l, MK_QKV);
-        if (!(ok = consume(st, a.gq, xr, [&](int cg, int) {
-              for (int lr = tid; lr < st.nloc; lr += kMkConsumers)
-                ll_store(a.ll_qkv + st.u0 + lr, row_value(st, a.gq, cg, lr), tg);
-            })))
-          break;
-        stamp(step, l, 0, 2);
-      }
-      // ---- attention (Q/K norm, RoPE, KV append, key-parallel splits) ----
-      if (attn_cta) {
-        AttnArgs at = a.at;
-        at.g_q = static_cast<const float*>(lp[9]);
-        at.g_k = static_cast<const float*>(lp[10]);
-        at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
-        at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
-        stamp(step, l, 1, 0);
-        attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? kAttnChunk<KT> / 2 : 8), AttnLlIo>(
-            at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
-            AttnLlIo{a.ll_qkv, a.ll_attn, a.ll_apart, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV),
-                     mk_tag(a, step, l, 1), vabort, a.err,
-                     (a.trace && step == 0)
-                         ? a.trace + ((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + 1) * kMkTraceEvents
-                         : nullptr});
-        stamp(step, l, 1, 2);
-        consumer_sync();  // the attention scratch is reused by the next layer's attention
-      }
-      // ---- O projection + residual ----
-      {
-        stamp(step, l, 2, 0);
-        const MkStageT& st = s_stage[MK_O];
-        if (st.nloc > 0) stage_x(a.ll_attn, mk_tag(a, step, l, 1), qw, nullptr, a.go, xr);
-        stamp(step, l, 2, 1);
-        const uint32_t tg = mk_tag(a, step, l, MK_O);
-        if (!(ok = consume(st, a.go, xr, [&](int cg, int) {
-              for (int lr = tid; lr < st.nloc; lr += kMkConsumers) {
-                const int row = st.u0 + lr;
-                const float prev =
-                    l == 0 ? load_f32<WT>(static_cast<const WT*>(a.embed) + static_cast<size_t>(tok) * a.H, row)
-                           : hown[lr];
-                const float hn = prev + row_value(st, a.go, cg, lr);
-                hown[lr] = hn;
-                ll_store(a.ll_h + row, hn, tg);
-              }
-            })))
-          break;
-        stamp(step, l, 2, 2);
-      }
-      // ---- gate/up with the post-attention RMSNorm, SwiGLU ----
-      {
-        stamp(step, l, 3, 0);
-        const MkStageT& st = s_stage[MK_GU];
-        if (st.nloc > 0) stage_x(a.ll_h, mk_tag(a, step, l, MK_O), a.H, g_post, a.gg, xr);
-        stamp(step, l, 3, 1);
-        const uint32_t tg = mk_tag(a, step, l, MK_GU);
-        if (!(ok = consume(st, a.gg, xr, [&](int cg, int) {
-              const int np = st.nloc >> 1;
-              for (int i = tid; i < np; i += kMkConsumers)
-                ll_store(a.ll_act + st.u0 + i,
-                         silu_f32(row_value(st, a.gg, cg, i)) * row_value(st, a.gg, cg, np + i), tg);
-            })))
-          break;
-        stamp(step, l, 3, 2);
-      }
-      // ---- down projection + residual ----
-      {
-        stamp(step, l, 4, 0);
-        const MkStageT& st = s_stage[MK_DOWN];
-        if (st.nloc > 0) stage_x(a.ll_act, mk_tag(a, step, l, MK_GU), a.I, nullptr, a.gd, xr);
-        stamp(step, l, 4, 1);
-        const uint32_t tg = mk_tag(a, step, l, MK_DOWN);
-        if (!(ok = consume(st, a.gd, xr, [&](int cg, int) {
-              for (int lr = tid; lr < st.nloc; lr += kMkConsumers) {
-                const float hn = hown[lr] + row_value(st, a.gd, cg, lr);
-                hown[lr] = hn;
-                ll_store(a.ll_h + st.u0 + lr, hn, tg);
-              }
-            })))
-          break;
-        stamp(step, l, 4, 2);
+        const uint32_t tg = mk_tag(a, step, l, sid);
+        ok = consume(st, gm, xr, [&](int cg, int) {
+          if (sid == MK_QKV) {
+            for (int lr = tid; lr < st.nloc; lr += kMkConsumers) ll_store(a.ll_qkv + st.u0 + lr, row_value(st, gm, cg, lr), tg);
+          } else if (sid == MK_GU) {
+            const int np = st.nloc >> 1;
+            for (int i = tid; i < np; i += kMkConsumers)
+              ll_store(a.ll_act + st.u0 + i, silu_f32(row_value(st, gm, cg, i)) * row_value(st, gm, cg, np + i), tg);
+          } else {
+            // O and DOWN: residual add into this CTA's rows of h (layer 0's O adds
+            // to the embedding row)
+            for (int lr = tid; lr < st.nloc; lr += kMkConsumers) {
+              const int row = st.u0 + lr;
+              const float prev = (sid == MK_O && l == 0)
+                                     ? load_f32<WT>(static_cast<const WT*>(a.embed) + static_cast<size_t>(tok) * a.H, row)
+                                     : hown[lr];
+              const float hn = prev + row_value(st, gm, cg, lr);
+              hown[lr] = hn;
+              ll_store(a.ll_h + row, hn, tg);
+            }
+          }
+        });
+        if (!ok) break;
+        stamp(step, l, ts, 2);
       }
     }
     if (!ok || *vabort || !mk_head_on(a, step)) continue;

@@ -503,11 +503,11 @@ void mk_pieces(const dec_config& g, int st, int c, int G, int nr[3]) {
   }
 }
 
-// Split-K geometry of stage st (input width `in`): 8 column parts (16 when a
-// part would exceed 256 columns, the TMA box limit), each 16-byte aligned;
-// R rows per box chosen to minimise the busiest CTA's streamed bytes plus a
-// fixed cost per box (a copy of a few KB runs below the streaming rate of
-// larger ones); boxes fit one ring slot.
+// Split-K geometry of stage st (input width `in`): 8 column parts, one per
+// consumer warp (16 when a part would exceed 256 columns, the TMA box limit;
+// 4, two warps each, when 8 parts would be at most 128 columns), each 16-byte
+// aligned; R rows per box chosen to minimise the busiest warp's streamed
+// bytes plus a fixed cost per box; boxes fit one ring slot.
 MkGeom mk_geom_for(const dec_config& g, int st, int in, int elem, int G) {
   MkGeom m{};
   const int align = 16 / elem;
@@ -516,10 +516,17 @@ MkGeom mk_geom_for(const dec_config& g, int st, int in, int elem, int G) {
     return (cw + align - 1) / align * align;
   };
   m.pw = 1;
+  m.wpp = 1;
   m.cw = width(kMkWarps);
   if (m.cw > 256) {
     m.pw = 2;
     m.cw = width(2 * kMkWarps);
+  } else if (m.cw <= 128) {
+    // narrow inputs: 4 parts of up to 256 columns, two warps each (alternate
+    // row groups). A box then holds fewer, longer rows for the same bytes,
+    // so a warp reduces fewer rows per byte.
+    m.wpp = 2;
+    m.cw = width(kMkWarps / 2);
   }
   m.kc = (m.cw + 127) / 128;
   // rows per box: the consumer unrolls over at most kMkRowsMax rows of a
@@ -528,13 +535,16 @@ MkGeom mk_geom_for(const dec_config& g, int st, int in, int elem, int G) {
   constexpr long long kBoxCost = 2048;
   long long best = -1;
   for (int R = 1; R <= rmax; ++R) {
+    // the busiest warp of the busiest CTA: its boxes' bytes plus a fixed cost
+    // per box (a copy of a few KB runs below the streaming rate of larger ones)
     long long worst = 0;
     for (int c = 0; c < G; ++c) {
       int nr[3];
       mk_pieces(g, st, c, G, nr);
-      long long cost = 0;
-      for (int p = 0; p < 3; ++p)
-        cost += static_cast<long long>((nr[p] + R - 1) / R) * (static_cast<long long>(R) * m.cw * elem + kBoxCost);
+      long long ng = 0;
+      for (int p = 0; p < 3; ++p) ng += (nr[p] + R - 1) / R;
+      const long long cost =
+          (ng + m.wpp - 1) / m.wpp * m.pw * (static_cast<long long>(R) * m.cw * elem + kBoxCost);
       worst = std::max(worst, cost);
     }
     if (best < 0 || worst <= best) {

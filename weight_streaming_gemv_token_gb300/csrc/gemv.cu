@@ -290,6 +290,7 @@ dec_status launch_q4(int R, const uint32_t* codes, const uint16_t* s, const uint
 // fixed cost per box; boxes fit one 8 KB slot.
 MkGeom plan_gemv_tma(int out, int in, int elem, int G) {
   MkGeom m{};
+  m.wpp = 1;  // one warp per column part
   const int align = 16 / elem;
   auto width = [&](int parts) {
     const int cw = (in + parts - 1) / parts;

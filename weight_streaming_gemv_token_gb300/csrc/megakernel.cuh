@@ -90,7 +90,15 @@ struct MkGeom {
   int32_t R;          // rows per box
   int32_t box_bytes;  // R * cw * element size
   int32_t gchunk;     // row groups per epilogue chunk
+  int32_t wpp;        // warps per part: 1, or 2 (one-part stages over 4 parts: warp w takes
+                      // part w % 4 and the row groups whose index has the parity of w / 4)
 };
+
+// Column part of warp w, and which of the part's warps it is (its row groups
+// are those with index % wpp == sub).
+__device__ __forceinline__ int mk_part(const MkGeom& g, int w) { return g.wpp == 2 ? (w & 3) : w; }
+__device__ __forceinline__ int mk_sub(const MkGeom& g, int w) { return g.wpp == 2 ? (w >> 2) : 0; }
+__device__ __forceinline__ int mk_wpp(const MkGeom& g) { return g.wpp == 2 ? 2 : 1; }
 
 struct MkArgs {
   const MkLayer* layers;  // device array [L]
@@ -492,6 +500,7 @@ struct MkCursor {
   int j, n;             // next box of the stage, boxes in the stage
   int t0, t1, t2, row0, row1, row2, g1, g2;
   int pw, cw, R, box_bytes;
+  int part, sub, wpp;   // this lane's warp: its column part, row-group parity, warps per part
   bool done;
 };
 
@@ -578,7 +587,10 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       const MkStageT& t = s_stage[cur.st];
       const MkGeom& gm = mk_geom(a, cur.st);
       cur.j = 0;
-      cur.n = t.ng * gm.pw;
+      cur.wpp = mk_wpp(gm);
+      cur.part = mk_part(gm, lane);
+      cur.sub = mk_sub(gm, lane);
+      cur.n = (t.ng > cur.sub ? (t.ng - cur.sub + cur.wpp - 1) / cur.wpp : 0) * gm.pw;  // this warp's row groups
       if (cur.n > 0) {
         cur.t0 = t.t0, cur.t1 = t.t1, cur.t2 = t.t2;
         cur.row0 = t.row0, cur.row1 = t.row1, cur.row2 = t.row2;
@@ -633,14 +645,16 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         }
         const int n = issued - retired;
         if (n > 0 && v + B - qv[0] > RB) break;  // not free yet
-        const int rg = cur.pw == 2 ? (cur.j >> 1) : cur.j, pj = cur.j - rg * cur.pw;
+        const int li = cur.pw == 2 ? (cur.j >> 1) : cur.j, pj = cur.j - li * cur.pw;
+        const int rg = cur.sub + cur.wpp * li;  // row group of this box
         const bool p0 = rg < cur.g1, p1 = !p0 && rg < cur.g2;
         const int gl = rg - (p0 ? 0 : p1 ? cur.g1 : cur.g2);
         const int t = p0 ? cur.t0 : p1 ? cur.t1 : cur.t2;
         const int y = (p0 ? cur.row0 : p1 ? cur.row1 : cur.row2) + gl * cur.R;
         const int q = issued % kMkQ;
         mbar_arrive_expect_tx(&wfull[q], static_cast<uint32_t>(cur.box_bytes));
-        tma_load_2d(wring + ph, mk_map(a, cur.layer, t), (w + kMkWarps * pj) * cur.cw, y, &wfull[q], pol);
+        tma_load_2d(wring + ph, mk_map(a, cur.layer, t), (cur.part + (kMkWarps / cur.wpp) * pj) * cur.cw, y, &wfull[q],
+                    pol);
 #pragma unroll
         for (int i = 0; i < kMkQ; ++i)
           if (i == n) qv[i] = v;
@@ -695,7 +709,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   // 128-column chunk q % 2), or -1.
   auto xcol = [&](const MkGeom& gm, int q, int in) {
     const int j = q >> 1, k = q & 1, off = 4 * lane + 128 * k;
-    const int col = (warp + kMkWarps * j) * gm.cw + off;
+    const int col = (mk_part(gm, warp) + (kMkWarps / mk_wpp(gm)) * j) * gm.cw + off;
     return (j < gm.pw && k < gm.kc && off < gm.cw && col < in) ? col : -1;
   };
   // CTA-wide RMSNorm scale from per-thread sums of squares.
@@ -794,7 +808,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       gv[q] = col >= 0 ? __ldg(reinterpret_cast<const float4*>(gain + col)) : make_float4(0, 0, 0, 0);
       ss = fmaf(xr[q].x, xr[q].x, fmaf(xr[q].y, xr[q].y, fmaf(xr[q].z, xr[q].z, fmaf(xr[q].w, xr[q].w, ss))));
     }
-    const float inv = norm_scale(ss, a.H);
+    // with two warps per part both hold the same columns: count them once
+    const float inv = norm_scale(mk_sub(gm, warp) == 0 ? ss : 0.f, a.H);
 #pragma unroll
     for (int q = 0; q < kMkXr; ++q) {
       xr[q].x = xr[q].x * inv * gv[q].x;
@@ -813,10 +828,19 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
 
   // Sum of the 8 warp partials of local row lr (chunk starting at row group cg).
   auto row_value = [&](const MkStageT& st, const MkGeom& gm, int cg, int lr) {
-    const float* p = part + mk_slot(st, gm.R, cg, lr) * kMkWarps;
+    const int slot = mk_slot(st, gm.R, cg, lr);
+    const float* p = part + slot * kMkWarps;
+    if (gm.wpp != 2) {
+      float v = p[0];
+#pragma unroll
+      for (int w = 1; w < kMkWarps; ++w) v += p[w];
+      return v;
+    }
+    // two warps per part: the row's partials are those of the warps of its parity
+    p += ((cg + slot / gm.R) & 1) * (kMkWarps / 2);
     float v = p[0];
 #pragma unroll
-    for (int w = 1; w < kMkWarps; ++w) v += p[w];
+    for (int w = 1; w < kMkWarps / 2; ++w) v += p[w];
     return v;
   };
 
@@ -841,7 +865,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     bool ok = true;
     for (int cg = 0; cg < ng; cg += gchunk) {
       const int ce = min(ng, cg + gchunk);
-      for (int rg = cg; rg < ce; ++rg) {
+      const int wpp = mk_wpp(gm), sub = mk_sub(gm, warp);
+      for (int rg = cg + (((sub - cg) % wpp) + wpp) % wpp; rg < ce; rg += wpp) {
         const bool p0 = rg < g1, p1 = !p0 && rg < g2;
         const int nr = min(R, (p0 ? nr0 : p1 ? nr1 : nr2) - (rg - (p0 ? 0 : p1 ? g1 : g2)) * R);
         float acc[RM];

@@ -257,6 +257,11 @@ struct MkW4<float> {
   __device__ __forceinline__ static float dot(const T& w, const float4& x, float acc) {
     return fmaf(w.x, x.x, fmaf(w.y, x.y, fmaf(w.z, x.z, fmaf(w.w, x.w, acc))));
   }
+  // even / odd columns into two accumulators, two products per instruction
+  __device__ __forceinline__ static void dot2(const T& w, const float4& x, float& ae, float& ao) {
+    ffma2(ae, ao, w.x, w.y, x.x, x.y);
+    ffma2(ae, ao, w.z, w.w, x.z, x.w);
+  }
 };
 template <>
 struct MkW4<uint16_t> {
@@ -269,6 +274,10 @@ struct MkW4<uint16_t> {
     return fmaf(__uint_as_float(w.x << 16), x.x,
                 fmaf(__uint_as_float(w.x & 0xFFFF0000u), x.y,
                      fmaf(__uint_as_float(w.y << 16), x.z, fmaf(__uint_as_float(w.y & 0xFFFF0000u), x.w, acc))));
+  }
+  __device__ __forceinline__ static void dot2(const T& w, const float4& x, float& ae, float& ao) {
+    ffma2(ae, ao, __uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u), x.x, x.y);
+    ffma2(ae, ao, __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u), x.z, x.w);
   }
 };
 
@@ -869,9 +878,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       for (int rg = cg + (((sub - cg) % wpp) + wpp) % wpp; rg < ce; rg += wpp) {
         const bool p0 = rg < g1, p1 = !p0 && rg < g2;
         const int nr = min(R, (p0 ? nr0 : p1 ? nr1 : nr2) - (rg - (p0 ? 0 : p1 ? g1 : g2)) * R);
-        float acc[RM];
+        float acc[RM], acc2[RM];  // even / odd columns of each row
 #pragma unroll
-        for (int r = 0; r < RM; ++r) acc[r] = 0.f;
+        for (int r = 0; r < RM; ++r) acc[r] = acc2[r] = 0.f;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           if (j >= pw) break;
@@ -896,7 +905,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
                 const float4 x = xr[2 * j + k];
 #pragma unroll
                 for (int r = 0; r < RM; ++r)
-                  if (r < nr) acc[r] = W::dot(W::lds(buf, r * cw + off), x, acc[r]);
+                  if (r < nr) W::dot2(W::lds(buf, r * cw + off), x, acc[r], acc2[r]);
               }
             }
             segstamp(2);
@@ -912,6 +921,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
             }
           }
         }
+#pragma unroll
+        for (int r = 0; r < RM; ++r) acc[r] += acc2[r];
         const float v = reduce_scatter<RM>(acc, lane);
         const int r = lane >> kSh;
         if (ok && (lane & ((1 << kSh) - 1)) == 0 && r < nr) part[((rg - cg) * R + r) * kMkWarps + warp] = v;

@@ -45,10 +45,10 @@ METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 
 # DRAM traffic of the persistent decode kernel per algorithmic byte, from ncu on a
 # 4-layer / 32768-vocabulary case of the same widths (profiles/decode_megakernel_small_full.md):
-# (392,428,032 read + 2,843,392 written) / 387,186,688 algorithmic bytes; the excess is the
+# (387,484,160 read + 2,817,280 written) / 387,186,688 algorithmic bytes; the excess is the
 # rows a tiled box reads past a CTA's row range. Set to None when the kernel changes until it
 # is measured again.
-MK_TRAFFIC_PER_ALG_BYTE = (392428032 + 2843392) / 387186688
+MK_TRAFFIC_PER_ALG_BYTE = (387484160 + 2817280) / 387186688
 # DRAM bytes (read + written) per launch of the standalone gemv kernel at 6144x1024 f32, from ncu
 # (profiles/gemv_tma_f32_6144x1024.md: 25,221,376-25,227,264 B read, 0 written over 8 launches);
 # None until measured for the current kernel.

@@ -863,6 +863,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   // ring barriers. After a failed wait the warp skips its data work but keeps
   // every barrier of the stage, so the CTA leaves the stage together at the
   // next chunk boundary.
+  uint64_t boxes_done_ns = 0;  // trace: when the CTA's warps finished a stage's first chunk of boxes
   auto consume_kc = [&](auto kc_tag, const MkStageT& st, const MkGeom& gm, const float4(&xr)[kMkXr],
                         auto&& epi) -> bool {
     constexpr int KC = decltype(kc_tag)::value;
@@ -929,6 +930,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       }
       consumer_sync();
       if (*vabort) return false;
+      if (a.trace && tid == 0 && cg == 0) boxes_done_ns = globaltimer_ns();
       epi(cg, ce);
       consumer_sync();
     }
@@ -940,7 +942,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     return consume_kc(std::integral_constant<int, 2>{}, st, gm, xr, epi);
   };
 
-  // Trace events per stage: 0 entry, 1 inputs staged, 2 outputs published.
+  // Trace events per stage: 0 entry, 1 inputs staged, 2 outputs published, 3 (projections)
+  // every warp of the CTA done with the boxes / (attention) key loop done.
   auto stamp = [&](int step, int l, int st, int ev) {
     if (a.trace && step == 0 && tid == 0)
       a.trace[((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + st) * kMkTraceEvents + ev] =
@@ -1066,6 +1069,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         });
         if (!ok) break;
         stamp(step, l, ts, 2);
+        if (a.trace && step == 0 && tid == 0)
+          a.trace[((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + ts) * kMkTraceEvents + 3] = boxes_done_ns;
       }
     }
     if (!ok || *vabort || !mk_head_on(a, step)) continue;

@@ -285,12 +285,13 @@ dec_status launch_q4(int R, const uint32_t* codes, const uint16_t* s, const uint
 }
 
 // Split-K geometry of one matrix for gemv_tma_kernel (the persistent decode
-// kernel's rules): 8 column parts (16 when a part would exceed 256 columns),
-// 16-byte aligned; R rows per box minimising the busiest CTA's bytes plus a
-// fixed cost per box; boxes fit one 8 KB slot.
+// kernel's rules): 8 column parts (16 when a part would exceed 256 columns; 4
+// parts of two warps each when 8 would be at most 128 columns), 16-byte
+// aligned; R rows per box minimising the busiest warp's bytes plus a fixed cost
+// per box; boxes fit one 8 KB slot.
 MkGeom plan_gemv_tma(int out, int in, int elem, int G) {
   MkGeom m{};
-  m.wpp = 1;  // one warp per column part
+  m.wpp = 1;  // one warp per column part (two for narrow inputs, below)
   const int align = 16 / elem;
   auto width = [&](int parts) {
     const int cw = (in + parts - 1) / parts;
@@ -301,15 +302,19 @@ MkGeom plan_gemv_tma(int out, int in, int elem, int G) {
   if (m.cw > 256) {
     m.pw = 2;
     m.cw = width(2 * kGtWarps);
+  } else if (m.cw <= 128) {
+    m.wpp = 2;  // 4 parts of up to 256 columns, two warps each (alternate row groups)
+    m.cw = width(kGtWarps / 2);
   }
   m.kc = (m.cw + 127) / 128;
-  const int rmax = std::min((elem == 4 ? 16 : 32) / m.kc, kMkSlot / (m.cw * elem));
+  const int rmax = std::min(kMkRowsMax / m.kc, kMkSlot / (m.cw * elem));
   const int lo = out / G, hi = (out + G - 1) / G;  // rows of the CTAs
   long long best = -1;
   for (int R = 1; R <= rmax; ++R) {
-    long long worst = 0;
+    long long worst = 0;  // the busiest warp's boxes
     for (int nr : {lo, hi})
-      worst = std::max(worst, static_cast<long long>((nr + R - 1) / R) * (static_cast<long long>(R) * m.cw * elem + 2048));
+      worst = std::max(worst, static_cast<long long>(((nr + R - 1) / R + m.wpp - 1) / m.wpp) *
+                                  (static_cast<long long>(R) * m.cw * elem + 2048));
     if (best < 0 || worst <= best) {
       best = worst;
       m.R = R;

@@ -37,7 +37,6 @@ struct GtArgs {
 template <typename WT>
 __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_constant__ CUtensorMap mapW,
                                                                  const GtArgs a) {
-  constexpr int RM16 = 16 * static_cast<int>(4 / sizeof(WT));
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_abort;
   const uint32_t RB = static_cast<uint32_t>(a.ring_bytes);
@@ -52,7 +51,9 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
   const MkGeom& gm = a.gm;
   const int R = gm.R, pw = gm.pw, cw = gm.cw;
   const int ng = (nrows + R - 1) / R;
-  const int nb = ng * pw;  // boxes per warp
+  const int wpp = mk_wpp(gm), np = kGtWarps / wpp;  // warps per part, parts
+  // boxes of warp w: its part's boxes of the row groups with index % wpp == w / np
+  auto boxes_of = [&](int w) { const int sub = w / np; return (ng > sub ? (ng - sub + wpp - 1) / wpp : 0) * pw; };
   const uint32_t B = (static_cast<uint32_t>(gm.box_bytes) + 127u) & ~127u;
   volatile int* vabort = &s_abort;
   if (tid < kGtWarps * kGtQ) {
@@ -77,7 +78,8 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
 #pragma unroll
     for (int i = 0; i < kGtQ; ++i) qv[i] = 0;
     int issued = 0, retired = 0;
-    const int total = active ? nb : 0;
+    const int total = active ? boxes_of(w) : 0;
+    const int wpart = w % np, wsub = w / np;
     uint64_t idle_since = 0;
     while (__any_sync(0xffffffffu, issued < total || retired < issued)) {
       bool progress = false;
@@ -95,10 +97,11 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
         }
         const int n = issued - retired;
         if (n > 0 && v + B - qv[0] > RB) break;
-        const int rg = pw == 2 ? (issued >> 1) : issued, pj = issued - rg * pw;
+        const int li = pw == 2 ? (issued >> 1) : issued, pj = issued - li * pw;
+        const int rg = wsub + wpp * li;
         const int q = issued % kGtQ;
         mbar_arrive_expect_tx(&wfull[q], static_cast<uint32_t>(gm.box_bytes));
-        tma_load_2d(wring + ph, &mapW, (w + kGtWarps * pj) * cw, u0 + rg * R, &wfull[q], pol);
+        tma_load_2d(wring + ph, &mapW, (wpart + np * pj) * cw, u0 + rg * R, &wfull[q], pol);
 #pragma unroll
         for (int i = 0; i < kGtQ; ++i)
           if (i == n) qv[i] = v;
@@ -134,12 +137,13 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
   uint64_t* mfull = full + warp * kGtQ;
   uint64_t* mempty = empty + warp * kGtQ;
   const unsigned char* myring = smem + static_cast<size_t>(warp) * RB;
-  // this lane's x elements: part j (warp + 8 j), 128-column chunk k, 4 columns
+  // this lane's x elements: part j (warp % np + np j), 128-column chunk k, 4 columns
+  const int mypart = warp % np, mysub = warp / np;
   float4 xr[kMkXr];
 #pragma unroll
   for (int q = 0; q < kMkXr; ++q) {
     const int j = q >> 1, k = q & 1, off = 4 * lane + 128 * k;
-    const int col = (warp + kGtWarps * j) * cw + off;
+    const int col = (mypart + np * j) * cw + off;
     xr[q] = (j < pw && k < gm.kc && off < cw && col < a.in) ? ldg4<WT>(a.x, col) : make_float4(0, 0, 0, 0);
   }
   int cq = 0;
@@ -147,16 +151,16 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
   bool ok = true;
   auto run = [&](auto kc_tag) {
     constexpr int KC = decltype(kc_tag)::value;
-    constexpr int RM = RM16 / KC;
+    constexpr int RM = kMkRowsMax / KC;  // rows per box, at most
     constexpr int kSh = RM == 32 ? 0 : RM == 16 ? 1 : RM == 8 ? 2 : 3;
     using W = MkW4<WT>;
     for (int cg = 0; cg < ng; cg += gm.gchunk) {
       const int ce = min(ng, cg + gm.gchunk);
-      for (int rg = cg; rg < ce; ++rg) {
+      for (int rg = cg + (((mysub - cg) % wpp) + wpp) % wpp; rg < ce; rg += wpp) {
         const int nr = min(R, nrows - rg * R);
-        float acc[RM];
+        float acc[RM], acc2[RM];  // even / odd columns of each row
 #pragma unroll
-        for (int r = 0; r < RM; ++r) acc[r] = 0.f;
+        for (int r = 0; r < RM; ++r) acc[r] = acc2[r] = 0.f;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
           if (j >= pw) break;
@@ -178,7 +182,7 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
                 const float4 x = xr[2 * j + k];
 #pragma unroll
                 for (int r = 0; r < RM; ++r)
-                  if (r < nr) acc[r] = W::dot(W::lds(buf, r * cw + off), x, acc[r]);
+                  if (r < nr) W::dot2(W::lds(buf, r * cw + off), x, acc[r], acc2[r]);
               }
             }
             __syncwarp();
@@ -189,6 +193,8 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
             }
           }
         }
+#pragma unroll
+        for (int r = 0; r < RM; ++r) acc[r] += acc2[r];
         const float v = reduce_scatter<RM>(acc, lane);
         const int r = lane >> kSh;
         if (ok && (lane & ((1 << kSh) - 1)) == 0 && r < nr) part[((rg - cg) * R + r) * kGtWarps + warp] = v;
@@ -197,10 +203,10 @@ __global__ void __launch_bounds__(kGtThreads, 2) gemv_tma_kernel(const __grid_co
       if (*vabort) return;
       const int r0 = cg * R, r1 = min(nrows, ce * R);
       for (int lr = r0 + tid; lr < r1; lr += kGtWarps * 32) {
-        const float* p = part + (lr - r0) * kGtWarps;
+        // the partials of the warps that own the row's group, in a fixed order
+        const float* p = part + (lr - r0) * kGtWarps + ((lr / R) % wpp) * np;
         float v = p[0];
-#pragma unroll
-        for (int w = 1; w < kGtWarps; ++w) v += p[w];
+        for (int w = 1; w < np; ++w) v += p[w];
         a.y[u0 + lr] = v;
       }
       asm volatile("bar.sync 1, %0;" ::"n"(kGtWarps * 32) : "memory");

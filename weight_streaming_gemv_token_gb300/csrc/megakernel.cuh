@@ -741,6 +741,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   auto stage_x = [&](const uint64_t* src, uint32_t tag, int in, const float* gain, const MkGeom& gm,
                      float4 (&xr)[kMkXr]) {
     constexpr int K = kMkMaxWidth / kMkConsumers;
+    // the gain of this lane's columns does not depend on the exchange: request
+    // it before polling so its latency is not on the stage's critical path
+    float4 gv[kMkXr];
+#pragma unroll
+    for (int q = 0; q < kMkXr; ++q) {
+      const int col = xcol(gm, q, in);
+      gv[q] = (gain && col >= 0) ? __ldg(reinterpret_cast<const float4*>(gain + col)) : make_float4(0, 0, 0, 0);
+    }
     uint64_t wv[K];
 #pragma unroll
     for (int k = 0; k < K; ++k) {
@@ -796,7 +804,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       if (col >= 0) {
         const float4 v = *reinterpret_cast<const float4*>(xs + col);
         if (gain) {
-          const float4 g = __ldg(reinterpret_cast<const float4*>(gain + col));
+          const float4 g = gv[q];
           xr[q] = make_float4(v.x * inv * g.x, v.y * inv * g.y, v.z * inv * g.z, v.w * inv * g.w);
         } else {
           xr[q] = v;

@@ -227,6 +227,53 @@ def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=5, min_bytes=1 << 3
     return per_launch / avg / 1e9, per_launch, avg, n
 
 
+def time_q4_cold_rows(W, torch, out, inp, stream, ntok, rows_options, rounds=5, min_bytes=1 << 30, gen=None):
+    """Cold GB/s of gemv_q4 for each rows-per-warp setting on one set of >= 1 GiB of distinct
+    packed matrices (each setting captured in its own graph); {R: (GB/s, bytes per launch, avg s)}."""
+    per = out * inp // 2 + out * (inp // 64) * 4
+    count = max(2, -(-min_bytes // per))
+    codes = [torch.randint(-2**31, 2**31 - 1, (out, inp // 8), dtype=torch.int32, device="cuda", generator=gen)
+             for _ in range(count)]
+    sc = [torch.empty((out, inp // 64), dtype=torch.float16, device="cuda").uniform_(0.001, 0.01, generator=gen)
+          for _ in range(count)]
+    bi = [torch.empty((out, inp // 64), dtype=torch.float16, device="cuda").normal_(0, 0.02, generator=gen)
+          for _ in range(count)]
+    x = torch.randn((ntok, inp), device="cuda", generator=gen).to(torch.bfloat16)
+    y = torch.empty((ntok, out), device="cuda")
+    per_launch = per + ntok * (inp * 2 + out * 4)
+    res = {}
+    prev = W.gemv_q4_rows_per_warp(ntok)
+    try:
+        for r in rows_options:
+            W.gemv_q4_rows_per_warp(ntok, r)
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(cap):
+                for i in range(count):
+                    W.gemv_q4(codes[i], sc[i], bi[i], x, y, out, inp, ntok, cap)
+            cap.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                for i in range(count):
+                    W.gemv_q4(codes[i], sc[i], bi[i], x, y, out, inp, ntok, cap)
+            graph.replay()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(rounds):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            avg = e0.elapsed_time(e1) / 1e3 / (rounds * count)
+            res[r] = (per_launch / avg / 1e9, per_launch, avg)
+            del graph
+    finally:
+        W.gemv_q4_rows_per_warp(ntok, prev if prev > 0 else -1)
+    del codes, sc, bi
+    torch.cuda.empty_cache()
+    return res
+
+
 def prefill_config(W, torch, hbm, tflops_peak):
     """BF16 Qwen3-0.6B shape with chunked prefill (tensor-core projections): the
     chunk size is tuned on a 2048-token Zipf(1.1) prompt with 8 outputs, then a
@@ -403,21 +450,17 @@ def gpu_arm(args):
                 for (o, i) in Wl.GEMV_SHAPES:
                     g, _, a, _ = time_gemv_cold(W, torch, dt, o, i, stream, gen=gen)
                     sweep[f"{dt} {o}x{i}"] = {"GB/s": round(g, 1), "frac": round(g / hbm, 4), "us": round(a * 1e6, 3)}
+            # rows per warp tuned per shape on the cold number ("Our Kernel Benchmark Was Measuring
+            # the System Cache"); "auto" is the library's default choice
             for ntok in (1, 2):
-                best = None
-                for r in (1, 2, 4, 8):
-                    W.gemv_q4_rows_per_warp(ntok, r)
-                    tot = 0.0
-                    for (o, i) in Wl.GEMV_SHAPES:
-                        g, _, a, _ = time_gemv_cold(W, torch, "q4", o, i, stream, ntok=ntok, gen=gen, rounds=2)
-                        tot += g
-                    if best is None or tot > best[1]:
-                        best = (r, tot)
-                W.gemv_q4_rows_per_warp(ntok, best[0])
                 for (o, i) in Wl.GEMV_SHAPES:
-                    g, _, a, _ = time_gemv_cold(W, torch, "q4", o, i, stream, ntok=ntok, gen=gen)
-                    sweep[f"q4 ntok={ntok} {o}x{i}"] = {"GB/s": round(g, 1), "frac": round(g / hbm, 4),
-                                                       "us": round(a * 1e6, 3), "rows_per_warp": best[0]}
+                    res = time_q4_cold_rows(W, torch, o, i, stream, ntok, (-1, 1, 2, 4, 8), gen=gen)
+                    best = max((r for r in res if r > 0), key=lambda r: res[r][0])
+                    g, _, a = res[best]
+                    sweep[f"q4 ntok={ntok} {o}x{i}"] = {
+                        "GB/s": round(g, 1), "frac": round(g / hbm, 4), "us": round(a * 1e6, 3), "rows_per_warp": best,
+                        "auto_GB/s": round(res[-1][0], 1),
+                        "by_rows_GB/s": {str(r): round(res[r][0], 1) for r in res if r > 0}}
             extra["gemv_cold"] = sweep
         if not args.no_prefill:
             extra["prefill"] = prefill_config(W, torch, hbm, measured_bf16_tflops())

@@ -220,13 +220,21 @@ dec_status gemv(int32_t wdtype, const void* d_W, const void* d_x, float* d_y, in
  * d_codes: uint32 [out][in/8], code j of word w in bits [4j, 4j+4), column
  * 8w+j; d_scale, d_bias: fp16 bits [out][in/64]; d_x: bfloat16 [ntok][in];
  * d_y: float32 [ntok][out]. ntok is 1 or 2; in % 64 == 0; d_codes 16-byte
- * aligned. Errors: DEC_EINVAL, DEC_ECUDA. */
+ * aligned. With in % 512 == 0 (in <= 16384) and 16-byte aligned scales,
+ * biases and x, the bulk-copy kernel runs: integer dot products of the codes
+ * with x in 16-bit fixed point per 32 columns (step a power of two, error at
+ * most 2^-15 of the 32 columns' largest |x|), float32 sums per row, fixed
+ * order. Otherwise a per-warp kernel dequantises to float32. Both are
+ * bit-reproducible. Errors: DEC_EINVAL, DEC_ECUDA. */
 dec_status gemv_q4(const uint32_t* d_codes, const uint16_t* d_scale, const uint16_t* d_bias, const uint16_t* d_x,
                    float* d_y, int32_t out, int32_t in, int32_t ntok, void* stream);
 
 /* Rows of W each warp of gemv_q4 handles per pass (1, 2, 4 or 8), for the
- * given ntok. r > 0 sets it, r == 0 only reads it. Returns the value in
- * effect, or -1 for a bad argument. Process-wide. */
+ * given ntok ("Our Kernel Benchmark Was Measuring the System Cache", "Why it
+ * mattered, concretely": tuned on the cold number). r > 0 sets it, r == -1
+ * returns to the automatic choice (the default: 1 when out <= 8 x the SM
+ * count, else 4), r == 0 only reads it. Returns the setting in effect (0:
+ * automatic), or -1 for a bad argument. Process-wide. */
 int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r);
 
 /* Reads (and if clear != 0 clears) the device error bits of gemv/gemv_q4

@@ -91,6 +91,12 @@ def test_host_side_argument_errors(lib):
     assert lib.gemv_q4(None, None, None, None, None, 0, 128, 1, None) == B.DEC_OK
     assert lib.gemv_q4_rows_per_warp(1, 3) == -1
     assert lib.gemv_q4_rows_per_warp(3, 1) == -1
+    assert lib.gemv_q4_rows_per_warp(1, -2) == -1
+    # the setting is host state: set, read back, and return to the automatic choice
+    assert lib.gemv_q4_rows_per_warp(2, 4) == 4
+    assert lib.gemv_q4_rows_per_warp(2, 0) == 4
+    assert lib.gemv_q4_rows_per_warp(2, -1) == 0
+    assert lib.gemv_q4_rows_per_warp(2, 0) == 0
     h = ctypes.c_void_p()
     cfg = B.dec_config(layers=1, hidden=64, inter=64, n_q=2, n_kv=1, head_dim=16, vocab=10, eps=1e-6,
                        rope_theta=1e4, wdtype=0, kvdtype=0, max_seq=8, chunk_cap=0)

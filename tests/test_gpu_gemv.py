@@ -136,7 +136,7 @@ def test_gemv_q4_small(ntok, shape, rows):
         bound = 2e-5 * (np.abs(O.widen(x)) @ wabs.T) + 1e-6
         assert np.all(np.abs(y - ref) <= bound)
     finally:
-        W.gemv_q4_rows_per_warp(ntok, prev)
+        W.gemv_q4_rows_per_warp(ntok, prev if prev > 0 else -1)
 
 
 @pytest.mark.parametrize("ntok", [1, 2])

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "common.h"
+#include "gemv_q4.cuh"
 #include "gemv_stream.cuh"
 #include "gemv_tma.cuh"
 
@@ -240,7 +241,7 @@ __global__ void __launch_bounds__(256) gemv_q4_kernel(const uint32_t* __restrict
   }
 }
 
-int g_q4_rows[3] = {0, 1, 2};  // rows per warp for ntok = 1, 2 (index by ntok)
+int g_q4_rows[3] = {0, 0, 0};  // rows per warp for ntok = 1, 2 (index by ntok); 0: chosen per launch
 
 template <int R, int NTOK>
 dec_status launch_q4_r(const uint32_t* codes, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
@@ -273,9 +274,89 @@ dec_status launch_q4_r(const uint32_t* codes, const uint16_t* s, const uint16_t*
   return DEC_OK;
 }
 
+// Bulk-copy 4-bit GEMV (gemv_q4.cuh): one CTA per SM (fewer when out is
+// smaller), a ring of as many stages of 16 R rows as the CTA needs and shared
+// memory holds. Needs in % 512 == 0 (every row range's scales are then a
+// multiple of 16 bytes) and 16-byte aligned scales, biases and x; *used is
+// false when the shape does not fit, so the caller takes the per-warp kernel.
+template <int R, int NTOK>
+dec_status launch_q4_bulk_r(const uint32_t* codes, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
+                            int out, int in, cudaStream_t st, const DeviceInfo& di, bool* used) {
+  *used = false;
+  auto kern = gemv_q4_bulk_kernel<R, NTOK>;
+  static size_t static_smem[64] = {};
+  static bool lifted[64] = {};
+  if (!lifted[di.device]) {
+    cudaFuncAttributes fa{};
+    WSG_CUDA_TRY(nullptr, cudaFuncGetAttributes(&fa, kern));
+    WSG_CUDA_TRY(nullptr, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(di.smem_optin - fa.sharedSizeBytes)));
+    static_smem[di.device] = fa.sharedSizeBytes;
+    lifted[di.device] = true;
+  }
+  constexpr int RC = kQ4Warps * R;
+  // One CTA per SM while each has at most 4 stages of rows (small matrices:
+  // the next launch's CTAs then fit beside them), else two per SM.
+  int G = out < di.sms ? out : di.sms;
+  if (static_cast<long long>(out) > 4ll * RC * di.sms) G = 2 * di.sms;
+  const long long rows_max = (static_cast<long long>(out) + G - 1) / G;
+  const long long nst = (rows_max + RC - 1) / RC;
+  const long long srows = rows_max < RC ? rows_max : RC;  // rows a stage holds
+  const long long stage = (srows * (in / 2 + in / 16) + 127) / 128 * 128;
+  const long long xbytes = static_cast<long long>(NTOK) * (in / 32) * (4 * 16 + 8);
+  // shared memory for two CTAs per SM
+  const long long budget = static_cast<long long>(di.smem_per_sm / 2) - 1024 -
+                           static_cast<long long>(static_smem[di.device]) - xbytes - 2ll * kQ4MaxStages * 8;
+  long long S = budget > 0 ? budget / stage : 0;
+  if (S > kQ4MaxStages) S = kQ4MaxStages;
+  if (S > nst) S = nst;
+  if (S < 1) return DEC_OK;
+  Q4Args a;
+  a.codes = codes;
+  a.scale = s;
+  a.bias = b;
+  a.x = x;
+  a.y = y;
+  a.out = out;
+  a.in = in;
+  a.nstages = static_cast<int>(S);
+  a.srows = static_cast<int>(srows);
+  a.stage_bytes = static_cast<uint32_t>(stage);
+  a.err = gemv_err_ptr(di.device);
+  if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv_q4: device error word unavailable");
+  const size_t smem = static_cast<size_t>(S * stage + xbytes + 2 * S * 8);
+  WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(G), dim3(kQ4Threads), smem, st, true, a));
+  *used = true;
+  return DEC_OK;
+}
+
+template <int NTOK>
+dec_status launch_q4_bulk(int R, const uint32_t* codes, const uint16_t* s, const uint16_t* b, const uint16_t* x,
+                          float* y, int out, int in, cudaStream_t st, const DeviceInfo& di, bool* used) {
+  *used = false;
+  if (in % 512 || in > 16384 || !aligned16(s) || !aligned16(b) || !aligned16(x)) return DEC_OK;
+  // a smaller R when a stage of the requested one does not fit
+  for (int r = R; r >= 1 && !*used; r >>= 1) {
+    dec_status e = DEC_OK;
+    switch (r) {
+      case 1: e = launch_q4_bulk_r<1, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
+      case 2: e = launch_q4_bulk_r<2, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
+      case 4: e = launch_q4_bulk_r<4, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
+      default: e = launch_q4_bulk_r<8, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
+    }
+    if (e != DEC_OK) return e;
+  }
+  return DEC_OK;
+}
+
 template <int NTOK>
 dec_status launch_q4(int R, const uint32_t* codes, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
                      int out, int in, cudaStream_t st, const DeviceInfo& di) {
+  {
+    bool used = false;
+    const dec_status e = launch_q4_bulk<NTOK>(R, codes, s, b, x, y, out, in, st, di, &used);
+    if (e != DEC_OK || used) return e;
+  }
   switch (R) {
     case 1: return launch_q4_r<1, NTOK>(codes, s, b, x, y, out, in, st, di);
     case 2: return launch_q4_r<2, NTOK>(codes, s, b, x, y, out, in, st, di);
@@ -465,15 +546,23 @@ extern "C" dec_status gemv_q4(const uint32_t* d_codes, const uint16_t* d_scale, 
   }
   if (!d_codes || !d_scale || !d_bias || !d_x) return fail(nullptr, DEC_EINVAL, "gemv_q4: NULL pointer");
   if (!aligned16(d_codes)) return fail(nullptr, DEC_EINVAL, "gemv_q4: codes must be 16-byte aligned");
-  const int R = g_q4_rows[ntok];
+  int R = g_q4_rows[ntok];
+  if (R == 0) {
+    // automatic: one row per warp when a CTA has at most one warp's worth of
+    // rows (out <= 8 per SM), else four (the cold-sweep optimum of large shapes);
+    // the per-warp fallback kernel keeps its own optimum (1 row, 2 for two tokens)
+    const bool bulk = in % 512 == 0 && in <= 16384 && aligned16(d_scale) && aligned16(d_bias) && aligned16(d_x);
+    R = bulk ? (static_cast<long long>(out) <= 8ll * di.sms ? 1 : 4) : ntok;
+  }
   if (ntok == 1) return launch_q4<1>(R, d_codes, d_scale, d_bias, d_x, d_y, out, in, s, di);
   return launch_q4<2>(R, d_codes, d_scale, d_bias, d_x, d_y, out, in, s, di);
 }
 
 extern "C" int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r) {
   if (ntok != 1 && ntok != 2) return -1;
-  if (r != 0 && r != 1 && r != 2 && r != 4 && r != 8) return -1;
+  if (r != -1 && r != 0 && r != 1 && r != 2 && r != 4 && r != 8) return -1;
   if (r > 0) g_q4_rows[ntok] = r;
+  if (r == -1) g_q4_rows[ntok] = 0;
   return g_q4_rows[ntok];
 }
 

@@ -1,0 +1,279 @@
+// 4-bit groupwise-affine GEMV streamed by bulk copies ("Our Kernel Benchmark
+// Was Measuring the System Cache", Summary and "Why it mattered, concretely":
+// the one-token matvec and its two-token variant, measured cold).
+//
+//  * Each CTA owns a contiguous range of rows. Its codes ([rows][in/8] u32)
+//    and its scales and biases ([rows][in/64] fp16) are three contiguous
+//    byte ranges, so one producer lane streams them with plain 1D bulk copies
+//    into a ring of stages of up to RC = 8 * R rows (one full/empty mbarrier
+//    pair per stage). The copies start before the kernel waits on its predecessor
+//    (programmatic dependent launch): the weights of a launch do not depend
+//    on earlier kernels, only x does.
+//  * 8 consumer warps: warp w takes rows w, w + 8, ... (R of them) of every
+//    stage, lane l the 32-column chunks l, l + 32, ... of those rows; one
+//    16-byte shared load brings a row's 32 codes of a chunk, and a chunk is
+//    half of a 64-column group, so it has one scale s and bias b. The CTA is
+//    sized for two per SM: large matrices run two per SM, small ones one, so
+//    the next launch's CTAs can start their copies beside it.
+//  * Integer dot products. Per chunk and token, x is written in 16-bit fixed
+//    point with the power-of-two step u = 2^(e-14), 2^e <= max|x| < 2^(e+1):
+//    xi = rint(x / u), |xi| <= 32640, split into a signed high byte and an
+//    unsigned low byte (xi = 256 hi + lo). A bfloat16 x whose exponent is at
+//    least e - 7 is represented exactly; smaller ones are within u/2, i.e.
+//    2^-15 of the chunk's largest |x|. The codes need no conversion:
+//    lo = word & 0x0F0F0F0F holds the even columns' codes and
+//    hi = word & 0xF0F0F0F0 16 times the odd columns' codes, one per byte, so
+//    four 4-way byte dot products (dp4a) per word accumulate exact integer sums
+//    against the matching x byte planes, and
+//    16 sum q xi = 16 (256 He + Le) + 256 Ho + Lo (below 2^28).
+//    The chunk adds s * u/16 * (that sum) + b * X to the row, X the chunk's
+//    float sum of x. All staged once per CTA.
+//  * A warp owns whole rows: a butterfly reduce-scatter over its lanes gives
+//    each row's sum, which one lane stores. No cross-warp sums: results are
+//    bit-reproducible.
+//
+// Every mbarrier wait is bounded; on a timeout the CTA raises an abort flag,
+// the producer waits (bounded) for its copies in flight, and the error word
+// records the cause.
+#pragma once
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "megakernel.cuh"  // reduce_scatter
+#include "ptx.cuh"
+
+namespace wsg {
+
+constexpr int kQ4Warps = 8;                     // consumer warps
+constexpr int kQ4Threads = kQ4Warps * 32 + 32;  // plus a producer warp
+constexpr int kQ4MaxStages = 16;
+
+struct Q4Args {
+  const uint32_t* codes;  // [out][in/8]
+  const uint16_t* scale;  // fp16 [out][in/64]
+  const uint16_t* bias;   // fp16 [out][in/64]
+  const uint16_t* x;      // bf16 [ntok][in]
+  float* y;               // [ntok][out]
+  int32_t out, in;
+  int32_t nstages;        // ring depth
+  int32_t srows;          // row capacity of a stage: min(RC, most rows of a CTA)
+  uint32_t stage_bytes;   // one stage: srows rows of codes, then of scales, then of biases (multiple of 128)
+  uint32_t* err;
+};
+
+__device__ __forceinline__ void q4_consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kQ4Warps * 32) : "memory");
+}
+
+// 4-way byte dot products: c + sum_k a.byte[k] * b.byte[k], a unsigned and b
+// signed (us) or both unsigned (uu).
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Shared memory: [ring: nstages x stage_bytes][xq: NTOK][4][nch] uint4 (the byte
+// planes of chunk c: high bytes of the even columns, low bytes of the even
+// columns, high and low bytes of the odd columns; word m of a plane holds
+// columns 32c + 8m + (0, 2, 4, 6) or + (1, 3, 5, 7))[xu: NTOK][nch] float2
+// (u / 16, X)][full: nstages][empty: nstages] mbarriers.
+template <int R, int NTOK>
+__global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Args a) {
+  constexpr int RC = kQ4Warps * R;
+  constexpr int NV = R * NTOK;  // row sums per lane before the reduction
+  constexpr int kLogNV = NV == 1 ? 0 : NV == 2 ? 1 : NV == 4 ? 2 : NV == 8 ? 3 : 4;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int in = a.in, nch = in >> 5;
+  const uint32_t cb = static_cast<uint32_t>(in) >> 1;   // code bytes per row
+  const uint32_t sbb = static_cast<uint32_t>(in) >> 5;  // scale (or bias) bytes per row
+  const int S = a.nstages;
+  unsigned char* ring = smem;
+  uint4* xq = reinterpret_cast<uint4*>(smem + static_cast<size_t>(S) * a.stage_bytes);
+  float2* xu = reinterpret_cast<float2*>(xq + NTOK * 4 * nch);
+  uint64_t* full = reinterpret_cast<uint64_t*>(xu + NTOK * nch);
+  uint64_t* empty = full + S;
+  volatile int* vabort = &s_abort;
+  const int c = blockIdx.x, G = gridDim.x;
+  const int r0 = static_cast<int>(static_cast<long long>(c) * a.out / G);
+  const int n = static_cast<int>(static_cast<long long>(c + 1) * a.out / G) - r0;
+  const int nst = (n + RC - 1) / RC;
+  if (tid == 0) {
+    s_abort = 0;
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kQ4Warps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  // ---- producer: one lane streams the CTA's stages ----
+  if (warp == kQ4Warps) {
+    if (lane != 0) return;
+    const uint64_t pol = l2_policy_evict_first();
+    const char* codes = reinterpret_cast<const char*>(a.codes);
+    const char* sc = reinterpret_cast<const char*>(a.scale);
+    const char* bi = reinterpret_cast<const char*>(a.bias);
+    int issued = 0;
+    for (int st = 0; st < nst; ++st) {
+      const int slot = st % S;
+      if (st >= S && !mbar_wait(&empty[slot], ((st / S) - 1) & 1)) {
+        *vabort = 1;
+        atomicOr(a.err, ERR_MBAR_TIMEOUT);
+      }
+      if (*vabort) break;
+      const int row = r0 + st * RC, rows = min(RC, n - st * RC);
+      unsigned char* dst = ring + static_cast<size_t>(slot) * a.stage_bytes;
+      mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(rows) * (cb + 2 * sbb));
+      bulk_g2s(dst, codes + static_cast<size_t>(row) * cb, rows * cb, &full[slot], pol);
+      bulk_g2s(dst + a.srows * cb, sc + static_cast<size_t>(row) * sbb, rows * sbb, &full[slot], pol);
+      bulk_g2s(dst + a.srows * (cb + sbb), bi + static_cast<size_t>(row) * sbb, rows * sbb, &full[slot], pol);
+      ++issued;
+    }
+    // After an abort: shared memory must outlive the copies already issued.
+    if (*vabort)
+      for (int k = max(0, issued - S); k < issued; ++k) mbar_wait(&full[k % S], (k / S) & 1);
+    return;
+  }
+
+  // ---- consumers ----
+  // x (it may come from the previous kernel): per chunk and token, the fixed
+  // point step, the byte planes and the float sum. Four consecutive lanes per
+  // chunk, lane m taking the 8 columns of word m (one 16-byte load) and
+  // building that word of all four planes; the butterfly max and sum over the
+  // four lanes leave the same value in each.
+  {
+    const int items = NTOK * nch * 4;
+    for (int it0 = warp * 32; it0 < items; it0 += kQ4Warps * 32) {
+      const int it = it0 + lane;
+      const bool valid = it < items;
+      const int t = valid ? it / (nch * 4) : 0, rem = it - t * nch * 4, ch = rem >> 2, m = rem & 3;
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (valid) u = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * in + 32 * ch + 8 * m));
+      const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+      float xv[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        xv[2 * k] = __uint_as_float(uw[k] << 16);             // column 8m + 2k
+        xv[2 * k + 1] = __uint_as_float(uw[k] & 0xFFFF0000u); // column 8m + 2k + 1
+      }
+      float mx = 0.f, X = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        mx = fmaxf(mx, fabsf(xv[j]));
+        X += xv[j];
+      }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        X += __shfl_xor_sync(0xffffffffu, X, o);
+      }
+      int e = 0;
+      if (mx > 0.f) {
+        frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1): 2^(e-1) <= mx < 2^e
+        e -= 1;
+      }
+      uint32_t he = 0, le = 0, ho = 0, lo = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int xe = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k], 14 - e))) : 0;
+        const int xo = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k + 1], 14 - e))) : 0;
+        he |= (static_cast<uint32_t>(xe >> 8) & 0xFFu) << (8 * k);
+        le |= (static_cast<uint32_t>(xe) & 0xFFu) << (8 * k);
+        ho |= (static_cast<uint32_t>(xo >> 8) & 0xFFu) << (8 * k);
+        lo |= (static_cast<uint32_t>(xo) & 0xFFu) << (8 * k);
+      }
+      if (valid) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(xq + t * 4 * nch + ch) + m;  // word m of plane 0
+        w[0] = he;
+        w[4 * nch] = le;
+        w[8 * nch] = ho;
+        w[12 * nch] = lo;
+        if (m == 0) xu[t * nch + ch] = make_float2(mx > 0.f ? scalbnf(1.0f, e - 18) : 0.f, X);
+      }
+    }
+  }
+  q4_consumer_sync();
+
+  bool ok = true;
+  for (int st = 0; st < nst && ok; ++st) {
+    const int slot = st % S;
+    ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], (st / S) & 1));
+    if (!ok) {
+      if (lane == 0) atomicOr(a.err, ERR_MBAR_TIMEOUT);
+      *vabort = 1;
+      break;
+    }
+    const int rows = min(RC, n - st * RC);
+    const unsigned char* base = ring + static_cast<size_t>(slot) * a.stage_bytes;
+    const unsigned char* sbase = base + a.srows * cb;
+    const unsigned char* bbase = sbase + a.srows * sbb;
+    float acc[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) acc[v] = 0.f;
+    for (int ch = lane; ch < nch; ch += 32) {
+      uint4 q[R];
+      float s[R], b[R];
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const int rr = warp + kQ4Warps * i;
+        if (rr < rows) {
+          q[i] = *reinterpret_cast<const uint4*>(base + rr * cb + 16 * ch);
+          s[i] = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(sbase + rr * sbb + 2 * (ch >> 1))));
+          b[i] = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(bbase + rr * sbb + 2 * (ch >> 1))));
+        } else {
+          q[i] = make_uint4(0, 0, 0, 0);
+          s[i] = b[i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) {
+        const uint4 phe = xq[(t * 4 + 0) * nch + ch], ple = xq[(t * 4 + 1) * nch + ch];
+        const uint4 pho = xq[(t * 4 + 2) * nch + ch], plo = xq[(t * 4 + 3) * nch + ch];
+        const float2 xs = xu[t * nch + ch];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          int he = 0, ho = 0;
+          uint32_t le = 0, lo = 0;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t w = m == 0 ? q[i].x : m == 1 ? q[i].y : m == 2 ? q[i].z : q[i].w;
+            const uint32_t ev = w & 0x0F0F0F0Fu;  // q of columns 8m, 8m+2, 8m+4, 8m+6
+            const uint32_t od = w & 0xF0F0F0F0u;  // 16 q of columns 8m+1, 8m+3, 8m+5, 8m+7
+            const uint32_t xhe = m == 0 ? phe.x : m == 1 ? phe.y : m == 2 ? phe.z : phe.w;
+            const uint32_t xle = m == 0 ? ple.x : m == 1 ? ple.y : m == 2 ? ple.z : ple.w;
+            const uint32_t xho = m == 0 ? pho.x : m == 1 ? pho.y : m == 2 ? pho.z : pho.w;
+            const uint32_t xlo = m == 0 ? plo.x : m == 1 ? plo.y : m == 2 ? plo.z : plo.w;
+            he = dp4a_us(ev, xhe, he);
+            le = dp4a_uu(ev, xle, le);
+            ho = dp4a_us(od, xho, ho);
+            lo = dp4a_uu(od, xlo, lo);
+          }
+          // 16 sum q xi, exact (below 2^28 in magnitude)
+          const int tot = 16 * (256 * he + static_cast<int>(le)) + 256 * ho + static_cast<int>(lo);
+          acc[i * NTOK + t] = fmaf(s[i] * xs.x, static_cast<float>(tot), fmaf(b[i], xs.y, acc[i * NTOK + t]));
+        }
+      }
+    }
+    // every lane's reads of the stage are in registers: release it
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    const float v = reduce_scatter<NV>(acc, lane);
+    const int vi = lane >> (5 - kLogNV), i = vi / NTOK, t = vi - i * NTOK;
+    const int rr = warp + kQ4Warps * i;
+    if ((lane & ((32 >> kLogNV) - 1)) == 0 && rr < rows)
+      a.y[static_cast<size_t>(t) * a.out + r0 + st * RC + rr] = v;
+  }
+}
+
+}  // namespace wsg

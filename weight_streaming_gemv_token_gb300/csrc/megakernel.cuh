@@ -296,13 +296,13 @@ __device__ __forceinline__ float4 ldg4<uint16_t>(const void* row, int i) {
                      __uint_as_float(u.y & 0xFFFF0000u));
 }
 
-// Butterfly reduce-scatter of N (4, 8, 16 or 32) per-lane values over the warp:
+// Butterfly reduce-scatter of N (1 to 32, a power of two) per-lane values over the warp:
 // at each step a lane keeps half of its values and adds the partner's copy of
 // them; the remaining steps are plain sums. Returns the full 32-lane sum of
 // value lane >> (5 - log2 N), held by every lane of that group.
 template <int N>
 __device__ __forceinline__ float reduce_scatter(float (&a)[N], int lane) {
-  static_assert(N == 4 || N == 8 || N == 16 || N == 32, "4 to 32 rows per box, a power of two");
+  static_assert(N == 1 || N == 2 || N == 4 || N == 8 || N == 16 || N == 32, "at most 32 values, a power of two");
   int o = 16;
 #pragma unroll
   for (int m = N; m > 1; m >>= 1, o >>= 1) {

@@ -13,6 +13,7 @@ decode: Qwen3-0.6B-shaped decoder (optionally fewer layers / a smaller
         inside the region.
 gemv:   --count distinct matrices of one shape (sized past L2 by default),
         one warm-up pass, then one launch per matrix inside the region.
+q4:     the same for gemv_q4 (4-bit codes, fp16 scales and biases, bf16 x).
 prefill: BF16 Qwen3-0.6B-shaped decoder (optionally fewer layers) with chunked
         prefill: a --prompt-token Zipf(1.1) prompt in chunks of --chunk rows,
         one untimed pass, then the whole prompt again inside the region.
@@ -87,6 +88,37 @@ def gemv(args):
     torch.cuda.profiler.stop()
 
 
+def q4(args):
+    from . import binding as B
+    from . import build
+
+    build.build()
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    out, inp, ntok = args.out, args.inp, args.ntok
+    per = out * inp // 2 + out * (inp // 64) * 4
+    count = args.count or max(2, -(-(256 << 20) // per))
+    codes = [torch.randint(-2**31, 2**31 - 1, (out, inp // 8), dtype=torch.int32, device="cuda", generator=g)
+             for _ in range(count)]
+    sc = [torch.empty((out, inp // 64), dtype=torch.float16, device="cuda").uniform_(0.001, 0.01, generator=g)
+          for _ in range(count)]
+    bi = [torch.empty((out, inp // 64), dtype=torch.float16, device="cuda").normal_(0, 0.02, generator=g)
+          for _ in range(count)]
+    x = torch.randn((ntok, inp), device="cuda", generator=g).to(torch.bfloat16)
+    y = torch.empty((ntok, out), device="cuda")
+    if args.rows:
+        B.gemv_q4_rows_per_warp(ntok, args.rows)
+    for i in range(count):
+        B.gemv_q4(codes[i], sc[i], bi[i], x, y, out, inp, ntok, None)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.start()
+    for i in range(count):
+        B.gemv_q4(codes[i], sc[i], bi[i], x, y, out, inp, ntok, None)
+    torch.cuda.synchronize()
+    torch.cuda.profiler.stop()
+    assert B.gemv_device_errors() == 0
+
+
 def prefill(args):
     import dataclasses
 
@@ -136,12 +168,18 @@ def main():
     gm.add_argument("--in", dest="inp", type=int, default=1024)
     gm.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
     gm.add_argument("--count", type=int, default=0)
+    qm = sub.add_parser("q4")
+    qm.add_argument("--out", type=int, default=151936)
+    qm.add_argument("--in", dest="inp", type=int, default=1024)
+    qm.add_argument("--ntok", type=int, default=1, choices=[1, 2])
+    qm.add_argument("--rows", type=int, default=0, help="rows per warp (0: the library default)")
+    qm.add_argument("--count", type=int, default=0)
     pf = sub.add_parser("prefill")
     pf.add_argument("--prompt", type=int, default=4096)
     pf.add_argument("--chunk", type=int, default=1024)
     pf.add_argument("--layers", type=int, default=0, help="fewer layers than the Qwen3-0.6B shape (0: 28)")
     args = ap.parse_args()
-    {"decode": decode, "gemv": gemv, "prefill": prefill}[args.mode](args)
+    {"decode": decode, "gemv": gemv, "q4": q4, "prefill": prefill}[args.mode](args)
 
 
 if __name__ == "__main__":

@@ -50,6 +50,23 @@ def test_gemv_full_shapes(dtype, shape):
     assert np.all(np.abs(y - ref) <= accumulation_bound(Wm, x, inp))
 
 
+# Shapes of the bulk-copy kernel (at least 16 rows and 96 KB of W per SM): ragged row
+# counts per CTA and stage, a partial last pass of the row, 1, 2 and 4 rows per warp.
+BULK = [("f32", (5000, 1000)), ("f32", (20003, 264)), ("bf16", (9000, 1000)), ("bf16", (60001, 256))]
+
+
+@pytest.mark.parametrize("dtype,shape", BULK)
+def test_gemv_bulk_shapes(dtype, shape):
+    W = lib()
+    out, inp = shape
+    Wm = Wl.gemv_matrix(out, inp, seed=out + inp, dtype=dtype)
+    x = Wl.gemv_vector(inp, seed=inp + 3, dtype=dtype)
+    y = run_gemv(W, dtype, Wm, x)
+    ref = O.gemv(Wm, x)
+    close(y, ref, FP32_TOL if dtype == "f32" else LOW_TOL, f"gemv {dtype} {shape}")
+    assert np.all(np.abs(y - ref) <= accumulation_bound(Wm, x, inp))
+
+
 def test_gemv_edge_cases():
     import torch
 

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "common.h"
+#include "gemv_bulk.cuh"
 #include "gemv_q4.cuh"
 #include "gemv_stream.cuh"
 #include "gemv_tma.cuh"
@@ -451,9 +452,93 @@ dec_status launch_gemv_tma(const void* W, const void* x, float* y, int out, int 
   return DEC_OK;
 }
 
+// Bulk-copy GEMV (gemv_bulk.cuh): one CTA per SM while each has at most 4
+// stages of rows (the next launch's CTAs then fit beside them), else two per
+// SM; stages of up to 8 R rows, as many as the CTA needs and two CTAs' share
+// of shared memory holds. Needs 16-byte aligned W and row bytes a multiple of
+// 16; *used is false when the shape does not fit.
+template <typename WT, int R>
+dec_status launch_gemv_bulk_r(const void* W, const void* x, float* y, int out, int in, cudaStream_t st,
+                              const DeviceInfo& di, bool* used) {
+  *used = false;
+  auto kern = gemv_bulk_kernel<WT, R>;
+  static size_t static_smem[64] = {};
+  static bool lifted[64] = {};
+  if (!lifted[di.device]) {
+    cudaFuncAttributes fa{};
+    WSG_CUDA_TRY(nullptr, cudaFuncGetAttributes(&fa, kern));
+    WSG_CUDA_TRY(nullptr, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(di.smem_optin - fa.sharedSizeBytes)));
+    static_smem[di.device] = fa.sharedSizeBytes;
+    lifted[di.device] = true;
+  }
+  constexpr int E = 16 / static_cast<int>(sizeof(WT));
+  constexpr int RC = kGbWarps * R;
+  const long long rb = static_cast<long long>(in) * sizeof(WT);
+  int G = out < di.sms ? out : di.sms;
+  if (static_cast<long long>(out) > 4ll * RC * di.sms) G = 2 * di.sms;
+  const long long rows_max = (static_cast<long long>(out) + G - 1) / G;
+  const long long np = (in + 32 * E - 1) / (32 * E);
+  const long long xbytes = np * 32 * E * 4;
+  const long long budget = static_cast<long long>(di.smem_per_sm / 2) - 1024 -
+                           static_cast<long long>(static_smem[di.device]) - xbytes - 2ll * kGbMaxStages * 8;
+  if (budget < rb) return DEC_OK;
+  long long srows = RC;
+  if (srows > rows_max) srows = rows_max;
+  if (srows > budget / rb) srows = budget / rb;
+  const long long stage = (srows * rb + 127) / 128 * 128;
+  const long long nst = (rows_max + srows - 1) / srows;
+  long long S = budget / stage;
+  if (S > kGbMaxStages) S = kGbMaxStages;
+  if (S > nst) S = nst;
+  if (S < 1) return DEC_OK;
+  GbArgs a;
+  a.W = W;
+  a.x = x;
+  a.y = y;
+  a.out = out;
+  a.in = in;
+  a.nstages = static_cast<int>(S);
+  a.srows = static_cast<int>(srows);
+  a.stage_bytes = static_cast<uint32_t>(stage);
+  a.err = gemv_err_ptr(di.device);
+  if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv: device error word unavailable");
+  const size_t smem = static_cast<size_t>(S * stage + xbytes + 2 * S * 8);
+  WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(G), dim3(kGbThreads), smem, st, true, a));
+  *used = true;
+  return DEC_OK;
+}
+
+// Used when every SM gets at least 16 rows and 96 KB of the matrix. Fewer,
+// longer rows, and the smaller matrices whose time is mostly the launch
+// handover, measured faster on the split-K kernel (its 8 warps share every
+// row, x sits in registers). Rows per warp: 1 while the matrix runs one CTA
+// per SM (stages of 8 rows, the finest pipeline), else a stage of 8 R rows
+// near 32 KB (float32 rows of 1024: R = 1).
+template <typename WT>
+dec_status launch_gemv_bulk(const void* W, const void* x, float* y, int out, int in, cudaStream_t st,
+                            const DeviceInfo& di, bool* used) {
+  *used = false;
+  const long long rb = static_cast<long long>(in) * sizeof(WT);
+  if (rb % 16 || !aligned16(W) || rb > (1ll << 20) || out < 16ll * di.sms ||
+      static_cast<long long>(out) * rb < 96ll * 1024 * di.sms)
+    return DEC_OK;
+  if (static_cast<long long>(out) <= 4ll * kGbWarps * di.sms)
+    return launch_gemv_bulk_r<WT, 1>(W, x, y, out, in, st, di, used);
+  const long long r = 32768 / (kGbWarps * rb);
+  if (r >= 4) return launch_gemv_bulk_r<WT, 4>(W, x, y, out, in, st, di, used);
+  if (r >= 2) return launch_gemv_bulk_r<WT, 2>(W, x, y, out, in, st, di, used);
+  return launch_gemv_bulk_r<WT, 1>(W, x, y, out, in, st, di, used);
+}
+
 template <typename WT, typename XT>
 dec_status launch_gemv(const void* W, const void* x, float* y, int out, int in, cudaStream_t st,
                        const DeviceInfo& di) {
+  {
+    bool used = false;
+    const dec_status s = launch_gemv_bulk<WT>(W, x, y, out, in, st, di, &used);
+    if (s != DEC_OK || used) return s;
+  }
   {
     bool used = false;
     const dec_status s = launch_gemv_tma<WT>(W, x, y, out, in, st, di, &used);

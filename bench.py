@@ -49,10 +49,11 @@ METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 # rows a tiled box reads past a CTA's row range. Set to None when the kernel changes until it
 # is measured again.
 MK_TRAFFIC_PER_ALG_BYTE = (387484160 + 2817280) / 387186688
-# DRAM bytes (read + written) per launch of the standalone gemv kernel at 6144x1024 f32, from ncu
-# (profiles/gemv_tma_f32_6144x1024.md: 25,221,376-25,227,264 B read, 0 written over 8 launches);
-# None until measured for the current kernel.
-GEMV_TRAFFIC = 25221632
+# DRAM bytes (read + written) per launch of the standalone gemv bulk-copy kernel at 151936x1024 f32
+# (the tied vocabulary shape), from ncu (profiles/gemv_bulk_151936x1024.md: 622,377,984 B read +
+# 3,492,352 B written); None until measured for the current kernel.
+GEMV_TRAFFIC = 622377984 + 3492352
+GEMV_ROOF_SHAPE = (151936, 1024)
 PROMPT = 32
 
 
@@ -435,14 +436,16 @@ def gpu_arm(args):
                 "bytes_per_launch": step_bytes * K, "launch_us": round(sec * 1e6, 1), "launches": 1,
                 "traffic_source": "ncu dram bytes of a 4-layer/32768-vocab case of the same widths, scaled by "
                                   "algorithmic bytes (profiles/decode_megakernel_small_full.md)"}
-        # the streaming GEMV engine alone at the gate/up shape, cold
-        gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", 6144, 1024, stream, gen=gen)
+        # the standalone GEMV alone at the tied-vocabulary shape (the step's largest product), cold
+        o, i = GEMV_ROOF_SHAPE
+        gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", o, i, stream, gen=gen)
         extra["roofline" if args.engine != "persistent" else "gemv_roofline"] = {
             "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
             # ncu dram__bytes_read+write per launch of this kernel on this shape; None until measured
-            # for the current kernel (profiles/gemv_tma_f32_6144x1024.md)
+            # for the current kernel (profiles/gemv_bulk_151936x1024.md)
             "traffic": GEMV_TRAFFIC, "peak_kind": peak_kind,
-            "kernel": "gemv_tma_kernel<f32> 6144x1024 (gate/up shape), standalone gemv entry, cold round-robin",
+            "kernel": f"gemv_bulk_kernel<float,1> {o}x{i} (tied vocabulary shape), standalone gemv entry, "
+                      "cold round-robin",
             "bytes_per_launch": per_launch, "avg_launch_us": round(avg * 1e6, 3), "launches": launches}
         if not args.no_sweep:
             sweep = {}

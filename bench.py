@@ -228,6 +228,37 @@ def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=5, min_bytes=1 << 3
     return per_launch / avg / 1e9, per_launch, avg, n
 
 
+def fixed_context_latency(dec, torch, s, stream, contexts=(0, 16, 64), trials=9, warm=3):
+    """Decode-forward latency at a fixed cache slot ("Megakernels", "Fixed-context methodology"):
+    after `ctx` prompt tokens, each trial rewinds to slot ctx and runs one full forward of the same
+    token (host token in, greedy token read back); median over the trials, wall clock and CUDA events."""
+    toks = [int(t) for t in Wl.prompt_uniform(max(contexts) + 1, s.vocab, seed=0)]
+    res = {}
+    for ctx in contexts:
+        dec.reset()
+        if ctx:
+            dec.prefill(toks[:ctx], is_last=False)
+        walls, devs, outs = [], [], set()
+        for i in range(warm + trials):
+            dec.rewind(ctx)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e0.record(stream)
+            nxt = dec.step(toks[ctx])
+            e1.record(stream)
+            torch.cuda.synchronize()
+            wall = time.perf_counter() - t0
+            outs.add(nxt)
+            if i >= warm:
+                walls.append(wall * 1e3)
+                devs.append(e0.elapsed_time(e1))
+        assert len(outs) == 1, "a repeated forward at one slot changed its token"
+        res[str(ctx)] = {"median_ms": round(statistics.median(walls), 4), "device_median_ms": round(statistics.median(devs), 4),
+                         "trials": trials}
+    return res
+
+
 def time_q4_cold_rows(W, torch, out, inp, stream, ntok, rows_options, rounds=5, min_bytes=1 << 30, gen=None):
     """Cold GB/s of gemv_q4 for each rows-per-warp setting on one set of >= 1 GiB of distinct
     packed matrices (each setting captured in its own graph); {R: (GB/s, bytes per launch, avg s)}."""
@@ -417,6 +448,7 @@ def gpu_arm(args):
     wall = time.perf_counter() - t0
     e2e_sec = barrier_max(max(wall, f0.elapsed_time(f1) / 1e3), ws)
     e2e_value = ws * n_e2e / e2e_sec
+    fixed = fixed_context_latency(dec, torch, s, stream)
     dec.close()
     del dec
     torch.cuda.empty_cache()
@@ -487,6 +519,7 @@ def gpu_arm(args):
                               "roofline_tokens_per_s": round(hbm * 1e9 / step_bytes, 1)},
             "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": 4, "steps": n_e2e},
+            "fixed_context": fixed,
             "gpu_launches": 1 if args.engine == "persistent" else K * (5 * s.layers + 1),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,

@@ -137,6 +137,14 @@ dec_status dec_load_weights(dec_ctx* ctx, const dec_weights* w);
  * "Long-document chunked prefill": timing starts before cache reset). */
 dec_status dec_reset(dec_ctx* ctx);
 
+/* Moves the position back to pos (0 <= pos <= current position): cache
+ * entries 0..pos-1 stay valid, the next forward runs at position pos and
+ * overwrites slot pos. This is how a fixed-context timing trial repeats one
+ * token at a fixed cache slot ("Megakernels", "Fixed-context methodology").
+ * Asynchronous on the context's stream. Errors: DEC_EINVAL (NULL, pos
+ * outside [0, position]), DEC_ECUDA. */
+dec_status dec_rewind(dec_ctx* ctx, int32_t pos);
+
 /* One forward of `token` at the current position p; writes K/V at p and
  * advances the position to p+1.
  * Without DEC_SKIP_LOGITS: final RMSNorm, tied vocabulary projection and

@@ -106,6 +106,7 @@ def test_host_side_argument_errors(lib):
     assert lib.dec_step(None, 0, 0, None, None) == B.DEC_EINVAL
     assert lib.dec_position(None) == -1
     assert lib.dec_reset(None) == B.DEC_EINVAL
+    assert lib.dec_rewind(None, 0) == B.DEC_EINVAL
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

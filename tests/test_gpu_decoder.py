@@ -256,3 +256,51 @@ def test_multistep_launch_is_bitwise_single_steps(engine, model, tiny_w, request
         assert torch.equal(ka[:, :29], kb[:, :29]), f"K layer {l}"
         assert torch.equal(va[:, :29], vb[:, :29]), f"V layer {l}"
     assert a.device_errors() == 0 and b.device_errors() == 0
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_rewind_repeats_a_fixed_slot(tiny_w, engine):
+    """dec_rewind: a forward repeated at one cache slot gives bit-identical logits and cache rows
+    (the fixed-context timing trial), and rewinding further back continues a different sequence
+    exactly as a fresh oracle that saw that sequence."""
+    import torch
+
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.TINY
+    prompt = [int(t) for t in Wl.prompt_uniform(8, s.vocab, seed=0)]
+    dec = Decoder(s, tiny_w, kv_dtype="f32", max_seq=16, engine=engine)
+    dec.reset()
+    for t in prompt[:5]:
+        dec.step(t, skip_logits=True)
+    assert dec.position == 5
+    la = torch.empty(s.vocab, device="cuda")
+    lb = torch.empty(s.vocab, device="cuda")
+    ta = dec.step(prompt[5], logits=la)
+    ka = [x.clone() for x in dec.kv(0)[:2]]
+    for _ in range(3):
+        dec.rewind(5)
+        assert dec.position == 5
+        tb = dec.step(prompt[5], logits=lb)
+        assert tb == ta and torch.equal(la, lb)
+        kb = dec.kv(0)[:2]
+        assert torch.equal(ka[0][:, :6], kb[0][:, :6]) and torch.equal(ka[1][:, :6], kb[1][:, :6])
+    # back to slot 3 with another continuation: matches an oracle that saw only that sequence
+    dec.rewind(3)
+    ora = O.OracleDecoder(s, tiny_w, kv_dtype="f32", max_seq=16)
+    for t in prompt[:3]:
+        ora.body(t)
+    seq = [prompt[7], prompt[6], prompt[0]]
+    for t in seq:
+        dec.step(t, logits=la)
+        close(la.cpu().numpy(), ora.step(t), FP32_TOL, "after rewind")
+    for l in range(s.layers):
+        K, V, n = dec.kv(l)
+        assert n == 6 == ora.pos
+        rk, rv = ora.kv(l)
+        close(kv_to_np(K[:, :n]), rk, FP32_TOL, f"K layer {l} after rewind")
+        close(kv_to_np(V[:, :n]), rv, FP32_TOL, f"V layer {l} after rewind")
+    with pytest.raises(lib().WsgError):
+        dec.rewind(7)  # beyond the current position
+    assert dec.device_errors() == 0
+    dec.close()

@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     dec_position,
     dec_prefill_chunk,
     dec_reset,
+    dec_rewind,
     dec_set_trace,
     dec_step,
     dec_trace_bytes,

@@ -24,7 +24,7 @@ DEC_DEVERR_WAIT_TIMEOUT, DEC_DEVERR_ARGMAX_NAN, DEC_DEVERR_BAD_TOKEN = 0x1, 0x2,
 
 # Every symbol include/wsg.h declares.
 EXPORTED = (
-    "dec_workspace_bytes", "dec_create", "dec_load_weights", "dec_reset", "dec_step", "dec_prefill_chunk",
+    "dec_workspace_bytes", "dec_create", "dec_load_weights", "dec_reset", "dec_rewind", "dec_step", "dec_prefill_chunk",
     "dec_generate", "dec_get_kv", "dec_position", "dec_trace_bytes", "dec_set_trace", "dec_device_errors",
     "dec_destroy", "dec_last_error",
     "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors", "greedy_head_noalloc", "gemm_bf16",
@@ -71,6 +71,7 @@ def library() -> ctypes.CDLL:
             "dec_create": (c_int32, [P(dec_config), c_void_p, c_size_t, c_void_p, P(c_void_p)]),
             "dec_load_weights": (c_int32, [c_void_p, P(dec_weights)]),
             "dec_reset": (c_int32, [c_void_p]),
+            "dec_rewind": (c_int32, [c_void_p, c_int32]),
             "dec_step": (c_int32, [c_void_p, c_int32, c_uint32, c_void_p, P(c_int32)]),
             "dec_prefill_chunk": (c_int32, [c_void_p, P(c_int32), c_int32, c_int32, c_void_p, P(c_int32)]),
             "dec_generate": (c_int32, [c_void_p, c_int32, c_int32, c_void_p]),
@@ -139,6 +140,10 @@ def dec_load_weights(ctx: int, weights: dec_weights):
 
 def dec_reset(ctx: int):
     _check(library().dec_reset(ctx), ctx)
+
+
+def dec_rewind(ctx: int, pos: int):
+    _check(library().dec_rewind(ctx, int(pos)), ctx)
 
 
 def dec_step(ctx: int, token: int, flags: int = 0, d_logits=None, want_next: bool = True) -> int | None:

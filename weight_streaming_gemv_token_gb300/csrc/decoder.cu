@@ -955,6 +955,20 @@ extern "C" dec_status dec_reset(dec_ctx* c) {
   return DEC_OK;
 }
 
+extern "C" dec_status dec_rewind(dec_ctx* c, int32_t pos) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_rewind: NULL context");
+  if (pos < 0 || pos > c->pos) return fail(&c->err, DEC_EINVAL, "dec_rewind: position %d outside [0, %d]", pos, c->pos);
+  c->pos = pos;
+  // The position word, and (persistent engine) the appended-row counts its
+  // attention waits on: rows below pos stay valid, rows from pos on are
+  // rewritten before anything reads them.
+  uint32_t* kvr = c->cfg.engine == DEC_ENGINE_PERSISTENT ? c->at<uint32_t>(c->L.kv_ready) : nullptr;
+  pf_control_kernel<<<1, 256, 0, c->stream>>>(c->at<int32_t>(c->L.ctrl), pos, kvr, c->cfg.layers * c->cfg.n_kv,
+                                              static_cast<uint32_t>(pos));
+  WSG_CUDA_TRY(&c->err, cudaGetLastError());
+  return DEC_OK;
+}
+
 extern "C" dec_status dec_step(dec_ctx* c, int32_t token, uint32_t flags, float* d_logits, int32_t* h_next) {
   if (!c) return fail(nullptr, DEC_EINVAL, "dec_step: NULL context");
   if (flags & ~DEC_SKIP_LOGITS) return fail(&c->err, DEC_EINVAL, "dec_step: unknown flags 0x%x", flags);

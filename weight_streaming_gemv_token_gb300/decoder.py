@@ -78,6 +78,10 @@ class Decoder:
     def reset(self):
         B.dec_reset(self.ctx)
 
+    def rewind(self, pos: int):
+        """Back to position pos (<= the current one); the next forward overwrites cache slot pos."""
+        B.dec_rewind(self.ctx, pos)
+
     @property
     def position(self) -> int:
         return B.dec_position(self.ctx)

@@ -228,6 +228,53 @@ def time_gemv_cold(W, torch, dtype, out, inp, stream, rounds=5, min_bytes=1 << 3
     return per_launch / avg / 1e9, per_launch, avg, n
 
 
+def lossless_config(W, torch, stream, headline_embed, hbm, K=200):
+    """Lossless bfloat16 storage of float32 weights ("Megakernels", "Lossless decode-weight
+    storage"): the float32 Qwen3-0.6B-shaped model converted from bfloat16 (every weight has zero
+    low 16 bits) decodes from float32 storage and from its packed bfloat16 halves (same values);
+    the headline model's random float32 weights are checked for eligibility too."""
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.QWEN3_06B
+    emb = torch.from_numpy(headline_embed).cuda()
+    tmp = torch.empty(emb.shape, dtype=torch.bfloat16, device="cuda")
+    bad = W.pack_bf16_exact(emb, tmp, emb.numel(), stream)
+    del emb, tmp
+    w = Wl.decoder_weights(s, seed=1, wdtype="f32_from_bf16")
+    prompt = Wl.prompt_uniform(PROMPT, s.vocab, seed=0)
+    res = {"workload": "Qwen3-0.6B-shaped decoder, float32 weights converted from bfloat16, float32 KV, "
+                       f"{K} greedy steps after a {PROMPT}-token prompt",
+           "headline_weights_eligible": bad == 0, "headline_embedding_inexact_values": int(bad)}
+    toks = {}
+    for packed in (False, True):
+        dec = Decoder(s, w, kv_dtype="f32", max_seq=PROMPT + K + 32, stream=stream, lossless=packed)
+        assert dec.lossless == packed
+        first = dec.prefill(prompt, is_last=True)
+        warm = dec.generate(first, 8)
+        torch.cuda.synchronize()
+        out = torch.empty(K, dtype=torch.int32, device="cuda")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dec.generate(int(warm[-1].item()), K, out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert dec.device_errors() == 0
+        toks[packed] = out.cpu()
+        sec = e0.elapsed_time(e1) / 1e3
+        elem = 2 if packed else 4
+        shp = Wl.tensor_shapes(s)
+        per_layer = sum(int(np.prod(shp[k])) for k in Wl.LAYER_TENSORS if not k.startswith("g_"))
+        wbytes = elem * (int(np.prod(shp["embed"])) + s.layers * per_layer)
+        res["packed" if packed else "float32"] = {
+            "tokens_per_s": round(K / sec, 1), "ms_per_step": round(sec / K * 1e3, 4),
+            "weight_bytes_per_step": wbytes, "weight_GB/s": round(wbytes * K / sec / 1e9, 1)}
+        dec.close()
+        del dec
+    res["same_tokens"] = bool(torch.equal(toks[False], toks[True]))
+    torch.cuda.empty_cache()
+    return res
+
+
 def fixed_context_latency(dec, torch, s, stream, contexts=(0, 16, 64), trials=9, warm=3):
     """Decode-forward latency at a fixed cache slot ("Megakernels", "Fixed-context methodology"):
     after `ctx` prompt tokens, each trial rewinds to slot ctx and runs one full forward of the same
@@ -499,6 +546,8 @@ def gpu_arm(args):
             extra["gemv_cold"] = sweep
         if not args.no_prefill:
             extra["prefill"] = prefill_config(W, torch, hbm, measured_bf16_tflops())
+        if not args.no_lossless:
+            extra["lossless_storage"] = lossless_config(W, torch, stream, weights["embed"], hbm)
 
     if rank == 0:
         cpu = None if args.no_cpu else cpu_baseline_sample(weights, prompt, budget_s=args.cpu_seconds)
@@ -601,6 +650,7 @@ def main():
     ap.add_argument("--engine", default="persistent", choices=["persistent", "staged"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-prefill", action="store_true", help="skip the BF16 chunked-prefill configuration")
+    ap.add_argument("--no-lossless", action="store_true", help="skip the lossless bfloat16 storage comparison")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = args.steps if args.steps is not None else 5

@@ -245,6 +245,17 @@ dec_status gemv_q4(const uint32_t* d_codes, const uint16_t* d_scale, const uint1
  * automatic), or -1 for a bad argument. Process-wide. */
 int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r);
 
+/* Lossless bfloat16 storage of float32 weights ("Megakernels", "Lossless
+ * decode-weight storage"): d_dst[i] = high 16 bits of d_src[i] for n
+ * elements (device pointers, any alignment), and *h_bad (host) = how many
+ * elements that storage does not hold exactly (low 16 bits non-zero, or not
+ * finite). With *h_bad == 0 the bfloat16 copy widens back to the same
+ * float32 bits, so a decoder created with wdtype DEC_BF16 over such copies
+ * computes the float32 model's forward on half the weight bytes. Runs on
+ * `stream` and synchronizes it to read the count. Calls on one device must
+ * not overlap (they share the count). Errors: DEC_EINVAL, DEC_ECUDA. */
+dec_status pack_bf16_exact(const float* d_src, uint16_t* d_dst, int64_t n, void* stream, int64_t* h_bad);
+
 /* Reads (and if clear != 0 clears) the device error bits of gemv/gemv_q4
  * on the current device; synchronizes the device. */
 dec_status gemv_device_errors(int32_t clear, uint32_t* bits);

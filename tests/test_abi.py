@@ -107,6 +107,11 @@ def test_host_side_argument_errors(lib):
     assert lib.dec_position(None) == -1
     assert lib.dec_reset(None) == B.DEC_EINVAL
     assert lib.dec_rewind(None, 0) == B.DEC_EINVAL
+    bad = ctypes.c_int64(7)
+    assert lib.pack_bf16_exact(None, None, -1, None, ctypes.byref(bad)) == B.DEC_EINVAL
+    assert lib.pack_bf16_exact(None, None, 4, None, ctypes.byref(bad)) == B.DEC_EINVAL
+    assert lib.pack_bf16_exact(None, None, 0, None, None) == B.DEC_EINVAL
+    assert lib.pack_bf16_exact(None, None, 0, None, ctypes.byref(bad)) == B.DEC_OK and bad.value == 0
 
 
 def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -37,4 +37,5 @@ from .binding import (  # noqa: F401
     gemv_q4_rows_per_warp,
     greedy_head_noalloc,
     library,
+    pack_bf16_exact,
 )

@@ -28,6 +28,7 @@ EXPORTED = (
     "dec_generate", "dec_get_kv", "dec_position", "dec_trace_bytes", "dec_set_trace", "dec_device_errors",
     "dec_destroy", "dec_last_error",
     "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors", "greedy_head_noalloc", "gemm_bf16",
+    "pack_bf16_exact",
 )
 
 
@@ -86,6 +87,7 @@ def library() -> ctypes.CDLL:
             "gemv_q4": (c_int32, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_void_p]),
             "gemv_q4_rows_per_warp": (c_int32, [c_int32, c_int32]),
             "gemv_device_errors": (c_int32, [c_int32, P(c_uint32)]),
+            "pack_bf16_exact": (c_int32, [c_void_p, c_void_p, ctypes.c_int64, c_void_p, P(ctypes.c_int64)]),
             "gemm_bf16": (c_int32, [c_void_p, c_void_p, c_void_p, c_int32, c_int32, c_int32, c_int32, c_int32, c_void_p]),
             "greedy_head_noalloc": (c_int32, [c_int32, c_void_p, c_void_p, c_void_p, c_float, c_int32, c_int32,
                                               c_void_p, c_void_p, c_void_p]),
@@ -211,6 +213,13 @@ def gemv_q4_rows_per_warp(ntok: int, r: int = 0) -> int:
     if v < 0:
         raise WsgError(DEC_EINVAL, f"gemv_q4_rows_per_warp({ntok}, {r})")
     return v
+
+
+def pack_bf16_exact(src, dst, n: int, stream=None) -> int:
+    """dst = high halves of the float32 src; returns how many elements that storage does not hold exactly."""
+    bad = ctypes.c_int64()
+    _check(library().pack_bf16_exact(_ptr(src), _ptr(dst), n, _stream(stream), ctypes.byref(bad)))
+    return bad.value
 
 
 def gemv_device_errors(clear: bool = True) -> int:

@@ -30,13 +30,41 @@ class Decoder:
 
     shape: an object with layers, hidden, inter, n_q, n_kv, head_dim, vocab,
     eps, rope_theta. weights: dict as made by workloads.decoder_weights
-    (numpy) or the same layout of device tensors.
+    (numpy) or the same layout of device tensors. lossless: with float32
+    weights, store them as bfloat16 when every value is one (self.lossless
+    tells whether that happened).
     """
 
     def __init__(self, shape, weights: dict, kv_dtype: str = "f32", max_seq: int = 4096, chunk_cap: int = 0,
-                 stream: torch.cuda.Stream | None = None, engine: str = "persistent"):
+                 stream: torch.cuda.Stream | None = None, engine: str = "persistent", lossless: bool = False):
         wd = weights.get("wdtype", "f32")
         self.shape = shape
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        # device copies of the weights; kept alive as long as the context
+        self.dev = {"embed": to_device(weights["embed"]), "g_final": to_device(weights["g_final"]),
+                    "layers": [{k: to_device(lw[k]) for k in _LAYER_KEYS} for lw in weights["layers"]]}
+        # Lossless storage ("Megakernels", "Lossless decode-weight storage"): float32 projections
+        # and embedding whose values are all bfloat16 values are kept as their bfloat16 halves and
+        # run on the bfloat16-weight kernels; any inexact tensor keeps the whole model in float32.
+        self.lossless = False
+        if lossless and wd == "f32":
+            self.stream.wait_stream(torch.cuda.current_stream())  # the uploads above
+            packed, bad = {}, 0
+            names = [("embed", None)] + [(k, i) for i in range(shape.layers) for k in _LAYER_KEYS
+                                         if not k.startswith("g_")]
+            for k, i in names:
+                src = self.dev[k] if i is None else self.dev["layers"][i][k]
+                dst = torch.empty(src.shape, dtype=torch.bfloat16, device="cuda")
+                bad += B.pack_bf16_exact(src, dst, src.numel(), self.stream)
+                packed[(k, i)] = dst
+            if bad == 0:
+                for (k, i), t in packed.items():
+                    if i is None:
+                        self.dev[k] = t
+                    else:
+                        self.dev["layers"][i][k] = t
+                wd, self.lossless = "bf16", True
+            del packed
         self.cfg = B.dec_config(
             layers=shape.layers, hidden=shape.hidden, inter=shape.inter, n_q=shape.n_q, n_kv=shape.n_kv,
             head_dim=shape.head_dim, vocab=shape.vocab, eps=shape.eps, rope_theta=shape.rope_theta,
@@ -45,15 +73,11 @@ class Decoder:
             max_seq=max_seq, chunk_cap=chunk_cap,
             engine=B.DEC_ENGINE_PERSISTENT if engine == "persistent" else B.DEC_ENGINE_STAGED)
         self.kv_dtype = kv_dtype
-        self.stream = stream if stream is not None else torch.cuda.current_stream()
         nbytes = B.dec_workspace_bytes(self.cfg)
         if nbytes == 0:
             raise B.WsgError(B.DEC_EINVAL, "invalid decoder configuration")
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         self.ctx = B.dec_create(self.cfg, self.workspace, nbytes, self.stream)
-        # device copies of the weights; kept alive as long as the context
-        self.dev = {"embed": to_device(weights["embed"]), "g_final": to_device(weights["g_final"]),
-                    "layers": [{k: to_device(lw[k]) for k in _LAYER_KEYS} for lw in weights["layers"]]}
         arr = (B.dec_layer_weights * shape.layers)()
         for i, lw in enumerate(self.dev["layers"]):
             for k in _LAYER_KEYS:

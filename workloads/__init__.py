@@ -102,9 +102,13 @@ def decoder_weights(s: DecoderShape, seed: int = 1, wdtype: str = "f32") -> dict
     ``wdtype == "bf16"`` the projection and embedding draws are rounded to
     bfloat16 and returned as uint16 bit arrays.
 
+    ``wdtype == "f32_from_bf16"`` gives the float32 model converted from the
+    bfloat16 one: the same rounded draws widened back to float32 (their low 16
+    bits are zero), tagged "f32".
+
     Returns {"embed", "g_final", "layers": [dict per layer]}.
     """
-    if wdtype not in ("f32", "bf16"):
+    if wdtype not in ("f32", "bf16", "f32_from_bf16"):
         raise ValueError(wdtype)
     rng = np.random.default_rng(seed)
     shapes = tensor_shapes(s)
@@ -116,13 +120,17 @@ def decoder_weights(s: DecoderShape, seed: int = 1, wdtype: str = "f32") -> dict
         if name.startswith("g_"):
             return (np.float32(1.0) + np.float32(0.1) * z).astype(np.float32)
         w = (np.float32(0.02) * z).astype(np.float32)
-        return f32_to_bf16_bits(w) if wdtype == "bf16" else w
+        if wdtype == "bf16":
+            return f32_to_bf16_bits(w)
+        if wdtype == "f32_from_bf16":
+            return bf16_bits_to_f32(f32_to_bf16_bits(w))
+        return w
 
     out = {"embed": draw("embed"), "layers": []}
     for _ in range(s.layers):
         out["layers"].append({name: draw(name) for name in LAYER_TENSORS})
     out["g_final"] = draw("g_final")
-    out["wdtype"] = wdtype
+    out["wdtype"] = "f32" if wdtype == "f32_from_bf16" else wdtype
     return out
 
 

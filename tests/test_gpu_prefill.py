@@ -97,6 +97,15 @@ def test_ragged_geometry_chunked_prefill():
     run_chunked(shape, w, prompt, 32, 3, "persistent")
 
 
+def test_fused_projection_launches_ragged_k():
+    """Q, K, V (and gate, up) widths that are whole 128-column tiles share one GEMM launch per
+    group; hidden 200 leaves a ragged K, 150 rows in chunks of 64 ragged row tiles."""
+    shape = Wl.DecoderShape(layers=2, hidden=200, inter=256, n_q=4, n_kv=2, head_dim=64, vocab=500)
+    w = Wl.decoder_weights(shape, seed=5, wdtype="bf16")
+    prompt = Wl.prompt_zipf(150, shape.vocab, seed=1)
+    run_chunked(shape, w, prompt, 64, 3, "persistent")
+
+
 def test_single_row_chunks():
     """Chunks of one row: the causal attention sees only the cache."""
     w = Wl.decoder_weights(Wl.TINY, seed=2, wdtype="bf16")

@@ -403,9 +403,26 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
   // amap + 3 (value and remainder of: 0 normed input, 1 attention output,
   // 2 SwiGLU output) and weight map `wm`
   auto gemm = [&](int amap, int wm, float* C, int ldc, int col0, int N, int K, bool acc) {
-    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, c->pf_wmap[wm].b, C, ldc, col0, n, N, K, acc,
+    const void* mb[1] = {c->pf_wmap[wm].b};
+    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, mb, nullptr, 1, C, ldc, col0, n, N, K, acc,
                             err, st, &c->err);
   };
+  // Several weights side by side in one launch (Q, K, V; gate, up): one grid
+  // over all their columns fills the GPU better than a launch per weight.
+  // Their widths must be whole 128-column tiles.
+  auto gemm_multi = [&](int amap, const int* wms, const int* widths, int nw, float* C, int ldc, int K) {
+    const void* mb[3];
+    int nb[2] = {0, 0}, N = 0;
+    for (int i = 0; i < nw; ++i) {
+      mb[i] = c->pf_wmap[wms[i]].b;
+      N += widths[i];
+      if (i + 1 < nw) nb[i] = N;
+    }
+    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, mb, nb, nw, C, ldc, 0, n, N, K, false, err, st,
+                            &c->err);
+  };
+  const bool fuse_qkv = qw % kGemmTileN == 0 && kvw % kGemmTileN == 0;
+  const bool fuse_gu = I % kGemmTileN == 0;
   pf_embed_norm_kernel<uint16_t><<<n, kPfThreads, 0, st>>>(c->at<int32_t>(L.tok), p0, c->w.embed, g.vocab,
                                                            c->layers[0].g_in, g.eps, H, X, AH, AH2, err);
   WSG_CUDA_TRY(&c->err, cudaGetLastError());
@@ -416,15 +433,24 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
       pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_in, g.eps, H, AH, AH2);
       WSG_CUDA_TRY(&c->err, cudaGetLastError());
     }
-    if ((s = gemm(0, wm + 0, QKV, W, 0, qw, H, false)) != DEC_OK) return s;
-    if ((s = gemm(0, wm + 1, QKV, W, qw, kvw, H, false)) != DEC_OK) return s;
-    if ((s = gemm(0, wm + 2, QKV, W, qw + kvw, kvw, H, false)) != DEC_OK) return s;
+    if (fuse_qkv) {
+      const int wms[3] = {wm + 0, wm + 1, wm + 2}, widths[3] = {qw, kvw, kvw};
+      if ((s = gemm_multi(0, wms, widths, 3, QKV, W, H)) != DEC_OK) return s;
+    } else {
+      if ((s = gemm(0, wm + 0, QKV, W, 0, qw, H, false)) != DEC_OK) return s;
+      if ((s = gemm(0, wm + 1, QKV, W, qw, kvw, H, false)) != DEC_OK) return s;
+      if ((s = gemm(0, wm + 2, QKV, W, qw + kvw, kvw, H, false)) != DEC_OK) return s;
+    }
     const size_t off = static_cast<size_t>(l) * c->kv_layer_elems() * dtype_bytes(g.kvdtype);
     void* kc = c->ws + L.kc + off;
     void* vc = c->ws + L.vc + off;
     pf_qk_rope_kv_kernel<KT><<<dim3(n, (g.n_q + 2 * g.n_kv + 3) / 4), 128, 0, st>>>(
         QKV, p0, g.n_q, g.n_kv, d, lw.g_q, lw.g_k, g.eps, rc, rs, kc, vc, g.max_seq);
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    // A chunk that does not end the prompt stops after the last layer's K/V
+    // write: later rows read only the cache, so that layer's attention output,
+    // O projection and MLP would feed nothing. The terminal chunk runs it all.
+    if (l == g.layers - 1 && !is_last) break;
     const float scale = 1.0f / std::sqrt(static_cast<float>(d));
     bool tc = false;
     if constexpr (sizeof(KT) == 2) {  // bfloat16 cache: tensor-core attention
@@ -448,8 +474,13 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     if ((s = gemm(1, wm + 3, X, H, 0, H, qw, true)) != DEC_OK) return s;  // O projection + residual
     pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_post, g.eps, H, AH, AH2);
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
-    if ((s = gemm(0, wm + 4, GU, 2 * I, 0, I, H, false)) != DEC_OK) return s;
-    if ((s = gemm(0, wm + 5, GU, 2 * I, I, I, H, false)) != DEC_OK) return s;
+    if (fuse_gu) {
+      const int wms[2] = {wm + 4, wm + 5}, widths[2] = {I, I};
+      if ((s = gemm_multi(0, wms, widths, 2, GU, 2 * I, H)) != DEC_OK) return s;
+    } else {
+      if ((s = gemm(0, wm + 4, GU, 2 * I, 0, I, H, false)) != DEC_OK) return s;
+      if ((s = gemm(0, wm + 5, GU, 2 * I, I, I, H, false)) != DEC_OK) return s;
+    }
     pf_swiglu_kernel<<<std::min(4 * c->di.sms, (n * I + 255) / 256), 256, 0, st>>>(GU, n, I, AI, AI2);
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     if ((s = gemm(2, wm + 6, X, H, 0, H, I, true)) != DEC_OK) return s;  // down projection + residual

@@ -8,8 +8,15 @@
 
 namespace wsg {
 
-dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* mapB, float* C, int ldc, int col0, int M,
-                            int N, int K, bool accumulate, uint32_t* err, cudaStream_t st, std::string* where) {
+static_assert(kGemmTileN == kTcBN, "the host's tile width is the kernel's");
+
+dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* const* mapsB, const int* nb, int nmaps,
+                            float* C, int ldc, int col0, int M, int N, int K, bool accumulate, uint32_t* err,
+                            cudaStream_t st, std::string* where) {
+  if (nmaps < 1 || nmaps > 3) return fail(where, DEC_EINVAL, "gemm: %d weight maps", nmaps);
+  for (int i = 1; i < nmaps; ++i)
+    if (nb[i - 1] % kTcBN || nb[i - 1] <= 0 || nb[i - 1] >= N || (i > 1 && nb[i - 1] <= nb[i - 2]))
+      return fail(where, DEC_EINVAL, "gemm: weight boundary %d is not a tile boundary inside N", nb[i - 1]);
   static bool ready[64] = {};
   DeviceInfo di;
   dec_status s = device_info(&di, where);
@@ -36,21 +43,25 @@ dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* map
   a.M = M;
   a.N = N;
   a.K = K;
+  a.nb1 = nmaps > 1 ? nb[0] : N;
+  a.nb2 = nmaps > 2 ? nb[1] : N;
   a.err = err;
   const dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
   const CUtensorMap& ma = *static_cast<const CUtensorMap*>(mapA);
   const CUtensorMap& ma2 = *static_cast<const CUtensorMap*>(mapA2 ? mapA2 : mapA);
-  const CUtensorMap& mb = *static_cast<const CUtensorMap*>(mapB);
+  const CUtensorMap& mb0 = *static_cast<const CUtensorMap*>(mapsB[0]);
+  const CUtensorMap& mb1 = *static_cast<const CUtensorMap*>(mapsB[nmaps > 1 ? 1 : 0]);
+  const CUtensorMap& mb2 = *static_cast<const CUtensorMap*>(mapsB[nmaps > 2 ? 2 : 0]);
   if (mapA2) {
     if (accumulate)
-      gemm_bf16_tc_kernel<TC_ADD, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb, a);
+      gemm_bf16_tc_kernel<TC_ADD, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
     else
-      gemm_bf16_tc_kernel<TC_STORE, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb, a);
+      gemm_bf16_tc_kernel<TC_STORE, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
   } else {
     if (accumulate)
-      gemm_bf16_tc_kernel<TC_ADD, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb, a);
+      gemm_bf16_tc_kernel<TC_ADD, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
     else
-      gemm_bf16_tc_kernel<TC_STORE, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb, a);
+      gemm_bf16_tc_kernel<TC_STORE, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
   }
   WSG_CUDA_TRY(where, cudaGetLastError());
   return DEC_OK;
@@ -77,6 +88,7 @@ extern "C" dec_status gemm_bf16(const uint16_t* d_A, const uint16_t* d_W, float*
   alignas(64) unsigned char ma[128], mb[128];
   if ((s = encode_gemm_operand(ma, d_A, M, K, nullptr)) != DEC_OK) return s;
   if ((s = encode_gemm_operand(mb, d_W, N, K, nullptr)) != DEC_OK) return s;
-  return launch_gemm_bf16(ma, nullptr, mb, d_C, ldc, 0, M, N, K, accumulate != 0, context_free_err_ptr(di.device),
-                          static_cast<cudaStream_t>(stream), nullptr);
+  const void* mbs[1] = {mb};
+  return launch_gemm_bf16(ma, nullptr, mbs, nullptr, 1, d_C, ldc, 0, M, N, K, accumulate != 0,
+                          context_free_err_ptr(di.device), static_cast<cudaStream_t>(stream), nullptr);
 }

@@ -5,7 +5,9 @@
 // [out][in]) in bfloat16 and FP32 accumulation.
 //
 // One CTA computes one 128 x 128 tile of C with tcgen05.mma (cta_group::1,
-// kind::f16, BF16 inputs, FP32 accumulator in tensor memory):
+// kind::f16, BF16 inputs, FP32 accumulator in tensor memory); one launch may
+// cover up to three weight matrices side by side in N (Q, K and V, or gate
+// and up), so the grid fills the GPU:
 //  * a TMA thread streams 128 x 64 tiles of A and W (128-byte swizzle) into a
 //    4-stage shared-memory ring (full mbarrier per stage, completed by the
 //    copies' transaction bytes);
@@ -55,6 +57,10 @@ struct TcArgs {
   int32_t ldc;   // row stride of C in elements
   int32_t col0;  // column of C where this product's column 0 goes
   int32_t M, N, K;
+  // Up to three weight matrices side by side in N: columns [0, nb1) come from
+  // mapB0, [nb1, nb2) from mapB1, [nb2, N) from mapB2 (nb1, nb2 multiples of
+  // the tile width, so no tile straddles two of them).
+  int32_t nb1, nb2;
   uint32_t* err;
 };
 
@@ -90,7 +96,8 @@ __device__ __forceinline__ void tma_load_2d_map(void* dst, const CUtensorMap* ma
 template <int EPI, bool SPLIT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
-                        const __grid_constant__ CUtensorMap mapB, const TcArgs a) {
+                        const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
+                        const __grid_constant__ CUtensorMap mapB2, const TcArgs a) {
   constexpr uint32_t kStage = tc_stage_bytes<SPLIT>();
   constexpr uint32_t kBOff = (SPLIT ? 2 : 1) * kTcABytes;  // W tile offset within a stage
   extern __shared__ __align__(1024) unsigned char tc_raw[];
@@ -124,6 +131,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ---- TMA: A and W tiles of every K block into the stage ring ----
+    const CUtensorMap* mapB = n0 < a.nb1 ? &mapB0 : n0 < a.nb2 ? &mapB1 : &mapB2;
+    const int wn0 = n0 - (n0 < a.nb1 ? 0 : n0 < a.nb2 ? a.nb1 : a.nb2);  // first row of this tile in its weight
     for (int kb = 0; kb < KB; ++kb) {
       const int s = kb % kTcStages;
       if (kb >= kTcStages && !mbar_wait(&empty[s], ((kb / kTcStages) - 1) & 1)) {
@@ -135,7 +144,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive_expect_tx(&full[s], kStage);
       tma_load_2d_map(st, &mapA, kb * kTcBK, m0, &full[s]);
       if (SPLIT) tma_load_2d_map(st + kTcABytes, &mapA2, kb * kTcBK, m0, &full[s]);
-      tma_load_2d_map(st + kBOff, &mapB, kb * kTcBK, n0, &full[s]);
+      tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, &full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA: four K = 16 steps per stage, accumulator in TMEM ----

@@ -459,7 +459,15 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
                                                                             : d == 16 ? pf_attn_tc_kernel<16> : nullptr;
       if (tk && 16 % group == 0) {
         const int rows_per_block = kPfTcWarps * (16 / group);
-        tk<<<dim3(g.n_kv, (n + rows_per_block - 1) / rows_per_block), kPfTcWarps * 32, 0, st>>>(
+        const size_t smem = pf_attn_tc_smem(d);
+        static bool lifted[64][4] = {};  // per device, per head size
+        const int hs = d == 128 ? 0 : d == 64 ? 1 : d == 32 ? 2 : 3;
+        if (!lifted[c->di.device][hs]) {
+          WSG_CUDA_TRY(&c->err, cudaFuncSetAttribute(tk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(smem)));
+          lifted[c->di.device][hs] = true;
+        }
+        tk<<<dim3(g.n_kv, (n + rows_per_block - 1) / rows_per_block), kPfTcWarps * 32, smem, st>>>(
             QKV, n, p0, g.n_q, g.n_kv, static_cast<const uint16_t*>(kc), static_cast<const uint16_t*>(vc), g.max_seq,
             scale, AO, AO2);
         tc = true;

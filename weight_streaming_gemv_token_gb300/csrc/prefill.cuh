@@ -244,14 +244,20 @@ __global__ void __launch_bounds__(kPfAttnRows * 32) pf_attn_kernel(const float* 
 // Flash-attention form with warp-level BF16 MMAs (m16n8k16, FP32
 // accumulation): a warp owns 16 query vectors, the group's query heads of
 // 16/group consecutive chunk rows (vector v = row * group + head), all on key
-// head g. For each tile of 64 keys (staged by the block: keys row-major,
-// values transposed, zero past the last key any row needs) the warp forms
-// S = Q K^T, masks keys past each row's position, updates the running max and
-// sum, and accumulates O += P V. Q and P enter the MMAs as bfloat16 value +
-// remainder pairs (two MMAs each), keys and values are the cache's bfloat16,
-// so scores and outputs keep float32 precision. Needs head_dim % 16 == 0 and
-// n_q / n_kv dividing 16.
+// head g. Tiles of 64 keys and their values are copied row-major into padded
+// shared-memory rows with cp.async (zero-filled past the last key any row of
+// the block sees), two tiles in flight, so a tile's copies overlap the
+// previous tile's MMAs; the value operand of O += P V is read transposed with
+// ldmatrix.trans. Per tile the warp forms S = Q K^T, masks keys past each
+// row's position, updates the running max and sum, and accumulates O += P V.
+// Q and P enter the MMAs as bfloat16 value + remainder pairs (two MMAs each),
+// keys and values are the cache's bfloat16, so scores and outputs keep
+// float32 precision. Needs head_dim % 16 == 0 and n_q / n_kv dividing 16.
 constexpr int kPfTcWarps = 4, kPfTcKeys = 64;
+
+// Dynamic shared memory of pf_attn_tc_kernel<D>: two stages of key and value
+// tiles, rows padded by 8 elements (conflict-free fragment and ldmatrix reads).
+constexpr size_t pf_attn_tc_smem(int D) { return 2ull * 2 * kPfTcKeys * (D + 8) * sizeof(uint16_t); }
 
 __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
@@ -260,6 +266,26 @@ __device__ __forceinline__ void mma_bf16_16816(float* c, uint32_t a0, uint32_t a
       "{%0, %1, %2, %3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 16-byte asynchronous copy global -> shared; src_bytes 0 fills zeros.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Two transposed 8x8 bfloat16 matrices: lanes 0-7 give the row addresses of
+// the first, lanes 8-15 of the second; thread t receives, per matrix, the
+// elements (2 (t % 4), t / 4) and (2 (t % 4) + 1, t / 4), low half first.
+__device__ __forceinline__ void ldmatrix_x2_trans(uint32_t& r0, uint32_t& r1, const void* row_addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(smem_u32(row_addr)));
 }
 
 // Two floats as a packed bfloat16 pair (low half: x) for value and remainder.
@@ -277,8 +303,10 @@ __global__ void __launch_bounds__(kPfTcWarps * 32) pf_attn_tc_kernel(const float
                                                                       uint16_t* AO2) {
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
   constexpr int NT = D / 8;   // n-tiles of O
-  __shared__ __align__(16) uint16_t Ks[kPfTcKeys][D + 8];
-  __shared__ __align__(16) uint16_t Vt[D][kPfTcKeys + 8];
+  constexpr int RS = D + 8;   // padded row length (elements)
+  extern __shared__ __align__(16) uint16_t pf_tc_smem[];
+  uint16_t* Kst = pf_tc_smem;                              // [2][kPfTcKeys][RS]
+  uint16_t* Vst = pf_tc_smem + 2 * kPfTcKeys * RS;         // [2][kPfTcKeys][RS]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
   const int g = blockIdx.x;
@@ -294,6 +322,18 @@ __global__ void __launch_bounds__(kPfTcWarps * 32) pf_attn_tc_kernel(const float
   const int row0 = rw + v0 / group, row1 = rw + v1 / group;
   const int pos0 = p0 + row0, pos1 = p0 + row1;
   const size_t kv_base = static_cast<size_t>(g) * max_seq * D;
+  // copies of one tile (keys t0.. into stage st): 16-byte pieces, zero past pmax
+  auto stage_tile = [&](int t0, int st) {
+    for (int i = threadIdx.x; i < kPfTcKeys * (D / 8); i += kPfTcWarps * 32) {
+      const int kk = i / (D / 8), e = (i - kk * (D / 8)) * 8;
+      const bool in = t0 + kk <= pmax;
+      const size_t at = kv_base + static_cast<size_t>(in ? t0 + kk : 0) * D + e;
+      cp_async16(Kst + (st * kPfTcKeys + kk) * RS + e, kc + at, in ? 16u : 0u);
+      cp_async16(Vst + (st * kPfTcKeys + kk) * RS + e, vc + at, in ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  stage_tile(0, 0);  // the first tile's copies overlap the Q set-up
 
   // Q fragments (value and remainder), zero for rows past the chunk
   uint32_t qh[KS][4], ql[KS][4];
@@ -318,30 +358,29 @@ __global__ void __launch_bounds__(kPfTcWarps * 32) pf_attn_tc_kernel(const float
   for (int j = 0; j < NT; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
-  for (int t0 = 0; t0 <= pmax; t0 += kPfTcKeys) {
-    __syncthreads();
-    // stage keys t0.. (row-major) and values (transposed); zero past pmax
-    for (int i = threadIdx.x; i < kPfTcKeys * (D / 8); i += kPfTcWarps * 32) {
-      const int kk = i / (D / 8), e = (i - kk * (D / 8)) * 8;
-      uint4 kv = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
-      if (t0 + kk <= pmax) {
-        const size_t at = kv_base + static_cast<size_t>(t0 + kk) * D + e;
-        kv = __ldg(reinterpret_cast<const uint4*>(kc + at));
-        vv = __ldg(reinterpret_cast<const uint4*>(vc + at));
-      }
-      *reinterpret_cast<uint4*>(&Ks[kk][e]) = kv;
-      const uint16_t* vh = reinterpret_cast<const uint16_t*>(&vv);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) Vt[e + u][kk] = vh[u];
+  for (int t0 = 0, it = 0; t0 <= pmax; t0 += kPfTcKeys, ++it) {
+    const int st = it & 1;
+    // the next tile's copies go into the other stage, freed by the barrier
+    // that ended the previous iteration
+    if (t0 + kPfTcKeys <= pmax) {
+      stage_tile(t0 + kPfTcKeys, st ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
     }
     __syncthreads();
-    if (t0 > pmax_w) continue;  // no row of this warp sees these keys
+    const uint16_t* Ks = Kst + st * kPfTcKeys * RS;
+    const uint16_t* Vs = Vst + st * kPfTcKeys * RS;
+    if (t0 > pmax_w) {  // no row of this warp sees these keys
+      __syncthreads();
+      continue;
+    }
     // S = Q K^T for 64 keys: 8 n-tiles of 8 keys
     float sc[kPfTcKeys / 8][4];
 #pragma unroll
     for (int j = 0; j < kPfTcKeys / 8; ++j) {
       sc[j][0] = sc[j][1] = sc[j][2] = sc[j][3] = 0.f;
-      const uint16_t* krow = &Ks[j * 8 + gid][0];
+      const uint16_t* krow = Ks + (j * 8 + gid) * RS;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const uint32_t b0 = *reinterpret_cast<const uint32_t*>(krow + ks * 16 + 2 * tig);
@@ -402,15 +441,17 @@ __global__ void __launch_bounds__(kPfTcWarps * 32) pf_attn_tc_kernel(const float
       pack_split(sc[2 * kk][2], sc[2 * kk][3], &ah[1], &al[1]);
       pack_split(sc[2 * kk + 1][0], sc[2 * kk + 1][1], &ah[2], &al[2]);
       pack_split(sc[2 * kk + 1][2], sc[2 * kk + 1][3], &ah[3], &al[3]);
+      // value rows kk*16 .. kk*16+15, columns j*8 ..: lane r < 16 points at row kk*16 + r
+      const uint16_t* vrow = Vs + (kk * 16 + (lane & 15)) * RS;
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        const uint16_t* vrow = &Vt[j * 8 + gid][0];
-        const uint32_t b0 = *reinterpret_cast<const uint32_t*>(vrow + kk * 16 + 2 * tig);
-        const uint32_t b1 = *reinterpret_cast<const uint32_t*>(vrow + kk * 16 + 8 + 2 * tig);
+        uint32_t b0, b1;
+        ldmatrix_x2_trans(b0, b1, vrow + j * 8);
         mma_bf16_16816(o[j], ah[0], ah[1], ah[2], ah[3], b0, b1);
         mma_bf16_16816(o[j], al[0], al[1], al[2], al[3], b0, b1);
       }
     }
+    __syncthreads();  // this stage is refilled two tiles on
   }
   // O / L as value and remainder
   const float i0 = 1.0f / l0, i1 = 1.0f / l1;

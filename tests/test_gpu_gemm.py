@@ -12,9 +12,13 @@ from gpu_util import dev, lib
 pytestmark = pytest.mark.gpu
 
 # (M, N, K): single elements, ragged M/N/K, several tiles, and the projections of
-# a 512-row chunk of the Qwen3-0.6B shape (QKV, O, gate/up, down).
+# a 512-row chunk of the Qwen3-0.6B shape (QKV, O, gate/up, down); these run
+# 64-column tiles (a grid of 128-column tiles would leave SMs idle). The last
+# two fill the GPU with 128-column tiles: the gate/up product of a 1024-row
+# chunk, and ragged M, N and K.
 SHAPES = [(1, 1, 8), (3, 5, 16), (128, 128, 64), (129, 130, 72), (200, 300, 96), (257, 64, 1024),
-          (512, 4096, 1024), (512, 1024, 2048), (300, 3072, 1024), (384, 1024, 3072)]
+          (512, 4096, 1024), (512, 1024, 2048), (300, 3072, 1024), (384, 1024, 3072),
+          (1024, 6144, 1024), (1100, 2500, 200)]
 
 
 def bf16_matrix(rows, cols, seed, scale=1.0):

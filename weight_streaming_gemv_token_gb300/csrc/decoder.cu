@@ -201,7 +201,8 @@ struct dec_ctx {
     unsigned char b[128];
   };
   Map128 pf_amap[6];
-  std::vector<Map128> pf_wmap;
+  std::vector<Map128> pf_wmap;    // weights in 128-row boxes (128-column tiles)
+  std::vector<Map128> pf_wmap64;  // the same in 64-row boxes (64-column tiles)
   std::string err;
 
   template <typename T>
@@ -402,9 +403,12 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
   // C[:, col0..col0+N) (=, or +=) rows . W^T with operand maps `amap` and
   // amap + 3 (value and remainder of: 0 normed input, 1 attention output,
   // 2 SwiGLU output) and weight map `wm`
+  // 64-column tiles when 128-column ones would leave SMs idle
+  auto wmap = [&](int wm, int bn) { return bn == 64 ? c->pf_wmap64[wm].b : c->pf_wmap[wm].b; };
   auto gemm = [&](int amap, int wm, float* C, int ldc, int col0, int N, int K, bool acc) {
-    const void* mb[1] = {c->pf_wmap[wm].b};
-    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, mb, nullptr, 1, C, ldc, col0, n, N, K, acc,
+    const int bn = gemm_tile_n(n, N, c->di.sms);
+    const void* mb[1] = {wmap(wm, bn)};
+    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, mb, nullptr, 1, bn, C, ldc, col0, n, N, K, acc,
                             err, st, &c->err);
   };
   // Several weights side by side in one launch (Q, K, V; gate, up): one grid
@@ -413,13 +417,15 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
   auto gemm_multi = [&](int amap, const int* wms, const int* widths, int nw, float* C, int ldc, int K) {
     const void* mb[3];
     int nb[2] = {0, 0}, N = 0;
-    for (int i = 0; i < nw; ++i) {
-      mb[i] = c->pf_wmap[wms[i]].b;
-      N += widths[i];
-      if (i + 1 < nw) nb[i] = N;
+    for (int i = 0; i < nw; ++i) N += widths[i];
+    const int bn = gemm_tile_n(n, N, c->di.sms);
+    for (int i = 0, acc = 0; i < nw; ++i) {
+      mb[i] = wmap(wms[i], bn);
+      acc += widths[i];
+      if (i + 1 < nw) nb[i] = acc;
     }
-    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, mb, nb, nw, C, ldc, 0, n, N, K, false, err, st,
-                            &c->err);
+    return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, mb, nb, nw, bn, C, ldc, 0, n, N, K, false, err,
+                            st, &c->err);
   };
   const bool fuse_qkv = qw % kGemmTileN == 0 && kvw % kGemmTileN == 0;
   const bool fuse_gu = I % kGemmTileN == 0;
@@ -880,12 +886,12 @@ extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_
   c->attn_smem = attn_smem_bytes(cfg->n_q / cfg->n_kv, cfg->head_dim);
   if (L.pf_rows > 0) {
     const dec_status ms[6] = {
-        encode_gemm_operand(c->pf_amap[0].b, c->ws + L.pf_ah, L.pf_rows, cfg->hidden, &c->err),
-        encode_gemm_operand(c->pf_amap[1].b, c->ws + L.pf_ao, L.pf_rows, qw, &c->err),
-        encode_gemm_operand(c->pf_amap[2].b, c->ws + L.pf_ai, L.pf_rows, cfg->inter, &c->err),
-        encode_gemm_operand(c->pf_amap[3].b, c->ws + L.pf_ah2, L.pf_rows, cfg->hidden, &c->err),
-        encode_gemm_operand(c->pf_amap[4].b, c->ws + L.pf_ao2, L.pf_rows, qw, &c->err),
-        encode_gemm_operand(c->pf_amap[5].b, c->ws + L.pf_ai2, L.pf_rows, cfg->inter, &c->err)};
+        encode_gemm_operand(c->pf_amap[0].b, c->ws + L.pf_ah, L.pf_rows, cfg->hidden, 128, &c->err),
+        encode_gemm_operand(c->pf_amap[1].b, c->ws + L.pf_ao, L.pf_rows, qw, 128, &c->err),
+        encode_gemm_operand(c->pf_amap[2].b, c->ws + L.pf_ai, L.pf_rows, cfg->inter, 128, &c->err),
+        encode_gemm_operand(c->pf_amap[3].b, c->ws + L.pf_ah2, L.pf_rows, cfg->hidden, 128, &c->err),
+        encode_gemm_operand(c->pf_amap[4].b, c->ws + L.pf_ao2, L.pf_rows, qw, 128, &c->err),
+        encode_gemm_operand(c->pf_amap[5].b, c->ws + L.pf_ai2, L.pf_rows, cfg->inter, 128, &c->err)};
     for (dec_status m : ms)
       if (m != DEC_OK) {
         thread_error() = c->err;
@@ -959,6 +965,7 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
     const dec_config& g = c->cfg;
     const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;
     c->pf_wmap.resize(static_cast<size_t>(g.layers) * kMkMapsPerLayer);
+    c->pf_wmap64.resize(static_cast<size_t>(g.layers) * kMkMapsPerLayer);
     for (int l = 0; l < g.layers; ++l) {
       const dec_layer_weights& x = c->layers[l];
       const struct {
@@ -968,8 +975,9 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
                               {x.w_o, g.hidden, qw},    {x.w_gate, g.inter, g.hidden}, {x.w_up, g.inter, g.hidden},
                               {x.w_down, g.hidden, g.inter}};
       for (int k = 0; k < kMkMapsPerLayer; ++k) {
-        const dec_status st =
-            encode_gemm_operand(c->pf_wmap[static_cast<size_t>(l) * kMkMapsPerLayer + k].b, t[k].p, t[k].rows, t[k].K, &c->err);
+        const size_t i = static_cast<size_t>(l) * kMkMapsPerLayer + k;
+        dec_status st = encode_gemm_operand(c->pf_wmap[i].b, t[k].p, t[k].rows, t[k].K, 128, &c->err);
+        if (st == DEC_OK) st = encode_gemm_operand(c->pf_wmap64[i].b, t[k].p, t[k].rows, t[k].K, 64, &c->err);
         if (st != DEC_OK) return st;
       }
     }

@@ -8,34 +8,65 @@
 
 namespace wsg {
 
-static_assert(kGemmTileN == kTcBN, "the host's tile width is the kernel's");
+static_assert(kGemmTileN == kTcBN, "the host's tile width is the kernel's widest");
+
+template <int BN>
+dec_status set_smem_once(int dev, std::string* where) {
+  static bool ready[64] = {};
+  if (ready[dev]) return DEC_OK;
+  WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE, false, BN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(tc_smem_bytes<false, BN>())));
+  WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD, false, BN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(tc_smem_bytes<false, BN>())));
+  WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE, true, BN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(tc_smem_bytes<true, BN>())));
+  WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD, true, BN>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(tc_smem_bytes<true, BN>())));
+  ready[dev] = true;
+  return DEC_OK;
+}
+
+template <int BN>
+void launch_tc(bool split, bool accumulate, dim3 grid, const CUtensorMap& ma, const CUtensorMap& ma2,
+               const CUtensorMap& mb0, const CUtensorMap& mb1, const CUtensorMap& mb2, const TcArgs& a,
+               cudaStream_t st) {
+  if (split) {
+    if (accumulate)
+      gemm_bf16_tc_kernel<TC_ADD, true, BN><<<grid, kTcThreads, tc_smem_bytes<true, BN>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
+    else
+      gemm_bf16_tc_kernel<TC_STORE, true, BN><<<grid, kTcThreads, tc_smem_bytes<true, BN>(), st>>>(ma, ma2, mb0, mb1, mb2,
+                                                                                                    a);
+  } else {
+    if (accumulate)
+      gemm_bf16_tc_kernel<TC_ADD, false, BN><<<grid, kTcThreads, tc_smem_bytes<false, BN>(), st>>>(ma, ma2, mb0, mb1, mb2,
+                                                                                                    a);
+    else
+      gemm_bf16_tc_kernel<TC_STORE, false, BN><<<grid, kTcThreads, tc_smem_bytes<false, BN>(), st>>>(ma, ma2, mb0, mb1,
+                                                                                                      mb2, a);
+  }
+}
+
+int gemm_tile_n(int M, int N, int sms) {
+  const long long tiles = static_cast<long long>((N + kTcBN - 1) / kTcBN) * ((M + kTcBM - 1) / kTcBM);
+  return tiles < sms ? 64 : 128;
+}
 
 dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* const* mapsB, const int* nb, int nmaps,
-                            float* C, int ldc, int col0, int M, int N, int K, bool accumulate, uint32_t* err,
+                            int bn, float* C, int ldc, int col0, int M, int N, int K, bool accumulate, uint32_t* err,
                             cudaStream_t st, std::string* where) {
+  if (bn != 64 && bn != 128) return fail(where, DEC_EINVAL, "gemm: tile width %d", bn);
   if (nmaps < 1 || nmaps > 3) return fail(where, DEC_EINVAL, "gemm: %d weight maps", nmaps);
   for (int i = 1; i < nmaps; ++i)
-    if (nb[i - 1] % kTcBN || nb[i - 1] <= 0 || nb[i - 1] >= N || (i > 1 && nb[i - 1] <= nb[i - 2]))
+    if (nb[i - 1] % bn || nb[i - 1] <= 0 || nb[i - 1] >= N || (i > 1 && nb[i - 1] <= nb[i - 2]))
       return fail(where, DEC_EINVAL, "gemm: weight boundary %d is not a tile boundary inside N", nb[i - 1]);
-  static bool ready[64] = {};
   DeviceInfo di;
   dec_status s = device_info(&di, where);
   if (s != DEC_OK) return s;
-  if (!ready[di.device]) {
-    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(tc_smem_bytes<false>())));
-    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(tc_smem_bytes<false>())));
-    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_STORE, true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(tc_smem_bytes<true>())));
-    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD, true>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(tc_smem_bytes<true>())));
-    ready[di.device] = true;
-  }
+  if ((s = bn == 64 ? set_smem_once<64>(di.device, where) : set_smem_once<128>(di.device, where)) != DEC_OK) return s;
   TcArgs a;
   a.C = C;
   a.ldc = ldc;
@@ -46,29 +77,22 @@ dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* con
   a.nb1 = nmaps > 1 ? nb[0] : N;
   a.nb2 = nmaps > 2 ? nb[1] : N;
   a.err = err;
-  const dim3 grid((N + kTcBN - 1) / kTcBN, (M + kTcBM - 1) / kTcBM);
+  const dim3 grid((N + bn - 1) / bn, (M + kTcBM - 1) / kTcBM);
   const CUtensorMap& ma = *static_cast<const CUtensorMap*>(mapA);
   const CUtensorMap& ma2 = *static_cast<const CUtensorMap*>(mapA2 ? mapA2 : mapA);
   const CUtensorMap& mb0 = *static_cast<const CUtensorMap*>(mapsB[0]);
   const CUtensorMap& mb1 = *static_cast<const CUtensorMap*>(mapsB[nmaps > 1 ? 1 : 0]);
   const CUtensorMap& mb2 = *static_cast<const CUtensorMap*>(mapsB[nmaps > 2 ? 2 : 0]);
-  if (mapA2) {
-    if (accumulate)
-      gemm_bf16_tc_kernel<TC_ADD, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
-    else
-      gemm_bf16_tc_kernel<TC_STORE, true><<<grid, kTcThreads, tc_smem_bytes<true>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
-  } else {
-    if (accumulate)
-      gemm_bf16_tc_kernel<TC_ADD, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
-    else
-      gemm_bf16_tc_kernel<TC_STORE, false><<<grid, kTcThreads, tc_smem_bytes<false>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
-  }
+  if (bn == 64)
+    launch_tc<64>(mapA2 != nullptr, accumulate, grid, ma, ma2, mb0, mb1, mb2, a, st);
+  else
+    launch_tc<128>(mapA2 != nullptr, accumulate, grid, ma, ma2, mb0, mb1, mb2, a, st);
   WSG_CUDA_TRY(where, cudaGetLastError());
   return DEC_OK;
 }
 
-dec_status encode_gemm_operand(void* out, const void* base, long long rows, int K, std::string* err) {
-  return encode_map_2d(out, base, rows, K, 2, kTcBK, kTcBM, true, err);
+dec_status encode_gemm_operand(void* out, const void* base, long long rows, int K, int box_rows, std::string* err) {
+  return encode_map_2d(out, base, rows, K, 2, kTcBK, box_rows, true, err);
 }
 
 }  // namespace wsg
@@ -86,9 +110,10 @@ extern "C" dec_status gemm_bf16(const uint16_t* d_A, const uint16_t* d_W, float*
   dec_status s = device_info(&di, nullptr);
   if (s != DEC_OK) return s;
   alignas(64) unsigned char ma[128], mb[128];
-  if ((s = encode_gemm_operand(ma, d_A, M, K, nullptr)) != DEC_OK) return s;
-  if ((s = encode_gemm_operand(mb, d_W, N, K, nullptr)) != DEC_OK) return s;
+  const int bn = gemm_tile_n(M, N, di.sms);
+  if ((s = encode_gemm_operand(ma, d_A, M, K, kTcBM, nullptr)) != DEC_OK) return s;
+  if ((s = encode_gemm_operand(mb, d_W, N, K, bn, nullptr)) != DEC_OK) return s;
   const void* mbs[1] = {mb};
-  return launch_gemm_bf16(ma, nullptr, mbs, nullptr, 1, d_C, ldc, 0, M, N, K, accumulate != 0,
+  return launch_gemm_bf16(ma, nullptr, mbs, nullptr, 1, bn, d_C, ldc, 0, M, N, K, accumulate != 0,
                           context_free_err_ptr(di.device), static_cast<cudaStream_t>(stream), nullptr);
 }

@@ -4,7 +4,7 @@
 // C += that product, with A (activation rows) and W (weights, row-major
 // [out][in]) in bfloat16 and FP32 accumulation.
 //
-// One CTA computes one 128 x 128 tile of C with tcgen05.mma (cta_group::1,
+// One CTA computes one 128 x 128 (or 128 x 64) tile of C with tcgen05.mma (cta_group::1,
 // kind::f16, BF16 inputs, FP32 accumulator in tensor memory); one launch may
 // cover up to three weight matrices side by side in N (Q, K and V, or gate
 // and up), so the grid fills the GPU:
@@ -34,18 +34,22 @@
 
 namespace wsg {
 
+// Tiles of C are kTcBM x BN, BN = 128 (kTcBN) or 64 (for grids that would not
+// fill the GPU with 128-column tiles).
 constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64, kTcStages = 4, kTcThreads = 128;
 constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
-constexpr uint32_t kTcBBytes = kTcBN * kTcBK * 2;  // 16 KB
-constexpr uint32_t kTcTmemCols = kTcBN;  // FP32 accumulator: 128 lanes x 128 columns
-// stage: A tile (and with SPLIT the A-remainder tile), then the W tile
-template <bool SPLIT>
-constexpr uint32_t tc_stage_bytes() {
-  return (SPLIT ? 2 : 1) * kTcABytes + kTcBBytes;
+template <int BN>
+constexpr uint32_t tc_b_bytes() {
+  return BN * kTcBK * 2;
 }
-template <bool SPLIT>
+// stage: A tile (and with SPLIT the A-remainder tile), then the W tile
+template <bool SPLIT, int BN>
+constexpr uint32_t tc_stage_bytes() {
+  return (SPLIT ? 2 : 1) * kTcABytes + tc_b_bytes<BN>();
+}
+template <bool SPLIT, int BN>
 constexpr size_t tc_smem_bytes() {
-  return kTcStages * tc_stage_bytes<SPLIT>() + 1024;  // plus alignment slack
+  return kTcStages * tc_stage_bytes<SPLIT, BN>() + 1024;  // plus alignment slack
 }
 
 enum : uint32_t { ERR_TC_TIMEOUT = 1u << 5 };
@@ -93,20 +97,22 @@ __device__ __forceinline__ void tma_load_2d_map(void* dst, const CUtensorMap* ma
       : "memory");
 }
 
-template <int EPI, bool SPLIT>
+template <int EPI, bool SPLIT, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
                         const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
                         const __grid_constant__ CUtensorMap mapB2, const TcArgs a) {
-  constexpr uint32_t kStage = tc_stage_bytes<SPLIT>();
+  static_assert(BN == 64 || BN == 128, "64- or 128-column tiles");
+  constexpr uint32_t kStage = tc_stage_bytes<SPLIT, BN>();
   constexpr uint32_t kBOff = (SPLIT ? 2 : 1) * kTcABytes;  // W tile offset within a stage
+  constexpr uint32_t kTmemCols = BN;                       // FP32 accumulator: 128 lanes x BN columns
   extern __shared__ __align__(1024) unsigned char tc_raw[];
   unsigned char* tsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], done;
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * kTcBN, m0 = blockIdx.y * kTcBM;
+  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kTcBM;
   const int KB = (a.K + kTcBK - 1) / kTcBK;
 
   if (tid == 0) {
@@ -120,7 +126,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                 "n"(kTcTmemCols)
+                 "n"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
@@ -148,7 +154,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA: four K = 16 steps per stage, accumulator in TMEM ----
-    constexpr uint32_t idesc = tc_idesc(kTcBM, kTcBN);
+    constexpr uint32_t idesc = tc_idesc(kTcBM, BN);
     bool ok = true;
     for (int kb = 0; kb < KB; ++kb) {
       const int s = kb % kTcStages;
@@ -194,7 +200,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int row = m0 + warp * 32 + lane;
   if (__all_sync(0xffffffffu, have)) {
 #pragma unroll 1
-    for (int c0 = 0; c0 < kTcBN; c0 += 32) {
+    for (int c0 = 0; c0 < BN; c0 += 32) {
       uint32_t v[32];
       const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c0);
       asm volatile(
@@ -244,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTcTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(kTmemCols) : "memory");
 }
 
 }  // namespace wsg

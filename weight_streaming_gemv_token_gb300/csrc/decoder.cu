@@ -55,7 +55,7 @@ struct Layout {
   size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn, ll_act,
       ll_tok, ll_apart, kv_ready, mk_layers, mk_maps, rope_cos, rope_sin, kc, vc;
   // chunked prefill (chunk_cap > 0): rows padded to a multiple of 128
-  size_t pf_x, pf_ah, pf_ah2, pf_qkv, pf_ao, pf_ao2, pf_gu, pf_ai, pf_ai2;  // *2: bfloat16 remainders
+  size_t pf_x, pf_ah, pf_ah2, pf_qkv, pf_ao, pf_ao2, pf_ai, pf_ai2;  // *2: bfloat16 remainders
   int pf_rows;
   size_t total;
 };
@@ -128,7 +128,6 @@ Layout make_layout(const dec_config& c) {
     L.pf_qkv = take(R * (qw + 2 * kvw) * 4);
     L.pf_ao = take(R * qw * 2);
     L.pf_ao2 = take(R * qw * 2);
-    L.pf_gu = take(R * 2 * c.inter * 4);
     L.pf_ai = take(R * c.inter * 2);
     L.pf_ai2 = take(R * c.inter * 2);
   }
@@ -393,7 +392,6 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
   float* QKV = c->at<float>(L.pf_qkv);
   uint16_t* AO = c->at<uint16_t>(L.pf_ao);
   uint16_t* AO2 = c->at<uint16_t>(L.pf_ao2);
-  float* GU = c->at<float>(L.pf_gu);
   uint16_t* AI = c->at<uint16_t>(L.pf_ai);
   uint16_t* AI2 = c->at<uint16_t>(L.pf_ai2);
   uint32_t* err = c->at<uint32_t>(L.err);
@@ -428,7 +426,6 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
                             st, &c->err);
   };
   const bool fuse_qkv = qw % kGemmTileN == 0 && kvw % kGemmTileN == 0;
-  const bool fuse_gu = I % kGemmTileN == 0;
   pf_embed_norm_kernel<uint16_t><<<n, kPfThreads, 0, st>>>(c->at<int32_t>(L.tok), p0, c->w.embed, g.vocab,
                                                            c->layers[0].g_in, g.eps, H, X, AH, AH2, err);
   WSG_CUDA_TRY(&c->err, cudaGetLastError());
@@ -488,15 +485,10 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     if ((s = gemm(1, wm + 3, X, H, 0, H, qw, true)) != DEC_OK) return s;  // O projection + residual
     pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_post, g.eps, H, AH, AH2);
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
-    if (fuse_gu) {
-      const int wms[2] = {wm + 4, wm + 5}, widths[2] = {I, I};
-      if ((s = gemm_multi(0, wms, widths, 2, GU, 2 * I, H)) != DEC_OK) return s;
-    } else {
-      if ((s = gemm(0, wm + 4, GU, 2 * I, 0, I, H, false)) != DEC_OK) return s;
-      if ((s = gemm(0, wm + 5, GU, 2 * I, I, I, H, false)) != DEC_OK) return s;
-    }
-    pf_swiglu_kernel<<<std::min(4 * c->di.sms, (n * I + 255) / 256), 256, 0, st>>>(GU, n, I, AI, AI2);
-    WSG_CUDA_TRY(&c->err, cudaGetLastError());
+    // gate/up with SwiGLU in the GEMM's epilogue: tiles pair 64 gate and 64 up outputs
+    if ((s = launch_gemm_swiglu(c->pf_amap[0].b, c->pf_amap[3].b, c->pf_wmap64[wm + 4].b, c->pf_wmap64[wm + 5].b, AI,
+                                AI2, I, n, I, H, err, st, &c->err)) != DEC_OK)
+      return s;
     if ((s = gemm(2, wm + 6, X, H, 0, H, I, true)) != DEC_OK) return s;  // down projection + residual
   }
   // Position word (the head's position, or the next one) and, for the

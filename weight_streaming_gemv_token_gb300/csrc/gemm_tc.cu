@@ -26,6 +26,10 @@ dec_status set_smem_once(int dev, std::string* where) {
   WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_ADD, true, BN>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(tc_smem_bytes<true, BN>())));
+  if constexpr (BN == 128)
+    WSG_CUDA_TRY(where, cudaFuncSetAttribute(gemm_bf16_tc_kernel<TC_SWIGLU, true, BN>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(tc_smem_bytes<true, BN>())));
   ready[dev] = true;
   return DEC_OK;
 }
@@ -48,6 +52,36 @@ void launch_tc(bool split, bool accumulate, dim3 grid, const CUtensorMap& ma, co
       gemm_bf16_tc_kernel<TC_STORE, false, BN><<<grid, kTcThreads, tc_smem_bytes<false, BN>(), st>>>(ma, ma2, mb0, mb1,
                                                                                                       mb2, a);
   }
+}
+
+dec_status launch_gemm_swiglu(const void* mapA, const void* mapA2, const void* mapGate64, const void* mapUp64,
+                              uint16_t* act, uint16_t* act2, int ld_act, int M, int I, int K, uint32_t* err,
+                              cudaStream_t st, std::string* where) {
+  DeviceInfo di;
+  dec_status s = device_info(&di, where);
+  if (s != DEC_OK) return s;
+  if ((s = set_smem_once<128>(di.device, where)) != DEC_OK) return s;
+  TcArgs a;
+  a.C = nullptr;
+  a.ldc = 0;
+  a.col0 = 0;
+  a.M = M;
+  a.N = 2 * I;
+  a.K = K;
+  a.nb1 = a.nb2 = 2 * I;
+  a.act = act;
+  a.act2 = act2;
+  a.ld_act = ld_act;
+  a.err = err;
+  const dim3 grid((I + 63) / 64, (M + kTcBM - 1) / kTcBM);  // 64 outputs (128 accumulator columns) per tile
+  const CUtensorMap& ma = *static_cast<const CUtensorMap*>(mapA);
+  const CUtensorMap& ma2 = *static_cast<const CUtensorMap*>(mapA2);
+  const CUtensorMap& mg = *static_cast<const CUtensorMap*>(mapGate64);
+  const CUtensorMap& mu = *static_cast<const CUtensorMap*>(mapUp64);
+  gemm_bf16_tc_kernel<TC_SWIGLU, true, 128><<<grid, kTcThreads, tc_smem_bytes<true, 128>(), st>>>(ma, ma2, mg, mu, mg,
+                                                                                                   a);
+  WSG_CUDA_TRY(where, cudaGetLastError());
+  return DEC_OK;
 }
 
 int gemm_tile_n(int M, int N, int sms) {

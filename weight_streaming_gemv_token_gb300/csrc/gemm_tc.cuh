@@ -16,6 +16,12 @@
 //    mbarrier; a final commit signals the accumulator complete;
 //  * all four warps then read their 32 TMEM lanes (rows) with tcgen05.ld and
 //    store (or add) their rows of C.
+// TC_SWIGLU (128-column tiles): tile j takes rows 64j..64j+63 of the gate
+// weights (mapB0, 64-row boxes) and the same rows of the up weights (mapB1)
+// as one 128-row W tile, so accumulator columns 0-63 hold gate and 64-127 up
+// of the same 64 outputs; the epilogue writes silu(gate) * up for them as a
+// bfloat16 value + remainder pair (the next GEMM's activation operand), and
+// the gate/up product never goes to memory.
 // With SPLIT the activation operand comes as two bfloat16 matrices, A = hi +
 // lo (hi the nearest bfloat16 of a float32 value, lo the nearest bfloat16 of
 // the remainder), and both products go into the same accumulator: the rows
@@ -30,6 +36,7 @@
 
 #include <cstdint>
 
+#include "gemv_stream.cuh"  // silu_f32
 #include "ptx.cuh"
 
 namespace wsg {
@@ -54,7 +61,9 @@ constexpr size_t tc_smem_bytes() {
 
 enum : uint32_t { ERR_TC_TIMEOUT = 1u << 5 };
 
-enum TcEpi : int { TC_STORE = 0, TC_ADD = 1 };
+// Epilogues: store C, add into C, or (TC_SWIGLU) the gate/up product's
+// SwiGLU written as bfloat16 value + remainder (see the kernel).
+enum TcEpi : int { TC_STORE = 0, TC_ADD = 1, TC_SWIGLU = 2 };
 
 struct TcArgs {
   float* C;
@@ -65,6 +74,10 @@ struct TcArgs {
   // mapB0, [nb1, nb2) from mapB1, [nb2, N) from mapB2 (nb1, nb2 multiples of
   // the tile width, so no tile straddles two of them).
   int32_t nb1, nb2;
+  // TC_SWIGLU: act / act2 [M][ld_act] receive the value and remainder of silu(gate) * up
+  uint16_t* act;
+  uint16_t* act2;
+  int32_t ld_act;
   uint32_t* err;
 };
 
@@ -97,12 +110,25 @@ __device__ __forceinline__ void tma_load_2d_map(void* dst, const CUtensorMap* ma
       : "memory");
 }
 
+// 32 consecutive accumulator columns of this warp's 32 lanes (one register each).
+__device__ __forceinline__ void tc_ld32(uint32_t (&v)[32], uint32_t taddr) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr));
+}
+
 template <int EPI, bool SPLIT, int BN>
 __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
                         const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
                         const __grid_constant__ CUtensorMap mapB2, const TcArgs a) {
   static_assert(BN == 64 || BN == 128, "64- or 128-column tiles");
+  static_assert(EPI != TC_SWIGLU || BN == 128, "the SwiGLU epilogue pairs 64 gate and 64 up columns");
   constexpr uint32_t kStage = tc_stage_bytes<SPLIT, BN>();
   constexpr uint32_t kBOff = (SPLIT ? 2 : 1) * kTcABytes;  // W tile offset within a stage
   constexpr uint32_t kTmemCols = BN;                       // FP32 accumulator: 128 lanes x BN columns
@@ -150,7 +176,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_arrive_expect_tx(&full[s], kStage);
       tma_load_2d_map(st, &mapA, kb * kTcBK, m0, &full[s]);
       if (SPLIT) tma_load_2d_map(st + kTcABytes, &mapA2, kb * kTcBK, m0, &full[s]);
-      tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, &full[s]);
+      if constexpr (EPI == TC_SWIGLU) {
+        tma_load_2d_map(st + kBOff, &mapB0, kb * kTcBK, n0 / 2, &full[s]);
+        tma_load_2d_map(st + kBOff + tc_b_bytes<64>(), &mapB1, kb * kTcBK, n0 / 2, &full[s]);
+      } else {
+        tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, &full[s]);
+      }
     }
   } else if (warp == 1 && lane == 0) {
     // ---- MMA: four K = 16 steps per stage, accumulator in TMEM ----
@@ -198,7 +229,51 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (!have && lane == 0) atomicOr(a.err, ERR_TC_TIMEOUT);
   tc_fence_after();
   const int row = m0 + warp * 32 + lane;
-  if (__all_sync(0xffffffffu, have)) {
+  if constexpr (EPI == TC_SWIGLU) {
+    if (__all_sync(0xffffffffu, have)) {
+      const int half = a.N / 2;  // outputs of the whole product
+#pragma unroll 1
+      for (int c0 = 0; c0 < 64; c0 += 32) {
+        uint32_t gv[32], uv[32];
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c0);
+        tc_ld32(gv, taddr);
+        tc_ld32(uv, taddr + 64);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        const int col0 = n0 / 2 + c0;
+        if (row < a.M) {
+          uint16_t* h = a.act + static_cast<size_t>(row) * a.ld_act + col0;
+          uint16_t* l = a.act2 + static_cast<size_t>(row) * a.ld_act + col0;
+          uint32_t hp[16], lp[16];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float v = silu_f32(__uint_as_float(gv[j])) * __uint_as_float(uv[j]);
+            const uint16_t hb = f32_to_bf16_rn(v), lb = f32_to_bf16_rn(v - bf16_to_f32(hb));
+            if (j & 1) {
+              hp[j >> 1] |= static_cast<uint32_t>(hb) << 16;
+              lp[j >> 1] |= static_cast<uint32_t>(lb) << 16;
+            } else {
+              hp[j >> 1] = hb;
+              lp[j >> 1] = lb;
+            }
+          }
+          if (col0 + 32 <= half && ((reinterpret_cast<uintptr_t>(h) | reinterpret_cast<uintptr_t>(l)) & 15u) == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              reinterpret_cast<uint4*>(h)[q] = make_uint4(hp[4 * q], hp[4 * q + 1], hp[4 * q + 2], hp[4 * q + 3]);
+              reinterpret_cast<uint4*>(l)[q] = make_uint4(lp[4 * q], lp[4 * q + 1], lp[4 * q + 2], lp[4 * q + 3]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (col0 + j < half) {
+                h[j] = static_cast<uint16_t>(hp[j >> 1] >> (16 * (j & 1)));
+                l[j] = static_cast<uint16_t>(lp[j >> 1] >> (16 * (j & 1)));
+              }
+          }
+        }
+      }
+    }
+  } else if (__all_sync(0xffffffffu, have)) {
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
       uint32_t v[32];

@@ -35,4 +35,12 @@ dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* con
                             int bn, float* C, int ldc, int col0, int M, int N, int K, bool accumulate, uint32_t* err,
                             cudaStream_t st, std::string* where);
 
+// Gate/up product of the chunk rows with SwiGLU fused: act / act2 [M][ld_act]
+// (bfloat16 value and remainder) = silu(A . Wg^T) * (A . Wu^T), A = A + A2
+// from mapA / mapA2, the gate and up weights [I][K] in 64-row boxes. The
+// gate/up product itself is not written. Asynchronous on st.
+dec_status launch_gemm_swiglu(const void* mapA, const void* mapA2, const void* mapGate64, const void* mapUp64,
+                              uint16_t* act, uint16_t* act2, int ld_act, int M, int I, int K, uint32_t* err,
+                              cudaStream_t st, std::string* where);
+
 }  // namespace wsg

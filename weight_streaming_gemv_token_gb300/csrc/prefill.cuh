@@ -8,8 +8,9 @@
 //   embedding gather + input RMSNorm (layer 0)   pf_embed_norm_kernel
 //   RMSNorm of the residual rows                  pf_norm_kernel
 //   per-head Q/K RMSNorm, RoPE, K/V cache append  pf_qk_rope_kv_kernel
-//   causal grouped-query attention                pf_attn_kernel
-//   SwiGLU of the gate/up rows                    pf_swiglu_kernel
+//   causal grouped-query attention                pf_attn_tc_kernel (bfloat16
+//                                                 cache), pf_attn_kernel
+// (SwiGLU runs in the gate/up GEMM's epilogue.)
 //
 // The residual rows stay float32; each GEMM operand row (normalised rows,
 // attention output, SwiGLU output) is written as a pair of bfloat16 rows,
@@ -468,17 +469,6 @@ __global__ void __launch_bounds__(kPfTcWarps * 32) pf_attn_tc_kernel(const float
       pf_split(o[j][2] * i1, AO, AO2, at);
       pf_split(o[j][3] * i1, AO, AO2, at + 1);
     }
-  }
-}
-
-// (AI, AI2)[r][j] = silu(GU[r][j]) * GU[r][I + j] as value and remainder.
-__global__ void pf_swiglu_kernel(const float* GU, int n, int I, uint16_t* AI, uint16_t* AI2) {
-  const size_t total = static_cast<size_t>(n) * I;
-  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const size_t r = i / I, j = i - r * I;
-    const float* gu = GU + r * 2 * I;
-    pf_split(silu_f32(gu[j]) * gu[I + j], AI, AI2, i);
   }
 }
 

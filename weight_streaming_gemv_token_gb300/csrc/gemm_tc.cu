@@ -73,7 +73,9 @@ dec_status launch_gemm_swiglu(const void* mapA, const void* mapA2, const void* m
   a.act2 = act2;
   a.ld_act = ld_act;
   a.err = err;
-  const dim3 grid((I + 63) / 64, (M + kTcBM - 1) / kTcBM);  // 64 outputs (128 accumulator columns) per tile
+  // 64 outputs (128 accumulator columns) per tile; persistent, one CTA per SM
+  const long long tiles = static_cast<long long>((I + 63) / 64) * ((M + kTcBM - 1) / kTcBM);
+  const dim3 grid(static_cast<unsigned>(tiles < di.sms ? tiles : di.sms));
   const CUtensorMap& ma = *static_cast<const CUtensorMap*>(mapA);
   const CUtensorMap& ma2 = *static_cast<const CUtensorMap*>(mapA2);
   const CUtensorMap& mg = *static_cast<const CUtensorMap*>(mapGate64);
@@ -111,7 +113,9 @@ dec_status launch_gemm_bf16(const void* mapA, const void* mapA2, const void* con
   a.nb1 = nmaps > 1 ? nb[0] : N;
   a.nb2 = nmaps > 2 ? nb[1] : N;
   a.err = err;
-  const dim3 grid((N + bn - 1) / bn, (M + kTcBM - 1) / kTcBM);
+  // persistent: one CTA per SM (fewer when there are fewer tiles)
+  const long long tiles = static_cast<long long>((N + bn - 1) / bn) * ((M + kTcBM - 1) / kTcBM);
+  const dim3 grid(static_cast<unsigned>(tiles < di.sms ? tiles : di.sms));
   const CUtensorMap& ma = *static_cast<const CUtensorMap*>(mapA);
   const CUtensorMap& ma2 = *static_cast<const CUtensorMap*>(mapA2 ? mapA2 : mapA);
   const CUtensorMap& mb0 = *static_cast<const CUtensorMap*>(mapsB[0]);

@@ -4,18 +4,22 @@
 // C += that product, with A (activation rows) and W (weights, row-major
 // [out][in]) in bfloat16 and FP32 accumulation.
 //
-// One CTA computes one 128 x 128 (or 128 x 64) tile of C with tcgen05.mma (cta_group::1,
-// kind::f16, BF16 inputs, FP32 accumulator in tensor memory); one launch may
-// cover up to three weight matrices side by side in N (Q, K and V, or gate
-// and up), so the grid fills the GPU:
-//  * a TMA thread streams 128 x 64 tiles of A and W (128-byte swizzle) into a
-//    4-stage shared-memory ring (full mbarrier per stage, completed by the
-//    copies' transaction bytes);
-//  * an MMA thread issues four K = 16 MMAs per stage from shared-memory
-//    descriptors and releases the stage with tcgen05.commit on its empty
-//    mbarrier; a final commit signals the accumulator complete;
-//  * all four warps then read their 32 TMEM lanes (rows) with tcgen05.ld and
-//    store (or add) their rows of C.
+// Tiles of C are 128 x 128 (or 128 x 64), computed with tcgen05.mma
+// (cta_group::1, kind::f16, BF16 inputs, FP32 accumulator in tensor memory);
+// one launch may cover up to three weight matrices side by side in N (Q, K
+// and V, or gate and up). The kernel is persistent: one CTA per SM walks the
+// tiles blockIdx.x, blockIdx.x + gridDim.x, ...
+//  * warp 0: a TMA thread streams 128 x 64 tiles of A and W (128-byte swizzle)
+//    of every K block of every tile into a 4-stage shared-memory ring (full
+//    mbarrier per stage, completed by the copies' transaction bytes);
+//  * warp 1: an MMA thread issues four K = 16 MMAs per stage from shared-
+//    memory descriptors into one of two accumulator buffers in tensor memory
+//    (alternating by tile), releases each stage with tcgen05.commit on its
+//    empty mbarrier and, after a tile's last stage, commits the buffer full;
+//  * warps 2-5: each reads its quarter of the accumulator lanes (32 rows) with
+//    tcgen05.ld, stores (or adds, or SwiGLUs) the rows and marks the buffer
+//    empty, while the MMA thread already fills the other buffer with the next
+//    tile: a tile's epilogue overlaps the next tile's main loop.
 // TC_SWIGLU (128-column tiles): tile j takes rows 64j..64j+63 of the gate
 // weights (mapB0, 64-row boxes) and the same rows of the up weights (mapB1)
 // as one 128-row W tile, so accumulator columns 0-63 hold gate and 64-127 up
@@ -43,7 +47,8 @@ namespace wsg {
 
 // Tiles of C are kTcBM x BN, BN = 128 (kTcBN) or 64 (for grids that would not
 // fill the GPU with 128-column tiles).
-constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64, kTcStages = 4, kTcThreads = 128;
+// Warps: 0 TMA, 1 MMA (and tensor-memory allocation), 2-5 epilogue.
+constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64, kTcStages = 4, kTcEpiWarps = 4, kTcThreads = 32 * (2 + kTcEpiWarps);
 constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
 template <int BN>
 constexpr uint32_t tc_b_bytes() {
@@ -122,120 +127,17 @@ __device__ __forceinline__ void tc_ld32(uint32_t (&v)[32], uint32_t taddr) {
       : "r"(taddr));
 }
 
-template <int EPI, bool SPLIT, int BN>
-__global__ void __launch_bounds__(kTcThreads, 1)
-    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
-                        const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
-                        const __grid_constant__ CUtensorMap mapB2, const TcArgs a) {
-  static_assert(BN == 64 || BN == 128, "64- or 128-column tiles");
-  static_assert(EPI != TC_SWIGLU || BN == 128, "the SwiGLU epilogue pairs 64 gate and 64 up columns");
-  constexpr uint32_t kStage = tc_stage_bytes<SPLIT, BN>();
-  constexpr uint32_t kBOff = (SPLIT ? 2 : 1) * kTcABytes;  // W tile offset within a stage
-  constexpr uint32_t kTmemCols = BN;                       // FP32 accumulator: 128 lanes x BN columns
-  extern __shared__ __align__(1024) unsigned char tc_raw[];
-  unsigned char* tsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], done;
-  __shared__ uint32_t tmem_base;
-  __shared__ int s_fail;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * BN, m0 = blockIdx.y * kTcBM;
-  const int KB = (a.K + kTcBK - 1) / kTcBK;
-
-  if (tid == 0) {
-    for (int s = 0; s < kTcStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(&done, 1);
-    s_fail = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                 "n"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base;
-
-  if (warp == 0 && lane == 0) {
-    // ---- TMA: A and W tiles of every K block into the stage ring ----
-    const CUtensorMap* mapB = n0 < a.nb1 ? &mapB0 : n0 < a.nb2 ? &mapB1 : &mapB2;
-    const int wn0 = n0 - (n0 < a.nb1 ? 0 : n0 < a.nb2 ? a.nb1 : a.nb2);  // first row of this tile in its weight
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % kTcStages;
-      if (kb >= kTcStages && !mbar_wait(&empty[s], ((kb / kTcStages) - 1) & 1)) {
-        s_fail = 1;
-        atomicOr(a.err, ERR_TC_TIMEOUT);
-        break;
-      }
-      unsigned char* st = tsm + static_cast<size_t>(s) * kStage;
-      mbar_arrive_expect_tx(&full[s], kStage);
-      tma_load_2d_map(st, &mapA, kb * kTcBK, m0, &full[s]);
-      if (SPLIT) tma_load_2d_map(st + kTcABytes, &mapA2, kb * kTcBK, m0, &full[s]);
-      if constexpr (EPI == TC_SWIGLU) {
-        tma_load_2d_map(st + kBOff, &mapB0, kb * kTcBK, n0 / 2, &full[s]);
-        tma_load_2d_map(st + kBOff + tc_b_bytes<64>(), &mapB1, kb * kTcBK, n0 / 2, &full[s]);
-      } else {
-        tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, &full[s]);
-      }
-    }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA: four K = 16 steps per stage, accumulator in TMEM ----
-    constexpr uint32_t idesc = tc_idesc(kTcBM, BN);
-    bool ok = true;
-    for (int kb = 0; kb < KB; ++kb) {
-      const int s = kb % kTcStages;
-      if (!mbar_wait(&full[s], (kb / kTcStages) & 1)) {
-        s_fail = 1;
-        atomicOr(a.err, ERR_TC_TIMEOUT);
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t sa = smem_u32(tsm + static_cast<size_t>(s) * kStage);
-      const uint32_t sb = sa + kBOff;
-#pragma unroll
-      for (int kk = 0; kk < kTcBK / 16; ++kk) {
-        const uint64_t db = tc_desc_sw128(sb + kk * 32);
-#pragma unroll
-        for (int part = 0; part < (SPLIT ? 2 : 1); ++part) {
-          const uint64_t da = tc_desc_sw128(sa + part * kTcABytes + kk * 32);
-          const uint32_t acc = (kb | kk | part) != 0;
-          asm volatile(
-              "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-              "l"(da), "l"(db), "r"(idesc), "r"(acc)
-              : "memory");
-        }
-      }
-      // the stage's shared memory is free once these MMAs have read it
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_u32(&empty[s]))
-                   : "memory");
-    }
-    if (ok)
-      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-                       smem_u32(&done))
-                   : "memory");
-  }
-
-  // ---- epilogue: warp w holds rows 32w..32w+31 of the tile in its TMEM lanes ----
-  __syncwarp();
-  const bool have = mbar_wait(&done, 0);
-  if (!have && lane == 0) atomicOr(a.err, ERR_TC_TIMEOUT);
-  tc_fence_after();
-  const int row = m0 + warp * 32 + lane;
+// Epilogue of one tile for one warp: its 32 rows (TMEM lanes at tbase), every
+// column of the tile; `row` is this lane's row of C.
+template <int EPI, int BN>
+__device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tbase, int row, int n0) {
   if constexpr (EPI == TC_SWIGLU) {
-    if (__all_sync(0xffffffffu, have)) {
+    {
       const int half = a.N / 2;  // outputs of the whole product
 #pragma unroll 1
       for (int c0 = 0; c0 < 64; c0 += 32) {
         uint32_t gv[32], uv[32];
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c0);
+        const uint32_t taddr = tbase + static_cast<uint32_t>(c0);
         tc_ld32(gv, taddr);
         tc_ld32(uv, taddr + 64);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
@@ -273,11 +175,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-  } else if (__all_sync(0xffffffffu, have)) {
+  } else {
 #pragma unroll 1
     for (int c0 = 0; c0 < BN; c0 += 32) {
       uint32_t v[32];
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(c0);
+      const uint32_t taddr = tbase + static_cast<uint32_t>(c0);
       asm volatile(
           "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
           "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -320,6 +222,161 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
       }
+    }
+  }
+}
+
+template <int EPI, bool SPLIT, int BN>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
+                        const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
+                        const __grid_constant__ CUtensorMap mapB2, const TcArgs a) {
+  static_assert(BN == 64 || BN == 128, "64- or 128-column tiles");
+  static_assert(EPI != TC_SWIGLU || BN == 128, "the SwiGLU epilogue pairs 64 gate and 64 up columns");
+  constexpr uint32_t kStage = tc_stage_bytes<SPLIT, BN>();
+  constexpr uint32_t kBOff = (SPLIT ? 2 : 1) * kTcABytes;  // W tile offset within a stage
+  constexpr uint32_t kTmemCols = 2 * BN;                   // two FP32 accumulators of 128 lanes x BN columns
+  extern __shared__ __align__(1024) unsigned char tc_raw[];
+  unsigned char* tsm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(tc_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ __align__(8) uint64_t full[kTcStages], empty[kTcStages], tfull[2], tempty[2], drain;
+  __shared__ uint32_t tmem_base;
+  __shared__ int s_fail;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ntn = (a.N + BN - 1) / BN, ntiles = ntn * ((a.M + kTcBM - 1) / kTcBM);
+  const int KB = (a.K + kTcBK - 1) / kTcBK;
+  volatile int* vfail = &s_fail;
+
+  if (tid == 0) {
+    for (int s = 0; s < kTcStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], kTcEpiWarps);
+    }
+    mbar_init(&drain, 1);
+    s_fail = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                 "n"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  auto fail = [&]() {
+    *vfail = 1;
+    atomicOr(a.err, ERR_TC_TIMEOUT);
+  };
+
+  if (warp == 0) {
+    // ---- TMA: A and W tiles of every K block of every tile into the stage ring ----
+    if (lane == 0) {
+      uint32_t gk = 0;  // k blocks issued by this CTA (ring position)
+      for (int t = blockIdx.x; t < ntiles && !*vfail; t += gridDim.x) {
+        const int n0 = (t % ntn) * BN, m0 = (t / ntn) * kTcBM;
+        const CUtensorMap* mapB = n0 < a.nb1 ? &mapB0 : n0 < a.nb2 ? &mapB1 : &mapB2;
+        const int wn0 = n0 - (n0 < a.nb1 ? 0 : n0 < a.nb2 ? a.nb1 : a.nb2);  // first row of the tile in its weight
+        for (int kb = 0; kb < KB; ++kb, ++gk) {
+          const int s = gk % kTcStages;
+          if (gk >= kTcStages && !mbar_wait(&empty[s], ((gk / kTcStages) - 1) & 1)) {
+            fail();
+            break;
+          }
+          if (*vfail) break;
+          unsigned char* st = tsm + static_cast<size_t>(s) * kStage;
+          mbar_arrive_expect_tx(&full[s], kStage);
+          tma_load_2d_map(st, &mapA, kb * kTcBK, m0, &full[s]);
+          if (SPLIT) tma_load_2d_map(st + kTcABytes, &mapA2, kb * kTcBK, m0, &full[s]);
+          if constexpr (EPI == TC_SWIGLU) {
+            tma_load_2d_map(st + kBOff, &mapB0, kb * kTcBK, n0 / 2, &full[s]);
+            tma_load_2d_map(st + kBOff + tc_b_bytes<64>(), &mapB1, kb * kTcBK, n0 / 2, &full[s]);
+          } else {
+            tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, &full[s]);
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---- MMA: four K = 16 steps per stage into the tile's accumulator buffer ----
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc_idesc(kTcBM, BN);
+      uint32_t gk = 0;
+      int li = 0;  // tiles of this CTA so far
+      for (int t = blockIdx.x; t < ntiles && !*vfail; t += gridDim.x, ++li) {
+        const int b = li & 1;
+        // the epilogue has drained this buffer (its tile two back)
+        if (li >= 2 && !mbar_wait(&tempty[b], ((li >> 1) - 1) & 1)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb, ++gk) {
+          const int s = gk % kTcStages;
+          if (!mbar_wait(&full[s], (gk / kTcStages) & 1)) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(tsm + static_cast<size_t>(s) * kStage);
+          const uint32_t sb = sa + kBOff;
+#pragma unroll
+          for (int kk = 0; kk < kTcBK / 16; ++kk) {
+            const uint64_t db = tc_desc_sw128(sb + kk * 32);
+#pragma unroll
+            for (int part = 0; part < (SPLIT ? 2 : 1); ++part) {
+              const uint64_t da = tc_desc_sw128(sa + part * kTcABytes + kk * 32);
+              const uint32_t acc = (kb | kk | part) != 0;
+              asm volatile(
+                  "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                  "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                  "l"(da), "l"(db), "r"(idesc), "r"(acc)
+                  : "memory");
+            }
+          }
+          // the stage's shared memory is free once these MMAs have read it
+          asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                           smem_u32(&empty[s]))
+                       : "memory");
+        }
+        if (!ok) break;
+        asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                         smem_u32(&tfull[b]))
+                     : "memory");
+      }
+      // every MMA this thread issued has completed before tensor memory is freed
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                       smem_u32(&drain))
+                   : "memory");
+      if (!mbar_wait(&drain, 0)) fail();
+    }
+  } else {
+    // ---- epilogue warps: warp w reads TMEM lanes (rows) 32 (w % 4) .. 32 (w % 4) + 31 ----
+    const int q = warp & 3;
+    int li = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++li) {
+      const int b = li & 1;
+      const bool have = mbar_wait(&tfull[b], (li >> 1) & 1);
+      if (!__all_sync(0xffffffffu, have)) {
+        if (lane == 0) fail();
+        break;
+      }
+      tc_fence_after();
+      const int n0 = (t % ntn) * BN, m0 = (t / ntn) * kTcBM;
+      const int row = m0 + q * 32 + lane;
+      const uint32_t tbase = tmem + static_cast<uint32_t>(b * BN) + (static_cast<uint32_t>(q * 32) << 16);
+      tc_epilogue<EPI, BN>(a, tbase, row, n0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[b]);
     }
   }
   tc_fence_before();

@@ -320,9 +320,6 @@ __device__ __forceinline__ float reduce_scatter(float (&a)[N], int lane) {
   return v;
 }
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
 
 // Warpgroup-wide register reallocation (every thread of the warpgroup executes it).
 template <int N>

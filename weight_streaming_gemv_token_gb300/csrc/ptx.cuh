@@ -65,6 +65,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
   return ok != 0;
 }
 
+// Plain arrival (count 1) on an mbarrier, release semantics.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // Non-blocking test of a phase parity.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t phase) {
   uint32_t ok;

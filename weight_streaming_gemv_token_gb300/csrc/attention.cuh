@@ -440,9 +440,9 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
           io.store_part(pb + d + 1, L);
         }
       } else {
-        // split 0: fold in the other splits in order, a few at a time (their
-        // words requested together, then polled)
-        constexpr int KC = 4;
+        // split 0: fold in the other splits in order, eight at a time (their
+        // words requested together, then polled; sixteen at a time spills)
+        constexpr int KC = 8;
         for (int k0 = 1; k0 < nsplit; k0 += KC) {
           float ov[KC], mv[KC], lv[KC];
           io.template poll_parts<KC>(pbase + k0 * pstride, pstride, min(KC, nsplit - k0), e, d, ov, mv, lv);

@@ -30,15 +30,15 @@ def check_token(got_logits, ref_logits, tok, tol, what):
         assert tok == ref_tok, f"{what}: GPU {tok} vs oracle {ref_tok}"
 
 
-def run_chunked(shape, weights, prompt, chunk, n_out, engine, kv_every=1):
+def run_chunked(shape, weights, prompt, chunk, n_out, engine, kv_every=1, kv_dtype="bf16"):
     import torch
 
     lib()
     from weight_streaming_gemv_token_gb300.decoder import Decoder
 
     max_seq = len(prompt) + n_out + 4
-    dec = Decoder(shape, weights, kv_dtype="bf16", max_seq=max_seq, chunk_cap=chunk, engine=engine)
-    ora = O.OracleDecoder(shape, weights, kv_dtype="bf16", max_seq=max_seq)
+    dec = Decoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq, chunk_cap=chunk, engine=engine)
+    ora = O.OracleDecoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq)
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
     # GPU: the prompt in chunks of `chunk` rows; oracle: token by token
     for c0 in range(0, len(prompt), chunk):
@@ -104,6 +104,16 @@ def test_fused_projection_launches_ragged_k():
     w = Wl.decoder_weights(shape, seed=5, wdtype="bf16")
     prompt = Wl.prompt_zipf(150, shape.vocab, seed=1)
     run_chunked(shape, w, prompt, 64, 3, "persistent")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "f32"])
+def test_head_dim_128_both_cache_types(kv_dtype):
+    """head_dim 128 (the Qwen3 head) with a bfloat16 cache (tensor-core attention) and a float32
+    cache (the CUDA-core attention kernel); 200 rows in chunks of 64 (ragged)."""
+    shape = Wl.DecoderShape(layers=2, hidden=256, inter=512, n_q=4, n_kv=2, head_dim=128, vocab=500)
+    w = Wl.decoder_weights(shape, seed=6, wdtype="bf16")
+    prompt = Wl.prompt_zipf(200, shape.vocab, seed=3)
+    run_chunked(shape, w, prompt, 64, 3, "persistent", kv_dtype=kv_dtype)
 
 
 def test_single_row_chunks():

@@ -48,7 +48,7 @@ METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 # (387,484,160 read + 2,817,280 written) / 387,186,688 algorithmic bytes; the excess is the
 # rows a tiled box reads past a CTA's row range. Set to None when the kernel changes until it
 # is measured again.
-MK_TRAFFIC_PER_ALG_BYTE = (387484160 + 2817280) / 387186688
+MK_TRAFFIC_PER_ALG_BYTE = (387497216 + 2738688) / 387186688
 # DRAM bytes (read + written) per launch of the standalone gemv bulk-copy kernel at 151936x1024 f32
 # (the tied vocabulary shape), from ncu (profiles/gemv_bulk_151936x1024.md: 622,377,984 B read +
 # 3,492,352 B written); None until measured for the current kernel.

@@ -138,12 +138,14 @@ def dist_setup():
 
 
 def barrier_max(value: float, ws: int) -> float:
+    """The largest value over the ranks (the slowest rank's time); NCCL reduces on the GPU, gloo on the CPU."""
     if ws == 1:
         return value
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 

@@ -150,7 +150,9 @@ dec_status dec_rewind(dec_ctx* ctx, int32_t pos);
  * Without DEC_SKIP_LOGITS: final RMSNorm, tied vocabulary projection and
  * argmax (lowest ID on ties) run too. d_logits (nullable, float32[vocab])
  * receives the logits; h_next (nullable) receives the greedy token, and
- * then the call synchronizes the stream to read it.
+ * then the call synchronizes the stream to read it. On the persistent engine
+ * the token is passed with the launch and the greedy token is written by the
+ * kernel into mapped page-locked host memory (no copy calls per step).
  * With DEC_SKIP_LOGITS: only the body runs; d_logits and h_next must be NULL.
  * Errors: DEC_ESTATE (no weights), DEC_ECAPACITY (p == max_seq),
  * DEC_EINVAL (token outside [0, vocab), bad flags). */

@@ -184,6 +184,7 @@ struct dec_ctx {
   int32_t pos = 0;
   int32_t* h_tok = nullptr;   // pinned [max_seq + 1], one slot per position
   int32_t* h_next = nullptr;  // pinned
+  int32_t* d_h_next = nullptr;  // h_next as the device addresses it (mapped)
   cudaGraphExec_t g_full = nullptr, g_body = nullptr;
   Plan p_qkv, p_o, p_gu, p_down, p_vocab;
   size_t attn_smem = 0;
@@ -725,8 +726,11 @@ dec_status plan_persistent(dec_ctx* c) {
 }
 
 // nsteps forwards at positions pos0.. in one cooperative launch.
-dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, bool head_last) {
+dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, bool head_last, int32_t first_tok = -1,
+                          int32_t* host_next = nullptr) {
   MkArgs a = c->mk;
+  a.first_tok = first_tok;
+  a.host_next = host_next;
   a.embed = c->w.embed;
   a.g_final = c->w.g_final;
   a.pos0 = pos0;
@@ -843,7 +847,8 @@ extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_
   };
   cudaError_t e = cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaMallocHost(&c->h_tok, sizeof(int32_t) * (cfg->max_seq + 1));
-  if (e == cudaSuccess) e = cudaMallocHost(&c->h_next, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaHostAlloc(&c->h_next, sizeof(int32_t), cudaHostAllocMapped);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->d_h_next), c->h_next, 0);
   if (e != cudaSuccess) return bail(fail(nullptr, DEC_ECUDA, "dec_create: %s", cudaGetErrorString(e)));
 
   // Rotary table: angle = p * theta^(-2i/d), evaluated in double, stored float32.
@@ -1020,10 +1025,32 @@ extern "C" dec_status dec_step(dec_ctx* c, int32_t token, uint32_t flags, float*
   const bool persistent = c->cfg.engine == DEC_ENGINE_PERSISTENT;
   dec_status s = persistent ? DEC_OK : ensure_graphs(c, full);
   if (s != DEC_OK) return s;
-  if ((s = put_tokens(c, &token, 1)) != DEC_OK) return s;
-  s = persistent ? run_persistent(c, c->pos, 1, full, false) : run_steps(c, full, 1);
-  if (s != DEC_OK) return s;
+  if (token < 0 || token >= c->cfg.vocab)
+    return fail(&c->err, DEC_EINVAL, "token %d is outside [0, %d)", token, c->cfg.vocab);
   const int32_t p = c->pos;
+  if (persistent) {
+    // The token goes in with the launch and the greedy token comes back through
+    // mapped host memory: no copies around the kernel.
+    c->h_tok[p] = token;
+    int32_t* hn = nullptr;
+    if (full && h_next) {
+      *c->h_next = -1;
+      hn = c->d_h_next;
+    }
+    if ((s = run_persistent(c, p, 1, full, false, token, hn)) != DEC_OK) return s;
+    c->pos += 1;
+    if (!full) return DEC_OK;
+    if (d_logits)
+      WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(d_logits, c->at<float>(c->L.logits), sizeof(float) * c->cfg.vocab,
+                                            cudaMemcpyDeviceToDevice, c->stream));
+    if (h_next) {
+      WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
+      *h_next = *static_cast<volatile int32_t*>(c->h_next);
+    }
+    return DEC_OK;
+  }
+  if ((s = put_tokens(c, &token, 1)) != DEC_OK) return s;
+  if ((s = run_steps(c, full, 1)) != DEC_OK) return s;
   c->pos += 1;
   if (full) return finish_head(c, p, d_logits, h_next);
   return DEC_OK;

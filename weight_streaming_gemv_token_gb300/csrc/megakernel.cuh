@@ -135,6 +135,8 @@ struct MkArgs {
   int32_t xs_floats, part_floats, hown_floats;
   int32_t pos0, nsteps;
   int32_t head_every, head_last;  // head on every step / on the last step
+  int32_t first_tok;   // >= 0: the first step's token (else read from tok[pos0])
+  int32_t* host_next;  // optional (host memory mapped to the device): the last step's greedy token
   uint64_t* trace;  // optional: [G][L + 1][5][4] globaltimer stamps of the first forward
 };
 
@@ -966,6 +968,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     if (step > 0 && a.head_every) {
       const uint64_t* p = a.ll_tok;
       tok = __float_as_int(ll_wait(p, mk_tag(a, step - 1, a.L, 0), ll_load(p), vabort, a.err));
+    } else if (step == 0 && a.first_tok >= 0) {
+      tok = a.first_tok;  // passed with the launch: no copy ahead of it
+      if (c == 0 && tid == 0) a.tok[pos] = tok;
     } else {
       tok = __ldcg(a.tok + pos);
     }
@@ -1140,6 +1145,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           atomicOr(a.err, ERR_ARGMAX_NAN);
         }
         a.tok[pos + 1] = gi;
+        if (a.host_next && step == a.nsteps - 1) *a.host_next = gi;  // read by the host after the launch
         *a.mcnt = 0u;
         ll_store_release(a.ll_tok, __int_as_float(gi), mk_tag(a, step, a.L, 0));
       }

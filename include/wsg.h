@@ -73,7 +73,9 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
 /* Decoder geometry and storage ("Megakernels", "What runs in the DSL").
  * Requirements: layers, hidden, inter, n_q, n_kv, head_dim, vocab > 0;
  * n_q % n_kv == 0; head_dim a multiple of 8 and <= 128; hidden, inter and
- * n_q*head_dim multiples of 8; wdtype DEC_F32 or DEC_BF16; kvdtype DEC_F32
+ * n_q*head_dim multiples of 8; wdtype DEC_F32, DEC_BF16 or DEC_Q4G64 (the
+ * 4-bit configuration: staged engine, chunk_cap 0, hidden, inter and
+ * n_q*head_dim multiples of 512 up to 16384); kvdtype DEC_F32
  * or DEC_BF16; max_seq >= 1 is the KV capacity in positions; chunk_cap is
  * the largest row count of one dec_prefill_chunk call that runs batched
  * (0: prompts are processed one token at a time). engine selects the
@@ -94,6 +96,10 @@ typedef struct {
 } dec_config;
 
 /* One layer's tensors, device pointers, row-major [out][in] in wdtype.
+ * With DEC_Q4G64 each matrix pointer (and embed) points at one buffer
+ * holding the codes [out][in/8] uint32 (code j of word w at bits
+ * [4j, 4j+4), column 8w+j), then the scales and then the biases
+ * [out][in/64] fp16: w = s * q + b per 64-column group.
  * w_q [n_q*head_dim][hidden], w_k and w_v [n_kv*head_dim][hidden],
  * w_o [hidden][n_q*head_dim], w_gate and w_up [inter][hidden],
  * w_down [hidden][inter]; gains are float32: g_in and g_post [hidden],
@@ -157,6 +163,23 @@ dec_status dec_rewind(dec_ctx* ctx, int32_t pos);
  * Errors: DEC_ESTATE (no weights), DEC_ECAPACITY (p == max_seq),
  * DEC_EINVAL (token outside [0, vocab), bad flags). */
 dec_status dec_step(dec_ctx* ctx, int32_t token, uint32_t flags, float* d_logits, int32_t* h_next);
+
+/* Two-token verify step of the 4-bit configuration (cfg.wdtype ==
+ * DEC_Q4G64): one forward of h_tokens[0] at position p and h_tokens[1] at
+ * p+1, where row 1 attends to row 0's cache entry, both through the final
+ * norm, the vocabulary projection and the argmax; every projection runs the
+ * two-token 4-bit matrix-vector product ("Our Kernel Benchmark Was Measuring
+ * the System Cache", Summary: the 4-bit matvec and its two-token variant,
+ * the shape of checking a drafted token). d_logits (nullable) receives
+ * float32[2][vocab]; h_next (nullable) receives int32[2], the greedy token
+ * after each row, and then the call synchronizes the stream to read them.
+ * Writes cache entries p and p+1 and advances the position to p+2; the
+ * token stream holds h_next[1] at p+2. A caller whose draft h_tokens[1]
+ * differs from h_next[0] rewinds to p+1 (dec_rewind) and continues from
+ * h_next[0].
+ * Errors: DEC_EINVAL (NULL, token outside [0, vocab), not the 4-bit
+ * configuration), DEC_ESTATE (no weights), DEC_ECAPACITY (p + 2 > max_seq). */
+dec_status dec_verify2(dec_ctx* ctx, const int32_t* h_tokens, float* d_logits, int32_t* h_next);
 
 /* Prompt rows h_tokens[0..n) at positions p..p+n-1 ("Chunked prefill for
  * long prompts"). If cfg.chunk_cap > 0 and n <= chunk_cap the rows run

@@ -77,6 +77,28 @@ def test_workspace_size_host_logic(lib):
         assert B.dec_workspace_bytes(c2) == 0, field
 
 
+def test_q4_configuration_rules(lib):
+    """The 4-bit configuration: staged engine, tokenwise prompts, widths multiples of 512; its
+    workspace holds two rows of activations and logits for the verify step."""
+    import workloads as Wl
+    from weight_streaming_gemv_token_gb300 import binding as B
+
+    s = Wl.QWEN3_06B
+    cfg = B.dec_config(layers=s.layers, hidden=s.hidden, inter=s.inter, n_q=s.n_q, n_kv=s.n_kv, head_dim=s.head_dim,
+                       vocab=s.vocab, eps=1e-6, rope_theta=1e6, wdtype=B.DEC_BF16, kvdtype=B.DEC_F32,
+                       max_seq=512, chunk_cap=0, engine=B.DEC_ENGINE_STAGED)
+    n_bf16 = B.dec_workspace_bytes(cfg)
+    cfg.wdtype = B.DEC_Q4G64
+    n_q4 = B.dec_workspace_bytes(cfg)
+    assert n_q4 >= n_bf16 + 4 * s.vocab  # a second logit row
+    for field, bad in [("engine", B.DEC_ENGINE_PERSISTENT), ("chunk_cap", 128), ("hidden", 1024 + 64),
+                       ("inter", 3072 + 256), ("n_q", 12)]:
+        c2 = B.dec_config.from_buffer_copy(cfg)
+        setattr(c2, field, bad)
+        assert B.dec_workspace_bytes(c2) == 0, field
+    assert lib.dec_verify2(None, None, None, None) == B.DEC_EINVAL
+
+
 def test_host_side_argument_errors(lib):
     from weight_streaming_gemv_token_gb300 import binding as B
 

@@ -25,7 +25,8 @@ def kv_to_np(t):
 ENGINES = ["persistent", "staged"]
 
 
-def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every=1, max_seq=None, engine="persistent"):
+def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every=1, max_seq=None, engine="persistent",
+                    oracle_weights=None, act_round=None):
     import torch
 
     W = lib()
@@ -33,7 +34,8 @@ def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every
 
     max_seq = max_seq or (len(prompt) + n_out + 4)
     dec = Decoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq, engine=engine)
-    ora = O.OracleDecoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq)
+    ora = O.OracleDecoder(shape, oracle_weights if oracle_weights is not None else weights, kv_dtype=kv_dtype,
+                          max_seq=max_seq, act_round=act_round)
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
     dec.reset()
     # tokenwise prefill: body only for all but the last prompt token

@@ -28,6 +28,7 @@ from .binding import (  # noqa: F401
     dec_set_trace,
     dec_step,
     dec_trace_bytes,
+    dec_verify2,
     dec_weights,
     dec_workspace_bytes,
     gemm_bf16,

@@ -28,7 +28,7 @@ EXPORTED = (
     "dec_generate", "dec_get_kv", "dec_position", "dec_trace_bytes", "dec_set_trace", "dec_device_errors",
     "dec_destroy", "dec_last_error",
     "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors", "greedy_head_noalloc", "gemm_bf16",
-    "pack_bf16_exact",
+    "pack_bf16_exact", "dec_verify2",
 )
 
 
@@ -73,6 +73,7 @@ def library() -> ctypes.CDLL:
             "dec_load_weights": (c_int32, [c_void_p, P(dec_weights)]),
             "dec_reset": (c_int32, [c_void_p]),
             "dec_rewind": (c_int32, [c_void_p, c_int32]),
+            "dec_verify2": (c_int32, [c_void_p, P(c_int32), c_void_p, P(c_int32)]),
             "dec_step": (c_int32, [c_void_p, c_int32, c_uint32, c_void_p, P(c_int32)]),
             "dec_prefill_chunk": (c_int32, [c_void_p, P(c_int32), c_int32, c_int32, c_void_p, P(c_int32)]),
             "dec_generate": (c_int32, [c_void_p, c_int32, c_int32, c_void_p]),
@@ -152,6 +153,15 @@ def dec_step(ctx: int, token: int, flags: int = 0, d_logits=None, want_next: boo
     nxt = c_int32(-1)
     _check(library().dec_step(ctx, token, flags, _ptr(d_logits), ctypes.byref(nxt) if want_next else None), ctx)
     return nxt.value if want_next else None
+
+
+def dec_verify2(ctx: int, tokens, d_logits=None) -> tuple[int, int]:
+    if len(tokens) != 2:
+        raise ValueError("dec_verify2 takes two tokens")
+    arr = (c_int32 * 2)(int(tokens[0]), int(tokens[1]))
+    nxt = (c_int32 * 2)(-1, -1)
+    _check(library().dec_verify2(ctx, arr, _ptr(d_logits), nxt), ctx)
+    return nxt[0], nxt[1]
 
 
 def dec_prefill_chunk(ctx: int, tokens, is_last: bool, d_logits=None, want_next: bool = True) -> int | None:

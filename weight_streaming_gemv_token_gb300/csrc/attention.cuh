@@ -38,6 +38,7 @@ struct AttnArgs {
   int32_t nsplit_max, tmin;
   float scale;  // 1/sqrt(d)
   uint32_t* err;
+  int32_t pos_add;  // attn_decode_kernel: the row's position is ctrl[0] + pos_add
 };
 
 template <typename KT>
@@ -503,7 +504,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const Attn
   __shared__ int s_last;
   pdl_trigger();
   pdl_wait();
-  const int pos = a.ctrl[0];
+  const int pos = a.ctrl[0] + a.pos_add;
   if (pos < 0 || pos >= a.max_seq) {
     if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) atomicOr(a.err, ERR_BAD_POSITION);
     return;

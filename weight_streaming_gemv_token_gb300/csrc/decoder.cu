@@ -28,6 +28,7 @@
 
 #include "attention.cuh"
 #include "common.h"
+#include "gemv_q4.cuh"
 #include "gemv_stream.cuh"
 #include "gemm_tc_host.h"
 #include "megakernel.cuh"
@@ -52,7 +53,8 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
 
 struct Layout {
-  size_t ctrl, err, tok, h, qkv, attn, act, logits, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn, ll_act,
+  size_t ctrl, err, tok, h, qkv, attn, act, logits, q4gu, q4next, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn,
+      ll_act,
       ll_tok, ll_apart, kv_ready, mk_layers, mk_maps, rope_cos, rope_sin, kc, vc;
   // chunked prefill (chunk_cap > 0): rows padded to a multiple of 128
   size_t pf_x, pf_ah, pf_ah2, pf_qkv, pf_ao, pf_ao2, pf_ai, pf_ai2;  // *2: bfloat16 remainders
@@ -73,7 +75,16 @@ bool config_ok(const dec_config* c, std::string* why) {
   if (c->head_dim % 8 || c->head_dim > 128) return bad("head_dim must be a multiple of 8 and <= 128");
   if (c->hidden % 8 || c->inter % 8 || (c->n_q * c->head_dim) % 8)
     return bad("hidden, inter and n_q*head_dim must be multiples of 8");
-  if (c->wdtype != DEC_F32 && c->wdtype != DEC_BF16) return bad("wdtype must be DEC_F32 or DEC_BF16");
+  if (c->wdtype != DEC_F32 && c->wdtype != DEC_BF16 && c->wdtype != DEC_Q4G64)
+    return bad("wdtype must be DEC_F32, DEC_BF16 or DEC_Q4G64");
+  if (c->wdtype == DEC_Q4G64) {
+    if (c->engine != DEC_ENGINE_STAGED) return bad("4-bit weights (DEC_Q4G64) run on the staged engine");
+    if (c->chunk_cap != 0) return bad("4-bit weights (DEC_Q4G64) take prompts one token at a time (chunk_cap 0)");
+    const int w[3] = {c->hidden, c->inter, c->n_q * c->head_dim};
+    for (int x : w)
+      if (x % 512 || x > 16384)
+        return bad("4-bit weights: hidden, inter and n_q*head_dim must be multiples of 512, at most 16384");
+  }
   if (c->kvdtype != DEC_F32 && c->kvdtype != DEC_BF16) return bad("kvdtype must be DEC_F32 or DEC_BF16");
   if (c->max_seq < 1) return bad("max_seq must be >= 1");
   if (c->chunk_cap < 0) return bad("chunk_cap must be >= 0");
@@ -94,14 +105,18 @@ Layout make_layout(const dec_config& c) {
   };
   const size_t qw = static_cast<size_t>(c.n_q) * c.head_dim, kvw = static_cast<size_t>(c.n_kv) * c.head_dim;
   const int group = c.n_q / c.n_kv;
+  const bool q4 = c.wdtype == DEC_Q4G64;
+  const size_t rows = q4 ? 2 : 1;  // the 4-bit configuration's verify step runs two rows
   L.ctrl = take(64 * 4);
   L.err = take(16);
   L.tok = take((static_cast<size_t>(c.max_seq) + 1) * 4);
-  L.h = take(static_cast<size_t>(c.hidden) * 4);
-  L.qkv = take((qw + 2 * kvw) * 4);
-  L.attn = take(qw * 4);
+  L.h = take(rows * c.hidden * 4);
+  L.qkv = take(rows * (qw + 2 * kvw) * 4);
+  L.attn = take(rows * qw * 4);
   L.act = take(static_cast<size_t>(c.inter) * 4);
-  L.logits = take(static_cast<size_t>(c.vocab) * 4);
+  L.logits = take(rows * c.vocab * 4);
+  L.q4gu = take(q4 ? rows * 2 * c.inter * 4 : 0);  // gate then up, per row
+  L.q4next = take(16);
   L.apart = take(static_cast<size_t>(c.n_kv) * kSplitMax * group * (c.head_dim + 2) * 4);
   L.acnt = take(static_cast<size_t>(c.n_kv) * 4);
   L.mval = take(kArgmaxPartsMax * 4);
@@ -183,9 +198,10 @@ struct dec_ctx {
   std::vector<dec_layer_weights> layers;
   int32_t pos = 0;
   int32_t* h_tok = nullptr;   // pinned [max_seq + 1], one slot per position
-  int32_t* h_next = nullptr;  // pinned
+  int32_t* h_next = nullptr;  // pinned, two slots
   int32_t* d_h_next = nullptr;  // h_next as the device addresses it (mapped)
   cudaGraphExec_t g_full = nullptr, g_body = nullptr;
+  cudaGraphExec_t g_verify = nullptr;  // 4-bit configuration: two rows through the head
   Plan p_qkv, p_o, p_gu, p_down, p_vocab;
   size_t attn_smem = 0;
   int nsplit_max = 1;
@@ -373,6 +389,255 @@ dec_status enqueue_step_t(dec_ctx* c, cudaStream_t st, bool full) {
   return DEC_OK;
 }
 
+
+// ---- 4-bit configuration ----
+//
+// Every projection (Q/K/V, O, gate/up, down and the tied vocabulary head) is a
+// 4-bit groupwise-affine matrix ("Our Kernel Benchmark Was Measuring the
+// System Cache", Summary: the 4-bit matvec and its two-token variant) streamed
+// by gemv_q4_bulk_kernel, whose prologue builds the bfloat16 x it consumes
+// (RMSNorm, SwiGLU or a plain rounding of the float32 attention output) and
+// whose epilogue stores or adds into the residual. A weight pointer points at
+// one buffer holding codes [rows][in/8] u32, then scales and then biases
+// [rows][in/64] fp16. Per layer: QKV (one launch over the three matrices),
+// attention once per row, O (+= residual), gate/up (one launch over both),
+// down (+= residual); then the head and the argmax. The verify step runs two
+// rows at positions p and p + 1 through the same launches (two-token x).
+
+Q4Seg q4_seg(const void* blob, int rows, int in, int y_off) {
+  const char* b = static_cast<const char*>(blob);
+  const size_t code_bytes = static_cast<size_t>(rows) * in / 2, sb = static_cast<size_t>(rows) * (in / 64) * 2;
+  Q4Seg s{};
+  s.codes = reinterpret_cast<const uint32_t*>(b);
+  s.scale = reinterpret_cast<const uint16_t*>(b + code_bytes);
+  s.bias = reinterpret_cast<const uint16_t*>(b + code_bytes + sb);
+  s.rows = rows;
+  s.y_off = y_off;
+  return s;
+}
+
+// h[t] = the dequantised embedding row of the token at position ctrl[0] + t:
+// w = s * q + b (product, then sum, each rounded to float32).
+__global__ void q4_embed_kernel(const int32_t* __restrict__ tok, const int32_t* __restrict__ ctrl,
+                                const unsigned char* __restrict__ E, int V, int H, float* __restrict__ h,
+                                uint32_t* err) {
+  pdl_wait();
+  const int t = blockIdx.x;
+  int token = tok[ctrl[0] + t];
+  if (token < 0 || token >= V) {
+    if (threadIdx.x == 0) atomicOr(err, ERR_BAD_TOKEN);
+    token = 0;
+  }
+  const uint32_t* codes = reinterpret_cast<const uint32_t*>(E) + static_cast<size_t>(token) * (H / 8);
+  const __half* sc = reinterpret_cast<const __half*>(E + static_cast<size_t>(V) * H / 2) + static_cast<size_t>(token) * (H / 64);
+  const __half* bi = sc + static_cast<size_t>(V) * (H / 64);
+  for (int j = threadIdx.x; j < H; j += blockDim.x) {
+    const uint32_t q = (codes[j >> 3] >> (4 * (j & 7))) & 0xFu;
+    h[static_cast<size_t>(t) * H + j] =
+        __fadd_rn(__fmul_rn(__half2float(sc[j >> 6]), static_cast<float>(q)), __half2float(bi[j >> 6]));
+  }
+}
+
+// Greedy token of each of the ntok logit rows (lowest ID on ties): CTA (b, t)
+// reduces a slice of row t to one candidate; the last CTA to finish reduces the
+// candidates, writes next[t], the token after the last row into the token
+// stream, and advances the position by ntok.
+constexpr int kQ4ArgmaxThreads = 256;
+__global__ void __launch_bounds__(kQ4ArgmaxThreads) q4_argmax_kernel(const float* __restrict__ logits, int V, int ntok,
+                                                                     float* part_val, int32_t* part_idx,
+                                                                     uint32_t* counter, int32_t* tok, int32_t* ctrl,
+                                                                     int32_t* next, uint32_t* err) {
+  __shared__ float sv[kQ4ArgmaxThreads / 32];
+  __shared__ int si[kQ4ArgmaxThreads / 32];
+  __shared__ int s_last;
+  pdl_wait();
+  const int P = gridDim.x, b = blockIdx.x, t = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  auto block_best = [&](float& bv, int& bi) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (argmax_better(ov, oi, bv, bi)) {
+        bv = ov;
+        bi = oi;
+      }
+    }
+    __syncthreads();
+    if (lane == 0) {
+      sv[warp] = bv;
+      si[warp] = bi;
+    }
+    __syncthreads();
+    bv = sv[0];
+    bi = si[0];
+    for (int w = 1; w < kQ4ArgmaxThreads / 32; ++w)
+      if (argmax_better(sv[w], si[w], bv, bi)) {
+        bv = sv[w];
+        bi = si[w];
+      }
+  };
+  const float* row = logits + static_cast<size_t>(t) * V;
+  const int i0 = static_cast<int>(static_cast<long long>(b) * V / P), i1 = static_cast<int>(static_cast<long long>(b + 1) * V / P);
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = i0 + tid; i < i1; i += kQ4ArgmaxThreads) {
+    const float v = __ldcg(row + i);
+    if (argmax_better(v, i, bv, bi)) {
+      bv = v;
+      bi = i;
+    }
+  }
+  block_best(bv, bi);
+  if (tid == 0) {
+    part_val[t * P + b] = bv;
+    part_idx[t * P + b] = bi;
+    __threadfence();
+    s_last = atomicAdd(counter, 1u) == static_cast<uint32_t>(P * ntok - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int pos = ctrl[0];
+  int last = 0;
+  for (int tt = 0; tt < ntok; ++tt) {
+    float gv = -INFINITY;
+    int gi = 0x7fffffff;
+    for (int k = tid; k < P; k += kQ4ArgmaxThreads) {
+      const float v = __ldcg(part_val + tt * P + k);
+      const int i = __ldcg(part_idx + tt * P + k);
+      if (argmax_better(v, i, gv, gi)) {
+        gv = v;
+        gi = i;
+      }
+    }
+    block_best(gv, gi);
+    if (gi == 0x7fffffff) {  // every logit of the row was NaN
+      gi = 0;
+      if (tid == 0) atomicOr(err, ERR_ARGMAX_NAN);
+    }
+    if (tid == 0) next[tt] = gi;
+    last = gi;
+  }
+  if (tid == 0) {
+    tok[pos + ntok] = last;
+    ctrl[0] = pos + ntok;
+    *counter = 0u;
+    __threadfence();
+  }
+}
+
+dec_status enqueue_step_q4(dec_ctx* c, cudaStream_t st, bool full, int ntok) {
+  const dec_config& g = c->cfg;
+  const int H = g.hidden, I = g.inter, d = g.head_dim;
+  const int qw = g.n_q * d, kvw = g.n_kv * d, qkvw = qw + 2 * kvw;
+  const int group = g.n_q / g.n_kv;
+  float* h = c->at<float>(c->L.h);
+  float* qkv = c->at<float>(c->L.qkv);
+  float* attn = c->at<float>(c->L.attn);
+  float* gu = c->at<float>(c->L.q4gu);
+  uint32_t* err = c->at<uint32_t>(c->L.err);
+  auto base = [&](int xm, int epi, const void* x, int x_ld, const float* gain, float* y, int ldy, int in) {
+    Q4Launch q = {};
+    q.xm = xm;
+    q.epi = epi;
+    q.ntok = ntok;
+    q.x = x;
+    q.x_ld = x_ld;
+    q.norm_g = gain;
+    q.eps = g.eps;
+    q.y = y;
+    q.ldy = ldy;
+    q.in = in;
+    q.pdl = true;
+    q.err = err;
+    return q;
+  };
+  WSG_CUDA_TRY(&c->err, launch_k(q4_embed_kernel, dim3(ntok), dim3(256), 0, st, false, c->at<int32_t>(c->L.tok),
+                                 c->at<int32_t>(c->L.ctrl), static_cast<const unsigned char*>(c->w.embed), g.vocab, H,
+                                 h, err));
+  dec_status s;
+  for (int l = 0; l < g.layers; ++l) {
+    const dec_layer_weights& lw = c->layers[l];
+    {
+      Q4Launch q = base(Q4X_NORM, Q4E_STORE, h, H, lw.g_in, qkv, qkvw, H);
+      q.seg[0] = q4_seg(lw.w_q, qw, H, 0);
+      q.seg[1] = q4_seg(lw.w_k, kvw, H, qw);
+      q.seg[2] = q4_seg(lw.w_v, kvw, H, qw + kvw);
+      q.nseg = 3;
+      if ((s = launch_q4_fused(q, st, &c->err)) != DEC_OK) return s;
+    }
+    for (int t = 0; t < ntok; ++t) {
+      AttnArgs a = {};
+      a.qkv = qkv + static_cast<size_t>(t) * qkvw;
+      a.g_q = lw.g_q;
+      a.g_k = lw.g_k;
+      a.eps = g.eps;
+      a.rope_cos = c->at<float>(c->L.rope_cos);
+      a.rope_sin = c->at<float>(c->L.rope_sin);
+      a.ctrl = c->at<int32_t>(c->L.ctrl);
+      a.pos_add = t;
+      const size_t off = static_cast<size_t>(l) * c->kv_layer_elems() * dtype_bytes(g.kvdtype);
+      a.kc = c->ws + c->L.kc + off;
+      a.vc = c->ws + c->L.vc + off;
+      a.max_seq = g.max_seq;
+      a.n_q = g.n_q;
+      a.n_kv = g.n_kv;
+      a.d = d;
+      a.out = attn + static_cast<size_t>(t) * qw;
+      a.part = c->at<float>(c->L.apart);
+      a.counter = c->at<uint32_t>(c->L.acnt);
+      a.nsplit_max = c->nsplit_max;
+      a.tmin = 64;
+      a.scale = 1.0f / sqrtf(static_cast<float>(d));
+      a.err = err;
+      cudaError_t e;
+      if (g.kvdtype == DEC_F32) {
+        auto k = (group <= 2) ? attn_decode_kernel<float, 2> : attn_decode_kernel<float, 8>;
+        e = launch_k(k, dim3(g.n_kv, c->nsplit_max), dim3(kAttnWarps * 32), c->attn_smem, st, true, a);
+      } else {
+        auto k = (group <= 2) ? attn_decode_kernel<uint16_t, 2> : attn_decode_kernel<uint16_t, 8>;
+        e = launch_k(k, dim3(g.n_kv, c->nsplit_max), dim3(kAttnWarps * 32), c->attn_smem, st, true, a);
+      }
+      WSG_CUDA_TRY(&c->err, e);
+    }
+    {
+      Q4Launch q = base(Q4X_F32, Q4E_ADD, attn, qw, nullptr, h, H, qw);
+      q.seg[0] = q4_seg(lw.w_o, H, qw, 0);
+      q.nseg = 1;
+      if ((s = launch_q4_fused(q, st, &c->err)) != DEC_OK) return s;
+    }
+    {
+      Q4Launch q = base(Q4X_NORM, Q4E_STORE, h, H, lw.g_post, gu, 2 * I, H);
+      q.seg[0] = q4_seg(lw.w_gate, I, H, 0);
+      q.seg[1] = q4_seg(lw.w_up, I, H, I);
+      q.nseg = 2;
+      if ((s = launch_q4_fused(q, st, &c->err)) != DEC_OK) return s;
+    }
+    {
+      Q4Launch q = base(Q4X_SWIGLU, Q4E_ADD, gu, 2 * I, nullptr, h, H, I);
+      q.seg[0] = q4_seg(lw.w_down, H, I, 0);
+      q.nseg = 1;
+      if ((s = launch_q4_fused(q, st, &c->err)) != DEC_OK) return s;
+    }
+  }
+  if (!full) {
+    WSG_CUDA_TRY(&c->err, launch_k(advance_kernel, dim3(1), dim3(32), 0, st, true, c->at<int32_t>(c->L.ctrl)));
+    return DEC_OK;
+  }
+  {
+    Q4Launch q = base(Q4X_NORM, Q4E_STORE, h, H, c->w.g_final, c->at<float>(c->L.logits), g.vocab, H);
+    q.seg[0] = q4_seg(c->w.embed, g.vocab, H, 0);
+    q.nseg = 1;
+    if ((s = launch_q4_fused(q, st, &c->err)) != DEC_OK) return s;
+  }
+  const int P = std::min(c->di.sms, kArgmaxPartsMax / 2);
+  WSG_CUDA_TRY(&c->err, launch_k(q4_argmax_kernel, dim3(P, ntok), dim3(kQ4ArgmaxThreads), 0, st, true,
+                                 static_cast<const float*>(c->at<float>(c->L.logits)), g.vocab, ntok,
+                                 c->at<float>(c->L.mval), c->at<int32_t>(c->L.midx), c->at<uint32_t>(c->L.mcnt),
+                                 c->at<int32_t>(c->L.tok), c->at<int32_t>(c->L.ctrl), c->at<int32_t>(c->L.q4next),
+                                 err));
+  return DEC_OK;
+}
 
 // ---- chunked prefill ----
 
@@ -757,10 +1022,11 @@ dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, boo
   return DEC_OK;
 }
 
-dec_status capture(dec_ctx* c, bool full, cudaGraphExec_t* out) {
+dec_status capture(dec_ctx* c, bool full, cudaGraphExec_t* out, int ntok = 1) {
   WSG_CUDA_TRY(&c->err, cudaStreamBeginCapture(c->cap, cudaStreamCaptureModeThreadLocal));
-  dec_status s = c->cfg.wdtype == DEC_F32 ? enqueue_step_t<float>(c, c->cap, full)
-                                          : enqueue_step_t<uint16_t>(c, c->cap, full);
+  dec_status s = c->cfg.wdtype == DEC_Q4G64 ? enqueue_step_q4(c, c->cap, full, ntok)
+                 : c->cfg.wdtype == DEC_F32 ? enqueue_step_t<float>(c, c->cap, full)
+                                            : enqueue_step_t<uint16_t>(c, c->cap, full);
   cudaGraph_t graph = nullptr;
   cudaError_t e = cudaStreamEndCapture(c->cap, &graph);
   if (s != DEC_OK) {
@@ -847,7 +1113,7 @@ extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_
   };
   cudaError_t e = cudaStreamCreateWithFlags(&c->cap, cudaStreamNonBlocking);
   if (e == cudaSuccess) e = cudaMallocHost(&c->h_tok, sizeof(int32_t) * (cfg->max_seq + 1));
-  if (e == cudaSuccess) e = cudaHostAlloc(&c->h_next, sizeof(int32_t), cudaHostAllocMapped);
+  if (e == cudaSuccess) e = cudaHostAlloc(&c->h_next, 2 * sizeof(int32_t), cudaHostAllocMapped);
   if (e == cudaSuccess) e = cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->d_h_next), c->h_next, 0);
   if (e != cudaSuccess) return bail(fail(nullptr, DEC_ECUDA, "dec_create: %s", cudaGetErrorString(e)));
 
@@ -983,7 +1249,8 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
   // Graphs bake in the weight pointers: drop any captured with older ones.
   if (c->g_full) cudaGraphExecDestroy(c->g_full);
   if (c->g_body) cudaGraphExecDestroy(c->g_body);
-  c->g_full = c->g_body = nullptr;
+  if (c->g_verify) cudaGraphExecDestroy(c->g_verify);
+  c->g_full = c->g_body = c->g_verify = nullptr;
   c->have_weights = true;
   return DEC_OK;
 }
@@ -1096,6 +1363,35 @@ extern "C" dec_status dec_prefill_chunk(dec_ctx* c, const int32_t* h_tokens, int
   return DEC_OK;
 }
 
+extern "C" dec_status dec_verify2(dec_ctx* c, const int32_t* h_tokens, float* d_logits, int32_t* h_next) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_verify2: NULL context");
+  if (!h_tokens) return fail(&c->err, DEC_EINVAL, "dec_verify2: NULL tokens");
+  if (c->cfg.wdtype != DEC_Q4G64) return fail(&c->err, DEC_EINVAL, "dec_verify2: needs the 4-bit configuration");
+  if (!c->have_weights) return fail(&c->err, DEC_ESTATE, "dec_verify2: weights not loaded");
+  if (c->pos + 2 > c->cfg.max_seq)
+    return fail(&c->err, DEC_ECAPACITY, "dec_verify2: positions %d, %d exceed max_seq %d", c->pos, c->pos + 1,
+                c->cfg.max_seq);
+  if (!c->g_verify) {
+    const dec_status s = capture(c, true, &c->g_verify, 2);
+    if (s != DEC_OK) return s;
+  }
+  dec_status s = put_tokens(c, h_tokens, 2);
+  if (s != DEC_OK) return s;
+  WSG_CUDA_TRY(&c->err, cudaGraphLaunch(c->g_verify, c->stream));
+  c->pos += 2;
+  if (d_logits)
+    WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(d_logits, c->at<float>(c->L.logits), 2 * sizeof(float) * c->cfg.vocab,
+                                          cudaMemcpyDeviceToDevice, c->stream));
+  if (h_next) {
+    WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->h_next, c->at<int32_t>(c->L.q4next), 2 * sizeof(int32_t),
+                                          cudaMemcpyDeviceToHost, c->stream));
+    WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
+    h_next[0] = c->h_next[0];
+    h_next[1] = c->h_next[1];
+  }
+  return DEC_OK;
+}
+
 extern "C" dec_status dec_generate(dec_ctx* c, int32_t token, int32_t n, int32_t* d_tokens_out) {
   if (!c) return fail(nullptr, DEC_EINVAL, "dec_generate: NULL context");
   if (n < 1 || !d_tokens_out) return fail(&c->err, DEC_EINVAL, "dec_generate: need n >= 1 and an output buffer");
@@ -1157,6 +1453,7 @@ extern "C" void dec_destroy(dec_ctx* c) {
   if (!c) return;
   if (c->stream || c->cap) cudaStreamSynchronize(c->stream);
   if (c->g_full) cudaGraphExecDestroy(c->g_full);
+  if (c->g_verify) cudaGraphExecDestroy(c->g_verify);
   if (c->g_body) cudaGraphExecDestroy(c->g_body);
   if (c->cap) cudaStreamDestroy(c->cap);
   if (c->h_tok) cudaFreeHost(c->h_tok);

@@ -275,32 +275,50 @@ dec_status launch_q4_r(const uint32_t* codes, const uint16_t* s, const uint16_t*
   return DEC_OK;
 }
 
-// Bulk-copy 4-bit GEMV (gemv_q4.cuh): one CTA per SM (fewer when out is
-// smaller), a ring of as many stages of 16 R rows as the CTA needs and shared
-// memory holds. Needs in % 512 == 0 (every row range's scales are then a
-// multiple of 16 bytes) and 16-byte aligned scales, biases and x; *used is
-// false when the shape does not fit, so the caller takes the per-warp kernel.
-template <int R, int NTOK>
-dec_status launch_q4_bulk_r(const uint32_t* codes, const uint16_t* s, const uint16_t* b, const uint16_t* x, float* y,
-                            int out, int in, cudaStream_t st, const DeviceInfo& di, bool* used) {
+// Bulk-copy 4-bit GEMV (gemv_q4.cuh): one CTA per SM (two when the rows
+// give each more than four stages), split between the segments in proportion
+// to their rows; a ring of as many stages of 8 R rows as the CTA needs and
+// shared memory holds. Needs in % 512 == 0 (every row range's scales are then
+// a multiple of 16 bytes) and 16-byte aligned codes, scales, biases and x;
+// *used is false when the shape does not fit.
+template <int R, int NTOK, int XM, int EPI>
+dec_status launch_q4_bulk_r(const Q4Launch& q, cudaStream_t st, const DeviceInfo& di, std::string* err, bool* used) {
   *used = false;
-  auto kern = gemv_q4_bulk_kernel<R, NTOK>;
+  auto kern = gemv_q4_bulk_kernel<R, NTOK, XM, EPI>;
   static size_t static_smem[64] = {};
   static bool lifted[64] = {};
   if (!lifted[di.device]) {
     cudaFuncAttributes fa{};
-    WSG_CUDA_TRY(nullptr, cudaFuncGetAttributes(&fa, kern));
-    WSG_CUDA_TRY(nullptr, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(di.smem_optin - fa.sharedSizeBytes)));
+    WSG_CUDA_TRY(err, cudaFuncGetAttributes(&fa, kern));
+    WSG_CUDA_TRY(err, cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(di.smem_optin - fa.sharedSizeBytes)));
     static_smem[di.device] = fa.sharedSizeBytes;
     lifted[di.device] = true;
   }
   constexpr int RC = kQ4Warps * R;
+  long long total = 0;
+  for (int k = 0; k < q.nseg; ++k) total += q.seg[k].rows;
   // One CTA per SM while each has at most 4 stages of rows (small matrices:
   // the next launch's CTAs then fit beside them), else two per SM.
-  int G = out < di.sms ? out : di.sms;
-  if (static_cast<long long>(out) > 4ll * RC * di.sms) G = 2 * di.sms;
-  const long long rows_max = (static_cast<long long>(out) + G - 1) / G;
+  long long G = total < di.sms ? total : di.sms;
+  if (total > 4ll * RC * di.sms) G = 2ll * di.sms;
+  if (G < q.nseg) G = q.nseg;
+  Q4Args a = {};
+  a.nseg = q.nseg;
+  long long rows_max = 0, c0 = 0;
+  for (int k = 0; k < q.nseg; ++k) {
+    a.seg[k] = q.seg[k];
+    a.seg[k].cta0 = static_cast<int32_t>(c0);
+    // CTAs of segment k: its share of G, at least one, leaving one for each later segment
+    long long ck = k + 1 == q.nseg ? G - c0 : (G * q.seg[k].rows + total / 2) / total;
+    if (ck < 1) ck = 1;
+    if (k + 1 < q.nseg && ck > G - c0 - (q.nseg - 1 - k)) ck = G - c0 - (q.nseg - 1 - k);
+    if (ck > q.seg[k].rows && q.seg[k].rows > 0) ck = q.seg[k].rows;
+    const long long rk = (q.seg[k].rows + ck - 1) / ck;
+    if (rk > rows_max) rows_max = rk;
+    c0 += ck;
+  }
+  const int in = q.in;
   const long long nst = (rows_max + RC - 1) / RC;
   const long long srows = rows_max < RC ? rows_max : RC;  // rows a stage holds
   const long long stage = (srows * (in / 2 + in / 16) + 127) / 128 * 128;
@@ -312,22 +330,37 @@ dec_status launch_q4_bulk_r(const uint32_t* codes, const uint16_t* s, const uint
   if (S > kQ4MaxStages) S = kQ4MaxStages;
   if (S > nst) S = nst;
   if (S < 1) return DEC_OK;
-  Q4Args a;
-  a.codes = codes;
-  a.scale = s;
-  a.bias = b;
-  a.x = x;
-  a.y = y;
-  a.out = out;
+  a.x = q.x;
+  a.x_ld = q.x_ld;
+  a.norm_g = q.norm_g;
+  a.eps = q.eps;
+  a.y = q.y;
+  a.ldy = q.ldy;
   a.in = in;
   a.nstages = static_cast<int>(S);
   a.srows = static_cast<int>(srows);
   a.stage_bytes = static_cast<uint32_t>(stage);
-  a.err = gemv_err_ptr(di.device);
-  if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv_q4: device error word unavailable");
+  a.err = q.err;
   const size_t smem = static_cast<size_t>(S * stage + xbytes + 2 * S * 8);
-  WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(G), dim3(kQ4Threads), smem, st, true, a));
+  WSG_CUDA_TRY(err, launch_k(kern, dim3(static_cast<unsigned>(c0)), dim3(kQ4Threads), smem, st, q.pdl, a));
   *used = true;
+  return DEC_OK;
+}
+
+template <int NTOK, int XM, int EPI>
+dec_status launch_q4_bulk_x(int R, const Q4Launch& q, cudaStream_t st, const DeviceInfo& di, std::string* err,
+                            bool* used) {
+  // a smaller R when a stage of the requested one does not fit
+  for (int r = R; r >= 1 && !*used; r >>= 1) {
+    dec_status e = DEC_OK;
+    switch (r) {
+      case 1: e = launch_q4_bulk_r<1, NTOK, XM, EPI>(q, st, di, err, used); break;
+      case 2: e = launch_q4_bulk_r<2, NTOK, XM, EPI>(q, st, di, err, used); break;
+      case 4: e = launch_q4_bulk_r<4, NTOK, XM, EPI>(q, st, di, err, used); break;
+      default: e = launch_q4_bulk_r<8, NTOK, XM, EPI>(q, st, di, err, used); break;
+    }
+    if (e != DEC_OK) return e;
+  }
   return DEC_OK;
 }
 
@@ -336,18 +369,19 @@ dec_status launch_q4_bulk(int R, const uint32_t* codes, const uint16_t* s, const
                           float* y, int out, int in, cudaStream_t st, const DeviceInfo& di, bool* used) {
   *used = false;
   if (in % 512 || in > 16384 || !aligned16(s) || !aligned16(b) || !aligned16(x)) return DEC_OK;
-  // a smaller R when a stage of the requested one does not fit
-  for (int r = R; r >= 1 && !*used; r >>= 1) {
-    dec_status e = DEC_OK;
-    switch (r) {
-      case 1: e = launch_q4_bulk_r<1, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
-      case 2: e = launch_q4_bulk_r<2, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
-      case 4: e = launch_q4_bulk_r<4, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
-      default: e = launch_q4_bulk_r<8, NTOK>(codes, s, b, x, y, out, in, st, di, used); break;
-    }
-    if (e != DEC_OK) return e;
-  }
-  return DEC_OK;
+  Q4Launch q = {};
+  q.seg[0] = {codes, s, b, out, 0, 0};
+  q.nseg = 1;
+  q.x = x;
+  q.x_ld = in;
+  q.y = y;
+  q.ldy = out;
+  q.in = in;
+  q.ntok = NTOK;
+  q.pdl = true;
+  q.err = gemv_err_ptr(di.device);
+  if (!q.err) return fail(nullptr, DEC_ECUDA, "gemv_q4: device error word unavailable");
+  return launch_q4_bulk_x<NTOK, Q4X_BF16, Q4E_STORE>(R, q, st, di, nullptr, used);
 }
 
 template <int NTOK>
@@ -650,6 +684,38 @@ extern "C" int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r) {
   if (r == -1) g_q4_rows[ntok] = 0;
   return g_q4_rows[ntok];
 }
+
+namespace wsg {
+
+dec_status launch_q4_fused(const Q4Launch& q, cudaStream_t st, std::string* err) {
+  DeviceInfo di;
+  const dec_status ds = device_info(&di, err);
+  if (ds != DEC_OK) return ds;
+  if (q.in % 512 || q.in > 16384 || q.nseg < 1 || q.nseg > kQ4MaxSegs || (q.ntok != 1 && q.ntok != 2))
+    return fail(err, DEC_EINVAL, "4-bit projection: in=%d (a multiple of 512 up to 16384), %d segments, %d tokens",
+                q.in, q.nseg, q.ntok);
+  long long total = 0;
+  for (int k = 0; k < q.nseg; ++k) total += q.seg[k].rows;
+  // one row per warp when a CTA has at most one warp's worth of rows, else four
+  const int R = total <= 8ll * di.sms ? 1 : 4;
+  bool used = false;
+  dec_status e;
+  const int key = (q.xm * 2 + q.epi) * 2 + (q.ntok - 1);
+  switch (key) {
+    case (Q4X_NORM * 2 + Q4E_STORE) * 2 + 0: e = launch_q4_bulk_x<1, Q4X_NORM, Q4E_STORE>(R, q, st, di, err, &used); break;
+    case (Q4X_NORM * 2 + Q4E_STORE) * 2 + 1: e = launch_q4_bulk_x<2, Q4X_NORM, Q4E_STORE>(R, q, st, di, err, &used); break;
+    case (Q4X_F32 * 2 + Q4E_ADD) * 2 + 0: e = launch_q4_bulk_x<1, Q4X_F32, Q4E_ADD>(R, q, st, di, err, &used); break;
+    case (Q4X_F32 * 2 + Q4E_ADD) * 2 + 1: e = launch_q4_bulk_x<2, Q4X_F32, Q4E_ADD>(R, q, st, di, err, &used); break;
+    case (Q4X_SWIGLU * 2 + Q4E_ADD) * 2 + 0: e = launch_q4_bulk_x<1, Q4X_SWIGLU, Q4E_ADD>(R, q, st, di, err, &used); break;
+    case (Q4X_SWIGLU * 2 + Q4E_ADD) * 2 + 1: e = launch_q4_bulk_x<2, Q4X_SWIGLU, Q4E_ADD>(R, q, st, di, err, &used); break;
+    default: return fail(err, DEC_EINVAL, "4-bit projection: prologue %d with epilogue %d is not built", q.xm, q.epi);
+  }
+  if (e != DEC_OK) return e;
+  if (!used) return fail(err, DEC_EINVAL, "4-bit projection: in=%d does not fit in shared memory", q.in);
+  return DEC_OK;
+}
+
+}  // namespace wsg
 
 extern "C" dec_status gemv_device_errors(int32_t clear, uint32_t* bits) {
   if (!bits) return fail(nullptr, DEC_EINVAL, "gemv_device_errors: NULL output");

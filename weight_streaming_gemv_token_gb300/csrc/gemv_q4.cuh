@@ -32,6 +32,14 @@
 //    each row's sum, which one lane stores. No cross-warp sums: results are
 //    bit-reproducible.
 //
+//  * The rows may come from up to three matrices (segments; the 4-bit decoder
+//    runs Q/K/V, and gate/up, as one launch): each segment gets its own run of
+//    CTAs, in proportion to its rows, and writes its own range of y.
+//  * x prologues (XM): bfloat16 x read as is; float32 x rounded to bfloat16;
+//    x = bf16(RMSNorm(h) * g) from a float32 residual row h; x =
+//    bf16(silu(gate) * up) from float32 gate/up rows. Epilogues: y = W x or
+//    y += W x (residual add).
+//
 // Every mbarrier wait is bounded; on a timeout the CTA raises an abort flag,
 // the producer waits (bounded) for its copies in flight, and the error word
 // records the cause.
@@ -39,8 +47,11 @@
 #include <cuda_fp16.h>
 
 #include <cstdint>
+#include <string>
 
-#include "megakernel.cuh"  // reduce_scatter
+#include "common.h"
+#include "gemv_stream.cuh"  // silu_f32
+#include "megakernel.cuh"   // reduce_scatter
 #include "ptx.cuh"
 
 namespace wsg {
@@ -48,19 +59,64 @@ namespace wsg {
 constexpr int kQ4Warps = 8;                     // consumer warps
 constexpr int kQ4Threads = kQ4Warps * 32 + 32;  // plus a producer warp
 constexpr int kQ4MaxStages = 16;
+constexpr int kQ4MaxSegs = 3;
+
+enum Q4X : int {
+  Q4X_BF16 = 0,    // x bf16 [ntok][x_ld]
+  Q4X_F32 = 1,     // x f32 [ntok][x_ld], rounded to bfloat16
+  Q4X_NORM = 2,    // x = bf16(h * rsqrt(mean(h^2) + eps) * g), h f32 [ntok][x_ld]
+  Q4X_SWIGLU = 3,  // x = bf16(silu(gu[j]) * gu[in + j]), gu f32 [ntok][x_ld]
+};
+
+enum Q4Epi : int {
+  Q4E_STORE = 0,  // y = W x
+  Q4E_ADD = 1,    // y += W x
+};
+
+struct Q4Seg {
+  const uint32_t* codes;  // [rows][in/8]
+  const uint16_t* scale;  // fp16 [rows][in/64]
+  const uint16_t* bias;   // fp16 [rows][in/64]
+  int32_t rows;
+  int32_t y_off;          // first row of y this segment writes
+  int32_t cta0;           // first CTA of this segment (segment 0: 0)
+};
 
 struct Q4Args {
-  const uint32_t* codes;  // [out][in/8]
-  const uint16_t* scale;  // fp16 [out][in/64]
-  const uint16_t* bias;   // fp16 [out][in/64]
-  const uint16_t* x;      // bf16 [ntok][in]
-  float* y;               // [ntok][out]
-  int32_t out, in;
+  Q4Seg seg[kQ4MaxSegs];
+  int32_t nseg;
+  const void* x;          // per the x prologue; row t starts at x + t * x_ld elements
+  int32_t x_ld;
+  const float* norm_g;    // Q4X_NORM: gain [in]
+  float eps;
+  float* y;               // y[t * ldy + y_off + row]
+  int32_t ldy, in;
   int32_t nstages;        // ring depth
   int32_t srows;          // row capacity of a stage: min(RC, most rows of a CTA)
   uint32_t stage_bytes;   // one stage: srows rows of codes, then of scales, then of biases (multiple of 128)
   uint32_t* err;
 };
+
+// Host description of one bulk 4-bit launch (gemv.cu builds the Q4Args).
+struct Q4Launch {
+  Q4Seg seg[kQ4MaxSegs];  // rows, y_off and pointers; cta0 is chosen by the launcher
+  int32_t nseg;
+  int32_t xm, epi, ntok;  // Q4X_*, Q4E_*, 1 or 2
+  const void* x;
+  int32_t x_ld;
+  const float* norm_g;
+  float eps;
+  float* y;
+  int32_t ldy, in;
+  bool pdl;
+  uint32_t* err;
+};
+
+// A 4-bit projection of the decoder (prologue / epilogue pairs NORM+STORE,
+// F32+ADD, SWIGLU+ADD). DEC_EINVAL when the shape does not fit the bulk kernel.
+dec_status launch_q4_fused(const Q4Launch& q, cudaStream_t st, std::string* err);
+
+__device__ __forceinline__ float q4_round_bf16(float f) { return bf16_to_f32(f32_to_bf16_rn(f)); }
 
 __device__ __forceinline__ void q4_consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kQ4Warps * 32) : "memory");
@@ -84,13 +140,14 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
 // columns, high and low bytes of the odd columns; word m of a plane holds
 // columns 32c + 8m + (0, 2, 4, 6) or + (1, 3, 5, 7))[xu: NTOK][nch] float2
 // (u / 16, X)][full: nstages][empty: nstages] mbarriers.
-template <int R, int NTOK>
+template <int R, int NTOK, int XM = Q4X_BF16, int EPI = Q4E_STORE>
 __global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Args a) {
   constexpr int RC = kQ4Warps * R;
   constexpr int NV = R * NTOK;  // row sums per lane before the reduction
   constexpr int kLogNV = NV == 1 ? 0 : NV == 2 ? 1 : NV == 4 ? 2 : NV == 8 ? 3 : 4;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_abort;
+  __shared__ float s_rs[kQ4Warps * NTOK];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int in = a.in, nch = in >> 5;
   const uint32_t cb = static_cast<uint32_t>(in) >> 1;   // code bytes per row
@@ -102,9 +159,14 @@ __global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Arg
   uint64_t* full = reinterpret_cast<uint64_t*>(xu + NTOK * nch);
   uint64_t* empty = full + S;
   volatile int* vabort = &s_abort;
-  const int c = blockIdx.x, G = gridDim.x;
-  const int r0 = static_cast<int>(static_cast<long long>(c) * a.out / G);
-  const int n = static_cast<int>(static_cast<long long>(c + 1) * a.out / G) - r0;
+  // this CTA's segment, and its rows [r0, r0 + n) of that segment
+  int k = 0;
+  while (k + 1 < a.nseg && static_cast<int>(blockIdx.x) >= a.seg[k + 1].cta0) ++k;
+  const Q4Seg sg = a.seg[k];
+  const int c = blockIdx.x - sg.cta0;
+  const int G = (k + 1 < a.nseg ? a.seg[k + 1].cta0 : static_cast<int>(gridDim.x)) - sg.cta0;
+  const int r0 = static_cast<int>(static_cast<long long>(c) * sg.rows / G);
+  const int n = static_cast<int>(static_cast<long long>(c + 1) * sg.rows / G) - r0;
   const int nst = (n + RC - 1) / RC;
   if (tid == 0) {
     s_abort = 0;
@@ -121,9 +183,9 @@ __global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Arg
   if (warp == kQ4Warps) {
     if (lane != 0) return;
     const uint64_t pol = l2_policy_evict_first();
-    const char* codes = reinterpret_cast<const char*>(a.codes);
-    const char* sc = reinterpret_cast<const char*>(a.scale);
-    const char* bi = reinterpret_cast<const char*>(a.bias);
+    const char* codes = reinterpret_cast<const char*>(sg.codes);
+    const char* sc = reinterpret_cast<const char*>(sg.scale);
+    const char* bi = reinterpret_cast<const char*>(sg.bias);
     int issued = 0;
     for (int st = 0; st < nst; ++st) {
       const int slot = st % S;
@@ -147,25 +209,88 @@ __global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Arg
   }
 
   // ---- consumers ----
-  // x (it may come from the previous kernel): per chunk and token, the fixed
-  // point step, the byte planes and the float sum. Four consecutive lanes per
-  // chunk, lane m taking the 8 columns of word m (one 16-byte load) and
-  // building that word of all four planes; the butterfly max and sum over the
-  // four lanes leave the same value in each.
+  // x may come from the previous kernel, and y may still be read by it.
+  pdl_wait();
+  const int ctid = tid;  // 0 .. kQ4Warps * 32 - 1
+  if (XM == Q4X_NORM) {
+    // 1 / RMS of each token's h, summed in a fixed order
+    const float* h = static_cast<const float*>(a.x);
+    for (int t = 0; t < NTOK; ++t) {
+      float ss = 0.f;
+      for (int i = 4 * ctid; i < in; i += 4 * kQ4Warps * 32) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(h + static_cast<size_t>(t) * a.x_ld + i));
+        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_rs[t * kQ4Warps + warp] = ss;
+    }
+    q4_consumer_sync();
+  }
+  float rs[NTOK];
+  if (XM == Q4X_NORM) {
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+      float ss = 0.f;
+      for (int w = 0; w < kQ4Warps; ++w) ss += s_rs[t * kQ4Warps + w];
+      rs[t] = rsqrtf(ss / static_cast<float>(in) + a.eps);
+    }
+  }
+  // x: per chunk and token, the fixed point step, the byte planes and the
+  // float sum. Four consecutive lanes per chunk, lane m taking the 8 columns
+  // of word m and building that word of all four planes; the butterfly max
+  // and sum over the four lanes leave the same value in each.
   {
     const int items = NTOK * nch * 4;
     for (int it0 = warp * 32; it0 < items; it0 += kQ4Warps * 32) {
       const int it = it0 + lane;
       const bool valid = it < items;
       const int t = valid ? it / (nch * 4) : 0, rem = it - t * nch * 4, ch = rem >> 2, m = rem & 3;
-      uint4 u = make_uint4(0, 0, 0, 0);
-      if (valid) u = __ldg(reinterpret_cast<const uint4*>(a.x + static_cast<size_t>(t) * in + 32 * ch + 8 * m));
-      const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+      const int col = 32 * ch + 8 * m;
       float xv[8];
+      if (XM == Q4X_BF16) {
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (valid)
+          u = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * a.x_ld +
+                                                    col));
+        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        xv[2 * k] = __uint_as_float(uw[k] << 16);             // column 8m + 2k
-        xv[2 * k + 1] = __uint_as_float(uw[k] & 0xFFFF0000u); // column 8m + 2k + 1
+        for (int k = 0; k < 4; ++k) {
+          xv[2 * k] = __uint_as_float(uw[k] << 16);              // column 8m + 2k
+          xv[2 * k + 1] = __uint_as_float(uw[k] & 0xFFFF0000u);  // column 8m + 2k + 1
+        }
+      } else {
+        const float* xr = static_cast<const float*>(a.x) + static_cast<size_t>(t) * a.x_ld + col;
+        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+        if (valid) {
+          v0 = __ldcg(reinterpret_cast<const float4*>(xr));
+          v1 = __ldcg(reinterpret_cast<const float4*>(xr + 4));
+        }
+        float f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        if (XM == Q4X_NORM) {
+          float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+          if (valid) {
+            g0 = __ldg(reinterpret_cast<const float4*>(a.norm_g + col));
+            g1 = __ldg(reinterpret_cast<const float4*>(a.norm_g + col + 4));
+          }
+          const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          float r = rs[0];
+#pragma unroll
+          for (int tt = 1; tt < NTOK; ++tt)
+            if (t == tt) r = rs[tt];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = (f[j] * r) * g[j];
+        } else if (XM == Q4X_SWIGLU) {
+          float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = u0;
+          if (valid) {
+            u0 = __ldcg(reinterpret_cast<const float4*>(xr + in));
+            u1 = __ldcg(reinterpret_cast<const float4*>(xr + in + 4));
+          }
+          const float up[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = silu_f32(f[j]) * up[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xv[j] = q4_round_bf16(f[j]);
       }
       float mx = 0.f, X = 0.f;
 #pragma unroll
@@ -271,8 +396,13 @@ __global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Arg
     const float v = reduce_scatter<NV>(acc, lane);
     const int vi = lane >> (5 - kLogNV), i = vi / NTOK, t = vi - i * NTOK;
     const int rr = warp + kQ4Warps * i;
-    if ((lane & ((32 >> kLogNV) - 1)) == 0 && rr < rows)
-      a.y[static_cast<size_t>(t) * a.out + r0 + st * RC + rr] = v;
+    if ((lane & ((32 >> kLogNV) - 1)) == 0 && rr < rows) {
+      float* yp = a.y + static_cast<size_t>(t) * a.ldy + sg.y_off + r0 + st * RC + rr;
+      if (EPI == Q4E_ADD)
+        *yp += v;
+      else
+        *yp = v;
+    }
   }
 }
 

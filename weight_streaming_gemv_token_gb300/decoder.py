@@ -15,6 +15,12 @@ from . import binding as B
 _LAYER_KEYS = ("w_q", "w_k", "w_v", "w_o", "w_gate", "w_up", "w_down", "g_in", "g_post", "g_q", "g_k")
 
 
+def q4_blob(m: dict, device="cuda") -> torch.Tensor:
+    """One device buffer holding a 4-bit matrix as the C ABI takes it: codes, then scales, then biases."""
+    parts = [np.ascontiguousarray(m[k]).view(np.uint8).reshape(-1) for k in ("packed", "scale", "bias")]
+    return torch.from_numpy(np.concatenate(parts)).to(device)
+
+
 def to_device(a, device="cuda") -> torch.Tensor:
     """numpy array -> device tensor; uint16 arrays are taken as bfloat16 bit patterns."""
     if isinstance(a, torch.Tensor):
@@ -41,8 +47,10 @@ class Decoder:
         self.shape = shape
         self.stream = stream if stream is not None else torch.cuda.current_stream()
         # device copies of the weights; kept alive as long as the context
-        self.dev = {"embed": to_device(weights["embed"]), "g_final": to_device(weights["g_final"]),
-                    "layers": [{k: to_device(lw[k]) for k in _LAYER_KEYS} for lw in weights["layers"]]}
+        up = q4_blob if wd == "q4" else to_device
+        self.dev = {"embed": up(weights["embed"]), "g_final": to_device(weights["g_final"]),
+                    "layers": [{k: (to_device if k.startswith("g_") else up)(lw[k]) for k in _LAYER_KEYS}
+                               for lw in weights["layers"]]}
         # Lossless storage ("Megakernels", "Lossless decode-weight storage"): float32 projections
         # and embedding whose values are all bfloat16 values are kept as their bfloat16 halves and
         # run on the bfloat16-weight kernels; any inexact tensor keeps the whole model in float32.
@@ -68,7 +76,7 @@ class Decoder:
         self.cfg = B.dec_config(
             layers=shape.layers, hidden=shape.hidden, inter=shape.inter, n_q=shape.n_q, n_kv=shape.n_kv,
             head_dim=shape.head_dim, vocab=shape.vocab, eps=shape.eps, rope_theta=shape.rope_theta,
-            wdtype=B.DEC_F32 if wd == "f32" else B.DEC_BF16,
+            wdtype={"f32": B.DEC_F32, "bf16": B.DEC_BF16, "q4": B.DEC_Q4G64}[wd],
             kvdtype=B.DEC_F32 if kv_dtype == "f32" else B.DEC_BF16,
             max_seq=max_seq, chunk_cap=chunk_cap,
             engine=B.DEC_ENGINE_PERSISTENT if engine == "persistent" else B.DEC_ENGINE_STAGED)
@@ -114,6 +122,10 @@ class Decoder:
         if skip_logits:
             return B.dec_step(self.ctx, int(token), B.DEC_SKIP_LOGITS, None, want_next=False)
         return B.dec_step(self.ctx, int(token), 0, logits, want_next=True)
+
+    def verify2(self, tokens, logits: torch.Tensor | None = None) -> tuple[int, int]:
+        """Two-token verify step (4-bit configuration): rows at p and p+1; the greedy token after each."""
+        return B.dec_verify2(self.ctx, tokens, logits)
 
     def prefill(self, tokens, is_last: bool = True, logits: torch.Tensor | None = None):
         return B.dec_prefill_chunk(self.ctx, tokens, is_last, logits if is_last else None, want_next=is_last)

@@ -50,6 +50,8 @@ class DecoderShape:
 
 # Tiny decoder with the Qwen3 structure (2 layers, hidden 64, ...).
 TINY = DecoderShape(layers=2, hidden=64, inter=192, n_q=4, n_kv=2, head_dim=16, vocab=512)
+# The smallest decoder the 4-bit configuration takes (widths multiples of 512).
+Q4_SMALL = DecoderShape(layers=2, hidden=512, inter=1024, n_q=4, n_kv=2, head_dim=128, vocab=1024)
 # Qwen3-0.6B geometry ("Megakernels", "What runs in the DSL").
 QWEN3_06B = DecoderShape(layers=28, hidden=1024, inter=3072, n_q=16, n_kv=8, head_dim=128, vocab=151936)
 
@@ -196,3 +198,39 @@ def q4_activations(inp: int, ntok: int, seed: int) -> np.ndarray:
     """x ~ N(0, 1) rounded to bf16, shape [ntok, in] as bf16 bits."""
     x = np.random.default_rng(seed).standard_normal((ntok, inp), dtype=np.float32)
     return f32_to_bf16_bits(x)
+
+
+def decoder_weights_q4(s: DecoderShape, seed: int = 1, group: int = 64) -> dict:
+    """Random 4-bit decoder: every projection and the tied embedding groupwise-affine.
+
+    Draw order from ``numpy.random.default_rng(seed)`` as in decoder_weights
+    (embed, each layer's LAYER_TENSORS, g_final). A matrix draws its codes
+    U{0..15}, then s ~ U(0.004, 0.008) and b = -7.5 s + 0.002 N(0, 1) per
+    64-column group (fp16), so w = s q + b is centred near zero with a spread
+    close to the 0.02 N(0, 1) float draws. Gains are 1 + 0.1 N(0, 1), float32.
+
+    Matrices are {"packed": uint32 [out, in/8], "scale", "bias": float16
+    [out, in/64]}. Returns {"embed", "g_final", "layers", "wdtype": "q4"}.
+    """
+    rng = np.random.default_rng(seed)
+    shapes = tensor_shapes(s)
+
+    def draw(name):
+        shp = shapes[name]
+        if name.startswith("g_"):
+            z = rng.standard_normal(int(np.prod(shp)), dtype=np.float32).reshape(shp)
+            return (np.float32(1.0) + np.float32(0.1) * z).astype(np.float32)
+        out, inp = shp
+        if inp % group:
+            raise ValueError("in must be a multiple of the group size")
+        codes = rng.integers(0, 16, size=(out, inp), dtype=np.uint8)
+        sc = rng.uniform(0.004, 0.008, size=(out, inp // group)).astype(np.float16)
+        bi = (-7.5 * sc.astype(np.float64) + 0.002 * rng.standard_normal((out, inp // group))).astype(np.float16)
+        return {"packed": pack_q4(codes), "scale": sc, "bias": bi}
+
+    out = {"embed": draw("embed"), "layers": []}
+    for _ in range(s.layers):
+        out["layers"].append({name: draw(name) for name in LAYER_TENSORS})
+    out["g_final"] = draw("g_final")
+    out["wdtype"] = "q4"
+    return out

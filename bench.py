@@ -15,7 +15,9 @@ Beside the headline line the JSON carries:
               shape) against the measured HBM copy bandwidth;
   gemv_cold   cold GB/s of gemv / gemv_q4 on the five layer shapes, each
               cycling >= 1 GiB of distinct matrices;
-  cpu_baseline the float64 oracle's decode rate on the host cores.
+  cpu_baseline the float64 oracle's decode rate on the host cores;
+  q4_decoder  the same decoder with 4-bit weights (staged engine): decode
+              rate against its own step roofline, and the two-token verify step.
 
 --impl reference times the oracle (the CPU restatement of the same forward)
 on a bounded sample of the same workload, on the host cores.
@@ -435,6 +437,72 @@ def prefill_config(W, torch, hbm, tflops_peak):
     }
 
 
+def q4_bytes_per_token(s, pos):
+    """Algorithmic bytes of one 4-bit forward at position pos: every 4-bit matrix once (codes
+    half a byte per weight, an fp16 scale and bias per 64 weights), the float32 K/V rows 0..pos
+    of every layer, the cache row written, the logits written."""
+    per_w = 0.5 + 4.0 / 64
+    per_layer = (s.q_width + 2 * s.kv_width) * s.hidden + s.hidden * s.q_width + 2 * s.inter * s.hidden + \
+        s.hidden * s.inter
+    weights = (s.layers * per_layer + s.vocab * s.hidden) * per_w
+    kv = s.layers * 2 * s.kv_width * 4 * (pos + 1)
+    return int(weights + kv + 4 * s.vocab)
+
+
+def q4_config(W, torch, stream, hbm, steps=256, verifies=64):
+    """Qwen3-0.6B shape in the 4-bit configuration (staged engine, CUDA graph per step): greedy
+    decode rate after a 32-token prompt, and the two-token verify step back to back."""
+    from weight_streaming_gemv_token_gb300 import binding as B
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.QWEN3_06B
+    w = Wl.decoder_weights_q4(s, seed=1)
+    prompt = Wl.prompt_uniform(PROMPT, s.vocab, seed=0)
+    dec = Decoder(s, w, kv_dtype="f32", max_seq=PROMPT + 8 + steps + 2 * (verifies + 4) + 8, stream=stream,
+                  engine="staged")
+    del w
+    first = dec.prefill(prompt, is_last=True)
+    out = torch.empty(steps + 4, dtype=torch.int32, device="cuda")
+    dec.generate(first, 4, out[:4])
+    torch.cuda.synchronize()
+    tok = int(out[3].item())
+    pos0 = dec.position
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    dec.generate(tok, steps, out[4:])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3
+    rate = steps / sec
+    bpt = q4_bytes_per_token(s, pos0 + steps // 2)
+    # verify steps back to back (no read-back), then one with the tokens read back
+    pair = [int(out[steps + 3].item()), int(out[steps + 2].item())]
+    for _ in range(3):
+        B.dec_verify2(dec.ctx, pair, None, want_next=False)
+    torch.cuda.synchronize()
+    vpos = dec.position
+    e0.record(stream)
+    for _ in range(verifies):
+        B.dec_verify2(dec.ctx, pair, None, want_next=False)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    vsec = e0.elapsed_time(e1) / 1e3 / verifies
+    vb = q4_bytes_per_token(s, vpos + verifies) + s.layers * 2 * s.kv_width * 4 * (vpos + verifies + 2) + 4 * s.vocab
+    assert dec.device_errors() == 0
+    dec.close()
+    return {
+        "workload": "Qwen3-0.6B-shaped decoder, 4-bit groupwise-affine weights (all projections and the tied head), "
+                    f"FP32 KV, staged engine, greedy decode after a {PROMPT}-token prompt",
+        "decode_tokens_per_s": round(rate, 1), "ms_per_step": round(sec / steps * 1e3, 4),
+        "bytes_per_token": bpt, "achieved_GB/s": round(bpt * rate / 1e9, 1), "peak": hbm,
+        "frac": round(bpt * rate / 1e9 / hbm, 4), "roofline_tokens_per_s": round(hbm * 1e9 / bpt, 1),
+        "gpu_launches_per_step": 5 * s.layers + 3,
+        "verify2": {"ms_per_call": round(vsec * 1e3, 4), "rows_per_s": round(2 / vsec, 1),
+                    "vs_two_steps": round(2 * sec / steps / vsec, 3), "bytes_per_call": vb,
+                    "frac": round(vb / vsec / 1e9 / hbm, 4)},
+    }
+
+
 def gpu_arm(args):
     import torch
 
@@ -550,6 +618,8 @@ def gpu_arm(args):
             extra["prefill"] = prefill_config(W, torch, hbm, measured_bf16_tflops())
         if not args.no_lossless:
             extra["lossless_storage"] = lossless_config(W, torch, stream, weights["embed"], hbm)
+        if not args.no_q4:
+            extra["q4_decoder"] = q4_config(W, torch, stream, hbm)
 
     if rank == 0:
         cpu = None if args.no_cpu else cpu_baseline_sample(weights, prompt, budget_s=args.cpu_seconds)
@@ -653,6 +723,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-prefill", action="store_true", help="skip the BF16 chunked-prefill configuration")
     ap.add_argument("--no-lossless", action="store_true", help="skip the lossless bfloat16 storage comparison")
+    ap.add_argument("--no-q4", action="store_true", help="skip the 4-bit decoder configuration")
     args = ap.parse_args()
     if args.impl == "reference":
         args.steps = args.steps if args.steps is not None else 5

@@ -25,8 +25,13 @@ def kv_to_np(t):
 ENGINES = ["persistent", "staged"]
 
 
+def rms_within(got, ref, rms_tol, what):
+    rms = float(np.sqrt(np.mean((np.asarray(got, np.float64) - ref) ** 2)))
+    assert rms <= rms_tol, f"{what}: rms difference {rms:.3e} above {rms_tol}"
+
+
 def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every=1, max_seq=None, engine="persistent",
-                    oracle_weights=None, act_round=None):
+                    oracle_weights=None, act_round=None, rms_tol=None):
     import torch
 
     W = lib()
@@ -50,6 +55,8 @@ def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every
         ref = ora.step(cur)
         got = logits.cpu().numpy()
         close(got, ref, tol, f"logits step {j}")
+        if rms_tol is not None:
+            rms_within(got, ref, rms_tol, f"logits step {j}")
         own, ok = O.argmax_lowest(got)
         assert ok and nxt == own, f"step {j}: GPU token {nxt} is not the argmax {own} of its own logits"
         srt = np.sort(ref)[::-1]

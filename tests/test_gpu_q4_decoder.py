@@ -13,7 +13,16 @@ import oracle as O
 import workloads as Wl
 
 from gpu_util import LOW_TOL, close, lib
-from test_gpu_decoder import kv_to_np, run_and_compare
+from test_gpu_decoder import kv_to_np, rms_within, run_and_compare
+
+# Full-size (28-layer) tolerance of the 4-bit configuration. Rounding each projection's input to
+# bfloat16 makes the logits depend on rounding decisions: the oracle against itself, with its
+# activations perturbed by 1e-7 .. 3e-5 (relative) before the rounding (the size of float32
+# arithmetic and of the kernel's 16-bit fixed-point x), moves the Qwen3-shape logits (scale ~0.9)
+# by up to 0.024 .. 0.034, rms 0.0034 .. 0.0044, whatever the perturbation. Elementwise 5e-2 and
+# an rms bound of 1e-2 keep a margin above that spread; a wrong kernel moves them far more.
+Q4_FULL_TOL = 5e-2
+Q4_FULL_RMS = 1e-2
 
 pytestmark = pytest.mark.gpu
 
@@ -38,7 +47,7 @@ def test_small_q4_every_logit_and_kv(small_q4, kv):
     run_and_compare(Wl.Q4_SMALL, w, prompt, 12, kv, LOW_TOL, engine="staged", oracle_weights=deq, act_round="bf16")
 
 
-def check_verify(shape, w, deq, prompt, drafts, kv="f32"):
+def check_verify(shape, w, deq, prompt, drafts, kv="f32", tol=LOW_TOL, rms_tol=None):
     """Prompt tokenwise, then verify steps of (current token, draft) pairs; every row's logits
     against the oracle's forward of the same rows, the cache after each, and the token rule."""
     import torch
@@ -61,18 +70,20 @@ def check_verify(shape, w, deq, prompt, drafts, kv="f32"):
         refs = [ora.step(cur), ora.step(int(draft))]
         got = logits.cpu().numpy()
         for r in range(2):
-            close(got[r], refs[r], LOW_TOL, f"verify {j} row {r}")
+            close(got[r], refs[r], tol, f"verify {j} row {r}")
+            if rms_tol is not None:
+                rms_within(got[r], refs[r], rms_tol, f"verify {j} row {r}")
             own, ok = O.argmax_lowest(got[r])
             assert ok and (n0, n1)[r] == own, f"verify {j} row {r}: token is not the argmax of its own logits"
             srt = np.sort(refs[r])[::-1]
-            if srt[0] - srt[1] > 2 * (LOW_TOL + LOW_TOL * abs(srt[0])):
+            if srt[0] - srt[1] > 2 * (tol + tol * abs(srt[0])):
                 assert (n0, n1)[r] == O.argmax_lowest(refs[r])[0]
         for l in range(shape.layers):
             K, V, n = dec.kv(l)
             assert n == ora.pos
             rk, rv = ora.kv(l)
-            close(kv_to_np(K[:, :n]), rk, LOW_TOL, f"K layer {l} verify {j}")
-            close(kv_to_np(V[:, :n]), rv, LOW_TOL, f"V layer {l} verify {j}")
+            close(kv_to_np(K[:, :n]), rk, tol, f"K layer {l} verify {j}")
+            close(kv_to_np(V[:, :n]), rv, tol, f"V layer {l} verify {j}")
         cur = n1
     assert dec.device_errors() == 0
     dec.close()
@@ -161,6 +172,7 @@ def test_qwen3_q4_generation_and_verify(qwen_q4):
     w, deq = qwen_q4
     s = Wl.QWEN3_06B
     prompt = Wl.prompt_uniform(4, s.vocab, seed=0)
-    run_and_compare(s, w, prompt, 3, "f32", LOW_TOL, check_kv_every=2, engine="staged", oracle_weights=deq,
-                    act_round="bf16")
-    check_verify(s, w, deq, Wl.prompt_uniform(3, s.vocab, seed=2), Wl.prompt_uniform(2, s.vocab, seed=4))
+    run_and_compare(s, w, prompt, 3, "f32", Q4_FULL_TOL, check_kv_every=2, engine="staged", oracle_weights=deq,
+                    act_round="bf16", rms_tol=Q4_FULL_RMS)
+    check_verify(s, w, deq, Wl.prompt_uniform(3, s.vocab, seed=2), Wl.prompt_uniform(2, s.vocab, seed=4),
+                 tol=Q4_FULL_TOL, rms_tol=Q4_FULL_RMS)

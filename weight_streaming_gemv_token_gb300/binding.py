@@ -155,13 +155,13 @@ def dec_step(ctx: int, token: int, flags: int = 0, d_logits=None, want_next: boo
     return nxt.value if want_next else None
 
 
-def dec_verify2(ctx: int, tokens, d_logits=None) -> tuple[int, int]:
+def dec_verify2(ctx: int, tokens, d_logits=None, want_next: bool = True) -> tuple[int, int] | None:
     if len(tokens) != 2:
         raise ValueError("dec_verify2 takes two tokens")
     arr = (c_int32 * 2)(int(tokens[0]), int(tokens[1]))
     nxt = (c_int32 * 2)(-1, -1)
-    _check(library().dec_verify2(ctx, arr, _ptr(d_logits), nxt), ctx)
-    return nxt[0], nxt[1]
+    _check(library().dec_verify2(ctx, arr, _ptr(d_logits), nxt if want_next else None), ctx)
+    return (nxt[0], nxt[1]) if want_next else None
 
 
 def dec_prefill_chunk(ctx: int, tokens, is_last: bool, d_logits=None, want_next: bool = True) -> int | None:

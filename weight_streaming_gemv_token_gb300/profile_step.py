@@ -8,7 +8,8 @@ Use under ncu with --profile-from-start off, e.g.
       python -m weight_streaming_gemv_token_gb300.profile_step gemv --out 6144 --in 1024 --count 8
 
 decode: Qwen3-0.6B-shaped decoder (optionally fewer layers / a smaller
-        vocabulary, for captures that must stay small) with seeded random
+        vocabulary, for captures that must stay small; --dtype q4 with
+        --engine staged for the 4-bit configuration) with seeded random
         weights, a uniform prompt, warm-up steps, then --steps decode steps
         inside the region.
 gemv:   --count distinct matrices of one shape (sized past L2 by default),
@@ -43,7 +44,7 @@ def decode(args):
         import dataclasses
 
         s = dataclasses.replace(s, layers=args.layers or s.layers, vocab=args.vocab or s.vocab)
-    w = Wl.decoder_weights(s, seed=1, wdtype=args.dtype)
+    w = Wl.decoder_weights_q4(s, seed=1) if args.dtype == "q4" else Wl.decoder_weights(s, seed=1, wdtype=args.dtype)
     prompt = Wl.prompt_uniform(args.prompt, s.vocab, seed=0)
     dec = Decoder(s, w, kv_dtype=args.kv, max_seq=args.prompt + args.warmup + args.steps + 4, engine=args.engine,
                   chunk_cap=args.chunk)
@@ -154,7 +155,7 @@ def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="mode", required=True)
     d = sub.add_parser("decode")
-    d.add_argument("--dtype", default="f32", choices=["f32", "bf16"])
+    d.add_argument("--dtype", default="f32", choices=["f32", "bf16", "q4"], help="q4: the 4-bit configuration (staged)")
     d.add_argument("--kv", default="f32", choices=["f32", "bf16"])
     d.add_argument("--prompt", type=int, default=32)
     d.add_argument("--warmup", type=int, default=3)

@@ -450,17 +450,24 @@ def q4_bytes_per_token(s, pos):
 
 
 def q4_config(W, torch, stream, hbm, steps=256, verifies=64):
-    """Qwen3-0.6B shape in the 4-bit configuration (staged engine, CUDA graph per step): greedy
-    decode rate after a 32-token prompt, and the two-token verify step back to back."""
+    """Qwen3-0.6B shape in the 4-bit configuration: greedy decode rate after a 32-token prompt on
+    the persistent engine (one cooperative launch for all steps) and on the staged engine (a CUDA
+    graph per step), and the two-token verify step back to back."""
+    w = Wl.decoder_weights_q4(Wl.QWEN3_06B, seed=1)
+    res = q4_engine(W, torch, stream, hbm, w, "staged", steps, verifies)
+    pers = q4_engine(W, torch, stream, hbm, w, "persistent", steps, verifies)
+    res["persistent_engine"] = {k: pers[k] for k in ("decode_tokens_per_s", "ms_per_step", "frac", "gpu_launches_per_step")}
+    return res
+
+
+def q4_engine(W, torch, stream, hbm, w, engine, steps, verifies):
     from weight_streaming_gemv_token_gb300 import binding as B
     from weight_streaming_gemv_token_gb300.decoder import Decoder
 
     s = Wl.QWEN3_06B
-    w = Wl.decoder_weights_q4(s, seed=1)
     prompt = Wl.prompt_uniform(PROMPT, s.vocab, seed=0)
     dec = Decoder(s, w, kv_dtype="f32", max_seq=PROMPT + 8 + steps + 2 * (verifies + 4) + 8, stream=stream,
-                  engine="staged")
-    del w
+                  engine=engine)
     first = dec.prefill(prompt, is_last=True)
     out = torch.empty(steps + 4, dtype=torch.int32, device="cuda")
     dec.generate(first, 4, out[:4])
@@ -492,11 +499,11 @@ def q4_config(W, torch, stream, hbm, steps=256, verifies=64):
     dec.close()
     return {
         "workload": "Qwen3-0.6B-shaped decoder, 4-bit groupwise-affine weights (all projections and the tied head), "
-                    f"FP32 KV, staged engine, greedy decode after a {PROMPT}-token prompt",
+                    f"FP32 KV, {engine} engine, greedy decode after a {PROMPT}-token prompt",
         "decode_tokens_per_s": round(rate, 1), "ms_per_step": round(sec / steps * 1e3, 4),
         "bytes_per_token": bpt, "achieved_GB/s": round(bpt * rate / 1e9, 1), "peak": hbm,
         "frac": round(bpt * rate / 1e9 / hbm, 4), "roofline_tokens_per_s": round(hbm * 1e9 / bpt, 1),
-        "gpu_launches_per_step": 5 * s.layers + 3,
+        "gpu_launches_per_step": round(1 / steps, 4) if engine == "persistent" else 5 * s.layers + 3,
         "verify2": {"ms_per_call": round(vsec * 1e3, 4), "rows_per_s": round(2 / vsec, 1),
                     "vs_two_steps": round(2 * sec / steps / vsec, 3), "bytes_per_call": vb,
                     "frac": round(vb / vsec / 1e9 / hbm, 4)},

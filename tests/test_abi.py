@@ -78,7 +78,7 @@ def test_workspace_size_host_logic(lib):
 
 
 def test_q4_configuration_rules(lib):
-    """The 4-bit configuration: staged engine, tokenwise prompts, widths multiples of 512; its
+    """The 4-bit configuration: either engine, tokenwise prompts, widths multiples of 512; its
     workspace holds two rows of activations and logits for the verify step."""
     import workloads as Wl
     from weight_streaming_gemv_token_gb300 import binding as B
@@ -91,7 +91,10 @@ def test_q4_configuration_rules(lib):
     cfg.wdtype = B.DEC_Q4G64
     n_q4 = B.dec_workspace_bytes(cfg)
     assert n_q4 >= n_bf16 + 4 * s.vocab  # a second logit row
-    for field, bad in [("engine", B.DEC_ENGINE_PERSISTENT), ("chunk_cap", 128), ("hidden", 1024 + 64),
+    c3 = B.dec_config.from_buffer_copy(cfg)
+    c3.engine = B.DEC_ENGINE_PERSISTENT
+    assert B.dec_workspace_bytes(c3) == n_q4
+    for field, bad in [("chunk_cap", 128), ("hidden", 1024 + 64),
                        ("inter", 3072 + 256), ("n_q", 12)]:
         c2 = B.dec_config.from_buffer_copy(cfg)
         setattr(c2, field, bad)

@@ -40,14 +40,56 @@ def small_q4():
     return w, dequantised(w)
 
 
+ENGINES = ["staged", "persistent"]
+
+
+@pytest.mark.parametrize("engine", ENGINES)
 @pytest.mark.parametrize("kv", ["f32", "bf16"])
-def test_small_q4_every_logit_and_kv(small_q4, kv):
+def test_small_q4_every_logit_and_kv(small_q4, kv, engine):
     w, deq = small_q4
     prompt = Wl.prompt_uniform(9, Wl.Q4_SMALL.vocab, seed=3)
-    run_and_compare(Wl.Q4_SMALL, w, prompt, 12, kv, LOW_TOL, engine="staged", oracle_weights=deq, act_round="bf16")
+    run_and_compare(Wl.Q4_SMALL, w, prompt, 12, kv, LOW_TOL, engine=engine, oracle_weights=deq, act_round="bf16")
 
 
-def check_verify(shape, w, deq, prompt, drafts, kv="f32", tol=LOW_TOL, rms_tol=None):
+@pytest.mark.parametrize("engine", ENGINES)
+def test_q4_generate_and_prefill_match_steps(small_q4, engine):
+    """One call running many forwards (dec_generate, a tokenwise prompt) gives the tokens, logits and
+    cache of the same forwards run one dec_step each, bit for bit."""
+    import torch
+
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    w, _ = small_q4
+    s = Wl.Q4_SMALL
+    prompt = [int(t) for t in Wl.prompt_uniform(7, s.vocab, seed=9)]
+    a = Decoder(s, w, max_seq=40, engine=engine)
+    b = Decoder(s, w, max_seq=40, engine=engine)
+    first = a.prefill(prompt, is_last=True)
+    for t in prompt[:-1]:
+        b.step(t, skip_logits=True)
+    assert b.step(prompt[-1]) == first
+    out = a.generate(first, 9).cpu().tolist()
+    cur, ref = first, []
+    for _ in range(9):
+        cur = b.step(cur)
+        ref.append(cur)
+    assert out == ref
+    la = torch.empty(s.vocab, device="cuda")
+    lb = torch.empty(s.vocab, device="cuda")
+    a.step(out[-1], logits=la)
+    b.step(out[-1], logits=lb)
+    assert torch.equal(la, lb)
+    for l in range(s.layers):
+        ka, va, na = a.kv(l)
+        kb, vb, nb = b.kv(l)
+        assert na == nb and torch.equal(ka[:, :na], kb[:, :nb]) and torch.equal(va[:, :na], vb[:, :nb])
+    assert a.device_errors() == 0 and b.device_errors() == 0
+    a.close()
+    b.close()
+
+
+def check_verify(shape, w, deq, prompt, drafts, kv="f32", tol=LOW_TOL, rms_tol=None, engine="staged"):
     """Prompt tokenwise, then verify steps of (current token, draft) pairs; every row's logits
     against the oracle's forward of the same rows, the cache after each, and the token rule."""
     import torch
@@ -56,7 +98,7 @@ def check_verify(shape, w, deq, prompt, drafts, kv="f32", tol=LOW_TOL, rms_tol=N
     from weight_streaming_gemv_token_gb300.decoder import Decoder
 
     max_seq = len(prompt) + 2 * len(drafts) + 4
-    dec = Decoder(shape, w, kv_dtype=kv, max_seq=max_seq, engine="staged")
+    dec = Decoder(shape, w, kv_dtype=kv, max_seq=max_seq, engine=engine)
     ora = O.OracleDecoder(shape, deq, kv_dtype=kv, max_seq=max_seq, act_round="bf16")
     for t in prompt[:-1]:
         dec.step(int(t), skip_logits=True)
@@ -89,11 +131,13 @@ def check_verify(shape, w, deq, prompt, drafts, kv="f32", tol=LOW_TOL, rms_tol=N
     dec.close()
 
 
-def test_small_q4_verify_two_rows(small_q4):
+@pytest.mark.parametrize("engine", ENGINES)
+def test_small_q4_verify_two_rows(small_q4, engine):
+    """Verify steps between single steps of either engine (the prompt goes through that engine)."""
     w, deq = small_q4
     prompt = Wl.prompt_uniform(6, Wl.Q4_SMALL.vocab, seed=5)
     drafts = Wl.prompt_uniform(5, Wl.Q4_SMALL.vocab, seed=6)
-    check_verify(Wl.Q4_SMALL, w, deq, prompt, drafts)
+    check_verify(Wl.Q4_SMALL, w, deq, prompt, drafts, engine=engine)
 
 
 def test_verify_accepts_and_rewinds_like_single_steps(small_q4):
@@ -142,7 +186,7 @@ def test_q4_config_errors(small_q4):
 
     w, _ = small_q4
     with pytest.raises(W.WsgError):
-        Decoder(Wl.Q4_SMALL, w, engine="persistent")
+        Decoder(Wl.Q4_SMALL, w, chunk_cap=128, engine="staged")
     d = Decoder(Wl.Q4_SMALL, w, max_seq=3, engine="staged")
     with pytest.raises(W.WsgError) as e:
         d.verify2([1, Wl.Q4_SMALL.vocab])
@@ -172,7 +216,8 @@ def test_qwen3_q4_generation_and_verify(qwen_q4):
     w, deq = qwen_q4
     s = Wl.QWEN3_06B
     prompt = Wl.prompt_uniform(4, s.vocab, seed=0)
-    run_and_compare(s, w, prompt, 3, "f32", Q4_FULL_TOL, check_kv_every=2, engine="staged", oracle_weights=deq,
-                    act_round="bf16", rms_tol=Q4_FULL_RMS)
+    for engine in ENGINES:
+        run_and_compare(s, w, prompt, 3, "f32", Q4_FULL_TOL, check_kv_every=2, engine=engine, oracle_weights=deq,
+                        act_round="bf16", rms_tol=Q4_FULL_RMS)
     check_verify(s, w, deq, Wl.prompt_uniform(3, s.vocab, seed=2), Wl.prompt_uniform(2, s.vocab, seed=4),
                  tol=Q4_FULL_TOL, rms_tol=Q4_FULL_RMS)

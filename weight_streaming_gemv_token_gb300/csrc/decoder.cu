@@ -33,6 +33,7 @@
 #include "gemm_tc_host.h"
 #include "megakernel.cuh"
 #include "prefill.cuh"
+#include "q4_persist.cuh"
 
 namespace wsg {
 void* mk_kernel_f32(bool kv_bf16, bool group_le2);
@@ -53,7 +54,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 size_t dtype_bytes(int dt) { return dt == DEC_F32 ? 4 : 2; }
 
 struct Layout {
-  size_t ctrl, err, tok, h, qkv, attn, act, logits, q4gu, q4next, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn,
+  size_t ctrl, err, tok, h, qkv, attn, act, logits, q4gu, q4next, q4bar, q4layers, apart, acnt, mval, midx, mcnt, ll_h, ll_qkv, ll_attn,
       ll_act,
       ll_tok, ll_apart, kv_ready, mk_layers, mk_maps, rope_cos, rope_sin, kc, vc;
   // chunked prefill (chunk_cap > 0): rows padded to a multiple of 128
@@ -78,7 +79,6 @@ bool config_ok(const dec_config* c, std::string* why) {
   if (c->wdtype != DEC_F32 && c->wdtype != DEC_BF16 && c->wdtype != DEC_Q4G64)
     return bad("wdtype must be DEC_F32, DEC_BF16 or DEC_Q4G64");
   if (c->wdtype == DEC_Q4G64) {
-    if (c->engine != DEC_ENGINE_STAGED) return bad("4-bit weights (DEC_Q4G64) run on the staged engine");
     if (c->chunk_cap != 0) return bad("4-bit weights (DEC_Q4G64) take prompts one token at a time (chunk_cap 0)");
     const int w[3] = {c->hidden, c->inter, c->n_q * c->head_dim};
     for (int x : w)
@@ -117,6 +117,7 @@ Layout make_layout(const dec_config& c) {
   L.logits = take(rows * c.vocab * 4);
   L.q4gu = take(q4 ? rows * 2 * c.inter * 4 : 0);  // gate then up, per row
   L.q4next = take(16);
+  L.q4bar = take(16);  // persistent 4-bit kernel: grid barrier words (cleared by dec_reset)
   L.apart = take(static_cast<size_t>(c.n_kv) * kSplitMax * group * (c.head_dim + 2) * 4);
   L.acnt = take(static_cast<size_t>(c.n_kv) * 4);
   L.mval = take(kArgmaxPartsMax * 4);
@@ -132,6 +133,7 @@ Layout make_layout(const dec_config& c) {
   L.kv_ready = take(static_cast<size_t>(c.layers) * c.n_kv * 4);
   L.mk_layers = take(static_cast<size_t>(c.layers) * sizeof(MkLayer));
   L.mk_maps = take((static_cast<size_t>(c.layers) * kMkMapsPerLayer + 1) * kMkMapBytes);
+  L.q4layers = take(q4 ? static_cast<size_t>(c.layers) * sizeof(Q4PLayer) : 0);
   L.rope_cos = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   L.rope_sin = take(static_cast<size_t>(c.max_seq) * (c.head_dim / 2) * 4);
   L.pf_rows = c.chunk_cap > 0 ? (c.chunk_cap + 127) / 128 * 128 : 0;
@@ -210,6 +212,8 @@ struct dec_ctx {
   uint32_t epoch = 0;         // tag prefix of the last persistent launch (1..4095)
   size_t mk_smem = 0;
   int mk_grid = 0;
+  Q4PArgs q4p{};  // persistent 4-bit kernel: argument template (per-call fields filled at launch)
+  size_t q4p_smem = 0;
   // chunked prefill: tensor maps of the GEMM operands (activation rows: normed
   // input, attention output, SwiGLU output, then their bfloat16 remainders;
   // weights: 7 per layer)
@@ -991,8 +995,120 @@ dec_status plan_persistent(dec_ctx* c) {
 }
 
 // nsteps forwards at positions pos0.. in one cooperative launch.
+void* q4p_kernel(const dec_config& g) {
+  const bool g2 = g.n_q / g.n_kv <= 2;
+  if (g.kvdtype == DEC_BF16)
+    return g2 ? reinterpret_cast<void*>(q4_persist_kernel<uint16_t, 2>)
+              : reinterpret_cast<void*>(q4_persist_kernel<uint16_t, 8>);
+  return g2 ? reinterpret_cast<void*>(q4_persist_kernel<float, 2>) : reinterpret_cast<void*>(q4_persist_kernel<float, 8>);
+}
+
+// Plan the persistent 4-bit kernel: one CTA per SM, a ring of as many chunk
+// stages as shared memory holds after the x planes and the attention scratch.
+dec_status plan_q4_persistent(dec_ctx* c) {
+  const dec_config& g = c->cfg;
+  const int G = c->di.sms;
+  const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;
+  const struct {
+    int rows, in;
+  } mats[8] = {{qw, g.hidden}, {kvw, g.hidden}, {g.hidden, qw}, {g.inter, g.hidden}, {g.hidden, g.inter},
+               {g.vocab, g.hidden}, {kvw, g.hidden}, {g.inter, g.hidden}};
+  size_t stage = 0;
+  for (const auto& m : mats) {
+    const long long rmax = std::min<long long>(kQ4pRC, (m.rows + G - 1) / G);
+    stage = std::max(stage, static_cast<size_t>(rmax) * (m.in / 2 + m.in / 16));
+  }
+  stage = (stage + 127) / 128 * 128;
+  const int in_max = std::max(g.hidden, std::max(qw, g.inter));
+  const size_t fixed = static_cast<size_t>(in_max / 32) * (4 * 16 + 8) +
+                       (attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 15) / 16 * 16;
+  void* k = q4p_kernel(g);
+  cudaFuncAttributes fa{};
+  WSG_CUDA_TRY(&c->err, cudaFuncGetAttributes(&fa, k));
+  const long long budget = static_cast<long long>(c->di.smem_optin) - static_cast<long long>(fa.sharedSizeBytes) -
+                           static_cast<long long>(fixed) - 1024;
+  long long S = budget > 0 ? budget / static_cast<long long>(stage + 16) : 0;
+  if (S > kQ4pMaxStages) S = kQ4pMaxStages;
+  if (S < 2) return fail(&c->err, DEC_EINVAL, "persistent 4-bit engine: a %zu-byte chunk stage does not fit", stage);
+  c->q4p_smem = static_cast<size_t>(S) * (stage + 16) + fixed;
+  WSG_CUDA_TRY(&c->err, cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(c->q4p_smem)));
+  int per_sm = 0;
+  WSG_CUDA_TRY(&c->err, cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kQ4pThreads, c->q4p_smem));
+  if (per_sm < 1) return fail(&c->err, DEC_EINVAL, "persistent 4-bit engine: no CTA fits on an SM");
+  if (g.n_kv * c->nsplit_max > G) return fail(&c->err, DEC_EINVAL, "persistent 4-bit engine: attention CTAs exceed the grid");
+  Q4PArgs& a = c->q4p;
+  a = Q4PArgs{};
+  a.layers = c->at<Q4PLayer>(c->L.q4layers);
+  a.L = g.layers;
+  a.H = g.hidden;
+  a.I = g.inter;
+  a.qw = qw;
+  a.kvw = kvw;
+  a.V = g.vocab;
+  a.eps = g.eps;
+  AttnArgs& at = a.at;
+  at.eps = g.eps;
+  at.rope_cos = c->at<float>(c->L.rope_cos);
+  at.rope_sin = c->at<float>(c->L.rope_sin);
+  at.kc = c->ws + c->L.kc;
+  at.vc = c->ws + c->L.vc;
+  at.max_seq = g.max_seq;
+  at.n_q = g.n_q;
+  at.n_kv = g.n_kv;
+  at.d = g.head_dim;
+  at.part = c->at<float>(c->L.apart);
+  at.counter = c->at<uint32_t>(c->L.acnt);
+  at.nsplit_max = c->nsplit_max;
+  at.tmin = 64;
+  at.scale = 1.0f / sqrtf(static_cast<float>(g.head_dim));
+  at.err = c->at<uint32_t>(c->L.err);
+  a.kv_layer_bytes = c->kv_layer_elems() * dtype_bytes(g.kvdtype);
+  a.h = c->at<float>(c->L.h);
+  a.qkv = c->at<float>(c->L.qkv);
+  a.attn = c->at<float>(c->L.attn);
+  a.gu = c->at<float>(c->L.q4gu);
+  a.logits = c->at<float>(c->L.logits);
+  a.mval = c->at<float>(c->L.mval);
+  a.midx = c->at<int32_t>(c->L.midx);
+  a.tok = c->at<int32_t>(c->L.tok);
+  a.ctrl = c->at<int32_t>(c->L.ctrl);
+  a.bar = c->at<unsigned long long>(c->L.q4bar);
+  a.nstages = static_cast<int32_t>(S);
+  a.stage_bytes = static_cast<uint32_t>(stage);
+  a.attn_bytes = static_cast<uint32_t>((attn_smem_bytes(g.n_q / g.n_kv, g.head_dim) + 15) / 16 * 16);
+  a.err = c->at<uint32_t>(c->L.err);
+  return DEC_OK;
+}
+
+dec_status run_q4_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, bool head_last, int32_t first_tok,
+                             int32_t* host_next) {
+  Q4PArgs a = c->q4p;
+  a.head = q4_seg(c->w.embed, c->cfg.vocab, c->cfg.hidden, 0);
+  a.g_final = c->w.g_final;
+  a.pos0 = pos0;
+  a.nsteps = nsteps;
+  a.head_every = head_every ? 1 : 0;
+  a.head_last = head_last ? 1 : 0;
+  a.first_tok = first_tok;
+  a.host_next = host_next;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(c->di.sms);
+  cfg.blockDim = dim3(kQ4pThreads);
+  cfg.dynamicSmemBytes = c->q4p_smem;
+  cfg.stream = c->stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&a};
+  WSG_CUDA_TRY(&c->err, cudaLaunchKernelExC(&cfg, q4p_kernel(c->cfg), args));
+  return DEC_OK;
+}
+
 dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, bool head_last, int32_t first_tok = -1,
                           int32_t* host_next = nullptr) {
+  if (c->cfg.wdtype == DEC_Q4G64) return run_q4_persistent(c, pos0, nsteps, head_every, head_last, first_tok, host_next);
   MkArgs a = c->mk;
   a.first_tok = first_tok;
   a.host_next = host_next;
@@ -1165,7 +1281,8 @@ extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_
   if (c->nsplit_max < 1) c->nsplit_max = 1;
   if (c->nsplit_max > kSplitMax) c->nsplit_max = kSplitMax;
   s = cfg->wdtype == DEC_F32 ? prepare_kernels<float>(c) : prepare_kernels<uint16_t>(c);
-  if (s == DEC_OK && cfg->engine == DEC_ENGINE_PERSISTENT) s = plan_persistent(c);
+  if (s == DEC_OK && cfg->engine == DEC_ENGINE_PERSISTENT)
+    s = cfg->wdtype == DEC_Q4G64 ? plan_q4_persistent(c) : plan_persistent(c);
   if (s != DEC_OK) {
     thread_error() = c->err;
     return bail(s);
@@ -1195,8 +1312,24 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
   }
   WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->ws + c->L.mk_layers, tab.data(), tab.size() * sizeof(MkLayer),
                                         cudaMemcpyHostToDevice, c->stream));
+  if (c->cfg.wdtype == DEC_Q4G64 && c->cfg.engine == DEC_ENGINE_PERSISTENT) {
+    // the persistent 4-bit kernel's layer table: each matrix as (codes, scales, biases, rows)
+    const dec_config& g = c->cfg;
+    const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;
+    std::vector<Q4PLayer> q4t(g.layers);
+    for (int l = 0; l < g.layers; ++l) {
+      const dec_layer_weights& x = c->layers[l];
+      q4t[l] = Q4PLayer{q4_seg(x.w_q, qw, g.hidden, 0),       q4_seg(x.w_k, kvw, g.hidden, 0),
+                        q4_seg(x.w_v, kvw, g.hidden, 0),      q4_seg(x.w_o, g.hidden, qw, 0),
+                        q4_seg(x.w_gate, g.inter, g.hidden, 0), q4_seg(x.w_up, g.inter, g.hidden, 0),
+                        q4_seg(x.w_down, g.hidden, g.inter, 0), x.g_in, x.g_post, x.g_q, x.g_k};
+    }
+    WSG_CUDA_TRY(&c->err, cudaMemcpyAsync(c->ws + c->L.q4layers, q4t.data(), q4t.size() * sizeof(Q4PLayer),
+                                          cudaMemcpyHostToDevice, c->stream));
+    WSG_CUDA_TRY(&c->err, cudaStreamSynchronize(c->stream));
+  }
   std::vector<CUtensorMap> maps;
-  if (c->cfg.engine == DEC_ENGINE_PERSISTENT) {
+  if (c->cfg.engine == DEC_ENGINE_PERSISTENT && c->cfg.wdtype != DEC_Q4G64) {
     // Tiled-copy descriptors of every weight matrix for the persistent engine.
     const dec_config& g = c->cfg;
     const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;

@@ -135,6 +135,210 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
+// Consumers (threads 0 .. kQ4Warps * 32 - 1): per chunk of 32 columns and
+// token, the fixed-point step, the byte planes and the float sum of x, built
+// by the x prologue XM; ends with a consumer barrier.
+template <int NTOK, int XM>
+__device__ __forceinline__ void q4_stage_x(const void* xp, int x_ld, const float* norm_g, float eps, int in, uint4* xq,
+                                           float2* xu, float* s_rs, int tid) {
+  const int warp = tid >> 5, lane = tid & 31, nch = in >> 5;
+  // One token of at most 8 columns per thread: the first pass reads exactly
+  // this thread's staging item (columns 8 tid .. 8 tid + 7) and keeps it.
+  constexpr bool kOne = XM == Q4X_NORM && NTOK == 1;
+  const bool keep = kOne && in <= 8 * kQ4Warps * 32;
+  float hv[8];
+  if (XM == Q4X_NORM) {
+    // 1 / RMS of each token's h, summed in a fixed order
+    const float* h = static_cast<const float*>(xp);
+    for (int t = 0; t < NTOK; ++t) {
+      float ss = 0.f;
+      if (keep) {
+        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+        if (8 * tid < in) {
+          v0 = __ldcg(reinterpret_cast<const float4*>(h + 8 * tid));
+          v1 = __ldcg(reinterpret_cast<const float4*>(h + 8 * tid + 4));
+        }
+        hv[0] = v0.x, hv[1] = v0.y, hv[2] = v0.z, hv[3] = v0.w;
+        hv[4] = v1.x, hv[5] = v1.y, hv[6] = v1.z, hv[7] = v1.w;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) ss = fmaf(hv[j], hv[j], ss);
+      } else {
+        for (int i = 4 * tid; i < in; i += 4 * kQ4Warps * 32) {
+          const float4 v = __ldcg(reinterpret_cast<const float4*>(h + static_cast<size_t>(t) * x_ld + i));
+          ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
+        }
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_rs[t * kQ4Warps + warp] = ss;
+    }
+    q4_consumer_sync();
+  }
+  float rs[NTOK];
+  if (XM == Q4X_NORM) {
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+      float ss = 0.f;
+      for (int w = 0; w < kQ4Warps; ++w) ss += s_rs[t * kQ4Warps + w];
+      rs[t] = rsqrtf(ss / static_cast<float>(in) + eps);
+    }
+  }
+  // x: per chunk and token, the fixed point step, the byte planes and the
+  // float sum. Four consecutive lanes per chunk, lane m taking the 8 columns
+  // of word m and building that word of all four planes; the butterfly max
+  // and sum over the four lanes leave the same value in each.
+  {
+    const int items = NTOK * nch * 4;
+    for (int it0 = warp * 32; it0 < items; it0 += kQ4Warps * 32) {
+      const int it = it0 + lane;
+      const bool valid = it < items;
+      const int t = valid ? it / (nch * 4) : 0, rem = it - t * nch * 4, ch = rem >> 2, m = rem & 3;
+      const int col = 32 * ch + 8 * m;
+      float xv[8];
+      if (XM == Q4X_BF16) {
+        uint4 u = make_uint4(0, 0, 0, 0);
+        if (valid)
+          u = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xp) + static_cast<size_t>(t) * x_ld +
+                                                    col));
+        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          xv[2 * k] = __uint_as_float(uw[k] << 16);              // column 8m + 2k
+          xv[2 * k + 1] = __uint_as_float(uw[k] & 0xFFFF0000u);  // column 8m + 2k + 1
+        }
+      } else {
+        const float* xr = static_cast<const float*>(xp) + static_cast<size_t>(t) * x_ld + col;
+        float f[8];
+        if (keep) {  // item it == tid: this thread's columns from the first pass
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = hv[j];
+        } else {
+          float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+          if (valid) {
+            v0 = __ldcg(reinterpret_cast<const float4*>(xr));
+            v1 = __ldcg(reinterpret_cast<const float4*>(xr + 4));
+          }
+          f[0] = v0.x, f[1] = v0.y, f[2] = v0.z, f[3] = v0.w;
+          f[4] = v1.x, f[5] = v1.y, f[6] = v1.z, f[7] = v1.w;
+        }
+        if (XM == Q4X_NORM) {
+          float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+          if (valid) {
+            g0 = __ldg(reinterpret_cast<const float4*>(norm_g + col));
+            g1 = __ldg(reinterpret_cast<const float4*>(norm_g + col + 4));
+          }
+          const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+          float r = rs[0];
+#pragma unroll
+          for (int tt = 1; tt < NTOK; ++tt)
+            if (t == tt) r = rs[tt];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = (f[j] * r) * g[j];
+        } else if (XM == Q4X_SWIGLU) {
+          float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = u0;
+          if (valid) {
+            u0 = __ldcg(reinterpret_cast<const float4*>(xr + in));
+            u1 = __ldcg(reinterpret_cast<const float4*>(xr + in + 4));
+          }
+          const float up[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+          for (int j = 0; j < 8; ++j) f[j] = silu_f32(f[j]) * up[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) xv[j] = q4_round_bf16(f[j]);
+      }
+      float mx = 0.f, X = 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        mx = fmaxf(mx, fabsf(xv[j]));
+        X += xv[j];
+      }
+#pragma unroll
+      for (int o = 1; o <= 2; o <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        X += __shfl_xor_sync(0xffffffffu, X, o);
+      }
+      int e = 0;
+      if (mx > 0.f) {
+        frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1): 2^(e-1) <= mx < 2^e
+        e -= 1;
+      }
+      uint32_t he = 0, le = 0, ho = 0, lo = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int xe = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k], 14 - e))) : 0;
+        const int xo = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k + 1], 14 - e))) : 0;
+        he |= (static_cast<uint32_t>(xe >> 8) & 0xFFu) << (8 * k);
+        le |= (static_cast<uint32_t>(xe) & 0xFFu) << (8 * k);
+        ho |= (static_cast<uint32_t>(xo >> 8) & 0xFFu) << (8 * k);
+        lo |= (static_cast<uint32_t>(xo) & 0xFFu) << (8 * k);
+      }
+      if (valid) {
+        uint32_t* w = reinterpret_cast<uint32_t*>(xq + t * 4 * nch + ch) + m;  // word m of plane 0
+        w[0] = he;
+        w[4 * nch] = le;
+        w[8 * nch] = ho;
+        w[12 * nch] = lo;
+        if (m == 0) xu[t * nch + ch] = make_float2(mx > 0.f ? scalbnf(1.0f, e - 18) : 0.f, X);
+      }
+    }
+  }
+  q4_consumer_sync();
+}
+
+// Consumers: add the chunk's row sums (rows w, w + 8, ... of warp w; lane
+// partials) for every token to acc[i * NTOK + t]. base: the chunk's codes
+// [rows][cb], then scales and biases [rows][sbb] at sbase and bbase.
+template <int R, int NTOK>
+__device__ __forceinline__ void q4_chunk_dot(const unsigned char* base, const unsigned char* sbase,
+                                             const unsigned char* bbase, int rows, uint32_t cb, uint32_t sbb, int nch,
+                                             const uint4* xq, const float2* xu, int warp, int lane,
+                                             float (&acc)[R * NTOK]) {
+    for (int ch = lane; ch < nch; ch += 32) {
+      uint4 q[R];
+      float s[R], b[R];
+#pragma unroll
+      for (int i = 0; i < R; ++i) {
+        const int rr = warp + kQ4Warps * i;
+        if (rr < rows) {
+          q[i] = *reinterpret_cast<const uint4*>(base + rr * cb + 16 * ch);
+          s[i] = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(sbase + rr * sbb + 2 * (ch >> 1))));
+          b[i] = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(bbase + rr * sbb + 2 * (ch >> 1))));
+        } else {
+          q[i] = make_uint4(0, 0, 0, 0);
+          s[i] = b[i] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < NTOK; ++t) {
+        const uint4 phe = xq[(t * 4 + 0) * nch + ch], ple = xq[(t * 4 + 1) * nch + ch];
+        const uint4 pho = xq[(t * 4 + 2) * nch + ch], plo = xq[(t * 4 + 3) * nch + ch];
+        const float2 xs = xu[t * nch + ch];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+          int he = 0, ho = 0;
+          uint32_t le = 0, lo = 0;
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            const uint32_t w = m == 0 ? q[i].x : m == 1 ? q[i].y : m == 2 ? q[i].z : q[i].w;
+            const uint32_t ev = w & 0x0F0F0F0Fu;  // q of columns 8m, 8m+2, 8m+4, 8m+6
+            const uint32_t od = w & 0xF0F0F0F0u;  // 16 q of columns 8m+1, 8m+3, 8m+5, 8m+7
+            const uint32_t xhe = m == 0 ? phe.x : m == 1 ? phe.y : m == 2 ? phe.z : phe.w;
+            const uint32_t xle = m == 0 ? ple.x : m == 1 ? ple.y : m == 2 ? ple.z : ple.w;
+            const uint32_t xho = m == 0 ? pho.x : m == 1 ? pho.y : m == 2 ? pho.z : pho.w;
+            const uint32_t xlo = m == 0 ? plo.x : m == 1 ? plo.y : m == 2 ? plo.z : plo.w;
+            he = dp4a_us(ev, xhe, he);
+            le = dp4a_uu(ev, xle, le);
+            ho = dp4a_us(od, xho, ho);
+            lo = dp4a_uu(od, xlo, lo);
+          }
+          // 16 sum q xi, exact (below 2^28 in magnitude)
+          const int tot = 16 * (256 * he + static_cast<int>(le)) + 256 * ho + static_cast<int>(lo);
+          acc[i * NTOK + t] = fmaf(s[i] * xs.x, static_cast<float>(tot), fmaf(b[i], xs.y, acc[i * NTOK + t]));
+        }
+      }
+    }
+}
+
 // Shared memory: [ring: nstages x stage_bytes][xq: NTOK][4][nch] uint4 (the byte
 // planes of chunk c: high bytes of the even columns, low bytes of the even
 // columns, high and low bytes of the odd columns; word m of a plane holds
@@ -211,124 +415,7 @@ __global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Arg
   // ---- consumers ----
   // x may come from the previous kernel, and y may still be read by it.
   pdl_wait();
-  const int ctid = tid;  // 0 .. kQ4Warps * 32 - 1
-  if (XM == Q4X_NORM) {
-    // 1 / RMS of each token's h, summed in a fixed order
-    const float* h = static_cast<const float*>(a.x);
-    for (int t = 0; t < NTOK; ++t) {
-      float ss = 0.f;
-      for (int i = 4 * ctid; i < in; i += 4 * kQ4Warps * 32) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(h + static_cast<size_t>(t) * a.x_ld + i));
-        ss = fmaf(v.x, v.x, fmaf(v.y, v.y, fmaf(v.z, v.z, fmaf(v.w, v.w, ss))));
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) s_rs[t * kQ4Warps + warp] = ss;
-    }
-    q4_consumer_sync();
-  }
-  float rs[NTOK];
-  if (XM == Q4X_NORM) {
-#pragma unroll
-    for (int t = 0; t < NTOK; ++t) {
-      float ss = 0.f;
-      for (int w = 0; w < kQ4Warps; ++w) ss += s_rs[t * kQ4Warps + w];
-      rs[t] = rsqrtf(ss / static_cast<float>(in) + a.eps);
-    }
-  }
-  // x: per chunk and token, the fixed point step, the byte planes and the
-  // float sum. Four consecutive lanes per chunk, lane m taking the 8 columns
-  // of word m and building that word of all four planes; the butterfly max
-  // and sum over the four lanes leave the same value in each.
-  {
-    const int items = NTOK * nch * 4;
-    for (int it0 = warp * 32; it0 < items; it0 += kQ4Warps * 32) {
-      const int it = it0 + lane;
-      const bool valid = it < items;
-      const int t = valid ? it / (nch * 4) : 0, rem = it - t * nch * 4, ch = rem >> 2, m = rem & 3;
-      const int col = 32 * ch + 8 * m;
-      float xv[8];
-      if (XM == Q4X_BF16) {
-        uint4 u = make_uint4(0, 0, 0, 0);
-        if (valid)
-          u = __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.x) + static_cast<size_t>(t) * a.x_ld +
-                                                    col));
-        const uint32_t uw[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          xv[2 * k] = __uint_as_float(uw[k] << 16);              // column 8m + 2k
-          xv[2 * k + 1] = __uint_as_float(uw[k] & 0xFFFF0000u);  // column 8m + 2k + 1
-        }
-      } else {
-        const float* xr = static_cast<const float*>(a.x) + static_cast<size_t>(t) * a.x_ld + col;
-        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
-        if (valid) {
-          v0 = __ldcg(reinterpret_cast<const float4*>(xr));
-          v1 = __ldcg(reinterpret_cast<const float4*>(xr + 4));
-        }
-        float f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        if (XM == Q4X_NORM) {
-          float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
-          if (valid) {
-            g0 = __ldg(reinterpret_cast<const float4*>(a.norm_g + col));
-            g1 = __ldg(reinterpret_cast<const float4*>(a.norm_g + col + 4));
-          }
-          const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-          float r = rs[0];
-#pragma unroll
-          for (int tt = 1; tt < NTOK; ++tt)
-            if (t == tt) r = rs[tt];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = (f[j] * r) * g[j];
-        } else if (XM == Q4X_SWIGLU) {
-          float4 u0 = make_float4(0.f, 0.f, 0.f, 0.f), u1 = u0;
-          if (valid) {
-            u0 = __ldcg(reinterpret_cast<const float4*>(xr + in));
-            u1 = __ldcg(reinterpret_cast<const float4*>(xr + in + 4));
-          }
-          const float up[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-#pragma unroll
-          for (int j = 0; j < 8; ++j) f[j] = silu_f32(f[j]) * up[j];
-        }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) xv[j] = q4_round_bf16(f[j]);
-      }
-      float mx = 0.f, X = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        mx = fmaxf(mx, fabsf(xv[j]));
-        X += xv[j];
-      }
-#pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        X += __shfl_xor_sync(0xffffffffu, X, o);
-      }
-      int e = 0;
-      if (mx > 0.f) {
-        frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1): 2^(e-1) <= mx < 2^e
-        e -= 1;
-      }
-      uint32_t he = 0, le = 0, ho = 0, lo = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int xe = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k], 14 - e))) : 0;
-        const int xo = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k + 1], 14 - e))) : 0;
-        he |= (static_cast<uint32_t>(xe >> 8) & 0xFFu) << (8 * k);
-        le |= (static_cast<uint32_t>(xe) & 0xFFu) << (8 * k);
-        ho |= (static_cast<uint32_t>(xo >> 8) & 0xFFu) << (8 * k);
-        lo |= (static_cast<uint32_t>(xo) & 0xFFu) << (8 * k);
-      }
-      if (valid) {
-        uint32_t* w = reinterpret_cast<uint32_t*>(xq + t * 4 * nch + ch) + m;  // word m of plane 0
-        w[0] = he;
-        w[4 * nch] = le;
-        w[8 * nch] = ho;
-        w[12 * nch] = lo;
-        if (m == 0) xu[t * nch + ch] = make_float2(mx > 0.f ? scalbnf(1.0f, e - 18) : 0.f, X);
-      }
-    }
-  }
-  q4_consumer_sync();
+  q4_stage_x<NTOK, XM>(a.x, a.x_ld, a.norm_g, a.eps, in, xq, xu, s_rs, tid);
 
   bool ok = true;
   for (int st = 0; st < nst && ok; ++st) {
@@ -346,50 +433,7 @@ __global__ void __launch_bounds__(kQ4Threads, 2) gemv_q4_bulk_kernel(const Q4Arg
     float acc[NV];
 #pragma unroll
     for (int v = 0; v < NV; ++v) acc[v] = 0.f;
-    for (int ch = lane; ch < nch; ch += 32) {
-      uint4 q[R];
-      float s[R], b[R];
-#pragma unroll
-      for (int i = 0; i < R; ++i) {
-        const int rr = warp + kQ4Warps * i;
-        if (rr < rows) {
-          q[i] = *reinterpret_cast<const uint4*>(base + rr * cb + 16 * ch);
-          s[i] = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(sbase + rr * sbb + 2 * (ch >> 1))));
-          b[i] = __half2float(__ushort_as_half(*reinterpret_cast<const uint16_t*>(bbase + rr * sbb + 2 * (ch >> 1))));
-        } else {
-          q[i] = make_uint4(0, 0, 0, 0);
-          s[i] = b[i] = 0.f;
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < NTOK; ++t) {
-        const uint4 phe = xq[(t * 4 + 0) * nch + ch], ple = xq[(t * 4 + 1) * nch + ch];
-        const uint4 pho = xq[(t * 4 + 2) * nch + ch], plo = xq[(t * 4 + 3) * nch + ch];
-        const float2 xs = xu[t * nch + ch];
-#pragma unroll
-        for (int i = 0; i < R; ++i) {
-          int he = 0, ho = 0;
-          uint32_t le = 0, lo = 0;
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            const uint32_t w = m == 0 ? q[i].x : m == 1 ? q[i].y : m == 2 ? q[i].z : q[i].w;
-            const uint32_t ev = w & 0x0F0F0F0Fu;  // q of columns 8m, 8m+2, 8m+4, 8m+6
-            const uint32_t od = w & 0xF0F0F0F0u;  // 16 q of columns 8m+1, 8m+3, 8m+5, 8m+7
-            const uint32_t xhe = m == 0 ? phe.x : m == 1 ? phe.y : m == 2 ? phe.z : phe.w;
-            const uint32_t xle = m == 0 ? ple.x : m == 1 ? ple.y : m == 2 ? ple.z : ple.w;
-            const uint32_t xho = m == 0 ? pho.x : m == 1 ? pho.y : m == 2 ? pho.z : pho.w;
-            const uint32_t xlo = m == 0 ? plo.x : m == 1 ? plo.y : m == 2 ? plo.z : plo.w;
-            he = dp4a_us(ev, xhe, he);
-            le = dp4a_uu(ev, xle, le);
-            ho = dp4a_us(od, xho, ho);
-            lo = dp4a_uu(od, xlo, lo);
-          }
-          // 16 sum q xi, exact (below 2^28 in magnitude)
-          const int tot = 16 * (256 * he + static_cast<int>(le)) + 256 * ho + static_cast<int>(lo);
-          acc[i * NTOK + t] = fmaf(s[i] * xs.x, static_cast<float>(tot), fmaf(b[i], xs.y, acc[i * NTOK + t]));
-        }
-      }
-    }
+    q4_chunk_dot<R, NTOK>(base, sbase, bbase, rows, cb, sbb, nch, xq, xu, warp, lane, acc);
     // every lane's reads of the stage are in registers: release it
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);

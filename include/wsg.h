@@ -74,8 +74,10 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
  * Requirements: layers, hidden, inter, n_q, n_kv, head_dim, vocab > 0;
  * n_q % n_kv == 0; head_dim a multiple of 8 and <= 128; hidden, inter and
  * n_q*head_dim multiples of 8; wdtype DEC_F32, DEC_BF16 or DEC_Q4G64 (the
- * 4-bit configuration: staged engine, chunk_cap 0, hidden, inter and
- * n_q*head_dim multiples of 512 up to 16384); kvdtype DEC_F32
+ * 4-bit configuration: chunk_cap 0, hidden, inter and n_q*head_dim
+ * multiples of 512 up to 16384; its persistent engine separates stages
+ * with grid barriers, and its staged engine is the faster of the two);
+ * kvdtype DEC_F32
  * or DEC_BF16; max_seq >= 1 is the KV capacity in positions; chunk_cap is
  * the largest row count of one dec_prefill_chunk call that runs batched
  * (0: prompts are processed one token at a time). engine selects the

@@ -135,6 +135,48 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
+// Word m (columns 32 ch + 8 m .. + 7, values xv, already bfloat16 values) of
+// token t's byte planes of chunk ch: four consecutive lanes hold the four words
+// of a chunk and reduce its largest |x| and its sum by shuffles, so every lane
+// of the warp calls this (valid: the item exists).
+__device__ __forceinline__ void q4_item_planes(const float (&xv)[8], int t, int ch, int m, int nch, bool valid,
+                                               uint4* xq, float2* xu) {
+  float mx = 0.f, X = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    mx = fmaxf(mx, fabsf(xv[j]));
+    X += xv[j];
+  }
+#pragma unroll
+  for (int o = 1; o <= 2; o <<= 1) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    X += __shfl_xor_sync(0xffffffffu, X, o);
+  }
+  int e = 0;
+  if (mx > 0.f) {
+    frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1): 2^(e-1) <= mx < 2^e
+    e -= 1;
+  }
+  uint32_t he = 0, le = 0, ho = 0, lo = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int xe = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k], 14 - e))) : 0;
+    const int xo = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k + 1], 14 - e))) : 0;
+    he |= (static_cast<uint32_t>(xe >> 8) & 0xFFu) << (8 * k);
+    le |= (static_cast<uint32_t>(xe) & 0xFFu) << (8 * k);
+    ho |= (static_cast<uint32_t>(xo >> 8) & 0xFFu) << (8 * k);
+    lo |= (static_cast<uint32_t>(xo) & 0xFFu) << (8 * k);
+  }
+  if (valid) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(xq + t * 4 * nch + ch) + m;  // word m of plane 0
+    w[0] = he;
+    w[4 * nch] = le;
+    w[8 * nch] = ho;
+    w[12 * nch] = lo;
+    if (m == 0) xu[t * nch + ch] = make_float2(mx > 0.f ? scalbnf(1.0f, e - 18) : 0.f, X);
+  }
+}
+
 // Consumers (threads 0 .. kQ4Warps * 32 - 1): per chunk of 32 columns and
 // token, the fixed-point step, the byte planes and the float sum of x, built
 // by the x prologue XM; ends with a consumer barrier.
@@ -246,40 +288,7 @@ __device__ __forceinline__ void q4_stage_x(const void* xp, int x_ld, const float
 #pragma unroll
         for (int j = 0; j < 8; ++j) xv[j] = q4_round_bf16(f[j]);
       }
-      float mx = 0.f, X = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        mx = fmaxf(mx, fabsf(xv[j]));
-        X += xv[j];
-      }
-#pragma unroll
-      for (int o = 1; o <= 2; o <<= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        X += __shfl_xor_sync(0xffffffffu, X, o);
-      }
-      int e = 0;
-      if (mx > 0.f) {
-        frexpf(mx, &e);  // mx = f 2^e, f in [0.5, 1): 2^(e-1) <= mx < 2^e
-        e -= 1;
-      }
-      uint32_t he = 0, le = 0, ho = 0, lo = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int xe = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k], 14 - e))) : 0;
-        const int xo = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k + 1], 14 - e))) : 0;
-        he |= (static_cast<uint32_t>(xe >> 8) & 0xFFu) << (8 * k);
-        le |= (static_cast<uint32_t>(xe) & 0xFFu) << (8 * k);
-        ho |= (static_cast<uint32_t>(xo >> 8) & 0xFFu) << (8 * k);
-        lo |= (static_cast<uint32_t>(xo) & 0xFFu) << (8 * k);
-      }
-      if (valid) {
-        uint32_t* w = reinterpret_cast<uint32_t*>(xq + t * 4 * nch + ch) + m;  // word m of plane 0
-        w[0] = he;
-        w[4 * nch] = le;
-        w[8 * nch] = ho;
-        w[12 * nch] = lo;
-        if (m == 0) xu[t * nch + ch] = make_float2(mx > 0.f ? scalbnf(1.0f, e - 18) : 0.f, X);
-      }
+      q4_item_planes(xv, t, ch, m, nch, valid, xq, xu);
     }
   }
   q4_consumer_sync();

@@ -62,6 +62,10 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
 #define DEC_DEVERR_WAIT_TIMEOUT 0x1u /* a bounded mbarrier wait gave up */
 #define DEC_DEVERR_ARGMAX_NAN 0x2u   /* all logits NaN; token 0 was returned */
 #define DEC_DEVERR_BAD_TOKEN 0x4u    /* a token ID outside [0, vocab) was read as 0 */
+#define DEC_DEVERR_BAD_POSITION 0x8u /* a position reached the KV capacity; the step did nothing */
+#define DEC_DEVERR_EXCHANGE_TIMEOUT 0x10u /* persistent engine: a wait for another CTA's words gave up */
+#define DEC_DEVERR_GEMM_TIMEOUT 0x20u     /* chunked prefill: a tensor-core GEMM pipeline wait gave up */
+#define DEC_DEVERR_BARRIER_TIMEOUT 0x40u  /* persistent 4-bit engine: a grid barrier gave up (dec_reset clears it) */
 
 /* dec_config.engine */
 #define DEC_ENGINE_PERSISTENT 0 /* one cooperative launch runs whole forwards (default) */

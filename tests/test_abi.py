@@ -147,3 +147,23 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(bld, "LIB", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         B.library()
+
+
+def test_device_error_bits_are_documented_once():
+    """Every error bit a kernel can set has its own value and is declared in the header (and the binding)."""
+    import glob
+
+    from weight_streaming_gemv_token_gb300 import binding as B
+
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    header = open(os.path.join(root, "include", "wsg.h")).read()
+    public = {n: int(v, 16) for n, v in re.findall(r"#define (DEC_DEVERR_\w+) (0x[0-9a-fA-F]+)u", header)}
+    internal = {}
+    for f in glob.glob(os.path.join(root, "weight_streaming_gemv_token_gb300", "csrc", "*.cu*")):
+        for n, k in re.findall(r"\b(ERR_\w+) = 1u << (\d+)", open(f).read()):
+            internal[n] = 1 << int(k)
+    assert len(set(internal.values())) == len(internal), internal
+    assert sorted(internal.values()) == sorted(public.values()), (internal, public)
+    for n, v in public.items():
+        assert getattr(B, n) == v

@@ -21,6 +21,8 @@ DEC_F32, DEC_BF16, DEC_Q4G64 = 0, 1, 2
 DEC_SKIP_LOGITS = 0x1
 DEC_ENGINE_PERSISTENT, DEC_ENGINE_STAGED = 0, 1
 DEC_DEVERR_WAIT_TIMEOUT, DEC_DEVERR_ARGMAX_NAN, DEC_DEVERR_BAD_TOKEN = 0x1, 0x2, 0x4
+DEC_DEVERR_BAD_POSITION, DEC_DEVERR_EXCHANGE_TIMEOUT, DEC_DEVERR_GEMM_TIMEOUT, DEC_DEVERR_BARRIER_TIMEOUT = (
+    0x8, 0x10, 0x20, 0x40)
 
 # Every symbol include/wsg.h declares.
 EXPORTED = (

@@ -58,7 +58,7 @@ constexpr int kQ4pThreads = kQ4Warps * 32 + 128;
 constexpr int kQ4pProducerRegs = 56;
 constexpr int kQ4pConsumerRegs = 224;
 
-enum : uint32_t { ERR_GRID_BARRIER_TIMEOUT = 1u << 5 };
+enum : uint32_t { ERR_GRID_BARRIER_TIMEOUT = 1u << 6 };
 
 struct Q4PLayer {
   Q4Seg q, k, v, o, gate, up, down;  // rows and pointers (y_off, cta0 unused)

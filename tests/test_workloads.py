@@ -44,3 +44,30 @@ def test_q4_decoder_weights_layout_and_spread():
     m = a["layers"][0]["w_gate"]
     wq = q4_dequant(m["packed"], m["scale"], m["bias"])
     assert abs(wq.mean()) < 2e-3 and 0.015 < wq.std() < 0.035
+
+
+def test_q4_weight_buffer_layout_matches_the_abi():
+    """A 4-bit matrix buffer is its codes [out][in/8] (uint32, code j of word w at bits 4j..4j+3 for
+    column 8w+j), then the scales and then the biases [out][in/64] (fp16), back to back."""
+    pytest = __import__("pytest")
+    pytest.importorskip("torch")
+    import workloads as Wl
+    from weight_streaming_gemv_token_gb300.decoder import q4_blob
+
+    out, inp = 24, 512
+    m = Wl.decoder_weights_q4(Wl.DecoderShape(layers=1, hidden=inp, inter=inp, n_q=4, n_kv=2, head_dim=128,
+                                              vocab=out), seed=3)["embed"]
+    b = q4_blob(m, device="cpu").numpy()
+    cb, sb = out * inp // 2, out * (inp // 64) * 2
+    assert b.dtype == np.uint8 and b.size == cb + 2 * sb
+    words = b[:cb].view(np.uint32).reshape(out, inp // 8)
+    np.testing.assert_array_equal(words, m["packed"])
+    np.testing.assert_array_equal(b[cb:cb + sb].view(np.float16).reshape(out, inp // 64), m["scale"])
+    np.testing.assert_array_equal(b[cb + sb:].view(np.float16).reshape(out, inp // 64), m["bias"])
+    # code j of word w is column 8w + j (low nibble first)
+    from oracle import q4_unpack
+
+    codes = q4_unpack(words)
+    assert int(codes[0, 9]) == (int(words[0, 1]) >> 4) & 0xF
+    # every section starts on a 16-byte boundary (bulk copies need it) when in % 512 == 0
+    assert cb % 16 == 0 and sb % 16 == 0

@@ -29,13 +29,11 @@ Readings of points the pages leave open (each also listed in the design notes):
   * query head h uses key/value head h // (n_q / n_kv);
   * cached keys are post-norm, post-RoPE; cached values are the raw projection;
   * no biases anywhere; the embedding matrix doubles as the vocabulary head;
-  * the 4-bit configuration (``act_round="bf16"``): weights are the exact
-    dequantised values s * q + b of the 4-bit groupwise-affine format, and
-    the vector entering each projection (the normed residual, the attention
-    output, the SwiGLU output, the final normed row) is rounded to bfloat16
-    first, the input format of the 4-bit matrix-vector product ("Our Kernel
-    Benchmark Was Measuring the System Cache", Summary). Everything else
-    stays float64.
+  * the 4-bit configuration is this same forward on the exact dequantised
+    weights s * q + b of the 4-bit groupwise-affine format ("Our Kernel
+    Benchmark Was Measuring the System Cache", Summary): the pages fix the
+    weight format, not the precision of the activations inside the decoder,
+    so the activations stay those of the float forward.
 """
 from __future__ import annotations
 
@@ -53,14 +51,11 @@ class OracleDecoder:
     g_in/g_post [H], g_q/g_k [d]. Arrays may be float32 or bf16 bit patterns.
     """
 
-    def __init__(self, shape, weights: dict, kv_dtype: str = "f32", max_seq: int = 4096, act_round: str | None = None):
+    def __init__(self, shape, weights: dict, kv_dtype: str = "f32", max_seq: int = 4096):
         if kv_dtype not in ("f32", "bf16"):
             raise ValueError(kv_dtype)
-        if act_round not in (None, "bf16"):
-            raise ValueError(act_round)
         self.s = shape
         self.kv_dtype = kv_dtype
-        self.act_round = act_round
         self.max_seq = int(max_seq)
         self.E = P.widen(weights["embed"])
         self.g_final = P.widen(weights["g_final"])
@@ -76,10 +71,6 @@ class OracleDecoder:
 
     def _store(self, x):
         return P.round_to_bf16(x) if self.kv_dtype == "bf16" else x
-
-    def _act(self, x):
-        """The vector entering a projection, in the projection's input format."""
-        return P.round_to_bf16(x) if self.act_round == "bf16" else x
 
     def kv(self, layer: int):
         """(K, V) cache of one layer, [n_kv, n_valid, d], as stored."""
@@ -98,7 +89,7 @@ class OracleDecoder:
         d, eps = s.head_dim, s.eps
         h = self.E[int(token)].copy()
         for l, w in enumerate(self.layers):
-            x = self._act(P.rmsnorm(h, w["g_in"], eps))
+            x = P.rmsnorm(h, w["g_in"], eps)
             q = (w["w_q"] @ x).reshape(s.n_q, d)
             k = (w["w_k"] @ x).reshape(s.n_kv, d)
             v = (w["w_v"] @ x).reshape(s.n_kv, d)
@@ -107,15 +98,15 @@ class OracleDecoder:
             self.K[l, :, p] = self._store(k)
             self.V[l, :, p] = self._store(v)
             o = P.gqa_decode_attention(q, self.K[l, :, : p + 1], self.V[l, :, : p + 1])
-            h = h + w["w_o"] @ self._act(o.reshape(-1))
-            x = self._act(P.rmsnorm(h, w["g_post"], eps))
-            h = h + w["w_down"] @ self._act(P.swiglu(w["w_gate"] @ x, w["w_up"] @ x))
+            h = h + w["w_o"] @ o.reshape(-1)
+            x = P.rmsnorm(h, w["g_post"], eps)
+            h = h + w["w_down"] @ P.swiglu(w["w_gate"] @ x, w["w_up"] @ x)
         self.pos = p + 1
         return h
 
     def head(self, h) -> np.ndarray:
         """Final RMSNorm and tied vocabulary projection: logits [V]."""
-        return self.E @ self._act(P.rmsnorm(h, self.g_final, self.s.eps))
+        return self.E @ P.rmsnorm(h, self.g_final, self.s.eps)
 
     def step(self, token: int) -> np.ndarray:
         """Full token-to-logits forward at the current position."""
@@ -143,7 +134,7 @@ class OracleDecoder:
         pos = p0 + np.arange(T)
         Hs = self.E[tokens]
         for l, w in enumerate(self.layers):
-            X = self._act(P.rmsnorm(Hs, w["g_in"], eps))
+            X = P.rmsnorm(Hs, w["g_in"], eps)
             Q = (X @ w["w_q"].T).reshape(T, s.n_q, d)
             K = (X @ w["w_k"].T).reshape(T, s.n_kv, d)
             V = (X @ w["w_v"].T).reshape(T, s.n_kv, d)
@@ -152,9 +143,9 @@ class OracleDecoder:
             self.K[l, :, p0 : p0 + T] = self._store(K).transpose(1, 0, 2)
             self.V[l, :, p0 : p0 + T] = self._store(V).transpose(1, 0, 2)
             O = P.causal_prefill_attention(Q, self.K[l, :, : p0 + T], self.V[l, :, : p0 + T], p0)
-            Hs = Hs + self._act(O.reshape(T, -1)) @ w["w_o"].T
-            X = self._act(P.rmsnorm(Hs, w["g_post"], eps))
-            Hs = Hs + self._act(P.swiglu(X @ w["w_gate"].T, X @ w["w_up"].T)) @ w["w_down"].T
+            Hs = Hs + O.reshape(T, -1) @ w["w_o"].T
+            X = P.rmsnorm(Hs, w["g_post"], eps)
+            Hs = Hs + P.swiglu(X @ w["w_gate"].T, X @ w["w_up"].T) @ w["w_down"].T
         self.pos = p0 + T
         return {"logits": {int(r): self.head(Hs[r]) for r in logit_rows}}
 

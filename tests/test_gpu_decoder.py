@@ -25,13 +25,8 @@ def kv_to_np(t):
 ENGINES = ["persistent", "staged"]
 
 
-def rms_within(got, ref, rms_tol, what):
-    rms = float(np.sqrt(np.mean((np.asarray(got, np.float64) - ref) ** 2)))
-    assert rms <= rms_tol, f"{what}: rms difference {rms:.3e} above {rms_tol}"
-
-
 def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every=1, max_seq=None, engine="persistent",
-                    oracle_weights=None, act_round=None, rms_tol=None):
+                    oracle_weights=None):
     import torch
 
     W = lib()
@@ -40,7 +35,7 @@ def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every
     max_seq = max_seq or (len(prompt) + n_out + 4)
     dec = Decoder(shape, weights, kv_dtype=kv_dtype, max_seq=max_seq, engine=engine)
     ora = O.OracleDecoder(shape, oracle_weights if oracle_weights is not None else weights, kv_dtype=kv_dtype,
-                          max_seq=max_seq, act_round=act_round)
+                          max_seq=max_seq)
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
     dec.reset()
     # tokenwise prefill: body only for all but the last prompt token
@@ -55,8 +50,6 @@ def run_and_compare(shape, weights, prompt, n_out, kv_dtype, tol, check_kv_every
         ref = ora.step(cur)
         got = logits.cpu().numpy()
         close(got, ref, tol, f"logits step {j}")
-        if rms_tol is not None:
-            rms_within(got, ref, rms_tol, f"logits step {j}")
         own, ok = O.argmax_lowest(got)
         assert ok and nxt == own, f"step {j}: GPU token {nxt} is not the argmax {own} of its own logits"
         srt = np.sort(ref)[::-1]

@@ -156,46 +156,3 @@ def test_regression_golden_tokens(tiny_weights, golden_dir):
     out = O.generate(m, W.prompt_uniform(8, W.TINY.vocab, seed=0), 8)
     assert out["tokens"] == [int(t) for t in ref["tokens"]]
     np.testing.assert_allclose(out["logits"][0][:16], ref["logits0_head"], rtol=1e-12)
-
-
-
-def test_bf16_input_reading_is_a_small_rounding_of_the_exact_forward():
-    """The 4-bit configuration's reading (each projection's input vector rounded to bfloat16):
-    it changes the logits, by no more than bfloat16 input rounding can, and in the head it is
-    exactly E @ bf16(RMSNorm(h) g)."""
-    s = W.TINY
-    w = W.decoder_weights(s, seed=1)
-    exact = O.OracleDecoder(s, w)
-    rounded = O.OracleDecoder(s, w, act_round="bf16")
-    for t in [int(t) for t in W.prompt_uniform(6, s.vocab, seed=2)]:
-        a, b = exact.step(t), rounded.step(t)
-        diff = np.abs(a - b)
-        assert diff.max() > 0
-        # each rounded input is within 2^-9 relative; the logits move by a few such units of their scale
-        assert diff.max() <= 0.05 * np.abs(a).max()
-    h = np.random.default_rng(3).standard_normal(s.hidden)
-    x = O.rmsnorm(h, O.widen(w["g_final"]), s.eps)
-    np.testing.assert_array_equal(rounded.head(h), O.widen(w["embed"]) @ O.round_to_bf16(x))
-    with pytest.raises(ValueError):
-        O.OracleDecoder(s, w, act_round="fp8")
-
-
-def test_bf16_input_reading_tokenwise_equals_batched_rows(tiny_weights):
-    """Both formulations of the forward round each projection's input at the same places: with the
-    4-bit configuration's reading they agree to float64 rounding (a rounding site missing from
-    either would move them by ~2^-9 relative, as the unrounded control shows)."""
-    prompt = W.prompt_uniform(9, W.TINY.vocab, seed=4)
-    a = O.OracleDecoder(W.TINY, tiny_weights, max_seq=32, act_round="bf16")
-    for t in prompt[:-1]:
-        a.body(t)
-    la = a.step(prompt[-1])
-    b = O.OracleDecoder(W.TINY, tiny_weights, max_seq=32, act_round="bf16")
-    b.prefill(prompt[:3], logit_rows=[])
-    lb = b.prefill(prompt[3:])["logits"][len(prompt) - 4]
-    for l in range(W.TINY.layers):
-        np.testing.assert_allclose(a.kv(l)[0], b.kv(l)[0], rtol=1e-9, atol=1e-12)
-        np.testing.assert_allclose(a.kv(l)[1], b.kv(l)[1], rtol=1e-9, atol=1e-12)
-    np.testing.assert_allclose(la, lb, rtol=1e-9, atol=1e-12)
-    c = O.OracleDecoder(W.TINY, tiny_weights, max_seq=32)
-    lc = c.prefill(prompt)["logits"][len(prompt) - 1]
-    assert np.abs(lc - la).max() > 1e-6

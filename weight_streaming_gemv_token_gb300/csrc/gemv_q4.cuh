@@ -17,10 +17,13 @@
 //    the next launch's CTAs can start their copies beside it.
 //  * Integer dot products. Per chunk and token, x is written in 16-bit fixed
 //    point with the power-of-two step u = 2^(e-14), 2^e <= max|x| < 2^(e+1):
-//    xi = rint(x / u), |xi| <= 32640, split into a signed high byte and an
-//    unsigned low byte (xi = 256 hi + lo). A bfloat16 x whose exponent is at
-//    least e - 7 is represented exactly; smaller ones are within u/2, i.e.
-//    2^-15 of the chunk's largest |x|. The codes need no conversion:
+//    xi = rint(x / u) clamped to [-32768, 32767], split into a signed high
+//    byte and an unsigned low byte (xi = 256 hi + lo). A bfloat16 x whose
+//    exponent is at least e - 7 is represented exactly (|xi| <= 32640, the
+//    clamp never acts); smaller ones are within u/2, i.e. 2^-15 of the
+//    chunk's largest |x|. A float32 x is within u/2 as well, or within u where
+//    the clamp acts (only values within 2^-16 of 2^(e+1)). The codes need no
+//    conversion:
 //    lo = word & 0x0F0F0F0F holds the even columns' codes and
 //    hi = word & 0xF0F0F0F0 16 times the odd columns' codes, one per byte, so
 //    four 4-way byte dot products (dp4a) per word accumulate exact integer sums
@@ -35,10 +38,11 @@
 //  * The rows may come from up to three matrices (segments; the 4-bit decoder
 //    runs Q/K/V, and gate/up, as one launch): each segment gets its own run of
 //    CTAs, in proportion to its rows, and writes its own range of y.
-//  * x prologues (XM): bfloat16 x read as is; float32 x rounded to bfloat16;
-//    x = bf16(RMSNorm(h) * g) from a float32 residual row h; x =
-//    bf16(silu(gate) * up) from float32 gate/up rows. Epilogues: y = W x or
-//    y += W x (residual add).
+//  * x prologues (XM): bfloat16 x read as is (the standalone product); float32
+//    x; x = RMSNorm(h) * g from a float32 residual row h; x = silu(gate) * up
+//    from float32 gate/up rows. The float32 forms go straight into the
+//    fixed-point planes: the decoder's activations are never rounded to a
+//    16-bit float. Epilogues: y = W x or y += W x (residual add).
 //
 // Every mbarrier wait is bounded; on a timeout the CTA raises an abort flag,
 // the producer waits (bounded) for its copies in flight, and the error word
@@ -63,9 +67,9 @@ constexpr int kQ4MaxSegs = 3;
 
 enum Q4X : int {
   Q4X_BF16 = 0,    // x bf16 [ntok][x_ld]
-  Q4X_F32 = 1,     // x f32 [ntok][x_ld], rounded to bfloat16
-  Q4X_NORM = 2,    // x = bf16(h * rsqrt(mean(h^2) + eps) * g), h f32 [ntok][x_ld]
-  Q4X_SWIGLU = 3,  // x = bf16(silu(gu[j]) * gu[in + j]), gu f32 [ntok][x_ld]
+  Q4X_F32 = 1,     // x f32 [ntok][x_ld]
+  Q4X_NORM = 2,    // x = h * rsqrt(mean(h^2) + eps) * g, h f32 [ntok][x_ld]
+  Q4X_SWIGLU = 3,  // x = silu(gu[j]) * gu[in + j], gu f32 [ntok][x_ld]
 };
 
 enum Q4Epi : int {
@@ -116,8 +120,6 @@ struct Q4Launch {
 // F32+ADD, SWIGLU+ADD). DEC_EINVAL when the shape does not fit the bulk kernel.
 dec_status launch_q4_fused(const Q4Launch& q, cudaStream_t st, std::string* err);
 
-__device__ __forceinline__ float q4_round_bf16(float f) { return bf16_to_f32(f32_to_bf16_rn(f)); }
-
 __device__ __forceinline__ void q4_consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kQ4Warps * 32) : "memory");
 }
@@ -135,7 +137,7 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
-// Word m (columns 32 ch + 8 m .. + 7, values xv, already bfloat16 values) of
+// Word m (columns 32 ch + 8 m .. + 7, float32 values xv) of
 // token t's byte planes of chunk ch: four consecutive lanes hold the four words
 // of a chunk and reduce its largest |x| and its sum by shuffles, so every lane
 // of the warp calls this (valid: the item exists).
@@ -160,8 +162,10 @@ __device__ __forceinline__ void q4_item_planes(const float (&xv)[8], int t, int 
   uint32_t he = 0, le = 0, ho = 0, lo = 0;
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    const int xe = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k], 14 - e))) : 0;
-    const int xo = mx > 0.f ? static_cast<int>(rintf(scalbnf(xv[2 * k + 1], 14 - e))) : 0;
+    // |x| < 2^(e+1) puts x / u below 2^15; a float32 x within 2^-16 of that
+    // rounds to 32768, one past the signed 16-bit range, hence the clamp
+    const int xe = mx > 0.f ? min(static_cast<int>(rintf(scalbnf(xv[2 * k], 14 - e))), 32767) : 0;
+    const int xo = mx > 0.f ? min(static_cast<int>(rintf(scalbnf(xv[2 * k + 1], 14 - e))), 32767) : 0;
     he |= (static_cast<uint32_t>(xe >> 8) & 0xFFu) << (8 * k);
     le |= (static_cast<uint32_t>(xe) & 0xFFu) << (8 * k);
     ho |= (static_cast<uint32_t>(xo >> 8) & 0xFFu) << (8 * k);
@@ -286,7 +290,7 @@ __device__ __forceinline__ void q4_stage_x(const void* xp, int x_ld, const float
           for (int j = 0; j < 8; ++j) f[j] = silu_f32(f[j]) * up[j];
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) xv[j] = q4_round_bf16(f[j]);
+        for (int j = 0; j < 8; ++j) xv[j] = f[j];
       }
       q4_item_planes(xv, t, ch, m, nch, valid, xq, xu);
     }

@@ -89,7 +89,11 @@ typedef enum { DEC_F32 = 0, DEC_BF16 = 1, DEC_Q4G64 = 2 } dec_dtype;
  * inside one persistent kernel (one CTA per SM, a producer warp streaming
  * weights through shared memory ahead of the consumers, grid barriers
  * between dependent stages); DEC_ENGINE_STAGED launches the per-stage
- * kernels as a CUDA graph. Both compute the same forward. */
+ * kernels as a CUDA graph. Both compute the same forward. Decode attention
+ * at position p splits the p + 1 cached keys of each key/value head into
+ * nsplit = min(ceil((p + 1) / 64), min(64, SMs / n_kv)) key-parallel ranges
+ * of ceil((p + 1) / nsplit) keys (the last one shorter), whose partial
+ * softmax sums are merged in split order. */
 typedef struct {
   int32_t layers, hidden, inter, n_q, n_kv, head_dim, vocab;
   float eps;        /* RMSNorm epsilon, e.g. 1e-6 */
@@ -128,20 +132,27 @@ typedef struct dec_ctx dec_ctx;
 
 /* Bytes of device workspace dec_create needs for cfg (KV cache, rotary
  * table, activations, argmax and attention partials, prefill scratch).
+ * The cache holds keys and values in the selected dtype ("Megakernels",
+ * "What runs in the DSL"), sized for max_seq positions, i.e. the P + N - 1
+ * entries a generation leaves ("GPU-wide end-to-end generation").
  * Returns 0 if cfg is invalid. */
 size_t dec_workspace_bytes(const dec_config* cfg);
 
-/* Creates a decoder on the current CUDA device. d_workspace (>= 256-byte
- * aligned, at least dec_workspace_bytes(cfg) bytes) must stay allocated
- * until dec_destroy. Builds the rotary table and clears the cache; returns
- * after that work has finished. stream: the stream later calls run on.
+/* Creates a decoder on the current CUDA device ("Megakernels", "What runs
+ * in the DSL": the host precomputes the rotary constants once, before any
+ * forward). d_workspace (>= 256-byte aligned, at least
+ * dec_workspace_bytes(cfg) bytes) must stay allocated until dec_destroy.
+ * Builds the rotary table and clears the cache; returns after that work has
+ * finished. stream: the stream later calls run on.
  * Errors: DEC_EINVAL (cfg, NULL, alignment), DEC_ENOMEM (workspace too
  * small), DEC_EDEVICE (not sm_103), DEC_ECUDA. */
 dec_status dec_create(const dec_config* cfg, void* d_workspace, size_t workspace_bytes, void* stream,
                       dec_ctx** out);
 
-/* Registers the caller's weight tensors (no copy: they must outlive the
- * context). Errors: DEC_EINVAL on a NULL or misaligned pointer. */
+/* Registers the caller's weight tensors ("Megakernels", "What runs in the
+ * DSL": the projections, norm gains and the tied embedding of the forward;
+ * no copy: they must outlive the context). Errors: DEC_EINVAL on a NULL or
+ * misaligned pointer, DEC_ECUDA. */
 dec_status dec_load_weights(dec_ctx* ctx, const dec_weights* w);
 
 /* Position back to 0 and every cache entry invalidated (the cache is
@@ -157,8 +168,10 @@ dec_status dec_reset(dec_ctx* ctx);
  * outside [0, position]), DEC_ECUDA. */
 dec_status dec_rewind(dec_ctx* ctx, int32_t pos);
 
-/* One forward of `token` at the current position p; writes K/V at p and
- * advances the position to p+1.
+/* One forward of `token` at the current position p ("Megakernels", "What
+ * runs in the DSL" for the forward; "GPU-wide end-to-end generation" for the
+ * greedy argmax with lowest-ID ties and the host reading the token ID);
+ * writes K/V at p and advances the position to p+1.
  * Without DEC_SKIP_LOGITS: final RMSNorm, tied vocabulary projection and
  * argmax (lowest ID on ties) run too. d_logits (nullable, float32[vocab])
  * receives the logits; h_next (nullable) receives the greedy token, and
@@ -205,9 +218,11 @@ dec_status dec_prefill_chunk(dec_ctx* ctx, const int32_t* h_tokens, int32_t n, i
  * Errors: DEC_ECAPACITY (p + n > max_seq), DEC_EINVAL, DEC_ESTATE. */
 dec_status dec_generate(dec_ctx* ctx, int32_t token, int32_t n, int32_t* d_tokens_out);
 
-/* Read access to one layer's cache: device pointers to K and V, each laid
- * out [n_kv][max_seq][head_dim] in kvdtype, and the number of valid
- * positions. Keys are stored after Q/K-norm and RoPE, values raw. */
+/* Read access to one layer's cache ("Benchmark methodology", "Long-document
+ * chunked prefill": validation checks every valid K/V entry of every layer):
+ * device pointers to K and V, each laid out [n_kv][max_seq][head_dim] in
+ * kvdtype, and the number of valid positions. Keys are stored after Q/K-norm
+ * and RoPE, values raw. Errors: DEC_EINVAL (NULL, layer out of range). */
 dec_status dec_get_kv(const dec_ctx* ctx, int32_t layer, const void** d_k, const void** d_v, int32_t* n_valid);
 
 /* Current position (number of valid cache entries). -1 if ctx is NULL. */
@@ -229,15 +244,37 @@ int32_t dec_position(const dec_ctx* ctx);
 size_t dec_trace_bytes(const dec_ctx* ctx);
 dec_status dec_set_trace(dec_ctx* ctx, uint64_t* d_trace, size_t bytes);
 
+/* Limit, in nanoseconds, of every wait of the persistent engines on another
+ * CTA's results (exchange words, appended-row counts, grid barriers); 0
+ * restores the default of 2 s. The pages give no API for this: the forward
+ * runs as ordered stages with no host waits between them ("Megakernels",
+ * "GPU-wide end-to-end generation"), so such waits are where a broken
+ * launch would otherwise stall. A wait that runs out makes the launch give
+ * up: the kernel sets DEC_DEVERR_EXCHANGE_TIMEOUT (float engine) or
+ * DEC_DEVERR_BARRIER_TIMEOUT (4-bit engine), waits for its own copies in
+ * flight (those waits keep a fixed 2 s limit) and returns; that call's
+ * outputs, tokens and cache entries are then undefined, and dec_reset
+ * restores a usable state. A limit of a few microseconds makes ordinary
+ * forwards give up, which is how the tests exercise that path. The staged
+ * engine has no such waits. Takes effect at the next launch.
+ * Errors: DEC_EINVAL (NULL). */
+dec_status dec_set_wait_limit(dec_ctx* ctx, uint64_t ns);
+
 /* Synchronizes the context's stream and returns (and, if clear != 0,
  * clears) the device error bits DEC_DEVERR_*. */
 dec_status dec_device_errors(dec_ctx* ctx, int32_t clear, uint32_t* bits);
 
-/* Frees host-side state and CUDA graphs. The workspace stays the caller's. */
+/* Frees host-side state and CUDA graphs. The workspace stays the caller's
+ * (the pages give no API; this is the counterpart of dec_create, which
+ * follows "Megakernels", "What runs in the DSL"). */
 void dec_destroy(dec_ctx* ctx);
 
 /* Message for the last failed call on ctx (ctx == NULL: last failure of a
- * context-free call on this thread). Never NULL. */
+ * context-free call on this thread). Never NULL. The pages give no API; the
+ * calls above report every failure with a status and this message instead
+ * of aborting or continuing silently ("Benchmark methodology", "Long-document
+ * chunked prefill": a failed check discards the whole run rather than
+ * leaving a partial result that looks successful). */
 const char* dec_last_error(const dec_ctx* ctx);
 
 /* y = W x ("Our Kernel Benchmark Was Measuring the System Cache":
@@ -287,8 +324,9 @@ int32_t gemv_q4_rows_per_warp(int32_t ntok, int32_t r);
  * not overlap (they share the count). Errors: DEC_EINVAL, DEC_ECUDA. */
 dec_status pack_bf16_exact(const float* d_src, uint16_t* d_dst, int64_t n, void* stream, int64_t* h_bad);
 
-/* Reads (and if clear != 0 clears) the device error bits of gemv/gemv_q4
- * on the current device; synchronizes the device. */
+/* Reads (and if clear != 0 clears) the device error bits of the
+ * context-free calls (gemv, gemv_q4, gemm_bf16, greedy_head_noalloc) on the
+ * current device; synchronizes the device. */
 dec_status gemv_device_errors(int32_t clear, uint32_t* bits);
 
 /* Greedy head for callers that cannot allocate device memory (the pages have
@@ -305,13 +343,17 @@ dec_status gemv_device_errors(int32_t clear, uint32_t* bits);
  * d_logits float32 [vocab] or NULL; d_token receives the int32 token.
  * Limits: at most 1024 CTAs of argmax partials (vocab x hidden beyond that is
  * rejected with DEC_EINVAL) and hidden small enough for the shared-memory
- * staging. The array persists on every device that loaded the library until
- * exit and is shared by all calls: calls that overlap on the GPU (other
- * streams, other threads) race on it and must be serialised by the caller.
- * The first call on a device looks up the array's address and sets the
- * kernel's shared-memory limit; make that first call before any stream
- * capture. Allocates nothing (no cudaMalloc, cudaFree or allocating library
- * routine). Errors: DEC_EINVAL, DEC_EDEVICE, DEC_ECUDA. */
+ * staging (DEC_EINVAL beyond it). The array persists on every device that
+ * loaded the library until exit and is shared by all calls: calls that
+ * overlap on the GPU (other streams, other threads) race on it and must be
+ * serialised by the caller. The first call on a device looks up the array's
+ * address and sets the kernel's shared-memory limit (under a lock, so first
+ * calls from several host threads are safe); make that first call before any
+ * stream capture. Device-side errors of the call (an all-NaN logit vector,
+ * which returns token 0; a bounded wait that gave up) set bits of the
+ * context-free error word that gemv_device_errors reads and clears.
+ * Allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Errors: DEC_EINVAL, DEC_EDEVICE, DEC_ECUDA. */
 dec_status greedy_head_noalloc(int32_t wdtype, const void* d_embed, const float* d_h, const float* d_gain, float eps,
                                int32_t vocab, int32_t hidden, float* d_logits, int32_t* d_token, void* stream);
 

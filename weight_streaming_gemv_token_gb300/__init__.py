@@ -26,6 +26,7 @@ from .binding import (  # noqa: F401
     dec_reset,
     dec_rewind,
     dec_set_trace,
+    dec_set_wait_limit,
     dec_step,
     dec_trace_bytes,
     dec_verify2,

@@ -30,7 +30,7 @@ EXPORTED = (
     "dec_generate", "dec_get_kv", "dec_position", "dec_trace_bytes", "dec_set_trace", "dec_device_errors",
     "dec_destroy", "dec_last_error",
     "gemv", "gemv_q4", "gemv_q4_rows_per_warp", "gemv_device_errors", "greedy_head_noalloc", "gemm_bf16",
-    "pack_bf16_exact", "dec_verify2",
+    "pack_bf16_exact", "dec_verify2", "dec_set_wait_limit",
 )
 
 
@@ -83,6 +83,7 @@ def library() -> ctypes.CDLL:
             "dec_position": (c_int32, [c_void_p]),
             "dec_trace_bytes": (c_size_t, [c_void_p]),
             "dec_set_trace": (c_int32, [c_void_p, c_void_p, c_size_t]),
+            "dec_set_wait_limit": (c_int32, [c_void_p, ctypes.c_uint64]),
             "dec_device_errors": (c_int32, [c_void_p, c_int32, P(c_uint32)]),
             "dec_destroy": (None, [c_void_p]),
             "dec_last_error": (ctypes.c_char_p, [c_void_p]),
@@ -195,6 +196,10 @@ def dec_trace_bytes(ctx: int) -> int:
 
 def dec_set_trace(ctx: int, d_trace, nbytes: int):
     _check(library().dec_set_trace(ctx, _ptr(d_trace), nbytes), ctx)
+
+
+def dec_set_wait_limit(ctx: int, ns: int):
+    _check(library().dec_set_wait_limit(ctx, int(ns)), ctx)
 
 
 def dec_device_errors(ctx: int, clear: bool = True) -> int:

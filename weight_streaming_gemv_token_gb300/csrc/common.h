@@ -40,9 +40,11 @@ struct DeviceInfo {
   int major = 0, minor = 0;
   size_t smem_optin = 0;
   size_t smem_per_sm = 0;
+  uint32_t* err = nullptr;  // device error word of the context-free entry points on this device
 };
 
-// Properties of the current device (cached per device).
+// Properties of the current device (cached per device; thread-safe), with
+// the device address of the context-free error word.
 dec_status device_info(DeviceInfo* out, std::string* err);
 
 // Launch `kern` with an optional programmatic-dependent-launch edge to the
@@ -71,9 +73,6 @@ cudaError_t allow_smem(K kern, size_t bytes) {
 }
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-// Device error word of the context-free entry points on device `dev`.
-uint32_t* context_free_err_ptr(int dev);
 
 // Tiled TMA descriptor (CUtensorMap, 128 bytes, opaque here) of a row-major
 // [rows][cols] matrix of `elem`-byte elements (2: bfloat16, 4: float32) with

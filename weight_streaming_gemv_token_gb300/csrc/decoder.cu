@@ -214,6 +214,7 @@ struct dec_ctx {
   int mk_grid = 0;
   Q4PArgs q4p{};  // persistent 4-bit kernel: argument template (per-call fields filled at launch)
   size_t q4p_smem = 0;
+  uint64_t xwait_ns = WSG_WAIT_LIMIT_NS;  // persistent engines: limit of a wait on another CTA
   // chunked prefill: tensor maps of the GEMM operands (activation rows: normed
   // input, attention output, SwiGLU output, then their bfloat16 remainders;
   // weights: 7 per layer)
@@ -1091,6 +1092,7 @@ dec_status run_q4_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, 
   a.head_last = head_last ? 1 : 0;
   a.first_tok = first_tok;
   a.host_next = host_next;
+  a.xwait_ns = c->xwait_ns;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c->di.sms);
   cfg.blockDim = dim3(kQ4pThreads);
@@ -1119,6 +1121,7 @@ dec_status run_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, boo
   a.head_every = head_every ? 1 : 0;
   a.head_last = head_last ? 1 : 0;
   a.trace = c->trace;
+  a.xwait_ns = c->xwait_ns;
   c->epoch = c->epoch % 4095 + 1;  // exchange tags never repeat between consecutive launches
   a.epoch = c->epoch;
   if (static_cast<long long>(nsteps) * (c->cfg.layers + 1) * 5 + 1 >= (1ll << 20))
@@ -1396,6 +1399,12 @@ extern "C" dec_status dec_reset(dec_ctx* c) {
   // control words, counters, activations and partials (everything before the layer table)
   WSG_CUDA_TRY(&c->err, cudaMemsetAsync(c->ws, 0, c->L.mk_layers, c->stream));
   WSG_CUDA_TRY(&c->err, cudaMemsetAsync(c->ws + c->L.kc, 0, c->L.total - c->L.kc, c->stream));
+  return DEC_OK;
+}
+
+extern "C" dec_status dec_set_wait_limit(dec_ctx* c, uint64_t ns) {
+  if (!c) return fail(nullptr, DEC_EINVAL, "dec_set_wait_limit: NULL context");
+  c->xwait_ns = ns == 0 ? WSG_WAIT_LIMIT_NS : ns;
   return DEC_OK;
 }
 

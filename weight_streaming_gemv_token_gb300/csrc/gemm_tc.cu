@@ -153,5 +153,5 @@ extern "C" dec_status gemm_bf16(const uint16_t* d_A, const uint16_t* d_W, float*
   if ((s = encode_gemm_operand(mb, d_W, N, K, bn, nullptr)) != DEC_OK) return s;
   const void* mbs[1] = {mb};
   return launch_gemm_bf16(ma, nullptr, mbs, nullptr, 1, bn, d_C, ldc, 0, M, N, K, accumulate != 0,
-                          context_free_err_ptr(di.device), static_cast<cudaStream_t>(stream), nullptr);
+                          di.err, static_cast<cudaStream_t>(stream), nullptr);
 }

@@ -23,6 +23,10 @@ std::string& thread_error() {
   return s;
 }
 
+// Device error word of the context-free entry points (gemv, gemv_q4,
+// gemm_bf16, greedy_head_noalloc); gemv_device_errors reads and clears it.
+__device__ uint32_t g_gemv_err;
+
 dec_status device_info(DeviceInfo* out, std::string* err) {
   static std::mutex mu;
   static DeviceInfo cache[64];
@@ -36,28 +40,18 @@ dec_status device_info(DeviceInfo* out, std::string* err) {
     if (p.major != 10 || p.minor != 3)
       return fail(err, DEC_EDEVICE, "device %d is sm_%d%d; this library is built for sm_103a", dev, p.major,
                   p.minor);
-    cache[dev].device = dev;
+    void* ew = nullptr;
+    WSG_CUDA_TRY(err, cudaGetSymbolAddress(&ew, g_gemv_err));
     cache[dev].sms = p.multiProcessorCount;
     cache[dev].major = p.major;
     cache[dev].minor = p.minor;
     cache[dev].smem_optin = p.sharedMemPerBlockOptin;
     cache[dev].smem_per_sm = p.sharedMemPerMultiprocessor;
+    cache[dev].err = static_cast<uint32_t*>(ew);
+    cache[dev].device = dev;  // last: marks the entry complete
   }
   *out = cache[dev];
   return DEC_OK;
-}
-
-// Device error word of the context-free entry points.
-__device__ uint32_t g_gemv_err;
-
-// Address of the device error word on device `dev` (looked up once).
-uint32_t* context_free_err_ptr(int dev) {
-  static uint32_t* ptrs[64] = {};
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_gemv_err) == cudaSuccess) ptrs[dev] = static_cast<uint32_t*>(p);
-  }
-  return ptrs[dev];
 }
 
 namespace {
@@ -65,8 +59,6 @@ namespace {
 constexpr int kNW = 8, kNSMAX = 8, kRING = 12288, kSEGMAX = 4096;
 // Matrices up to this size are prefetched into L2 whole at kernel start.
 constexpr long long kL2PrefetchMax = 64ll << 20;
-
-uint32_t* gemv_err_ptr(int dev) { return context_free_err_ptr(dev); }
 
 // Lift a kernel's dynamic shared memory limit to the device maximum, once per device.
 template <typename K>
@@ -379,7 +371,7 @@ dec_status launch_q4_bulk(int R, const uint32_t* codes, const uint16_t* s, const
   q.in = in;
   q.ntok = NTOK;
   q.pdl = true;
-  q.err = gemv_err_ptr(di.device);
+  q.err = di.err;
   if (!q.err) return fail(nullptr, DEC_ECUDA, "gemv_q4: device error word unavailable");
   return launch_q4_bulk_x<NTOK, Q4X_BF16, Q4E_STORE>(R, q, st, di, nullptr, used);
 }
@@ -479,7 +471,7 @@ dec_status launch_gemv_tma(const void* W, const void* x, float* y, int out, int 
   a.in = in;
   a.gm = gm;
   a.ring_bytes = static_cast<int>(ring);
-  a.err = gemv_err_ptr(di.device);
+  a.err = di.err;
   if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv: device error word unavailable");
   WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(G), dim3(kGtThreads), smem, st, true, map, a));
   *used = true;
@@ -535,7 +527,7 @@ dec_status launch_gemv_bulk_r(const void* W, const void* x, float* y, int out, i
   a.nstages = static_cast<int>(S);
   a.srows = static_cast<int>(srows);
   a.stage_bytes = static_cast<uint32_t>(stage);
-  a.err = gemv_err_ptr(di.device);
+  a.err = di.err;
   if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv: device error word unavailable");
   const size_t smem = static_cast<size_t>(S * stage + xbytes + 2 * S * 8);
   WSG_CUDA_TRY(nullptr, launch_k(kern, dim3(G), dim3(kGbThreads), smem, st, true, a));
@@ -606,7 +598,7 @@ dec_status launch_gemv(const void* W, const void* x, float* y, int out, int in, 
     if (smem <= di.smem_optin) {
       auto kern = gemv_stream_kernel<WT, XT, PRO_X, EPI_STORE, kNW, kNSMAX, kRING>;
       static bool done[64] = {};
-      a.err = gemv_err_ptr(di.device);
+      a.err = di.err;
       if (!a.err) return fail(nullptr, DEC_ECUDA, "gemv: device error word unavailable");
       a.y = y;
       a.l2_prefetch = static_cast<long long>(out) * row_bytes <= kL2PrefetchMax;

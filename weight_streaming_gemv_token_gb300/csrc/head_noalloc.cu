@@ -9,6 +9,8 @@
 // needs scratch for the per-CTA argmax partials, the last-CTA counter and a
 // position word; here the scratch is a file-scope device array instead of a
 // caller-provided workspace.
+#include <mutex>
+
 #include "common.h"
 #include "gemv_stream.cuh"
 
@@ -18,21 +20,27 @@ namespace {
 constexpr int kNW = 8, kNSMAX = 8, kRING = 12288, kSEGMAX = 4096;
 
 // Scratch layout: argmax partial values [kMaxCtas] float, partial indices
-// [kMaxCtas] int32, then counter, position word, error word, and two token slots.
+// [kMaxCtas] int32, then counter, position word and two token slots. Device
+// errors go to the context-free error word (gemv_device_errors).
 constexpr int kMaxCtas = 1024;
 constexpr size_t kOffIdx = sizeof(float) * kMaxCtas;
 constexpr size_t kOffCounter = kOffIdx + sizeof(int32_t) * kMaxCtas;
 constexpr size_t kOffCtrl = kOffCounter + 4;
-constexpr size_t kOffErr = kOffCtrl + 4;
-constexpr size_t kOffTok = kOffErr + 4;
+constexpr size_t kOffTok = kOffCtrl + 4;
 constexpr size_t kScratchBytes = ((kOffTok + 8) + 255) / 256 * 256;  // 8448 bytes per device
 
 static __device__ __align__(256) unsigned char g_head_scratch[kScratchBytes];
 
+constexpr int kMaxDevices = 64;
+
 struct DeviceSetup {
   unsigned char* scratch = nullptr;  // device address of g_head_scratch
+  size_t smem_limit[2] = {0, 0};     // dynamic shared memory lifted for the float32 / bfloat16 kernel
   bool ready = false;
 };
+
+std::mutex g_setup_mu;
+DeviceSetup g_setup[kMaxDevices];
 
 }  // namespace
 }  // namespace wsg
@@ -55,32 +63,43 @@ extern "C" dec_status greedy_head_noalloc(int32_t wdtype, const void* d_embed, c
   dec_status st = device_info(&di, nullptr);
   if (st != DEC_OK) return st;
 
-  // One-time set-up per device (on the first call with that device current):
-  // the scratch's device address and the kernel's shared-memory limit.
-  static DeviceSetup setup[64];
-  DeviceSetup& ds = setup[di.device];
-  auto kern = wdtype == DEC_F32 ? gemv_stream_kernel<float, float, PRO_NORM, EPI_ARGMAX, kNW, kNSMAX, kRING>
-                                : gemv_stream_kernel<uint16_t, float, PRO_NORM, EPI_ARGMAX, kNW, kNSMAX, kRING>;
-  if (!ds.ready) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_head_scratch);
-    if (e != cudaSuccess)
-      return fail(nullptr, DEC_ECUDA, "greedy_head_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
-    // dynamic limit = device maximum minus the kernel's static shared memory
-    auto lift = [&](auto k) {
-      cudaFuncAttributes fa{};
-      cudaError_t r = cudaFuncGetAttributes(&fa, k);
-      if (r != cudaSuccess) return r;
-      return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(di.smem_optin - fa.sharedSizeBytes));
-    };
-    e = lift(gemv_stream_kernel<float, float, PRO_NORM, EPI_ARGMAX, kNW, kNSMAX, kRING>);
-    if (e == cudaSuccess) e = lift(gemv_stream_kernel<uint16_t, float, PRO_NORM, EPI_ARGMAX, kNW, kNSMAX, kRING>);
-    if (e != cudaSuccess)
-      return fail(nullptr, DEC_ECUDA, "greedy_head_noalloc: cudaFuncSetAttribute failed: %s", cudaGetErrorString(e));
-    ds.scratch = static_cast<unsigned char*>(p);
-    ds.ready = true;
+  // One-time set-up per device (on the first call with that device current),
+  // under a lock so that first calls from several host threads are safe: the
+  // scratch's device address and the kernels' shared-memory limits.
+  if (di.device < 0 || di.device >= kMaxDevices)
+    return fail(nullptr, DEC_EDEVICE, "greedy_head_noalloc: device ordinal %d out of range", di.device);
+  using KernT = void (*)(GemvArgs);
+  const KernT kerns[2] = {gemv_stream_kernel<float, float, PRO_NORM, EPI_ARGMAX, kNW, kNSMAX, kRING>,
+                          gemv_stream_kernel<uint16_t, float, PRO_NORM, EPI_ARGMAX, kNW, kNSMAX, kRING>};
+  const int ki = wdtype == DEC_F32 ? 0 : 1;
+  DeviceSetup ds;
+  {
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    DeviceSetup& slot = g_setup[di.device];
+    if (!slot.ready) {
+      void* p = nullptr;
+      cudaError_t e = cudaGetSymbolAddress(&p, g_head_scratch);
+      if (e != cudaSuccess)
+        return fail(nullptr, DEC_ECUDA, "greedy_head_noalloc: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+      // dynamic limit = device maximum minus the kernel's static shared memory
+      size_t lim[2];
+      for (int k = 0; k < 2; ++k) {
+        cudaFuncAttributes fa{};
+        e = cudaFuncGetAttributes(&fa, kerns[k]);
+        lim[k] = di.smem_optin - fa.sharedSizeBytes;
+        if (e == cudaSuccess)
+          e = cudaFuncSetAttribute(kerns[k], cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(lim[k]));
+        if (e != cudaSuccess)
+          return fail(nullptr, DEC_ECUDA, "greedy_head_noalloc: kernel set-up failed: %s", cudaGetErrorString(e));
+      }
+      slot.scratch = static_cast<unsigned char*>(p);
+      slot.smem_limit[0] = lim[0];
+      slot.smem_limit[1] = lim[1];
+      slot.ready = true;
+    }
+    ds = slot;
   }
+  const KernT kern = kerns[ki];
 
   // Launch shape (same plan as the decoder's head).
   int spr = static_cast<int>((row_bytes + kSEGMAX - 1) / kSEGMAX);
@@ -96,9 +115,9 @@ extern "C" dec_status greedy_head_noalloc(int32_t wdtype, const void* d_embed, c
     return fail(nullptr, DEC_EINVAL, "greedy_head_noalloc: vocab %d x hidden %d needs more than %d CTAs of scratch",
                 vocab, hidden, kMaxCtas);
   const size_t smem = gemv_smem_bytes(gemv_ring_bytes<kNW, kNSMAX, kRING>(), hidden, max_rows, spr);
-  if (smem > di.smem_optin)
+  if (smem > ds.smem_limit[ki])
     return fail(nullptr, DEC_EINVAL, "greedy_head_noalloc: hidden %d needs %zu B of shared memory (max %zu)", hidden,
-                smem, di.smem_optin);
+                smem, ds.smem_limit[ki]);
 
   GemvArgs a = {};
   a.w.base[0] = a.w.base[1] = a.w.base[2] = static_cast<const char*>(d_embed);
@@ -118,7 +137,7 @@ extern "C" dec_status greedy_head_noalloc(int32_t wdtype, const void* d_embed, c
   a.part_idx = reinterpret_cast<int32_t*>(ds.scratch + kOffIdx);
   a.counter = reinterpret_cast<uint32_t*>(ds.scratch + kOffCounter);
   a.ctrl = reinterpret_cast<int32_t*>(ds.scratch + kOffCtrl);
-  a.err = reinterpret_cast<uint32_t*>(ds.scratch + kOffErr);
+  a.err = di.err;
   a.tok_w = reinterpret_cast<int32_t*>(ds.scratch + kOffTok);
   a.l2_prefetch = 0;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

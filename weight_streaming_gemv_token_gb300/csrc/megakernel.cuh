@@ -138,6 +138,7 @@ struct MkArgs {
   int32_t first_tok;   // >= 0: the first step's token (else read from tok[pos0])
   int32_t* host_next;  // optional (host memory mapped to the device): the last step's greedy token
   uint64_t* trace;  // optional: [G][L + 1][5][4] globaltimer stamps of the first forward
+  uint64_t xwait_ns;  // limit of a wait for another CTA's words (exchange words, cache counts)
 };
 
 // Trace points per stage: entry, activations staged, segments consumed, barrier passed.
@@ -365,18 +366,24 @@ __device__ __forceinline__ uint64_t ll_load(const uint64_t* p) {
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// Whether a bounded poll reads the clock in its round r: in round 1 (by then
+// at least one load has followed the start time) and every 64th round after,
+// so a limit shorter than a round trip ends any wait that one reload did not
+// satisfy.
+__device__ __forceinline__ bool poll_check_due(int r) { return r == 1 || (r & 63) == 63; }
+
 // Value of an exchange word once its tag is `tag`; bounded poll. On timeout
 // raises the abort flag, records the error and returns 0.
 __device__ __forceinline__ float ll_wait(const uint64_t* p, uint32_t tag, uint64_t w, volatile int* abort,
-                                         uint32_t* err) {
+                                         uint32_t* err, uint64_t limit_ns) {
   if (static_cast<uint32_t>(w >> 32) == tag) return __uint_as_float(static_cast<uint32_t>(w));
   const uint64_t t0 = globaltimer_ns();
   for (int it = 0;; ++it) {
     w = ll_load(p);
     if (static_cast<uint32_t>(w >> 32) == tag) return __uint_as_float(static_cast<uint32_t>(w));
-    if ((it & 63) == 63) {
+    if (poll_check_due(it)) {
       if (*abort) return 0.f;
-      if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicOr(err, ERR_EXCHANGE_TIMEOUT);
         return 0.f;
@@ -397,6 +404,7 @@ struct AttnLlIo {
   uint32_t tag_in, tag_out;
   volatile int* abort;
   uint32_t* err;
+  uint64_t wait_ns;      // limit of a wait for another CTA's words
   uint64_t* trace_slot;  // this CTA's [4] stamps of the stage, or NULL
   __device__ __forceinline__ void mark(int ev) const {
     if (trace_slot) trace_slot[ev] = globaltimer_ns();
@@ -416,9 +424,9 @@ struct AttnLlIo {
 #pragma unroll
       for (int k = 0; k < N; ++k) stale |= static_cast<uint32_t>(w[k] >> 32) != tag;
       if (!stale) break;
-      if ((round & 63) == 63) {
+      if (poll_check_due(round)) {
         if (*abort) break;
-        if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > wait_ns) {
           *abort = 1;
           atomicOr(err, ERR_EXCHANGE_TIMEOUT);
           break;
@@ -476,15 +484,16 @@ struct AttnLlIo {
 };
 
 // Bounded wait until *p >= v, with acquire semantics.
-__device__ __forceinline__ bool wait_at_least(const uint32_t* p, uint32_t v, volatile int* abort, uint32_t* err) {
+__device__ __forceinline__ bool wait_at_least(const uint32_t* p, uint32_t v, volatile int* abort, uint32_t* err,
+                                              uint64_t limit_ns) {
   const uint64_t t0 = globaltimer_ns();
   for (int it = 0;; ++it) {
     uint32_t x;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(x) : "l"(p) : "memory");
     if (x >= v) return true;
-    if ((it & 63) == 63) {
+    if (poll_check_due(it)) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicOr(err, ERR_EXCHANGE_TIMEOUT);
         return false;
@@ -761,9 +770,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
 #pragma unroll
         for (int k = 0; k < K; ++k) stale |= static_cast<uint32_t>(wv[k] >> 32) != tag;
         if (!stale) break;
-        if ((round & 63) == 63) {
+        if (poll_check_due(round)) {
           if (*vabort) break;
-          if (globaltimer_ns() - t0 > WSG_WAIT_LIMIT_NS) {
+          if (globaltimer_ns() - t0 > a.xwait_ns) {
             *vabort = 1;
             atomicOr(a.err, ERR_EXCHANGE_TIMEOUT);
             break;
@@ -967,7 +976,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     int tok;
     if (step > 0 && a.head_every) {
       const uint64_t* p = a.ll_tok;
-      tok = __float_as_int(ll_wait(p, mk_tag(a, step - 1, a.L, 0), ll_load(p), vabort, a.err));
+      tok = __float_as_int(ll_wait(p, mk_tag(a, step - 1, a.L, 0), ll_load(p), vabort, a.err, a.xwait_ns));
     } else if (step == 0 && a.first_tok >= 0) {
       tok = a.first_tok;  // passed with the launch: no copy ahead of it
       if (c == 0 && tid == 0) a.tok[pos] = tok;
@@ -985,7 +994,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
       // rows of h) before writing anything.
       for (int i = tid; i < a.H; i += kMkConsumers) {
         const uint64_t* p = a.ll_h + i;
-        ll_wait(p, mk_tag(a, step - 1, a.L - 1, MK_DOWN), ll_load(p), vabort, a.err);
+        ll_wait(p, mk_tag(a, step - 1, a.L - 1, MK_DOWN), ll_load(p), vabort, a.err, a.xwait_ns);
       }
       consumer_sync();
     }
@@ -1009,7 +1018,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? kAttnChunk<KT> / 2 : 8), AttnLlIo>(
               at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
               AttnLlIo{a.ll_qkv, a.ll_attn, a.ll_apart, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV),
-                       mk_tag(a, step, l, 1), vabort, a.err,
+                       mk_tag(a, step, l, 1), vabort, a.err, a.xwait_ns,
                        (a.trace && step == 0)
                            ? a.trace + ((static_cast<size_t>(c) * (a.L + 1) + l) * kMkTraceStages + 1) * kMkTraceEvents
                            : nullptr});
@@ -1041,7 +1050,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           // Keys and values before pos do not depend on this token: make sure the
           // rows of earlier positions are published (acquire) and pull this
           // CTA's attention range of them into L2 while QKV runs.
-          if (pos > 0) wait_at_least(a.kv_ready + l * a.n_kv + c % a.n_kv, static_cast<uint32_t>(pos), vabort, a.err);
+          if (pos > 0)
+            wait_at_least(a.kv_ready + l * a.n_kv + c % a.n_kv, static_cast<uint32_t>(pos), vabort, a.err, a.xwait_ns);
           int t0, t1, ns;
           if (attn_split_range(a.at, c / a.n_kv, pos, &t0, &t1, &ns)) {
             t1 = min(t1, pos);

@@ -89,6 +89,7 @@ struct Q4PArgs {
   uint32_t stage_bytes;    // multiple of 128
   uint32_t attn_bytes;     // attention scratch in shared memory (multiple of 16)
   uint32_t* err;
+  uint64_t xwait_ns;       // limit of a grid-barrier wait
 };
 
 // Threads 0..255 of every CTA; ends with all of this CTA's consumers past the
@@ -96,28 +97,26 @@ struct Q4PArgs {
 // first: it is set from the first arrival). Returns false if the barrier (or
 // another CTA) gave up.
 __device__ __forceinline__ bool q4p_grid_sync(unsigned long long* bar, unsigned long long G, unsigned long long& target,
-                                              volatile int* vabort, uint32_t* err, int tid) {
+                                              volatile int* vabort, uint32_t* err, int tid, uint64_t limit_ns) {
   q4_consumer_sync();
   if (tid == 0 && !*vabort) {
     unsigned long long old;
     asm volatile("atom.add.release.gpu.global.u64 %0, [%1], 1;" : "=l"(old) : "l"(bar) : "memory");
     if (target == 0) target = old - old % G;  // the launch's base
     target += G;
-    uint64_t t0 = 0;
+    const uint64_t t0 = globaltimer_ns();
     for (int it = 0;; ++it) {
       unsigned long long v;
       asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(bar) : "memory");
       if (v >= target) break;
-      if ((it & 63) == 63) {
+      if (it == 1 || (it & 63) == 63) {  // the clock on the first re-poll, then every 64th
         unsigned long long ab;
         asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(ab) : "l"(bar + 1) : "memory");
         if (ab) {
           *vabort = 1;
           break;
         }
-        const uint64_t now = globaltimer_ns();
-        if (t0 == 0) t0 = now;
-        if (now - t0 > WSG_WAIT_LIMIT_NS) {
+        if (globaltimer_ns() - t0 > limit_ns) {
           atomicOr(err, ERR_GRID_BARRIER_TIMEOUT);
           atomicExch(bar + 1, 1ull);
           *vabort = 1;
@@ -252,7 +251,7 @@ __global__ void __launch_bounds__(kQ4pThreads, 1) q4_persist_kernel(const Q4PArg
       }
     }
   };
-  auto sync_all = [&]() { ok = ok && q4p_grid_sync(a.bar, static_cast<unsigned long long>(G), target, vabort, a.err, tid); };
+  auto sync_all = [&]() { ok = ok && q4p_grid_sync(a.bar, static_cast<unsigned long long>(G), target, vabort, a.err, tid, a.xwait_ns); };
 
   const int attn_ctas = a.at.n_kv * a.at.nsplit_max;
   int gi = 0;  // the previous step's greedy token

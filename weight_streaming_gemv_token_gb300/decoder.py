@@ -151,5 +151,9 @@ class Decoder:
 
         return view(k), view(v), n
 
+    def set_wait_limit(self, ns: int):
+        """Limit of the persistent engines' waits on other CTAs (0: the 2 s default)."""
+        B.dec_set_wait_limit(self.ctx, ns)
+
     def device_errors(self, clear: bool = True) -> int:
         return B.dec_device_errors(self.ctx, clear)

@@ -45,15 +45,14 @@ import workloads as Wl  # noqa: E402
 
 METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 
-# DRAM traffic of the persistent decode kernel per algorithmic byte, from ncu on a
-# 4-layer / 32768-vocabulary case of the same widths (profiles/decode_megakernel_small_full.md):
-# (387,484,160 read + 2,817,280 written) / 387,186,688 algorithmic bytes; the excess is the
-# rows a tiled box reads past a CTA's row range. Set to None when the kernel changes until it
-# is measured again.
+# DRAM traffic of the persistent decode kernel per algorithmic byte, from an ncu capture of a
+# 4-layer / 32768-vocabulary case of the same widths: (387,484,160 read + 2,817,280 written) /
+# 387,186,688 algorithmic bytes; the excess is the rows a tiled box reads past a CTA's row range.
+# Set to None when the kernel changes until it is measured again.
 MK_TRAFFIC_PER_ALG_BYTE = (387497216 + 2738688) / 387186688
 # DRAM bytes (read + written) per launch of the standalone gemv bulk-copy kernel at 151936x1024 f32
-# (the tied vocabulary shape), from ncu (profiles/gemv_bulk_151936x1024.md: 622,377,984 B read +
-# 3,492,352 B written); None until measured for the current kernel.
+# (the tied vocabulary shape), from an ncu capture: 622,377,984 B read + 3,492,352 B written; None
+# until measured for the current kernel.
 GEMV_TRAFFIC = 622377984 + 3492352
 GEMV_ROOF_SHAPE = (151936, 1024)
 PROMPT = 32
@@ -591,14 +590,14 @@ def gpu_arm(args):
                 "peak_kind": peak_kind, "kernel": "decode_megakernel<float,float,2> (one cooperative launch, K steps)",
                 "bytes_per_launch": step_bytes * K, "launch_us": round(sec * 1e6, 1), "launches": 1,
                 "traffic_source": "ncu dram bytes of a 4-layer/32768-vocab case of the same widths, scaled by "
-                                  "algorithmic bytes (profiles/decode_megakernel_small_full.md)"}
+                                  "algorithmic bytes"}
         # the standalone GEMV alone at the tied-vocabulary shape (the step's largest product), cold
         o, i = GEMV_ROOF_SHAPE
         gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", o, i, stream, gen=gen)
         extra["roofline" if args.engine != "persistent" else "gemv_roofline"] = {
             "bound": "hbm", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4),
             # ncu dram__bytes_read+write per launch of this kernel on this shape; None until measured
-            # for the current kernel (profiles/gemv_bulk_151936x1024.md)
+            # for the current kernel
             "traffic": GEMV_TRAFFIC, "peak_kind": peak_kind,
             "kernel": f"gemv_bulk_kernel<float,1> {o}x{i} (tied vocabulary shape), standalone gemv entry, "
                       "cold round-robin",

@@ -3,9 +3,9 @@
 Use under ncu with --profile-from-start off, e.g.
 
   ncu --profile-from-start off --metrics gpu__time_duration.sum --clock-control none --csv \\
-      python -m weight_streaming_gemv_token_gb300.profile_step decode --steps 1
+      python profile_step.py decode --steps 1
   ncu --profile-from-start off --set full --clock-control none -k regex:gemv_stream -c 3 -o prof \\
-      python -m weight_streaming_gemv_token_gb300.profile_step gemv --out 6144 --in 1024 --count 8
+      python profile_step.py gemv --out 6144 --in 1024 --count 8
 
 decode: Qwen3-0.6B-shaped decoder (optionally fewer layers / a smaller
         vocabulary, for captures that must stay small; --dtype q4 with
@@ -27,7 +27,7 @@ import sys
 
 import torch
 
-ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
@@ -35,8 +35,8 @@ if ROOT not in sys.path:
 def decode(args):
     import workloads as Wl
 
-    from . import build
-    from .decoder import Decoder
+    from weight_streaming_gemv_token_gb300 import build
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
 
     build.build()
     s = Wl.QWEN3_06B
@@ -66,8 +66,8 @@ def decode(args):
 
 
 def gemv(args):
-    from . import binding as B
-    from . import build
+    from weight_streaming_gemv_token_gb300 import binding as B
+    from weight_streaming_gemv_token_gb300 import build
 
     build.build()
     g = torch.Generator(device="cuda")
@@ -90,8 +90,8 @@ def gemv(args):
 
 
 def q4(args):
-    from . import binding as B
-    from . import build
+    from weight_streaming_gemv_token_gb300 import binding as B
+    from weight_streaming_gemv_token_gb300 import build
 
     build.build()
     g = torch.Generator(device="cuda")
@@ -125,8 +125,8 @@ def prefill(args):
 
     import workloads as Wl
 
-    from . import build
-    from .decoder import Decoder
+    from weight_streaming_gemv_token_gb300 import build
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
 
     build.build()
     s = Wl.QWEN3_06B

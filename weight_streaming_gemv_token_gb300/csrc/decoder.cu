@@ -1,8 +1,8 @@
-// Decoder runtime: the batch-1 token-to-logits forward as one CUDA graph.
+// Decoder runtime: the batch-1 token-to-logits forward, on two engines.
 //
 // Step structure ("Megakernels", "GPU-wide end-to-end generation" lists eight
 // ordered stages per layer plus embedding, final norm and vocabulary
-// projection, then two argmax passes). Here fusion leaves five kernels per
+// projection, then two argmax passes). Here fusion leaves five stages per
 // layer and one for the head:
 //
 //   layer l:  QKV GEMV      (input RMSNorm fused as prologue; layer 0 also
@@ -14,10 +14,15 @@
 //   head:     vocab GEMV    (final RMSNorm prologue; logits; both argmax
 //                            passes; next token and position advance)
 //
-// Token and position live in device memory, so the same instantiated graph
-// replays for every step. Kernels after the first carry a programmatic
-// dependent-launch edge: each GEMV starts streaming its weights while its
-// predecessor finishes, and waits only before reading activations.
+// The persistent engine (the default) runs these stages for any number of
+// forwards inside one cooperative launch (megakernel.cuh; q4_persist.cuh for
+// 4-bit weights). The staged engine launches one kernel per stage, captured
+// once as a CUDA graph: token and position live in device memory, so the same
+// instantiated graph replays for every step, and kernels after the first
+// carry a programmatic dependent-launch edge, so each GEMV starts streaming
+// its weights while its predecessor finishes and waits only before reading
+// activations. Chunked prefill (prefill.cuh, gemm_tc.cuh) runs prompt rows
+// together on the tensor cores.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -309,6 +309,41 @@ def fixed_context_latency(dec, torch, s, stream, contexts=(0, 16, 64), trials=9,
     return res
 
 
+def generation_timings(dec, torch, s, pairs=((8, 8), (8, 16), (32, 8), (32, 16)), warm=2, trials=5):
+    """Greedy generation timed the pages' way ("Megakernels", "GPU-wide end-to-end generation";
+    "Benchmark methodology", "Median of paired per-trial ratios"): from before the cache reset to
+    the final token ID on the host, with the host reading every token (dec_step). TTFT ends when
+    the first output (from the final prompt row) is on the host; the decode rate uses the N - 1
+    forwards after it. Two warm-up generations, then the median of five trials, each of which must
+    reproduce the warm-up's token IDs."""
+    res = {}
+    for P, N in pairs:
+        prompt = [int(t) for t in Wl.prompt_uniform(P, s.vocab, seed=0)]
+        ref, tt, tot, rate = None, [], [], []
+        for i in range(warm + trials):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            dec.reset()
+            cur = dec.prefill(prompt, is_last=True)
+            t1 = time.perf_counter()
+            toks = [cur]
+            for _ in range(N - 1):
+                cur = dec.step(cur)
+                toks.append(cur)
+            t2 = time.perf_counter()
+            if ref is None:
+                ref = toks
+            assert toks == ref, f"generation {P}/{N}: a trial changed its token IDs"
+            if i >= warm:
+                tt.append((t1 - t0) * 1e3)
+                tot.append((t2 - t0) * 1e3)
+                rate.append((N - 1) / (t2 - t1))
+        res[f"{P}/{N}"] = {"ttft_ms": round(statistics.median(tt), 3), "total_ms": round(statistics.median(tot), 3),
+                           "decode_tokens_per_s": round(statistics.median(rate), 1), "trials": trials,
+                           "outputs": len(ref)}
+    return res
+
+
 def time_q4_cold_rows(W, torch, out, inp, stream, ntok, rows_options, rounds=5, min_bytes=1 << 30, gen=None):
     """Cold GB/s of gemv_q4 for each rows-per-warp setting on one set of >= 1 GiB of distinct
     packed matrices (each setting captured in its own graph); {R: (GB/s, bytes per launch, avg s)}."""
@@ -509,6 +544,39 @@ def q4_engine(W, torch, stream, hbm, w, engine, steps, verifies):
     }
 
 
+def summary(line):
+    """The line's figures in a few hundred characters: fractions of the measured peak per GEMV
+    shape (in the order of workloads.GEMV_SHAPES), the generation timings (TTFT ms, total ms,
+    decode tokens/s), the 4-bit and chunked-prefill configurations and the oracle on the CPU."""
+    def r3(v):
+        return None if v is None else round(v, 3)
+
+    out = {"tok_s": line["value"], "step_frac": line["step_roofline"]["frac"], "e2e_tok_s": line["e2e"]["value"]}
+    g = line.get("gemv_cold")
+    if g:
+        for dt, key in (("f32", "f32"), ("bf16", "bf16"), ("q4 ntok=1", "q4n1"), ("q4 ntok=2", "q4n2")):
+            out[f"gemv_frac_{key}"] = [r3(g.get(f"{dt} {o}x{i}", {}).get("frac")) for (o, i) in Wl.GEMV_SHAPES]
+    gen = line.get("generation")
+    if gen:
+        out["gen_ttft_total_rate"] = {k: [v["ttft_ms"], v["total_ms"], v["decode_tokens_per_s"]] for k, v in gen.items()}
+    q = line.get("q4_decoder")
+    if q:
+        pe = q.get("persistent_engine", {})
+        out["q4"] = {"staged_tok_s": q["decode_tokens_per_s"], "staged_frac": q["frac"],
+                     "persistent_tok_s": pe.get("decode_tokens_per_s"), "persistent_frac": pe.get("frac"),
+                     "verify2_ms": q["verify2"]["ms_per_call"]}
+    p = line.get("prefill")
+    if p:
+        h = p["held_out"]
+        out["prefill"] = {"chunk": p["chunk"], "ttft_ms": h["ttft_ms"], "decode_tok_s": h["decode_tokens_per_s"],
+                          "decode_frac": h["decode_step_roofline_frac"], "tflops": h["prefill_tflops_algorithmic"]}
+    c = line.get("cpu_baseline")
+    if c:
+        one = c.get("one_core") or {}
+        out["cpu"] = {"tok_s": c["value"], "tok_s_1core": one.get("decode_tokens_per_s"), "cores": c["cores"]}
+    return out
+
+
 def gpu_arm(args):
     import torch
 
@@ -572,6 +640,7 @@ def gpu_arm(args):
     e2e_sec = barrier_max(max(wall, f0.elapsed_time(f1) / 1e3), ws)
     e2e_value = ws * n_e2e / e2e_sec
     fixed = fixed_context_latency(dec, torch, s, stream)
+    generation = generation_timings(dec, torch, s)
     dec.close()
     del dec
     torch.cuda.empty_cache()
@@ -647,11 +716,13 @@ def gpu_arm(args):
             "e2e": {"value": round(e2e_value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 4,
                     "d2h_bytes_per_step": 4, "steps": n_e2e},
             "fixed_context": fixed,
+            "generation": generation,
             "gpu_launches": 1 if args.engine == "persistent" else K * (5 * s.layers + 1),
             "clocks": clk.summary(),
             "cpu_baseline": cpu,
         }
         line.update(extra)
+        line["summary"] = summary(line)  # last, so that a tail of the line keeps it
         print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist
@@ -661,25 +732,83 @@ def gpu_arm(args):
 
 # ---------------------------------------------------------------- CPU side ----
 
-def cpu_baseline_sample(weights, prompt, budget_s=15.0, min_tokens=3):
-    """The oracle's decode rate on the host cores: a bounded number of tokens after a short prompt."""
+def oracle_decode_rate(weights, prompt, budget_s, min_tokens=3, max_tokens=200):
+    """The oracle's greedy decode rate (tokens/s) after the prompt, for about budget_s seconds."""
     import oracle as O
 
     s = Wl.QWEN3_06B
-    m = O.OracleDecoder(s, weights, kv_dtype="f32", max_seq=len(prompt) + 256)
+    m = O.OracleDecoder(s, weights, kv_dtype="f32", max_seq=len(prompt) + max_tokens + 8)
     for t in prompt[:-1]:
         m.body(int(t))
     cur = int(prompt[-1])
     n = 0
     t0 = time.perf_counter()
-    while n < min_tokens or (time.perf_counter() - t0 < budget_s and n < 200):
-        lg = m.step(cur)
-        cur, _ = O.argmax_lowest(lg)
+    while n < min_tokens or (time.perf_counter() - t0 < budget_s and n < max_tokens):
+        cur, _ = O.argmax_lowest(m.step(cur))
         n += 1
-    sec = time.perf_counter() - t0
-    return {"value": round(n / sec, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+    return n, n / (time.perf_counter() - t0)
+
+
+def oracle_gemv_rates(shapes, dtypes):
+    """The oracle's GEMV (float64 product of the widened or dequantised matrix) in GB/s of the
+    same algorithmic bytes the GPU sweep counts: one call per shape, as the oracle stands."""
+    import oracle as O
+
+    res = {}
+    for dt in dtypes:
+        for (o, i) in shapes:
+            if dt.startswith("q4"):
+                ntok = 2 if dt == "q4 ntok=2" else 1
+                m = Wl.q4_matrix(o, i, seed=o + i)
+                x = Wl.q4_activations(i, ntok, seed=7)
+                if ntok == 1:
+                    x = x[0]
+                fn = lambda: O.gemv_q4(m["packed"], m["scale"], m["bias"], x)  # noqa: E731
+                nbytes = o * i // 2 + o * (i // 64) * 4 + ntok * (2 * i + 4 * o)
+            else:
+                Wm = Wl.gemv_matrix(o, i, seed=o + i, dtype=dt)
+                x = Wl.gemv_vector(i, seed=7, dtype=dt)
+                fn = lambda: O.gemv(Wm, x)  # noqa: E731
+                e = 4 if dt == "f32" else 2
+                nbytes = o * i * e + i * e + 4 * o
+            t0 = time.perf_counter()
+            fn()
+            res[f"{dt} {o}x{i}"] = round(nbytes / (time.perf_counter() - t0) / 1e9, 3)
+    return res
+
+
+def cpu_one_core_worker():
+    """Run in a child process whose BLAS is limited to one thread: oracle decode rate and f32 GEMV GB/s."""
+    s = Wl.QWEN3_06B
+    weights = Wl.decoder_weights(s, seed=1)
+    prompt = Wl.prompt_uniform(PROMPT, s.vocab, seed=0)
+    n, rate = oracle_decode_rate(weights, prompt, budget_s=6.0, min_tokens=2)
+    del weights
+    gemv = oracle_gemv_rates(Wl.GEMV_SHAPES, ("f32",))
+    print(json.dumps({"decode_tokens_per_s": round(rate, 4), "decode_tokens": n, "gemv_GB/s": gemv}), flush=True)
+
+
+def cpu_baseline_sample(weights, prompt, budget_s=10.0):
+    """The oracle on the host cores: decode rate on all cores (the line's value), the same on one
+    core (a child process with one BLAS thread), and its GEMV GB/s on the five layer shapes in
+    float32, bfloat16 and 4-bit (one and two tokens) on all cores, float32 on one core."""
+    n, rate = oracle_decode_rate(weights, prompt, budget_s)
+    gemv = oracle_gemv_rates(Wl.GEMV_SHAPES, ("f32", "bf16", "q4 ntok=1", "q4 ntok=2"))
+    one = None
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker"], env=env, capture_output=True,
+                           text=True, timeout=300)
+        if r.returncode == 0 and r.stdout.strip():
+            one = json.loads(r.stdout.strip().splitlines()[-1])
+        else:
+            one = {"error": (r.stderr or "no output").strip().splitlines()[-1][:200]}
+    except (subprocess.TimeoutExpired, OSError, ValueError) as e:
+        one = {"error": str(e)[:200]}
+    return {"value": round(rate, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} greedy decode forwards of the FP32 Qwen3-0.6B-shaped decoder after the {len(prompt)}-token "
-                      f"prompt (float64 numpy oracle, BLAS threads = host cores)"}
+                      f"prompt (float64 numpy oracle, BLAS threads = host cores)",
+            "one_core": one, "gemv_GB/s": gemv}
 
 
 def reference_arm(args):
@@ -723,14 +852,18 @@ def main():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=100)
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-sweep", action="store_true", help="skip the cold GEMV sweep")
     ap.add_argument("--engine", default="persistent", choices=["persistent", "staged"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-prefill", action="store_true", help="skip the BF16 chunked-prefill configuration")
     ap.add_argument("--no-lossless", action="store_true", help="skip the lossless bfloat16 storage comparison")
     ap.add_argument("--no-q4", action="store_true", help="skip the 4-bit decoder configuration")
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_worker:
+        cpu_one_core_worker()
+        return
     if args.impl == "reference":
         args.steps = args.steps if args.steps is not None else 5
         args.warmup = args.warmup if args.warmup is not None else 1

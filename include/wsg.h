@@ -237,10 +237,11 @@ int32_t dec_position(const dec_ctx* ctx);
  * holds the head (stage 0: vocabulary GEMV, stage 1 event 0: argmax done).
  * Events: 0 stage entry, 1 inputs received and staged (includes waiting
  * for the producing stage), 2 outputs published, 3 unused (attention: key
- * loop done). After that block, [512][4] uint64
- * SM clock stamps (clock64) of the first 512 weight segments consumed by
- * warp 0 of CTA 0: wait begins, data ready, dot reduced, next copy issued.
- * NULL turns tracing off. */
+ * loop done). After that block, [8][512][4] uint64 for each consumer warp of
+ * CTA 0 and the first 512 weight boxes it consumes in the launch: SM clock
+ * stamps (clock64) when the box's wait begins, when its data is ready and
+ * when its dot products are issued, then the %globaltimer stamp of the wait's
+ * beginning. NULL turns tracing off. */
 size_t dec_trace_bytes(const dec_ctx* ctx);
 dec_status dec_set_trace(dec_ctx* ctx, uint64_t* d_trace, size_t bytes);
 

@@ -1574,7 +1574,7 @@ extern "C" int32_t dec_position(const dec_ctx* c) { return c ? c->pos : -1; }
 extern "C" size_t dec_trace_bytes(const dec_ctx* c) {
   if (!c || c->cfg.engine != DEC_ENGINE_PERSISTENT) return 0;
   return (static_cast<size_t>(c->mk_grid) * (c->cfg.layers + 1) * kMkTraceStages * kMkTraceEvents +
-          static_cast<size_t>(kMkTraceSegs) * kMkTraceSegEvents) *
+          static_cast<size_t>(kMkWarps) * kMkTraceSegs * kMkTraceSegEvents) *
          sizeof(uint64_t);
 }
 

@@ -143,8 +143,10 @@ struct MkArgs {
 
 // Trace points per stage: entry, activations staged, segments consumed, barrier passed.
 constexpr int kMkTraceStages = 5, kMkTraceEvents = 4;
-// Per-box trace of warp 0 of CTA 0 (first kMkTraceSegs boxes of the first
-// forward), after the stage trace: wait begins, data ready, dot done, box released.
+// Per-box trace of every consumer warp of CTA 0 (first kMkTraceSegs boxes of
+// each, from the launch's start), after the stage trace: [warp][box][event],
+// events: wait begins, data ready, dot done (SM clock), and the %globaltimer
+// stamp of the wait's beginning (to place the box among the stage events).
 constexpr int kMkTraceSegs = 512, kMkTraceSegEvents = 4;
 
 enum MkStageKind : int { MK_QKV = 0, MK_O = 1, MK_GU = 2, MK_DOWN = 3, MK_VOCAB = 4 };
@@ -619,6 +621,29 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     }
   };
 
+  // Keys and values of positions before pos do not depend on the token:
+  // pull this CTA's attention range of them into L2 ahead of the attention
+  // stage. A prefetch is only a hint (L2 is where writes become visible), so
+  // it needs no ordering; the attention stage acquires the rows before reading
+  // them. Issued by the producer warp, whose copies share the copy engine's
+  // queue, so no consumer warp waits for room in it.
+  auto prefetch_attn = [&](int step, int l) {
+    if (!(c < a.n_kv * a.at.nsplit_max) || step >= a.nsteps) return;
+    const int pos = a.pos0 + step;
+    int t0, t1, ns;
+    if (attn_split_range(a.at, c / a.n_kv, pos, &t0, &t1, &ns)) {
+      t1 = min(t1, pos);
+      if (t1 > t0) {
+        const size_t eb = a.kv_layer_bytes / (static_cast<size_t>(a.n_kv) * a.at.max_seq * a.d);
+        const size_t off = static_cast<size_t>(l) * a.kv_layer_bytes +
+                           ((static_cast<size_t>(c % a.n_kv) * a.at.max_seq + t0) * a.d) * eb;
+        const uint32_t bytes = static_cast<uint32_t>(static_cast<size_t>(t1 - t0) * a.d * eb);
+        bulk_prefetch_l2(static_cast<const char*>(a.at.kc) + off, bytes);
+        bulk_prefetch_l2(static_cast<const char*>(a.at.vc) + off, bytes);
+      }
+    }
+  };
+
   // ------------------------------------------------------------------ producer ----
   if (warp >= kMkWarps) {
     setmaxnreg_dec<kMkProducerRegs>();
@@ -637,6 +662,8 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     const uint64_t pol = l2_policy_evict_first();
     if (active) cur_settle();
     cur.done = cur.done || !active;
+    // lane 0's cursor enters every layer's QKV stage (every CTA has QKV rows)
+    if (lane == 0 && !cur.done && cur.st == MK_QKV) prefetch_attn(cur.step, cur.layer);
     uint32_t vhead = 0, phead = 0;  // virtual and ring offset of the next box
     uint32_t qv[kMkQ];              // virtual offsets of the boxes in flight, oldest first
 #pragma unroll
@@ -682,6 +709,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         if (++cur.j >= cur.n) {
           cur_next_stage();
           cur_settle();
+          if (lane == 0 && !cur.done && cur.st == MK_QKV) prefetch_attn(cur.step, cur.layer);
         }
       }
       if (__any_sync(0xffffffffu, progress)) {
@@ -845,10 +873,14 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   };
 
   uint64_t* segtrace = nullptr;
-  if (a.trace && c == 0 && warp == 0)
-    segtrace = a.trace + static_cast<size_t>(G) * (a.L + 1) * kMkTraceStages * kMkTraceEvents;
+  if (a.trace && c == 0)
+    segtrace = a.trace + static_cast<size_t>(G) * (a.L + 1) * kMkTraceStages * kMkTraceEvents +
+               static_cast<size_t>(warp) * kMkTraceSegs * kMkTraceSegEvents;
   auto segstamp = [&](int ev) {
-    if (segtrace && lane == 0 && consumed < kMkTraceSegs) segtrace[consumed * kMkTraceSegEvents + ev] = clock64();
+    if (segtrace && lane == 0 && consumed < kMkTraceSegs) {
+      segtrace[consumed * kMkTraceSegEvents + ev] = clock64();
+      if (ev == 0) segtrace[consumed * kMkTraceSegEvents + 3] = globaltimer_ns();
+    }
   };
 
   // Sum of the 8 warp partials of local row lr (chunk starting at row group cg).
@@ -930,7 +962,6 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
             // registers): release its bytes to the producer
             __syncwarp();
             if (lane == 0) mbar_arrive(&mempty[cq]);
-            segstamp(3);
             ++consumed;
             if (++cq == kMkQ) {
               cq = 0;
@@ -1015,6 +1046,16 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           at.kc = static_cast<char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
           at.vc = static_cast<char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
           stamp(step, l, 1, 0);
+          {
+            // Cache rows below pos were appended by earlier forwards: every
+            // thread acquires their published count before reading them, so
+            // no barrier is needed; the wait overlaps the one for q/k/v. Every
+            // active split acquires, the one appending row pos included, so
+            // each published count covers all rows below it.
+            int t0, t1, ns;
+            if (pos > 0 && attn_split_range(a.at, c / a.n_kv, pos, &t0, &t1, &ns))
+              wait_at_least(a.kv_ready + l * a.n_kv + c % a.n_kv, static_cast<uint32_t>(pos), vabort, a.err, a.xwait_ns);
+          }
           attn_decode_body<KT, GMAX, kMkConsumers, ConsumerSync, (GMAX <= 2 ? kAttnChunk<KT> / 2 : 8), AttnLlIo>(
               at, c % a.n_kv, c / a.n_kv, pos, ascratch, tid, ConsumerSync{}, &s_last,
               AttnLlIo{a.ll_qkv, a.ll_attn, a.ll_apart, a.kv_ready + l * a.n_kv, mk_tag(a, step, l, MK_QKV),
@@ -1046,25 +1087,6 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
           }
         }
         stamp(step, l, ts, 1);
-        if (sid == MK_QKV && tid == 0 && attn_cta) {
-          // Keys and values before pos do not depend on this token: make sure the
-          // rows of earlier positions are published (acquire) and pull this
-          // CTA's attention range of them into L2 while QKV runs.
-          if (pos > 0)
-            wait_at_least(a.kv_ready + l * a.n_kv + c % a.n_kv, static_cast<uint32_t>(pos), vabort, a.err, a.xwait_ns);
-          int t0, t1, ns;
-          if (attn_split_range(a.at, c / a.n_kv, pos, &t0, &t1, &ns)) {
-            t1 = min(t1, pos);
-            if (t1 > t0) {
-              const size_t eb = a.kv_layer_bytes / (static_cast<size_t>(a.n_kv) * a.at.max_seq * a.d);
-              const size_t off = static_cast<size_t>(l) * a.kv_layer_bytes +
-                                 ((static_cast<size_t>(c % a.n_kv) * a.at.max_seq + t0) * a.d) * eb;
-              const uint32_t bytes = static_cast<uint32_t>(static_cast<size_t>(t1 - t0) * a.d * eb);
-              bulk_prefetch_l2(static_cast<const char*>(a.at.kc) + off, bytes);
-              bulk_prefetch_l2(static_cast<const char*>(a.at.vc) + off, bytes);
-            }
-          }
-        }
         const uint32_t tg = mk_tag(a, step, l, sid);
         ok = consume(st, gm, xr, [&](int cg, int) {
           if (sid == MK_QKV) {

@@ -228,16 +228,19 @@ dec_status dec_get_kv(const dec_ctx* ctx, int32_t layer, const void** d_k, const
 /* Current position (number of valid cache entries). -1 if ctx is NULL. */
 int32_t dec_position(const dec_ctx* ctx);
 
-/* Stage tracing of the persistent engine. dec_trace_bytes: size of the
+/* Stage tracing of the persistent engines. dec_trace_bytes: size of the
  * trace buffer (0 for the staged engine). dec_set_trace: with a non-NULL
  * device buffer of at least that size, every later persistent launch writes,
  * for its first forward, one %globaltimer stamp (nanoseconds) per
  * [cta][layer 0..layers][stage 0..4][event 0..3] as uint64. Stages 0-4 of a
  * layer are QKV, attention, O, gate/up, down; the extra layer index `layers`
  * holds the head (stage 0: vocabulary GEMV, stage 1 event 0: argmax done).
- * Events: 0 stage entry, 1 inputs received and staged (includes waiting
- * for the producing stage), 2 outputs published, 3 unused (attention: key
- * loop done). After that block, [8][512][4] uint64 for each consumer warp of
+ * Float engine events: 0 stage entry, 1 inputs received and staged (includes
+ * waiting for the producing stage), 2 outputs published, 3 every warp done
+ * with the stage's weight boxes (attention: key loop done). 4-bit engine
+ * events: 0 stage entry, 1 input vector staged in fixed point, 2 products
+ * (attention: the attention body) done, 3 the grid barrier after the stage
+ * passed; its head has events 0-2 of stage 0 only. After that block, [8][512][4] uint64 for each consumer warp of
  * CTA 0 and the first 512 weight boxes it consumes in the launch: SM clock
  * stamps (clock64) when the box's wait begins, when its data is ready and
  * when its dot products are issued, then the %globaltimer stamp of the wait's

@@ -1098,6 +1098,7 @@ dec_status run_q4_persistent(dec_ctx* c, int pos0, int nsteps, bool head_every, 
   a.first_tok = first_tok;
   a.host_next = host_next;
   a.xwait_ns = c->xwait_ns;
+  a.trace = c->trace;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(c->di.sms);
   cfg.blockDim = dim3(kQ4pThreads);
@@ -1573,7 +1574,8 @@ extern "C" int32_t dec_position(const dec_ctx* c) { return c ? c->pos : -1; }
 
 extern "C" size_t dec_trace_bytes(const dec_ctx* c) {
   if (!c || c->cfg.engine != DEC_ENGINE_PERSISTENT) return 0;
-  return (static_cast<size_t>(c->mk_grid) * (c->cfg.layers + 1) * kMkTraceStages * kMkTraceEvents +
+  const size_t G = c->cfg.wdtype == DEC_Q4G64 ? static_cast<size_t>(c->di.sms) : static_cast<size_t>(c->mk_grid);
+  return (G * (c->cfg.layers + 1) * kMkTraceStages * kMkTraceEvents +
           static_cast<size_t>(kMkWarps) * kMkTraceSegs * kMkTraceSegEvents) *
          sizeof(uint64_t);
 }

@@ -90,6 +90,7 @@ struct Q4PArgs {
   uint32_t attn_bytes;     // attention scratch in shared memory (multiple of 16)
   uint32_t* err;
   uint64_t xwait_ns;       // limit of a grid-barrier wait
+  uint64_t* trace;         // optional: [G][L + 1][5][4] globaltimer stamps of the first forward
 };
 
 // Threads 0..255 of every CTA; ends with all of this CTA's consumers past the
@@ -201,8 +202,25 @@ __global__ void __launch_bounds__(kQ4pThreads, 1) q4_persist_kernel(const Q4PArg
     for (int step = 0; step < a.nsteps && ok; ++step) {
       for (int l = 0; l < a.L && ok; ++l) {
         const Q4PLayer& w = a.layers[l];
-        ok = put(w.q, a.H) && put(w.k, a.H) && put(w.v, a.H) && put(w.o, a.qw) && put(w.gate, a.H) &&
-             put(w.up, a.H) && put(w.down, a.I);
+        ok = put(w.q, a.H);
+        // This CTA's attention keys and values of the earlier positions (they
+        // do not depend on the token): into L2 while the layer's projections
+        // run. A prefetch is only a hint; the attention reads them after the
+        // grid barriers that order it after their writes.
+        if (ok && c < a.at.n_kv * a.at.nsplit_max) {
+          int t0, t1, ns;
+          const int pos = a.pos0 + step;
+          if (attn_split_range(a.at, c % a.at.nsplit_max, pos, &t0, &t1, &ns) && min(t1, pos) > t0) {
+            const size_t rb = static_cast<size_t>(a.at.d) * sizeof(KT);
+            const size_t off = static_cast<size_t>(l) * a.kv_layer_bytes +
+                               (static_cast<size_t>(c / a.at.nsplit_max) * a.at.max_seq + t0) * rb;
+            const uint32_t bytes = static_cast<uint32_t>(static_cast<size_t>(min(t1, pos) - t0) * rb);
+            bulk_prefetch_l2(static_cast<const char*>(a.at.kc) + off, bytes);
+            bulk_prefetch_l2(static_cast<const char*>(a.at.vc) + off, bytes);
+          }
+        }
+        ok = ok && put(w.k, a.H) && put(w.v, a.H) && put(w.o, a.qw) && put(w.gate, a.H) && put(w.up, a.H) &&
+             put(w.down, a.I);
       }
       if (ok && has_head(step)) ok = put(a.head, a.H);
     }
@@ -254,6 +272,12 @@ __global__ void __launch_bounds__(kQ4pThreads, 1) q4_persist_kernel(const Q4PArg
   auto sync_all = [&]() { ok = ok && q4p_grid_sync(a.bar, static_cast<unsigned long long>(G), target, vabort, a.err, tid, a.xwait_ns); };
 
   const int attn_ctas = a.at.n_kv * a.at.nsplit_max;
+  // Trace of the first forward (tid 0 of every CTA): per layer and stage (QKV,
+  // attention, O, gate/up, down; the head as layer L, stage 0), the stage's
+  // entry, its x staged, its products done, and the grid barrier after it.
+  auto stamp = [&](int step, int l, int st, int ev) {
+    if (a.trace && step == 0 && tid == 0) a.trace[((static_cast<size_t>(c) * (a.L + 1) + l) * 5 + st) * 4 + ev] = globaltimer_ns();
+  };
   int gi = 0;  // the previous step's greedy token
   for (int step = 0; step < a.nsteps && ok; ++step) {
     const int pos = a.pos0 + step;
@@ -286,40 +310,59 @@ __global__ void __launch_bounds__(kQ4pThreads, 1) q4_persist_kernel(const Q4PArg
     for (int l = 0; l < a.L && ok; ++l) {
       const Q4PLayer& w = a.layers[l];
       // Q, K, V with the input RMSNorm
+      stamp(step, l, 0, 0);
       q4_stage_x<1, Q4X_NORM>(a.h, a.H, w.g_in, a.eps, a.H, xq, xu, s_rs, tid);
+      stamp(step, l, 0, 1);
       consume(w.q, a.H, a.qkv, 0, false);
       consume(w.k, a.H, a.qkv, a.qw, false);
       consume(w.v, a.H, a.qkv, a.qw + a.kvw, false);
+      stamp(step, l, 0, 2);
       sync_all();
+      stamp(step, l, 0, 3);
       if (!ok) break;
       // attention
+      stamp(step, l, 1, 0);
       if (c < attn_ctas) {
         AttnArgs at = a.at;
         at.g_q = w.g_q;
         at.g_k = w.g_k;
         at.kc = static_cast<unsigned char*>(a.at.kc) + static_cast<size_t>(l) * a.kv_layer_bytes;
         at.vc = static_cast<unsigned char*>(a.at.vc) + static_cast<size_t>(l) * a.kv_layer_bytes;
-        attn_decode_body<KT, GMAX, kQ4Warps * 32, Q4pSync, GMAX <= 2 ? kAttnChunk<KT> : kAttnChunk<KT> / 2>(
+        attn_decode_body<KT, GMAX, kQ4Warps * 32, Q4pSync, GMAX <= 2 ? kAttnChunk<KT> / 2 : 8>(
             at, c / a.at.nsplit_max, c % a.at.nsplit_max, pos, asmem, tid, Q4pSync{}, &s_last,
             AttnPlainIo{a.qkv, a.attn});
       }
+      stamp(step, l, 1, 2);
       sync_all();
+      stamp(step, l, 1, 3);
       if (!ok) break;
       // O + residual
+      stamp(step, l, 2, 0);
       q4_stage_x<1, Q4X_F32>(a.attn, a.qw, nullptr, 0.f, a.qw, xq, xu, s_rs, tid);
+      stamp(step, l, 2, 1);
       consume(w.o, a.qw, a.h, 0, true);
+      stamp(step, l, 2, 2);
       sync_all();
+      stamp(step, l, 2, 3);
       if (!ok) break;
       // gate / up with the post-attention RMSNorm
+      stamp(step, l, 3, 0);
       q4_stage_x<1, Q4X_NORM>(a.h, a.H, w.g_post, a.eps, a.H, xq, xu, s_rs, tid);
+      stamp(step, l, 3, 1);
       consume(w.gate, a.H, a.gu, 0, false);
       consume(w.up, a.H, a.gu, a.I, false);
+      stamp(step, l, 3, 2);
       sync_all();
+      stamp(step, l, 3, 3);
       if (!ok) break;
       // down (SwiGLU prologue) + residual
+      stamp(step, l, 4, 0);
       q4_stage_x<1, Q4X_SWIGLU>(a.gu, 2 * a.I, nullptr, 0.f, a.I, xq, xu, s_rs, tid);
+      stamp(step, l, 4, 1);
       consume(w.down, a.I, a.h, 0, true);
+      stamp(step, l, 4, 2);
       sync_all();
+      stamp(step, l, 4, 3);
     }
     if (!ok) break;
     if (!has_head(step)) {
@@ -327,8 +370,11 @@ __global__ void __launch_bounds__(kQ4pThreads, 1) q4_persist_kernel(const Q4PArg
       continue;
     }
     // head: final RMSNorm, this CTA's logits slice and its best candidate
+    stamp(step, a.L, 0, 0);
     q4_stage_x<1, Q4X_NORM>(a.h, a.H, a.g_final, a.eps, a.H, xq, xu, s_rs, tid);
+    stamp(step, a.L, 0, 1);
     consume(a.head, a.H, a.logits, 0, false);
+    stamp(step, a.L, 0, 2);
     q4_consumer_sync();
     {
       int r0, n;

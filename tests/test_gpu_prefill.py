@@ -116,6 +116,33 @@ def test_head_dim_128_both_cache_types(kv_dtype):
     run_chunked(shape, w, prompt, 64, 3, "persistent", kv_dtype=kv_dtype)
 
 
+@pytest.mark.parametrize("n_q,n_kv", [(2, 2), (4, 2), (8, 2), (8, 1)])
+def test_head_dim_128_query_groups(n_q, n_kv):
+    """head_dim 128 with a bfloat16 cache (the tcgen05 attention: 128 query vectors per CTA, 128 /
+    group rows) for groups of 1, 2, 4 and 8 query heads per key/value head; 300 rows in chunks of
+    128 (128 + 128 + 44), so the later chunks walk five key tiles of 64 and the last block is
+    ragged."""
+    shape = Wl.DecoderShape(layers=2, hidden=256, inter=512, n_q=n_q, n_kv=n_kv, head_dim=128, vocab=500)
+    w = Wl.decoder_weights(shape, seed=11, wdtype="bf16")
+    prompt = Wl.prompt_zipf(300, shape.vocab, seed=4)
+    run_chunked(shape, w, prompt, 128, 2, "persistent")
+
+
+def test_head_dim_128_peaked_scores():
+    """Q and K norm gains scaled by 3 (scores of standard deviation ~9): in layer 0, 193 of the 944
+    (row, query head) pairs with more than 64 keys meet a later key tile whose maximum passes the
+    reference maximum by more than 2^8, so the attention rescales its output accumulator mid-walk.
+    (At a gain of 6 the forward itself is ill-conditioned: the float64 forward with only the
+    value + remainder operand roundings applied already moves layer-1 keys past the tolerance.)"""
+    shape = Wl.DecoderShape(layers=2, hidden=256, inter=512, n_q=4, n_kv=2, head_dim=128, vocab=500)
+    w = Wl.decoder_weights(shape, seed=12, wdtype="bf16")
+    for lw in w["layers"]:
+        lw["g_q"] = (lw["g_q"] * 3).astype(np.float32)
+        lw["g_k"] = (lw["g_k"] * 3).astype(np.float32)
+    prompt = Wl.prompt_zipf(300, shape.vocab, seed=5)
+    run_chunked(shape, w, prompt, 128, 2, "staged")
+
+
 def test_single_row_chunks():
     """Chunks of one row: the causal attention sees only the cache."""
     w = Wl.decoder_weights(Wl.TINY, seed=2, wdtype="bf16")

@@ -38,6 +38,7 @@
 #include "gemm_tc_host.h"
 #include "megakernel.cuh"
 #include "prefill.cuh"
+#include "prefill_attn_tc.cuh"
 #include "q4_persist.cuh"
 
 namespace wsg {
@@ -229,6 +230,10 @@ struct dec_ctx {
   Map128 pf_amap[6];
   std::vector<Map128> pf_wmap;    // weights in 128-row boxes (128-column tiles)
   std::vector<Map128> pf_wmap64;  // the same in 64-row boxes (64-column tiles)
+  // the whole K and V cache [layers * n_kv * max_seq][128] in 64 x 64 boxes
+  // (bfloat16 cache, head size 128: pf_attn_tmem_kernel)
+  Map128 pf_kvmap[2];
+  bool pf_attn_tmem = false;
   std::string err;
 
   template <typename T>
@@ -732,7 +737,31 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     if (l == g.layers - 1 && !is_last) break;
     const float scale = 1.0f / std::sqrt(static_cast<float>(d));
     bool tc = false;
-    if constexpr (sizeof(KT) == 2) {  // bfloat16 cache: tensor-core attention
+    if (c->pf_attn_tmem) {  // bfloat16 cache, head size 128: tcgen05 attention
+      static bool lifted[64] = {};  // per device
+      if (!lifted[c->di.device]) {
+        WSG_CUDA_TRY(&c->err, cudaFuncSetAttribute(pf_attn_tmem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   static_cast<int>(kAtSmem)));
+        lifted[c->di.device] = true;
+      }
+      PfAttnArgs aa;
+      aa.qkv = QKV;
+      aa.AO = AO;
+      aa.AO2 = AO2;
+      aa.err = err;
+      aa.n = n;
+      aa.p0 = p0;
+      aa.n_q = g.n_q;
+      aa.n_kv = g.n_kv;
+      aa.kv_row0 = l * g.n_kv * g.max_seq;
+      aa.max_seq = g.max_seq;
+      aa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+      const int rows = kAtBM / group;
+      pf_attn_tmem_kernel<<<dim3(g.n_kv, (n + rows - 1) / rows), kAtThreads, kAtSmem, st>>>(
+          *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[0].b),
+          *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[1].b), aa);
+      tc = true;
+    } else if constexpr (sizeof(KT) == 2) {  // bfloat16 cache: warp-level tensor-core attention
       void (*tk)(const float*, int, int, int, int, const uint16_t*, const uint16_t*, int, float, uint16_t*, uint16_t*) =
           d == 128 ? pf_attn_tc_kernel<128> : d == 64 ? pf_attn_tc_kernel<64> : d == 32 ? pf_attn_tc_kernel<32>
                                                                             : d == 16 ? pf_attn_tc_kernel<16> : nullptr;
@@ -1285,6 +1314,19 @@ extern "C" dec_status dec_create(const dec_config* cfg, void* d_workspace, size_
         thread_error() = c->err;
         return bail(m);
       }
+    const long long kv_rows = static_cast<long long>(cfg->layers) * cfg->n_kv * cfg->max_seq;
+    if (cfg->kvdtype == DEC_BF16 && cfg->head_dim == kAtD && kAtBM % (cfg->n_q / cfg->n_kv) == 0 &&
+        kv_rows + kAtBN < (1ll << 31)) {
+      for (int i = 0; i < 2; ++i) {
+        const dec_status m = encode_map_2d(c->pf_kvmap[i].b, c->ws + (i ? L.vc : L.kc), kv_rows, kAtD, 2, 64, kAtBN,
+                                           true, &c->err);
+        if (m != DEC_OK) {
+          thread_error() = c->err;
+          return bail(m);
+        }
+      }
+      c->pf_attn_tmem = true;
+    }
   }
   c->nsplit_max = di.sms / cfg->n_kv;
   if (c->nsplit_max < 1) c->nsplit_max = 1;

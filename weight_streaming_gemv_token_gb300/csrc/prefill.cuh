@@ -8,8 +8,11 @@
 //   embedding gather + input RMSNorm (layer 0)   pf_embed_norm_kernel
 //   RMSNorm of the residual rows                  pf_norm_kernel
 //   per-head Q/K RMSNorm, RoPE, K/V cache append  pf_qk_rope_kv_kernel
-//   causal grouped-query attention                pf_attn_tc_kernel (bfloat16
-//                                                 cache), pf_attn_kernel
+//   causal grouped-query attention                pf_attn_tmem_kernel
+//                                                 (prefill_attn_tc.cuh: bfloat16
+//                                                 cache, head size 128),
+//                                                 pf_attn_tc_kernel (other
+//                                                 bfloat16 heads), pf_attn_kernel
 // (SwiGLU runs in the gate/up GEMM's epilogue.)
 //
 // The residual rows stay float32; each GEMM operand row (normalised rows,

@@ -5,26 +5,26 @@
 //
 // A CTA owns 128 query vectors of one key/value head g: the group's query
 // heads of 128 / group consecutive chunk rows (vector v = row * group + head),
-// one per tensor-memory lane, and walks the key tiles of 64 positions from 0
-// up to the last position any of its rows sees (flash-attention form):
+// one per tensor-memory lane, and walks the key tiles of 128 positions from 0
+// up to the last position any of its rows sees (flash-attention form). Q and
+// the probabilities P stay in tensor memory and enter the products as the A
+// operand from there; shared memory holds only key and value tiles, so each
+// MMA reads one 4 KB operand slice from shared memory:
 //
-//   warp 0      one thread streams each tile's keys and values (two 64 x 64
+//   warp 0      one thread streams each tile's keys and values (two 128 x 64
 //               boxes each, 128-byte swizzle) from the whole-cache tensor maps
-//               into a 3-stage key ring and a 2-stage value ring (a key tile is
-//               free once its scores are computed, so keys run further ahead);
-//   warp 1      one thread issues S_j = Q K_j^T (M 128, N 64, into one of two
+//               into 3-stage key and value rings;
+//   warp 1      one thread issues S_j = Q K_j^T (M 128, N 128, into one of two
 //               score buffers in tensor memory) one tile ahead, then, once the
-//               probabilities of tile j are in shared memory (one of two
-//               buffers, so the softmax of tile j + 1 does not wait for this
-//               product), O += P_j V_j
-//               (M 128, N 128; the value tile is read in its stored,
-//               value-contiguous layout as an MN-major operand);
+//               probabilities of tile j have replaced its scores in that
+//               buffer, O += P_j V_j (M 128, N 128; the value tile is read in
+//               its stored, value-contiguous layout as an MN-major operand);
 //   warps 2-9   two threads per vector, each on half of the tile's keys
 //               (warps w and w + 4 share the tensor-memory lanes of w % 4):
-//               read 32 scores (tcgen05.ld), mask keys past the vector's
+//               read 64 scores (tcgen05.ld), mask keys past the vector's
 //               position, exchange the half maxima, exponentiate against a
 //               reference maximum, add to a running half sum and write the
-//               half probability row into shared memory for the P V product.
+//               half probability row over the scores (tcgen05.st).
 //
 // The running maximum is a reference that moves only when a tile's maximum
 // passes it by more than 2^8: probabilities stay below 256, and the rare move
@@ -37,6 +37,10 @@
 // the cache's bfloat16, accumulation is FP32: scores and outputs keep about 16
 // mantissa bits, as in the single-token path's float32 attention. The output
 // is written as a bfloat16 value + remainder pair, the O projection's operand.
+//
+// Tensor memory (512 columns, one CTA per SM): score / probability buffers at
+// columns 0 and 128 (probabilities: value at +0..63, remainder at +64..127,
+// two bfloat16 per column), O at 256, Q value at 384 and remainder at 448.
 //
 // Every wait is bounded; on a timeout the CTA records ERR_TC_TIMEOUT, stops,
 // waits for its issued MMAs and frees its tensor memory.
@@ -52,17 +56,16 @@ namespace wsg {
 
 constexpr int kAtD = 128;                                // head size
 constexpr int kAtBM = 128;                               // query vectors per CTA (tensor-memory lanes)
-constexpr int kAtBN = 64;                                // keys per tile
-constexpr int kAtKStages = 3, kAtVStages = 2;            // key / value tiles in flight
+constexpr int kAtBN = 128;                               // keys per tile
+constexpr int kAtKStages = 3, kAtVStages = 3;            // key / value tiles in flight
 constexpr int kAtSoftWarps = 8;                          // two per lane quarter of tensor memory
 constexpr int kAtThreads = 32 * (2 + kAtSoftWarps);      // TMA warp, MMA warp, softmax warps
-constexpr uint32_t kAtQBytes = kAtBM * kAtD * 2;         // one bfloat16 part of Q: 32 KB
-constexpr uint32_t kAtKBytes = kAtBN * kAtD * 2;         // a key (or value) tile: 16 KB, two 64-column boxes
-constexpr uint32_t kAtBoxBytes = kAtKBytes / 2;          // 64 keys x 64 columns
-constexpr uint32_t kAtPBytes = kAtBM * kAtBN * 2;        // one bfloat16 part of P: 16 KB
-constexpr uint32_t kAtTmemCols = 256;                    // S buffers at 0 and 64, O at 128
+constexpr uint32_t kAtKBytes = kAtBN * kAtD * 2;         // a key (or value) tile: 32 KB, two 64-column boxes
+constexpr uint32_t kAtBoxBytes = kAtKBytes / 2;          // 128 keys x 64 columns
+constexpr uint32_t kAtTmemCols = 512;                    // S / P buffers at 0 and 128, O at 256, Q at 384
+constexpr uint32_t kAtTmO = 256, kAtTmQ = 384;
 constexpr float kAtRescaleLog2 = 8.f;                    // reference moves past this margin (log2 units)
-constexpr size_t kAtSmem = 2 * kAtQBytes + (kAtKStages + kAtVStages) * kAtKBytes + 2 * 2 * kAtPBytes + 1024;
+constexpr size_t kAtSmem = (kAtKStages + kAtVStages) * kAtKBytes + 1024;
 
 struct PfAttnArgs {
   const float* qkv;  // [n][(n_q + 2 n_kv) D] chunk rows: Q after its norm and RoPE, then K, V
@@ -93,6 +96,17 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t da, uint64_t db,
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
       "l"(da), "l"(db), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// The same with the A operand (M x 16, two bfloat16 per column, lane = row)
+// in tensor memory at a_tmem.
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t db, uint32_t idesc,
+                                              uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+      "r"(a_tmem), "l"(db), "r"(idesc), "r"(acc)
       : "memory");
 }
 
@@ -134,30 +148,23 @@ __device__ __forceinline__ float at_exp2(float x) {
   return y;
 }
 
-// Byte offset of the 16-byte piece `chunk` (0-7) of row `row` in a K-major
-// tile of 128-byte rows with 128-byte swizzle (1024-byte aligned base).
-__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
-  return static_cast<uint32_t>(row) * 128u + (static_cast<uint32_t>(chunk ^ (row & 7)) << 4);
-}
-
 // Grid: (n_kv, ceil(n / (128 / group))), kAtThreads threads, kAtSmem bytes of
 // dynamic shared memory. kmap / vmap: the whole K / V cache as a 2D bfloat16
-// tensor [layers * n_kv * max_seq][128] in 64 x 64 boxes with 128-byte swizzle.
+// tensor [layers * n_kv * max_seq][128] in 128-row x 64-column boxes with
+// 128-byte swizzle.
 __global__ void __launch_bounds__(kAtThreads, 1)
     pf_attn_tmem_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                         const PfAttnArgs a) {
   extern __shared__ __align__(1024) unsigned char at_raw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(at_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* Qs = sm;                                   // [hi, lo] x two 64-column blocks of 128 rows
-  unsigned char* Ks = sm + 2 * kAtQBytes;                   // key stages: box 0 (columns 0-63), box 1
+  unsigned char* Ks = sm;                                   // key stages: box 0 (columns 0-63), box 1
   unsigned char* Vs = Ks + kAtKStages * kAtKBytes;          // value stages, the same
-  unsigned char* Ps = Vs + kAtVStages * kAtKBytes;          // [buffer][hi, lo] x 128 rows x 64 keys
   __shared__ __align__(8) uint64_t k_full[kAtKStages], k_empty[kAtKStages], v_full[kAtVStages], v_empty[kAtVStages];
-  __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done[2], drain;
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done, drain;
   __shared__ __align__(8) uint64_t pair_bar[4];  // the two softmax warps of a lane quarter
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
-  __shared__ float xch[2][2][kAtBM];  // softmax: [tile parity][half][vector] half maxima, then half sums
+  __shared__ float xch[2][2][kAtBM];  // softmax: [exchange parity][half][vector] half maxima, then half sums
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = blockIdx.x;
   const int group = a.n_q / a.n_kv, rows = kAtBM / group;
@@ -175,12 +182,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
     for (int b = 0; b < 2; ++b) {
+      mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], kAtSoftWarps);
-      mbar_init(&o_done[b], 1);
     }
+    mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     for (int i = 0; i < 4; ++i) mbar_init(&pair_bar[i], 64);
     s_fail = 0;
@@ -192,43 +198,46 @@ __global__ void __launch_bounds__(kAtThreads, 1)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  // Q as bfloat16 value and remainder, K-major with 128-byte swizzle: vector v,
-  // elements 8c .. 8c + 7 (c = 0..15) at block c / 8, row v, piece c % 8.
-  {
-    const int W = (a.n_q + 2 * a.n_kv) * kAtD;
-    for (int i = tid; i < kAtBM * (kAtD / 8); i += kAtThreads) {
-      const int v = i >> 4, c = i & 15;
-      const int row = r0 + v / group;
-      float x[8];
-      if (row < a.n) {
-        const float4* q = reinterpret_cast<const float4*>(a.qkv + static_cast<size_t>(row) * W +
-                                                          (g * group + v % group) * kAtD + c * 8);
-        const float4 x0 = q[0], x1 = q[1];
-        x[0] = x0.x, x[1] = x0.y, x[2] = x0.z, x[3] = x0.w, x[4] = x1.x, x[5] = x1.y, x[6] = x1.z, x[7] = x1.w;
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = 0.f;
-      }
-      uint32_t h[4], l[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) at_pack_split(x[2 * k], x[2 * k + 1], &h[k], &l[k]);
-      const uint32_t off = (c >> 3) * (kAtQBytes / 2) + sw128_off(v, c & 7);
-      *reinterpret_cast<uint4*>(Qs + off) = make_uint4(h[0], h[1], h[2], h[3]);
-      *reinterpret_cast<uint4*>(Qs + kAtQBytes + off) = make_uint4(l[0], l[1], l[2], l[3]);
-    }
-  }
-  fence_proxy_async_smem();  // the tensor cores read Q through the async proxy
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base;
+  const int q = warp & 3, half = (warp - 2) >> 2;  // softmax warps: lane quarter, half of the keys / of D
+  const int v = q * 32 + lane;
+  const int row = r0 + v / group;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);  // this warp's lanes
+  if (warp >= 2) {
+    // Q row v as bfloat16 value and remainder into tensor memory: this thread
+    // converts elements 64 half .. 64 half + 63 (32 columns of each part)
+    uint32_t qh[32], ql[32];
+    if (row < a.n) {
+      const int W = (a.n_q + 2 * a.n_kv) * kAtD;
+      const float4* src = reinterpret_cast<const float4*>(a.qkv + static_cast<size_t>(row) * W +
+                                                          (g * group + v % group) * kAtD + half * (kAtD / 2));
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float4 x = src[k];
+        at_pack_split(x.x, x.y, &qh[2 * k], &ql[2 * k]);
+        at_pack_split(x.z, x.w, &qh[2 * k + 1], &ql[2 * k + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 32; ++k) qh[k] = ql[k] = 0u;
+    }
+    tc_st32(tl + kAtTmQ + half * 32, qh);
+    tc_st32(tl + kAtTmQ + 64 + half * 32, ql);
+    tc_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   auto fail = [&]() {
     *vfail = 1;
     atomicOr(a.err, ERR_TC_TIMEOUT);
   };
 
   if (warp == 0) {
-    // ---- TMA: keys of tile j into key stage j % 3, values into value stage j % 2 ----
+    // ---- TMA: keys and values of tile j into stage j % 3 of their rings ----
     if (lane == 0) {
       const int y0 = a.kv_row0 + g * a.max_seq;
       for (int j = 0; j < T && !*vfail; ++j) {
@@ -257,7 +266,6 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = tc_idesc(kAtBM, kAtBN);
       constexpr uint32_t idO = tc_idesc(kAtBM, kAtD) | (1u << 16);  // B (values) MN-major
-      const uint32_t qa = smem_u32(Qs), pa = smem_u32(Ps);
       auto issue_s = [&](int j) -> bool {
         const int s = j % kAtKStages;
         if (!mbar_wait(&k_full[s], (j / kAtKStages) & 1)) return false;
@@ -268,10 +276,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         for (int kk = 0; kk < kAtD / 16; ++kk) {
           const uint64_t db = tc_desc_sw128(kb + (kk >> 2) * kAtBoxBytes + (kk & 3) * 32);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint64_t da = tc_desc_sw128(qa + part * kAtQBytes + (kk >> 2) * (kAtQBytes / 2) + (kk & 3) * 32);
-            tc_mma_f16(d, da, db, idS, (kk | part) != 0);
-          }
+          for (int part = 0; part < 2; ++part)
+            tc_mma_f16_ts(d, tmem + kAtTmQ + part * 64 + kk * 8, db, idS, (kk | part) != 0);
         }
         tc_commit(&k_empty[s]);  // the key stage is free once these MMAs have read it
         tc_commit(&s_full[j & 1]);
@@ -279,8 +285,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       };
       bool ok = issue_s(0);
       for (int j = 0; ok && j < T; ++j) {
-        // S_{j+1} goes into the buffer of S_{j-1}, whose scores the softmax
-        // warps had read before they signalled P_{j-1}
+        // S_{j+1} goes into the buffer of P_{j-1}: issued after P_{j-1} V_{j-1},
+        // it overwrites those probabilities only once that product has read them
         if (j + 1 < T && !issue_s(j + 1)) {
           ok = false;
           break;
@@ -296,19 +302,18 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         }
         tc_fence_after();
         const uint32_t vb = smem_u32(Vs + static_cast<size_t>(s) * kAtKBytes);
+        const uint32_t pb = tmem + static_cast<uint32_t>((j & 1) * kAtBN);
 #pragma unroll
         for (int kk = 0; kk < kAtBN / 16; ++kk) {
           // keys 16 kk .. 16 kk + 15: two 8-row groups 1024 bytes apart; value
           // columns 64 .. 127 in the second box
           const uint64_t db = tc_desc_sw128_mn(vb + kk * 2048, kAtBoxBytes, 1024);
 #pragma unroll
-          for (int part = 0; part < 2; ++part) {
-            const uint64_t da = tc_desc_sw128(pa + ((j & 1) * 2 + part) * kAtPBytes + kk * 32);
-            tc_mma_f16(tmem + 2 * kAtBN, da, db, idO, (j | kk | part) != 0);
-          }
+          for (int part = 0; part < 2; ++part)
+            tc_mma_f16_ts(tmem + kAtTmO, pb + part * 64 + kk * 8, db, idO, (j | kk | part) != 0);
         }
-        tc_commit(&v_empty[s]);     // the value stage is free once these MMAs have read it
-        tc_commit(&o_done[j & 1]);  // O holds tiles 0..j; P buffer j % 2 may be overwritten
+        tc_commit(&v_empty[s]);  // the value stage is free once these MMAs have read it
+        tc_commit(&o_done);      // O holds tiles 0..j
       }
       if (!ok) fail();
       // every MMA this thread issued has completed before tensor memory is freed
@@ -317,19 +322,19 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     }
   } else {
     // ---- softmax: two threads per vector (tensor-memory lane), half a tile each ----
-    const int q = warp & 3, half = (warp - 2) >> 2;
-    const int v = q * 32 + lane;
-    const int row = r0 + v / group;
     const int pos = a.p0 + min(row, last_row);  // rows past the chunk reuse the last row's keys
-    const uint32_t tl = tmem + (static_cast<uint32_t>(q * 32) << 16);
-    const uint32_t to = tl + 2 * kAtBN + half * (kAtD / 2);  // this thread's half of O
+    const uint32_t to = tl + kAtTmO + half * (kAtD / 2);  // this thread's half of O
     const float c = a.scale_log2;
     float m_ref = -INFINITY, lsum = 0.f;  // reference (log2 units, shared by the pair), half sum
     bool ok = true;
-    // exchange k of the pair: both threads of every vector have written xch[k & 1]
+    // exchange k of the pair: both threads of every vector have written
+    // xch[k & 1] (and finished their tensor-memory reads before it)
     auto pair_done = [&](int k) {
+      tc_fence_before();
       mbar_arrive(&pair_bar[q]);
-      return __all_sync(0xffffffffu, mbar_wait(&pair_bar[q], k & 1));
+      const bool r = __all_sync(0xffffffffu, mbar_wait(&pair_bar[q], k & 1));
+      tc_fence_after();
+      return r;
     };
     for (int j = 0; j < T; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1))) {
@@ -337,24 +342,26 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sv[32];
-      tc_ld32(sv, tl + static_cast<uint32_t>((j & 1) * kAtBN + half * 32));
+      const uint32_t tb = tl + static_cast<uint32_t>((j & 1) * kAtBN);
+      uint32_t s0[32], s1[32];
+      tc_ld32(s0, tb + half * 64);
+      tc_ld32(s1, tb + half * 64 + 32);
       tc_wait_ld();
-      // keys t0 .. t0 + 31 of this half; k <= lim are visible
-      const int lim = pos - (j * kAtBN + half * 32);
-      float x[32];
-      if (__all_sync(0xffffffffu, lim >= 31)) {
+      // keys t0 .. t0 + 63 of this half; k <= lim are visible
+      const int lim = pos - (j * kAtBN + half * 64);
+      float x[64];
+      if (__all_sync(0xffffffffu, lim >= 63)) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = __uint_as_float(sv[k]);
+        for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(k < 32 ? s0[k] : s1[k - 32]);
       } else {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) x[k] = k <= lim ? __uint_as_float(sv[k]) : -INFINITY;
+        for (int k = 0; k < 64; ++k) x[k] = k <= lim ? __uint_as_float(k < 32 ? s0[k] : s1[k - 32]) : -INFINITY;
       }
-      float mh[16];
+      float mh[32];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) mh[k] = fmaxf(x[k], x[k + 16]);
+      for (int k = 0; k < 32; ++k) mh[k] = fmaxf(x[k], x[k + 32]);
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
         for (int k = 0; k < w; ++k) mh[k] = fmaxf(mh[k], mh[k + w]);
       xch[j & 1][half][v] = mh[0];
@@ -363,21 +370,19 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         break;
       }
       const float mx = fmaxf(mh[0], xch[j & 1][half ^ 1][v]) * c;
-      bool waited = false;
       const bool move = mx > m_ref + kAtRescaleLog2;
       if (__any_sync(0xffffffffu, move)) {
         const float nref = move ? mx : m_ref;
         const float f = nref == m_ref ? 1.f : at_exp2(m_ref - nref);  // 0 on the first move
         lsum *= f;
         if (j > 0) {
-          // O holds tiles 0..j-1 once P_{j-1} V_{j-1} has completed (and with
-          // it every earlier product)
-          if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
+          // O holds tiles 0..j-1 once P_{j-1} V_{j-1} has completed (P_{j-2}
+          // V_{j-2} had, before S_j that this thread has read)
+          if (!__all_sync(0xffffffffu, mbar_wait(&o_done, (j - 1) & 1))) {
             ok = false;
             break;
           }
           tc_fence_after();
-          waited = true;
 #pragma unroll 1
           for (int c0 = 0; c0 < kAtD / 2; c0 += 32) {
             uint32_t o[32];
@@ -387,44 +392,31 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
             tc_st32(to + c0, o);
           }
-          tc_wait_st();
         }
         m_ref = nref;
       }
-      uint32_t ph[16], pl[16];
-      float sh[16];
+      // probabilities over the scores: value at columns 32 half .., remainder at 64 + 32 half ..
+      uint32_t ph[32], pl[32];
+      float sh[32];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
+      for (int k = 0; k < 32; ++k) {
         const float p0 = at_exp2(fmaf(x[2 * k], c, -m_ref)), p1 = at_exp2(fmaf(x[2 * k + 1], c, -m_ref));
         sh[k] = p0 + p1;
         at_pack_split(p0, p1, &ph[k], &pl[k]);
       }
 #pragma unroll
-      for (int w = 8; w >= 1; w >>= 1)
+      for (int w = 16; w >= 1; w >>= 1)
 #pragma unroll
         for (int k = 0; k < w; ++k) sh[k] += sh[k + w];
       lsum += sh[0];
-      // P_{j-2} V_{j-2} has read probability buffer j % 2
-      if (j > 1 && !waited) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&o_done[j & 1], ((j - 2) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-      }
-      unsigned char* Ph = Ps + (j & 1) * 2 * kAtPBytes;
-      unsigned char* Pl = Ph + kAtPBytes;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint32_t off = sw128_off(v, 4 * half + k);
-        *reinterpret_cast<uint4*>(Ph + off) = make_uint4(ph[4 * k], ph[4 * k + 1], ph[4 * k + 2], ph[4 * k + 3]);
-        *reinterpret_cast<uint4*>(Pl + off) = make_uint4(pl[4 * k], pl[4 * k + 1], pl[4 * k + 2], pl[4 * k + 3]);
-      }
-      fence_proxy_async_smem();
+      tc_st32(tb + half * 32, ph);
+      tc_st32(tb + 64 + half * 32, pl);
+      tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[j & 1]);
     }
-    if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_done[(T - 1) & 1], ((T - 1) >> 1) & 1))) ok = false;
+    if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_done, (T - 1) & 1))) ok = false;
     xch[T & 1][half][v] = lsum;
     if (!pair_done(T)) ok = false;  // (after a failure the pair may be out of step: bounded either way)
     if (ok) {

@@ -143,6 +143,36 @@ def test_head_dim_128_peaked_scores():
     run_chunked(shape, w, prompt, 128, 2, "staged")
 
 
+def test_qwen3_widths_1024_row_chunk_repeated():
+    """Three layers of the Qwen3-0.6B widths, one 1024-row chunk, three times on fresh decoders:
+    the attention's CTAs walk one to eight key tiles of 128 (rows 128-255 two), so the waits
+    on the output accumulator of the last tile run against products still in flight; every
+    layer's K/V after each run against the oracle."""
+    import dataclasses
+
+    import torch
+
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = dataclasses.replace(Wl.QWEN3_06B, layers=3)
+    w = Wl.decoder_weights(s, seed=1, wdtype="bf16")
+    prompt = [int(t) for t in Wl.prompt_zipf(1024, s.vocab, seed=2)]
+    ora = O.OracleDecoder(s, w, kv_dtype="bf16", max_seq=1032)
+    ora.prefill(prompt, logit_rows=[])
+    for rep in range(3):
+        dec = Decoder(s, w, kv_dtype="bf16", max_seq=1032, chunk_cap=1024)
+        dec.prefill(prompt, is_last=False)
+        torch.cuda.synchronize()
+        for l in range(s.layers):
+            K, V, n = dec.kv(l)
+            rk, rv = ora.kv(l)
+            close(kv_to_np(K[:, :n]), rk, LOW_TOL, f"run {rep}: K layer {l}")
+            close(kv_to_np(V[:, :n]), rv, LOW_TOL, f"run {rep}: V layer {l}")
+        assert dec.device_errors() == 0
+        dec.close()
+
+
 def test_single_row_chunks():
     """Chunks of one row: the causal attention sees only the cache."""
     w = Wl.decoder_weights(Wl.TINY, seed=2, wdtype="bf16")

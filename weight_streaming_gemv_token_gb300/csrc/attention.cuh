@@ -198,7 +198,13 @@ struct AttnPlainIo {
   __device__ __forceinline__ void store_part(size_t, float) const {}
   template <int KC>
   __device__ __forceinline__ void poll_parts(size_t, size_t, int, int, int, float*, float*, float*) const {}
+  template <int KO>
+  __device__ __forceinline__ void poll_merge(size_t, int, int, int, int, int, int, float*, float*) const {}
 };
+
+// Split 0 merges up to this many other splits in one polling round (their
+// O words in registers, their (M, L) pairs through shared memory).
+constexpr int kAttnMergeOne = 24;
 
 template <typename KT, int GMAX, int NT, typename Sync, int CK = kAttnChunk<KT>, typename Io = AttnPlainIo>
 __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s, int pos, float* asmem, int tid,
@@ -417,7 +423,48 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
   }
   sync();
   const bool merger = Io::kPolledMerge && nsplit > 1 && s == 0;
-  for (int idx = tid; idx < group * d; idx += NT) {
+  // Split 0 in one round: every thread one output element (group * d <= NT),
+  // the other splits' (M, L) pairs fitting in the q/k/v scratch (dead now).
+  const bool one_round = merger && group * d <= NT && nsplit - 1 <= kAttnMergeOne &&
+                         2 * (nsplit - 1) * group <= (group + 2) * d && 2 * (nsplit - 1) * group <= NT;
+  if constexpr (Io::kPolledMerge) {
+    if (one_round) {
+      const int h = tid / d, e = tid - h * d;
+      const bool have = tid < group * d;
+      // this split's own (M, L, O) of element (h, e) from the warps
+      float M = -INFINITY, L = 0.f, O = 0.f;
+      if (have) {
+        for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w * group + h]);
+        for (int w = 0; w < kAttnWarps; ++w) {
+          const float f = expf(wm[w * group + h] - M);
+          L += wl[w * group + h] * f;
+          O += wo[(w * group + h) * d + e] * f;
+        }
+      }
+      const int nml = 2 * (nsplit - 1) * group;
+      float ov[kAttnMergeOne], mlv;
+      io.template poll_merge<kAttnMergeOne>(static_cast<size_t>(g) * a.nsplit_max * group * (d + 2), nsplit, group,
+                                           have ? h : 0, have ? e : 0, d, tid < nml ? tid : -1, ov, &mlv);
+      float* sml = qn;  // [split - 1][head][M, L]
+      if (tid < nml) sml[tid] = mlv;
+      sync();
+      if (have) {
+        float Mx = M;
+        for (int k = 1; k < nsplit; ++k) Mx = fmaxf(Mx, sml[((k - 1) * group + h) * 2]);
+        const float f0 = expf(M - Mx);
+        float Lx = L * f0, Ox = O * f0;
+#pragma unroll
+        for (int j = 0; j < kAttnMergeOne; ++j) {
+          if (j + 1 >= nsplit) break;
+          const float f = expf(sml[(j * group + h) * 2] - Mx);
+          Lx = fmaf(sml[(j * group + h) * 2 + 1], f, Lx);
+          Ox = fmaf(ov[j], f, Ox);
+        }
+        io.store_out((g * group + h) * d + e, Ox / Lx);
+      }
+    }
+  }
+  for (int idx = one_round ? group * d : tid; idx < group * d; idx += NT) {
     const int h = idx / d, e = idx - h * d;
     float M = -INFINITY;
     for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w * group + h]);

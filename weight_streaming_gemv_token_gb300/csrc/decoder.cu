@@ -707,6 +707,14 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
                             st, &c->err);
   };
   const bool fuse_qkv = qw % kGemmTileN == 0 && kvw % kGemmTileN == 0;
+  // RMSNorm of the residual rows into the next GEMM's operand pair
+  const bool norm4 = H % 4 == 0 && H <= 4 * kPfNormPieces * kPfThreads;
+  auto norm = [&](const float* Xr, const float* gain, float eps, int Hn, uint16_t* A, uint16_t* A2) {
+    if (norm4 && (reinterpret_cast<uintptr_t>(gain) & 15u) == 0)
+      pf_norm4_kernel<<<n, kPfThreads, 0, st>>>(Xr, gain, eps, Hn, A, A2);
+    else
+      pf_norm_kernel<<<n, kPfThreads, 0, st>>>(Xr, gain, eps, Hn, A, A2);
+  };
   pf_embed_norm_kernel<uint16_t><<<n, kPfThreads, 0, st>>>(c->at<int32_t>(L.tok), p0, c->w.embed, g.vocab,
                                                            c->layers[0].g_in, g.eps, H, X, AH, AH2, err);
   WSG_CUDA_TRY(&c->err, cudaGetLastError());
@@ -714,7 +722,7 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     const dec_layer_weights& lw = c->layers[l];
     const int wm = l * kMkMapsPerLayer;
     if (l > 0) {
-      pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_in, g.eps, H, AH, AH2);
+      norm(X, lw.g_in, g.eps, H, AH, AH2);
       WSG_CUDA_TRY(&c->err, cudaGetLastError());
     }
     if (fuse_qkv) {
@@ -728,8 +736,16 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     const size_t off = static_cast<size_t>(l) * c->kv_layer_elems() * dtype_bytes(g.kvdtype);
     void* kc = c->ws + L.kc + off;
     void* vc = c->ws + L.vc + off;
-    pf_qk_rope_kv_kernel<KT><<<dim3(n, (g.n_q + 2 * g.n_kv + 3) / 4), 128, 0, st>>>(
-        QKV, p0, g.n_q, g.n_kv, d, lw.g_q, lw.g_k, g.eps, rc, rs, kc, vc, g.max_seq);
+    if (d == 128 || d == 64 || d == 32) {
+      auto rk = d == 128 ? pf_qk_rope_kv_vec_kernel<KT, 4>
+                         : d == 64 ? pf_qk_rope_kv_vec_kernel<KT, 2> : pf_qk_rope_kv_vec_kernel<KT, 1>;
+      const long long pairs = static_cast<long long>(n) * (g.n_q + 2 * g.n_kv);
+      rk<<<static_cast<unsigned>((pairs + 7) / 8), 256, 0, st>>>(QKV, n, p0, g.n_q, g.n_kv, lw.g_q, lw.g_k, g.eps,
+                                                                 rc, rs, kc, vc, g.max_seq);
+    } else {
+      pf_qk_rope_kv_kernel<KT><<<dim3(n, (g.n_q + 2 * g.n_kv + 3) / 4), 128, 0, st>>>(
+          QKV, p0, g.n_q, g.n_kv, d, lw.g_q, lw.g_k, g.eps, rc, rs, kc, vc, g.max_seq);
+    }
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     // A chunk that does not end the prompt stops after the last layer's K/V
     // write: later rows read only the cache, so that layer's attention output,
@@ -788,7 +804,7 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     }
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     if ((s = gemm(1, wm + 3, X, H, 0, H, qw, true)) != DEC_OK) return s;  // O projection + residual
-    pf_norm_kernel<<<n, kPfThreads, 0, st>>>(X, lw.g_post, g.eps, H, AH, AH2);
+    norm(X, lw.g_post, g.eps, H, AH, AH2);
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     // gate/up with SwiGLU in the GEMM's epilogue: tiles pair 64 gate and 64 up outputs
     if ((s = launch_gemm_swiglu(c->pf_amap[0].b, c->pf_amap[3].b, c->pf_wmap64[wm + 4].b, c->pf_wmap64[wm + 5].b, AI,

@@ -479,6 +479,29 @@ struct AttnLlIo {
       lv[k] = __uint_as_float(static_cast<uint32_t>(w[3 * k + 2]));
     }
   }
+  // One round for split 0's merge: element e of head h's O of splits 1 ..
+  // nsplit - 1 into ov[0 .. nsplit - 2], and word `ml` (< 0: none) of the
+  // splits' (M, L) pairs, ordered split, head, M then L, into *mlv. gbase:
+  // word offset of (head g, split 0, query head 0); a split's block of group
+  // heads is group (d + 2) words long.
+  template <int KO>
+  __device__ __forceinline__ void poll_merge(size_t gbase, int nsplit, int group, int h, int e, int d, int ml,
+                                             float* ov, float* mlv) const {
+    uint64_t w[KO + 1];
+    const uint64_t* pg = part + gbase;
+    const size_t hs = static_cast<size_t>(d) + 2, ss = static_cast<size_t>(group) * hs;
+    poll<KO + 1>(
+        [&](int j) -> const uint64_t* {
+          if (j < KO) return j < nsplit - 1 ? pg + (j + 1) * ss + h * hs + e : nullptr;
+          if (ml < 0) return nullptr;
+          const int k = 1 + ml / (2 * group), hh = (ml >> 1) % group;
+          return pg + k * ss + hh * hs + d + (ml & 1);
+        },
+        tag_out, w);
+#pragma unroll
+    for (int j = 0; j < KO; ++j) ov[j] = __uint_as_float(static_cast<uint32_t>(w[j]));
+    *mlv = __uint_as_float(static_cast<uint32_t>(w[KO]));
+  }
   __device__ __forceinline__ void publish_kv(int g, int pos) const {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(kv_ready + g), "r"(static_cast<uint32_t>(pos + 1))
                  : "memory");
@@ -626,7 +649,10 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
   // stage. A prefetch is only a hint (L2 is where writes become visible), so
   // it needs no ordering; the attention stage acquires the rows before reading
   // them. Issued by the producer warp, whose copies share the copy engine's
-  // queue, so no consumer warp waits for room in it.
+  // queue, so no consumer warp waits for room in it. The rows of layer l + 1
+  // are final while layer l runs, so they are requested as soon as the issue
+  // cursor leaves layer l's QKV stage: a layer ahead of their attention, while
+  // the latency-bound projection stages leave HBM time unused.
   auto prefetch_attn = [&](int step, int l) {
     if (!(c < a.n_kv * a.at.nsplit_max) || step >= a.nsteps) return;
     const int pos = a.pos0 + step;
@@ -641,6 +667,20 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         bulk_prefetch_l2(static_cast<const char*>(a.at.kc) + off, bytes);
         bulk_prefetch_l2(static_cast<const char*>(a.at.vc) + off, bytes);
       }
+    }
+  };
+
+  // Next (step, layer) whose attention range to prefetch, as step * L + layer.
+  int pf_next = 0;
+  auto prefetch_ahead = [&]() {
+    if (cur.done) return;
+    const int here = cur.step * a.L + cur.layer;
+    // at a layer's QKV stage its own range is due (if not requested yet);
+    // past it, the next layer's
+    const int want = cur.st == MK_QKV ? here : here + 1;
+    while (pf_next <= want) {
+      prefetch_attn(pf_next / a.L, pf_next % a.L);
+      ++pf_next;
     }
   };
 
@@ -662,8 +702,9 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
     const uint64_t pol = l2_policy_evict_first();
     if (active) cur_settle();
     cur.done = cur.done || !active;
-    // lane 0's cursor enters every layer's QKV stage (every CTA has QKV rows)
-    if (lane == 0 && !cur.done && cur.st == MK_QKV) prefetch_attn(cur.step, cur.layer);
+    // lane 0's cursor requests the attention ranges (every CTA has QKV rows,
+    // so it passes every layer's QKV stage)
+    if (lane == 0) prefetch_ahead();
     uint32_t vhead = 0, phead = 0;  // virtual and ring offset of the next box
     uint32_t qv[kMkQ];              // virtual offsets of the boxes in flight, oldest first
 #pragma unroll
@@ -709,7 +750,7 @@ __global__ void __launch_bounds__(kMkThreads, 1) decode_megakernel(const MkArgs 
         if (++cur.j >= cur.n) {
           cur_next_stage();
           cur_settle();
-          if (lane == 0 && !cur.done && cur.st == MK_QKV) prefetch_attn(cur.step, cur.layer);
+          if (lane == 0) prefetch_ahead();
         }
       }
       if (__any_sync(0xffffffffu, progress)) {

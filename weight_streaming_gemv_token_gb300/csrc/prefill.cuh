@@ -89,6 +89,51 @@ __global__ void __launch_bounds__(kPfThreads) pf_norm_kernel(const float* X, con
   for (int i = threadIdx.x; i < H; i += kPfThreads) pf_split(x[i] * inv * g[i], A, A2, base + i);
 }
 
+// Row r: (A, A2) = RMSNorm(X[r]) * g, for H % 4 == 0 and H <= 4096: each
+// thread keeps its (up to four) 4-element pieces in registers between the sum
+// of squares and the scaled, split write.
+constexpr int kPfNormPieces = 4;
+__global__ void __launch_bounds__(kPfThreads) pf_norm4_kernel(const float* X, const float* g, float eps, int H,
+                                                               uint16_t* A, uint16_t* A2) {
+  __shared__ float red[kPfThreads / 32];
+  const int r = blockIdx.x, n4 = H >> 2;
+  const float4* x = reinterpret_cast<const float4*>(X + static_cast<size_t>(r) * H);
+  float4 xv[kPfNormPieces];
+  float ss = 0.f;
+#pragma unroll
+  for (int k = 0; k < kPfNormPieces; ++k) {
+    const int i = threadIdx.x + k * kPfThreads;
+    xv[k] = i < n4 ? x[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    ss = fmaf(xv[k].x, xv[k].x, fmaf(xv[k].y, xv[k].y, fmaf(xv[k].z, xv[k].z, fmaf(xv[k].w, xv[k].w, ss))));
+  }
+  ss = warp_sum(ss);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = ss;
+  __syncthreads();
+  float t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kPfThreads / 32; ++w) t += red[w];
+  const float inv = 1.0f / sqrtf(t / static_cast<float>(H) + eps);
+  uint2* a = reinterpret_cast<uint2*>(A + static_cast<size_t>(r) * H);
+  uint2* a2 = reinterpret_cast<uint2*>(A2 + static_cast<size_t>(r) * H);
+  const float4* g4 = reinterpret_cast<const float4*>(g);
+#pragma unroll
+  for (int k = 0; k < kPfNormPieces; ++k) {
+    const int i = threadIdx.x + k * kPfThreads;
+    if (i < n4) {
+      const float4 gv = g4[i];
+      const float y0 = xv[k].x * inv * gv.x, y1 = xv[k].y * inv * gv.y, y2 = xv[k].z * inv * gv.z,
+                  y3 = xv[k].w * inv * gv.w;
+      const uint16_t h0 = f32_to_bf16_rn(y0), h1 = f32_to_bf16_rn(y1), h2 = f32_to_bf16_rn(y2),
+                     h3 = f32_to_bf16_rn(y3);
+      const uint16_t l0 = f32_to_bf16_rn(y0 - bf16_to_f32(h0)), l1 = f32_to_bf16_rn(y1 - bf16_to_f32(h1)),
+                     l2 = f32_to_bf16_rn(y2 - bf16_to_f32(h2)), l3 = f32_to_bf16_rn(y3 - bf16_to_f32(h3));
+      a[i] = make_uint2(h0 | (static_cast<uint32_t>(h1) << 16), h2 | (static_cast<uint32_t>(h3) << 16));
+      a2[i] = make_uint2(l0 | (static_cast<uint32_t>(l1) << 16), l2 | (static_cast<uint32_t>(l3) << 16));
+    }
+  }
+}
+
 // One warp per (row, head) over the n_q + 2 n_kv heads of the row's raw
 // projections (row stride W = (n_q + 2 n_kv) d): q heads are normalised
 // (g_q), rotated and written back in place; k heads are normalised (g_k),
@@ -138,6 +183,69 @@ __global__ void __launch_bounds__(128) pf_qk_rope_kv_kernel(float* qkv, int p0, 
       store1<KT>(kc, (static_cast<size_t>(gk) * max_seq + p) * d + i, lo);
       store1<KT>(kc, (static_cast<size_t>(gk) * max_seq + p) * d + i + half, hi);
     }
+  }
+}
+
+// pf_qk_rope_kv_kernel for head size d = 32 EPL (EPL = 1, 2 or 4), one warp
+// per (row, head) with the head in registers, EPL consecutive elements per
+// lane: RoPE pairs element i with i + d / 2, which lane l ^ 16 holds. Eight
+// warps per block over the n (n_q + 2 n_kv) (row, head) pairs.
+template <typename KT, int EPL>
+__global__ void __launch_bounds__(256) pf_qk_rope_kv_vec_kernel(float* qkv, int n, int p0, int n_q, int n_kv,
+                                                                 const float* g_q, const float* g_k, float eps,
+                                                                 const float* rope_cos, const float* rope_sin,
+                                                                 void* kc, void* vc, int max_seq) {
+  static_assert(EPL == 1 || EPL == 2 || EPL == 4, "head size 32, 64 or 128");
+  constexpr int d = 32 * EPL, half = d / 2;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nh = n_q + 2 * n_kv;
+  const int gw = blockIdx.x * 8 + warp;
+  if (gw >= n * nh) return;
+  const int r = gw / nh, h = gw - r * nh;
+  const int p = p0 + r;
+  float* v = qkv + static_cast<size_t>(r) * nh * d + static_cast<size_t>(h) * d + lane * EPL;
+  float x[EPL];
+  if constexpr (EPL == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(v);
+    x[0] = t.x, x[1] = t.y, x[2] = t.z, x[3] = t.w;
+  } else if constexpr (EPL == 2) {
+    const float2 t = *reinterpret_cast<const float2*>(v);
+    x[0] = t.x, x[1] = t.y;
+  } else {
+    x[0] = v[0];
+  }
+  auto store_cache = [&](void* base, int head, const float* y) {
+    const size_t at = (static_cast<size_t>(head) * max_seq + p) * d + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) store1<KT>(base, at + e, y[e]);
+  };
+  if (h >= n_q + n_kv) {  // value head: append
+    store_cache(vc, h - n_q - n_kv, x);
+    return;
+  }
+  const bool is_q = h < n_q;
+  const float* g = (is_q ? g_q : g_k) + lane * EPL;
+  float ss = 0.f;
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) ss = fmaf(x[e], x[e], ss);
+  ss = warp_sum(ss);
+  const float inv = 1.0f / sqrtf(ss / static_cast<float>(d) + eps);
+  const int ci = (lane & 15) * EPL;
+  const float* cs = rope_cos + static_cast<size_t>(p) * half + ci;
+  const float* sn = rope_sin + static_cast<size_t>(p) * half + ci;
+  float y[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL; ++e) {
+    const float own = x[e] * inv * g[e];
+    const float other = __shfl_xor_sync(0xffffffffu, own, 16);
+    // lanes 0-15 hold a = element i, lanes 16-31 b = element i + d/2
+    y[e] = lane < 16 ? own * cs[e] - other * sn[e] : other * sn[e] + own * cs[e];
+  }
+  if (is_q) {
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) v[e] = y[e];
+  } else {
+    store_cache(kc, h - n_q, y);
   }
 }
 

@@ -160,7 +160,11 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   unsigned char* Ks = sm;                                   // key stages: box 0 (columns 0-63), box 1
   unsigned char* Vs = Ks + kAtKStages * kAtKBytes;          // value stages, the same
   __shared__ __align__(8) uint64_t k_full[kAtKStages], k_empty[kAtKStages], v_full[kAtVStages], v_empty[kAtVStages];
-  __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done, drain;
+  // o_done[b]: completions of the P V products of tiles j = b, b + 2, ...; a
+  // parity wait on a barrier is only sound while the completion before the one
+  // awaited has happened, which for the product of tile j means that of tile
+  // j - 2 (done once S_j, issued after it, is)
+  __shared__ __align__(8) uint64_t s_full[2], p_full[2], o_done[2], drain;
   __shared__ __align__(8) uint64_t pair_bar[4];  // the two softmax warps of a lane quarter
   __shared__ uint32_t tmem_base;
   __shared__ int s_fail;
@@ -185,8 +189,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
     for (int b = 0; b < 2; ++b) {
       mbar_init(&s_full[b], 1);
       mbar_init(&p_full[b], kAtSoftWarps);
+      mbar_init(&o_done[b], 1);
     }
-    mbar_init(&o_done, 1);
     mbar_init(&drain, 1);
     for (int i = 0; i < 4; ++i) mbar_init(&pair_bar[i], 64);
     s_fail = 0;
@@ -313,7 +317,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
             tc_mma_f16_ts(tmem + kAtTmO, pb + part * 64 + kk * 8, db, idO, (j | kk | part) != 0);
         }
         tc_commit(&v_empty[s]);  // the value stage is free once these MMAs have read it
-        tc_commit(&o_done);      // O holds tiles 0..j
+        tc_commit(&o_done[j & 1]);  // O holds tiles 0..j
       }
       if (!ok) fail();
       // every MMA this thread issued has completed before tensor memory is freed
@@ -376,9 +380,9 @@ __global__ void __launch_bounds__(kAtThreads, 1)
         const float f = nref == m_ref ? 1.f : at_exp2(m_ref - nref);  // 0 on the first move
         lsum *= f;
         if (j > 0) {
-          // O holds tiles 0..j-1 once P_{j-1} V_{j-1} has completed (P_{j-2}
-          // V_{j-2} had, before S_j that this thread has read)
-          if (!__all_sync(0xffffffffu, mbar_wait(&o_done, (j - 1) & 1))) {
+          // O holds tiles 0..j-1 once P_{j-1} V_{j-1} has completed (P_{j-3}
+          // V_{j-3} had, before S_j that this thread has read)
+          if (!__all_sync(0xffffffffu, mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1))) {
             ok = false;
             break;
           }
@@ -416,7 +420,7 @@ __global__ void __launch_bounds__(kAtThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[j & 1]);
     }
-    if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_done, (T - 1) & 1))) ok = false;
+    if (ok && !__all_sync(0xffffffffu, mbar_wait(&o_done[(T - 1) & 1], ((T - 1) >> 1) & 1))) ok = false;
     xch[T & 1][half][v] = lsum;
     if (!pair_done(T)) ok = false;  // (after a failure the pair may be out of step: bounded either way)
     if (ok) {

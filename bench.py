@@ -412,7 +412,7 @@ def prefill_config(W, torch, hbm, tflops_peak):
 
     tuning = {}
     prompt = Wl.prompt_zipf(2048, s.vocab, seed=0)
-    for chunk in (128, 256, 512, 1024):
+    for chunk in (128, 256, 512, 1024, 2048):
         dec = Decoder(s, w, kv_dtype="bf16", max_seq=2048 + 16, chunk_cap=chunk)
         ttft(dec, prompt, chunk)  # warm-up (lazy set-up)
         runs = [ttft(dec, prompt, chunk)[0] for _ in range(3)]

@@ -228,7 +228,8 @@ struct dec_ctx {
     unsigned char b[128];
   };
   Map128 pf_amap[6];
-  std::vector<Map128> pf_wmap;    // weights in 128-row boxes (128-column tiles)
+  std::vector<Map128> pf_wmap256;  // weights in 256-row boxes (256-column tiles)
+  std::vector<Map128> pf_wmap;     // weights in 128-row boxes (128-column tiles; gate/up of 256-column ones)
   std::vector<Map128> pf_wmap64;  // the same in 64-row boxes (64-column tiles)
   // the whole K and V cache [layers * n_kv * max_seq][128] in 64 x 64 boxes
   // (bfloat16 cache, head size 128: pf_attn_tmem_kernel)
@@ -679,25 +680,31 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
   const float* rc = c->at<float>(L.rope_cos);
   const float* rs = c->at<float>(L.rope_sin);
   dec_status s;
-  // C[:, col0..col0+N) (=, or +=) rows . W^T with operand maps `amap` and
-  // amap + 3 (value and remainder of: 0 normed input, 1 attention output,
-  // 2 SwiGLU output) and weight map `wm`
-  // 64-column tiles when 128-column ones would leave SMs idle
-  auto wmap = [&](int wm, int bn) { return bn == 64 ? c->pf_wmap64[wm].b : c->pf_wmap[wm].b; };
+  // weight map `wm` in boxes of the tile width (gemm_plan picks the width)
+  auto wmap = [&](int wm, int bn) {
+    return bn == 64 ? c->pf_wmap64[wm].b : bn == 128 ? c->pf_wmap[wm].b : c->pf_wmap256[wm].b;
+  };
+  // C[:, col0..col0+N) (=, or += with accumulate) rows . W^T with operand
+  // maps `amap` and amap + 3 (value and remainder of: 0 normed input, 1
+  // attention output, 2 SwiGLU output) and weight map `wm`
   auto gemm = [&](int amap, int wm, float* C, int ldc, int col0, int N, int K, bool acc) {
-    const int bn = gemm_tile_n(n, N, c->di.sms);
+    const int bn = gemm_plan(n, N, K, c->di.sms, 0, true);
     const void* mb[1] = {wmap(wm, bn)};
     return launch_gemm_bf16(c->pf_amap[amap].b, c->pf_amap[amap + 3].b, mb, nullptr, 1, bn, C, ldc, col0, n, N, K, acc,
                             err, st, &c->err);
   };
-  // Several weights side by side in one launch (Q, K, V; gate, up): one grid
-  // over all their columns fills the GPU better than a launch per weight.
-  // Their widths must be whole 128-column tiles.
+  // Several weights side by side in one launch (Q, K, V): one grid over all
+  // their columns fills the GPU better than a launch per weight. Their widths
+  // are whole 128-column tiles; 256-column tiles where they are whole ones.
   auto gemm_multi = [&](int amap, const int* wms, const int* widths, int nw, float* C, int ldc, int K) {
     const void* mb[3];
-    int nb[2] = {0, 0}, N = 0;
-    for (int i = 0; i < nw; ++i) N += widths[i];
-    const int bn = gemm_tile_n(n, N, c->di.sms);
+    int nb[2] = {0, 0}, N = 0, orb = 0;
+    for (int i = 0; i < nw; ++i) {
+      N += widths[i];
+      if (i + 1 < nw) orb |= N;  // the boundary after weight i
+    }
+    const int align = orb & -orb;  // largest power of two dividing every boundary (0: none)
+    const int bn = gemm_plan(n, N, K, c->di.sms, align, true);
     for (int i = 0, acc = 0; i < nw; ++i) {
       mb[i] = wmap(wms[i], bn);
       acc += widths[i];
@@ -807,7 +814,10 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     norm(X, lw.g_post, g.eps, H, AH, AH2);
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     // gate/up with SwiGLU in the GEMM's epilogue: tiles pair 64 gate and 64 up outputs
-    if ((s = launch_gemm_swiglu(c->pf_amap[0].b, c->pf_amap[3].b, c->pf_wmap64[wm + 4].b, c->pf_wmap64[wm + 5].b, AI,
+    const int gbn = gemm_plan(n, 2 * I, H, c->di.sms, 256, true) == 256 ? 256 : 128;
+    const void* gmap = gbn == 256 ? c->pf_wmap[wm + 4].b : c->pf_wmap64[wm + 4].b;
+    const void* umap = gbn == 256 ? c->pf_wmap[wm + 5].b : c->pf_wmap64[wm + 5].b;
+    if ((s = launch_gemm_swiglu(c->pf_amap[0].b, c->pf_amap[3].b, gmap, umap, gbn, AI,
                                 AI2, I, n, I, H, err, st, &c->err)) != DEC_OK)
       return s;
     if ((s = gemm(2, wm + 6, X, H, 0, H, I, true)) != DEC_OK) return s;  // down projection + residual
@@ -1427,6 +1437,7 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
     // Tensor-core GEMM operand maps of every weight matrix (chunked prefill).
     const dec_config& g = c->cfg;
     const int qw = g.n_q * g.head_dim, kvw = g.n_kv * g.head_dim;
+    c->pf_wmap256.resize(static_cast<size_t>(g.layers) * kMkMapsPerLayer);
     c->pf_wmap.resize(static_cast<size_t>(g.layers) * kMkMapsPerLayer);
     c->pf_wmap64.resize(static_cast<size_t>(g.layers) * kMkMapsPerLayer);
     for (int l = 0; l < g.layers; ++l) {
@@ -1439,7 +1450,8 @@ extern "C" dec_status dec_load_weights(dec_ctx* c, const dec_weights* w) {
                               {x.w_down, g.hidden, g.inter}};
       for (int k = 0; k < kMkMapsPerLayer; ++k) {
         const size_t i = static_cast<size_t>(l) * kMkMapsPerLayer + k;
-        dec_status st = encode_gemm_operand(c->pf_wmap[i].b, t[k].p, t[k].rows, t[k].K, 128, &c->err);
+        dec_status st = encode_gemm_operand(c->pf_wmap256[i].b, t[k].p, t[k].rows, t[k].K, 256, &c->err);
+        if (st == DEC_OK) st = encode_gemm_operand(c->pf_wmap[i].b, t[k].p, t[k].rows, t[k].K, 128, &c->err);
         if (st == DEC_OK) st = encode_gemm_operand(c->pf_wmap64[i].b, t[k].p, t[k].rows, t[k].K, 64, &c->err);
         if (st != DEC_OK) return st;
       }

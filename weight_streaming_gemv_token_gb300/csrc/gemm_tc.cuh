@@ -4,14 +4,14 @@
 // C += that product, with A (activation rows) and W (weights, row-major
 // [out][in]) in bfloat16 and FP32 accumulation.
 //
-// Tiles of C are 128 x 128 (or 128 x 64), computed with tcgen05.mma
+// Tiles of C are 128 x 256, 128 x 128 or 128 x 64, computed with tcgen05.mma
 // (cta_group::1, kind::f16, BF16 inputs, FP32 accumulator in tensor memory);
 // one launch may cover up to three weight matrices side by side in N (Q, K
 // and V, or gate and up). The kernel is persistent: one CTA per SM walks the
 // tiles blockIdx.x, blockIdx.x + gridDim.x, ...
 //  * warp 0: a TMA thread streams 128 x 64 tiles of A and W (128-byte swizzle)
-//    of every K block of every tile into a 4-stage shared-memory ring (full
-//    mbarrier per stage, completed by the copies' transaction bytes);
+//    of every K block of every tile into a 3- or 4-stage shared-memory ring
+//    (full mbarrier per stage, completed by the copies' transaction bytes);
 //  * warp 1: an MMA thread issues four K = 16 MMAs per stage from shared-
 //    memory descriptors into one of two accumulator buffers in tensor memory
 //    (alternating by tile), releases each stage with tcgen05.commit on its
@@ -20,12 +20,12 @@
 //    tcgen05.ld, stores (or adds, or SwiGLUs) the rows and marks the buffer
 //    empty, while the MMA thread already fills the other buffer with the next
 //    tile: a tile's epilogue overlaps the next tile's main loop.
-// TC_SWIGLU (128-column tiles): tile j takes rows 64j..64j+63 of the gate
-// weights (mapB0, 64-row boxes) and the same rows of the up weights (mapB1)
-// as one 128-row W tile, so accumulator columns 0-63 hold gate and 64-127 up
-// of the same 64 outputs; the epilogue writes silu(gate) * up for them as a
-// bfloat16 value + remainder pair (the next GEMM's activation operand), and
-// the gate/up product never goes to memory.
+// TC_SWIGLU (128- or 256-column tiles): tile j takes rows BN/2 j .. BN/2 j +
+// BN/2 - 1 of the gate weights (mapB0, BN/2-row boxes) and the same rows of
+// the up weights (mapB1) as one W tile, so accumulator columns 0..BN/2-1 hold
+// gate and BN/2..BN-1 up of the same BN/2 outputs; the epilogue writes
+// silu(gate) * up for them as a bfloat16 value + remainder pair (the next
+// GEMM's activation operand), and the gate/up product never goes to memory.
 // With SPLIT the activation operand comes as two bfloat16 matrices, A = hi +
 // lo (hi the nearest bfloat16 of a float32 value, lo the nearest bfloat16 of
 // the remainder), and both products go into the same accumulator: the rows
@@ -45,10 +45,10 @@
 
 namespace wsg {
 
-// Tiles of C are kTcBM x BN, BN = 128 (kTcBN) or 64 (for grids that would not
-// fill the GPU with 128-column tiles).
+// Tiles of C are kTcBM x BN, BN = 256 (kTcBN), 128 or 64 (for grids that
+// would not fill the GPU with wider tiles).
 // Warps: 0 TMA, 1 MMA (and tensor-memory allocation), 2-5 epilogue.
-constexpr int kTcBM = 128, kTcBN = 128, kTcBK = 64, kTcStages = 4, kTcEpiWarps = 4, kTcThreads = 32 * (2 + kTcEpiWarps);
+constexpr int kTcBM = 128, kTcBN = 256, kTcBK = 64, kTcEpiWarps = 4, kTcThreads = 32 * (2 + kTcEpiWarps);
 constexpr uint32_t kTcABytes = kTcBM * kTcBK * 2;  // 16 KB
 template <int BN>
 constexpr uint32_t tc_b_bytes() {
@@ -59,9 +59,14 @@ template <bool SPLIT, int BN>
 constexpr uint32_t tc_stage_bytes() {
   return (SPLIT ? 2 : 1) * kTcABytes + tc_b_bytes<BN>();
 }
+// four stages where they fit in 200 KB, else three
+template <bool SPLIT, int BN>
+constexpr int tc_stages() {
+  return 4 * tc_stage_bytes<SPLIT, BN>() <= 200u * 1024u ? 4 : 3;
+}
 template <bool SPLIT, int BN>
 constexpr size_t tc_smem_bytes() {
-  return kTcStages * tc_stage_bytes<SPLIT, BN>() + 1024;  // plus alignment slack
+  return tc_stages<SPLIT, BN>() * tc_stage_bytes<SPLIT, BN>() + 1024;  // plus alignment slack
 }
 
 enum : uint32_t { ERR_TC_TIMEOUT = 1u << 5 };
@@ -135,11 +140,11 @@ __device__ __forceinline__ void tc_epilogue(const TcArgs& a, uint32_t tbase, int
     {
       const int half = a.N / 2;  // outputs of the whole product
 #pragma unroll 1
-      for (int c0 = 0; c0 < 64; c0 += 32) {
+      for (int c0 = 0; c0 < BN / 2; c0 += 32) {
         uint32_t gv[32], uv[32];
         const uint32_t taddr = tbase + static_cast<uint32_t>(c0);
         tc_ld32(gv, taddr);
-        tc_ld32(uv, taddr + 64);
+        tc_ld32(uv, taddr + BN / 2);
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
         const int col0 = n0 / 2 + c0;
         if (row < a.M) {
@@ -231,8 +236,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     gemm_bf16_tc_kernel(const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapA2,
                         const __grid_constant__ CUtensorMap mapB0, const __grid_constant__ CUtensorMap mapB1,
                         const __grid_constant__ CUtensorMap mapB2, const TcArgs a) {
-  static_assert(BN == 64 || BN == 128, "64- or 128-column tiles");
-  static_assert(EPI != TC_SWIGLU || BN == 128, "the SwiGLU epilogue pairs 64 gate and 64 up columns");
+  static_assert(BN == 64 || BN == 128 || BN == 256, "64-, 128- or 256-column tiles");
+  static_assert(EPI != TC_SWIGLU || BN >= 128, "the SwiGLU epilogue pairs BN/2 gate and BN/2 up columns");
+  constexpr int kTcStages = tc_stages<SPLIT, BN>();
   constexpr uint32_t kStage = tc_stage_bytes<SPLIT, BN>();
   constexpr uint32_t kBOff = (SPLIT ? 2 : 1) * kTcABytes;  // W tile offset within a stage
   constexpr uint32_t kTmemCols = 2 * BN;                   // two FP32 accumulators of 128 lanes x BN columns
@@ -295,7 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (SPLIT) tma_load_2d_map(st + kTcABytes, &mapA2, kb * kTcBK, m0, &full[s]);
           if constexpr (EPI == TC_SWIGLU) {
             tma_load_2d_map(st + kBOff, &mapB0, kb * kTcBK, n0 / 2, &full[s]);
-            tma_load_2d_map(st + kBOff + tc_b_bytes<64>(), &mapB1, kb * kTcBK, n0 / 2, &full[s]);
+            tma_load_2d_map(st + kBOff + tc_b_bytes<BN / 2>(), &mapB1, kb * kTcBK, n0 / 2, &full[s]);
           } else {
             tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, &full[s]);
           }

@@ -49,7 +49,7 @@ METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 # 4-layer / 32768-vocabulary case of the same widths: (387,733,504 read + 3,089,920 written) /
 # 387,186,688 algorithmic bytes; the excess is the rows a tiled box reads past a CTA's row range.
 # Set to None when the kernel changes until it is measured again.
-MK_TRAFFIC_PER_ALG_BYTE = (387733504 + 3089920) / 387186688
+MK_TRAFFIC_PER_ALG_BYTE = (387498496 + 2787584) / 387186688
 # DRAM bytes (read + written) per launch of the standalone gemv bulk-copy kernel at 151936x1024 f32
 # (the tied vocabulary shape), from an ncu capture: 622,377,984 B read + 3,492,352 B written; None
 # until measured for the current kernel.

@@ -12,13 +12,13 @@ from gpu_util import dev, lib
 pytestmark = pytest.mark.gpu
 
 # (M, N, K): single elements, ragged M/N/K, several tiles, and the projections of
-# a 512-row chunk of the Qwen3-0.6B shape (QKV, O, gate/up, down); these run
-# 64-column tiles (a grid of 128-column tiles would leave SMs idle). The last
-# two fill the GPU with 128-column tiles: the gate/up product of a 1024-row
-# chunk, and ragged M, N and K.
+# a 512-row chunk of the Qwen3-0.6B shape (QKV, O, gate/up, down). The tile
+# width is planned per launch: the small products run 64-column tiles, the
+# 512-row QKV shape 128-column ones, and the last three 256-column tiles (the
+# gate/up product of a 1024-row chunk, then ragged M, N and K twice).
 SHAPES = [(1, 1, 8), (3, 5, 16), (128, 128, 64), (129, 130, 72), (200, 300, 96), (257, 64, 1024),
           (512, 4096, 1024), (512, 1024, 2048), (300, 3072, 1024), (384, 1024, 3072),
-          (1024, 6144, 1024), (1100, 2500, 200)]
+          (1024, 6144, 1024), (1100, 2500, 200), (1900, 3000, 264)]
 
 
 def bf16_matrix(rows, cols, seed, scale=1.0):
@@ -61,6 +61,20 @@ def test_gemm_accumulate_and_column_stride():
     A = bf16_matrix(M, K, 21)
     Wm = bf16_matrix(N, K, 22, 0.02)
     rng = np.random.default_rng(23)
+    init = rng.standard_normal((M, ldc)).astype(np.float32)
+    got = run(W_, A, Wm, M, N, K, ldc=ldc, init=init, accumulate=True)
+    ref = init[:, :N].astype(np.float64) + O.project_rows(A, Wm)
+    assert np.all(np.abs(got[:, :N] - ref) <= bound(A, Wm, K) + 2.0 ** -23 * np.abs(ref))
+    np.testing.assert_array_equal(got[:, N:], init[:, N:])
+
+
+def test_gemm_accumulate_wide_tiles():
+    """accumulate with 256-column tiles (1100 x 2500 x 200) and a row stride past N."""
+    W_ = lib()
+    M, N, K, ldc = 1100, 2500, 200, 2504
+    A = bf16_matrix(M, K, 31)
+    Wm = bf16_matrix(N, K, 32, 0.02)
+    rng = np.random.default_rng(33)
     init = rng.standard_normal((M, ldc)).astype(np.float32)
     got = run(W_, A, Wm, M, N, K, ldc=ldc, init=init, accumulate=True)
     ref = init[:, :N].astype(np.float64) + O.project_rows(A, Wm)

@@ -143,11 +143,9 @@ def test_head_dim_128_peaked_scores():
     run_chunked(shape, w, prompt, 128, 2, "staged")
 
 
-def test_qwen3_widths_1024_row_chunk_repeated():
-    """Three layers of the Qwen3-0.6B widths, one 1024-row chunk, three times on fresh decoders:
-    the attention's CTAs walk one to eight key tiles of 128 (rows 128-255 two), so the waits
-    on the output accumulator of the last tile run against products still in flight; every
-    layer's K/V after each run against the oracle."""
+def qwen3_widths_one_chunk(rows, reps):
+    """Three layers of the Qwen3-0.6B widths, one chunk of `rows` rows, `reps` times on fresh
+    decoders; every layer's K/V after each run against the oracle."""
     import dataclasses
 
     import torch
@@ -157,11 +155,11 @@ def test_qwen3_widths_1024_row_chunk_repeated():
 
     s = dataclasses.replace(Wl.QWEN3_06B, layers=3)
     w = Wl.decoder_weights(s, seed=1, wdtype="bf16")
-    prompt = [int(t) for t in Wl.prompt_zipf(1024, s.vocab, seed=2)]
-    ora = O.OracleDecoder(s, w, kv_dtype="bf16", max_seq=1032)
+    prompt = [int(t) for t in Wl.prompt_zipf(rows, s.vocab, seed=2)]
+    ora = O.OracleDecoder(s, w, kv_dtype="bf16", max_seq=rows + 8)
     ora.prefill(prompt, logit_rows=[])
-    for rep in range(3):
-        dec = Decoder(s, w, kv_dtype="bf16", max_seq=1032, chunk_cap=1024)
+    for rep in range(reps):
+        dec = Decoder(s, w, kv_dtype="bf16", max_seq=rows + 8, chunk_cap=rows)
         dec.prefill(prompt, is_last=False)
         torch.cuda.synchronize()
         for l in range(s.layers):
@@ -171,6 +169,19 @@ def test_qwen3_widths_1024_row_chunk_repeated():
             close(kv_to_np(V[:, :n]), rv, LOW_TOL, f"run {rep}: V layer {l}")
         assert dec.device_errors() == 0
         dec.close()
+
+
+def test_qwen3_widths_1024_row_chunk_repeated():
+    """A 1024-row chunk three times: the attention's CTAs walk one to eight key tiles of 128
+    (rows 128-255 two), so the waits on the output accumulator of the last tile run against
+    products still in flight."""
+    qwen3_widths_one_chunk(1024, 3)
+
+
+def test_qwen3_widths_2048_row_chunk():
+    """A 2048-row chunk: the Q/K/V and gate/up products take 256-column tiles (the SwiGLU
+    epilogue pairing 128 gate and 128 up outputs), O and down 128-column ones."""
+    qwen3_widths_one_chunk(2048, 1)
 
 
 def test_single_row_chunks():

@@ -717,10 +717,9 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
   // RMSNorm of the residual rows into the next GEMM's operand pair
   const bool norm4 = H % 4 == 0 && H <= 4 * kPfNormPieces * kPfThreads;
   auto norm = [&](const float* Xr, const float* gain, float eps, int Hn, uint16_t* A, uint16_t* A2) {
-    if (norm4 && (reinterpret_cast<uintptr_t>(gain) & 15u) == 0)
-      pf_norm4_kernel<<<n, kPfThreads, 0, st>>>(Xr, gain, eps, Hn, A, A2);
-    else
-      pf_norm_kernel<<<n, kPfThreads, 0, st>>>(Xr, gain, eps, Hn, A, A2);
+    return norm4 && (reinterpret_cast<uintptr_t>(gain) & 15u) == 0
+               ? launch_k(pf_norm4_kernel, dim3(n), dim3(kPfThreads), 0, st, true, Xr, gain, eps, Hn, A, A2)
+               : launch_k(pf_norm_kernel, dim3(n), dim3(kPfThreads), 0, st, true, Xr, gain, eps, Hn, A, A2);
   };
   pf_embed_norm_kernel<uint16_t><<<n, kPfThreads, 0, st>>>(c->at<int32_t>(L.tok), p0, c->w.embed, g.vocab,
                                                            c->layers[0].g_in, g.eps, H, X, AH, AH2, err);
@@ -729,7 +728,7 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     const dec_layer_weights& lw = c->layers[l];
     const int wm = l * kMkMapsPerLayer;
     if (l > 0) {
-      norm(X, lw.g_in, g.eps, H, AH, AH2);
+      WSG_CUDA_TRY(&c->err, norm(X, lw.g_in, g.eps, H, AH, AH2));
       WSG_CUDA_TRY(&c->err, cudaGetLastError());
     }
     if (fuse_qkv) {
@@ -747,11 +746,13 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
       auto rk = d == 128 ? pf_qk_rope_kv_vec_kernel<KT, 4>
                          : d == 64 ? pf_qk_rope_kv_vec_kernel<KT, 2> : pf_qk_rope_kv_vec_kernel<KT, 1>;
       const long long pairs = static_cast<long long>(n) * (g.n_q + 2 * g.n_kv);
-      rk<<<static_cast<unsigned>((pairs + 7) / 8), 256, 0, st>>>(QKV, n, p0, g.n_q, g.n_kv, lw.g_q, lw.g_k, g.eps,
-                                                                 rc, rs, kc, vc, g.max_seq);
+      WSG_CUDA_TRY(&c->err, launch_k(rk, dim3(static_cast<unsigned>((pairs + 7) / 8)), dim3(256), 0, st, true, QKV, n,
+                                     p0, g.n_q, g.n_kv, static_cast<const float*>(lw.g_q),
+                                     static_cast<const float*>(lw.g_k), g.eps, rc, rs, kc, vc, g.max_seq));
     } else {
-      pf_qk_rope_kv_kernel<KT><<<dim3(n, (g.n_q + 2 * g.n_kv + 3) / 4), 128, 0, st>>>(
-          QKV, p0, g.n_q, g.n_kv, d, lw.g_q, lw.g_k, g.eps, rc, rs, kc, vc, g.max_seq);
+      WSG_CUDA_TRY(&c->err, launch_k(pf_qk_rope_kv_kernel<KT>, dim3(n, (g.n_q + 2 * g.n_kv + 3) / 4), dim3(128), 0,
+                                     st, true, QKV, p0, g.n_q, g.n_kv, d, static_cast<const float*>(lw.g_q),
+                                     static_cast<const float*>(lw.g_k), g.eps, rc, rs, kc, vc, g.max_seq));
     }
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     // A chunk that does not end the prompt stops after the last layer's K/V
@@ -780,9 +781,9 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
       aa.max_seq = g.max_seq;
       aa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
       const int rows = kAtBM / group;
-      pf_attn_tmem_kernel<<<dim3(g.n_kv, (n + rows - 1) / rows), kAtThreads, kAtSmem, st>>>(
-          *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[0].b),
-          *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[1].b), aa);
+      WSG_CUDA_TRY(&c->err, launch_k(pf_attn_tmem_kernel, dim3(g.n_kv, (n + rows - 1) / rows), dim3(kAtThreads),
+                                     kAtSmem, st, true, *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[0].b),
+                                     *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[1].b), aa));
       tc = true;
     } else if constexpr (sizeof(KT) == 2) {  // bfloat16 cache: warp-level tensor-core attention
       void (*tk)(const float*, int, int, int, int, const uint16_t*, const uint16_t*, int, float, uint16_t*, uint16_t*) =
@@ -798,20 +799,23 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
                                                      static_cast<int>(smem)));
           lifted[c->di.device][hs] = true;
         }
-        tk<<<dim3(g.n_kv, (n + rows_per_block - 1) / rows_per_block), kPfTcWarps * 32, smem, st>>>(
-            QKV, n, p0, g.n_q, g.n_kv, static_cast<const uint16_t*>(kc), static_cast<const uint16_t*>(vc), g.max_seq,
-            scale, AO, AO2);
+        WSG_CUDA_TRY(&c->err, launch_k(tk, dim3(g.n_kv, (n + rows_per_block - 1) / rows_per_block),
+                                       dim3(kPfTcWarps * 32), smem, st, true, static_cast<const float*>(QKV), n, p0,
+                                       g.n_q, g.n_kv, static_cast<const uint16_t*>(kc),
+                                       static_cast<const uint16_t*>(vc), g.max_seq, scale, AO, AO2));
         tc = true;
       }
     }
     if (!tc) {
       auto ak = group <= 2 ? pf_attn_kernel<KT, 2> : pf_attn_kernel<KT, 8>;
-      ak<<<dim3(g.n_kv, (n + kPfAttnRows - 1) / kPfAttnRows), kPfAttnRows * 32, 0, st>>>(
-          QKV, n, p0, g.n_q, g.n_kv, d, kc, vc, g.max_seq, scale, AO, AO2);
+      WSG_CUDA_TRY(&c->err, launch_k(ak, dim3(g.n_kv, (n + kPfAttnRows - 1) / kPfAttnRows), dim3(kPfAttnRows * 32), 0,
+                                     st, true, static_cast<const float*>(QKV), n, p0, g.n_q, g.n_kv, d,
+                                     static_cast<const void*>(kc), static_cast<const void*>(vc), g.max_seq, scale, AO,
+                                     AO2));
     }
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     if ((s = gemm(1, wm + 3, X, H, 0, H, qw, true)) != DEC_OK) return s;  // O projection + residual
-    norm(X, lw.g_post, g.eps, H, AH, AH2);
+    WSG_CUDA_TRY(&c->err, norm(X, lw.g_post, g.eps, H, AH, AH2));
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
     // gate/up with SwiGLU in the GEMM's epilogue: tiles pair 64 gate and 64 up outputs
     const int gbn = gemm_plan(n, 2 * I, H, c->di.sms, 256, true) == 256 ? 256 : 128;

@@ -40,11 +40,13 @@ dec_status set_smem_all(int dev, std::string* where) {
   return set_smem_once<256>(dev, where);
 }
 
+// A launch may begin (set-up, weight tiles) while the previous kernel of the
+// stream finishes: the kernel waits for it before its activation reads and C.
 template <int EPI, bool SPLIT, int BN>
 cudaError_t launch_one(dim3 grid, const CUtensorMap& ma, const CUtensorMap& ma2, const CUtensorMap& mb0,
                        const CUtensorMap& mb1, const CUtensorMap& mb2, const TcArgs& a, cudaStream_t st) {
-  gemm_bf16_tc_kernel<EPI, SPLIT, BN><<<grid, kTcThreads, tc_smem_bytes<SPLIT, BN>(), st>>>(ma, ma2, mb0, mb1, mb2, a);
-  return cudaGetLastError();
+  return launch_k(gemm_bf16_tc_kernel<EPI, SPLIT, BN>, grid, dim3(kTcThreads), tc_smem_bytes<SPLIT, BN>(), st, true,
+                  ma, ma2, mb0, mb1, mb2, a);
 }
 
 template <int BN>

@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();  // the next launch may start its own set-up and weight loads
   const uint32_t tmem = tmem_base;
   auto fail = [&]() {
     *vfail = 1;
@@ -282,12 +283,40 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   if (warp == 0) {
     // ---- TMA: A and W tiles of every K block of every tile into the stage ring ----
+    // The weights never depend on earlier kernels: the first ring's worth of
+    // W tiles is requested before waiting for the kernel this launch follows
+    // (programmatic dependent launch), the activation tiles after it.
     if (lane == 0) {
+      auto tile_of = [&](int t, int* n0, int* m0, const CUtensorMap** mapB, int* wn0) {
+        *n0 = (t % ntn) * BN;
+        *m0 = (t / ntn) * kTcBM;
+        *mapB = *n0 < a.nb1 ? &mapB0 : *n0 < a.nb2 ? &mapB1 : &mapB2;
+        *wn0 = *n0 - (*n0 < a.nb1 ? 0 : *n0 < a.nb2 ? a.nb1 : a.nb2);  // first row of the tile in its weight
+      };
+      auto load_w = [&](unsigned char* st, int kb, int n0, const CUtensorMap* mapB, int wn0, uint64_t* bar) {
+        if constexpr (EPI == TC_SWIGLU) {
+          tma_load_2d_map(st + kBOff, &mapB0, kb * kTcBK, n0 / 2, bar);
+          tma_load_2d_map(st + kBOff + tc_b_bytes<BN / 2>(), &mapB1, kb * kTcBK, n0 / 2, bar);
+        } else {
+          tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, bar);
+        }
+      };
+      uint32_t pre = 0;  // stages whose W tiles went out before the wait
+      for (int t = blockIdx.x; t < ntiles && pre < static_cast<uint32_t>(kTcStages); t += gridDim.x) {
+        int n0, m0, wn0;
+        const CUtensorMap* mapB;
+        tile_of(t, &n0, &m0, &mapB, &wn0);
+        for (int kb = 0; kb < KB && pre < static_cast<uint32_t>(kTcStages); ++kb, ++pre) {
+          mbar_arrive_expect_tx(&full[pre], kStage);
+          load_w(tsm + static_cast<size_t>(pre) * kStage, kb, n0, mapB, wn0, &full[pre]);
+        }
+      }
+      pdl_wait();
       uint32_t gk = 0;  // k blocks issued by this CTA (ring position)
       for (int t = blockIdx.x; t < ntiles && !*vfail; t += gridDim.x) {
-        const int n0 = (t % ntn) * BN, m0 = (t / ntn) * kTcBM;
-        const CUtensorMap* mapB = n0 < a.nb1 ? &mapB0 : n0 < a.nb2 ? &mapB1 : &mapB2;
-        const int wn0 = n0 - (n0 < a.nb1 ? 0 : n0 < a.nb2 ? a.nb1 : a.nb2);  // first row of the tile in its weight
+        int n0, m0, wn0;
+        const CUtensorMap* mapB;
+        tile_of(t, &n0, &m0, &mapB, &wn0);
         for (int kb = 0; kb < KB; ++kb, ++gk) {
           const int s = gk % kTcStages;
           if (gk >= kTcStages && !mbar_wait(&empty[s], ((gk / kTcStages) - 1) & 1)) {
@@ -296,17 +325,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           if (*vfail) break;
           unsigned char* st = tsm + static_cast<size_t>(s) * kStage;
-          mbar_arrive_expect_tx(&full[s], kStage);
+          if (gk >= pre) {
+            mbar_arrive_expect_tx(&full[s], kStage);
+            load_w(st, kb, n0, mapB, wn0, &full[s]);
+          }
           tma_load_2d_map(st, &mapA, kb * kTcBK, m0, &full[s]);
           if (SPLIT) tma_load_2d_map(st + kTcABytes, &mapA2, kb * kTcBK, m0, &full[s]);
-          if constexpr (EPI == TC_SWIGLU) {
-            tma_load_2d_map(st + kBOff, &mapB0, kb * kTcBK, n0 / 2, &full[s]);
-            tma_load_2d_map(st + kBOff + tc_b_bytes<BN / 2>(), &mapB1, kb * kTcBK, n0 / 2, &full[s]);
-          } else {
-            tma_load_2d_map(st + kBOff, mapB, kb * kTcBK, wn0, &full[s]);
-          }
         }
       }
+      // a stage whose W tile went out ahead must not be left pending at exit
+      for (uint32_t k = gk; k < pre; ++k) mbar_wait(&full[k], 0);
+    } else {
+      pdl_wait();
     }
   } else if (warp == 1) {
     // ---- MMA: four K = 16 steps per stage into the tile's accumulator buffer ----
@@ -366,6 +396,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ---- epilogue warps: warp w reads TMEM lanes (rows) 32 (w % 4) .. 32 (w % 4) + 31 ----
+    pdl_wait();  // C (and the SwiGLU output) may be read or written by the kernel before
     const int q = warp & 3;
     int li = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++li) {

@@ -79,6 +79,8 @@ __global__ void __launch_bounds__(kPfThreads) pf_embed_norm_kernel(const int32_t
 // Row r: (A, A2) = RMSNorm(X[r]) * g.
 __global__ void __launch_bounds__(kPfThreads) pf_norm_kernel(const float* X, const float* g, float eps, int H,
                                                               uint16_t* A, uint16_t* A2) {
+  pdl_trigger();
+  pdl_wait();  // inputs come from the previous kernel
   __shared__ float red[kPfThreads / 32];
   const int r = blockIdx.x;
   const float* x = X + static_cast<size_t>(r) * H;
@@ -95,6 +97,8 @@ __global__ void __launch_bounds__(kPfThreads) pf_norm_kernel(const float* X, con
 constexpr int kPfNormPieces = 4;
 __global__ void __launch_bounds__(kPfThreads) pf_norm4_kernel(const float* X, const float* g, float eps, int H,
                                                                uint16_t* A, uint16_t* A2) {
+  pdl_trigger();
+  pdl_wait();  // inputs come from the previous kernel
   __shared__ float red[kPfThreads / 32];
   const int r = blockIdx.x, n4 = H >> 2;
   const float4* x = reinterpret_cast<const float4*>(X + static_cast<size_t>(r) * H);
@@ -144,6 +148,8 @@ __global__ void __launch_bounds__(128) pf_qk_rope_kv_kernel(float* qkv, int p0, 
                                                              const float* g_q, const float* g_k, float eps,
                                                              const float* rope_cos, const float* rope_sin, void* kc,
                                                              void* vc, int max_seq) {
+  pdl_trigger();
+  pdl_wait();  // inputs come from the previous kernel
   __shared__ float buf[4][128];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x, h = blockIdx.y * 4 + warp;
@@ -195,6 +201,8 @@ __global__ void __launch_bounds__(256) pf_qk_rope_kv_vec_kernel(float* qkv, int 
                                                                  const float* g_q, const float* g_k, float eps,
                                                                  const float* rope_cos, const float* rope_sin,
                                                                  void* kc, void* vc, int max_seq) {
+  pdl_trigger();
+  pdl_wait();  // inputs come from the previous kernel
   static_assert(EPL == 1 || EPL == 2 || EPL == 4, "head size 32, 64 or 128");
   constexpr int d = 32 * EPL, half = d / 2;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -262,6 +270,8 @@ __global__ void __launch_bounds__(kPfAttnRows * 32) pf_attn_kernel(const float* 
                                                                     float scale, uint16_t* AO, uint16_t* AO2) {
   __shared__ __align__(16) float Ks[kPfAttnKeys][128];
   __shared__ __align__(16) float Vs[kPfAttnKeys][128];
+  pdl_trigger();
+  pdl_wait();  // Q, keys and values come from the previous kernels
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x, r0 = blockIdx.y * kPfAttnRows;
   const int group = n_q / n_kv, W = (n_q + 2 * n_kv) * d;
@@ -414,6 +424,8 @@ __global__ void __launch_bounds__(kPfTcWarps * 32) pf_attn_tc_kernel(const float
                                                                       int max_seq, float scale, uint16_t* AO,
                                                                       uint16_t* AO2) {
   constexpr int KS = D / 16;  // k-steps of S = Q K^T
+  pdl_trigger();
+  pdl_wait();  // Q, keys and values come from the previous kernels
   constexpr int NT = D / 8;   // n-tiles of O
   constexpr int RS = D + 8;   // padded row length (elements)
   extern __shared__ __align__(16) uint16_t pf_tc_smem[];

@@ -205,6 +205,8 @@ __global__ void __launch_bounds__(kAtThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_trigger();
+  pdl_wait();  // Q and this chunk's cache rows come from the previous kernels
   const uint32_t tmem = tmem_base;
   const int q = warp & 3, half = (warp - 2) >> 2;  // softmax warps: lane quarter, half of the keys / of D
   const int v = q * 32 + lane;

@@ -252,7 +252,11 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
   VRow vr[CK];
   // The current position's row is not read from the cache (it is written by
   // this kernel): its key and value come from shared memory instead.
-  auto issue = [&](int cb) {
+  // Keys and values of the chunk at cb into registers. In the loop the next
+  // chunk's keys are requested once this chunk's scores are done, and its
+  // values once this chunk's values are accumulated, so each chunk's loads
+  // overlap the previous chunk's work without more registers.
+  auto issue_k = [&](int cb) {
 #pragma unroll
     for (int ps = 0; ps < NPASS; ++ps) {
       const int t = cb + ps * 8 + kq;
@@ -265,6 +269,8 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
                         : make_uint4(0, 0, 0, 0);
       }
     }
+  };
+  auto issue_v = [&](int cb) {
 #pragma unroll
     for (int j = 0; j < CK; ++j) {
       const int t = cb + j;
@@ -273,6 +279,10 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
                   ? __ldcg(reinterpret_cast<const VRow*>(vbytes + static_cast<size_t>(t) * row_bytes) + lane)
                   : z;
     }
+  };
+  auto issue = [&](int cb) {
+    issue_k(cb);
+    issue_v(cb);
   };
   // Nothing below depends on this token until its q/k/v arrive: the gains,
   // the RoPE row and the first chunk of cached keys/values are requested
@@ -317,7 +327,6 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
   }
 
   for (int cb = w0; cb < w1; cb += CK) {
-    if (cb != w0) issue(cb);
     // scores of this lane's key in every pass, for every head
     float sc[NPASS][GMAX];
 #pragma unroll
@@ -364,6 +373,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
         sc[ps][h] = t < w1 ? acc[h] * a.scale : -INFINITY;
       }
     }
+    if (cb + CK < w1) issue_k(cb + CK);
     // online softmax over the chunk; pr = this lane's key's probability per pass
     float pr[NPASS][GMAX];
 #pragma unroll
@@ -408,6 +418,7 @@ __device__ __forceinline__ void attn_decode_body(const AttnArgs& a, int g, int s
         o[h].w = fmaf(pj, v.w, o[h].w);
       }
     }
+    if (cb + CK < w1) issue_v(cb + CK);
   }
 
   if (tid == 0) io.mark(3);

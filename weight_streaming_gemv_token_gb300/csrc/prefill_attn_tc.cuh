@@ -42,6 +42,10 @@
 // columns 0 and 128 (probabilities: value at +0..63, remainder at +64..127,
 // two bfloat16 per column), O at 256, Q value at 384 and remainder at 448.
 //
+// Launched as a programmatic dependent of the previous kernel (RoPE and the
+// cache append of this chunk's rows): barrier and tensor-memory set-up run
+// before the dependency wait, everything that reads Q or the cache after it.
+//
 // Every wait is bounded; on a timeout the CTA records ERR_TC_TIMEOUT, stops,
 // waits for its issued MMAs and frees its tensor memory.
 #pragma once
@@ -91,16 +95,9 @@ __device__ __forceinline__ uint64_t tc_desc_sw128_mn(uint32_t saddr, uint32_t lb
   return d;
 }
 
-__device__ __forceinline__ void tc_mma_f16(uint32_t d, uint64_t da, uint64_t db, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(da), "l"(db), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// The same with the A operand (M x 16, two bfloat16 per column, lane = row)
-// in tensor memory at a_tmem.
+// D (+)= A B with A (M x 16, two bfloat16 per column, lane = row) in tensor
+// memory at a_tmem and B from the shared-memory descriptor db; kind::f16,
+// FP32 accumulator at tensor-memory address d (accumulate when acc != 0).
 __device__ __forceinline__ void tc_mma_f16_ts(uint32_t d, uint32_t a_tmem, uint64_t db, uint32_t idesc,
                                               uint32_t acc) {
   asm volatile(

@@ -289,6 +289,10 @@ const char* dec_last_error(const dec_ctx* ctx);
  * in a fixed order (bit-reproducible). out, in >= 0 (out == 0: no work;
  * in == 0: y = 0). Any alignment is accepted; 16-byte aligned W with
  * in*sizeof(elem) a multiple of 16 takes the bulk-copy streaming path.
+ * Ordering: the call is a programmatic dependent of the previous kernel on
+ * `stream` and starts streaming W before that kernel has finished (x and y
+ * only after), so W, a weight matrix, must not be written by the kernel
+ * enqueued immediately before the call; anything earlier is ordered.
  * Errors: DEC_EINVAL, DEC_ECUDA. */
 dec_status gemv(int32_t wdtype, const void* d_W, const void* d_x, float* d_y, int32_t out, int32_t in, void* stream);
 
@@ -305,7 +309,10 @@ dec_status gemv(int32_t wdtype, const void* d_W, const void* d_x, float* d_y, in
  * with x in 16-bit fixed point per 32 columns (step a power of two, error at
  * most 2^-15 of the 32 columns' largest |x|), float32 sums per row, fixed
  * order. Otherwise a per-warp kernel dequantises to float32. Both are
- * bit-reproducible. Errors: DEC_EINVAL, DEC_ECUDA. */
+ * bit-reproducible. Like gemv, the call may start reading the codes, scales
+ * and biases before the previous kernel on `stream` has finished (x and y
+ * only after it): they must not be written by the kernel enqueued
+ * immediately before the call. Errors: DEC_EINVAL, DEC_ECUDA. */
 dec_status gemv_q4(const uint32_t* d_codes, const uint16_t* d_scale, const uint16_t* d_bias, const uint16_t* d_x,
                    float* d_y, int32_t out, int32_t in, int32_t ntok, void* stream);
 
@@ -368,9 +375,13 @@ dec_status greedy_head_noalloc(int32_t wdtype, const void* d_embed, const float*
  * C[m][n] += that sum). A [M][K] and W [N][K] are bfloat16, row-major,
  * 16-byte aligned (W is a weight matrix in the decoder's [out][in] layout);
  * C is float32 with row stride ldc >= N. Products are exact in FP32 and
- * accumulated in FP32 (tcgen05 tensor cores, tiles of 128 x 128 x 64).
- * K must be a multiple of 8. Asynchronous on `stream`; device errors (a
- * bounded wait that gave up) are reported by gemv_device_errors.
+ * accumulated in FP32 (tcgen05 tensor cores; 128-row tiles 256, 128 or 64
+ * columns wide, chosen per call by the operand bytes the busiest SM
+ * streams). K must be a multiple of 8. Asynchronous on `stream`; like gemv
+ * the call may start reading W before the previous kernel on `stream` has
+ * finished (A and C only after it), so W must not be written by the kernel
+ * enqueued immediately before it. Device errors (a bounded wait that gave
+ * up) are reported by gemv_device_errors.
  * Errors: DEC_EINVAL (sizes, alignment), DEC_EDEVICE, DEC_ECUDA. */
 dec_status gemm_bf16(const uint16_t* d_A, const uint16_t* d_W, float* d_C, int32_t M, int32_t N, int32_t K,
                      int32_t ldc, int32_t accumulate, void* stream);

@@ -120,8 +120,8 @@ def test_head_dim_128_both_cache_types(kv_dtype):
 def test_head_dim_128_query_groups(n_q, n_kv):
     """head_dim 128 with a bfloat16 cache (the tcgen05 attention: 128 query vectors per CTA, 128 /
     group rows) for groups of 1, 2, 4 and 8 query heads per key/value head; 300 rows in chunks of
-    128 (128 + 128 + 44), so the later chunks walk five key tiles of 64 and the last block is
-    ragged."""
+    128 (128 + 128 + 44), so the later chunks walk two and three key tiles of 128 and the last
+    tile and row block are ragged."""
     shape = Wl.DecoderShape(layers=2, hidden=256, inter=512, n_q=n_q, n_kv=n_kv, head_dim=128, vocab=500)
     w = Wl.decoder_weights(shape, seed=11, wdtype="bf16")
     prompt = Wl.prompt_zipf(300, shape.vocab, seed=4)
@@ -129,9 +129,10 @@ def test_head_dim_128_query_groups(n_q, n_kv):
 
 
 def test_head_dim_128_peaked_scores():
-    """Q and K norm gains scaled by 3 (scores of standard deviation ~9): in layer 0, 193 of the 944
-    (row, query head) pairs with more than 64 keys meet a later key tile whose maximum passes the
-    reference maximum by more than 2^8, so the attention rescales its output accumulator mid-walk.
+    """Q and K norm gains scaled by 3 (scores of standard deviation ~9): in layer 0 of the float64
+    forward, 45 of the 688 (row, query head) pairs with more than 128 keys meet a later key tile of
+    128 whose maximum passes the reference maximum by more than 2^8 (log2 units), so the attention
+    rescales its output accumulator mid-walk.
     (At a gain of 6 the forward itself is ill-conditioned: the float64 forward with only the
     value + remainder operand roundings applied already moves layer-1 keys past the tolerance.)"""
     shape = Wl.DecoderShape(layers=2, hidden=256, inter=512, n_q=4, n_kv=2, head_dim=128, vocab=500)

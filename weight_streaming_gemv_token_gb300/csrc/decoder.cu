@@ -785,7 +785,7 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
                                      kAtSmem, st, true, *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[0].b),
                                      *reinterpret_cast<const CUtensorMap*>(c->pf_kvmap[1].b), aa));
       tc = true;
-    } else if constexpr (sizeof(KT) == 2) {  // bfloat16 cache: warp-level tensor-core attention
+    } else if constexpr (sizeof(KT) == 2) {  // bfloat16 cache, other head sizes or groups: warp-level MMAs
       void (*tk)(const float*, int, int, int, int, const uint16_t*, const uint16_t*, int, float, uint16_t*, uint16_t*) =
           d == 128 ? pf_attn_tc_kernel<128> : d == 64 ? pf_attn_tc_kernel<64> : d == 32 ? pf_attn_tc_kernel<32>
                                                                             : d == 16 ? pf_attn_tc_kernel<16> : nullptr;
@@ -817,7 +817,7 @@ dec_status run_chunk_prefill_t(dec_ctx* c, int p0, int n, bool is_last) {
     if ((s = gemm(1, wm + 3, X, H, 0, H, qw, true)) != DEC_OK) return s;  // O projection + residual
     WSG_CUDA_TRY(&c->err, norm(X, lw.g_post, g.eps, H, AH, AH2));
     WSG_CUDA_TRY(&c->err, cudaGetLastError());
-    // gate/up with SwiGLU in the GEMM's epilogue: tiles pair 64 gate and 64 up outputs
+    // gate/up with SwiGLU in the GEMM's epilogue: a tile pairs bn/2 gate and bn/2 up outputs
     const int gbn = gemm_plan(n, 2 * I, H, c->di.sms, 256, true) == 256 ? 256 : 128;
     const void* gmap = gbn == 256 ? c->pf_wmap[wm + 4].b : c->pf_wmap64[wm + 4].b;
     const void* umap = gbn == 256 ? c->pf_wmap[wm + 5].b : c->pf_wmap64[wm + 5].b;

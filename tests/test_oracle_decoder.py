@@ -7,6 +7,7 @@ same forward (token by token versus batched rows), and by invariants that a
 wrongly wired layer would break.
 """
 import copy
+import dataclasses
 import os
 
 import numpy as np
@@ -156,3 +157,105 @@ def test_regression_golden_tokens(tiny_weights, golden_dir):
     out = O.generate(m, W.prompt_uniform(8, W.TINY.vocab, seed=0), 8)
     assert out["tokens"] == [int(t) for t in ref["tokens"]]
     np.testing.assert_allclose(out["logits"][0][:16], ref["logits0_head"], rtol=1e-12)
+
+
+# -- rescaling invariants -----------------------------------------------------------
+# Each pair of weight changes below leaves the forward unchanged under the model's
+# definition and changes it under a plausible miswiring (the norm named in the
+# test id missing or given the wrong gain, gate and up swapped, a normalised
+# value path, a wrong query-to-key/value-head grouping). Factors are powers of
+# two, so the float32 weights change exactly; the invariants are exact as the
+# RMSNorm eps goes to 0 (at 1e-6 against mean squares of q of ~0.025 they move
+# the logits by ~4e-5), so these forwards run the tiny shape with eps = 1e-12.
+TINY_SMALL_EPS = dataclasses.replace(W.TINY, eps=1e-12)
+
+
+def _logits_and_cache(weights, prompt, kv="f32"):
+    m = O.OracleDecoder(TINY_SMALL_EPS, weights, kv_dtype=kv, max_seq=16)
+    for t in prompt[:-1]:
+        m.body(t)
+    return m.step(prompt[-1]), m
+
+
+def _scaled(weights, **factors):
+    w = copy.deepcopy(weights)
+    for lw in w["layers"]:
+        for name, f in factors.items():
+            lw[name] = (lw[name] * np.float32(f)).astype(np.float32)
+    return w
+
+
+INVARIANT_PROMPT = [5, 300, 17, 17, 411, 2]
+
+
+def _assert_same_forward(a, b):
+    np.testing.assert_allclose(a, b, rtol=1e-9, atol=1e-9 * np.abs(a).max())
+
+
+def _assert_other_forward(a, b):
+    assert np.abs(a - b).max() > 1e-3 * np.abs(a).max()
+
+
+@pytest.mark.parametrize("name,factors", [
+    ("q_norm", dict(w_q=4.0)),                           # q is normalised per head
+    ("q_k_norms", dict(w_q=4.0, w_k=0.25)),              # and so is k
+    ("input_norm_gain", dict(g_in=4.0, w_q=0.25, w_k=0.25, w_v=0.25)),
+    ("post_attention_norm_gain", dict(g_post=4.0, w_gate=0.25, w_up=0.25)),
+    ("value_path_linear", dict(w_v=4.0, w_o=0.25)),      # v is not normalised
+    ("up_linear", dict(w_up=-1.0, w_down=-1.0)),         # silu(gate) * up: odd in up
+])
+def test_forward_invariant_under_rescaling(tiny_weights, name, factors):
+    ref, _ = _logits_and_cache(tiny_weights, INVARIANT_PROMPT)
+    got, _ = _logits_and_cache(_scaled(tiny_weights, **factors), INVARIANT_PROMPT)
+    _assert_same_forward(ref, got)
+
+
+@pytest.mark.parametrize("factors", [
+    dict(w_gate=-1.0, w_down=-1.0),   # the gate is not odd: silu(-z) != -silu(z)
+    dict(g_post=4.0),                 # the MLP sees the post-attention gain
+    dict(g_in=4.0),                   # and the value path the input gain
+])
+def test_forward_changes_under_an_uncompensated_rescaling(tiny_weights, factors):
+    """Counterparts of the invariants: these changes are not undone, and each moves
+    the logits by far more than the invariants' tolerance."""
+    ref, _ = _logits_and_cache(tiny_weights, INVARIANT_PROMPT)
+    got, _ = _logits_and_cache(_scaled(tiny_weights, **factors), INVARIANT_PROMPT)
+    _assert_other_forward(ref, got)
+
+
+def test_cached_values_scale_with_the_value_projection(tiny_weights):
+    """The cache holds raw values: scaling w_v by 4 scales every cached value by
+    exactly 4 in layer 0 (whose input does not depend on w_v) and leaves the keys
+    alone."""
+    _, a = _logits_and_cache(tiny_weights, INVARIANT_PROMPT)
+    _, b = _logits_and_cache(_scaled(tiny_weights, w_v=4.0), INVARIANT_PROMPT)
+    np.testing.assert_array_equal(b.kv(0)[1], 4.0 * a.kv(0)[1])
+    np.testing.assert_array_equal(b.kv(0)[0], a.kv(0)[0])
+
+
+def test_key_value_head_permutation(tiny_weights):
+    """Swapping the two key/value heads together with the query heads that read
+    them (query head h reads key/value head h // group) and with the matching
+    columns of w_o leaves the logits unchanged; swapping only the key/value heads
+    does not."""
+    s = W.TINY
+    d, group = s.head_dim, s.n_q // s.n_kv
+    perm_kv = [1, 0]
+    perm_q = [perm_kv[h // group] * group + h % group for h in range(s.n_q)]
+
+    def rows(m, perm):
+        return np.concatenate([m[p * d:(p + 1) * d] for p in perm], axis=0)
+
+    w = copy.deepcopy(tiny_weights)
+    only_kv = copy.deepcopy(tiny_weights)
+    for lw, lo in zip(w["layers"], only_kv["layers"]):
+        for m in (lw, lo):
+            m["w_k"] = rows(m["w_k"], perm_kv)
+            m["w_v"] = rows(m["w_v"], perm_kv)
+        lw["w_q"] = rows(lw["w_q"], perm_q)
+        lw["w_o"] = rows(lw["w_o"].T, perm_q).T.copy()
+    ref, _ = _logits_and_cache(tiny_weights, INVARIANT_PROMPT)
+    got, _ = _logits_and_cache(w, INVARIANT_PROMPT)
+    _assert_same_forward(ref, got)
+    bad, _ = _logits_and_cache(only_kv, INVARIANT_PROMPT)
+    _assert_other_forward(ref, bad)

@@ -187,6 +187,40 @@ def test_qwen3_fp32_prefill_and_generate_one_launch(qwen_f32):
     assert dec.device_errors() == 0
 
 
+def test_qwen3_fp32_bench_launch_configuration(qwen_f32):
+    """The launch sequence bench.py times with --steps 20 --warmup 5: the 32-token prompt in one
+    launch, 5 warm-up steps in one launch, then 20 steps in one launch (positions 37-56), in a
+    cache sized as the bench sizes it. Every token against the oracle teacher-forced on the GPU's
+    tokens (equal wherever the oracle's top-2 gap exceeds twice the tolerance), then every layer's
+    whole cache (57 positions) at 1e-3."""
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.QWEN3_06B
+    prompt = Wl.prompt_uniform(32, s.vocab, seed=0)
+    dec = Decoder(s, qwen_f32, kv_dtype="f32", max_seq=32 + 1 + 5 + 20 + 1 + 2 * 100 + 8)
+    dec.reset()
+    first = dec.prefill(prompt, is_last=True)
+    warm = dec.generate(first, 5).cpu().tolist()
+    timed = dec.generate(warm[-1], 20).cpu().tolist()
+    toks = [first] + warm + timed
+    assert dec.position == 32 + 25 and dec.device_errors() == 0
+    ora = O.OracleDecoder(s, qwen_f32, max_seq=64)
+    ref = O.generate(ora, prompt, len(toks), forced=toks)
+    for j, (got, lg) in enumerate(zip(toks, ref["logits"])):
+        srt = np.sort(lg)[::-1]
+        if srt[0] - srt[1] > 2 * (FP32_TOL + FP32_TOL * abs(srt[0])):
+            assert got == O.argmax_lowest(lg)[0], f"token {j}: GPU {got}, oracle {O.argmax_lowest(lg)[0]}"
+    assert ora.pos == dec.position
+    for l in range(s.layers):
+        K, V, n = dec.kv(l)
+        rk, rv = ora.kv(l)
+        assert n == ora.pos
+        close(kv_to_np(K[:, :n]), rk, FP32_TOL, f"K layer {l}")
+        close(kv_to_np(V[:, :n]), rv, FP32_TOL, f"V layer {l}")
+    dec.close()
+
+
 def test_api_errors(tiny_w):
     import torch
 

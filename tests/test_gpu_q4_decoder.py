@@ -212,3 +212,38 @@ def test_qwen3_q4_generation_and_verify(qwen_q4):
     for engine in ENGINES:
         check_verify(s, w, deq, Wl.prompt_uniform(3, s.vocab, seed=2), Wl.prompt_uniform(2, s.vocab, seed=4),
                      engine=engine)
+
+
+@pytest.mark.parametrize("engine", ENGINES)
+def test_qwen3_q4_bench_launch_configuration(qwen_q4, engine):
+    """The launch sequence bench.py times for the 4-bit configuration on each engine: the 32-token
+    prompt, 4 warm-up steps in one call, then 256 steps in one call (positions 36-291), in a cache
+    sized as the bench sizes it. Every token against the oracle on the dequantised weights,
+    teacher-forced on the GPU's tokens (equal wherever the oracle's top-2 gap exceeds twice the
+    tolerance), then every layer's whole cache (292 positions) at 2e-2."""
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    w, deq = qwen_q4
+    s = Wl.QWEN3_06B
+    prompt = Wl.prompt_uniform(32, s.vocab, seed=0)
+    dec = Decoder(s, w, kv_dtype="f32", max_seq=32 + 8 + 256 + 2 * (64 + 4) + 8, engine=engine)
+    first = dec.prefill(prompt, is_last=True)
+    warm = dec.generate(first, 4).cpu().tolist()
+    timed = dec.generate(warm[-1], 256).cpu().tolist()
+    toks = [first] + warm + timed
+    assert dec.position == 32 + 4 + 256 and dec.device_errors() == 0
+    ora = O.OracleDecoder(s, deq, max_seq=300)
+    ref = O.generate(ora, prompt, len(toks), forced=toks)
+    for j, (got, lg) in enumerate(zip(toks, ref["logits"])):
+        srt = np.sort(lg)[::-1]
+        if srt[0] - srt[1] > 2 * (LOW_TOL + LOW_TOL * abs(srt[0])):
+            assert got == O.argmax_lowest(lg)[0], f"token {j}: GPU {got}, oracle {O.argmax_lowest(lg)[0]}"
+    assert ora.pos == dec.position
+    for l in range(s.layers):
+        K, V, n = dec.kv(l)
+        rk, rv = ora.kv(l)
+        assert n == ora.pos
+        close(kv_to_np(K[:, :n]), rk, LOW_TOL, f"K layer {l}")
+        close(kv_to_np(V[:, :n]), rv, LOW_TOL, f"V layer {l}")
+    dec.close()

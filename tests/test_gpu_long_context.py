@@ -167,3 +167,36 @@ def test_qwen3_bf16_held_out_size_against_oracle(C):
         tw.close()
     decode_and_check(dec, ora, s, tok, n_out, LOW_TOL)
     dec.close()
+
+
+@pytest.mark.slow
+def test_qwen3_bf16_held_out_generation_as_benched():
+    """The held-out generation exactly as bench.py runs it: the 4,096-token prompt in 2,048-row
+    chunks into a 5,128-row cache, then the remaining 1,023 outputs in one launch (positions
+    4,096-5,118, 19 splits per key/value head). The oracle prefills the same chunks and follows the
+    GPU's tokens (one batched forward over them, the same mathematics as stepping): every token
+    equal to the oracle's wherever its top-2 gap exceeds twice the tolerance, and every layer's
+    whole cache (5,119 positions) at the end."""
+    lib()
+    from weight_streaming_gemv_token_gb300.decoder import Decoder
+
+    s = Wl.QWEN3_06B
+    P, C, N = 4096, 2048, 1024
+    w = Wl.decoder_weights(s, seed=1, wdtype="bf16")
+    prompt = [int(t) for t in Wl.prompt_zipf(P, s.vocab, seed=2)]
+    dec = Decoder(s, w, kv_dtype="bf16", max_seq=P + N + 8, chunk_cap=C)
+    for c0 in range(0, P, C):
+        first = dec.prefill(prompt[c0:c0 + C], is_last=c0 + C >= P)
+    toks = [first] + dec.generate(first, N - 1).cpu().tolist()
+    assert dec.position == P + N - 1 and dec.device_errors() == 0
+    ora = O.OracleDecoder(s, w, kv_dtype="bf16", max_seq=P + N)
+    for c0 in range(0, P, C):
+        out = ora.prefill(prompt[c0:c0 + C], logit_rows=[C - 1] if c0 + C >= P else [])
+    forced = ora.prefill(toks[:-1], logit_rows=list(range(N - 1)))["logits"]
+    refs = [out["logits"][C - 1]] + [forced[r] for r in range(N - 1)]
+    for j, (got, lg) in enumerate(zip(toks, refs)):
+        srt = np.sort(lg)[::-1]
+        if srt[0] - srt[1] > 2 * (LOW_TOL + LOW_TOL * abs(srt[0])):
+            assert got == O.argmax_lowest(lg)[0], f"output {j}: GPU {got}, oracle {O.argmax_lowest(lg)[0]}"
+    check_prefix(dec, ora, s, P + N - 1, LOW_TOL, "after 1,024 outputs")
+    dec.close()

@@ -90,6 +90,26 @@ def test_tokenwise_equals_batched_rows(tiny_weights, kv):
     np.testing.assert_allclose(la, lb, rtol=1e-10 if kv == "f32" else 1e-2, atol=1e-12 if kv == "f32" else 1e-3)
 
 
+def test_batched_continuation_logits_equal_steps(tiny_weights):
+    """Teacher forcing in one call: after a chunked prompt, a batched forward over forced tokens
+    with logits on every row gives each row the logits that stepping through the same tokens gives
+    (the long-context GPU tests follow the GPU's tokens this way)."""
+    prompt = W.prompt_zipf(40, W.TINY.vocab, seed=2)
+    forced = W.prompt_uniform(12, W.TINY.vocab, seed=5)
+    a = O.OracleDecoder(W.TINY, tiny_weights, kv_dtype="bf16", max_seq=64)
+    b = O.OracleDecoder(W.TINY, tiny_weights, kv_dtype="bf16", max_seq=64)
+    for m in (a, b):
+        m.prefill(prompt[:16], logit_rows=[])
+        m.prefill(prompt[16:], logit_rows=[])
+    rows = a.prefill(forced, logit_rows=list(range(len(forced))))["logits"]
+    for r, t in enumerate(forced):
+        np.testing.assert_allclose(rows[r], b.step(int(t)), rtol=1e-12, atol=1e-12)
+    assert a.pos == b.pos == 52
+    for l in range(W.TINY.layers):
+        np.testing.assert_array_equal(a.kv(l)[0], b.kv(l)[0])
+        np.testing.assert_array_equal(a.kv(l)[1], b.kv(l)[1])
+
+
 def test_bf16_cache_holds_bf16_values(tiny_weights):
     m = O.OracleDecoder(W.TINY, tiny_weights, kv_dtype="bf16", max_seq=16)
     for t in W.prompt_uniform(4, W.TINY.vocab, seed=0):

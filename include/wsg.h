@@ -212,8 +212,12 @@ dec_status dec_verify2(dec_ctx* ctx, const int32_t* h_tokens, float* d_logits, i
 dec_status dec_prefill_chunk(dec_ctx* ctx, const int32_t* h_tokens, int32_t n, int32_t is_last, float* d_logits,
                              int32_t* h_next);
 
-/* n greedy forwards without host involvement: the first input is `token`
- * at the current position, each later input is the previous output. Writes
+/* n greedy forwards without host involvement ("Megakernels", "GPU-wide
+ * end-to-end generation": token IDs in, generated IDs out, the cache
+ * advancing by one entry per forward and the next token chosen on the GPU
+ * by the lowest-ID argmax; there the host reads each ID before the next
+ * forward, here the ID stays on the device): the first input is `token` at
+ * the current position, each later input is the previous output. Writes
  * the n outputs to d_tokens_out (device int32[n]). Asynchronous.
  * Errors: DEC_ECAPACITY (p + n > max_seq), DEC_EINVAL, DEC_ESTATE. */
 dec_status dec_generate(dec_ctx* ctx, int32_t token, int32_t n, int32_t* d_tokens_out);
@@ -225,11 +229,16 @@ dec_status dec_generate(dec_ctx* ctx, int32_t token, int32_t n, int32_t* d_token
  * and RoPE, values raw. Errors: DEC_EINVAL (NULL, layer out of range). */
 dec_status dec_get_kv(const dec_ctx* ctx, int32_t layer, const void** d_k, const void** d_v, int32_t* n_valid);
 
-/* Current position (number of valid cache entries). -1 if ctx is NULL. */
+/* Current position (number of valid cache entries; after a P-token prompt
+ * and N outputs it is P + N - 1, the count "Megakernels", "GPU-wide
+ * end-to-end generation" validates). -1 if ctx is NULL. */
 int32_t dec_position(const dec_ctx* ctx);
 
-/* Stage tracing of the persistent engines. dec_trace_bytes: size of the
- * trace buffer (0 for the staged engine). dec_set_trace: with a non-NULL
+/* Stage tracing of the persistent engines. The pages give no tracing API;
+ * "Our Kernel Benchmark Was Measuring the System Cache", "Key takeaways",
+ * warns that a synchronizing profiler only bounds a kernel's time from
+ * below, so the engines stamp their own stages on the device instead.
+ * dec_trace_bytes: size of the trace buffer (0 for the staged engine). dec_set_trace: with a non-NULL
  * device buffer of at least that size, every later persistent launch writes,
  * for its first forward, one %globaltimer stamp (nanoseconds) per
  * [cta][layer 0..layers][stage 0..4][event 0..3] as uint64. Stages 0-4 of a
@@ -265,7 +274,12 @@ dec_status dec_set_trace(dec_ctx* ctx, uint64_t* d_trace, size_t bytes);
 dec_status dec_set_wait_limit(dec_ctx* ctx, uint64_t ns);
 
 /* Synchronizes the context's stream and returns (and, if clear != 0,
- * clears) the device error bits DEC_DEVERR_*. */
+ * clears) the device error bits DEC_DEVERR_* listed above, among them an
+ * all-NaN logit vector at the argmax (the lowest-ID argmax of "Megakernels",
+ * "GPU-wide end-to-end generation" has no answer there) and waits that gave
+ * up. A set bit marks the affected call's outputs as invalid, as a failed check
+ * invalidates a run in "Benchmark methodology", "Long-document chunked
+ * prefill". Errors: DEC_EINVAL (NULL), DEC_ECUDA. */
 dec_status dec_device_errors(dec_ctx* ctx, int32_t clear, uint32_t* bits);
 
 /* Frees host-side state and CUDA graphs. The workspace stays the caller's

@@ -351,11 +351,17 @@ dec_status pack_bf16_exact(const float* d_src, uint16_t* d_dst, int64_t n, void*
 
 /* Reads (and if clear != 0 clears) the device error bits of the
  * context-free calls (gemv, gemv_q4, gemm_bf16, greedy_head_noalloc) on the
- * current device; synchronizes the device. */
+ * current device; synchronizes the device. The bits mean what they mean for
+ * dec_device_errors (the argmax rule of "Megakernels", "GPU-wide end-to-end
+ * generation"; bounded waits that gave up). Errors: DEC_EINVAL (NULL),
+ * DEC_ECUDA. */
 dec_status gemv_device_errors(int32_t clear, uint32_t* bits);
 
-/* Greedy head for callers that cannot allocate device memory (the pages have
- * no counterpart of this call). Some callers cannot call cudaMalloc: code
+/* Greedy head for callers that cannot allocate device memory. The operation
+ * is the decode step's head: the final RMSNorm and tied vocabulary
+ * projection of "Megakernels", "What runs in the DSL", then the lowest-ID
+ * argmax of "GPU-wide end-to-end generation"; the pages have no entry point
+ * that runs it alone without allocating. Some callers cannot call cudaMalloc: code
  * running inside a host framework that owns every device allocation, or a
  * generation loop that must not risk the device synchronisation an
  * allocation can cause. This call computes x = RMSNorm(h) * gain (eps as

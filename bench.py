@@ -46,10 +46,11 @@ import workloads as Wl  # noqa: E402
 METRIC = "batch-1 decode tokens/s + cold GEMV HBM GB/s (% of GB300 peak), 1 GPU"
 
 # DRAM traffic of the persistent decode kernel per algorithmic byte, from an ncu capture of a
-# 4-layer / 32768-vocabulary case of the same widths: (387,733,504 read + 3,089,920 written) /
-# 387,186,688 algorithmic bytes; the excess is the rows a tiled box reads past a CTA's row range.
-# Set to None when the kernel changes until it is measured again.
-MK_TRAFFIC_PER_ALG_BYTE = (387498496 + 2787584) / 387186688
+# 4-layer / 32768-vocabulary case of the same widths. The last capture, (387,498,496 read +
+# 2,787,584 written) / 387,186,688 algorithmic bytes = 1.008, predates the decode attention's
+# change to request each warp's next key and value chunks later in its loop (the same rows, read
+# once each), so the figure is not reported until it is measured again.
+MK_TRAFFIC_PER_ALG_BYTE = None
 # DRAM bytes (read + written) per launch of the standalone gemv bulk-copy kernel at 151936x1024 f32
 # (the tied vocabulary shape), from an ncu capture: 622,377,984 B read + 3,492,352 B written; None
 # until measured for the current kernel.
@@ -658,8 +659,10 @@ def gpu_arm(args):
                 "traffic": (round(MK_TRAFFIC_PER_ALG_BYTE * step_bytes * K) if MK_TRAFFIC_PER_ALG_BYTE else None),
                 "peak_kind": peak_kind, "kernel": "decode_megakernel<float,float,2> (one cooperative launch, K steps)",
                 "bytes_per_launch": step_bytes * K, "launch_us": round(sec * 1e6, 1), "launches": 1,
-                "traffic_source": "ncu dram bytes of a 4-layer/32768-vocab case of the same widths, scaled by "
-                                  "algorithmic bytes"}
+                "traffic_source": ("ncu dram bytes of a 4-layer/32768-vocab case of the same widths, scaled by "
+                                   "algorithmic bytes" if MK_TRAFFIC_PER_ALG_BYTE else
+                                   "not measured for the current kernel (last capture, before a change of the "
+                                   "attention's load order: 1.008 of algorithmic bytes)")}
         # the standalone GEMV alone at the tied-vocabulary shape (the step's largest product), cold
         o, i = GEMV_ROOF_SHAPE
         gbs, per_launch, avg, launches = time_gemv_cold(W, torch, "f32", o, i, stream, gen=gen)
